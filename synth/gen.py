@@ -1,0 +1,216 @@
+"""Seeded generators for every input of the routed-MoE slot-pool layer.
+
+Recipe (the same for every consumer):
+  * expert matrices W_gate, W_up, W_down ~ N(0, 0.02), stored as fp32, bf16
+    (round-to-nearest-even) or fp8 e4m3 with one fp32 scale per 128x128 block
+    (scale = block amax / 448, codes by torch's e4m3 conversion);
+  * router weight W_r ~ N(0, 0.02) in the activation dtype; router bias
+    b_e = -s * ln(rank_e) for a seeded permutation rank of 1..E (Zipf(s));
+  * decode hidden states: an independent AR(1) stream per (layer, token lane),
+    x_0 ~ N(0,1), x_t = rho * x_{t-1} + sqrt(1 - rho^2) * eps;
+  * prefill hidden states: i.i.d. N(0,1);
+  * initial slot fill: per layer a seeded random choice of its quota of experts.
+
+Small cases are drawn with numpy (Philox) on the host; full-size weights are
+drawn with torch's device generator (Philox) chunk by chunk, because tens of
+GB cannot be drawn on the host in reasonable time.  Per-tensor seeds are a
+hash of (workload, layer, tensor name, base seed).
+
+Nothing here computes any part of the MoE layer; storage encodings (bf16
+rounding, fp8 block quantisation) only produce the stored weights.
+"""
+import hashlib
+import math
+
+import numpy as np
+
+from .configs import F32, BF16, FP8_E4M3_B128, Workload
+
+FP8_MAX = 448.0
+
+
+def seed_for(wl_name: str, layer: int, tensor: str, base_seed: int = 0) -> int:
+    h = hashlib.sha256(f"{wl_name}/{layer}/{tensor}/{base_seed}".encode()).digest()
+    return int.from_bytes(h[:8], "little") & ((1 << 63) - 1)
+
+
+def np_rng(seed: int) -> np.random.Generator:
+    return np.random.Generator(np.random.Philox(seed))
+
+
+def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round fp32 to bf16 (nearest, ties to even); returns the uint16 bit patterns."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+    lsb = (u >> 16) & 1
+    r = (u + 0x7FFF + lsb) >> 16
+    return r.astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    """Storage helper for generators only (widening is exact)."""
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def quantize_fp8_blocks(w: np.ndarray):
+    """fp32 [R, C] (R, C multiples of 128) -> (uint8 e4m3 codes [R,C], fp32 scales [R/128, C/128])."""
+    import torch
+    R, C = w.shape
+    assert R % 128 == 0 and C % 128 == 0
+    t = torch.from_numpy(np.ascontiguousarray(w, dtype=np.float32))
+    blk = t.view(R // 128, 128, C // 128, 128)
+    amax = blk.abs().amax(dim=(1, 3))
+    scale = torch.where(amax > 0, amax / FP8_MAX, torch.ones_like(amax))
+    q = (blk / scale[:, None, :, None]).clamp(-FP8_MAX, FP8_MAX).to(torch.float8_e4m3fn)
+    codes = q.view(torch.uint8).reshape(R, C).numpy().copy()
+    return codes, scale.numpy().astype(np.float32)
+
+
+# ----------------------------------------------------------------------------
+# host (numpy) generators: small cases and everything the CPU tests touch
+# ----------------------------------------------------------------------------
+
+def expert_fp32(wl: Workload, layer: int, expert: int, base_seed: int = 0):
+    """The three expert matrices as drawn (fp32, before storage rounding)."""
+    g = np_rng(seed_for(wl.name, layer, f"expert{expert}", base_seed))
+    w_gate = (g.standard_normal((wl.I, wl.H), dtype=np.float32) * np.float32(0.02))
+    w_up = (g.standard_normal((wl.I, wl.H), dtype=np.float32) * np.float32(0.02))
+    w_down = (g.standard_normal((wl.H, wl.I), dtype=np.float32) * np.float32(0.02))
+    return w_gate, w_up, w_down
+
+
+def encode_expert(wl: Workload, w_gate, w_up, w_down):
+    """Stored form of one expert: dict with w13 [2I,H], w2 [H,I] (+ s13, s2 for fp8)."""
+    w13 = np.concatenate([w_gate, w_up], axis=0)
+    if wl.weight_dtype == F32:
+        return {"w13": w13.astype(np.float32), "w2": np.asarray(w_down, np.float32)}
+    if wl.weight_dtype == BF16:
+        return {"w13": f32_to_bf16_bits(w13), "w2": f32_to_bf16_bits(w_down)}
+    c13, s13 = quantize_fp8_blocks(w13)
+    c2, s2 = quantize_fp8_blocks(w_down)
+    return {"w13": c13, "w2": c2, "s13": s13, "s2": s2}
+
+
+def expert_stored(wl: Workload, layer: int, expert: int, base_seed: int = 0):
+    return encode_expert(wl, *expert_fp32(wl, layer, expert, base_seed))
+
+
+def shared_expert_stored(wl: Workload, layer: int, base_seed: int = 0):
+    g = np_rng(seed_for(wl.name, layer, "shared", base_seed))
+    w_gate = g.standard_normal((wl.I, wl.H), dtype=np.float32) * np.float32(0.02)
+    w_up = g.standard_normal((wl.I, wl.H), dtype=np.float32) * np.float32(0.02)
+    w_down = g.standard_normal((wl.H, wl.I), dtype=np.float32) * np.float32(0.02)
+    return encode_expert(wl, w_gate, w_up, w_down)
+
+
+def expert_record_bytes(wl: Workload, stored) -> bytes:
+    """Pack one stored expert into the host-pool record layout (padded)."""
+    o13, o2, os13, os2, rec = wl.expert_layout()
+    buf = np.zeros(rec, np.uint8)
+    for key, off in (("w13", o13), ("w2", o2), ("s13", os13), ("s2", os2)):
+        if key in stored:
+            raw = np.ascontiguousarray(stored[key]).view(np.uint8).ravel()
+            buf[off:off + raw.size] = raw
+    return buf
+
+
+def zipf_bias(wl: Workload, layer: int, s: float, base_seed: int = 0) -> np.ndarray:
+    """b_e = -s * ln(rank_e); rank is a seeded permutation of 1..E."""
+    g = np_rng(seed_for(wl.name, layer, "rank", base_seed))
+    rank = g.permutation(wl.E) + 1
+    return (-s * np.log(rank.astype(np.float64))).astype(np.float32)
+
+
+def router_stored(wl: Workload, layer: int, s=None, base_seed: int = 0):
+    """(W_r stored [E,H] as fp32 or bf16 bits, bias fp32 [E])."""
+    g = np_rng(seed_for(wl.name, layer, "router", base_seed))
+    w = g.standard_normal((wl.E, wl.H), dtype=np.float32) * np.float32(0.02)
+    b = zipf_bias(wl, layer, wl.zipf_s if s is None else s, base_seed)
+    if wl.act_dtype == BF16:
+        return f32_to_bf16_bits(w), b
+    return w, b
+
+
+def decode_hidden(wl: Workload, layer: int, T: int, steps: int, base_seed: int = 0):
+    """AR(1) hidden states [steps, T, H] as drawn in fp32 (store with store_act)."""
+    g = np_rng(seed_for(wl.name, layer, f"ar1_T{T}", base_seed))
+    rho = np.float32(wl.ar_rho)
+    c = np.float32(math.sqrt(1.0 - wl.ar_rho ** 2))
+    out = np.empty((steps, T, wl.H), np.float32)
+    x = g.standard_normal((T, wl.H), dtype=np.float32)
+    for t in range(steps):
+        if t > 0:
+            x = rho * x + c * g.standard_normal((T, wl.H), dtype=np.float32)
+        out[t] = x
+    return out
+
+
+def prefill_hidden(wl: Workload, layer: int, T: int, base_seed: int = 0):
+    g = np_rng(seed_for(wl.name, layer, f"prefill_T{T}", base_seed))
+    return g.standard_normal((T, wl.H), dtype=np.float32)
+
+
+def store_act(wl: Workload, x: np.ndarray) -> np.ndarray:
+    """Activation storage: fp32 as is, bf16 as uint16 bits."""
+    if wl.act_dtype == BF16:
+        return f32_to_bf16_bits(x)
+    return np.ascontiguousarray(x, np.float32)
+
+
+def initial_lut(wl: Workload, base_seed: int = 0, S=None) -> np.ndarray:
+    """Per layer a seeded random quota(l) experts, slots handed out in draw order."""
+    S = wl.S if S is None else S
+    lut = np.full((wl.L, wl.E), -1, np.int32)
+    nxt = 0
+    base, extra = divmod(S, wl.L)
+    for l in range(wl.L):
+        q = min(base + (1 if l < extra else 0), wl.E)
+        g = np_rng(seed_for(wl.name, l, "fill", base_seed))
+        for e in g.permutation(wl.E)[:q]:
+            lut[l, e] = nxt
+            nxt += 1
+    return lut
+
+
+# ----------------------------------------------------------------------------
+# device (torch) generators for full-size weights
+# ----------------------------------------------------------------------------
+
+def torch_expert_chunk(wl: Workload, layer: int, e0: int, n: int, device, base_seed: int = 0):
+    """Draw experts [e0, e0+n) of one layer on `device`; returns (w13 [n,2I,H], w2 [n,H,I]) fp32."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed_for(wl.name, layer, f"dev_experts{e0}_{n}", base_seed))
+    w13 = torch.randn((n, 2 * wl.I, wl.H), generator=g, device=device, dtype=torch.float32).mul_(0.02)
+    w2 = torch.randn((n, wl.H, wl.I), generator=g, device=device, dtype=torch.float32).mul_(0.02)
+    return w13, w2
+
+
+def torch_quantize_fp8_blocks(w):
+    """Device version of quantize_fp8_blocks for [n, R, C] fp32 -> (uint8 [n,R,C], fp32 [n,R/128,C/128])."""
+    import torch
+    n, R, C = w.shape
+    blk = w.view(n, R // 128, 128, C // 128, 128)
+    amax = blk.abs().amax(dim=(2, 4))
+    scale = torch.where(amax > 0, amax / FP8_MAX, torch.ones_like(amax))
+    q = (blk / scale[:, :, None, :, None]).clamp(-FP8_MAX, FP8_MAX).to(torch.float8_e4m3fn)
+    return q.view(torch.uint8).reshape(n, R, C), scale.contiguous()
+
+
+def torch_encode_records(wl: Workload, w13, w2):
+    """Stored records [n, record_bytes] uint8 on the device from fp32 w13/w2 chunks."""
+    import torch
+    n = w13.shape[0]
+    o13, o2, os13, os2, rec = wl.expert_layout()
+    out = torch.zeros((n, rec), dtype=torch.uint8, device=w13.device)
+    if wl.weight_dtype == F32:
+        parts = [(o13, w13.contiguous()), (o2, w2.contiguous())]
+    elif wl.weight_dtype == BF16:
+        parts = [(o13, w13.to(torch.bfloat16)), (o2, w2.to(torch.bfloat16))]
+    else:
+        c13, s13 = torch_quantize_fp8_blocks(w13)
+        c2, s2 = torch_quantize_fp8_blocks(w2)
+        parts = [(o13, c13), (o2, c2), (os13, s13), (os2, s2)]
+    for off, t in parts:
+        raw = t.contiguous().view(n, -1).view(torch.uint8)
+        out[:, off:off + raw.shape[1]] = raw
+    return out
