@@ -1,0 +1,544 @@
+// C ABI of libmoeslot (declared in include/moeslot.h): argument checks, the
+// pool's device memory, and the per-layer launch sequence.
+//
+// Decode / slot-pool forward of one layer, all on the caller's stream:
+//   route_logits -> gate_topk -> plan (history, table, victims, permutation)
+//   -> miss_copy (device-started, from the mapped host pool) -> gate_up -> down
+// Nothing in that sequence synchronises with the host or allocates, so it can
+// be captured in a CUDA graph (SeqMoE "Mechanism": the graph never waits for
+// the host to notice a miss).
+//
+// Staged prefill (MoE-CORE "Mechanism"): two staging regions, each one whole
+// MoE layer; layer l reads region l mod 2; while it computes, the other region
+// holds (or receives) layer l+1, and the region l releases is refilled with
+// layer l+2 on the pool's copy stream.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "moeslot_internal.cuh"
+
+using namespace moeslot;
+
+namespace moeslot {
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+}  // namespace moeslot
+
+static thread_local std::string g_err;
+
+static moe_status fail(moe_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return st;
+}
+
+#define CUDA_TRY(call)                                                                    \
+  do {                                                                                    \
+    cudaError_t e_ = (call);                                                              \
+    if (e_ != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
+  } while (0)
+
+struct moe_pool {
+  moe_config cfg;
+  int device = 0;
+  PoolDev d;
+  Scratch sc;
+  const uint8_t* host_pool = nullptr;
+  size_t host_bytes = 0;
+  const void* router_w = nullptr;
+  const float* router_b = nullptr;
+  int last_T = 0;
+  bool last_gap_valid = false;
+  cudaStream_t copy_stream = nullptr;
+  cudaEvent_t ready[2] = {nullptr, nullptr};
+  cudaEvent_t released[2] = {nullptr, nullptr};
+  int staged_layer[2] = {-1, -1};
+  uint64_t staged_count = 0;
+  uint64_t launches = 0;
+  std::vector<void*> allocs;
+};
+
+static size_t elt_bytes(int dt) { return dt == MOE_F32 ? 4 : dt == MOE_BF16 ? 2 : 1; }
+
+static moe_status check_config(const moe_config* c) {
+  if (!c) return fail(MOE_ERR_INVALID, "config is NULL");
+  if (c->num_layers < 1) return fail(MOE_ERR_INVALID, "num_layers must be >= 1");
+  if (c->num_experts < 1 || c->num_experts > 256) return fail(MOE_ERR_INVALID, "num_experts must be in 1..256");
+  if (c->top_k < 1 || c->top_k > c->num_experts || c->top_k > 32)
+    return fail(MOE_ERR_INVALID, "top_k must be in 1..min(num_experts, 32)");
+  if (c->num_slots < 1) return fail(MOE_ERR_INVALID, "num_slots must be >= 1");
+  if (c->window < 1 || c->window > 64) return fail(MOE_ERR_INVALID, "window must be in 1..64");
+  if (c->max_tokens < 1) return fail(MOE_ERR_INVALID, "max_tokens must be >= 1");
+  if (c->gating != MOE_GATE_SOFTMAX_RENORM && c->gating != MOE_GATE_SIGMOID_RENORM)
+    return fail(MOE_ERR_INVALID, "unknown gating");
+  if (c->evict_policy < MOE_EVICT_CORE || c->evict_policy > MOE_EVICT_LRU)
+    return fail(MOE_ERR_INVALID, "unknown evict_policy");
+  if (c->staging_regions != 0 && c->staging_regions != 2)
+    return fail(MOE_ERR_INVALID, "staging_regions must be 0 or 2");
+  if (c->has_shared_expert != 0 && c->has_shared_expert != 1)
+    return fail(MOE_ERR_INVALID, "has_shared_expert must be 0 or 1");
+  if (!(c->ema_decay >= 0.f && c->ema_decay <= 1.f)) return fail(MOE_ERR_INVALID, "ema_decay must be in [0, 1]");
+  for (int i = 0; i < 4; ++i)
+    if (!(c->core_w[i] >= 0.f)) return fail(MOE_ERR_INVALID, "core_w must be nonnegative");
+  const bool ok_pair = (c->weight_dtype == MOE_F32 && c->act_dtype == MOE_F32) ||
+                       (c->weight_dtype == MOE_BF16 && c->act_dtype == MOE_BF16) ||
+                       (c->weight_dtype == MOE_FP8_E4M3_B128 && c->act_dtype == MOE_BF16);
+  if (!ok_pair) return fail(MOE_ERR_INVALID, "supported (weight, act) dtypes: (f32,f32), (bf16,bf16), (fp8,bf16)");
+  const int cw = (int)(16 / elt_bytes(c->weight_dtype));
+  const int ca = (int)(16 / elt_bytes(c->act_dtype));
+  const int q = cw > ca ? cw : ca;
+  if (c->hidden < q || c->hidden % q || c->inter < q || c->inter % q)
+    return fail(MOE_ERR_INVALID, "hidden and inter must be positive multiples of %d for these dtypes", q);
+  if (c->weight_dtype == MOE_FP8_E4M3_B128 && (c->hidden % 128 || c->inter % 128))
+    return fail(MOE_ERR_INVALID, "fp8 block-scaled weights need hidden and inter multiples of 128");
+  return MOE_OK;
+}
+
+static Layout layout_of(const moe_config* c) {
+  Layout L;
+  const size_t eb = elt_bytes(c->weight_dtype);
+  const size_t H = c->hidden, I = c->inter;
+  const size_t w13 = 2 * I * H * eb, w2 = H * I * eb;
+  size_t s13 = 0, s2 = 0;
+  if (c->weight_dtype == MOE_FP8_E4M3_B128) {
+    s13 = (2 * I / 128) * (H / 128) * 4;
+    s2 = (H / 128) * (I / 128) * 4;
+  }
+  L.off13 = 0;
+  L.off2 = w13;
+  L.offs13 = w13 + w2;
+  L.offs2 = w13 + w2 + s13;
+  const size_t raw = w13 + w2 + s13 + s2;
+  L.rec = (raw + 4095) / 4096 * 4096;
+  return L;
+}
+
+// The API functions below were declared extern "C" by moeslot.h, so their
+// definitions keep C linkage.
+
+MOE_API const char* moe_last_error(void) { return g_err.c_str(); }
+
+MOE_API moe_status moe_expert_layout(const moe_config* cfg, size_t* w13_off, size_t* w2_off, size_t* s13_off,
+                                     size_t* s2_off, size_t* record_bytes) {
+  moe_status st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  const Layout L = layout_of(cfg);
+  if (w13_off) *w13_off = L.off13;
+  if (w2_off) *w2_off = L.off2;
+  if (s13_off) *s13_off = L.offs13;
+  if (s2_off) *s2_off = L.offs2;
+  if (record_bytes) *record_bytes = L.rec;
+  return MOE_OK;
+}
+
+MOE_API moe_status moe_host_alloc(size_t bytes, void** out) {
+  if (!out || bytes == 0) return fail(MOE_ERR_INVALID, "moe_host_alloc: bad arguments");
+  *out = nullptr;
+  cudaError_t e = cudaHostAlloc(out, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+  if (e != cudaSuccess) {
+    *out = nullptr;
+    return fail(MOE_ERR_OOM, "cudaHostAlloc(%zu): %s", bytes, cudaGetErrorString(e));
+  }
+  return MOE_OK;
+}
+
+MOE_API moe_status moe_host_free(void* p) {
+  if (!p) return MOE_OK;
+  CUDA_TRY(cudaFreeHost(p));
+  return MOE_OK;
+}
+
+static moe_status pool_alloc(moe_pool* P, void** out, size_t bytes) {
+  *out = nullptr;
+  if (bytes == 0) bytes = 16;
+  cudaError_t e = cudaMalloc(out, bytes);
+  if (e != cudaSuccess) {
+    *out = nullptr;
+    cudaGetLastError();
+    return fail(MOE_ERR_OOM, "cudaMalloc(%zu): %s", bytes, cudaGetErrorString(e));
+  }
+  P->allocs.push_back(*out);
+  return MOE_OK;
+}
+
+template <typename T>
+static moe_status palloc(moe_pool* P, T** out, size_t count, int fill_byte) {
+  void* v = nullptr;
+  moe_status st = pool_alloc(P, &v, count * sizeof(T));
+  if (st != MOE_OK) return st;
+  *out = static_cast<T*>(v);
+  if (cudaMemset(v, fill_byte, count * sizeof(T)) != cudaSuccess)
+    return fail(MOE_ERR_CUDA, "cudaMemset failed");
+  return MOE_OK;
+}
+
+static void pool_free_all(moe_pool* P) {
+  for (void* p : P->allocs) cudaFree(p);
+  P->allocs.clear();
+  for (int r = 0; r < 2; ++r) {
+    if (P->ready[r]) cudaEventDestroy(P->ready[r]);
+    if (P->released[r]) cudaEventDestroy(P->released[r]);
+  }
+  if (P->copy_stream) cudaStreamDestroy(P->copy_stream);
+}
+
+MOE_API moe_status moe_pool_create(const moe_config* cfg, const void* host_pool, size_t host_pool_bytes,
+                                   const void* router_w, const float* router_b, const void* shared_w, int device,
+                                   moe_pool** out) {
+  if (!out) return fail(MOE_ERR_INVALID, "out is NULL");
+  *out = nullptr;
+  moe_status st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  const Layout lay = layout_of(cfg);
+  const size_t L = cfg->num_layers, E = cfg->num_experts;
+  if (!host_pool) return fail(MOE_ERR_INVALID, "host_pool is NULL");
+  if (host_pool_bytes < L * E * lay.rec)
+    return fail(MOE_ERR_INVALID, "host_pool_bytes %zu < L*E*record_bytes %zu", host_pool_bytes, L * E * lay.rec);
+  if (!router_w || !router_b) return fail(MOE_ERR_INVALID, "router weights are NULL");
+  if (cfg->has_shared_expert && !shared_w) return fail(MOE_ERR_INVALID, "shared_w is NULL but has_shared_expert");
+  int ndev = 0;
+  CUDA_TRY(cudaGetDeviceCount(&ndev));
+  if (device < 0 || device >= ndev) return fail(MOE_ERR_INVALID, "device %d out of range", device);
+  CUDA_TRY(cudaSetDevice(device));
+
+  // The pool must be page-locked host memory: the staging copies are
+  // asynchronous DMA and the miss kernel reads it through its mapped address.
+  // (On a Grace host pageable memory is device-reachable too, so the memory
+  // type is checked explicitly.)
+  cudaPointerAttributes attr;
+  void* hdev = nullptr;
+  if (cudaPointerGetAttributes(&attr, host_pool) != cudaSuccess || attr.type != cudaMemoryTypeHost ||
+      cudaHostGetDevicePointer(&hdev, const_cast<void*>(host_pool), 0) != cudaSuccess || !hdev) {
+    cudaGetLastError();
+    return fail(MOE_ERR_INVALID, "host_pool is not pinned, mapped host memory");
+  }
+
+  moe_pool* P = new moe_pool();
+  P->cfg = *cfg;
+  P->device = device;
+  P->host_pool = static_cast<const uint8_t*>(host_pool);
+  P->host_bytes = host_pool_bytes;
+  P->router_w = router_w;
+  P->router_b = router_b;
+  PoolDev& d = P->d;
+  d.L = cfg->num_layers; d.E = cfg->num_experts; d.k = cfg->top_k; d.H = cfg->hidden; d.I = cfg->inter;
+  d.S = cfg->num_slots; d.W = cfg->window;
+  d.wdt = cfg->weight_dtype; d.adt = cfg->act_dtype; d.gating = cfg->gating;
+  d.shared = cfg->has_shared_expert; d.policy = cfg->evict_policy;
+  d.lam = cfg->ema_decay;
+  d.one_minus_lam = 1.0f - cfg->ema_decay;
+  d.cw0 = cfg->core_w[0]; d.cw1 = cfg->core_w[1]; d.cw2 = cfg->core_w[2]; d.cw3 = cfg->core_w[3];
+  d.lay = lay;
+  d.host_dev = static_cast<const uint8_t*>(hdev);
+  d.shared_w = static_cast<const uint8_t*>(shared_w);
+
+  const size_t S = d.S, W = d.W, Tm = cfg->max_tokens, k = d.k;
+  const size_t rows = Tm * k + Tm;
+  const size_t asz = elt_bytes(cfg->act_dtype);
+#define PA(ptr, n, fill)                         \
+  do {                                           \
+    st = palloc(P, &(ptr), (n), (fill));         \
+    if (st != MOE_OK) goto fail_out;             \
+  } while (0)
+  PA(d.slots, S * lay.rec, 0);
+  if (cfg->staging_regions == 2) PA(d.staging, 2 * E * lay.rec, 0);
+  else d.staging = nullptr;
+  PA(d.lut, L * E, 0xff);
+  PA(d.owner, S, 0xff);
+  PA(d.tag, S, 0);
+  PA(d.prot_epoch, S, 0);
+  PA(d.epoch, 1, 0);
+  PA(d.hist_s, L * W * E, 0);
+  PA(d.hist_sel, L * W * E, 0);
+  PA(d.ema, L * E, 0);
+  PA(d.last_sel, L * E, 0xff);
+  PA(d.score, L * E, 0);
+  PA(d.step, L, 0);
+  PA(d.status, 1, 0);
+  PA(d.stats, ST_COUNT, 0);
+  PA(P->sc.logits, Tm * E, 0);
+  PA(P->sc.probs, Tm * E, 0);
+  PA(P->sc.ids, Tm * k, 0);
+  PA(P->sc.w, Tm * k, 0);
+  PA(P->sc.gap, Tm, 0);
+  PA(P->sc.slots_out, Tm * k, 0);
+  PA(P->sc.perm_tok, rows, 0);
+  PA(P->sc.perm_w, rows, 0);
+  PA(P->sc.perm_ent, Tm * k, 0);
+  PA(P->sc.offs, E + 1, 0);
+  PA(P->sc.work, E + 1, 0);
+  PA(P->sc.n_work, 1, 0);
+  PA(P->sc.copies, E + 1, 0);
+  PA(P->sc.n_copy, 1, 0);
+  {
+    uint8_t* hb = nullptr;
+    PA(hb, rows * (size_t)d.I * asz, 0);
+    P->sc.h = hb;
+  }
+#undef PA
+  if (cudaStreamCreateWithFlags(&P->copy_stream, cudaStreamNonBlocking) != cudaSuccess) {
+    st = fail(MOE_ERR_CUDA, "cudaStreamCreate failed");
+    goto fail_out;
+  }
+  for (int r = 0; r < 2; ++r) {
+    if (cudaEventCreateWithFlags(&P->ready[r], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&P->released[r], cudaEventDisableTiming) != cudaSuccess) {
+      st = fail(MOE_ERR_CUDA, "cudaEventCreate failed");
+      goto fail_out;
+    }
+    cudaEventRecord(P->ready[r], P->copy_stream);
+    cudaEventRecord(P->released[r], P->copy_stream);
+  }
+  if (cudaDeviceSynchronize() != cudaSuccess) {
+    st = fail(MOE_ERR_CUDA, "pool initialisation failed: %s", cudaGetErrorString(cudaGetLastError()));
+    goto fail_out;
+  }
+  *out = P;
+  return MOE_OK;
+fail_out:
+  pool_free_all(P);
+  delete P;
+  return st;
+}
+
+MOE_API moe_status moe_pool_destroy(moe_pool* P) {
+  if (!P) return MOE_OK;
+  cudaSetDevice(P->device);
+  cudaDeviceSynchronize();
+  pool_free_all(P);
+  delete P;
+  return MOE_OK;
+}
+
+MOE_API moe_status moe_set_lut(moe_pool* P, const int32_t* lut_host, void* stream) {
+  if (!P || !lut_host) return fail(MOE_ERR_INVALID, "moe_set_lut: NULL argument");
+  const int L = P->d.L, E = P->d.E, S = P->d.S;
+  std::vector<int32_t> owner(S, -1);
+  for (int i = 0; i < L * E; ++i) {
+    const int s = lut_host[i];
+    if (s < -1 || s >= S) return fail(MOE_ERR_INVALID, "lut[%d] = %d is not a slot id or -1", i, s);
+    if (s >= 0) {
+      if (owner[s] >= 0) return fail(MOE_ERR_INVALID, "slot %d assigned twice", s);
+      owner[s] = i;
+    }
+  }
+  CUDA_TRY(cudaSetDevice(P->device));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CUDA_TRY(cudaStreamSynchronize(s));
+  CUDA_TRY(cudaMemcpy(P->d.lut, lut_host, sizeof(int32_t) * L * E, cudaMemcpyHostToDevice));
+  CUDA_TRY(cudaMemcpy(P->d.owner, owner.data(), sizeof(int32_t) * S, cudaMemcpyHostToDevice));
+  P->launches += launch_rebuild_owner(P->d, s);
+  const size_t rec = P->d.lay.rec;
+  for (int sl = 0; sl < S; ++sl) {
+    if (owner[sl] < 0) continue;
+    CUDA_TRY(cudaMemcpyAsync(P->d.slots + (size_t)sl * rec, P->host_pool + (size_t)owner[sl] * rec, rec,
+                             cudaMemcpyHostToDevice, s));
+  }
+  CUDA_TRY(cudaGetLastError());
+  return MOE_OK;
+}
+
+MOE_API moe_status moe_load_slot(moe_pool* P, int32_t layer, int32_t expert, int32_t slot, void* stream) {
+  if (!P) return fail(MOE_ERR_INVALID, "pool is NULL");
+  if (layer < 0 || layer >= P->d.L || expert < 0 || expert >= P->d.E || slot < 0 || slot >= P->d.S)
+    return fail(MOE_ERR_INVALID, "moe_load_slot: layer/expert/slot out of range");
+  CUDA_TRY(cudaSetDevice(P->device));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  P->launches += launch_load_slot(P->d, P->sc, layer, expert, slot, s);
+  P->launches += launch_miss_copy(P->d, P->sc, s);
+  CUDA_TRY(cudaGetLastError());
+  return MOE_OK;
+}
+
+static void stage_layer(moe_pool* P, int layer, int r) {
+  const size_t bytes = (size_t)P->d.E * P->d.lay.rec;
+  cudaStreamWaitEvent(P->copy_stream, P->released[r], 0);
+  cudaMemcpyAsync(P->d.staging + (size_t)r * bytes, P->host_pool + (size_t)layer * bytes, bytes,
+                  cudaMemcpyHostToDevice, P->copy_stream);
+  cudaEventRecord(P->ready[r], P->copy_stream);
+  P->staged_layer[r] = layer;
+  P->staged_count += 1;
+}
+
+static moe_status run_layer(moe_pool* P, int layer, const void* x, int T, void* out, bool staged,
+                            const int32_t* ids_in, const float* w_in, const float* probs_in, cudaStream_t s) {
+  PoolDev& d = P->d;
+  Scratch& sc = P->sc;
+  const int32_t* ids = ids_in ? ids_in : sc.ids;
+  const float* w = w_in ? w_in : sc.w;
+  const float* probs = probs_in ? probs_in : sc.probs;
+  int region = 0;
+  if (staged) {
+    region = layer % 2;
+    if (P->staged_layer[region] != layer) stage_layer(P, layer, region);
+    if (layer + 1 < d.L && P->staged_layer[1 - region] != layer + 1) stage_layer(P, layer + 1, 1 - region);
+    CUDA_TRY(cudaStreamWaitEvent(s, P->ready[region], 0));
+  }
+  if (!ids_in) {
+    P->launches += launch_route_logits(d, layer, x, T, P->router_w, P->router_b, sc.logits, s);
+    P->launches += launch_gate_topk(d, sc.logits, T, sc.ids, sc.w, sc.probs, sc.gap, s);
+  }
+  const int flags = staged ? (PLAN_HISTORY | PLAN_PERMUTE | PLAN_STAGED) : (PLAN_HISTORY | PLAN_CACHE | PLAN_PERMUTE);
+  P->launches += launch_plan(d, sc, layer, T, ids, w, probs, flags, region, s);
+  if (!staged) P->launches += launch_miss_copy(d, sc, s);
+  P->launches += launch_ffn(d, sc, T, x, out, T * d.k + T, s);
+  if (staged) {
+    CUDA_TRY(cudaEventRecord(P->released[region], s));
+    if (layer + 2 < d.L) stage_layer(P, layer + 2, region);
+  }
+  CUDA_TRY(cudaGetLastError());
+  if (ids_in) {
+    // keep the supplied routing for moe_get_routing
+    CUDA_TRY(cudaMemcpyAsync(sc.ids, ids_in, sizeof(int32_t) * T * d.k, cudaMemcpyDeviceToDevice, s));
+    CUDA_TRY(cudaMemcpyAsync(sc.w, w_in, sizeof(float) * T * d.k, cudaMemcpyDeviceToDevice, s));
+    CUDA_TRY(cudaMemcpyAsync(sc.probs, probs_in, sizeof(float) * T * d.E, cudaMemcpyDeviceToDevice, s));
+  }
+  P->last_T = T;
+  P->last_gap_valid = ids_in == nullptr;
+  return MOE_OK;
+}
+
+static int layer_quota_host(moe_pool* P, int layer) {
+  // K_l: slots layer l holds now (host copy of the owner table; AUTO mode only)
+  std::vector<int32_t> owner(P->d.S);
+  cudaMemcpy(owner.data(), P->d.owner, sizeof(int32_t) * P->d.S, cudaMemcpyDeviceToHost);
+  int n = 0;
+  for (int o : owner)
+    if (o >= 0 && o / P->d.E == layer) ++n;
+  return n;
+}
+
+MOE_API moe_status moe_forward(moe_pool* P, int32_t layer, const void* x, int32_t T, void* out, int32_t mode,
+                               void* stream) {
+  if (!P) return fail(MOE_ERR_INVALID, "pool is NULL");
+  if (layer < 0 || layer >= P->d.L) return fail(MOE_ERR_INVALID, "layer %d out of range", layer);
+  if (T < 0) return fail(MOE_ERR_INVALID, "T must be >= 0");
+  if (T > P->cfg.max_tokens) return fail(MOE_ERR_CAPACITY, "T=%d exceeds max_tokens=%d", T, P->cfg.max_tokens);
+  if (mode != MOE_MODE_AUTO && mode != MOE_MODE_DECODE && mode != MOE_MODE_PREFILL_STAGED)
+    return fail(MOE_ERR_INVALID, "unknown mode %d", mode);
+  if (T == 0) return MOE_OK;
+  if (!x || !out) return fail(MOE_ERR_INVALID, "x/out is NULL");
+  if (x == out) return fail(MOE_ERR_INVALID, "out must not alias x");
+  if (mode == MOE_MODE_PREFILL_STAGED && P->cfg.staging_regions != 2)
+    return fail(MOE_ERR_INVALID, "staged prefill needs staging_regions == 2");
+  CUDA_TRY(cudaSetDevice(P->device));
+  bool staged = mode == MOE_MODE_PREFILL_STAGED;
+  if (mode == MOE_MODE_AUTO && P->cfg.staging_regions == 2) {
+    const int Kl = layer_quota_host(P, layer);
+    staged = T >= Kl / P->d.k;
+  }
+  return run_layer(P, layer, x, T, out, staged, nullptr, nullptr, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+MOE_API moe_status moe_forward_routed(moe_pool* P, int32_t layer, const void* x, int32_t T, const int32_t* ids,
+                                      const float* w, const float* probs, void* out, void* stream) {
+  if (!P) return fail(MOE_ERR_INVALID, "pool is NULL");
+  if (layer < 0 || layer >= P->d.L) return fail(MOE_ERR_INVALID, "layer %d out of range", layer);
+  if (T < 0) return fail(MOE_ERR_INVALID, "T must be >= 0");
+  if (T > P->cfg.max_tokens) return fail(MOE_ERR_CAPACITY, "T=%d exceeds max_tokens=%d", T, P->cfg.max_tokens);
+  if (T == 0) return MOE_OK;
+  if (!x || !out || !ids || !w || !probs) return fail(MOE_ERR_INVALID, "NULL argument");
+  if (x == out) return fail(MOE_ERR_INVALID, "out must not alias x");
+  CUDA_TRY(cudaSetDevice(P->device));
+  return run_layer(P, layer, x, T, out, false, ids, w, probs, static_cast<cudaStream_t>(stream));
+}
+
+MOE_API moe_status moe_update_scores(moe_pool* P, int32_t layer, const int32_t* ids, const float* probs, int32_t T,
+                                     void* stream) {
+  if (!P) return fail(MOE_ERR_INVALID, "pool is NULL");
+  if (layer < 0 || layer >= P->d.L) return fail(MOE_ERR_INVALID, "layer %d out of range", layer);
+  if (T < 1) return fail(MOE_ERR_INVALID, "T must be >= 1");
+  if (T > P->cfg.max_tokens) return fail(MOE_ERR_CAPACITY, "T=%d exceeds max_tokens=%d", T, P->cfg.max_tokens);
+  if (!ids || !probs) return fail(MOE_ERR_INVALID, "NULL argument");
+  CUDA_TRY(cudaSetDevice(P->device));
+  P->launches += launch_plan(P->d, P->sc, layer, T, ids, nullptr, probs, PLAN_HISTORY, 0,
+                             static_cast<cudaStream_t>(stream));
+  CUDA_TRY(cudaGetLastError());
+  return MOE_OK;
+}
+
+MOE_API moe_status moe_get_status(moe_pool* P) {
+  if (!P) return fail(MOE_ERR_INVALID, "pool is NULL");
+  CUDA_TRY(cudaSetDevice(P->device));
+  CUDA_TRY(cudaDeviceSynchronize());
+  int32_t st = 0;
+  CUDA_TRY(cudaMemcpy(&st, P->d.status, sizeof st, cudaMemcpyDeviceToHost));
+  return static_cast<moe_status>(st);
+}
+
+MOE_API moe_status moe_clear_status(moe_pool* P) {
+  if (!P) return fail(MOE_ERR_INVALID, "pool is NULL");
+  CUDA_TRY(cudaSetDevice(P->device));
+  CUDA_TRY(cudaDeviceSynchronize());
+  CUDA_TRY(cudaMemset(P->d.status, 0, sizeof(int32_t)));
+  return MOE_OK;
+}
+
+MOE_API moe_status moe_get_routing(moe_pool* P, int32_t* ids, float* w, float* probs, float* gap, int32_t* slots,
+                                   int32_t* perm, int32_t* offs, int32_t cap_T, int32_t* T_out) {
+  if (!P) return fail(MOE_ERR_INVALID, "pool is NULL");
+  const int T = P->last_T, k = P->d.k, E = P->d.E;
+  if (T_out) *T_out = T;
+  if (cap_T < T) return fail(MOE_ERR_CAPACITY, "cap_T=%d < last T=%d", cap_T, T);
+  CUDA_TRY(cudaSetDevice(P->device));
+  CUDA_TRY(cudaDeviceSynchronize());
+  if (T == 0) return MOE_OK;
+  if (ids) CUDA_TRY(cudaMemcpy(ids, P->sc.ids, sizeof(int32_t) * T * k, cudaMemcpyDeviceToHost));
+  if (w) CUDA_TRY(cudaMemcpy(w, P->sc.w, sizeof(float) * T * k, cudaMemcpyDeviceToHost));
+  if (probs) CUDA_TRY(cudaMemcpy(probs, P->sc.probs, sizeof(float) * T * E, cudaMemcpyDeviceToHost));
+  if (gap) {
+    if (P->last_gap_valid) CUDA_TRY(cudaMemcpy(gap, P->sc.gap, sizeof(float) * T, cudaMemcpyDeviceToHost));
+    else
+      for (int t = 0; t < T; ++t) gap[t] = INFINITY;
+  }
+  if (slots) CUDA_TRY(cudaMemcpy(slots, P->sc.slots_out, sizeof(int32_t) * T * k, cudaMemcpyDeviceToHost));
+  if (perm) CUDA_TRY(cudaMemcpy(perm, P->sc.perm_ent, sizeof(int32_t) * T * k, cudaMemcpyDeviceToHost));
+  if (offs) CUDA_TRY(cudaMemcpy(offs, P->sc.offs, sizeof(int32_t) * (E + 1), cudaMemcpyDeviceToHost));
+  return MOE_OK;
+}
+
+MOE_API moe_status moe_get_state(moe_pool* P, int32_t* lut, int32_t* owner, uint32_t* tag, float* score) {
+  if (!P) return fail(MOE_ERR_INVALID, "pool is NULL");
+  CUDA_TRY(cudaSetDevice(P->device));
+  CUDA_TRY(cudaDeviceSynchronize());
+  const size_t LE = (size_t)P->d.L * P->d.E, S = P->d.S;
+  if (lut) CUDA_TRY(cudaMemcpy(lut, P->d.lut, sizeof(int32_t) * LE, cudaMemcpyDeviceToHost));
+  if (owner) CUDA_TRY(cudaMemcpy(owner, P->d.owner, sizeof(int32_t) * S, cudaMemcpyDeviceToHost));
+  if (tag) CUDA_TRY(cudaMemcpy(tag, P->d.tag, sizeof(uint32_t) * S, cudaMemcpyDeviceToHost));
+  if (score) CUDA_TRY(cudaMemcpy(score, P->d.score, sizeof(float) * LE, cudaMemcpyDeviceToHost));
+  return MOE_OK;
+}
+
+MOE_API moe_status moe_get_stats(moe_pool* P, moe_stats* out) {
+  if (!P || !out) return fail(MOE_ERR_INVALID, "NULL argument");
+  CUDA_TRY(cudaSetDevice(P->device));
+  CUDA_TRY(cudaDeviceSynchronize());
+  unsigned long long v[ST_COUNT];
+  CUDA_TRY(cudaMemcpy(v, P->d.stats, sizeof v, cudaMemcpyDeviceToHost));
+  out->steps = v[ST_STEPS];
+  out->hits = v[ST_HITS];
+  out->misses = v[ST_MISSES];
+  out->bypass = v[ST_BYPASS];
+  out->evictions = v[ST_EVICT];
+  out->bytes_copied = v[ST_BYTES];
+  out->near_ties = v[ST_NEAR_TIES];
+  out->staged_layers = P->staged_count;
+  return MOE_OK;
+}
+
+MOE_API uint64_t moe_launch_count(const moe_pool* P) { return P ? P->launches : 0; }

@@ -1,0 +1,77 @@
+// Step a6: the device-started miss copy (SeqMoE "Mechanism": the device owns
+// the cache metadata and starts the miss copy itself, from a kernel on the
+// main stream, out of a pinned, mapped host pool, so a captured graph never
+// waits for the host).  On GB300 the mapped host pool is read over
+// NVLink-C2C with 16-byte loads; the slot is written with 16-byte stores.
+//
+// The copy list is produced on the device by the plan kernel, so the grid is
+// fixed at launch: each CTA takes an equal share of every record.
+#include "moeslot_internal.cuh"
+
+namespace moeslot {
+
+constexpr int kCopyThreads = 512;
+constexpr int kCopyUnroll = 8;
+
+__global__ void __launch_bounds__(kCopyThreads)
+miss_copy_kernel(const CopyJob* __restrict__ jobs, const int32_t* __restrict__ n_jobs, size_t rec16) {
+  const int n = *n_jobs;
+  const size_t stride = (size_t)gridDim.x * kCopyThreads;
+  for (int j = 0; j < n; ++j) {
+    const uint4* __restrict__ src = reinterpret_cast<const uint4*>(jobs[j].src);
+    uint4* __restrict__ dst = reinterpret_cast<uint4*>(jobs[j].dst);
+    size_t i = (size_t)blockIdx.x * kCopyThreads + threadIdx.x;
+    for (; i + (kCopyUnroll - 1) * stride < rec16; i += kCopyUnroll * stride) {
+      uint4 v[kCopyUnroll];
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u) v[u] = __ldcs(src + i + u * stride);
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u) dst[i + u * stride] = v[u];
+    }
+    for (; i < rec16; i += stride) dst[i] = __ldcs(src + i);
+  }
+}
+
+int launch_miss_copy(const PoolDev& p, const Scratch& sc, cudaStream_t s) {
+  miss_copy_kernel<<<2 * sm_count(), kCopyThreads, 0, s>>>(sc.copies, sc.n_copy, p.lay.rec / 16);
+  return 1;
+}
+
+// Host-initiated placement (moe_load_slot): one thread updates the table —
+// the slot's occupant leaves, a previous slot of the expert becomes free, the
+// slot's tag grows — and writes a one-element copy list for miss_copy_kernel.
+__global__ void load_slot_kernel(PoolDev p, Scratch sc, int layer, int expert, int slot) {
+  const int le = layer * p.E + expert;
+  const int prev = p.lut[le];
+  if (prev == slot) {
+    *sc.n_copy = 0;
+    return;
+  }
+  if (prev >= 0 && prev < p.S) p.owner[prev] = -1;
+  const int occ = p.owner[slot];
+  if (occ >= 0 && occ < p.L * p.E) p.lut[occ] = -1;
+  p.owner[slot] = le;
+  p.lut[le] = slot;
+  p.tag[slot] += 1u;
+  sc.copies[0].src = p.host_dev + (size_t)le * p.lay.rec;
+  sc.copies[0].dst = p.slots + (size_t)slot * p.lay.rec;
+  *sc.n_copy = 1;
+}
+
+int launch_load_slot(const PoolDev& p, const Scratch& sc, int layer, int expert, int slot, cudaStream_t s) {
+  load_slot_kernel<<<1, 1, 0, s>>>(p, sc, layer, expert, slot);
+  return 1;
+}
+
+// After a whole-table upload: every occupied slot got a new occupant.
+__global__ void rebuild_owner_kernel(PoolDev p) {
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s < p.S && p.owner[s] >= 0) p.tag[s] += 1u;
+}
+
+int launch_rebuild_owner(const PoolDev& p, cudaStream_t s) {
+  rebuild_owner_kernel<<<(p.S + 255) / 256, 256, 0, s>>>(p);
+  return 1;
+}
+
+}  // namespace moeslot

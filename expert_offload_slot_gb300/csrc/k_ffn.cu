@@ -1,0 +1,306 @@
+// Steps a8 (SwiGLU experts) and a9 (weighted combine) for the memory-bound
+// token counts of decode.
+//
+// Expert (RapidMoE §4.5, Eq. 7): y = W_down (SiLU(W_gate x) ⊙ W_up x), SiLU on
+// the gate projection only.  Combine (CAP §II-A, Eq. 1; RapidMoE Table 2):
+// out[t] = sum_j w[t, j] * y_j(t) (+ the shared expert with weight 1).
+//
+// With a handful of tokens per expert the layer streams U expert records from
+// HBM once and does a few FMAs per weight: the bound is HBM bandwidth.  Two
+// kernels:
+//   gate_up : every warp owns a contiguous, balanced range of (expert, row i)
+//             pairs over all active experts; it streams gate row i and up row
+//             I+i once with 16-byte loads and serves every token of that expert
+//             from L1, writing h = SiLU(g) * u for each token row.
+//   down    : every CTA owns a block of output features; for each active expert
+//             in ascending id (shared expert last) it streams those W_down rows
+//             once and accumulates w * (W_down h) per token in shared memory.
+//             The combine is therefore fused, deterministic and atomic-free.
+// Weights may be fp32, bf16, or fp8 e4m3 with 128x128 fp32 block scales (the
+// scale multiplies each 16-element partial dot product, which stays inside
+// one 128-wide block).
+#include <cuda_fp8.h>
+
+#include "moeslot_internal.cuh"
+
+namespace moeslot {
+
+struct FfnArgs {
+  const WorkEntry* work;
+  const int32_t* n_work;
+  const void* x;
+  const int32_t* perm_tok;
+  const float* perm_w;
+  void* h;
+  void* out;
+  int H, I, T;
+  size_t off13, off2, offs13, offs2;
+};
+
+template <typename WT> struct WTraits;
+template <> struct WTraits<float> {
+  static constexpr int CW = 4;
+  static constexpr bool kScaled = false;
+  __device__ __forceinline__ static void cvt(const uint4& q, float* v) {
+    v[0] = __uint_as_float(q.x); v[1] = __uint_as_float(q.y);
+    v[2] = __uint_as_float(q.z); v[3] = __uint_as_float(q.w);
+  }
+};
+template <> struct WTraits<uint16_t> {
+  static constexpr int CW = 8;
+  static constexpr bool kScaled = false;
+  __device__ __forceinline__ static void cvt(const uint4& q, float* v) {
+    v[0] = bf16lo(q.x); v[1] = bf16hi(q.x); v[2] = bf16lo(q.y); v[3] = bf16hi(q.y);
+    v[4] = bf16lo(q.z); v[5] = bf16hi(q.z); v[6] = bf16lo(q.w); v[7] = bf16hi(q.w);
+  }
+};
+template <> struct WTraits<uint8_t> {   // fp8 e4m3 codes
+  static constexpr int CW = 16;
+  static constexpr bool kScaled = true;
+  __device__ __forceinline__ static void pair(uint32_t w, float* v) {
+    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
+    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+    v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+  }
+  __device__ __forceinline__ static void cvt(const uint4& q, float* v) {
+    pair(q.x, v); pair(q.y, v + 4); pair(q.z, v + 8); pair(q.w, v + 12);
+  }
+};
+
+// N activation elements starting at p (16-byte aligned) as fp32.
+template <typename AT, int N> struct Act;
+template <int N> struct Act<float, N> {
+  __device__ __forceinline__ static void load(const float* p, float* v) {
+#pragma unroll
+    for (int q = 0; q < N / 4; ++q) {
+      const float4 f = *reinterpret_cast<const float4*>(p + 4 * q);
+      v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
+    }
+  }
+  __device__ __forceinline__ static void store1(float* p, float v) { *p = v; }
+};
+template <int N> struct Act<uint16_t, N> {
+  __device__ __forceinline__ static void load(const uint16_t* p, float* v) {
+#pragma unroll
+    for (int q = 0; q < N / 8; ++q) {
+      const uint4 u = *reinterpret_cast<const uint4*>(p + 8 * q);
+      v[8 * q + 0] = bf16lo(u.x); v[8 * q + 1] = bf16hi(u.x);
+      v[8 * q + 2] = bf16lo(u.y); v[8 * q + 3] = bf16hi(u.y);
+      v[8 * q + 4] = bf16lo(u.z); v[8 * q + 5] = bf16hi(u.z);
+      v[8 * q + 6] = bf16lo(u.w); v[8 * q + 7] = bf16hi(u.w);
+    }
+  }
+  __device__ __forceinline__ static void store1(uint16_t* p, float v) { *p = f32_to_bf16_rn(v); }
+};
+
+__device__ __forceinline__ float silu(float a) { return a / (1.f + expf(-a)); }
+
+constexpr int kFfnWarps = 8;
+constexpr int kTokChunk = 8;    // tokens served per pass over a weight row
+
+template <typename WT, typename AT>
+__global__ void __launch_bounds__(kFfnWarps * 32)
+ffn_gate_up_kernel(FfnArgs a) {
+  constexpr int CW = WTraits<WT>::CW;
+  constexpr int UNR = CW == 16 ? 2 : 4;
+  constexpr int NT = kTokChunk;
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * kFfnWarps + (threadIdx.x >> 5);
+  const int nw = gridDim.x * kFfnWarps;
+  const int n_work = *a.n_work;
+  const int H = a.H, I = a.I;
+  const long long total = (long long)n_work * I;
+  const long long p0 = total * gw / nw, p1 = total * (gw + 1) / nw;
+  const AT* __restrict__ x = static_cast<const AT*>(a.x);
+  AT* __restrict__ hout = static_cast<AT*>(a.h);
+
+  for (long long pp = p0; pp < p1; ++pp) {
+    const int u = (int)(pp / I), i = (int)(pp % I);
+    const WorkEntry ent = a.work[u];
+    const WT* __restrict__ gate = reinterpret_cast<const WT*>(ent.rec + a.off13) + (size_t)i * H;
+    const WT* __restrict__ up = gate + (size_t)I * H;
+    const float* sg = nullptr;
+    const float* su = nullptr;
+    if constexpr (WTraits<WT>::kScaled) {
+      const float* s13 = reinterpret_cast<const float*>(ent.rec + a.offs13);
+      sg = s13 + (size_t)(i / 128) * (H / 128);
+      su = s13 + (size_t)((I + i) / 128) * (H / 128);
+    }
+    for (int tc = 0; tc < ent.n; tc += NT) {
+      const int nr = min(NT, ent.n - tc);
+      int tok[NT];
+#pragma unroll
+      for (int r = 0; r < NT; ++r) tok[r] = r < nr ? a.perm_tok[ent.row0 + tc + r] : 0;
+      float ag[NT], au[NT];
+#pragma unroll
+      for (int r = 0; r < NT; ++r) { ag[r] = 0.f; au[r] = 0.f; }
+      for (int h0 = lane * CW; h0 < H; h0 += 32 * CW * UNR) {
+        uint4 rg[UNR], ru[UNR];
+#pragma unroll
+        for (int q = 0; q < UNR; ++q) {
+          const int h = h0 + q * 32 * CW;
+          if (h < H) {
+            rg[q] = __ldcs(reinterpret_cast<const uint4*>(gate + h));
+            ru[q] = __ldcs(reinterpret_cast<const uint4*>(up + h));
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < UNR; ++q) {
+          const int h = h0 + q * 32 * CW;
+          if (h < H) {
+            float wg[CW], wu[CW];
+            WTraits<WT>::cvt(rg[q], wg);
+            WTraits<WT>::cvt(ru[q], wu);
+            float gs = 1.f, us = 1.f;
+            if constexpr (WTraits<WT>::kScaled) { gs = sg[h / 128]; us = su[h / 128]; }
+#pragma unroll
+            for (int r = 0; r < NT; ++r) {
+              if (r < nr) {
+                float xv[CW];
+                Act<AT, CW>::load(x + (size_t)tok[r] * H + h, xv);
+                float dg = 0.f, du = 0.f;
+#pragma unroll
+                for (int c = 0; c < CW; ++c) { dg = fmaf(wg[c], xv[c], dg); du = fmaf(wu[c], xv[c], du); }
+                if constexpr (WTraits<WT>::kScaled) { ag[r] = fmaf(gs, dg, ag[r]); au[r] = fmaf(us, du, au[r]); }
+                else { ag[r] += dg; au[r] += du; }
+              }
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < NT; ++r) {
+        if (r < nr) {
+          const float g = warp_sum(ag[r]);
+          const float uu = warp_sum(au[r]);
+          if (lane == 0) Act<AT, 8>::store1(hout + (size_t)(ent.row0 + tc + r) * I + i, silu(g) * uu);
+        }
+      }
+    }
+  }
+}
+
+constexpr int kDownRowsPerWarp = 2;
+constexpr int kDownRows = kFfnWarps * kDownRowsPerWarp;   // output features per CTA
+
+template <typename WT, typename AT>
+__global__ void __launch_bounds__(kFfnWarps * 32)
+ffn_down_combine_kernel(FfnArgs a) {
+  constexpr int CW = WTraits<WT>::CW;
+  constexpr int NT = kTokChunk;
+  constexpr int RPW = kDownRowsPerWarp;
+  extern __shared__ float acc_s[];   // [kDownRows][T]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int H = a.H, I = a.I, T = a.T;
+  const int h0 = blockIdx.x * kDownRows;
+  for (int j = threadIdx.x; j < kDownRows * T; j += blockDim.x) acc_s[j] = 0.f;
+  __syncthreads();
+  const int n_work = *a.n_work;
+  const AT* __restrict__ hin = static_cast<const AT*>(a.h);
+  int hr[RPW];
+#pragma unroll
+  for (int rr = 0; rr < RPW; ++rr) hr[rr] = min(h0 + warp * RPW + rr, H - 1);
+  for (int u = 0; u < n_work; ++u) {
+    const WorkEntry ent = a.work[u];
+    const WT* __restrict__ w2 = reinterpret_cast<const WT*>(ent.rec + a.off2);
+    const float* s2 = nullptr;
+    if constexpr (WTraits<WT>::kScaled) s2 = reinterpret_cast<const float*>(ent.rec + a.offs2);
+    for (int tc = 0; tc < ent.n; tc += NT) {
+      const int nr = min(NT, ent.n - tc);
+      float acc[RPW][NT];
+#pragma unroll
+      for (int rr = 0; rr < RPW; ++rr)
+#pragma unroll
+        for (int r = 0; r < NT; ++r) acc[rr][r] = 0.f;
+      for (int i0 = lane * CW; i0 < I; i0 += 32 * CW) {
+        float wv[RPW][CW];
+        float sc[RPW];
+#pragma unroll
+        for (int rr = 0; rr < RPW; ++rr) {
+          const uint4 q = __ldcs(reinterpret_cast<const uint4*>(w2 + (size_t)hr[rr] * I + i0));
+          WTraits<WT>::cvt(q, wv[rr]);
+          sc[rr] = 1.f;
+          if constexpr (WTraits<WT>::kScaled) sc[rr] = s2[(size_t)(hr[rr] / 128) * (I / 128) + i0 / 128];
+        }
+#pragma unroll
+        for (int r = 0; r < NT; ++r) {
+          if (r < nr) {
+            float hv[CW];
+            Act<AT, CW>::load(hin + (size_t)(ent.row0 + tc + r) * I + i0, hv);
+#pragma unroll
+            for (int rr = 0; rr < RPW; ++rr) {
+              float d = 0.f;
+#pragma unroll
+              for (int c = 0; c < CW; ++c) d = fmaf(wv[rr][c], hv[c], d);
+              if constexpr (WTraits<WT>::kScaled) acc[rr][r] = fmaf(sc[rr], d, acc[rr][r]);
+              else acc[rr][r] += d;
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < NT; ++r) {
+        if (r < nr) {
+          const int row = ent.row0 + tc + r;
+          const int t = a.perm_tok[row];
+          const float wgt = a.perm_w[row];
+#pragma unroll
+          for (int rr = 0; rr < RPW; ++rr) {
+            const float v = warp_sum(acc[rr][r]);
+            if (lane == 0 && h0 + warp * RPW + rr < H) {
+              float* dst = &acc_s[(warp * RPW + rr) * T + t];
+              *dst = *dst + wgt * v;
+            }
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  AT* __restrict__ out = static_cast<AT*>(a.out);
+  for (int j = threadIdx.x; j < kDownRows * T; j += blockDim.x) {
+    const int t = j / kDownRows, rr = j % kDownRows;
+    if (h0 + rr < H) Act<AT, 8>::store1(out + (size_t)t * H + h0 + rr, acc_s[rr * T + t]);
+  }
+}
+
+template <typename WT, typename AT>
+static int launch_ffn_t(const FfnArgs& a, int T, cudaStream_t s) {
+  static bool configured = false;
+  const size_t smem = (size_t)kDownRows * T * sizeof(float);
+  if (!configured) {
+    cudaFuncSetAttribute(ffn_down_combine_kernel<WT, AT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         200 * 1024);
+    configured = true;
+  }
+  ffn_gate_up_kernel<WT, AT><<<2 * sm_count(), kFfnWarps * 32, 0, s>>>(a);
+  ffn_down_combine_kernel<WT, AT><<<(a.H + kDownRows - 1) / kDownRows, kFfnWarps * 32, smem, s>>>(a);
+  return 2;
+}
+
+int launch_ffn(const PoolDev& p, const Scratch& sc, int T, const void* x, void* out, int max_rows,
+               cudaStream_t s) {
+  (void)max_rows;
+  FfnArgs a;
+  a.work = sc.work;
+  a.n_work = sc.n_work;
+  a.x = x;
+  a.perm_tok = sc.perm_tok;
+  a.perm_w = sc.perm_w;
+  a.h = sc.h;
+  a.out = out;
+  a.H = p.H;
+  a.I = p.I;
+  a.T = T;
+  a.off13 = p.lay.off13;
+  a.off2 = p.lay.off2;
+  a.offs13 = p.lay.offs13;
+  a.offs2 = p.lay.offs2;
+  if (p.wdt == MOE_F32) return launch_ffn_t<float, float>(a, T, s);
+  if (p.wdt == MOE_BF16) return launch_ffn_t<uint16_t, uint16_t>(a, T, s);
+  return launch_ffn_t<uint8_t, uint16_t>(a, T, s);
+}
+
+}  // namespace moeslot

@@ -1,0 +1,184 @@
+// Steps a1 (router projection) and a2 (gate + top-k).
+//
+// a1: z[t, e] = sum_h x[t, h] * W_r[e, h] + b[e]   (RapidMoE §2.1: the gate is a
+//     linear projection of the token).  fp32 accumulation of bf16/fp32 inputs.
+// a2: one warp per token.  Top-k by descending logit with ties to the lower
+//     expert id (RapidMoE §2.1); the k weights are renormalised (CAP §II-A,
+//     Eq. 1): softmax-renorm exp(z_j - z_max) / sum_topk exp(z_i - z_max), or
+//     sigmoid-renorm sigma(z_j) / sum_topk sigma(z_i).  It also writes the
+//     per-expert probability (full softmax or sigmoid) used by the routing
+//     history, and the gap between the k-th and (k+1)-th logit.
+#include "moeslot_internal.cuh"
+
+namespace moeslot {
+
+template <typename AT> struct Vec16;
+template <> struct Vec16<float> {
+  static constexpr int C = 4;
+  __device__ __forceinline__ static void load(const float* p, float* v) {
+    float4 q = __ldg(reinterpret_cast<const float4*>(p));
+    v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+  }
+};
+template <> struct Vec16<uint16_t> {   // bf16 bit patterns
+  static constexpr int C = 8;
+  __device__ __forceinline__ static void load(const uint16_t* p, float* v) {
+    uint4 q = __ldg(reinterpret_cast<const uint4*>(p));
+    v[0] = bf16lo(q.x); v[1] = bf16hi(q.x); v[2] = bf16lo(q.y); v[3] = bf16hi(q.y);
+    v[4] = bf16lo(q.z); v[5] = bf16hi(q.z); v[6] = bf16lo(q.w); v[7] = bf16hi(q.w);
+  }
+};
+
+constexpr int kRouteWarps = 8;   // experts per CTA (one per warp)
+constexpr int kRouteTok = 8;     // tokens per CTA row
+
+template <typename AT>
+__global__ void __launch_bounds__(kRouteWarps * 32)
+route_logits_kernel(const AT* __restrict__ x, const AT* __restrict__ wr, const float* __restrict__ b,
+                    float* __restrict__ z, int T, int E, int H) {
+  constexpr int C = Vec16<AT>::C;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * kRouteWarps + warp;
+  const int t0 = blockIdx.y * kRouteTok;
+  if (e >= E) return;
+  const int nt = min(kRouteTok, T - t0);
+  float acc[kRouteTok];
+#pragma unroll
+  for (int r = 0; r < kRouteTok; ++r) acc[r] = 0.f;
+  const AT* wrow = wr + (size_t)e * H;
+  for (int h = lane * C; h < H; h += 32 * C) {
+    float wv[C];
+    Vec16<AT>::load(wrow + h, wv);
+#pragma unroll
+    for (int r = 0; r < kRouteTok; ++r) {
+      if (r < nt) {
+        float xv[C];
+        Vec16<AT>::load(x + (size_t)(t0 + r) * H + h, xv);
+#pragma unroll
+        for (int c = 0; c < C; ++c) acc[r] = fmaf(wv[c], xv[c], acc[r]);
+      }
+    }
+  }
+  const float bias = b[e];
+#pragma unroll
+  for (int r = 0; r < kRouteTok; ++r) {
+    if (r < nt) {
+      float v = warp_sum(acc[r]);
+      if (lane == 0) z[(size_t)(t0 + r) * E + e] = v + bias;
+    }
+  }
+}
+
+int launch_route_logits(const PoolDev& p, int layer, const void* x, int T, const void* router_w,
+                        const float* router_b, float* logits, cudaStream_t s) {
+  dim3 grid((p.E + kRouteWarps - 1) / kRouteWarps, (T + kRouteTok - 1) / kRouteTok);
+  const size_t wofs = (size_t)layer * p.E * p.H;
+  const float* b = router_b + (size_t)layer * p.E;
+  if (p.adt == MOE_BF16) {
+    route_logits_kernel<uint16_t><<<grid, kRouteWarps * 32, 0, s>>>(
+        (const uint16_t*)x, (const uint16_t*)router_w + wofs, b, logits, T, p.E, p.H);
+  } else {
+    route_logits_kernel<float><<<grid, kRouteWarps * 32, 0, s>>>(
+        (const float*)x, (const float*)router_w + wofs, b, logits, T, p.E, p.H);
+  }
+  return 1;
+}
+
+// ------------------------------------------------------------------ gate + top-k
+constexpr int kGateWarps = 8;
+constexpr int kMaxPerLane = 8;   // E <= 256
+
+__global__ void __launch_bounds__(kGateWarps * 32)
+gate_topk_kernel(const float* __restrict__ z, int T, int E, int k, int gating, int32_t* __restrict__ ids,
+                 float* __restrict__ w, float* __restrict__ probs, float* __restrict__ gap,
+                 unsigned long long* stats) {
+  __shared__ float zsel[kGateWarps][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kGateWarps + warp;
+  if (t >= T) return;
+  float v[kMaxPerLane];
+  bool taken[kMaxPerLane];
+  float zmax = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < kMaxPerLane; ++j) {
+    const int e = lane + 32 * j;
+    taken[j] = e >= E;
+    v[j] = e < E ? z[(size_t)t * E + e] : -INFINITY;
+    zmax = fmaxf(zmax, v[j]);
+  }
+  zmax = warp_max(zmax);
+
+  // per-expert probability for the routing history
+  if (gating == MOE_GATE_SOFTMAX_RENORM) {
+    float part = 0.f, ex[kMaxPerLane];
+#pragma unroll
+    for (int j = 0; j < kMaxPerLane; ++j) {
+      ex[j] = taken[j] ? 0.f : expf(v[j] - zmax);
+      part += ex[j];
+    }
+    const float den = warp_sum(part);
+#pragma unroll
+    for (int j = 0; j < kMaxPerLane; ++j)
+      if (!taken[j]) probs[(size_t)t * E + lane + 32 * j] = ex[j] / den;
+  } else {
+#pragma unroll
+    for (int j = 0; j < kMaxPerLane; ++j)
+      if (!taken[j]) probs[(size_t)t * E + lane + 32 * j] = 1.f / (1.f + expf(-v[j]));
+  }
+
+  // top-k: k rounds of a warp arg-max (ties to the lower expert id), plus one
+  // more round for the best unselected logit when k < E
+  float next_best = INFINITY;
+  const int rounds = k < E ? k + 1 : k;
+  for (int r = 0; r < rounds; ++r) {
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < kMaxPerLane; ++j) {
+      const int e = lane + 32 * j;
+      if (!taken[j] && (v[j] > bv || (v[j] == bv && e < be))) { bv = v[j]; be = e; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+    }
+    if (r < k) {
+#pragma unroll
+      for (int j = 0; j < kMaxPerLane; ++j)
+        if (lane + 32 * j == be) taken[j] = true;
+      if (lane == 0) {
+        ids[(size_t)t * k + r] = be;
+        zsel[warp][r] = bv;
+      }
+    } else {
+      next_best = bv;
+    }
+  }
+  __syncwarp();
+  const float zk = zsel[warp][k - 1];
+  const float g = k < E ? zk - next_best : INFINITY;
+  if (lane == 0) {
+    gap[t] = g;
+    if (g < 1e-4f) atomicAdd(&stats[ST_NEAR_TIES], 1ull);
+  }
+  // renormalised weights of the k selected experts
+  float num = 0.f;
+  if (lane < k) {
+    const float zj = zsel[warp][lane];
+    num = gating == MOE_GATE_SOFTMAX_RENORM ? expf(zj - zmax) : 1.f / (1.f + expf(-zj));
+  }
+  const float den = warp_sum(num);
+  if (lane < k) w[(size_t)t * k + lane] = num / den;
+}
+
+int launch_gate_topk(const PoolDev& p, const float* logits, int T, int32_t* ids, float* w, float* probs,
+                     float* gap, cudaStream_t s) {
+  const int grid = (T + kGateWarps - 1) / kGateWarps;
+  gate_topk_kernel<<<grid, kGateWarps * 32, 0, s>>>(logits, T, p.E, p.k, p.gating, ids, w, probs, gap,
+                                                     p.stats);
+  return 1;
+}
+
+}  // namespace moeslot

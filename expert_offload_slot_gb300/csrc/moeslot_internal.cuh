@@ -1,0 +1,132 @@
+// Internal declarations of libmoeslot: the pool object, the per-call work
+// list shared between kernels, and small device helpers.  Nothing here is
+// part of the C ABI (include/moeslot.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moeslot.h"
+
+namespace moeslot {
+
+// One expert that this call must evaluate: its record (slot, staging region,
+// host pool for a bypassed miss, or the shared expert), and its rows
+// [row0, row0 + n) of the expert-sorted token order.
+struct WorkEntry {
+  const uint8_t* rec;
+  int32_t row0;
+  int32_t n;
+  int32_t expert;   // routed expert id, or -1 for the shared expert
+  int32_t pad;
+};
+
+// One device-started miss copy: record bytes from the mapped host pool to a slot.
+struct CopyJob {
+  const uint8_t* src;
+  uint8_t* dst;
+};
+
+enum StatIdx {
+  ST_STEPS = 0, ST_HITS, ST_MISSES, ST_BYPASS, ST_EVICT, ST_BYTES, ST_NEAR_TIES, ST_STAGED, ST_COUNT
+};
+
+// Plan-kernel switches.
+enum PlanFlags {
+  PLAN_HISTORY = 1,    // a3: update routing history and eviction scores
+  PLAN_CACHE = 2,      // a4/a5: table rewrite, misses, victims, copy list
+  PLAN_PERMUTE = 4,    // a7 + work list
+  PLAN_STAGED = 8      // work list points into a staging region (identity table)
+};
+
+struct Layout {
+  size_t rec, off13, off2, offs13, offs2;
+};
+
+struct PoolDev {           // device-side pointers handed to kernels by value
+  int32_t L, E, k, H, I, S, W;
+  int32_t wdt, adt, gating, shared, policy;
+  float lam, one_minus_lam, cw0, cw1, cw2, cw3;
+  Layout lay;
+  const uint8_t* host_dev;     // device-visible base of the mapped host pool
+  uint8_t* slots;              // fixed base of the slot pool
+  uint8_t* staging;            // 2 * E records, or null
+  const uint8_t* shared_w;     // L shared-expert records, or null
+  int32_t* lut;                // [L*E]
+  int32_t* owner;              // [S]
+  uint32_t* tag;               // [S]
+  int32_t* prot_epoch;         // [S]
+  int32_t* epoch;              // [1]
+  float* hist_s;               // [L][W][E]
+  uint8_t* hist_sel;           // [L][W][E]
+  float* ema;                  // [L][E]
+  int32_t* last_sel;           // [L][E]
+  float* score;                // [L][E]
+  int32_t* step;               // [L]
+  int32_t* status;             // sticky
+  unsigned long long* stats;   // [ST_COUNT]
+};
+
+struct Scratch {
+  float* logits;      // [Tmax, E]
+  float* probs;       // [Tmax, E]
+  int32_t* ids;       // [Tmax, k]
+  float* w;           // [Tmax, k]
+  float* gap;         // [Tmax]
+  int32_t* slots_out; // [Tmax, k]
+  int32_t* perm_tok;  // [Tmax*k + Tmax]   token of each expert-sorted row
+  float* perm_w;      // [Tmax*k + Tmax]   routing weight of each row
+  int32_t* perm_ent;  // [Tmax*k]          flat entry t*k+j of each row
+  int32_t* offs;      // [E+1]
+  WorkEntry* work;    // [E+1]
+  int32_t* n_work;    // [1]
+  CopyJob* copies;    // [E+1]
+  int32_t* n_copy;    // [1]
+  void* h;            // [(Tmax*k + Tmax), I] act dtype
+};
+
+// ----------------------------------------------------------------- device helpers
+__device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
+  atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x40);  // quiet NaN
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// ----------------------------------------------------------------- launchers
+// Each returns the number of kernels it launched (0 or more); errors from the
+// launch itself surface through cudaGetLastError in the caller.
+int launch_route_logits(const PoolDev& p, int layer, const void* x, int T, const void* router_w,
+                        const float* router_b, float* logits, cudaStream_t s);
+int launch_gate_topk(const PoolDev& p, const float* logits, int T, int32_t* ids, float* w, float* probs,
+                     float* gap, cudaStream_t s);
+int launch_plan(const PoolDev& p, const Scratch& sc, int layer, int T, const int32_t* ids, const float* w,
+                const float* probs, int flags, int region, cudaStream_t s);
+int launch_miss_copy(const PoolDev& p, const Scratch& sc, cudaStream_t s);
+int launch_ffn(const PoolDev& p, const Scratch& sc, int T, const void* x, void* out, int max_rows,
+               cudaStream_t s);
+int launch_load_slot(const PoolDev& p, const Scratch& sc, int layer, int expert, int slot, cudaStream_t s);
+int launch_rebuild_owner(const PoolDev& p, cudaStream_t s);
+
+int sm_count();
+
+}  // namespace moeslot

@@ -1,0 +1,216 @@
+/*
+ * moeslot.h — C ABI of a routed Mixture-of-Experts layer whose experts are read
+ * from one shared, fixed-address slot pool on a single GB300 GPU (sm_103a).
+ *
+ * What the layer computes (one call of moe_forward, one MoE layer, T tokens):
+ *   a1 router        z = x · W_rᵀ + b                      RapidMoE §2.1
+ *   a2 gate + top-k  softmax- or sigmoid-renormalised over the k largest
+ *                    logits                                  RapidMoE §2.1; CAP §II-A Eq. 1
+ *   a3 history       per-expert routing history and eviction score
+ *                    (MoE-CORE windowed/EMA score, HybriMoE Minus Recent
+ *                    Score, or LRU)                          MoE-CORE "Mechanism"; HybriMoE "Mechanism"
+ *   a4 table         expert_id -> slot_id lookup; resident/missing detection
+ *                                                            SeqMoE "Mechanism"
+ *   a5 victims       a missing expert takes a free slot or the lowest-score
+ *                    slot that this step does not need       MoE-CORE / HybriMoE "Mechanism"
+ *   a6 miss copy     started by the device: a kernel reads the expert from
+ *                    the pinned, mapped host pool into its slot  SeqMoE "Mechanism"
+ *   a7 permute       token rows grouped by expert (stable)
+ *   a8 experts       SwiGLU: W_down (SiLU(W_gate x) ⊙ W_up x)   RapidMoE §4.5 Eq. 7
+ *   a9 combine       out[t] = Σ_j w[t,j] · y_j (+ shared expert, weight 1)
+ *                                                            CAP §II-A Eq. 1; RapidMoE Table 2
+ *   a10 staging      large prefills read whole layers from two swapped
+ *                    layer-sized staging regions             MoE-CORE "Mechanism"
+ *
+ * Conventions
+ *   - Every call is stream-ordered and asynchronous unless it says otherwise.
+ *   - Argument errors are returned synchronously (MOE_ERR_INVALID) and nothing
+ *     is launched.
+ *   - Errors the device finds (an out-of-range id or slot) are written once
+ *     into a sticky device status word; moe_get_status() reads it.  Kernels
+ *     never trap.
+ *   - No C++ exception crosses this boundary.
+ *   - The pool owns every device buffer it allocates (slots, staging regions,
+ *     table, history, per-call scratch).  The caller owns the host pool, the
+ *     router and shared-expert weights, x and out.
+ *   - A decode call (MOE_MODE_DECODE) performs no host synchronisation and
+ *     allocates nothing, so a sequence of such calls can be captured into a
+ *     CUDA graph.
+ *   - One pool must not be used from two streams at once: calls on one pool
+ *     share its scratch and its table.
+ *
+ * Expert record (the unit of the host pool, of a slot and of a staging region)
+ *   w13  [2I, H] row-major: rows 0..I-1 are W_gate, rows I..2I-1 are W_up
+ *   w2   [H, I]  row-major: W_down
+ *   s13  [2I/128, H/128] fp32 block scales   (MOE_FP8_E4M3_B128 only)
+ *   s2   [H/128, I/128]  fp32 block scales   (MOE_FP8_E4M3_B128 only)
+ *   The record is padded to a multiple of 4096 bytes; moe_expert_layout()
+ *   returns the offsets.  Element (i, j) of a block-scaled fp8 matrix is
+ *   e4m3(q[i,j]) * scale[i/128][j/128].
+ */
+#ifndef MOESLOT_H
+#define MOESLOT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+typedef struct moe_pool moe_pool;   /* opaque */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID = 1,    /* bad argument or configuration                      */
+  MOE_ERR_OOM = 2,        /* a device allocation failed                         */
+  MOE_ERR_CUDA = 3,       /* a CUDA runtime call failed                         */
+  MOE_ERR_CAPACITY = 4,   /* T exceeds the pool's max_tokens                    */
+  MOE_ERR_TIMEOUT = 5,    /* a bounded device-side wait gave up (reserved)      */
+  MOE_ERR_TAG = 6,        /* a slot tag did not match (reserved)                */
+  MOE_ERR_BOUNDS = 7      /* the device met an expert id or slot out of range   */
+} moe_status;
+
+enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_FP8_E4M3_B128 = 2 };          /* dtypes   */
+enum { MOE_GATE_SOFTMAX_RENORM = 0, MOE_GATE_SIGMOID_RENORM = 1 };  /* gating   */
+enum { MOE_EVICT_CORE = 0, MOE_EVICT_MRS = 1, MOE_EVICT_LRU = 2 };  /* policy   */
+enum { MOE_MODE_AUTO = 0, MOE_MODE_DECODE = 1, MOE_MODE_PREFILL_STAGED = 2 };
+
+typedef struct {
+  int32_t num_layers;        /* L                                                  */
+  int32_t num_experts;       /* E routed experts per layer, 1..256                 */
+  int32_t top_k;             /* k, 1..min(E, 32)                                   */
+  int32_t hidden;            /* H: multiple of 128 (f32), 256 (bf16), 512 (fp8)   */
+  int32_t inter;             /* I: multiple of 128 (f32), 256 (bf16), 512 (fp8)   */
+  int32_t num_slots;         /* S slots in the shared pool, >= 1                   */
+  int32_t weight_dtype;      /* MOE_F32, MOE_BF16 or MOE_FP8_E4M3_B128             */
+  int32_t act_dtype;         /* MOE_F32 or MOE_BF16 (x, out, router weights)       */
+  int32_t gating;            /* MOE_GATE_*                                         */
+  int32_t has_shared_expert; /* 0 or 1: one always-resident shared expert / layer  */
+  int32_t evict_policy;      /* MOE_EVICT_*                                        */
+  int32_t window;            /* W steps of routing history, 1..64 (16 typical)     */
+  float ema_decay;           /* lambda of the selection EMA (0.9 typical)          */
+  float core_w[4];           /* MoE-CORE weights: count, EMA, score, recency       */
+  int32_t staging_regions;   /* 0, or 2 for double-buffered full-layer prefill     */
+  int32_t max_tokens;        /* largest T any call on this pool will pass          */
+} moe_config;
+
+typedef struct {
+  uint64_t steps;            /* history updates performed                          */
+  uint64_t hits;             /* needed experts found resident                      */
+  uint64_t misses;           /* needed experts not resident                        */
+  uint64_t bypass;           /* misses read straight from the host pool (no slot)  */
+  uint64_t evictions;        /* occupants replaced                                 */
+  uint64_t bytes_copied;     /* host -> slot bytes moved by miss copies            */
+  uint64_t near_ties;        /* tokens whose k-th/(k+1)-th logit gap is < 1e-4     */
+  uint64_t staged_layers;    /* layers copied into a staging region               */
+} moe_stats;
+
+/* Byte layout of one expert record for `cfg` (see the header comment).  Any
+ * output pointer may be NULL.  Returns MOE_ERR_INVALID for a bad config. */
+MOE_API moe_status moe_expert_layout(const moe_config* cfg, size_t* w13_off, size_t* w2_off,
+                                     size_t* s13_off, size_t* s2_off, size_t* record_bytes);
+
+/* Pinned, mapped host memory for a host pool (cudaHostAlloc with the mapped
+ * and portable flags).  Blocking.  Free it with moe_host_free. */
+MOE_API moe_status moe_host_alloc(size_t bytes, void** out);
+MOE_API moe_status moe_host_free(void* p);
+
+/* Create a pool on `device`.  Blocking; allocates all device memory the pool
+ * will ever use (slots: num_slots records at one fixed base address).
+ *   host_pool       caller-owned pinned host memory (moe_host_alloc, or
+ *                   cudaHostAlloc/cudaHostRegister with the mapped flag) holding
+ *                   L*E expert records, record (l, e) at (l*E + e)*record_bytes;
+ *                   it must stay valid and unchanged while the pool lives
+ *   host_pool_bytes at least L*E*record_bytes
+ *   router_w        device, [L][E][H] in act_dtype; caller-owned, outlives pool
+ *   router_b        device, fp32 [L][E]; caller-owned, outlives pool
+ *   shared_w        device, L expert records (one shared expert per layer) when
+ *                   cfg->has_shared_expert, else NULL; caller-owned
+ * The table starts empty (every expert missing, every slot free). */
+MOE_API moe_status moe_pool_create(const moe_config* cfg, const void* host_pool, size_t host_pool_bytes,
+                                   const void* router_w, const float* router_b, const void* shared_w,
+                                   int device, moe_pool** out);
+MOE_API moe_status moe_pool_destroy(moe_pool* pool);   /* blocking; NULL is a no-op */
+
+/* Replace the whole expert_id -> slot_id table (SeqMoE "Mechanism").
+ *   lut_host  host, int32 [L*E]: slot id, or -1 for "not resident"; each slot
+ *             may appear at most once.
+ * Every assigned slot is filled from the host pool on `stream` and its tag is
+ * incremented.  Routing history is kept.  Blocking on the host only for the
+ * small table upload. */
+MOE_API moe_status moe_set_lut(moe_pool* pool, const int32_t* lut_host, void* stream);
+
+/* Host-initiated placement of expert (layer, expert) into `slot`: the slot's
+ * occupant is evicted, a previous slot of this expert becomes free, the record
+ * is copied by the device-side copy kernel and the slot's tag incremented. */
+MOE_API moe_status moe_load_slot(moe_pool* pool, int32_t layer, int32_t expert, int32_t slot, void* stream);
+
+/* One MoE layer forward (steps a1..a9, or a10 for a staged prefill).
+ *   x     device [T, H] act_dtype;   out  device [T, H] act_dtype (may not alias x)
+ *   T     0..max_tokens; T == 0 returns MOE_OK and does nothing
+ *   mode  MOE_MODE_DECODE: slot pool path, misses copied by the device;
+ *         MOE_MODE_PREFILL_STAGED: the whole layer is read from a staging
+ *         region (needs staging_regions == 2); the history is still updated;
+ *         MOE_MODE_AUTO: staged when staging_regions == 2 and
+ *         T >= floor(K_l / k), K_l being the slots layer l holds now
+ *         (MoE-CORE "Mechanism"), else the slot pool path.
+ * A staged call stages layer l (if not already there) and queues layer l+2
+ * into the region it releases; it synchronises the host with nothing but may
+ * make `stream` wait for the pool's internal copy stream. */
+MOE_API moe_status moe_forward(moe_pool* pool, int32_t layer, const void* x, int32_t T, void* out,
+                               int32_t mode, void* stream);
+
+/* Same as a slot-pool moe_forward, with the routing supplied by the caller
+ * (steps a3..a9 only):
+ *   ids   device int32 [T, k], distinct experts per token
+ *   w     device fp32 [T, k] routing weights used in the combine
+ *   probs device fp32 [T, E] per-expert probabilities used for the history */
+MOE_API moe_status moe_forward_routed(moe_pool* pool, int32_t layer, const void* x, int32_t T,
+                                      const int32_t* ids, const float* w, const float* probs,
+                                      void* out, void* stream);
+
+/* Step a3 alone: one history/score update of `layer` from device ids [T, k]
+ * and device fp32 probs [T, E]. */
+MOE_API moe_status moe_update_scores(moe_pool* pool, int32_t layer, const int32_t* ids, const float* probs,
+                                     int32_t T, void* stream);
+
+/* Blocking: synchronises the device, returns the sticky device status (MOE_OK
+ * if no device-side error was recorded).  moe_clear_status resets it. */
+MOE_API moe_status moe_get_status(moe_pool* pool);
+MOE_API moe_status moe_clear_status(moe_pool* pool);
+
+/* Blocking: host copies of the last forward's routing (any pointer may be NULL).
+ *   ids [T,k] int32, w [T,k] fp32, probs [T,E] fp32, gap [T] fp32 (the k-th
+ *   minus the (k+1)-th fp32 logit; +inf when k == E or the routing was
+ *   supplied), slots [T,k] int32 (slot read, -1 = read from the host pool),
+ *   perm [T*k] int32 (flat entry t*k+j at each expert-sorted row),
+ *   offs [E+1] int32 (row offset of each expert).  *T_out receives T. */
+MOE_API moe_status moe_get_routing(moe_pool* pool, int32_t* ids, float* w, float* probs, float* gap,
+                                   int32_t* slots, int32_t* perm, int32_t* offs, int32_t cap_T,
+                                   int32_t* T_out);
+
+/* Blocking: host copies of the cache state (any pointer may be NULL).
+ *   lut [L*E] int32, owner [S] int32 (l*E+e or -1), tag [S] uint32,
+ *   score [L*E] fp32 (eviction score as of each layer's last update). */
+MOE_API moe_status moe_get_state(moe_pool* pool, int32_t* lut, int32_t* owner, uint32_t* tag, float* score);
+
+/* Blocking: cumulative counters. */
+MOE_API moe_status moe_get_stats(moe_pool* pool, moe_stats* out);
+
+/* Number of kernel launches the library issued since the pool was created. */
+MOE_API uint64_t moe_launch_count(const moe_pool* pool);
+
+/* Text of the last error returned on this thread ("" if none). */
+MOE_API const char* moe_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOESLOT_H */

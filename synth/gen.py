@@ -214,3 +214,64 @@ def torch_encode_records(wl: Workload, w13, w2):
         raw = t.contiguous().view(n, -1).view(torch.uint8)
         out[:, off:off + raw.shape[1]] = raw
     return out
+
+
+# ----------------------------------------------------------------------------
+# whole-workload assembly (format only: record packing, no layer arithmetic)
+# ----------------------------------------------------------------------------
+
+def record_to_stored(wl: Workload, rec: np.ndarray):
+    """Parse one host-pool record (uint8) back into the stored dict (w13, w2[, s13, s2])."""
+    o13, o2, os13, os2, _ = wl.expert_layout()
+    H, I = wl.H, wl.I
+    if wl.weight_dtype == F32:
+        dt, eb = np.float32, 4
+    elif wl.weight_dtype == BF16:
+        dt, eb = np.uint16, 2
+    else:
+        dt, eb = np.uint8, 1
+    out = {"w13": rec[o13:o13 + 2 * I * H * eb].view(dt).reshape(2 * I, H).copy(),
+           "w2": rec[o2:o2 + H * I * eb].view(dt).reshape(H, I).copy()}
+    if wl.weight_dtype == FP8_E4M3_B128:
+        n13 = (2 * I // 128) * (H // 128)
+        n2 = (H // 128) * (I // 128)
+        out["s13"] = rec[os13:os13 + 4 * n13].view(np.float32).reshape(2 * I // 128, H // 128).copy()
+        out["s2"] = rec[os2:os2 + 4 * n2].view(np.float32).reshape(H // 128, I // 128).copy()
+    return out
+
+
+def fill_host_pool(wl: Workload, host_u8, device=None, base_seed: int = 0, chunk: int = 16):
+    """Write all L*E expert records into a host buffer (record (l, e) at (l*E+e)*record_bytes).
+
+    host_u8: numpy uint8 view (device=None: numpy generator, per-expert seeds) or a
+    torch uint8 CPU tensor (device given: torch generator on that device, per-chunk seeds).
+    """
+    rec = wl.expert_layout()[4]
+    if device is None:
+        for l in range(wl.L):
+            for e in range(wl.E):
+                off = (l * wl.E + e) * rec
+                host_u8[off:off + rec] = expert_record_bytes(wl, expert_stored(wl, l, e, base_seed))
+        return
+    import torch
+    for l in range(wl.L):
+        for e0 in range(0, wl.E, chunk):
+            n = min(chunk, wl.E - e0)
+            w13, w2 = torch_expert_chunk(wl, l, e0, n, device, base_seed)
+            recs = torch_encode_records(wl, w13, w2)
+            del w13, w2
+            off = (l * wl.E + e0) * rec
+            host_u8[off:off + n * rec].copy_(recs.view(-1))
+            del recs
+    torch.cuda.synchronize(device)
+
+
+def shared_records(wl: Workload, base_seed: int = 0) -> np.ndarray:
+    """L shared-expert records, uint8 [L * record_bytes]."""
+    return np.concatenate([expert_record_bytes(wl, shared_expert_stored(wl, l, base_seed)) for l in range(wl.L)])
+
+
+def routers(wl: Workload, zipf_s=None, base_seed: int = 0):
+    """(W_r stored [L, E, H], b fp32 [L, E]) for every layer."""
+    ws, bs = zip(*(router_stored(wl, l, zipf_s, base_seed) for l in range(wl.L)))
+    return np.stack(ws), np.stack(bs)
