@@ -1,0 +1,460 @@
+#!/usr/bin/env python
+"""Benchmark of the slot-pool MoE layer on GB300.
+
+Workload (default): the Qwen3-30B-A3B-shaped decode — 48 MoE layers, hidden
+2048, 128 experts, top-8, intermediate 768, bf16 weights and activations, a
+shared slot pool of round(0.45 * 48 * 128) = 2765 slots, Zipf(s=1.0) router
+bias, AR(1) (rho = 0.8) drift of the hidden states, MoE-CORE eviction score.
+Weights are random (seeded), never a checkpoint.
+
+One "step" is one decode step of T tokens through all 48 layers: every stage
+of the layer (router, gate/top-k, history, table, victims, device-started miss
+copies, permutation, expert FFN, combine) runs in the library's kernels, the
+48 moe_forward calls being captured once into a CUDA graph.  The metric is
+MoE-layer tokens/s = (steps * T * 48) / elapsed.
+
+Printed (rank 0, one JSON line): value (inputs already in HBM), e2e (same
+metric through the C ABI with host buffers: per-step pinned H2D of x and D2H of
+the output inside the timed region), roofline of the dominant kernel (expert
+gate/up streaming, timed per launch with CUDA events in a profiling pass of the
+same workload), clocks sampled with nvidia-smi during the timed region, and the
+CPU oracle timed on a bounded sample as cpu_baseline.
+
+--impl reference times the CPU oracle itself on the same workload and prints
+the same line with "impl": "reference".
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD_LABEL = {"qwen3_decode": "qwen3-30b-a3b-shaped-decode"}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="qwen3_decode")
+    ap.add_argument("--batch", type=int, default=16, help="decode tokens per step (headline)")
+    ap.add_argument("--sweep", default="1,4", help="other decode batches reported under 'sweep' ('' for none)")
+    ap.add_argument("--prof-steps", type=int, default=32)
+    ap.add_argument("--cpu-sample", type=int, default=12, help="oracle layer-steps in cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_setup(n_gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+class Clocks:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in out.strip().splitlines():
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ our arm
+class DecodeBench:
+    def __init__(self, wl, max_T, device):
+        import numpy as np
+        import torch
+
+        import expert_offload_slot_gb300 as moe
+        from synth import gen
+        self.moe, self.wl, self.device = moe, wl, device
+        self.rec = wl.expert_layout()[4]
+        self.cfg = moe.make_config(wl.L, wl.E, wl.k, wl.H, wl.I, wl.S, wl.weight_dtype, wl.act_dtype, wl.gating,
+                                   wl.shared, wl.evict, wl.window, 0.9, (0.25, 0.25, 0.25, 0.25), 0, max_T)
+        t0 = time.time()
+        self.host = moe.HostPool(wl.L * wl.E * self.rec)
+        gen.fill_host_pool(wl, self.host.torch(), device=device)
+        w_r, b = gen.routers(wl)
+        wr = w_r.view(np.int16) if wl.act_dtype == 1 else w_r
+        self.w_r = torch.from_numpy(np.ascontiguousarray(wr)).to(device)
+        self.b = torch.from_numpy(b).to(device)
+        self.shared = torch.from_numpy(gen.shared_records(wl)).to(device) if wl.shared else None
+        self.pool = moe.Pool(self.cfg, self.host.ptr, self.host.nbytes, self.w_r, self.b, self.shared,
+                             device=torch.cuda.current_device())
+        self.pool.set_lut(gen.initial_lut(wl))
+        torch.cuda.synchronize()
+        self.setup_s = time.time() - t0
+
+    def capture(self, x_in, out, stream):
+        import torch
+        n0 = self.pool.launch_count()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for l in range(self.wl.L):
+                self.pool.forward(l, x_in[l], out[l], self.moe.MOE_MODE_DECODE)
+        return g, self.pool.launch_count() - n0
+
+    def run(self, T, W, K, prof_steps, clocks=None, world=1, e2e=True):
+        import torch
+        wl, moe = self.wl, self.moe
+        dev = self.device
+        xs = __import__("synth").gen.torch_decode_hidden(wl, T, W + K, dev)
+        s = torch.cuda.Stream()
+        x_in = torch.empty((wl.L, T, wl.H), dtype=xs.dtype, device=dev)
+        out = torch.empty_like(x_in)
+        with torch.cuda.stream(s):
+            x_in.copy_(xs[0])
+            for l in range(wl.L):                    # one eager step before capture
+                self.pool.forward(l, x_in[l], out[l], moe.MOE_MODE_DECODE)
+        s.synchronize()
+        g, launches_per_step = self.capture(x_in, out, s)
+        with torch.cuda.stream(s):
+            for i in range(W):
+                x_in.copy_(xs[i])
+                g.replay()
+        s.synchronize()
+        st0 = self.pool.stats()
+        barrier(world)
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if clocks:
+            clocks.start()
+        with torch.cuda.stream(s):
+            ev0.record(s)
+            for i in range(W, W + K):
+                x_in.copy_(xs[i])
+                g.replay()
+            ev1.record(s)
+        s.synchronize()
+        torch.cuda.synchronize()
+        ms = ev0.elapsed_time(ev1)
+        clk = clocks.stop() if clocks else None
+        barrier(world)
+        st1 = self.pool.stats()
+        res = {"T": T, "ms": ms, "steps": K, "launches_per_step": launches_per_step,
+               "hits": st1["hits"] - st0["hits"], "misses": st1["misses"] - st0["misses"],
+               "bytes_copied": st1["bytes_copied"] - st0["bytes_copied"], "clocks": clk}
+        res["status"] = self.pool.status()
+        # profiling pass: per-stage CUDA-event times of every layer, same workload continued
+        res["prof"] = self.profile(xs, x_in, out, s, T, prof_steps)
+        if e2e:
+            res["e2e"] = self.run_e2e(xs, g, x_in, out, s, W, K)
+        del g
+        return res
+
+    def profile(self, xs, x_in, out, s, T, P):
+        import torch
+        wl = self.wl
+        self.pool.profile_enable(True)
+        gp, _ = self.capture(x_in, out, s)
+        stage = [0.0] * self.moe.MOE_NUM_STAGES
+        st0 = self.pool.stats()
+        n = 0
+        for i in range(P):
+            with torch.cuda.stream(s):
+                x_in.copy_(xs[i % xs.shape[0]])
+                gp.replay()
+            s.synchronize()
+            for l in range(wl.L):
+                v = self.pool.profile_read(l)
+                stage = [a + b for a, b in zip(stage, v)]
+                n += 1
+        st1 = self.pool.stats()
+        self.pool.profile_enable(False)
+        del gp
+        U = (st1["hits"] - st0["hits"]) + (st1["misses"] - st0["misses"])
+        if wl.shared:
+            U += n                              # the shared expert is streamed by every launch
+        return {"launches": n, "stage_ms": stage, "sum_U": U, "T": T,
+                "bytes_copied": st1["bytes_copied"] - st0["bytes_copied"]}
+
+    def run_e2e(self, xs, g, x_in, out, s, W, K):
+        """Same metric through the C ABI with host buffers: H2D of x and D2H of out every step."""
+        import torch
+        x_host = xs[W:W + K].cpu().pin_memory()
+        out_host = torch.empty_like(x_host).pin_memory()
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            ev0.record(s)
+            for i in range(K):
+                x_in.copy_(x_host[i], non_blocking=True)
+                g.replay()
+                out_host[i].copy_(out, non_blocking=True)
+            ev1.record(s)
+        s.synchronize()
+        ms = ev0.elapsed_time(ev1)
+        nb = x_in.numel() * x_in.element_size()
+        return {"ms": ms, "h2d": nb, "d2h": nb}
+
+    def close(self):
+        self.pool.close()
+        self.host.free()
+
+
+def gate_up_bytes(wl, sum_U, launches, T):
+    """Algorithmic bytes of all gate/up launches: U expert w13 blocks + x reads + h writes."""
+    eb = wl.weight_elt_bytes
+    w13 = 2 * wl.I * wl.H * eb
+    per_launch_act = T * wl.H * wl.act_elt_bytes + T * wl.k * wl.I * wl.act_elt_bytes
+    return sum_U * w13 + launches * per_launch_act
+
+
+def step_bytes(wl, U_per_layer, T):
+    """Algorithmic HBM bytes of one layer-step: router + U expert records + x in and out."""
+    eb = wl.weight_elt_bytes
+    Be = 3 * wl.H * wl.I * eb
+    return wl.E * wl.H * wl.act_elt_bytes + U_per_layer * Be + 2 * T * wl.H * wl.act_elt_bytes
+
+
+# ------------------------------------------------------------------ oracle arm
+class OracleSample:
+    """The CPU oracle as it stands, on the first layer-steps of the same workload."""
+
+    def __init__(self, wl, T, n_layers, n_steps, device):
+        import numpy as np
+
+        from synth import gen
+        self.wl, self.T = wl, T
+        self.rec = wl.expert_layout()[4]
+        self.n_layers, self.n_steps = n_layers, n_steps
+        self.records = {l: gen.device_layer_records(wl, l, device).cpu().numpy() for l in range(n_layers)}
+        self.w_r, self.b = gen.routers(wl)
+        xs = gen.torch_decode_hidden(wl, T, n_steps, device)
+        self.xs = xs.view(__import__("torch").int16).cpu().numpy().view(np.uint16) if wl.act_dtype == 1 \
+            else xs.cpu().numpy()
+        self.lut = gen.initial_lut(wl)
+
+    def run(self, max_layer_steps):
+        import numpy as np
+
+        from oracle.cache import SlotPoolSim
+        from oracle.layer import layer_from_stored
+        from synth import gen
+        wl = self.wl
+        sim = SlotPoolSim(wl.L, wl.E, wl.S, wl.evict, wl.window)
+        sim.set_lut(self.lut)
+        done = 0
+        t0 = time.perf_counter()
+        for t in range(self.n_steps):
+            for l in range(self.n_layers):
+                if done >= max_layer_steps:
+                    break
+                recs = self.records[l]
+                out, r = layer_from_stored(self.xs[t, l], wl.act_dtype, self.w_r[l], self.b[l],
+                                           lambda e: gen.record_to_stored(wl, recs[e]), wl.weight_dtype, wl.I,
+                                           wl.k, wl.gating)
+                sim.update_scores(l, r["ids"], r["probs"].astype(np.float32))
+                sim.plan(l, r["ids"])
+                done += 1
+        el = time.perf_counter() - t0
+        return done, el
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        return max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
+    except Exception:
+        return os.cpu_count()
+
+
+def cpu_baseline(wl, T, n_layer_steps, device):
+    n_layers = min(4, wl.L)
+    n_steps = (n_layer_steps + n_layers - 1) // n_layers
+    o = OracleSample(wl, T, n_layers, n_steps, device)
+    done, el = o.run(n_layer_steps)
+    return {"value": done * T / el, "unit": "MoE-layer tokens/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{done} layer-steps (layers 0-{n_layers - 1} x first {n_steps} decode steps, T={T}) "
+                      f"of the same workload, numpy float64, {el:.1f} s"}
+
+
+def main():
+    args = parse_args()
+    import torch
+
+    from synth import get_workload
+    wl = get_workload(args.workload)
+    rank, world, local = dist_setup(args.gpus)
+    label = WORKLOAD_LABEL.get(args.workload, args.workload)
+    T = args.batch
+    base_cfg = {"workload": label, "layers": wl.L, "experts": wl.E, "top_k": wl.k, "hidden": wl.H,
+                "inter": wl.I, "slots": wl.S, "residency": wl.residency, "batch_tokens": T,
+                "evict": ["moe-core", "mrs", "lru"][wl.evict], "router_bias_zipf_s": wl.zipf_s,
+                "ar1_rho": wl.ar_rho, "graph": "48 moe_forward calls captured once per step",
+                "l2": "no flush: a step streams ~48*U expert records (GBs) >> 129 MB L2"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        n = min(args.steps, 24)
+        o = OracleSample(wl, T, min(4, wl.L), (n + 3) // 4, "cuda")
+        o.run(min(args.warmup, 2))
+        done, el = o.run(n)
+        v = done * T / el
+        line = {"impl": "reference", "metric": "MoE-layer tokens/s (decode)", "value": v,
+                "unit": "MoE-layer tokens/s", "n_gpus": 1, "steps": done, "warmup": min(args.warmup, 2),
+                "ms_per_step": el * 1e3 / done, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64", "data": "synthetic (seeded random weights, AR(1) hidden states)",
+                "config": dict(base_cfg, reference_step="one layer-step of the oracle (T tokens, one layer)"),
+                "cpu_baseline": {"value": v, "unit": "MoE-layer tokens/s", "cores": blas_threads(),
+                                 "kind": "oracle", "sample": f"{done} layer-steps of the requested {args.steps}"},
+                "e2e": {"value": v, "unit": "MoE-layer tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import expert_offload_slot_gb300 as moe  # noqa: F401  (fails loudly without the library)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    sweep_T = [int(v) for v in args.sweep.split(",") if v.strip()] if args.sweep else []
+    max_T = max([T] + sweep_T)
+    bench = DecodeBench(wl, max_T, dev)
+    try:
+        sweep = {}
+        for t in sweep_T:
+            r = bench.run(t, args.warmup, args.steps, max(4, args.prof_steps // 2), None, world, e2e=False)
+            sweep[str(t)] = {"tokens_per_s": r["steps"] * t * wl.L / (r["ms"] / 1e3),
+                             "us_per_layer": r["ms"] * 1e3 / (r["steps"] * wl.L),
+                             "hit_rate": r["hits"] / max(1, r["hits"] + r["misses"]),
+                             "stage_us_per_layer": {n: v * 1e3 / max(1, r["prof"]["launches"])
+                                                    for n, v in zip(moe.STAGES, r["prof"]["stage_ms"])}}
+        clocks = Clocks(local) if rank == 0 else None
+        r = bench.run(T, args.warmup, args.steps, args.prof_steps, clocks, world, e2e=True)
+    finally:
+        pass
+    ms = max_over_ranks(r["ms"], world)
+    tokens = sum_over_ranks(r["steps"] * T * wl.L, world)
+    value = tokens / (ms / 1e3)
+    e2e_ms = max_over_ranks(r["e2e"]["ms"], world)
+    e2e_value = tokens / (e2e_ms / 1e3)
+
+    prof = r["prof"]
+    peak, peak_kind = load_peaks()
+    gu_ms = prof["stage_ms"][3]
+    gu_bytes = gate_up_bytes(wl, prof["sum_U"], prof["launches"], T)
+    achieved = gu_bytes / (gu_ms / 1e3) / 1e9
+    layer_steps = prof["launches"]
+    U_mean = prof["sum_U"] / max(1, layer_steps)
+    prof_layer_us = sum(prof["stage_ms"]) * 1e3 / max(1, layer_steps)
+    layer_bytes = step_bytes(wl, U_mean, T)
+    if rank != 0:
+        bench.close()
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, T, args.cpu_sample, dev)
+    line = {
+        "metric": "MoE-layer tokens/s (decode)", "value": value, "unit": "MoE-layer tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / r["steps"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded random N(0,0.02) weights, Zipf router bias, AR(1) hidden states)",
+        "config": dict(base_cfg, parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+        "us_per_layer": ms * 1e3 / (r["steps"] * wl.L),
+        "hit_rate": r["hits"] / max(1, r["hits"] + r["misses"]),
+        "miss_copy_GB": r["bytes_copied"] / 1e9,
+        "e2e": {"value": e2e_value, "unit": "MoE-layer tokens/s", "h2d_bytes_per_step": r["e2e"]["h2d"],
+                "d2h_bytes_per_step": r["e2e"]["d2h"]},
+        "roofline": {"bound": "hbm", "kernel": "ffn_gate_up_kernel", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                     "peak_source": f"{peak_kind} hbm_gbs", "launches_timed": prof["launches"],
+                     "bytes_per_launch": gu_bytes / max(1, prof["launches"]),
+                     "us_per_launch": gu_ms * 1e3 / max(1, prof["launches"])},
+        "layer_roofline": {"algorithmic_bytes_per_layer": layer_bytes, "mean_U": U_mean,
+                           "us_per_layer_profiled": prof_layer_us,
+                           "frac": layer_bytes / (prof_layer_us * 1e-6) / 1e9 / peak},
+        "stage_us_per_layer": {n: v * 1e3 / max(1, layer_steps) for n, v in zip(moe.STAGES, prof["stage_ms"])},
+        "clocks": r["clocks"],
+        "gpu_launches": r["launches_per_step"] * r["steps"],
+        "status": moe.STATUS_NAMES.get(r["status"], r["status"]),
+        "sweep": sweep,
+        "setup_s": bench.setup_s,
+        "cpu_baseline": cpu,
+    }
+    bench.close()
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

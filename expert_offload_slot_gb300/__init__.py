@@ -24,6 +24,8 @@ MOE_F32, MOE_BF16, MOE_FP8_E4M3_B128 = 0, 1, 2
 MOE_GATE_SOFTMAX_RENORM, MOE_GATE_SIGMOID_RENORM = 0, 1
 MOE_EVICT_CORE, MOE_EVICT_MRS, MOE_EVICT_LRU = 0, 1, 2
 MOE_MODE_AUTO, MOE_MODE_DECODE, MOE_MODE_PREFILL_STAGED = 0, 1, 2
+STAGES = ("route", "plan", "copy", "gate_up", "down")
+MOE_NUM_STAGES = len(STAGES)
 
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID", 2: "MOE_ERR_OOM", 3: "MOE_ERR_CUDA", 4: "MOE_ERR_CAPACITY",
                 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_TAG", 7: "MOE_ERR_BOUNDS"}
@@ -62,6 +64,8 @@ _sig = {
     "moe_get_state": (_i32, [_vp, _vp, _vp, _vp, _vp]),
     "moe_get_stats": (_i32, [_vp, _P(moe_stats)]),
     "moe_launch_count": (ctypes.c_uint64, [_vp]),
+    "moe_profile_enable": (_i32, [_vp, _i32]),
+    "moe_profile_read": (_i32, [_vp, _i32, _P(ctypes.c_float)]),
     "moe_last_error": (ctypes.c_char_p, []),
 }
 for _name, (_res, _args) in _sig.items():
@@ -229,6 +233,14 @@ class Pool:
         s = moe_stats()
         _check(_lib.moe_get_stats(self.h, ctypes.byref(s)), "moe_get_stats")
         return {n: getattr(s, n) for n, _ in moe_stats._fields_}
+
+    def profile_enable(self, on=True):
+        _check(_lib.moe_profile_enable(self.h, int(on)), "moe_profile_enable")
+
+    def profile_read(self, layer):
+        v = (ctypes.c_float * MOE_NUM_STAGES)()
+        _check(_lib.moe_profile_read(self.h, layer, v), "moe_profile_read")
+        return list(v)
 
     def launch_count(self):
         return int(_lib.moe_launch_count(self.h))

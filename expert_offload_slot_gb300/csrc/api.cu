@@ -71,6 +71,8 @@ struct moe_pool {
   uint64_t staged_count = 0;
   uint64_t launches = 0;
   std::vector<void*> allocs;
+  bool prof_on = false;
+  std::vector<cudaEvent_t> prof_ev;   // [L][MOE_NUM_STAGES + 1]
 };
 
 static size_t elt_bytes(int dt) { return dt == MOE_F32 ? 4 : dt == MOE_BF16 ? 2 : 1; }
@@ -190,6 +192,8 @@ static moe_status palloc(moe_pool* P, T** out, size_t count, int fill_byte) {
 static void pool_free_all(moe_pool* P) {
   for (void* p : P->allocs) cudaFree(p);
   P->allocs.clear();
+  for (cudaEvent_t e : P->prof_ev) cudaEventDestroy(e);
+  P->prof_ev.clear();
   for (int r = 0; r < 2; ++r) {
     if (P->ready[r]) cudaEventDestroy(P->ready[r]);
     if (P->released[r]) cudaEventDestroy(P->released[r]);
@@ -389,14 +393,26 @@ static moe_status run_layer(moe_pool* P, int layer, const void* x, int T, void* 
     if (layer + 1 < d.L && P->staged_layer[1 - region] != layer + 1) stage_layer(P, layer + 1, 1 - region);
     CUDA_TRY(cudaStreamWaitEvent(s, P->ready[region], 0));
   }
+  const int NB = MOE_NUM_STAGES + 1;
+  auto mark = [&](int i) {
+    // External: inside a stream capture this becomes an event-record node
+    if (P->prof_on) cudaEventRecordWithFlags(P->prof_ev[(size_t)layer * NB + i], s, cudaEventRecordExternal);
+  };
+  mark(0);
   if (!ids_in) {
     P->launches += launch_route_logits(d, layer, x, T, P->router_w, P->router_b, sc.logits, s);
     P->launches += launch_gate_topk(d, sc.logits, T, sc.ids, sc.w, sc.probs, sc.gap, s);
   }
+  mark(1);
   const int flags = staged ? (PLAN_HISTORY | PLAN_PERMUTE | PLAN_STAGED) : (PLAN_HISTORY | PLAN_CACHE | PLAN_PERMUTE);
   P->launches += launch_plan(d, sc, layer, T, ids, w, probs, flags, region, s);
+  mark(2);
   if (!staged) P->launches += launch_miss_copy(d, sc, s);
-  P->launches += launch_ffn(d, sc, T, x, out, T * d.k + T, s);
+  mark(3);
+  P->launches += launch_ffn_gate_up(d, sc, T, x, s);
+  mark(4);
+  P->launches += launch_ffn_down(d, sc, T, out, s);
+  mark(5);
   if (staged) {
     CUDA_TRY(cudaEventRecord(P->released[region], s));
     if (layer + 2 < d.L) stage_layer(P, layer + 2, region);
@@ -542,3 +558,28 @@ MOE_API moe_status moe_get_stats(moe_pool* P, moe_stats* out) {
 }
 
 MOE_API uint64_t moe_launch_count(const moe_pool* P) { return P ? P->launches : 0; }
+
+MOE_API moe_status moe_profile_enable(moe_pool* P, int32_t on) {
+  if (!P) return fail(MOE_ERR_INVALID, "pool is NULL");
+  CUDA_TRY(cudaSetDevice(P->device));
+  if (on && P->prof_ev.empty()) {
+    const size_t n = (size_t)P->d.L * (MOE_NUM_STAGES + 1);
+    P->prof_ev.resize(n, nullptr);
+    for (size_t i = 0; i < n; ++i) CUDA_TRY(cudaEventCreate(&P->prof_ev[i]));
+  }
+  P->prof_on = on != 0;
+  return MOE_OK;
+}
+
+MOE_API moe_status moe_profile_read(moe_pool* P, int32_t layer, float* stage_ms) {
+  if (!P || !stage_ms) return fail(MOE_ERR_INVALID, "NULL argument");
+  if (layer < 0 || layer >= P->d.L) return fail(MOE_ERR_INVALID, "layer out of range");
+  if (P->prof_ev.empty()) return fail(MOE_ERR_INVALID, "profiling was never enabled");
+  CUDA_TRY(cudaSetDevice(P->device));
+  const size_t b = (size_t)layer * (MOE_NUM_STAGES + 1);
+  for (int i = 0; i < MOE_NUM_STAGES; ++i) {
+    CUDA_TRY(cudaEventSynchronize(P->prof_ev[b + i + 1]));
+    CUDA_TRY(cudaEventElapsedTime(&stage_ms[i], P->prof_ev[b + i], P->prof_ev[b + i + 1]));
+  }
+  return MOE_OK;
+}

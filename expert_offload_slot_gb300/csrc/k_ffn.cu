@@ -266,23 +266,7 @@ ffn_down_combine_kernel(FfnArgs a) {
   }
 }
 
-template <typename WT, typename AT>
-static int launch_ffn_t(const FfnArgs& a, int T, cudaStream_t s) {
-  static bool configured = false;
-  const size_t smem = (size_t)kDownRows * T * sizeof(float);
-  if (!configured) {
-    cudaFuncSetAttribute(ffn_down_combine_kernel<WT, AT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         200 * 1024);
-    configured = true;
-  }
-  ffn_gate_up_kernel<WT, AT><<<2 * sm_count(), kFfnWarps * 32, 0, s>>>(a);
-  ffn_down_combine_kernel<WT, AT><<<(a.H + kDownRows - 1) / kDownRows, kFfnWarps * 32, smem, s>>>(a);
-  return 2;
-}
-
-int launch_ffn(const PoolDev& p, const Scratch& sc, int T, const void* x, void* out, int max_rows,
-               cudaStream_t s) {
-  (void)max_rows;
+static FfnArgs ffn_args(const PoolDev& p, const Scratch& sc, int T, const void* x, void* out) {
   FfnArgs a;
   a.work = sc.work;
   a.n_work = sc.n_work;
@@ -298,9 +282,36 @@ int launch_ffn(const PoolDev& p, const Scratch& sc, int T, const void* x, void* 
   a.off2 = p.lay.off2;
   a.offs13 = p.lay.offs13;
   a.offs2 = p.lay.offs2;
-  if (p.wdt == MOE_F32) return launch_ffn_t<float, float>(a, T, s);
-  if (p.wdt == MOE_BF16) return launch_ffn_t<uint16_t, uint16_t>(a, T, s);
-  return launch_ffn_t<uint8_t, uint16_t>(a, T, s);
+  return a;
+}
+
+int launch_ffn_gate_up(const PoolDev& p, const Scratch& sc, int T, const void* x, cudaStream_t s) {
+  const FfnArgs a = ffn_args(p, sc, T, x, nullptr);
+  const int grid = 2 * sm_count();
+  if (p.wdt == MOE_F32) ffn_gate_up_kernel<float, float><<<grid, kFfnWarps * 32, 0, s>>>(a);
+  else if (p.wdt == MOE_BF16) ffn_gate_up_kernel<uint16_t, uint16_t><<<grid, kFfnWarps * 32, 0, s>>>(a);
+  else ffn_gate_up_kernel<uint8_t, uint16_t><<<grid, kFfnWarps * 32, 0, s>>>(a);
+  return 1;
+}
+
+template <typename WT, typename AT>
+static void launch_down_t(const FfnArgs& a, int T, cudaStream_t s) {
+  static bool configured = false;
+  if (!configured) {
+    cudaFuncSetAttribute(ffn_down_combine_kernel<WT, AT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         200 * 1024);
+    configured = true;
+  }
+  const size_t smem = (size_t)kDownRows * T * sizeof(float);
+  ffn_down_combine_kernel<WT, AT><<<(a.H + kDownRows - 1) / kDownRows, kFfnWarps * 32, smem, s>>>(a);
+}
+
+int launch_ffn_down(const PoolDev& p, const Scratch& sc, int T, void* out, cudaStream_t s) {
+  const FfnArgs a = ffn_args(p, sc, T, nullptr, out);
+  if (p.wdt == MOE_F32) launch_down_t<float, float>(a, T, s);
+  else if (p.wdt == MOE_BF16) launch_down_t<uint16_t, uint16_t>(a, T, s);
+  else launch_down_t<uint8_t, uint16_t>(a, T, s);
+  return 1;
 }
 
 }  // namespace moeslot

@@ -122,8 +122,8 @@ int launch_gate_topk(const PoolDev& p, const float* logits, int T, int32_t* ids,
 int launch_plan(const PoolDev& p, const Scratch& sc, int layer, int T, const int32_t* ids, const float* w,
                 const float* probs, int flags, int region, cudaStream_t s);
 int launch_miss_copy(const PoolDev& p, const Scratch& sc, cudaStream_t s);
-int launch_ffn(const PoolDev& p, const Scratch& sc, int T, const void* x, void* out, int max_rows,
-               cudaStream_t s);
+int launch_ffn_gate_up(const PoolDev& p, const Scratch& sc, int T, const void* x, cudaStream_t s);
+int launch_ffn_down(const PoolDev& p, const Scratch& sc, int T, void* out, cudaStream_t s);
 int launch_load_slot(const PoolDev& p, const Scratch& sc, int layer, int expert, int slot, cudaStream_t s);
 int launch_rebuild_owner(const PoolDev& p, cudaStream_t s);
 

@@ -86,8 +86,8 @@ typedef struct {
   int32_t num_layers;        /* L                                                  */
   int32_t num_experts;       /* E routed experts per layer, 1..256                 */
   int32_t top_k;             /* k, 1..min(E, 32)                                   */
-  int32_t hidden;            /* H: multiple of 128 (f32), 256 (bf16), 512 (fp8)   */
-  int32_t inter;             /* I: multiple of 128 (f32), 256 (bf16), 512 (fp8)   */
+  int32_t hidden;            /* H: multiple of 4 (f32), 8 (bf16), 16 and 128 (fp8) */
+  int32_t inter;             /* I: same rule as H                                  */
   int32_t num_slots;         /* S slots in the shared pool, >= 1                   */
   int32_t weight_dtype;      /* MOE_F32, MOE_BF16 or MOE_FP8_E4M3_B128             */
   int32_t act_dtype;         /* MOE_F32 or MOE_BF16 (x, out, router weights)       */
@@ -203,6 +203,20 @@ MOE_API moe_status moe_get_state(moe_pool* pool, int32_t* lut, int32_t* owner, u
 
 /* Blocking: cumulative counters. */
 MOE_API moe_status moe_get_stats(moe_pool* pool, moe_stats* out);
+
+/* Per-stage timing with CUDA events (off by default).  While enabled, every
+ * forward records pool-owned events on its stream between its stages (inside
+ * a captured graph they become event nodes); moe_profile_read returns, for the
+ * latest forward of `layer`, the elapsed milliseconds of each stage.  Enabling
+ * creates L*(MOE_NUM_STAGES+1) events and is blocking. */
+enum { MOE_STAGE_ROUTE = 0,   /* router GEMV + gate/top-k                     */
+       MOE_STAGE_PLAN = 1,    /* history, table, victims, permutation         */
+       MOE_STAGE_COPY = 2,    /* device-started miss copies                   */
+       MOE_STAGE_GATE_UP = 3, /* expert gate/up projections + SiLU            */
+       MOE_STAGE_DOWN = 4,    /* expert down projection + weighted combine    */
+       MOE_NUM_STAGES = 5 };
+MOE_API moe_status moe_profile_enable(moe_pool* pool, int32_t on);
+MOE_API moe_status moe_profile_read(moe_pool* pool, int32_t layer, float* stage_ms /* [MOE_NUM_STAGES] */);
 
 /* Number of kernel launches the library issued since the pool was created. */
 MOE_API uint64_t moe_launch_count(const moe_pool* pool);

@@ -255,14 +255,10 @@ def fill_host_pool(wl: Workload, host_u8, device=None, base_seed: int = 0, chunk
         return
     import torch
     for l in range(wl.L):
-        for e0 in range(0, wl.E, chunk):
-            n = min(chunk, wl.E - e0)
-            w13, w2 = torch_expert_chunk(wl, l, e0, n, device, base_seed)
-            recs = torch_encode_records(wl, w13, w2)
-            del w13, w2
-            off = (l * wl.E + e0) * rec
-            host_u8[off:off + n * rec].copy_(recs.view(-1))
-            del recs
+        recs = device_layer_records(wl, l, device, base_seed, chunk)
+        off = l * wl.E * rec
+        host_u8[off:off + wl.E * rec].copy_(recs.view(-1))
+        del recs
     torch.cuda.synchronize(device)
 
 
@@ -275,3 +271,45 @@ def routers(wl: Workload, zipf_s=None, base_seed: int = 0):
     """(W_r stored [L, E, H], b fp32 [L, E]) for every layer."""
     ws, bs = zip(*(router_stored(wl, l, zipf_s, base_seed) for l in range(wl.L)))
     return np.stack(ws), np.stack(bs)
+
+
+def device_layer_records(wl: Workload, layer: int, device, base_seed: int = 0, chunk: int = 16):
+    """All E expert records of one layer drawn on `device` (same values fill_host_pool writes)."""
+    import torch
+    rec = wl.expert_layout()[4]
+    out = torch.empty((wl.E, rec), dtype=torch.uint8, device=device)
+    for e0 in range(0, wl.E, chunk):
+        n = min(chunk, wl.E - e0)
+        w13, w2 = torch_expert_chunk(wl, layer, e0, n, device, base_seed)
+        out[e0:e0 + n] = torch_encode_records(wl, w13, w2)
+    return out
+
+
+def torch_decode_hidden(wl: Workload, T: int, steps: int, device, base_seed: int = 0, layers=None):
+    """AR(1) hidden states for every layer on `device`: bf16/fp32 tensor [steps, L, T, H].
+
+    x_0 ~ N(0,1); x_t = rho x_{t-1} + sqrt(1-rho^2) eps_t, one independent stream per (layer, token lane).
+    """
+    import torch
+    L = wl.L if layers is None else layers
+    g = torch.Generator(device=device)
+    g.manual_seed(seed_for(wl.name, -1, f"dev_ar1_T{T}", base_seed))
+    dt = torch.bfloat16 if wl.act_dtype == BF16 else torch.float32
+    out = torch.empty((steps, L, T, wl.H), dtype=dt, device=device)
+    c = math.sqrt(1.0 - wl.ar_rho ** 2)
+    x = torch.randn((L, T, wl.H), generator=g, device=device)
+    for t in range(steps):
+        if t > 0:
+            x = wl.ar_rho * x + c * torch.randn((L, T, wl.H), generator=g, device=device)
+        out[t] = x.to(dt)
+    return out
+
+
+def torch_prefill_hidden(wl: Workload, T: int, device, base_seed: int = 0, layers=None):
+    """i.i.d. N(0,1) prefill hidden states on `device`: [L, T, H] in the activation dtype."""
+    import torch
+    L = wl.L if layers is None else layers
+    g = torch.Generator(device=device)
+    g.manual_seed(seed_for(wl.name, -1, f"dev_prefill_T{T}", base_seed))
+    dt = torch.bfloat16 if wl.act_dtype == BF16 else torch.float32
+    return torch.randn((L, T, wl.H), generator=g, device=device).to(dt)
