@@ -67,6 +67,7 @@ _sig = {
     "moe_profile_enable": (_i32, [_vp, _i32]),
     "moe_profile_read": (_i32, [_vp, _i32, _P(ctypes.c_float)]),
     "moe_last_error": (ctypes.c_char_p, []),
+    "moe_route_topk_noalloc": (_i32, [_i32, _i32, _i32, _i32, _i32, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -124,6 +125,20 @@ def moe_expert_layout(cfg):
     v = [_sz() for _ in range(5)]
     _check(_lib.moe_expert_layout(ctypes.byref(cfg), *[ctypes.byref(x) for x in v]), "moe_expert_layout")
     return tuple(x.value for x in v)   # (w13_off, w2_off, s13_off, s2_off, record_bytes)
+
+
+MOE_NOALLOC_MAX_LOGITS = 65536
+
+
+def moe_route_topk_noalloc(E, k, H, act_dtype, gating, x, router_w, router_b, ids, w, probs, gap, stream=None):
+    """Router + top-k without any device allocation (scratch in a static device array).
+
+    For callers that cannot allocate device memory where they route tokens; see
+    include/moeslot.h.  All outputs are caller-owned device tensors.
+    """
+    _check(_lib.moe_route_topk_noalloc(E, k, H, act_dtype, gating, _ptr(x), x.shape[0], _ptr(router_w),
+                                       _ptr(router_b), _ptr(ids), _ptr(w), _ptr(probs), _ptr(gap),
+                                       _stream(stream)), "moe_route_topk_noalloc")
 
 
 class HostPool:

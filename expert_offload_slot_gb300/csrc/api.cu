@@ -47,6 +47,13 @@ static moe_status fail(moe_status st, const char* fmt, ...) {
   return st;
 }
 
+namespace moeslot {
+moe_status set_last_error(moe_status st, const char* msg) {
+  g_err = msg;
+  return st;
+}
+}  // namespace moeslot
+
 #define CUDA_TRY(call)                                                                    \
   do {                                                                                    \
     cudaError_t e_ = (call);                                                              \

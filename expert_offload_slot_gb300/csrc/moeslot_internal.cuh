@@ -128,5 +128,6 @@ int launch_load_slot(const PoolDev& p, const Scratch& sc, int layer, int expert,
 int launch_rebuild_owner(const PoolDev& p, cudaStream_t s);
 
 int sm_count();
+moe_status set_last_error(moe_status st, const char* msg);   // text for moe_last_error()
 
 }  // namespace moeslot

@@ -218,6 +218,30 @@ enum { MOE_STAGE_ROUTE = 0,   /* router GEMV + gate/top-k                     */
 MOE_API moe_status moe_profile_enable(moe_pool* pool, int32_t on);
 MOE_API moe_status moe_profile_read(moe_pool* pool, int32_t layer, float* stage_ms /* [MOE_NUM_STAGES] */);
 
+/* Router projection + gate/top-k (steps a1, a2) with no device allocation.
+ * The pages have no counterpart: this exists for callers that cannot call
+ * cudaMalloc where they route tokens — code running while a CUDA graph is
+ * captured in global capture mode, or hosts whose framework owns the device
+ * memory budget and forbids third-party allocations — and so cannot create a
+ * moe_pool.  The fp32 logits scratch is a file-scope device array of
+ * MOE_NOALLOC_MAX_LOGITS floats held by every device that loads the library
+ * until exit; T * num_experts above it returns MOE_ERR_CAPACITY.  All calls on
+ * a device share that array: calls whose kernels overlap on the GPU race.
+ * Runs on the current device and on `stream`; the first call on a device looks
+ * up the array's device address (cudaGetSymbolAddress), so make it before any
+ * stream capture.  Calls no allocating routine.
+ *   x         device [T, hidden] act_dtype (MOE_F32 or MOE_BF16)
+ *   router_w  device [num_experts, hidden] act_dtype (one layer's W_r)
+ *   router_b  device fp32 [num_experts]
+ *   ids [T, top_k] int32, w [T, top_k] fp32, probs [T, num_experts] fp32,
+ *   gap [T] fp32: device outputs, as moe_get_routing describes them.
+ * Argument errors return MOE_ERR_INVALID; T == 0 returns MOE_OK. */
+#define MOE_NOALLOC_MAX_LOGITS 65536
+MOE_API moe_status moe_route_topk_noalloc(int32_t num_experts, int32_t top_k, int32_t hidden, int32_t act_dtype,
+                                          int32_t gating, const void* x, int32_t T, const void* router_w,
+                                          const float* router_b, int32_t* ids, float* w, float* probs, float* gap,
+                                          void* stream);
+
 /* Number of kernel launches the library issued since the pool was created. */
 MOE_API uint64_t moe_launch_count(const moe_pool* pool);
 
