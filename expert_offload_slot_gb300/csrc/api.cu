@@ -14,6 +14,7 @@
 // layer l+2 on the pool's copy stream.
 #include <cstdarg>
 #include <cstdio>
+#include <algorithm>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -80,6 +81,7 @@ struct moe_pool {
   std::vector<void*> allocs;
   bool prof_on = false;
   std::vector<cudaEvent_t> prof_ev;   // [L][MOE_NUM_STAGES + 1]
+  TcMaps* tc_maps = nullptr;          // tensor maps of the record array (bf16 weights)
 };
 
 static size_t elt_bytes(int dt) { return dt == MOE_F32 ? 4 : dt == MOE_BF16 ? 2 : 1; }
@@ -197,6 +199,8 @@ static moe_status palloc(moe_pool* P, T** out, size_t count, int fill_byte) {
 }
 
 static void pool_free_all(moe_pool* P) {
+  if (P->tc_maps) tc_maps_destroy(P->tc_maps);
+  P->tc_maps = nullptr;
   for (void* p : P->allocs) cudaFree(p);
   P->allocs.clear();
   for (cudaEvent_t e : P->prof_ev) cudaEventDestroy(e);
@@ -256,7 +260,6 @@ MOE_API moe_status moe_pool_create(const moe_config* cfg, const void* host_pool,
   d.cw0 = cfg->core_w[0]; d.cw1 = cfg->core_w[1]; d.cw2 = cfg->core_w[2]; d.cw3 = cfg->core_w[3];
   d.lay = lay;
   d.host_dev = static_cast<const uint8_t*>(hdev);
-  d.shared_w = static_cast<const uint8_t*>(shared_w);
 
   const size_t S = d.S, W = d.W, Tm = cfg->max_tokens, k = d.k;
   const size_t rows = Tm * k + Tm;
@@ -266,9 +269,24 @@ MOE_API moe_status moe_pool_create(const moe_config* cfg, const void* host_pool,
     st = palloc(P, &(ptr), (n), (fill));         \
     if (st != MOE_OK) goto fail_out;             \
   } while (0)
-  PA(d.slots, S * lay.rec, 0);
-  if (cfg->staging_regions == 2) PA(d.staging, 2 * E * lay.rec, 0);
-  else d.staging = nullptr;
+  {
+    // one record array: [S slots | one-step records for misses that get no slot | 2E staging | L shared]
+    const long long need = std::min<long long>((long long)E, (long long)Tm * (long long)k) - (long long)S;
+    d.n_bypass = need > 0 ? (int)need : 0;
+    d.rid_staging0 = (int)S + d.n_bypass;
+    const int n_stage = cfg->staging_regions == 2 ? 2 * (int)E : 0;
+    d.rid_shared0 = d.rid_staging0 + n_stage;
+    d.n_records = d.rid_shared0 + (cfg->has_shared_expert ? (int)L : 0);
+    PA(d.records, (size_t)d.n_records * lay.rec, 0);
+    d.slots = d.records;
+    d.staging = n_stage ? d.records + (size_t)d.rid_staging0 * lay.rec : nullptr;
+    d.shared_w = cfg->has_shared_expert ? d.records + (size_t)d.rid_shared0 * lay.rec : nullptr;
+    if (cfg->has_shared_expert &&
+        cudaMemcpy(const_cast<uint8_t*>(d.shared_w), shared_w, L * lay.rec, cudaMemcpyDefault) != cudaSuccess) {
+      st = fail(MOE_ERR_CUDA, "copying the shared experts failed");
+      goto fail_out;
+    }
+  }
   PA(d.lut, L * E, 0xff);
   PA(d.owner, S, 0xff);
   PA(d.tag, S, 0);
@@ -300,6 +318,23 @@ MOE_API moe_status moe_pool_create(const moe_config* cfg, const void* host_pool,
     uint8_t* hb = nullptr;
     PA(hb, rows * (size_t)d.I * asz, 0);
     P->sc.h = hb;
+  }
+  if (cfg->weight_dtype == MOE_BF16) {
+    // tensor-core expert path (T <= 256): dense routing weights, h buffer, split partials
+    const int np = std::min(tc_npad((int)Tm), 256);
+    P->sc.npad_max = np;
+    PA(P->sc.wmat, (E + 1) * (size_t)np, 0);
+    PA(P->sc.hbuf, (E + 1) * (size_t)np * d.I, 0);
+    PA(P->sc.partial, (size_t)2 * sm_count() * 2 * np * 128, 0);
+    const size_t tiles = std::max((E + 1) * (size_t)((d.I + 127) / 128), (size_t)((d.H + 127) / 128));
+    PA(P->sc.counters, tiles, 0);
+    P->tc_maps = tc_maps_create(d, P->sc);
+    if (!P->tc_maps) {
+      st = fail(MOE_ERR_CUDA, "creating the tensor maps of the record array failed");
+      goto fail_out;
+    }
+  } else {
+    P->sc.npad_max = 0;
   }
 #undef PA
   if (cudaStreamCreateWithFlags(&P->copy_stream, cudaStreamNonBlocking) != cudaSuccess) {
@@ -357,7 +392,7 @@ MOE_API moe_status moe_set_lut(moe_pool* P, const int32_t* lut_host, void* strea
   const size_t rec = P->d.lay.rec;
   for (int sl = 0; sl < S; ++sl) {
     if (owner[sl] < 0) continue;
-    CUDA_TRY(cudaMemcpyAsync(P->d.slots + (size_t)sl * rec, P->host_pool + (size_t)owner[sl] * rec, rec,
+    CUDA_TRY(cudaMemcpyAsync(P->d.records + (size_t)sl * rec, P->host_pool + (size_t)owner[sl] * rec, rec,
                              cudaMemcpyHostToDevice, s));
   }
   CUDA_TRY(cudaGetLastError());
@@ -412,13 +447,21 @@ static moe_status run_layer(moe_pool* P, int layer, const void* x, int T, void* 
   }
   mark(1);
   const int flags = staged ? (PLAN_HISTORY | PLAN_PERMUTE | PLAN_STAGED) : (PLAN_HISTORY | PLAN_CACHE | PLAN_PERMUTE);
-  P->launches += launch_plan(d, sc, layer, T, ids, w, probs, flags, region, s);
+  const bool use_tc = P->tc_maps && tc_npad(T) <= sc.npad_max;
+  P->launches += launch_plan(d, sc, layer, T, ids, w, probs, flags, region, use_tc ? tc_npad(T) : 0, s);
   mark(2);
   if (!staged) P->launches += launch_miss_copy(d, sc, s);
   mark(3);
-  P->launches += launch_ffn_gate_up(d, sc, T, x, s);
+  if (use_tc) {
+    const int n = launch_tc_gate_up(d, sc, P->tc_maps, T, x, s);
+    if (n < 0) return fail(MOE_ERR_INVALID, "x must be 16-byte aligned for the tensor-core path");
+    P->launches += n;
+  } else {
+    P->launches += launch_ffn_gate_up(d, sc, T, x, s);
+  }
   mark(4);
-  P->launches += launch_ffn_down(d, sc, T, out, s);
+  if (use_tc) P->launches += launch_tc_down(d, sc, P->tc_maps, T, out, s);
+  else P->launches += launch_ffn_down(d, sc, T, out, s);
   mark(5);
   if (staged) {
     CUDA_TRY(cudaEventRecord(P->released[region], s));
@@ -457,6 +500,8 @@ MOE_API moe_status moe_forward(moe_pool* P, int32_t layer, const void* x, int32_
   if (T == 0) return MOE_OK;
   if (!x || !out) return fail(MOE_ERR_INVALID, "x/out is NULL");
   if (x == out) return fail(MOE_ERR_INVALID, "out must not alias x");
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(out)) & 15)
+    return fail(MOE_ERR_INVALID, "x and out must be 16-byte aligned");
   if (mode == MOE_MODE_PREFILL_STAGED && P->cfg.staging_regions != 2)
     return fail(MOE_ERR_INVALID, "staged prefill needs staging_regions == 2");
   CUDA_TRY(cudaSetDevice(P->device));
@@ -489,7 +534,7 @@ MOE_API moe_status moe_update_scores(moe_pool* P, int32_t layer, const int32_t* 
   if (T > P->cfg.max_tokens) return fail(MOE_ERR_CAPACITY, "T=%d exceeds max_tokens=%d", T, P->cfg.max_tokens);
   if (!ids || !probs) return fail(MOE_ERR_INVALID, "NULL argument");
   CUDA_TRY(cudaSetDevice(P->device));
-  P->launches += launch_plan(P->d, P->sc, layer, T, ids, nullptr, probs, PLAN_HISTORY, 0,
+  P->launches += launch_plan(P->d, P->sc, layer, T, ids, nullptr, probs, PLAN_HISTORY, 0, 0,
                              static_cast<cudaStream_t>(stream));
   CUDA_TRY(cudaGetLastError());
   return MOE_OK;

@@ -54,7 +54,7 @@ __global__ void load_slot_kernel(PoolDev p, Scratch sc, int layer, int expert, i
   p.lut[le] = slot;
   p.tag[slot] += 1u;
   sc.copies[0].src = p.host_dev + (size_t)le * p.lay.rec;
-  sc.copies[0].dst = p.slots + (size_t)slot * p.lay.rec;
+  sc.copies[0].dst = p.records + (size_t)slot * p.lay.rec;
   *sc.n_copy = 1;
 }
 

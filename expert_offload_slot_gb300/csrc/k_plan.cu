@@ -28,7 +28,7 @@ constexpr int kMaxE = 256;
 struct PlanArgs {
   PoolDev p;
   Scratch sc;
-  int layer, T, flags, region;
+  int layer, T, flags, region, npad;
   const int32_t* ids;
   const float* w;
   const float* probs;
@@ -90,6 +90,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
   __shared__ int base[kMaxE];
   __shared__ int wcnt[kPlanWarps][kMaxE];
   __shared__ int miss_list[kMaxE];
+  __shared__ int bypass_rid[kMaxE];   // one-step record of a miss that got no slot, or -1
+  __shared__ int pos_of[kMaxE];       // work-list position of each expert, or -1
   __shared__ unsigned long long red64[kPlanWarps];
   __shared__ float redf[kPlanWarps];
   __shared__ int sh_misc[8];   // 0: n_miss, 1: epoch, 2: hits, 3: n_copy, 4: bypass, 5: evictions, 6: n_work
@@ -99,7 +101,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
   const int E = p.E, k = p.k, T = a.T, l = a.layer, W = p.W;
   const int Tk = T * k;
 
-  for (int e = tid; e < E; e += kPlanThreads) cnt[e] = 0;
+  for (int e = tid; e < E; e += kPlanThreads) {
+    cnt[e] = 0;
+    bypass_rid[e] = -1;
+    pos_of[e] = -1;
+  }
   if (tid < 8) sh_misc[tid] = 0;
   __syncthreads();
   for (int i = tid; i < Tk; i += kPlanThreads) {
@@ -238,7 +244,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
       }
       if (tid == 0) {
         if (victim < 0) {
-          sh_misc[4] += 1;                            // served from the host pool this step
+          // no slot can be freed: copy into a one-step record for this call only
+          const int b = sh_misc[4];
+          sh_misc[4] = b + 1;
+          int rid = 0;
+          if (b < p.n_bypass) rid = p.S + b;
+          else set_status(p.status, MOE_ERR_CAPACITY);
+          bypass_rid[e] = rid;
+          const int nc = sh_misc[3];
+          a.sc.copies[nc].src = p.host_dev + ((size_t)l * E + e) * rec;
+          a.sc.copies[nc].dst = p.records + (size_t)rid * rec;
+          sh_misc[3] = nc + 1;
         } else {
           const int old = p.owner[victim];
           if (old >= 0) {
@@ -265,7 +281,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
       atomicAdd(&p.stats[ST_MISSES], (unsigned long long)n_miss);
       atomicAdd(&p.stats[ST_BYPASS], (unsigned long long)sh_misc[4]);
       atomicAdd(&p.stats[ST_EVICT], (unsigned long long)sh_misc[5]);
-      atomicAdd(&p.stats[ST_BYTES], (unsigned long long)sh_misc[3] * rec);
+      atomicAdd(&p.stats[ST_BYTES], (unsigned long long)sh_misc[3] * rec);   // slot fills + one-step records
     }
     __syncthreads();
   } else if (tid == 0) {
@@ -353,34 +369,37 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
       for (int w2 = 0; w2 < warp; ++w2) before += (int)red64[w2];
       const int pos = before + __popc(has_bal & ((1u << lane) - 1u));
       const int e = tid;
-      WorkEntry we;
+      int rid;
       if (a.flags & PLAN_STAGED) {
-        we.rec = p.staging + ((size_t)a.region * E + e) * p.lay.rec;
+        rid = p.rid_staging0 + a.region * E + e;
       } else {
         const int sl = p.lut[(size_t)l * E + e];
-        we.rec = (sl >= 0 && sl < p.S) ? p.slots + (size_t)sl * p.lay.rec
-                                       : p.host_dev + ((size_t)l * E + e) * p.lay.rec;
+        rid = (sl >= 0 && sl < p.S) ? sl : (bypass_rid[e] >= 0 ? bypass_rid[e] : 0);
       }
+      WorkEntry we;
+      we.rec = p.records + (size_t)rid * p.lay.rec;
       we.row0 = offs[e];
       we.n = offs[e + 1] - offs[e];
       we.expert = e;
-      we.pad = 0;
+      we.rid = rid;
       a.sc.work[pos] = we;
+      pos_of[e] = pos;
     }
     if (tid == 0) {
       int n = 0;
       for (int w2 = 0; w2 < kMaxE / 32; ++w2) n += (int)red64[w2];
       if (p.shared) {
         WorkEntry we;
-        we.rec = p.shared_w + (size_t)l * p.lay.rec;
+        we.rid = p.rid_shared0 + l;
+        we.rec = p.records + (size_t)we.rid * p.lay.rec;
         we.row0 = Tk;
         we.n = T;
         we.expert = -1;
-        we.pad = 0;
         a.sc.work[n] = we;
         n += 1;
       }
       *a.sc.n_work = n;
+      sh_misc[6] = n;
     }
     if (p.shared) {
       for (int t = tid; t < T; t += kPlanThreads) {
@@ -388,11 +407,25 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
         a.sc.perm_w[Tk + t] = 1.f;
       }
     }
+    // dense routing weights for the tensor-core path: wmat[pos][t] = w of token t for that entry
+    if (a.npad > 0) {
+      __syncthreads();
+      const int nw = sh_misc[6];
+      const int np = a.npad;
+      for (int j = tid; j < nw * np; j += kPlanThreads) a.sc.wmat[j] = 0.f;
+      __syncthreads();
+      for (int i = tid; i < Tk; i += kPlanThreads) {
+        const int e = a.ids[i];
+        if ((unsigned)e < (unsigned)E && pos_of[e] >= 0) a.sc.wmat[(size_t)pos_of[e] * np + i / k] = a.w[i];
+      }
+      if (p.shared)
+        for (int t = tid; t < T; t += kPlanThreads) a.sc.wmat[(size_t)(nw - 1) * np + t] = 1.f;
+    }
   }
 }
 
 int launch_plan(const PoolDev& p, const Scratch& sc, int layer, int T, const int32_t* ids, const float* w,
-                const float* probs, int flags, int region, cudaStream_t s) {
+                const float* probs, int flags, int region, int npad, cudaStream_t s) {
   PlanArgs a;
   a.p = p;
   a.sc = sc;
@@ -400,6 +433,7 @@ int launch_plan(const PoolDev& p, const Scratch& sc, int layer, int T, const int
   a.T = T;
   a.flags = flags;
   a.region = region;
+  a.npad = npad;
   a.ids = ids;
   a.w = w;
   a.probs = probs;

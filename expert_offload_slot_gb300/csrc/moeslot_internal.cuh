@@ -18,7 +18,7 @@ struct WorkEntry {
   int32_t row0;
   int32_t n;
   int32_t expert;   // routed expert id, or -1 for the shared expert
-  int32_t pad;
+  int32_t rid;      // record index in the pool's record array
 };
 
 // One device-started miss copy: record bytes from the mapped host pool to a slot.
@@ -49,9 +49,12 @@ struct PoolDev {           // device-side pointers handed to kernels by value
   float lam, one_minus_lam, cw0, cw1, cw2, cw3;
   Layout lay;
   const uint8_t* host_dev;     // device-visible base of the mapped host pool
-  uint8_t* slots;              // fixed base of the slot pool
-  uint8_t* staging;            // 2 * E records, or null
-  const uint8_t* shared_w;     // L shared-expert records, or null
+  // One record array: [S slots | n_bypass one-step records | 2E staging | L shared].
+  uint8_t* records;
+  int32_t n_bypass, rid_staging0, rid_shared0, n_records;
+  uint8_t* slots;              // == records: the fixed base of the slot pool
+  uint8_t* staging;            // records + rid_staging0 * rec, or null
+  const uint8_t* shared_w;     // records + rid_shared0 * rec, or null
   int32_t* lut;                // [L*E]
   int32_t* owner;              // [S]
   uint32_t* tag;               // [S]
@@ -83,6 +86,12 @@ struct Scratch {
   CopyJob* copies;    // [E+1]
   int32_t* n_copy;    // [1]
   void* h;            // [(Tmax*k + Tmax), I] act dtype
+  // tensor-core decode path (dense token columns)
+  int32_t npad_max;   // largest padded token count of that path (<= 256)
+  float* wmat;        // [E+1][npad] routing weight of each token for each work entry (0 if not routed)
+  uint16_t* hbuf;     // [E+1][npad][I] bf16: w * SiLU(g) * u
+  float* partial;     // split-reduce partial tiles
+  int32_t* counters;  // per-tile arrival counters (self-resetting)
 };
 
 // ----------------------------------------------------------------- device helpers
@@ -120,10 +129,18 @@ int launch_route_logits(const PoolDev& p, int layer, const void* x, int T, const
 int launch_gate_topk(const PoolDev& p, const float* logits, int T, int32_t* ids, float* w, float* probs,
                      float* gap, cudaStream_t s);
 int launch_plan(const PoolDev& p, const Scratch& sc, int layer, int T, const int32_t* ids, const float* w,
-                const float* probs, int flags, int region, cudaStream_t s);
+                const float* probs, int flags, int region, int npad, cudaStream_t s);
 int launch_miss_copy(const PoolDev& p, const Scratch& sc, cudaStream_t s);
 int launch_ffn_gate_up(const PoolDev& p, const Scratch& sc, int T, const void* x, cudaStream_t s);
 int launch_ffn_down(const PoolDev& p, const Scratch& sc, int T, void* out, cudaStream_t s);
+
+// tensor-core (tcgen05) expert path: bf16 weights, T <= 256 tokens
+struct TcMaps;                      // host-side tensor maps of a pool (k_tc.cu)
+TcMaps* tc_maps_create(const PoolDev& p, const Scratch& sc);
+void tc_maps_destroy(TcMaps* m);
+int tc_npad(int T);                 // padded token count (multiple of 16)
+int launch_tc_gate_up(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, const void* x, cudaStream_t s);
+int launch_tc_down(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, void* out, cudaStream_t s);
 int launch_load_slot(const PoolDev& p, const Scratch& sc, int layer, int expert, int slot, cudaStream_t s);
 int launch_rebuild_owner(const PoolDev& p, cudaStream_t s);
 

@@ -101,13 +101,14 @@ typedef struct {
   int32_t max_tokens;        /* largest T any call on this pool will pass          */
 } moe_config;
 
-typedef struct {
+typedef struct {   /* cumulative counters of a pool */
   uint64_t steps;            /* history updates performed                          */
   uint64_t hits;             /* needed experts found resident                      */
   uint64_t misses;           /* needed experts not resident                        */
-  uint64_t bypass;           /* misses read straight from the host pool (no slot)  */
+  uint64_t bypass;           /* misses that got no slot (every slot held an expert
+                                this step needs): copied into a one-step record   */
   uint64_t evictions;        /* occupants replaced                                 */
-  uint64_t bytes_copied;     /* host -> slot bytes moved by miss copies            */
+  uint64_t bytes_copied;     /* host -> device bytes moved by miss copies          */
   uint64_t near_ties;        /* tokens whose k-th/(k+1)-th logit gap is < 1e-4     */
   uint64_t staged_layers;    /* layers copied into a staging region               */
 } moe_stats;
@@ -189,7 +190,8 @@ MOE_API moe_status moe_clear_status(moe_pool* pool);
 /* Blocking: host copies of the last forward's routing (any pointer may be NULL).
  *   ids [T,k] int32, w [T,k] fp32, probs [T,E] fp32, gap [T] fp32 (the k-th
  *   minus the (k+1)-th fp32 logit; +inf when k == E or the routing was
- *   supplied), slots [T,k] int32 (slot read, -1 = read from the host pool),
+ *   supplied), slots [T,k] int32 (slot read; -1 = a one-step copy, -2 = a
+ *   staging region),
  *   perm [T*k] int32 (flat entry t*k+j at each expert-sorted row),
  *   offs [E+1] int32 (row offset of each expert).  *T_out receives T. */
 MOE_API moe_status moe_get_routing(moe_pool* pool, int32_t* ids, float* w, float* probs, float* gap,
