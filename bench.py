@@ -49,6 +49,9 @@ def parse_args():
     ap.add_argument("--prof-steps", type=int, default=32)
     ap.add_argument("--cpu-sample", type=int, default=12, help="oracle layer-steps in cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling only: run the workload's layer shape with fewer layers (0 = all)")
+    ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
 
 
@@ -219,7 +222,8 @@ class DecodeBench:
                "bytes_copied": st1["bytes_copied"] - st0["bytes_copied"], "clocks": clk}
         res["status"] = self.pool.status()
         # profiling pass: per-stage CUDA-event times of every layer, same workload continued
-        res["prof"] = self.profile(xs, x_in, out, s, T, prof_steps)
+        res["prof"] = self.profile(xs, x_in, out, s, T, prof_steps) if prof_steps > 0 else \
+            {"launches": 0, "stage_ms": [0.0] * self.moe.MOE_NUM_STAGES, "sum_U": 0, "T": T, "bytes_copied": 0}
         if e2e:
             res["e2e"] = self.run_e2e(xs, g, x_in, out, s, W, K)
         del g
@@ -275,12 +279,11 @@ class DecodeBench:
         self.host.free()
 
 
-def gate_up_bytes(wl, sum_U, launches, T):
-    """Algorithmic bytes of all gate/up launches: U expert w13 blocks + x reads + h writes."""
-    eb = wl.weight_elt_bytes
-    w13 = 2 * wl.I * wl.H * eb
-    per_launch_act = T * wl.H * wl.act_elt_bytes + T * wl.k * wl.I * wl.act_elt_bytes
-    return sum_U * w13 + launches * per_launch_act
+def ffn_algorithmic_bytes(wl, sum_U, bytes_copied, layer_steps, T):
+    """HBM bytes the expert FFN must move: the U expert records it reads (3*H*I weights each),
+    the miss bytes it writes into slots, and x in / out once per layer-step."""
+    Be = 3 * wl.H * wl.I * wl.weight_elt_bytes
+    return sum_U * Be + bytes_copied + layer_steps * 2 * T * wl.H * wl.act_elt_bytes
 
 
 def step_bytes(wl, U_per_layer, T):
@@ -356,8 +359,13 @@ def main():
     args = parse_args()
     import torch
 
+    import dataclasses
+
     from synth import get_workload
     wl = get_workload(args.workload)
+    if args.layers:
+        # a reduced case for profiler captures: same layer shape, fewer layers, same residency
+        wl = dataclasses.replace(wl, L=args.layers)
     rank, world, local = dist_setup(args.gpus)
     label = WORKLOAD_LABEL.get(args.workload, args.workload)
     T = args.batch
@@ -401,22 +409,22 @@ def main():
                              "stage_us_per_layer": {n: v * 1e3 / max(1, r["prof"]["launches"])
                                                     for n, v in zip(moe.STAGES, r["prof"]["stage_ms"])}}
         clocks = Clocks(local) if rank == 0 else None
-        r = bench.run(T, args.warmup, args.steps, args.prof_steps, clocks, world, e2e=True)
+        r = bench.run(T, args.warmup, args.steps, args.prof_steps, clocks, world, e2e=not args.no_e2e)
     finally:
         pass
     ms = max_over_ranks(r["ms"], world)
     tokens = sum_over_ranks(r["steps"] * T * wl.L, world)
     value = tokens / (ms / 1e3)
-    e2e_ms = max_over_ranks(r["e2e"]["ms"], world)
+    e2e_ms = max_over_ranks(r["e2e"]["ms"], world) if "e2e" in r else float("nan")
     e2e_value = tokens / (e2e_ms / 1e3)
 
     prof = r["prof"]
     peak, peak_kind = load_peaks()
-    gu_ms = prof["stage_ms"][3]
-    gu_bytes = gate_up_bytes(wl, prof["sum_U"], prof["launches"], T)
-    achieved = gu_bytes / (gu_ms / 1e3) / 1e9
+    ffn_ms = prof["stage_ms"][moe.STAGES.index("ffn")] + prof["stage_ms"][moe.STAGES.index("copy")]
     layer_steps = prof["launches"]
     U_mean = prof["sum_U"] / max(1, layer_steps)
+    ffn_bytes = ffn_algorithmic_bytes(wl, prof["sum_U"], prof["bytes_copied"], layer_steps, T)
+    achieved = ffn_bytes / (ffn_ms / 1e3) / 1e9 if ffn_ms > 0 else 0.0
     prof_layer_us = sum(prof["stage_ms"]) * 1e3 / max(1, layer_steps)
     layer_bytes = step_bytes(wl, U_mean, T)
     if rank != 0:
@@ -434,16 +442,16 @@ def main():
         "us_per_layer": ms * 1e3 / (r["steps"] * wl.L),
         "hit_rate": r["hits"] / max(1, r["hits"] + r["misses"]),
         "miss_copy_GB": r["bytes_copied"] / 1e9,
-        "e2e": {"value": e2e_value, "unit": "MoE-layer tokens/s", "h2d_bytes_per_step": r["e2e"]["h2d"],
-                "d2h_bytes_per_step": r["e2e"]["d2h"]},
-        "roofline": {"bound": "hbm", "kernel": "ffn_gate_up_kernel", "achieved": achieved, "peak": peak,
-                     "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+        "e2e": {"value": e2e_value, "unit": "MoE-layer tokens/s",
+                "h2d_bytes_per_step": r.get("e2e", {}).get("h2d"), "d2h_bytes_per_step": r.get("e2e", {}).get("d2h")},
+        "roofline": {"bound": "hbm", "kernel": "tc_fused_decode_kernel (miss copies + gate/up + down + combine)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
                      "peak_source": f"{peak_kind} hbm_gbs", "launches_timed": prof["launches"],
-                     "bytes_per_launch": gu_bytes / max(1, prof["launches"]),
-                     "us_per_launch": gu_ms * 1e3 / max(1, prof["launches"])},
+                     "bytes_per_launch": ffn_bytes / max(1, prof["launches"]),
+                     "us_per_launch": ffn_ms * 1e3 / max(1, prof["launches"])},
         "layer_roofline": {"algorithmic_bytes_per_layer": layer_bytes, "mean_U": U_mean,
                            "us_per_layer_profiled": prof_layer_us,
-                           "frac": layer_bytes / (prof_layer_us * 1e-6) / 1e9 / peak},
+                           "frac": layer_bytes / (prof_layer_us * 1e-6) / 1e9 / peak if prof_layer_us else 0.0},
         "stage_us_per_layer": {n: v * 1e3 / max(1, layer_steps) for n, v in zip(moe.STAGES, prof["stage_ms"])},
         "clocks": r["clocks"],
         "gpu_launches": r["launches_per_step"] * r["steps"],

@@ -24,7 +24,7 @@ MOE_F32, MOE_BF16, MOE_FP8_E4M3_B128 = 0, 1, 2
 MOE_GATE_SOFTMAX_RENORM, MOE_GATE_SIGMOID_RENORM = 0, 1
 MOE_EVICT_CORE, MOE_EVICT_MRS, MOE_EVICT_LRU = 0, 1, 2
 MOE_MODE_AUTO, MOE_MODE_DECODE, MOE_MODE_PREFILL_STAGED = 0, 1, 2
-STAGES = ("route", "plan", "copy", "gate_up", "down")
+STAGES = ("route", "plan", "copy", "ffn")
 MOE_NUM_STAGES = len(STAGES)
 
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID", 2: "MOE_ERR_OOM", 3: "MOE_ERR_CUDA", 4: "MOE_ERR_CAPACITY",

@@ -82,6 +82,8 @@ struct moe_pool {
   bool prof_on = false;
   std::vector<cudaEvent_t> prof_ev;   // [L][MOE_NUM_STAGES + 1]
   TcMaps* tc_maps = nullptr;          // tensor maps of the record array (bf16 weights)
+  cudaStream_t side = nullptr;        // miss copies run here, beside gate/up over resident experts
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
 };
 
 static size_t elt_bytes(int dt) { return dt == MOE_F32 ? 4 : dt == MOE_BF16 ? 2 : 1; }
@@ -124,6 +126,16 @@ static Layout layout_of(const moe_config* c) {
   Layout L;
   const size_t eb = elt_bytes(c->weight_dtype);
   const size_t H = c->hidden, I = c->inter;
+  if (c->weight_dtype == MOE_BF16) {
+    // 128 x 64 tiles in 128-byte-swizzled order: w13 [I/128][H/64][gate, up], w2 [H/128][I/64]
+    const size_t mt_i = (I + 127) / 128, kb_h = (H + 63) / 64, mt_h = (H + 127) / 128, kb_i = (I + 63) / 64;
+    const size_t w13 = 2 * mt_i * kb_h * 16384, w2 = mt_h * kb_i * 16384;
+    L.off13 = 0;
+    L.off2 = w13;
+    L.offs13 = L.offs2 = w13 + w2;
+    L.rec = (w13 + w2 + 4095) / 4096 * 4096;
+    return L;
+  }
   const size_t w13 = 2 * I * H * eb, w2 = H * I * eb;
   size_t s13 = 0, s2 = 0;
   if (c->weight_dtype == MOE_FP8_E4M3_B128) {
@@ -210,6 +222,9 @@ static void pool_free_all(moe_pool* P) {
     if (P->released[r]) cudaEventDestroy(P->released[r]);
   }
   if (P->copy_stream) cudaStreamDestroy(P->copy_stream);
+  if (P->side) cudaStreamDestroy(P->side);
+  if (P->ev_fork) cudaEventDestroy(P->ev_fork);
+  if (P->ev_join) cudaEventDestroy(P->ev_join);
 }
 
 MOE_API moe_status moe_pool_create(const moe_config* cfg, const void* host_pool, size_t host_pool_bytes,
@@ -222,6 +237,8 @@ MOE_API moe_status moe_pool_create(const moe_config* cfg, const void* host_pool,
   const Layout lay = layout_of(cfg);
   const size_t L = cfg->num_layers, E = cfg->num_experts;
   if (!host_pool) return fail(MOE_ERR_INVALID, "host_pool is NULL");
+  if ((E + 1) * (lay.rec / 16) >= (1ull << 32))
+    return fail(MOE_ERR_INVALID, "expert record too large for the copy kernel's 32-bit index space");
   if (host_pool_bytes < L * E * lay.rec)
     return fail(MOE_ERR_INVALID, "host_pool_bytes %zu < L*E*record_bytes %zu", host_pool_bytes, L * E * lay.rec);
   if (!router_w || !router_b) return fail(MOE_ERR_INVALID, "router weights are NULL");
@@ -300,6 +317,7 @@ MOE_API moe_status moe_pool_create(const moe_config* cfg, const void* host_pool,
   PA(d.step, L, 0);
   PA(d.status, 1, 0);
   PA(d.stats, ST_COUNT, 0);
+  P->sc.tmax = (int32_t)Tm;
   PA(P->sc.logits, Tm * E, 0);
   PA(P->sc.probs, Tm * E, 0);
   PA(P->sc.ids, Tm * k, 0);
@@ -314,6 +332,9 @@ MOE_API moe_status moe_pool_create(const moe_config* cfg, const void* host_pool,
   PA(P->sc.n_work, 1, 0);
   PA(P->sc.copies, E + 1, 0);
   PA(P->sc.n_copy, 1, 0);
+  PA(P->sc.ticket, 1, 0);
+  PA(P->sc.elist, 2 * (E + 1), 0);     // written by the plan kernel for every pool
+  PA(P->sc.ecount, 2, 0);
   {
     uint8_t* hb = nullptr;
     PA(hb, rows * (size_t)d.I * asz, 0);
@@ -325,9 +346,19 @@ MOE_API moe_status moe_pool_create(const moe_config* cfg, const void* host_pool,
     P->sc.npad_max = np;
     PA(P->sc.wmat, (E + 1) * (size_t)np, 0);
     PA(P->sc.hbuf, (E + 1) * (size_t)np * d.I, 0);
-    PA(P->sc.partial, (size_t)2 * sm_count() * 2 * np * 128, 0);
+    PA(P->sc.partial, tc_partial_floats(d, P->sc), 0);
     const size_t tiles = std::max((E + 1) * (size_t)((d.I + 127) / 128), (size_t)((d.H + 127) / 128));
-    PA(P->sc.counters, tiles, 0);
+    P->sc.n_counters = 3 * tiles;
+    PA(P->sc.counters, P->sc.n_counters, 0);
+    PA(P->sc.grid_bar, 2, 0);
+    if ((size_t)tc_npad((int)Tm) > (size_t)np) {
+      // gather path for calls with more tokens than the dense path takes
+      PA(P->sc.inv, Tm * k, 0);
+      PA(P->sc.ntile0, E + 2, 0);
+      PA(P->sc.n_rows, 1, 0);
+      PA(P->sc.xp, rows * (size_t)d.H, 0);
+      PA(P->sc.y, rows * (size_t)d.H, 0);
+    }
     P->tc_maps = tc_maps_create(d, P->sc);
     if (!P->tc_maps) {
       st = fail(MOE_ERR_CUDA, "creating the tensor maps of the record array failed");
@@ -337,6 +368,12 @@ MOE_API moe_status moe_pool_create(const moe_config* cfg, const void* host_pool,
     P->sc.npad_max = 0;
   }
 #undef PA
+  if (cudaStreamCreateWithFlags(&P->side, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&P->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&P->ev_join, cudaEventDisableTiming) != cudaSuccess) {
+    st = fail(MOE_ERR_CUDA, "creating the side stream failed");
+    goto fail_out;
+  }
   if (cudaStreamCreateWithFlags(&P->copy_stream, cudaStreamNonBlocking) != cudaSuccess) {
     st = fail(MOE_ERR_CUDA, "cudaStreamCreate failed");
     goto fail_out;
@@ -436,33 +473,53 @@ static moe_status run_layer(moe_pool* P, int layer, const void* x, int T, void* 
     CUDA_TRY(cudaStreamWaitEvent(s, P->ready[region], 0));
   }
   const int NB = MOE_NUM_STAGES + 1;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (P->prof_on) cudaStreamIsCapturing(s, &cap);
   auto mark = [&](int i) {
-    // External: inside a stream capture this becomes an event-record node
-    if (P->prof_on) cudaEventRecordWithFlags(P->prof_ev[(size_t)layer * NB + i], s, cudaEventRecordExternal);
+    if (!P->prof_on) return;
+    // inside a stream capture an event needs the external flag to become an event-record node
+    if (cap == cudaStreamCaptureStatusActive)
+      cudaEventRecordWithFlags(P->prof_ev[(size_t)layer * NB + i], s, cudaEventRecordExternal);
+    else
+      cudaEventRecord(P->prof_ev[(size_t)layer * NB + i], s);
   };
   mark(0);
   if (!ids_in) {
-    P->launches += launch_route_logits(d, layer, x, T, P->router_w, P->router_b, sc.logits, s);
-    P->launches += launch_gate_topk(d, sc.logits, T, sc.ids, sc.w, sc.probs, sc.gap, s);
+    if (route_fused_ok(d, T)) {
+      P->launches += launch_route_gate_fused(d, layer, x, T, P->router_w, P->router_b, sc, s);
+    } else {
+      P->launches += launch_route_logits(d, layer, x, T, P->router_w, P->router_b, sc.logits, s);
+      P->launches += launch_gate_topk(d, sc.logits, T, sc.ids, sc.w, sc.probs, sc.gap, s);
+    }
   }
   mark(1);
   const int flags = staged ? (PLAN_HISTORY | PLAN_PERMUTE | PLAN_STAGED) : (PLAN_HISTORY | PLAN_CACHE | PLAN_PERMUTE);
-  const bool use_tc = P->tc_maps && tc_npad(T) <= sc.npad_max;
-  P->launches += launch_plan(d, sc, layer, T, ids, w, probs, flags, region, use_tc ? tc_npad(T) : 0, s);
+  const bool tc = P->tc_maps != nullptr;                 // bf16 weights: tensor-core path
+  const bool use_tc = tc && tc_npad(T) <= sc.npad_max;   // dense token columns
+  const bool gather = tc && !use_tc;                     // expert-grouped token tiles
+  P->launches += launch_plan(d, sc, layer, T, ids, w, probs, gather ? (flags | PLAN_GATHER) : flags, region,
+                             use_tc ? tc_npad(T) : 0, s);
   mark(2);
-  if (!staged) P->launches += launch_miss_copy(d, sc, s);
-  mark(3);
   if (use_tc) {
-    const int n = launch_tc_gate_up(d, sc, P->tc_maps, T, x, s);
+    // miss copies, gate/up and down + combine in one cooperative kernel
+    mark(3);
+    const int n = launch_tc_fused_decode(d, sc, P->tc_maps, T, x, out, s);
+    if (n == -1) return fail(MOE_ERR_INVALID, "x must be 16-byte aligned for the tensor-core path");
+    if (n < 0) return fail(MOE_ERR_CUDA, "cooperative launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+    P->launches += n;
+  } else if (gather) {
+    if (!staged) P->launches += launch_miss_copy(d, sc, s);
+    mark(3);
+    const int n = launch_tc_gather(d, sc, P->tc_maps, T, x, out, s);
     if (n < 0) return fail(MOE_ERR_INVALID, "x must be 16-byte aligned for the tensor-core path");
     P->launches += n;
   } else {
+    if (!staged) P->launches += launch_miss_copy(d, sc, s);
+    mark(3);
     P->launches += launch_ffn_gate_up(d, sc, T, x, s);
+    P->launches += launch_ffn_down(d, sc, T, out, s);
   }
   mark(4);
-  if (use_tc) P->launches += launch_tc_down(d, sc, P->tc_maps, T, out, s);
-  else P->launches += launch_ffn_down(d, sc, T, out, s);
-  mark(5);
   if (staged) {
     CUDA_TRY(cudaEventRecord(P->released[region], s));
     if (layer + 2 < d.L) stage_layer(P, layer + 2, region);

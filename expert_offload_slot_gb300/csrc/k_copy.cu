@@ -13,27 +13,41 @@ namespace moeslot {
 constexpr int kCopyThreads = 512;
 constexpr int kCopyUnroll = 8;
 
+// Every (job, 16-byte chunk) pair is one index of a flat space; each thread
+// keeps kCopyUnroll independent loads from the host in flight before storing.
+// The job of an index is idx / rec16, taken as the high word of idx * magic
+// with magic = ceil(2^64 / rec16): exact for every idx < 2^32.
 __global__ void __launch_bounds__(kCopyThreads)
-miss_copy_kernel(const CopyJob* __restrict__ jobs, const int32_t* __restrict__ n_jobs, size_t rec16) {
-  const int n = *n_jobs;
-  const size_t stride = (size_t)gridDim.x * kCopyThreads;
-  for (int j = 0; j < n; ++j) {
-    const uint4* __restrict__ src = reinterpret_cast<const uint4*>(jobs[j].src);
-    uint4* __restrict__ dst = reinterpret_cast<uint4*>(jobs[j].dst);
-    size_t i = (size_t)blockIdx.x * kCopyThreads + threadIdx.x;
-    for (; i + (kCopyUnroll - 1) * stride < rec16; i += kCopyUnroll * stride) {
-      uint4 v[kCopyUnroll];
+miss_copy_kernel(const CopyJob* __restrict__ jobs, const int32_t* __restrict__ n_jobs, uint32_t rec16,
+                 unsigned long long magic) {
+  const uint32_t n = (uint32_t)*n_jobs;
+  if (n == 0) return;
+  const uint32_t total = n * rec16;
+  const uint32_t stride = gridDim.x * kCopyThreads;
+  for (uint32_t base = blockIdx.x * kCopyThreads + threadIdx.x; base < total; base += stride * kCopyUnroll) {
+    uint4 v[kCopyUnroll];
+    uint4* dst[kCopyUnroll];
 #pragma unroll
-      for (int u = 0; u < kCopyUnroll; ++u) v[u] = __ldcs(src + i + u * stride);
-#pragma unroll
-      for (int u = 0; u < kCopyUnroll; ++u) dst[i + u * stride] = v[u];
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const uint32_t idx = base + u * stride;
+      dst[u] = nullptr;
+      if (idx < total) {
+        const uint32_t j = (uint32_t)__umul64hi((unsigned long long)idx, magic);
+        const uint32_t c = idx - j * rec16;
+        v[u] = __ldcs(reinterpret_cast<const uint4*>(jobs[j].src) + c);
+        dst[u] = reinterpret_cast<uint4*>(jobs[j].dst) + c;
+      }
     }
-    for (; i < rec16; i += stride) dst[i] = __ldcs(src + i);
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u)
+      if (dst[u]) __stcs(dst[u], v[u]);
   }
 }
 
 int launch_miss_copy(const PoolDev& p, const Scratch& sc, cudaStream_t s) {
-  miss_copy_kernel<<<2 * sm_count(), kCopyThreads, 0, s>>>(sc.copies, sc.n_copy, p.lay.rec / 16);
+  const uint32_t rec16 = (uint32_t)(p.lay.rec / 16);
+  const unsigned long long magic = ~0ull / rec16 + 1ull;
+  miss_copy_kernel<<<2 * sm_count(), kCopyThreads, 0, s>>>(sc.copies, sc.n_copy, rec16, magic);
   return 1;
 }
 

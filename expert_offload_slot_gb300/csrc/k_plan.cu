@@ -1,9 +1,8 @@
 // Steps a3 (routing history and eviction score), a4 (expert_id -> slot_id
 // rewrite and miss detection), a5 (victim choice and table update) and a7
-// (stable permutation of token rows by expert, and the work list the expert
-// kernels consume).  One CTA per layer call: the victim sequence of a layer is
-// a chain of dependent decisions, and the whole working set (E <= 256 experts,
-// one layer's slots) fits a CTA.
+// (stable permutation of token rows by expert, and the work lists the expert
+// kernels consume).  One CTA per layer call: the victims of a layer are a
+// chain of dependent decisions and the whole working set fits a CTA.
 //
 // Sources: SeqMoE "Mechanism" (slot pool shared by all layers at one fixed
 // base; a table rewrites expert_id to slot_id; the device owns the cache
@@ -15,8 +14,16 @@
 // Recent Score); RapidMoE §4.3 (token-averaged router score for multi-token
 // steps).
 //
+// Latency plan: everything the decisions read (the layer's ring history, the
+// step's probabilities, the table row, the owner of every slot) is staged into
+// shared memory in one round trip; victims come from block arg-mins over
+// shared memory; the table, owners, tags and copy list are then written in
+// parallel without reading global memory again.
+//
 // Score arithmetic uses explicitly rounded fp32 operations in a fixed order
-// (no contraction), because the scores decide integer victim choices.
+// (no contraction), because the scores decide integer victim choices.  The
+// token average sums blocks of 32 consecutive tokens in ascending order, then
+// the block sums in ascending order.
 #include "moeslot_internal.cuh"
 
 namespace moeslot {
@@ -24,6 +31,10 @@ namespace moeslot {
 constexpr int kPlanThreads = 1024;
 constexpr int kPlanWarps = kPlanThreads / 32;
 constexpr int kMaxE = 256;
+constexpr int kTokBlock = 32;
+constexpr int kOwnerSmemMax = 24576;   // slots whose owner is staged in shared memory
+constexpr int kIdsSmemMax = 4096;      // routing entries (T*k) staged in shared memory
+constexpr int kStageUnroll = 8;        // loads in flight per thread while staging
 
 struct PlanArgs {
   PoolDev p;
@@ -32,6 +43,8 @@ struct PlanArgs {
   const int32_t* ids;
   const float* w;
   const float* probs;
+  int owner_cap;        // slots staged in shared memory (S, or 0 for the global-memory path)
+  int tok_rows;         // rows of the token staging area
 };
 
 // Orderable key: (score ascending, slot ascending).  -0 is folded into +0.
@@ -68,82 +81,202 @@ __device__ unsigned long long block_min_u64(unsigned long long v, unsigned long 
   return out;
 }
 
-__device__ float block_max_f(float v, float* red) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  v = warp_max(v);
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  if (warp == 0) {
-    float r = lane < kPlanWarps ? red[lane] : -INFINITY;
-    r = warp_max(r);
-    if (lane == 0) red[0] = r;
+struct SmemLayout {
+  size_t hs, hsel, tok, owner, prot, ids, w, total;
+};
+
+__host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~size_t(15); }
+
+__host__ __device__ inline SmemLayout plan_smem_layout(int E, int W, int tok_rows, int owner_cap) {
+  SmemLayout L;
+  size_t off = 0;
+  L.hs = off;
+  off = align16(off + (size_t)W * E * 4);
+  L.hsel = off;
+  off = align16(off + (size_t)W * E);
+  L.tok = off;   // token staging, later reused by the permutation's per-warp counts
+  const size_t tok_bytes = (size_t)tok_rows * E * 4, wc_bytes = (size_t)kPlanWarps * E * 4;
+  off = align16(off + (tok_bytes > wc_bytes ? tok_bytes : wc_bytes));
+  L.owner = off;
+  off = align16(off + (size_t)owner_cap * 4);
+  L.prot = off;
+  off = align16(off + (size_t)((owner_cap + 31) / 32) * 4);
+  L.ids = off;
+  off = align16(off + (size_t)kIdsSmemMax * 4);
+  L.w = off;
+  off = align16(off + (size_t)kIdsSmemMax * 4);
+  L.total = off;
+  return L;
+}
+
+// Copy n elements global -> shared with kStageUnroll loads in flight per thread.
+template <typename T>
+__device__ __forceinline__ void stage_copy(T* dst, const T* __restrict__ src, int n) {
+  for (int j0 = threadIdx.x; j0 < n; j0 += kPlanThreads * kStageUnroll) {
+    T v[kStageUnroll];
+#pragma unroll
+    for (int u = 0; u < kStageUnroll; ++u) {
+      const int j = j0 + u * kPlanThreads;
+      if (j < n) v[u] = src[j];
+    }
+#pragma unroll
+    for (int u = 0; u < kStageUnroll; ++u) {
+      const int j = j0 + u * kPlanThreads;
+      if (j < n) dst[j] = v[u];
+    }
   }
-  __syncthreads();
-  const float out = red[0];
-  __syncthreads();
-  return out;
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
   __shared__ int cnt[kMaxE];
   __shared__ int offs[kMaxE + 1];
   __shared__ int base[kMaxE];
-  __shared__ int wcnt[kPlanWarps][kMaxE];
+  __shared__ int lut_s[kMaxE];
+  __shared__ float score_s[kMaxE];
   __shared__ int miss_list[kMaxE];
+  __shared__ int victim_s[kMaxE];
+  __shared__ int old_s[kMaxE];
   __shared__ int bypass_rid[kMaxE];   // one-step record of a miss that got no slot, or -1
   __shared__ int pos_of[kMaxE];       // work-list position of each expert, or -1
+  __shared__ int missed[kMaxE];       // 1 if the expert was not resident at the start of this step
+  __shared__ int wtmp[3][kMaxE / 32];
   __shared__ unsigned long long red64[kPlanWarps];
-  __shared__ float redf[kPlanWarps];
-  __shared__ int sh_misc[8];   // 0: n_miss, 1: epoch, 2: hits, 3: n_copy, 4: bypass, 5: evictions, 6: n_work
+  __shared__ float red4[kPlanWarps][4];
+  __shared__ int sh_misc[12];   // 0 n_miss, 2 hits, 4 bypass, 5 evictions, 6 n_work
+  extern __shared__ __align__(16) uint8_t dsm[];
 
   const PoolDev& p = a.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = p.E, k = p.k, T = a.T, l = a.layer, W = p.W;
   const int Tk = T * k;
+  const SmemLayout SL = plan_smem_layout(E, W, a.tok_rows, a.owner_cap);
+  float* hs = reinterpret_cast<float*>(dsm + SL.hs);
+  uint8_t* hsel = dsm + SL.hsel;
+  float* tok = reinterpret_cast<float*>(dsm + SL.tok);
+  int* wcnt = reinterpret_cast<int*>(dsm + SL.tok);          // [kPlanWarps][E], after the history phase
+  int* owner_s = reinterpret_cast<int*>(dsm + SL.owner);
+  uint32_t* prot = reinterpret_cast<uint32_t*>(dsm + SL.prot);
+  const bool owner_in_smem = a.owner_cap >= p.S;
+  // routing entries: shared memory when they fit, else global memory
+  const bool ids_in_smem = Tk <= kIdsSmemMax;
+  int32_t* ids_s = reinterpret_cast<int32_t*>(dsm + SL.ids);
+  float* w_s = reinterpret_cast<float*>(dsm + SL.w);
+  const int32_t* ids = ids_in_smem ? ids_s : a.ids;
+  const float* wrt = ids_in_smem ? w_s : a.w;
 
+  // ------------------------------------------------------------ stage (one round trip)
   for (int e = tid; e < E; e += kPlanThreads) {
     cnt[e] = 0;
     bypass_rid[e] = -1;
     pos_of[e] = -1;
+    missed[e] = 0;
   }
-  if (tid < 8) sh_misc[tid] = 0;
+  if (tid < 12) sh_misc[tid] = 0;
+  const bool hist = (a.flags & PLAN_HISTORY) != 0;
+  const bool cache = (a.flags & PLAN_CACHE) != 0;
+  int t_step = 0;
+  float ema0 = 0.f;
+  int last0 = -1;
+  if (ids_in_smem) {
+    stage_copy(ids_s, a.ids, Tk);
+    if (a.w && (a.flags & PLAN_PERMUTE)) stage_copy(w_s, a.w, Tk);
+  }
+  if (hist) {
+    t_step = p.step[l];
+    stage_copy(hs, p.hist_s + (size_t)l * W * E, W * E);
+    stage_copy(hsel, p.hist_sel + (size_t)l * W * E, W * E);
+    if (T <= kTokBlock) {
+      stage_copy(tok, a.probs, T * E);
+    } else {
+      // block partial sums: tok[b][e] = sum of probs over tokens [32b, 32b+32), ascending
+      const int nblk = (T + kTokBlock - 1) / kTokBlock;
+      for (int j = tid; j < nblk * E; j += kPlanThreads) {
+        const int b = j / E, e = j - b * E;
+        const int t0 = b * kTokBlock, t1 = min(T, t0 + kTokBlock);
+        float v[kTokBlock];
+#pragma unroll
+        for (int q = 0; q < kTokBlock; ++q) v[q] = t0 + q < t1 ? a.probs[(size_t)(t0 + q) * E + e] : 0.f;
+        float s = 0.f;
+#pragma unroll
+        for (int q = 0; q < kTokBlock; ++q)
+          if (t0 + q < t1) s = __fadd_rn(s, v[q]);
+        tok[j] = s;
+      }
+    }
+    if (tid < E) {
+      ema0 = p.ema[(size_t)l * E + tid];
+      last0 = p.last_sel[(size_t)l * E + tid];
+    }
+  }
+  if (cache) {
+    if (tid < E) lut_s[tid] = p.lut[(size_t)l * E + tid];
+    if (owner_in_smem) {
+      stage_copy(owner_s, p.owner, p.S);
+      for (int j = tid; j < (p.S + 31) / 32; j += kPlanThreads) prot[j] = 0u;
+    }
+  }
   __syncthreads();
   for (int i = tid; i < Tk; i += kPlanThreads) {
-    const int e = a.ids[i];
+    const int e = ids[i];
     if ((unsigned)e >= (unsigned)E) set_status(p.status, MOE_ERR_BOUNDS);
     else atomicAdd(&cnt[e], 1);
   }
   __syncthreads();
 
   // ------------------------------------------------------------ a3 history
-  if (a.flags & PLAN_HISTORY) {
-    const int t = p.step[l];
+  if (hist) {
+    const int t = t_step;
     const int ring = t % W;
+    const bool mine = tid < E;
     float s = 0.f, m = 0.f;
     int count = 0, age = 0;
-    const bool mine = tid < E;
     if (mine) {
       const int e = tid;
-      for (int tt = 0; tt < T; ++tt) s = __fadd_rn(s, a.probs[(size_t)tt * E + e]);
+      if (T <= kTokBlock) {
+        for (int tt = 0; tt < T; ++tt) s = __fadd_rn(s, tok[tt * E + e]);
+      } else {
+        const int nblk = (T + kTokBlock - 1) / kTokBlock;
+        for (int b = 0; b < nblk; ++b) s = __fadd_rn(s, tok[b * E + e]);
+      }
       s = __fdiv_rn(s, (float)T);
       const int sel = cnt[e] > 0 ? 1 : 0;
+      hs[ring * E + e] = s;
+      hsel[ring * E + e] = (uint8_t)sel;
       const size_t he = ((size_t)l * W + ring) * E + e;
       p.hist_s[he] = s;
       p.hist_sel[he] = (uint8_t)sel;
-      const size_t le = (size_t)l * E + e;
-      m = __fadd_rn(__fmul_rn(p.lam, p.ema[le]), __fmul_rn(p.one_minus_lam, sel ? 1.f : 0.f));
-      p.ema[le] = m;
-      if (sel) p.last_sel[le] = t;
-      age = t - p.last_sel[le];
-      for (int j = 0; j < W; ++j) count += p.hist_sel[((size_t)l * W + j) * E + e];
+      m = __fadd_rn(__fmul_rn(p.lam, ema0), __fmul_rn(p.one_minus_lam, sel ? 1.f : 0.f));
+      p.ema[(size_t)l * E + e] = m;
+      int last = last0;
+      if (sel) {
+        last = t;
+        p.last_sel[(size_t)l * E + e] = t;
+      }
+      age = t - last;
+      for (int j = 0; j < W; ++j) count += hsel[j * E + e];
     }
     float sc = 0.f;
     if (p.policy == MOE_EVICT_CORE) {
-      // all threads take part in the reductions
-      const float cmax = block_max_f(mine ? (float)count : -INFINITY, redf);
-      const float mmax = block_max_f(mine ? m : -INFINITY, redf);
-      const float smax = block_max_f(mine ? s : -INFINITY, redf);
-      const float amax = block_max_f(mine ? (float)age : -INFINITY, redf);
+      // the four layer maxima in one block reduction
+      float v4[4] = {mine ? (float)count : -INFINITY, mine ? m : -INFINITY, mine ? s : -INFINITY,
+                     mine ? (float)age : -INFINITY};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) v4[q] = warp_max(v4[q]);
+      if (lane == 0) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) red4[warp][q] = v4[q];
+      }
+      __syncthreads();
+      if (warp == 0) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float r = red4[lane][q];
+          r = warp_max(r);
+          if (lane == 0) red4[0][q] = r;
+        }
+      }
+      __syncthreads();
+      const float cmax = red4[0][0], mmax = red4[0][1], smax = red4[0][2], amax = red4[0][3];
       if (mine) {
         const float c_hat = cmax > 0.f ? __fdiv_rn((float)count, cmax) : 0.f;
         const float m_hat = mmax > 0.f ? __fdiv_rn(m, mmax) : 0.f;
@@ -158,81 +291,89 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
         float acc = 0.f;
         for (int j = W - 1; j >= 0; --j) {         // oldest step of the window first
           const int idx = ((t - j) % W + W) % W;
-          acc = __fadd_rn(acc, p.hist_s[((size_t)l * W + idx) * E + tid]);
+          acc = __fadd_rn(acc, hs[idx * E + tid]);
         }
         sc = __fsub_rn(acc, s);
       }
     } else {
-      if (mine) sc = (float)p.last_sel[(size_t)l * E + tid];
+      if (mine) sc = (float)(t - age);             // last selection step, -1 if never
     }
-    if (mine) p.score[(size_t)l * E + tid] = sc;
-    __syncthreads();
+    if (mine) {
+      p.score[(size_t)l * E + tid] = sc;
+      score_s[tid] = sc;
+    }
     if (tid == 0) {
       p.step[l] = t + 1;
       atomicAdd(&p.stats[ST_STEPS], 1ull);
     }
+    __syncthreads();
+  } else if (cache) {
+    if (tid < E) score_s[tid] = p.score[(size_t)l * E + tid];
+    __syncthreads();
   }
 
   // ------------------------------------------------------- a4/a5 table, misses
-  if (a.flags & PLAN_CACHE) {
-    if (tid == 0) sh_misc[1] = *p.epoch + 1;
-    __syncthreads();
-    const int ep = sh_misc[1];
+  if (cache) {
+    const int S = p.S;
+    const size_t rec = p.lay.rec;
+    int ep = 0;
+    if (!owner_in_smem) ep = *p.epoch + 1;
     // protect resident needed experts; list misses in ascending expert id
     int is_miss = 0;
     if (tid < E && cnt[tid] > 0) {
-      const int sl = p.lut[(size_t)l * E + tid];
-      if (sl >= 0 && sl < p.S) {
-        p.prot_epoch[sl] = ep;
+      const int sl = lut_s[tid];
+      if (sl >= 0 && sl < S) {
+        if (owner_in_smem) atomicOr(&prot[sl >> 5], 1u << (sl & 31));
+        else p.prot_epoch[sl] = ep;
         atomicAdd(&sh_misc[2], 1);
       } else {
-        if (sl >= p.S) set_status(p.status, MOE_ERR_BOUNDS);
+        if (sl >= S) set_status(p.status, MOE_ERR_BOUNDS);
         is_miss = 1;
+        missed[tid] = 1;
       }
     }
-    // compaction by warp ballots (all lanes of warps 0..7 take part)
     unsigned miss_bal = 0;
     if (warp < (kMaxE / 32)) {
       miss_bal = __ballot_sync(0xffffffffu, is_miss);
-      if (lane == 0) wcnt[0][warp] = __popc(miss_bal);
+      if (lane == 0) wtmp[0][warp] = __popc(miss_bal);
     }
     __syncthreads();
     if (warp < (kMaxE / 32) && is_miss) {
       int before = 0;
-      for (int w2 = 0; w2 < warp; ++w2) before += wcnt[0][w2];
+      for (int w2 = 0; w2 < warp; ++w2) before += wtmp[0][w2];
       miss_list[before + __popc(miss_bal & ((1u << lane) - 1u))] = tid;
     }
     if (tid == 0) {
       int n = 0;
-      for (int w2 = 0; w2 < kMaxE / 32; ++w2) n += wcnt[0][w2];
+      for (int w2 = 0; w2 < kMaxE / 32; ++w2) n += wtmp[0][w2];
       sh_misc[0] = n;
     }
     __syncthreads();
     const int n_miss = sh_misc[0];
-    const size_t rec = p.lay.rec;
+    // victims, one miss at a time (ascending expert id): lowest free slot, else the
+    // lowest-score slot of this layer that this step does not need, else of another layer
     for (int mi = 0; mi < n_miss; ++mi) {
-      const int e = miss_list[mi];
-      // lowest free slot
       unsigned long long key = ~0ull;
-      for (int s2 = tid; s2 < p.S; s2 += kPlanThreads)
-        if (p.owner[s2] < 0) { key = (unsigned long long)s2; break; }
+      for (int s2 = tid; s2 < S; s2 += kPlanThreads) {
+        const int o = owner_in_smem ? owner_s[s2] : p.owner[s2];
+        if (o < 0) { key = (unsigned long long)s2; break; }
+      }
       key = block_min_u64(key, red64);
       int victim = key == ~0ull ? -1 : (int)key;
       if (victim < 0) {
-        // lowest score among this layer's slots that this step does not need
         key = ~0ull;
-        for (int s2 = tid; s2 < p.S; s2 += kPlanThreads) {
-          const int o = p.owner[s2];
-          if (o >= 0 && o < p.L * E && o / E == l && p.prot_epoch[s2] != ep) {
-            const unsigned long long kk = score_key(p.score[o], s2);
+        for (int s2 = tid; s2 < S; s2 += kPlanThreads) {
+          const int o = owner_in_smem ? owner_s[s2] : p.owner[s2];
+          const bool pr = owner_in_smem ? ((prot[s2 >> 5] >> (s2 & 31)) & 1u) != 0u : p.prot_epoch[s2] == ep;
+          if (o >= 0 && o < p.L * E && o / E == l && !pr) {
+            const unsigned long long kk = score_key(score_s[o - l * E], s2);
             key = kk < key ? kk : key;
           }
         }
         key = block_min_u64(key, red64);
         if (key == ~0ull) {
-          // lowest score among other layers' slots
-          for (int s2 = tid; s2 < p.S; s2 += kPlanThreads) {
-            const int o = p.owner[s2];
+          for (int s2 = tid; s2 < S; s2 += kPlanThreads) {
+            const int o = owner_in_smem ? owner_s[s2] : p.owner[s2];
             if (o >= 0 && o < p.L * E && o / E != l) {
               const unsigned long long kk = score_key(p.score[o], s2);
               key = kk < key ? kk : key;
@@ -243,45 +384,55 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
         victim = key == ~0ull ? -1 : (int)(key & 0xffffffffu);
       }
       if (tid == 0) {
+        const int e = miss_list[mi];
+        victim_s[mi] = victim;
         if (victim < 0) {
-          // no slot can be freed: copy into a one-step record for this call only
-          const int b = sh_misc[4];
-          sh_misc[4] = b + 1;
+          old_s[mi] = -1;
+          const int b = sh_misc[4]++;
           int rid = 0;
-          if (b < p.n_bypass) rid = p.S + b;
+          if (b < p.n_bypass) rid = S + b;
           else set_status(p.status, MOE_ERR_CAPACITY);
           bypass_rid[e] = rid;
-          const int nc = sh_misc[3];
-          a.sc.copies[nc].src = p.host_dev + ((size_t)l * E + e) * rec;
-          a.sc.copies[nc].dst = p.records + (size_t)rid * rec;
-          sh_misc[3] = nc + 1;
         } else {
-          const int old = p.owner[victim];
-          if (old >= 0) {
-            if (old < p.L * E) p.lut[old] = -1;
-            else set_status(p.status, MOE_ERR_BOUNDS);
-            sh_misc[5] += 1;
+          const int old = owner_in_smem ? owner_s[victim] : p.owner[victim];
+          old_s[mi] = old;
+          if (old >= 0) sh_misc[5] += 1;
+          if (owner_in_smem) {
+            owner_s[victim] = l * E + e;
+            prot[victim >> 5] |= 1u << (victim & 31);
+          } else {
+            p.owner[victim] = l * E + e;
+            p.prot_epoch[victim] = ep;
           }
-          p.owner[victim] = l * E + e;
-          p.lut[(size_t)l * E + e] = victim;
-          p.tag[victim] += 1u;
-          p.prot_epoch[victim] = ep;
-          const int nc = sh_misc[3];
-          a.sc.copies[nc].src = p.host_dev + ((size_t)l * E + e) * rec;
-          a.sc.copies[nc].dst = p.slots + (size_t)victim * rec;
-          sh_misc[3] = nc + 1;
+          lut_s[e] = victim;
         }
       }
       __syncthreads();
     }
+    // apply the decisions in parallel: table, owners, tags, copy list (one copy per miss)
+    if (tid < n_miss) {
+      const int e = miss_list[tid], v = victim_s[tid], old = old_s[tid];
+      CopyJob job;
+      job.src = p.host_dev + ((size_t)l * E + e) * rec;
+      if (v >= 0) {
+        if (old >= 0 && old < p.L * E) p.lut[old] = -1;
+        p.lut[(size_t)l * E + e] = v;
+        p.owner[v] = l * E + e;
+        atomicAdd(&p.tag[v], 1u);
+        job.dst = p.records + (size_t)v * rec;
+      } else {
+        job.dst = p.records + (size_t)bypass_rid[e] * rec;
+      }
+      a.sc.copies[tid] = job;
+    }
     if (tid == 0) {
-      *a.sc.n_copy = sh_misc[3];
-      *p.epoch = ep;
+      *a.sc.n_copy = n_miss;
+      if (!owner_in_smem) *p.epoch = ep;
       atomicAdd(&p.stats[ST_HITS], (unsigned long long)sh_misc[2]);
       atomicAdd(&p.stats[ST_MISSES], (unsigned long long)n_miss);
       atomicAdd(&p.stats[ST_BYPASS], (unsigned long long)sh_misc[4]);
       atomicAdd(&p.stats[ST_EVICT], (unsigned long long)sh_misc[5]);
-      atomicAdd(&p.stats[ST_BYTES], (unsigned long long)sh_misc[3] * rec);   // slot fills + one-step records
+      atomicAdd(&p.stats[ST_BYTES], (unsigned long long)n_miss * rec);   // slot fills + one-step records
     }
     __syncthreads();
   } else if (tid == 0) {
@@ -290,6 +441,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
 
   // ------------------------------------------------------ a7 permutation
   if (a.flags & PLAN_PERMUTE) {
+    if (!cache && tid < E) lut_s[tid] = p.lut[(size_t)l * E + tid];
     // exclusive scan of the per-expert counts (warp 0, 32 experts per pass)
     if (warp == 0) {
       int run = 0;
@@ -316,30 +468,31 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
       const int i = c0 + tid;
       int e = -1;
       if (i < Tk) {
-        e = a.ids[i];
+        e = ids[i];
         if ((unsigned)e >= (unsigned)E) e = -1;
       }
-      for (int j = tid; j < kPlanWarps * E; j += kPlanThreads) wcnt[j / E][j % E] = 0;
+      for (int j = tid; j < kPlanWarps * E; j += kPlanThreads) wcnt[j] = 0;
       __syncthreads();
       const unsigned peers = __match_any_sync(0xffffffffu, e);
       const int rank = __popc(peers & ((1u << lane) - 1u));
-      if (e >= 0 && rank == 0) wcnt[warp][e] = __popc(peers);
+      if (e >= 0 && rank == 0) wcnt[warp * E + e] = __popc(peers);
       __syncthreads();
       for (int ee = tid; ee < E; ee += kPlanThreads) {
         int run = 0;
         for (int w2 = 0; w2 < kPlanWarps; ++w2) {
-          const int c = wcnt[w2][ee];
-          wcnt[w2][ee] = run;
+          const int c = wcnt[w2 * E + ee];
+          wcnt[w2 * E + ee] = run;
           run += c;
         }
-        cnt[ee] = run;    // this pass's total for the expert (counts are no longer needed)
+        cnt[ee] = run;    // this pass's total for the expert (the full counts are in offs)
       }
       __syncthreads();
       if (e >= 0) {
-        const int r = base[e] + wcnt[warp][e] + rank;
+        const int r = base[e] + wcnt[warp * E + e] + rank;
         a.sc.perm_tok[r] = i / k;
-        a.sc.perm_w[r] = a.w[i];
+        a.sc.perm_w[r] = wrt[i];
         a.sc.perm_ent[r] = i;
+        if (a.flags & PLAN_GATHER) a.sc.inv[i] = r;
       }
       __syncthreads();
       for (int ee = tid; ee < E; ee += kPlanThreads) base[ee] += cnt[ee];
@@ -347,21 +500,24 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     }
     // slot read by every (t, j) entry
     for (int i = tid; i < Tk; i += kPlanThreads) {
-      const int e = a.ids[i];
+      const int e = ids[i];
       int sl = -1;
-      if ((unsigned)e < (unsigned)E) {
-        if (a.flags & PLAN_STAGED) sl = -2;      // read from a staging region
-        else sl = p.lut[(size_t)l * E + e];
-      }
+      if ((unsigned)e < (unsigned)E) sl = (a.flags & PLAN_STAGED) ? -2 : lut_s[e];
       a.sc.slots_out[i] = sl;
     }
     // work list: experts with rows, ascending id, then the shared expert
     int has = 0;
     if (tid < E) has = (offs[tid + 1] - offs[tid]) > 0;
-    unsigned has_bal = 0;
+    unsigned has_bal = 0, hit_bal = 0, mis_bal = 0;
     if (warp < kMaxE / 32) {
       has_bal = __ballot_sync(0xffffffffu, has);
-      if (lane == 0) red64[warp] = __popc(has_bal);
+      hit_bal = __ballot_sync(0xffffffffu, has && !(tid < E && missed[tid]));
+      mis_bal = __ballot_sync(0xffffffffu, has && (tid < E && missed[tid]));
+      if (lane == 0) {
+        red64[warp] = __popc(has_bal);
+        wtmp[1][warp] = __popc(hit_bal);
+        wtmp[2][warp] = __popc(mis_bal);
+      }
     }
     __syncthreads();
     if (warp < kMaxE / 32 && has) {
@@ -373,7 +529,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
       if (a.flags & PLAN_STAGED) {
         rid = p.rid_staging0 + a.region * E + e;
       } else {
-        const int sl = p.lut[(size_t)l * E + e];
+        const int sl = lut_s[e];
         rid = (sl >= 0 && sl < p.S) ? sl : (bypass_rid[e] >= 0 ? bypass_rid[e] : 0);
       }
       WorkEntry we;
@@ -384,6 +540,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
       we.rid = rid;
       a.sc.work[pos] = we;
       pos_of[e] = pos;
+      // entries that need no copy this step, and entries that do (both in expert order)
+      const unsigned lower = (1u << lane) - 1u;
+      if (missed[e]) {
+        int b = 0;
+        for (int w2 = 0; w2 < warp; ++w2) b += wtmp[2][w2];
+        a.sc.elist[(E + 1) + b + __popc(mis_bal & lower)] = pos;
+      } else {
+        int b = 0;
+        for (int w2 = 0; w2 < warp; ++w2) b += wtmp[1][w2];
+        a.sc.elist[b + __popc(hit_bal & lower)] = pos;
+      }
     }
     if (tid == 0) {
       int n = 0;
@@ -398,6 +565,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
         a.sc.work[n] = we;
         n += 1;
       }
+      int nh = 0, nm = 0;
+      for (int w2 = 0; w2 < kMaxE / 32; ++w2) {
+        nh += wtmp[1][w2];
+        nm += wtmp[2][w2];
+      }
+      if (p.shared) a.sc.elist[nh++] = n - 1;    // the shared expert is always resident
+      a.sc.ecount[0] = nh;
+      a.sc.ecount[1] = nm;
       *a.sc.n_work = n;
       sh_misc[6] = n;
     }
@@ -407,21 +582,63 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
         a.sc.perm_w[Tk + t] = 1.f;
       }
     }
+    __syncthreads();
+    // gather path: first 128-token tile of every entry (entries in ascending expert id, shared last)
+    if ((a.flags & PLAN_GATHER) && warp == 0) {
+      int run = 0;
+      for (int e0 = 0; e0 < E; e0 += 32) {
+        const int e = e0 + lane;
+        const int c = e < E ? offs[e + 1] - offs[e] : 0;
+        const int v = (c + 127) / 128;
+        int inc = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, inc, o);
+          if (lane >= o) inc += y;
+        }
+        if (e < E && c > 0) a.sc.ntile0[pos_of[e]] = run + inc - v;
+        run += __shfl_sync(0xffffffffu, inc, 31);
+      }
+      if (lane == 0) {
+        const int nw = sh_misc[6];
+        if (p.shared) {
+          a.sc.ntile0[nw - 1] = run;
+          run += (T + 127) / 128;
+        }
+        a.sc.ntile0[nw] = run;
+        *a.sc.n_rows = Tk + (p.shared ? T : 0);
+      }
+    }
     // dense routing weights for the tensor-core path: wmat[pos][t] = w of token t for that entry
     if (a.npad > 0) {
-      __syncthreads();
       const int nw = sh_misc[6];
       const int np = a.npad;
       for (int j = tid; j < nw * np; j += kPlanThreads) a.sc.wmat[j] = 0.f;
       __syncthreads();
       for (int i = tid; i < Tk; i += kPlanThreads) {
-        const int e = a.ids[i];
-        if ((unsigned)e < (unsigned)E && pos_of[e] >= 0) a.sc.wmat[(size_t)pos_of[e] * np + i / k] = a.w[i];
+        const int e = ids[i];
+        if ((unsigned)e < (unsigned)E && pos_of[e] >= 0) a.sc.wmat[(size_t)pos_of[e] * np + i / k] = wrt[i];
       }
       if (p.shared)
         for (int t = tid; t < T; t += kPlanThreads) a.sc.wmat[(size_t)(nw - 1) * np + t] = 1.f;
     }
   }
+}
+
+size_t plan_smem_bytes(const PoolDev& p, int Tmax, int* owner_cap_out, int* tok_rows_out) {
+  // T <= 32 stages the probabilities themselves (up to 32 rows); larger T stages
+  // one partial sum per 32-token block
+  const int nblk = (Tmax + kTokBlock - 1) / kTokBlock;
+  const int tok_rows = nblk > kTokBlock ? nblk : kTokBlock;
+  int cap = p.S <= kOwnerSmemMax ? p.S : 0;
+  SmemLayout L = plan_smem_layout(p.E, p.W, tok_rows, cap);
+  if (L.total > 200 * 1024) {          // very large pools: owners stay in global memory
+    cap = 0;
+    L = plan_smem_layout(p.E, p.W, tok_rows, 0);
+  }
+  if (owner_cap_out) *owner_cap_out = cap;
+  if (tok_rows_out) *tok_rows_out = tok_rows;
+  return L.total;
 }
 
 int launch_plan(const PoolDev& p, const Scratch& sc, int layer, int T, const int32_t* ids, const float* w,
@@ -437,7 +654,13 @@ int launch_plan(const PoolDev& p, const Scratch& sc, int layer, int T, const int
   a.ids = ids;
   a.w = w;
   a.probs = probs;
-  plan_kernel<<<1, kPlanThreads, 0, s>>>(a);
+  const size_t smem = plan_smem_bytes(p, sc.tmax, &a.owner_cap, &a.tok_rows);
+  static size_t configured = 0;
+  if (smem > configured) {
+    cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    configured = smem;
+  }
+  plan_kernel<<<1, kPlanThreads, smem, s>>>(a);
   return 1;
 }
 

@@ -1,5 +1,6 @@
 // Step a8 (SwiGLU experts) and a9 (combine) on the 5th-generation tensor cores
-// (tcgen05, accumulators in TMEM, operands staged in shared memory by TMA).
+// (tcgen05, accumulators in TMEM, operands staged in shared memory by the
+// Tensor Memory Accelerator).
 //
 // Expert (RapidMoE §4.5, Eq. 7): y = W_down (SiLU(W_gate x) ⊙ W_up x).
 // Combine (CAP §II-A, Eq. 1): out[t] = sum_j w[t,j] y_j(t) (+ shared expert).
@@ -18,6 +19,18 @@
 //              W_down_u[tile] · hbuf[u]ᵀ
 //            i.e. the combine is accumulated in TMEM in a fixed order (entries
 //            ascending, shared expert last); epilogue: out[t][h] = D (bf16).
+//
+// Weights: a bf16 expert record is stored as 128-row x 64-column tiles
+// already in the 128-byte-swizzled order the MMA descriptor reads (w13 as
+// [I/128][H/64][gate, up], w2 as [H/128][I/64]), so every pipeline stage is
+// ONE contiguous bulk copy (32 KB gate+up, or 16 KB down) that streams from
+// HBM at full burst length.  Activations (x, h) come through TMA tensor maps.
+//
+// Large token counts (T > 256) use the gather modes: tokens are grouped by
+// expert (x rows gathered once), each (entry, 128-token tile, 128-row tile) is
+// a unit, gate/up writes w * SiLU(g) * u per expert row, down writes one bf16
+// row per (token, expert) and a combine kernel sums each token's k rows in
+// ascending expert order (plus the shared expert).
 //
 // When there are fewer output tiles than SMs, each tile's reduction (K for
 // gate_up, the entry list for down) is split over several CTAs; each writes
@@ -40,8 +53,7 @@
 namespace moeslot {
 
 struct TcMaps {
-  CUtensorMap w13;   // [R records][2I rows][H]  bf16, box 64 x 128 x 1
-  CUtensorMap w2;    // [R records][H rows][I]   bf16, box 64 x 128 x 1
+  int dummy;         // weights need no tensor map (tiled records, bulk copies)
 };
 
 namespace tc {
@@ -51,7 +63,9 @@ constexpr int BK = 64;           // K elements per stage (one 128-byte swizzle r
 constexpr int kThreads = 192;
 constexpr int kMaxStages = 8;
 constexpr int kSmemBudget = 200 * 1024;
-constexpr int kModeGateUp = 0, kModeDown = 1;
+constexpr int kModeGateUp = 0, kModeDown = 1, kModeGateUpGather = 2, kModeDownGather = 3;
+constexpr int kGatherBN = 128;   // tokens per tile in the gather modes
+constexpr uint32_t kTileBytes = BM * BK * 2;   // one 128 x 64 bf16 tile
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -95,6 +109,23 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
       "[%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// Contiguous global -> shared copy by the bulk-copy engine, completing on `bar`.
+// Expert weights are read once per layer step, so they are marked evict-first
+// in L2: the stream then does not push out the small state every layer
+// re-reads (tables, history, activations, the code of the other kernels).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(l2_evict_first_policy())
       : "memory");
 }
 
@@ -153,62 +184,113 @@ __device__ __forceinline__ uint32_t idesc_bf16(int n) {
 struct Args {
   const WorkEntry* work;
   const int32_t* n_work;
+  const int32_t* sel;        // gate_up dense: the entries to process (indices into work), or null for all
+  const int32_t* sel_count;
+  const int32_t* ntile0;     // gather modes: first 128-token tile of each entry ([E+2], prefix)
+  const uint8_t* records;    // record array base
+  size_t rec, off13, off2;   // record bytes, w13 / w2 tile offsets
   int T, N, H, I, num_sms, stages;
-  const float* wmat;   // [E+1][N]
-  uint16_t* hbuf;      // [E+1][N][I]
-  uint16_t* out;       // [T][H]
+  int max_split_units;       // capacity of `partial` in (tile, split) units of this call's size
+  const float* wmat;         // dense: [E+1][N] routing weight per (entry, token)
+  const float* perm_w;       // gather: routing weight of each expert-sorted row
+  uint16_t* hbuf;            // dense: [E+1][N][I]; gather: h rows [rows][I]
+  uint16_t* out;             // dense down: [T][H]; gather down: Y rows [rows][H]
   float* partial;
   int32_t* counters;
   int32_t* status;
 };
 
+__host__ __device__ constexpr bool is_gate_up(int mode) { return mode == kModeGateUp || mode == kModeGateUpGather; }
+__host__ __device__ constexpr bool is_gather(int mode) { return mode >= kModeGateUpGather; }
+
 struct Plan {             // the unit decomposition, identical in every role
-  int tiles, splits, units, kblocks, mt_per_entry, n_work;
+  int tiles, splits, units, kblocks, mt_per_entry, n_work, n_sel, n_ntiles;
 };
 
+// Split count that keeps the most SMs busy: units = tiles * s spread over
+// the grid, utilisation (units / grid) / ceil(units / grid); ties to fewer splits.
+__device__ __forceinline__ int best_splits(int tiles, int smax, int grid, int cap) {
+  if (tiles <= 0) return 1;
+  int best = 1;
+  float best_eff = 0.f;
+  for (int sp = 1; sp <= smax; ++sp) {
+    const int units = tiles * sp;
+    if (sp > 1 && units > cap) break;          // the partial buffer holds at most `cap` units
+    const int rounds = (units + grid - 1) / grid;
+    const float eff = (float)units / (float)(rounds * grid);
+    if (eff > best_eff + 1e-6f) { best_eff = eff; best = sp; }
+  }
+  return best;
+}
+
 template <int MODE>
-__device__ __forceinline__ Plan make_plan(const Args& a) {
+__device__ __forceinline__ Plan make_plan(const Args& a, int grid) {
   Plan p;
   p.n_work = *a.n_work;
+  p.n_ntiles = 0;
   if (MODE == kModeGateUp) {
+    p.n_sel = a.sel ? *a.sel_count : p.n_work;
     p.mt_per_entry = (a.I + BM - 1) / BM;
-    p.tiles = p.n_work * p.mt_per_entry;
+    p.tiles = p.n_sel * p.mt_per_entry;
     p.kblocks = (a.H + BK - 1) / BK;
-    int sp = p.tiles > 0 ? (a.num_sms + p.tiles - 1) / p.tiles : 1;
-    sp = min(sp, min(p.kblocks, 8));
-    p.splits = max(sp, 1);
-  } else {
+    p.splits = best_splits(p.tiles, min(p.kblocks, 8), grid, a.max_split_units);
+  } else if (MODE == kModeDown) {
+    p.n_sel = p.n_work;
     p.mt_per_entry = (a.H + BM - 1) / BM;
     p.tiles = p.n_work > 0 ? p.mt_per_entry : 0;
     p.kblocks = (a.I + BK - 1) / BK;
-    int sp = p.tiles > 0 ? (a.num_sms + p.tiles - 1) / p.tiles : 1;
-    sp = min(sp, min(p.n_work, 16));
-    p.splits = max(sp, 1);
+    p.splits = best_splits(p.tiles, min(max(p.n_work, 1), 16), grid, a.max_split_units);
+  } else {
+    p.n_sel = p.n_work;
+    p.n_ntiles = a.ntile0[p.n_work];
+    p.mt_per_entry = MODE == kModeGateUpGather ? (a.I + BM - 1) / BM : (a.H + BM - 1) / BM;
+    p.kblocks = MODE == kModeGateUpGather ? (a.H + BK - 1) / BK : (a.I + BK - 1) / BK;
+    p.tiles = p.n_ntiles * p.mt_per_entry;
+    p.splits = 1;
   }
   p.units = p.tiles * p.splits;
   return p;
 }
 
-// Iterations of one unit: (entry, k-block) pairs in order.
+// One unit: rows mt of entry range [u0, u1), K blocks [kb0, kb1), token tile nt (gather).
 struct UnitRange {
-  int tile, split, mt, u0, u1, kb0, kb1;
+  int tile, split, mt, u0, u1, kb0, kb1, nt;
 };
 
 template <int MODE>
-__device__ __forceinline__ UnitRange unit_range(const Plan& p, int unit) {
+__device__ __forceinline__ UnitRange unit_range(const Plan& p, const Args& a, int unit) {
   UnitRange r;
   r.tile = unit / p.splits;
   r.split = unit % p.splits;
+  r.nt = 0;
   if (MODE == kModeGateUp) {
-    r.u0 = r.tile / p.mt_per_entry;
+    const int si = r.tile / p.mt_per_entry;
+    r.u0 = a.sel ? a.sel[si] : si;
     r.u1 = r.u0 + 1;
     r.mt = r.tile % p.mt_per_entry;
     r.kb0 = r.split * p.kblocks / p.splits;
     r.kb1 = (r.split + 1) * p.kblocks / p.splits;
-  } else {
+  } else if (MODE == kModeDown) {
     r.mt = r.tile;
     r.u0 = r.split * p.n_work / p.splits;
     r.u1 = (r.split + 1) * p.n_work / p.splits;
+    r.kb0 = 0;
+    r.kb1 = p.kblocks;
+  } else {
+    // unit = ntile0[u] * MT + mt * nts(u) + nt: entries' units are consecutive
+    const int MT = p.mt_per_entry;
+    int lo = 0, hi = p.n_work - 1;
+    while (lo < hi) {                      // last u with ntile0[u] * MT <= unit
+      const int mid = (lo + hi + 1) >> 1;
+      if (a.ntile0[mid] * MT <= unit) lo = mid;
+      else hi = mid - 1;
+    }
+    const int nts = a.ntile0[lo + 1] - a.ntile0[lo];
+    const int local = unit - a.ntile0[lo] * MT;
+    r.u0 = lo;
+    r.u1 = lo + 1;
+    r.mt = local / nts;
+    r.nt = local % nts;
     r.kb0 = 0;
     r.kb1 = p.kblocks;
   }
@@ -217,13 +299,50 @@ __device__ __forceinline__ UnitRange unit_range(const Plan& p, int unit) {
 
 __device__ __forceinline__ float silu(float v) { return v / (1.f + expf(-v)); }
 
+// Epilogue store of one 16-column chunk.  Gate/up: d0 = W_gate x, d1 = W_up x;
+// down: d0 = D.  Column j is token c0+j (dense) or row row_base+c0+j (gather).
+template <int MODE>
+__device__ __forceinline__ void store_chunk(const Args& a, const UnitRange& r, int m, int c0, const float* d0,
+                                            const float* d1, int row_base, int row_end) {
+  const int N = a.N;
+  if (MODE == kModeGateUp) {
+    if (m >= a.I) return;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int t = c0 + j;
+      const float wgt = t < a.T ? a.wmat[(size_t)r.u0 * N + t] : 0.f;
+      const float hv = wgt != 0.f ? wgt * silu(d0[j]) * d1[j] : 0.f;
+      a.hbuf[((size_t)r.u0 * N + t) * a.I + m] = f32_to_bf16_rn(hv);
+    }
+  } else if (MODE == kModeDown) {
+    if (m >= a.H) return;
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (c0 + j < a.T) a.out[(size_t)(c0 + j) * a.H + m] = f32_to_bf16_rn(d0[j]);
+  } else if (MODE == kModeGateUpGather) {
+    if (m >= a.I) return;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int row = row_base + c0 + j;
+      if (row < row_end) a.hbuf[(size_t)row * a.I + m] = f32_to_bf16_rn(a.perm_w[row] * silu(d0[j]) * d1[j]);
+    }
+  } else {
+    if (m >= a.H) return;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int row = row_base + c0 + j;
+      if (row < row_end) a.out[(size_t)row * a.H + m] = f32_to_bf16_rn(d0[j]);
+    }
+  }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
-tc_expert_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b, Args a) {
-  constexpr int NACC = MODE == kModeGateUp ? 2 : 1;
+tc_expert_kernel(const __grid_constant__ CUtensorMap map_b, Args a) {
+  constexpr int NACC = is_gate_up(MODE) ? 2 : 1;
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
-  __shared__ __align__(8) uint64_t tfull_bar, tempty_bar, drain_bar;
+  __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_sh, last_sh;
   extern __shared__ uint8_t smem_raw[];
@@ -232,19 +351,24 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = a.N;
   const int S = a.stages;
-  const uint32_t a_bytes = BM * BK * 2;                       // 16 KB per A tile
+  const uint32_t a_bytes = NACC * kTileBytes;                 // 16 KB (down) or 32 KB (gate + up)
   const uint32_t b_bytes = (uint32_t)N * BK * 2;              // N rows of 128 B
-  const uint32_t stage_bytes = ((NACC * a_bytes + b_bytes) + 1023) & ~1023u;
+  const uint32_t stage_bytes = (a_bytes + b_bytes + 1023) & ~1023u;
+  // two accumulator buffers when they fit, so one unit's epilogue overlaps the next unit's MMAs
+  const int nbuf = 2 * NACC * N <= 512 ? 2 : 1;
+  const uint32_t acc_cols = (uint32_t)(NACC * N);
   uint32_t ncols = 32;
-  while (ncols < (uint32_t)(NACC * N)) ncols <<= 1;
+  while (ncols < (uint32_t)nbuf * acc_cols) ncols <<= 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    mbar_init(&tfull_bar, 1);
-    mbar_init(&tempty_bar, 4);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull_bar[b], 1);
+      mbar_init(&tempty_bar[b], 4);
+    }
     mbar_init(&drain_bar, 1);
     abort_sh = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -255,33 +379,32 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
   fence_after();
   const uint32_t tmem = tmem_base_sh;
 
-  const Plan pl = make_plan<MODE>(a);
+  const Plan pl = make_plan<MODE>(a, gridDim.x);
   const uint32_t idesc = idesc_bf16(N);
+  const int kb_per_row = is_gate_up(MODE) ? (a.H + BK - 1) / BK : (a.I + BK - 1) / BK;
 
   if (warp == 0) {
-    // ------------------------------------------------------------- TMA producer
+    // ------------------------------------------------------------- producer
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
       for (int unit = blockIdx.x; unit < pl.units && ok; unit += gridDim.x) {
-        const UnitRange r = unit_range<MODE>(pl, unit);
+        const UnitRange r = unit_range<MODE>(pl, a, unit);
         for (int u = r.u0; u < r.u1 && ok; ++u) {
-          const int rid = a.work[u].rid;
+          const WorkEntry we = a.work[u];
+          const uint8_t* wbase = a.records + (size_t)we.rid * a.rec +
+                                 (is_gate_up(MODE) ? a.off13 : a.off2) +
+                                 (size_t)r.mt * kb_per_row * a_bytes;
+          const int brow = is_gather(MODE) ? we.row0 + r.nt * kGatherBN : 0;
           for (int kb = r.kb0; kb < r.kb1; ++kb, ++it) {
             const int s = it % S;
             if (it >= (uint32_t)S && !mbar_wait(&empty_bar[s], ((it / S) - 1) & 1)) { ok = false; break; }
             if (abort_sh) { ok = false; break; }
             uint8_t* st = smem + (size_t)s * stage_bytes;
-            mbar_expect_tx(&full_bar[s], NACC * a_bytes + b_bytes);
-            const int k0 = kb * BK;
-            if (MODE == kModeGateUp) {
-              tma_load_3d(st, &map_a, &full_bar[s], k0, r.mt * BM, rid);
-              tma_load_3d(st + a_bytes, &map_a, &full_bar[s], k0, a.I + r.mt * BM, rid);
-              tma_load_3d(st + 2 * a_bytes, &map_b, &full_bar[s], k0, 0, 0);
-            } else {
-              tma_load_3d(st, &map_a, &full_bar[s], k0, r.mt * BM, rid);
-              tma_load_3d(st + a_bytes, &map_b, &full_bar[s], k0, 0, u);
-            }
+            mbar_expect_tx(&full_bar[s], a_bytes + b_bytes);
+            bulk_load(st, wbase + (size_t)kb * a_bytes, a_bytes, &full_bar[s]);
+            const int bsel = MODE == kModeDown ? u : 0;
+            tma_load_3d(st + a_bytes, &map_b, &full_bar[s], kb * BK, brow, bsel);
           }
         }
       }
@@ -305,9 +428,11 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
       int local = 0;
       bool ok = true;
       for (int unit = blockIdx.x; unit < pl.units && ok; unit += gridDim.x, ++local) {
-        const UnitRange r = unit_range<MODE>(pl, unit);
-        if (local > 0 && !mbar_wait(&tempty_bar, (local - 1) & 1)) { ok = false; break; }
+        const UnitRange r = unit_range<MODE>(pl, a, unit);
+        const int buf = local % nbuf, use = local / nbuf;
+        if (use > 0 && !mbar_wait(&tempty_bar[buf], (use - 1) & 1)) { ok = false; break; }
         fence_after();
+        const uint32_t dacc = tmem + (uint32_t)buf * acc_cols;
         uint32_t acc = 0;
         for (int u = r.u0; u < r.u1 && ok; ++u) {
           for (int kb = r.kb0; kb < r.kb1; ++kb, ++it) {
@@ -316,18 +441,18 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
             fence_after();
             const uint32_t base = smem_u32(smem + (size_t)s * stage_bytes);
             const uint64_t da = desc_sw128(base);
-            const uint64_t db = desc_sw128(base + NACC * a_bytes);
+            const uint64_t db = desc_sw128(base + a_bytes);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
               // advance 16 bf16 = 32 bytes along K inside the swizzle atom
-              mma_bf16(tmem, da + 2 * kk, db + 2 * kk, idesc, acc);
-              if (MODE == kModeGateUp) mma_bf16(tmem + N, da + (a_bytes >> 4) + 2 * kk, db + 2 * kk, idesc, acc);
+              mma_bf16(dacc, da + 2 * kk, db + 2 * kk, idesc, acc);
+              if (NACC == 2) mma_bf16(dacc + N, da + (kTileBytes >> 4) + 2 * kk, db + 2 * kk, idesc, acc);
               acc = 1;
             }
             mma_commit(&empty_bar[s]);
           }
         }
-        if (ok) mma_commit(&tfull_bar);
+        if (ok) mma_commit(&tfull_bar[buf]);
       }
       if (!ok) {
         set_status(a.status, MOE_ERR_TIMEOUT);
@@ -339,46 +464,41 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
     }
   } else {
     // ------------------------------------------------------------- epilogue (warps 2..5)
-    const int q = warp & 3;                 // TMEM lane quarter this warp may access
-    const int row = q * 32 + lane;          // tile row == TMEM lane
-    const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
     // Every epilogue warp runs the same number of iterations and reaches every
     // named barrier even after a timeout, so no warp can be left waiting.
+    const int q = warp & 3;                 // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;          // tile row == TMEM lane
+    const uint32_t trow0 = tmem + ((uint32_t)(q * 32) << 16);
     int local = 0;
     for (int unit = blockIdx.x; unit < pl.units; unit += gridDim.x, ++local) {
-      const UnitRange r = unit_range<MODE>(pl, unit);
+      const UnitRange r = unit_range<MODE>(pl, a, unit);
+      const int buf = local % nbuf;
+      const uint32_t trow = trow0 + (uint32_t)buf * acc_cols;
       bool live = !abort_sh;
-      if (live && !mbar_wait(&tfull_bar, local & 1)) {
+      if (live && !mbar_wait(&tfull_bar[buf], (local / nbuf) & 1)) {
         set_status(a.status, MOE_ERR_TIMEOUT);
         abort_sh = 1;
         live = false;
       }
       if (live) fence_after();
-      const int m = r.mt * BM + row;                           // output row (i for gate_up, h for down)
-      const int mlimit = MODE == kModeGateUp ? a.I : a.H;
+      const int m = r.mt * BM + row;                           // output row (i for gate/up, h for down)
+      int row_base = 0, row_end = 0;
+      if (is_gather(MODE)) {
+        const WorkEntry we = a.work[r.u0];
+        row_base = we.row0 + r.nt * kGatherBN;
+        row_end = we.row0 + we.n;
+      }
       if (pl.splits == 1) {
         if (!live) continue;
         for (int c0 = 0; c0 < N; c0 += 16) {
           float d0[16], d1[16];
           tmem_ld16(trow + c0, d0);
-          if (MODE == kModeGateUp) tmem_ld16(trow + N + c0, d1);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int t = c0 + j;
-            if (m < mlimit) {
-              if (MODE == kModeGateUp) {
-                const float wgt = t < a.T ? a.wmat[(size_t)r.u0 * N + t] : 0.f;
-                const float hv = wgt != 0.f ? wgt * silu(d0[j]) * d1[j] : 0.f;
-                a.hbuf[((size_t)r.u0 * N + t) * a.I + m] = f32_to_bf16_rn(hv);
-              } else if (t < a.T) {
-                a.out[(size_t)t * a.H + m] = f32_to_bf16_rn(d0[j]);
-              }
-            }
-          }
+          if (NACC == 2) tmem_ld16(trow + N + c0, d1);
+          store_chunk<MODE>(a, r, m, c0, d0, d1, row_base, row_end);
         }
         fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty_bar);
+        if (lane == 0) mbar_arrive(&tempty_bar[buf]);
       } else {
         if (live) {
           // this split's partial tile, [acc][column][row] fp32
@@ -386,16 +506,16 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
           for (int c0 = 0; c0 < N; c0 += 16) {
             float d0[16], d1[16];
             tmem_ld16(trow + c0, d0);
-            if (MODE == kModeGateUp) tmem_ld16(trow + N + c0, d1);
+            if (NACC == 2) tmem_ld16(trow + N + c0, d1);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               mine[(size_t)(c0 + j) * BM + row] = d0[j];
-              if (MODE == kModeGateUp) mine[(size_t)N * BM + (size_t)(c0 + j) * BM + row] = d1[j];
+              if (NACC == 2) mine[(size_t)N * BM + (size_t)(c0 + j) * BM + row] = d1[j];
             }
           }
           fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&tempty_bar);
+          if (lane == 0) mbar_arrive(&tempty_bar[buf]);
           __threadfence();
         }
         asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -413,22 +533,28 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
         if (last_sh && live) {
           __threadfence();
           const float* base = a.partial + (size_t)r.tile * pl.splits * NACC * N * BM;
-          for (int t = 0; t < N; ++t) {
-            float s0 = 0.f, s1 = 0.f;
-            for (int sp = 0; sp < pl.splits; ++sp) {       // fixed order: deterministic
-              const float* pt = base + (size_t)sp * NACC * N * BM;
-              s0 += __ldcg(pt + (size_t)t * BM + row);
-              if (MODE == kModeGateUp) s1 += __ldcg(pt + (size_t)N * BM + (size_t)t * BM + row);
-            }
-            if (m < mlimit) {
-              if (MODE == kModeGateUp) {
-                const float wgt = t < a.T ? a.wmat[(size_t)r.u0 * N + t] : 0.f;
-                const float hv = wgt != 0.f ? wgt * silu(s0) * s1 : 0.f;
-                a.hbuf[((size_t)r.u0 * N + t) * a.I + m] = f32_to_bf16_rn(hv);
-              } else if (t < a.T) {
-                a.out[(size_t)t * a.H + m] = f32_to_bf16_rn(s0);
+          for (int c0 = 0; c0 < N; c0 += 16) {
+            // 16 columns at a time: each split's 16 (x2) values are loaded together,
+            // then added in split order (deterministic)
+            float s0[16], s1[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) { s0[j] = 0.f; s1[j] = 0.f; }
+            for (int sp = 0; sp < pl.splits; ++sp) {
+              const float* pt = base + (size_t)sp * NACC * N * BM + (size_t)c0 * BM + row;
+              float v0[16], v1[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v0[j] = __ldcg(pt + (size_t)j * BM);
+              if (NACC == 2) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v1[j] = __ldcg(pt + (size_t)N * BM + (size_t)j * BM);
+              }
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                s0[j] += v0[j];
+                if (NACC == 2) s1[j] += v1[j];
               }
             }
+            store_chunk<MODE>(a, r, m, c0, s0, s1, row_base, row_end);
           }
         }
         asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -439,6 +565,414 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
   __syncthreads();
   fence_after();
   if (warp == 1) tmem_dealloc(tmem, ncols);
+}
+
+// ----------------------------------------------------------------- fused decode FFN
+// One persistent kernel per layer for the dense token path (cooperative launch:
+// every CTA is resident, so CTAs may wait on each other with bounded spins):
+//   phase 0: gate/up of the entries already resident, while four copy warps
+//            per CTA pull this step's misses from the mapped host pool
+//            (NVLink-C2C reads) into their records;
+//   phase 1: gate/up of the entries copied this step — after grid barrier A
+//            (every CTA's copy warps done);
+//   phase 2: down + combine over all entries — after grid barrier B (every
+//            CTA's gate/up epilogue done, so h is complete).
+// The grid barriers are flip-bit counters: each CTA adds 1 (CTA 0 adds
+// 2^31 - (G-1)), so the high bit flips exactly when all G CTAs have arrived and
+// the low bits return to their old value, ready for the next launch.
+constexpr int kCopyWarps = 4;
+constexpr int kFusedThreads = kThreads + 32 * kCopyWarps;
+
+struct FusedArgs {
+  const CopyJob* jobs;
+  const int32_t* n_jobs;
+  uint32_t rec16;
+  unsigned long long magic;     // ceil(2^64 / rec16): job index = high word of idx * magic
+  uint32_t* grid_bar;           // [2]: A copies done, B gate/up done
+  const int32_t* sel[2];        // phase 0 / 1 entry lists
+  const int32_t* sel_count[2];
+  float* partial[3];            // per-phase split partial regions
+  int32_t* counters[3];
+  int max_split_units[3];
+};
+
+// Release this CTA's prior writes (of the calling thread, after a CTA-level
+// barrier) and arrive.
+__device__ __forceinline__ void grid_arrive(uint32_t* bar) {
+  const uint32_t inc = blockIdx.x == 0 ? 0x80000000u - (gridDim.x - 1u) : 1u;
+  asm volatile("fence.acq_rel.gpu;\n red.release.gpu.global.add.u32 [%0], %1;" ::"l"(bar), "r"(inc) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Wait until the barrier's high bit differs from its value at kernel start (~1 s bound).
+__device__ __noinline__ bool grid_wait(uint32_t* bar, uint32_t start_bit) {
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 0;; ++it) {
+    if ((ld_acquire(bar) & 0x80000000u) != start_bit) return true;
+    if ((it & 63u) == 63u && global_ns() - t0 > 1000000000ull) return false;
+    __nanosleep(32);
+  }
+}
+
+template <int MODE>
+__device__ __forceinline__ Plan phase_plan(Args a, const FusedArgs& f, int phase, int grid) {
+  if (phase < 2) {
+    a.sel = f.sel[phase];
+    a.sel_count = f.sel_count[phase];
+  }
+  a.max_split_units = f.max_split_units[phase];
+  return make_plan<MODE>(a, grid);
+}
+
+__global__ void __launch_bounds__(kFusedThreads, 1)
+tc_fused_decode_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_h, Args a,
+                       FusedArgs f) {
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
+  __shared__ uint32_t tmem_base_sh, start_bit_sh[2];
+  __shared__ volatile int abort_sh, last_sh;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = a.N;
+  const int S = a.stages;
+  const uint32_t b_bytes = (uint32_t)N * BK * 2;
+  const uint32_t stage_bytes = (2 * kTileBytes + b_bytes + 1023) & ~1023u;   // sized for gate/up
+  const int nbuf = 4 * N <= 512 ? 2 : 1;
+  const uint32_t acc_cols = (uint32_t)(2 * N);
+  uint32_t ncols = 32;
+  while (ncols < (uint32_t)nbuf * acc_cols) ncols <<= 1;
+
+  if (threadIdx.x == 0) {
+    // the barriers cannot have flipped yet: this CTA has not arrived
+    start_bit_sh[0] = *reinterpret_cast<volatile uint32_t*>(&f.grid_bar[0]) & 0x80000000u;
+    start_bit_sh[1] = *reinterpret_cast<volatile uint32_t*>(&f.grid_bar[1]) & 0x80000000u;
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull_bar[b], 1);
+      mbar_init(&tempty_bar[b], 4);
+    }
+    mbar_init(&drain_bar, 1);
+    abort_sh = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(&tmem_base_sh, ncols);
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const uint32_t idesc = idesc_bf16(N);
+  const int kb_h = (a.H + BK - 1) / BK, kb_i = (a.I + BK - 1) / BK;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      // phase-2 stages whose weight tile is in flight but whose h tile waits for barrier B
+      int pend_s[kMaxStages], pend_kb[kMaxStages], pend_u[kMaxStages];
+      int npend = 0;
+      bool h_ready = false;
+      auto resolve_h = [&]() -> bool {
+        if (!grid_wait(&f.grid_bar[1], start_bit_sh[1])) return false;
+        asm volatile("fence.proxy.async.global;" ::: "memory");   // generic writes -> async-proxy reads
+        for (int q = 0; q < npend; ++q)
+          tma_load_3d(smem + (size_t)pend_s[q] * stage_bytes + kTileBytes, &map_h, &full_bar[pend_s[q]],
+                      pend_kb[q] * BK, 0, pend_u[q]);
+        npend = 0;
+        h_ready = true;
+        return true;
+      };
+      for (int ph = 0; ph < 3 && ok; ++ph) {
+        const bool gu = ph < 2;
+        if (ph == 1) {
+          if (!grid_wait(&f.grid_bar[0], start_bit_sh[0])) { ok = false; break; }
+          asm volatile("fence.proxy.async.global;" ::: "memory");   // copied records -> bulk-copy reads
+        }
+        const Plan pl = gu ? phase_plan<kModeGateUp>(a, f, ph, gridDim.x) : phase_plan<kModeDown>(a, f, ph, gridDim.x);
+        Args aa = a;
+        if (gu) { aa.sel = f.sel[ph]; aa.sel_count = f.sel_count[ph]; }
+        const uint32_t a_bytes = gu ? 2 * kTileBytes : kTileBytes;
+        for (int unit = blockIdx.x; unit < pl.units && ok; unit += gridDim.x) {
+          const UnitRange r = gu ? unit_range<kModeGateUp>(pl, aa, unit) : unit_range<kModeDown>(pl, aa, unit);
+          for (int u = r.u0; u < r.u1 && ok; ++u) {
+            const WorkEntry we = a.work[u];
+            const uint8_t* wbase = a.records + (size_t)we.rid * a.rec + (gu ? a.off13 : a.off2) +
+                                   (size_t)r.mt * (gu ? kb_h : kb_i) * a_bytes;
+            for (int kb = r.kb0; kb < r.kb1; ++kb, ++it) {
+              const int s = it % S;
+              // a ring full of stages waiting for h can only drain once h is complete
+              if (!gu && !h_ready && npend == S && !resolve_h()) { ok = false; break; }
+              if (it >= (uint32_t)S && !mbar_wait(&empty_bar[s], ((it / S) - 1) & 1)) { ok = false; break; }
+              if (abort_sh) { ok = false; break; }
+              uint8_t* st = smem + (size_t)s * stage_bytes;
+              mbar_expect_tx(&full_bar[s], a_bytes + b_bytes);
+              bulk_load(st, wbase + (size_t)kb * a_bytes, a_bytes, &full_bar[s]);
+              if (gu) {
+                tma_load_3d(st + a_bytes, &map_x, &full_bar[s], kb * BK, 0, 0);
+              } else if (h_ready) {
+                tma_load_3d(st + a_bytes, &map_h, &full_bar[s], kb * BK, 0, u);
+              } else {
+                pend_s[npend] = s;
+                pend_kb[npend] = kb;
+                pend_u[npend] = u;
+                ++npend;
+              }
+            }
+          }
+        }
+      }
+      if (ok && !h_ready && !resolve_h()) ok = false;   // every CTA waits for barrier B once
+      if (!ok) {
+        set_status(a.status, MOE_ERR_TIMEOUT);
+        abort_sh = 1;
+      }
+      const uint32_t issued = it;
+      for (int s = 0; s < S; ++s) {
+        if ((uint32_t)s < issued) {
+          const uint32_t last = issued - 1 - ((issued - 1 - s) % S);
+          mbar_wait(&full_bar[s], (last / S) & 1);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0;
+      int local = 0;
+      bool ok = true;
+      for (int ph = 0; ph < 3 && ok; ++ph) {
+        const bool gu = ph < 2;
+        const Plan pl = gu ? phase_plan<kModeGateUp>(a, f, ph, gridDim.x) : phase_plan<kModeDown>(a, f, ph, gridDim.x);
+        Args aa = a;
+        if (gu) { aa.sel = f.sel[ph]; aa.sel_count = f.sel_count[ph]; }
+        const uint32_t a_bytes = gu ? 2 * kTileBytes : kTileBytes;
+        for (int unit = blockIdx.x; unit < pl.units && ok; unit += gridDim.x, ++local) {
+          const UnitRange r = gu ? unit_range<kModeGateUp>(pl, aa, unit) : unit_range<kModeDown>(pl, aa, unit);
+          const int buf = local % nbuf, use = local / nbuf;
+          if (use > 0 && !mbar_wait(&tempty_bar[buf], (use - 1) & 1)) { ok = false; break; }
+          fence_after();
+          const uint32_t dacc = tmem + (uint32_t)buf * acc_cols;
+          uint32_t acc = 0;
+          for (int u = r.u0; u < r.u1 && ok; ++u) {
+            for (int kb = r.kb0; kb < r.kb1; ++kb, ++it) {
+              const int s = it % S;
+              if (!mbar_wait(&full_bar[s], (it / S) & 1) || abort_sh) { ok = false; break; }
+              fence_after();
+              const uint32_t base = smem_u32(smem + (size_t)s * stage_bytes);
+              const uint64_t da = desc_sw128(base);
+              const uint64_t db = desc_sw128(base + a_bytes);
+#pragma unroll
+              for (int kk = 0; kk < BK / 16; ++kk) {
+                mma_bf16(dacc, da + 2 * kk, db + 2 * kk, idesc, acc);
+                if (gu) mma_bf16(dacc + N, da + (kTileBytes >> 4) + 2 * kk, db + 2 * kk, idesc, acc);
+                acc = 1;
+              }
+              mma_commit(&empty_bar[s]);
+            }
+          }
+          if (ok) mma_commit(&tfull_bar[buf]);
+        }
+      }
+      if (!ok) {
+        set_status(a.status, MOE_ERR_TIMEOUT);
+        abort_sh = 1;
+      }
+      mma_commit(&drain_bar);
+      mbar_wait(&drain_bar, 0);
+    }
+  } else if (warp < kThreads / 32) {
+    // ------------------------------------------------------------- epilogue (warps 2..5)
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const uint32_t trow0 = tmem + ((uint32_t)(q * 32) << 16);
+    int local = 0;
+    for (int ph = 0; ph < 3; ++ph) {
+      const bool gu = ph < 2;
+      if (ph == 2) {
+        // every gate/up epilogue of this CTA is done: tell the grid (barrier B)
+        __threadfence();
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (warp == 2 && lane == 0) grid_arrive(&f.grid_bar[1]);
+      }
+      const Plan pl = gu ? phase_plan<kModeGateUp>(a, f, ph, gridDim.x) : phase_plan<kModeDown>(a, f, ph, gridDim.x);
+      Args aa = a;
+      if (gu) { aa.sel = f.sel[ph]; aa.sel_count = f.sel_count[ph]; }
+      for (int unit = blockIdx.x; unit < pl.units; unit += gridDim.x, ++local) {
+        const UnitRange r = gu ? unit_range<kModeGateUp>(pl, aa, unit) : unit_range<kModeDown>(pl, aa, unit);
+        const int buf = local % nbuf;
+        const uint32_t trow = trow0 + (uint32_t)buf * acc_cols;
+        bool live = !abort_sh;
+        if (live && !mbar_wait(&tfull_bar[buf], (local / nbuf) & 1)) {
+          set_status(a.status, MOE_ERR_TIMEOUT);
+          abort_sh = 1;
+          live = false;
+        }
+        if (live) fence_after();
+        const int m = r.mt * BM + row;
+        if (pl.splits == 1) {
+          if (!live) continue;
+          for (int c0 = 0; c0 < N; c0 += 16) {
+            float d0[16], d1[16];
+            tmem_ld16(trow + c0, d0);
+            if (gu) {
+              tmem_ld16(trow + N + c0, d1);
+              store_chunk<kModeGateUp>(a, r, m, c0, d0, d1, 0, 0);
+            } else {
+              store_chunk<kModeDown>(a, r, m, c0, d0, d1, 0, 0);
+            }
+          }
+          fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+        } else {
+          const int nacc = gu ? 2 : 1;
+          float* part = f.partial[ph];
+          if (live) {
+            float* mine = part + ((size_t)r.tile * pl.splits + r.split) * nacc * N * BM;
+            for (int c0 = 0; c0 < N; c0 += 16) {
+              float d0[16], d1[16];
+              tmem_ld16(trow + c0, d0);
+              if (gu) tmem_ld16(trow + N + c0, d1);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                mine[(size_t)(c0 + j) * BM + row] = d0[j];
+                if (gu) mine[(size_t)N * BM + (size_t)(c0 + j) * BM + row] = d1[j];
+              }
+            }
+            fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+            __threadfence();
+          }
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+          if (warp == 2 && lane == 0) {
+            last_sh = 0;
+            if (!abort_sh) {
+              const int old = atomicAdd(&f.counters[ph][r.tile], 1);
+              if (old == pl.splits - 1) {
+                last_sh = 1;
+                f.counters[ph][r.tile] = 0;
+              }
+            }
+          }
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+          if (last_sh && live) {
+            __threadfence();
+            const float* base = part + (size_t)r.tile * pl.splits * nacc * N * BM;
+            for (int c0 = 0; c0 < N; c0 += 16) {
+              float s0[16], s1[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) { s0[j] = 0.f; s1[j] = 0.f; }
+              for (int sp = 0; sp < pl.splits; ++sp) {
+                const float* pt = base + (size_t)sp * nacc * N * BM + (size_t)c0 * BM + row;
+                float v0[16], v1[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v0[j] = __ldcg(pt + (size_t)j * BM);
+                if (gu) {
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) v1[j] = __ldcg(pt + (size_t)N * BM + (size_t)j * BM);
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  s0[j] += v0[j];
+                  if (gu) s1[j] += v1[j];
+                }
+              }
+              if (gu) store_chunk<kModeGateUp>(a, r, m, c0, s0, s1, 0, 0);
+              else store_chunk<kModeDown>(a, r, m, c0, s0, s1, 0, 0);
+            }
+          }
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------- copy warps (6..9)
+    const uint32_t n = (uint32_t)*f.n_jobs;
+    const uint32_t total = n * f.rec16;
+    const uint32_t stride = gridDim.x * (32u * kCopyWarps);
+    const uint32_t ctid = (uint32_t)(warp - kThreads / 32) * 32u + lane;
+    constexpr int CU = 16;   // loads in flight per copy thread
+    for (uint32_t base = blockIdx.x * (32u * kCopyWarps) + ctid; base < total; base += stride * CU) {
+      uint4 v[CU];
+      uint4* dst[CU];
+#pragma unroll
+      for (int u = 0; u < CU; ++u) {
+        const uint32_t idx = base + (uint32_t)u * stride;
+        dst[u] = nullptr;
+        if (idx < total) {
+          const uint32_t j = (uint32_t)__umul64hi((unsigned long long)idx, f.magic);
+          const uint32_t c = idx - j * f.rec16;
+          v[u] = __ldcs(reinterpret_cast<const uint4*>(f.jobs[j].src) + c);
+          dst[u] = reinterpret_cast<uint4*>(f.jobs[j].dst) + c;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < CU; ++u)
+        if (dst[u]) __stcs(dst[u], v[u]);
+    }
+    __threadfence();
+    asm volatile("bar.sync 2, %0;" ::"n"(32 * kCopyWarps) : "memory");
+    if (warp == kThreads / 32 && lane == 0) grid_arrive(&f.grid_bar[0]);
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  if (warp == 1) tmem_dealloc(tmem, ncols);
+}
+
+// ----------------------------------------------------------------- gather / combine (T > 256)
+// x rows in expert-sorted order: xp[r] = x[perm_tok[r]] (shared-expert rows included).
+__global__ void gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm_tok,
+                                   const int32_t* __restrict__ n_rows, uint16_t* __restrict__ xp, int H) {
+  const int rows = *n_rows;
+  const int vec = H / 8;   // uint4 per row
+  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)perm_tok[r] * H);
+    uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)r * H);
+    for (int c = threadIdx.x; c < vec; c += blockDim.x) dst[c] = src[c];
+  }
+}
+
+// out[t] = sum over the token's k rows in ascending expert id of Y[row] (+ its shared-expert row).
+__global__ void combine_rows_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ inv, int T, int k,
+                                    int shared, uint16_t* __restrict__ out, int H) {
+  const int t = blockIdx.x;
+  if (t >= T) return;
+  int rows[32];
+  for (int j = 0; j < k; ++j) rows[j] = inv[t * k + j];
+  for (int j = 1; j < k; ++j) {            // rows are grouped by ascending expert id
+    const int v = rows[j];
+    int q = j - 1;
+    while (q >= 0 && rows[q] > v) { rows[q + 1] = rows[q]; --q; }
+    rows[q + 1] = v;
+  }
+  for (int h2 = threadIdx.x; h2 < H / 2; h2 += blockDim.x) {
+    float s0 = 0.f, s1 = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const uint32_t v = reinterpret_cast<const uint32_t*>(y + (size_t)rows[j] * H)[h2];
+      s0 += bf16lo(v);
+      s1 += bf16hi(v);
+    }
+    if (shared) {
+      const uint32_t v = reinterpret_cast<const uint32_t*>(y + (size_t)(T * k + t) * H)[h2];
+      s0 += bf16lo(v);
+      s1 += bf16hi(v);
+    }
+    reinterpret_cast<uint32_t*>(out + (size_t)t * H)[h2] =
+        (uint32_t)f32_to_bf16_rn(s0) | ((uint32_t)f32_to_bf16_rn(s1) << 16);
+  }
 }
 
 // ----------------------------------------------------------------- host side
@@ -485,66 +1019,162 @@ int stages_for(int nacc, int N) {
   return s;
 }
 
+template <int MODE>
+int launch_mode(Args a, const CUtensorMap& mb, cudaStream_t s) {
+  constexpr int NACC = is_gate_up(MODE) ? 2 : 1;
+  a.stages = stages_for(NACC, a.N);
+  configure_once<MODE>();
+  const size_t smem = (size_t)a.stages * (((NACC * BM * BK * 2 + a.N * BK * 2) + 1023) & ~1023) + 1024;
+  tc_expert_kernel<MODE><<<sm_count(), kThreads, smem, s>>>(mb, a);
+  return 1;
+}
+
 }  // namespace tc
 
 TcMaps* tc_maps_create(const PoolDev& p, const Scratch& sc) {
+  (void)p;
   (void)sc;
-  TcMaps* m = new TcMaps();
-  const uint64_t H = p.H, I = p.I, R = p.n_records, rec = p.lay.rec;
-  bool ok = tc::make_map_3d(&m->w13, p.records + p.lay.off13, H, 2 * I, R, H * 2, rec, tc::BM) &&
-            tc::make_map_3d(&m->w2, p.records + p.lay.off2, I, H, R, I * 2, rec, tc::BM);
-  if (!ok) {
-    delete m;
-    return nullptr;
-  }
-  return m;
+  if (!tc::encode_fn()) return nullptr;
+  return new TcMaps();
 }
 
 void tc_maps_destroy(TcMaps* m) { delete m; }
 
 int tc_npad(int T) { return (T + 15) / 16 * 16; }
 
-static tc::Args tc_args(const PoolDev& p, const Scratch& sc, int T) {
+// Three equal regions (one per phase of the fused kernel); the unfused kernels use the first.
+size_t tc_partial_floats(const PoolDev& p, const Scratch& sc) {
+  (void)p;
+  return (size_t)3 * 4 * sm_count() * 2 * sc.npad_max * tc::BM;
+}
+
+static tc::Args tc_args(const PoolDev& p, const Scratch& sc, int T, int N) {
   tc::Args a;
   a.work = sc.work;
   a.n_work = sc.n_work;
+  a.sel = nullptr;
+  a.sel_count = nullptr;
+  a.ntile0 = sc.ntile0;
+  a.records = p.records;
+  a.rec = p.lay.rec;
+  a.off13 = p.lay.off13;
+  a.off2 = p.lay.off2;
   a.T = T;
-  a.N = tc_npad(T);
+  a.N = N;
   a.H = p.H;
   a.I = p.I;
   a.num_sms = sm_count();
+  a.stages = 1;
   a.wmat = sc.wmat;
+  a.perm_w = sc.perm_w;
   a.hbuf = sc.hbuf;
   a.out = nullptr;
   a.partial = sc.partial;
   a.counters = sc.counters;
   a.status = p.status;
+  a.max_split_units = (int)(tc_partial_floats(p, sc) / 3 / ((size_t)2 * N * tc::BM));
   return a;
 }
 
-int launch_tc_gate_up(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, const void* x, cudaStream_t s) {
-  tc::Args a = tc_args(p, sc, T);
-  a.stages = tc::stages_for(2, a.N);
-  CUtensorMap xm;   // x [T][H] as a 3-D map with one "record"
-  if (!tc::make_map_3d(&xm, x, (uint64_t)p.H, (uint64_t)T, 1, (uint64_t)p.H * 2, (uint64_t)p.H * 2 * T, a.N)) {
-    return -1;
+int launch_tc_gate_up(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, const void* x, int sel,
+                      cudaStream_t s) {
+  (void)m;
+  tc::Args a = tc_args(p, sc, T, tc_npad(T));
+  if (sel >= 0) {
+    a.sel = sc.elist + (size_t)sel * (p.E + 1);
+    a.sel_count = sc.ecount + sel;
   }
-  tc::configure_once<tc::kModeGateUp>();
-  const size_t smem = (size_t)a.stages * (((2 * tc::BM * tc::BK * 2 + a.N * tc::BK * 2) + 1023) & ~1023) + 1024;
-  tc::tc_expert_kernel<tc::kModeGateUp><<<sm_count(), tc::kThreads, smem, s>>>(m->w13, xm, a);
-  return 1;
+  CUtensorMap xm;   // x [T][H] as a 3-D map with one "record"
+  if (!tc::make_map_3d(&xm, x, (uint64_t)p.H, (uint64_t)T, 1, (uint64_t)p.H * 2, (uint64_t)p.H * 2 * T, a.N))
+    return -1;
+  return tc::launch_mode<tc::kModeGateUp>(a, xm, s);
 }
 
 int launch_tc_down(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, void* out, cudaStream_t s) {
-  tc::Args a = tc_args(p, sc, T);
+  (void)m;
+  tc::Args a = tc_args(p, sc, T, tc_npad(T));
   a.out = static_cast<uint16_t*>(out);
-  a.stages = tc::stages_for(1, a.N);
+  a.max_split_units = (int)(tc_partial_floats(p, sc) / 3 / ((size_t)1 * a.N * tc::BM));
   CUtensorMap hm;   // hbuf [E+1][N][I]
   const uint64_t I = p.I, N = a.N;
   if (!tc::make_map_3d(&hm, sc.hbuf, I, N, (uint64_t)p.E + 1, I * 2, N * I * 2, a.N)) return -1;
-  tc::configure_once<tc::kModeDown>();
-  const size_t smem = (size_t)a.stages * (((tc::BM * tc::BK * 2 + a.N * tc::BK * 2) + 1023) & ~1023) + 1024;
-  tc::tc_expert_kernel<tc::kModeDown><<<sm_count(), tc::kThreads, smem, s>>>(m->w2, hm, a);
+  return tc::launch_mode<tc::kModeDown>(a, hm, s);
+}
+
+// Gather path: xp = x rows by expert; h = gate/up per row; y = down per row; out = combine.
+int launch_tc_gather(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, const void* x, void* out,
+                     cudaStream_t s) {
+  (void)m;
+  const int rows_max = T * p.k + (p.shared ? T : 0);
+  tc::gather_rows_kernel<<<2 * sm_count(), 256, 0, s>>>(static_cast<const uint16_t*>(x), sc.perm_tok, sc.n_rows,
+                                                         sc.xp, p.H);
+  tc::Args a = tc_args(p, sc, T, tc::kGatherBN);
+  a.max_split_units = 0;
+  a.hbuf = static_cast<uint16_t*>(sc.h);
+  CUtensorMap xm;
+  if (!tc::make_map_3d(&xm, sc.xp, (uint64_t)p.H, (uint64_t)rows_max, 1, (uint64_t)p.H * 2,
+                       (uint64_t)p.H * 2 * rows_max, tc::kGatherBN))
+    return -1;
+  int n = 1 + tc::launch_mode<tc::kModeGateUpGather>(a, xm, s);
+  tc::Args b = a;
+  b.out = sc.y;
+  CUtensorMap hm;
+  if (!tc::make_map_3d(&hm, sc.h, (uint64_t)p.I, (uint64_t)rows_max, 1, (uint64_t)p.I * 2,
+                       (uint64_t)p.I * 2 * rows_max, tc::kGatherBN))
+    return -1;
+  n += tc::launch_mode<tc::kModeDownGather>(b, hm, s);
+  tc::combine_rows_kernel<<<T, 256, 0, s>>>(sc.y, sc.inv, T, p.k, p.shared, static_cast<uint16_t*>(out), p.H);
+  return n + 1;
+}
+
+
+// Fused dense decode FFN (miss copies + gate/up + down + combine), one cooperative launch.
+int launch_tc_fused_decode(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, const void* x, void* out,
+                           cudaStream_t s) {
+  (void)m;
+  const int N = tc_npad(T);
+  tc::Args a = tc_args(p, sc, T, N);
+  a.out = static_cast<uint16_t*>(out);
+  a.stages = tc::stages_for(2, N);
+  CUtensorMap xm, hm;
+  if (!tc::make_map_3d(&xm, x, (uint64_t)p.H, (uint64_t)T, 1, (uint64_t)p.H * 2, (uint64_t)p.H * 2 * T, N)) return -1;
+  const uint64_t I = p.I;
+  if (!tc::make_map_3d(&hm, sc.hbuf, I, (uint64_t)N, (uint64_t)p.E + 1, I * 2, (uint64_t)N * I * 2, N)) return -1;
+  tc::FusedArgs f;
+  f.jobs = sc.copies;
+  f.n_jobs = sc.n_copy;
+  f.rec16 = (uint32_t)(p.lay.rec / 16);
+  f.magic = ~0ull / f.rec16 + 1ull;
+  f.grid_bar = sc.grid_bar;
+  for (int ph = 0; ph < 2; ++ph) {
+    f.sel[ph] = sc.elist + (size_t)ph * (p.E + 1);
+    f.sel_count[ph] = sc.ecount + ph;
+  }
+  const size_t region = tc_partial_floats(p, sc) / 3;
+  const size_t ctiles = sc.n_counters / 3;
+  for (int ph = 0; ph < 3; ++ph) {
+    f.partial[ph] = sc.partial + region * ph;
+    f.counters[ph] = sc.counters + ctiles * ph;
+  }
+  for (int ph = 0; ph < 3; ++ph) f.max_split_units[ph] = (int)(region / ((size_t)(ph < 2 ? 2 : 1) * N * tc::BM));
+  static bool configured = false;
+  if (!configured) {
+    cudaFuncSetAttribute(tc::tc_fused_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         tc::kSmemBudget + 1024);
+    configured = true;
+  }
+  const size_t smem = (size_t)a.stages * (((2 * tc::BM * tc::BK * 2 + N * tc::BK * 2) + 1023) & ~1023) + 1024;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(sm_count());
+  cfg.blockDim = dim3(tc::kFusedThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, tc::tc_fused_decode_kernel, xm, hm, a, f) != cudaSuccess) return -2;
   return 1;
 }
 

@@ -36,7 +36,8 @@ enum PlanFlags {
   PLAN_HISTORY = 1,    // a3: update routing history and eviction scores
   PLAN_CACHE = 2,      // a4/a5: table rewrite, misses, victims, copy list
   PLAN_PERMUTE = 4,    // a7 + work list
-  PLAN_STAGED = 8      // work list points into a staging region (identity table)
+  PLAN_STAGED = 8,     // work list points into a staging region (identity table)
+  PLAN_GATHER = 16     // also write inv, ntile0, n_rows for the gather path
 };
 
 struct Layout {
@@ -71,6 +72,7 @@ struct PoolDev {           // device-side pointers handed to kernels by value
 };
 
 struct Scratch {
+  int32_t tmax;       // max_tokens of the pool
   float* logits;      // [Tmax, E]
   float* probs;       // [Tmax, E]
   int32_t* ids;       // [Tmax, k]
@@ -85,13 +87,24 @@ struct Scratch {
   int32_t* n_work;    // [1]
   CopyJob* copies;    // [E+1]
   int32_t* n_copy;    // [1]
+  int32_t* ticket;    // [1] last-CTA ticket of the fused routing kernel (self-resetting)
   void* h;            // [(Tmax*k + Tmax), I] act dtype
   // tensor-core decode path (dense token columns)
   int32_t npad_max;   // largest padded token count of that path (<= 256)
   float* wmat;        // [E+1][npad] routing weight of each token for each work entry (0 if not routed)
   uint16_t* hbuf;     // [E+1][npad][I] bf16: w * SiLU(g) * u
   float* partial;     // split-reduce partial tiles
-  int32_t* counters;  // per-tile arrival counters (self-resetting)
+  int32_t* counters;  // per-tile arrival counters (self-resetting), 3 regions
+  size_t n_counters;
+  uint32_t* grid_bar; // [2] flip-bit grid barriers of the fused decode kernel
+  int32_t* elist;     // [2][E+1]: work entries already resident / copied this step
+  int32_t* ecount;    // [2]
+  // tensor-core gather path (T > npad_max)
+  int32_t* inv;       // [Tmax*k]   expert-sorted row of each flat entry t*k+j
+  int32_t* ntile0;    // [E+2]      first 128-token tile of each work entry (prefix)
+  int32_t* n_rows;    // [1]        expert-sorted rows of this call (T*k [+ T shared])
+  uint16_t* xp;       // [(Tmax*k + Tmax), H] x rows in expert-sorted order
+  uint16_t* y;        // [(Tmax*k + Tmax), H] per-row expert outputs
 };
 
 // ----------------------------------------------------------------- device helpers
@@ -128,6 +141,10 @@ int launch_route_logits(const PoolDev& p, int layer, const void* x, int T, const
                         const float* router_b, float* logits, cudaStream_t s);
 int launch_gate_topk(const PoolDev& p, const float* logits, int T, int32_t* ids, float* w, float* probs,
                      float* gap, cudaStream_t s);
+// one launch for router + gate when T and H are small enough (decode)
+bool route_fused_ok(const PoolDev& p, int T);
+int launch_route_gate_fused(const PoolDev& p, int layer, const void* x, int T, const void* router_w,
+                            const float* router_b, const Scratch& sc, cudaStream_t s);
 int launch_plan(const PoolDev& p, const Scratch& sc, int layer, int T, const int32_t* ids, const float* w,
                 const float* probs, int flags, int region, int npad, cudaStream_t s);
 int launch_miss_copy(const PoolDev& p, const Scratch& sc, cudaStream_t s);
@@ -139,8 +156,15 @@ struct TcMaps;                      // host-side tensor maps of a pool (k_tc.cu)
 TcMaps* tc_maps_create(const PoolDev& p, const Scratch& sc);
 void tc_maps_destroy(TcMaps* m);
 int tc_npad(int T);                 // padded token count (multiple of 16)
-int launch_tc_gate_up(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, const void* x, cudaStream_t s);
+size_t tc_partial_floats(const PoolDev& p, const Scratch& sc);   // size of Scratch::partial
+// sel: 0 = resident entries, 1 = entries copied this step, -1 = all
+int launch_tc_gate_up(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, const void* x, int sel,
+                      cudaStream_t s);
 int launch_tc_down(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, void* out, cudaStream_t s);
+int launch_tc_gather(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, const void* x, void* out,
+                     cudaStream_t s);
+int launch_tc_fused_decode(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, const void* x, void* out,
+                           cudaStream_t s);
 int launch_load_slot(const PoolDev& p, const Scratch& sc, int layer, int expert, int slot, cudaStream_t s);
 int launch_rebuild_owner(const PoolDev& p, cudaStream_t s);
 

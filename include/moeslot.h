@@ -211,12 +211,12 @@ MOE_API moe_status moe_get_stats(moe_pool* pool, moe_stats* out);
  * a captured graph they become event nodes); moe_profile_read returns, for the
  * latest forward of `layer`, the elapsed milliseconds of each stage.  Enabling
  * creates L*(MOE_NUM_STAGES+1) events and is blocking. */
-enum { MOE_STAGE_ROUTE = 0,   /* router GEMV + gate/top-k                     */
-       MOE_STAGE_PLAN = 1,    /* history, table, victims, permutation         */
-       MOE_STAGE_COPY = 2,    /* device-started miss copies                   */
-       MOE_STAGE_GATE_UP = 3, /* expert gate/up projections + SiLU            */
-       MOE_STAGE_DOWN = 4,    /* expert down projection + weighted combine    */
-       MOE_NUM_STAGES = 5 };
+enum { MOE_STAGE_ROUTE = 0,     /* router GEMV + gate/top-k                        */
+       MOE_STAGE_PLAN = 1,      /* history, table, victims, permutation            */
+       MOE_STAGE_COPY = 2,      /* miss copies run as their own kernel (0 when the
+                                   expert kernel does them itself)                 */
+       MOE_STAGE_FFN = 3,       /* expert gate/up, down and weighted combine       */
+       MOE_NUM_STAGES = 4 };
 MOE_API moe_status moe_profile_enable(moe_pool* pool, int32_t on);
 MOE_API moe_status moe_profile_read(moe_pool* pool, int32_t layer, float* stage_ms /* [MOE_NUM_STAGES] */);
 

@@ -61,12 +61,21 @@ class Workload:
         return {F32: 4, BF16: 2}[self.act_dtype]
 
     def expert_layout(self):
-        """Byte offsets of one expert's record: w13 [2I,H], w2 [H,I], then fp8 block scales.
+        """Byte offsets of one expert's record.
 
-        Returns (w13_off, w2_off, s13_off, s2_off, record_bytes).  The record is
-        padded to a multiple of 4096 bytes so every slot starts page-aligned.
+        Returns (w13_off, w2_off, s13_off, s2_off, record_bytes).  fp32 and fp8
+        records hold w13 [2I,H] and w2 [H,I] row-major (fp8 followed by its block
+        scales).  bf16 records hold the same matrices cut into 128-row x 64-column
+        tiles (see synth.gen.tile_sw128): w13 as [I/128][H/64][gate, up] tiles and
+        w2 as [H/128][I/64] tiles, 16 KiB each.  Records are padded to 4096 bytes.
         """
         eb = self.weight_elt_bytes
+        if self.weight_dtype == BF16:
+            mt_i, kb_h = -(-self.I // 128), -(-self.H // 64)
+            mt_h, kb_i = -(-self.H // 128), -(-self.I // 64)
+            w13 = 2 * mt_i * kb_h * 16384
+            w2 = mt_h * kb_i * 16384
+            return 0, w13, w13 + w2, w13 + w2, (w13 + w2 + 4095) // 4096 * 4096
         w13 = 2 * self.I * self.H * eb
         w2 = self.H * self.I * eb
         s13 = s2 = 0

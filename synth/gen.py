@@ -102,10 +102,53 @@ def shared_expert_stored(wl: Workload, layer: int, base_seed: int = 0):
     return encode_expert(wl, w_gate, w_up, w_down)
 
 
+# --- the bf16 record format: 128 x 64 tiles in 128-byte-swizzled order -------
+# Element (r, c) of a tile (row r < 128, column c < 64) sits at byte
+# r*128 + ((c // 8) ^ (r % 8)) * 16 + (c % 8) * 2: each 128-byte row holds eight
+# 16-byte chunks whose order is XOR-permuted by the row index mod 8.  Matrix
+# rows/columns beyond the matrix are zero.
+
+def _swz_perm():
+    r = np.arange(128)[:, None]
+    p = np.arange(8)[None, :]
+    return p ^ (r % 8)                      # logical chunk held by physical chunk p of row r
+
+
+def tile_sw128(w: np.ndarray) -> np.ndarray:
+    """uint16 [R, C] -> uint16 [ceil(R/128), ceil(C/64), 128, 64] in swizzled tile order."""
+    R, C = w.shape
+    mt, kb = -(-R // 128), -(-C // 64)
+    pad = np.zeros((mt * 128, kb * 64), np.uint16)
+    pad[:R, :C] = w
+    t = pad.reshape(mt, 128, kb, 64).transpose(0, 2, 1, 3).reshape(mt, kb, 128, 8, 8)
+    idx = np.broadcast_to(_swz_perm()[None, None, :, :, None], t.shape)
+    return np.take_along_axis(t, idx, axis=3).reshape(mt, kb, 128, 64)
+
+
+def untile_sw128(tiles: np.ndarray, R: int, C: int) -> np.ndarray:
+    """Inverse of tile_sw128."""
+    mt, kb = tiles.shape[:2]
+    t = tiles.reshape(mt, kb, 128, 8, 8)
+    out = np.empty_like(t)
+    perm = _swz_perm()
+    for r in range(128):                    # physical chunk p holds logical chunk perm[r, p]
+        out[:, :, r, perm[r], :] = t[:, :, r, :, :]
+    return out.reshape(mt, kb, 128, 64).transpose(0, 2, 1, 3).reshape(mt * 128, kb * 64)[:R, :C]
+
+
 def expert_record_bytes(wl: Workload, stored) -> bytes:
     """Pack one stored expert into the host-pool record layout (padded)."""
     o13, o2, os13, os2, rec = wl.expert_layout()
     buf = np.zeros(rec, np.uint8)
+    if wl.weight_dtype == BF16:
+        I = wl.I
+        g = tile_sw128(stored["w13"][:I])
+        u = tile_sw128(stored["w13"][I:])
+        w13 = np.stack([g, u], axis=2)      # [I/128][H/64][gate, up][128][64]
+        w2 = tile_sw128(stored["w2"])       # [H/128][I/64][128][64]
+        buf[o13:o13 + w13.nbytes] = w13.view(np.uint8).ravel()
+        buf[o2:o2 + w2.nbytes] = w2.view(np.uint8).ravel()
+        return buf
     for key, off in (("w13", o13), ("w2", o2), ("s13", os13), ("s2", os2)):
         if key in stored:
             raw = np.ascontiguousarray(stored[key]).view(np.uint8).ravel()
@@ -196,6 +239,19 @@ def torch_quantize_fp8_blocks(w):
     return q.view(torch.uint8).reshape(n, R, C), scale.contiguous()
 
 
+def torch_tile_sw128(w):
+    """Device version of tile_sw128 for a batch [n, R, C] -> [n, R/128, C/64, 128, 64] (any 16-bit dtype)."""
+    import torch
+    n, R, C = w.shape
+    mt, kb = -(-R // 128), -(-C // 64)
+    pad = torch.zeros((n, mt * 128, kb * 64), dtype=w.dtype, device=w.device)
+    pad[:, :R, :C] = w
+    t = pad.view(n, mt, 128, kb, 64).permute(0, 1, 3, 2, 4).reshape(n, mt, kb, 128, 8, 8)
+    perm = torch.from_numpy(_swz_perm()).to(w.device)
+    idx = perm.view(1, 1, 1, 128, 8, 1).expand(n, mt, kb, 128, 8, 8)
+    return torch.gather(t, 4, idx).reshape(n, mt, kb, 128, 64).contiguous()
+
+
 def torch_encode_records(wl: Workload, w13, w2):
     """Stored records [n, record_bytes] uint8 on the device from fp32 w13/w2 chunks."""
     import torch
@@ -205,7 +261,10 @@ def torch_encode_records(wl: Workload, w13, w2):
     if wl.weight_dtype == F32:
         parts = [(o13, w13.contiguous()), (o2, w2.contiguous())]
     elif wl.weight_dtype == BF16:
-        parts = [(o13, w13.to(torch.bfloat16)), (o2, w2.to(torch.bfloat16))]
+        I = wl.I
+        g = torch_tile_sw128(w13[:, :I].to(torch.bfloat16))
+        u = torch_tile_sw128(w13[:, I:].to(torch.bfloat16))
+        parts = [(o13, torch.stack([g, u], dim=3)), (o2, torch_tile_sw128(w2.to(torch.bfloat16)))]
     else:
         c13, s13 = torch_quantize_fp8_blocks(w13)
         c2, s2 = torch_quantize_fp8_blocks(w2)
@@ -224,6 +283,14 @@ def record_to_stored(wl: Workload, rec: np.ndarray):
     """Parse one host-pool record (uint8) back into the stored dict (w13, w2[, s13, s2])."""
     o13, o2, os13, os2, _ = wl.expert_layout()
     H, I = wl.H, wl.I
+    if wl.weight_dtype == BF16:
+        mt_i, kb_h = -(-I // 128), -(-H // 64)
+        mt_h, kb_i = -(-H // 128), -(-I // 64)
+        w13 = rec[o13:o13 + 2 * mt_i * kb_h * 16384].view(np.uint16).reshape(mt_i, kb_h, 2, 128, 64)
+        w2 = rec[o2:o2 + mt_h * kb_i * 16384].view(np.uint16).reshape(mt_h, kb_i, 128, 64)
+        gate = untile_sw128(w13[:, :, 0], I, H)
+        up = untile_sw128(w13[:, :, 1], I, H)
+        return {"w13": np.concatenate([gate, up], axis=0).copy(), "w2": untile_sw128(w2, H, I).copy()}
     if wl.weight_dtype == F32:
         dt, eb = np.float32, 4
     elif wl.weight_dtype == BF16:

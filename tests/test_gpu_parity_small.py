@@ -168,3 +168,21 @@ def test_fp8_block_scaled_with_shared_expert():
         assert verdict != "diverged"
     finally:
         rig.close()
+
+
+@pytest.mark.parametrize("T", [17, 257, 600])
+def test_bf16_dense_and_gather_paths_with_shared_expert(T):
+    """T <= 256 takes the dense tensor-core path, larger T the expert-grouped (gather) path."""
+    wl = variant(get_workload("qwen3_decode"), name="gather_bf16", L=2, E=32, k=4, H=512, I=320,
+                 residency=0.5, shared=True, zipf_s=0.5)
+    rig = Rig(wl, max_tokens=640)
+    try:
+        for l in range(wl.L):
+            xs = gen.store_act(wl, gen.prefill_hidden(wl, l, T))
+            out = rig.forward(l, xs)
+            ref, r = rig.oracle_forward(l, xs)
+            ok = check_routing(rig.pool.routing(640), r, wl.k)
+            check_output(wl, out, ref, ok)
+        assert rig.pool.status() == moe.MOE_OK
+    finally:
+        rig.close()

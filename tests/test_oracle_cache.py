@@ -178,3 +178,18 @@ def test_permutation_properties_and_python_sorted():
             rows = perm[offs[e]:offs[e + 1]]
             assert np.all(ids.reshape(-1)[rows] == e)
             assert np.all(np.diff(rows // k) > 0)          # stable: ascending tokens within an expert
+
+
+def test_token_average_is_blocked_in_32s_and_plain_for_short_steps():
+    rng = np.random.default_rng(5)
+    for T in (1, 7, 32, 33, 100):
+        p = rng.random((T, 6)).astype(np.float32)
+        sim = SlotPoolSim(L=1, E=6, S=2, policy=EVICT_MRS, window=2)
+        s = sim.update_scores(0, np.zeros((T, 1), np.int64), p)
+        blocks = [p[b:b + 32].astype(np.float64).sum(0) for b in range(0, T, 32)]
+        np.testing.assert_allclose(s, np.sum(blocks, 0) / T, rtol=1e-5)
+        if T <= 32:
+            acc = np.zeros(6, np.float32)
+            for row in p:
+                acc = acc + row
+            np.testing.assert_array_equal(s, acc / np.float32(T))
