@@ -52,6 +52,8 @@ def parse_args():
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: run the workload's layer shape with fewer layers (0 = all)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--probe-link", action="store_true",
+                    help="measure the host->GPU link: device-started record copies vs DMA, then exit")
     return ap.parse_args()
 
 
@@ -74,22 +76,29 @@ def barrier(world):
         dist.barrier()
 
 
+def _reduce_device():
+    import torch.distributed as dist
+    return "cuda" if dist.get_backend() == "nccl" else "cpu"
+
+
 def max_over_ranks(v, world):
+    """Slowest rank's value (replicas: the job takes as long as its slowest GPU)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=_reduce_device())
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
 
 def sum_over_ranks(v, world):
+    """Work done by all replicas together."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=_reduce_device())
     dist.all_reduce(t, op=dist.ReduceOp.SUM)
     return float(t.item())
 
@@ -355,6 +364,46 @@ def cpu_baseline(wl, T, n_layer_steps, device):
                       f"of the same workload, numpy float64, {el:.1f} s"}
 
 
+def probe_link(wl):
+    """Host -> GPU bandwidth of the library's device-started record copy (moe_load_slot) and of DMA."""
+    import numpy as np
+    import torch
+
+    import expert_offload_slot_gb300 as moe
+    from synth import gen
+    one = __import__("dataclasses").replace(wl, L=1)
+    rec = one.expert_layout()[4]
+    cfg = moe.make_config(1, one.E, one.k, one.H, one.I, 16, one.weight_dtype, one.act_dtype, max_tokens=16)
+    host = moe.HostPool(one.E * rec)
+    wr = torch.zeros((one.E, one.H), dtype=torch.bfloat16, device="cuda")
+    b = torch.zeros(one.E, dtype=torch.float32, device="cuda")
+    pool = moe.Pool(cfg, host.ptr, host.nbytes, wr, b)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for e in range(4):
+        pool.load_slot(0, e, e % 16)
+    torch.cuda.synchronize()
+    n = 64
+    ev0.record()
+    for i in range(n):
+        pool.load_slot(0, 4 + i % (one.E - 4), i % 16)
+    ev1.record()
+    torch.cuda.synchronize()
+    kern = n * rec / (ev0.elapsed_time(ev1) / 1e3) / 1e9
+    src = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
+    dst = torch.empty_like(src, device="cuda")
+    dst.copy_(src, non_blocking=True)
+    torch.cuda.synchronize()
+    ev0.record()
+    dst.copy_(src, non_blocking=True)
+    ev1.record()
+    torch.cuda.synchronize()
+    dma = src.numel() / (ev0.elapsed_time(ev1) / 1e3) / 1e9
+    pool.close()
+    host.free()
+    return {"probe": "link", "record_bytes": rec, "device_started_copy_GBps": kern, "dma_h2d_GBps": dma,
+            "us_per_record": rec / kern / 1e3}
+
+
 def main():
     args = parse_args()
     import torch
@@ -367,6 +416,10 @@ def main():
         # a reduced case for profiler captures: same layer shape, fewer layers, same residency
         wl = dataclasses.replace(wl, L=args.layers)
     rank, world, local = dist_setup(args.gpus)
+    if args.probe_link:
+        if rank == 0:
+            print(json.dumps(probe_link(wl)))
+        return
     label = WORKLOAD_LABEL.get(args.workload, args.workload)
     T = args.batch
     base_cfg = {"workload": label, "layers": wl.L, "experts": wl.E, "top_k": wl.k, "hidden": wl.H,
