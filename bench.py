@@ -47,11 +47,13 @@ def parse_args():
     ap.add_argument("--batch", type=int, default=16, help="decode tokens per step (headline)")
     ap.add_argument("--sweep", default="1,4", help="other decode batches reported under 'sweep' ('' for none)")
     ap.add_argument("--prof-steps", type=int, default=32)
-    ap.add_argument("--cpu-sample", type=int, default=12, help="oracle layer-steps in cpu_baseline")
+    ap.add_argument("--cpu-sample", type=int, default=32, help="oracle layer-steps in cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: run the workload's layer shape with fewer layers (0 = all)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--configs", default="qwen3_hit,qwen3_prefill,dsv3,mixtral",
+                    help="other workloads measured at N=1 and reported under 'configs' ('' for none)")
     ap.add_argument("--probe-link", action="store_true",
                     help="measure the host->GPU link: device-started record copies vs DMA, then exit")
     return ap.parse_args()
@@ -110,7 +112,13 @@ class Clocks:
               "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index):
+        # nvidia-smi numbers GPUs physically; the device's UUID names the one this process uses
         self.idx = gpu_index
+        try:
+            import torch
+            self.idx = "GPU-" + str(torch.cuda.get_device_properties(gpu_index).uuid)
+        except Exception:
+            pass
         self.proc = None
 
     def start(self):
@@ -154,9 +162,31 @@ def load_peaks():
     return 6800.0, "fallback"
 
 
+def load_tc_peak():
+    """Dense bf16 TFLOP/s: measured burst figure, else the fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f)["bf16_tflops"]
+    return 1900.0
+
+
 # ------------------------------------------------------------------ our arm
-class DecodeBench:
-    def __init__(self, wl, max_T, device):
+def host_chunk(wl):
+    """Experts drawn per device chunk when filling a host pool (bounded fp32 temporaries, ~3 GB)."""
+    per = 3 * wl.H * wl.I * 4
+    return max(1, min(16, (3 << 30) // per))
+
+
+class PoolBench:
+    """One slot pool over a pinned host pool, driven through the C ABI.
+
+    host: an already-filled HostPool to share (its weights are those of `host_wl`), else one is
+    allocated and filled with this workload's weights.  slots overrides the slot count (L*E gives the
+    all-resident hit path).  staging adds the two layer-sized prefill regions.
+    """
+
+    def __init__(self, wl, max_T, device, host=None, slots=None, staging=False):
         import numpy as np
         import torch
 
@@ -164,11 +194,16 @@ class DecodeBench:
         from synth import gen
         self.moe, self.wl, self.device = moe, wl, device
         self.rec = wl.expert_layout()[4]
-        self.cfg = moe.make_config(wl.L, wl.E, wl.k, wl.H, wl.I, wl.S, wl.weight_dtype, wl.act_dtype, wl.gating,
-                                   wl.shared, wl.evict, wl.window, 0.9, (0.25, 0.25, 0.25, 0.25), 0, max_T)
+        self.S = wl.S if slots is None else slots
+        self.cfg = moe.make_config(wl.L, wl.E, wl.k, wl.H, wl.I, self.S, wl.weight_dtype, wl.act_dtype, wl.gating,
+                                   wl.shared, wl.evict, wl.window, 0.9, (0.25, 0.25, 0.25, 0.25),
+                                   2 if staging else 0, max_T)
         t0 = time.time()
-        self.host = moe.HostPool(wl.L * wl.E * self.rec)
-        gen.fill_host_pool(wl, self.host.torch(), device=device)
+        self.own_host = host is None
+        if host is None:
+            host = moe.HostPool(wl.L * wl.E * self.rec)
+            gen.fill_host_pool(wl, host.torch(), device=device, chunk=host_chunk(wl))
+        self.host = host
         w_r, b = gen.routers(wl)
         wr = w_r.view(np.int16) if wl.act_dtype == 1 else w_r
         self.w_r = torch.from_numpy(np.ascontiguousarray(wr)).to(device)
@@ -176,7 +211,7 @@ class DecodeBench:
         self.shared = torch.from_numpy(gen.shared_records(wl)).to(device) if wl.shared else None
         self.pool = moe.Pool(self.cfg, self.host.ptr, self.host.nbytes, self.w_r, self.b, self.shared,
                              device=torch.cuda.current_device())
-        self.pool.set_lut(gen.initial_lut(wl))
+        self.pool.set_lut(gen.initial_lut(wl, S=self.S))
         torch.cuda.synchronize()
         self.setup_s = time.time() - t0
 
@@ -189,7 +224,8 @@ class DecodeBench:
                 self.pool.forward(l, x_in[l], out[l], self.moe.MOE_MODE_DECODE)
         return g, self.pool.launch_count() - n0
 
-    def run(self, T, W, K, prof_steps, clocks=None, world=1, e2e=True):
+    def decode(self, T, W, K, prof_steps, clocks=None, world=1, e2e=True):
+        """W warm-up and K timed decode steps (one CUDA graph of L moe_forward calls per step)."""
         import torch
         wl, moe = self.wl, self.moe
         dev = self.device
@@ -231,14 +267,22 @@ class DecodeBench:
                "bytes_copied": st1["bytes_copied"] - st0["bytes_copied"], "clocks": clk}
         res["status"] = self.pool.status()
         # profiling pass: per-stage CUDA-event times of every layer, same workload continued
-        res["prof"] = self.profile(xs, x_in, out, s, T, prof_steps) if prof_steps > 0 else \
+        res["prof"] = self.profile_decode(xs, x_in, out, s, T, prof_steps) if prof_steps > 0 else \
             {"launches": 0, "stage_ms": [0.0] * self.moe.MOE_NUM_STAGES, "sum_U": 0, "T": T, "bytes_copied": 0}
         if e2e:
             res["e2e"] = self.run_e2e(xs, g, x_in, out, s, W, K)
         del g
         return res
 
-    def profile(self, xs, x_in, out, s, T, P):
+    def _collect(self, stage, n):
+        for l in range(self.wl.L):
+            v = self.pool.profile_read(l)
+            for i in range(len(stage)):
+                stage[i] += v[i]
+            n += 1
+        return n
+
+    def profile_decode(self, xs, x_in, out, s, T, P):
         import torch
         wl = self.wl
         self.pool.profile_enable(True)
@@ -251,10 +295,7 @@ class DecodeBench:
                 x_in.copy_(xs[i % xs.shape[0]])
                 gp.replay()
             s.synchronize()
-            for l in range(wl.L):
-                v = self.pool.profile_read(l)
-                stage = [a + b for a, b in zip(stage, v)]
-                n += 1
+            n = self._collect(stage, n)
         st1 = self.pool.stats()
         self.pool.profile_enable(False)
         del gp
@@ -263,6 +304,43 @@ class DecodeBench:
             U += n                              # the shared expert is streamed by every launch
         return {"launches": n, "stage_ms": stage, "sum_U": U, "T": T,
                 "bytes_copied": st1["bytes_copied"] - st0["bytes_copied"]}
+
+    def prefill(self, T, W, K, prof_steps=1):
+        """Staged prefill of T tokens through all L layers (two swapped layer-sized staging regions,
+        layer l+2 copied while l+1 computes), eager launches: W warm-up and K timed steps."""
+        import torch
+        wl, moe = self.wl, self.moe
+        x = __import__("synth").gen.torch_prefill_hidden(wl, T, self.device)
+        out = torch.empty_like(x)
+        s = torch.cuda.Stream()
+
+        def step():
+            for l in range(wl.L):
+                self.pool.forward(l, x[l], out[l], moe.MOE_MODE_PREFILL_STAGED, stream=s)
+
+        for _ in range(W):
+            step()
+        s.synchronize()
+        st0 = self.pool.stats()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        ev0.record(s)
+        for _ in range(K):
+            step()
+        ev1.record(s)
+        torch.cuda.synchronize()
+        ms = ev0.elapsed_time(ev1)
+        st1 = self.pool.stats()
+        self.pool.profile_enable(True)
+        stage, n = [0.0] * moe.MOE_NUM_STAGES, 0
+        for _ in range(prof_steps):
+            step()
+            s.synchronize()
+            n = self._collect(stage, n)
+        self.pool.profile_enable(False)
+        return {"T": T, "ms": ms, "steps": K, "status": self.pool.status(),
+                "staged": st1["staged_layers"] - st0["staged_layers"],
+                "prof": {"launches": n, "stage_ms": stage}}
 
     def run_e2e(self, xs, g, x_in, out, s, W, K):
         """Same metric through the C ABI with host buffers: H2D of x and D2H of out every step."""
@@ -283,23 +361,152 @@ class DecodeBench:
         nb = x_in.numel() * x_in.element_size()
         return {"ms": ms, "h2d": nb, "d2h": nb}
 
-    def close(self):
+    def close(self, keep_host=False):
         self.pool.close()
-        self.host.free()
+        if self.own_host and not keep_host:
+            self.host.free()
+
+
+def expert_bytes(wl):
+    """Stored bytes of one expert's three matrices (3*H*I elements, plus fp8 block scales)."""
+    be = 3 * wl.H * wl.I * wl.weight_elt_bytes
+    if wl.weight_dtype == 2:
+        be += 3 * (wl.H // 128) * (wl.I // 128) * 4
+    return be
 
 
 def ffn_algorithmic_bytes(wl, sum_U, bytes_copied, layer_steps, T):
-    """HBM bytes the expert FFN must move: the U expert records it reads (3*H*I weights each),
-    the miss bytes it writes into slots, and x in / out once per layer-step."""
-    Be = 3 * wl.H * wl.I * wl.weight_elt_bytes
-    return sum_U * Be + bytes_copied + layer_steps * 2 * T * wl.H * wl.act_elt_bytes
+    """HBM bytes the expert FFN must move: the U expert records it reads, the miss bytes it writes
+    into slots, and x in / out once per layer-step."""
+    return sum_U * expert_bytes(wl) + bytes_copied + layer_steps * 2 * T * wl.H * wl.act_elt_bytes
 
 
 def step_bytes(wl, U_per_layer, T):
     """Algorithmic HBM bytes of one layer-step: router + U expert records + x in and out."""
-    eb = wl.weight_elt_bytes
-    Be = 3 * wl.H * wl.I * eb
-    return wl.E * wl.H * wl.act_elt_bytes + U_per_layer * Be + 2 * T * wl.H * wl.act_elt_bytes
+    return wl.E * wl.H * wl.act_elt_bytes + U_per_layer * expert_bytes(wl) + 2 * T * wl.H * wl.act_elt_bytes
+
+
+def prefill_flops(wl, T):
+    """Routed expert FLOPs of one layer (2*T*k*3*H*I), the shared expert's, and the router's."""
+    f = 2 * T * wl.k * 3 * wl.H * wl.I + 2 * T * wl.H * wl.E
+    if wl.shared:
+        f += 2 * T * 3 * wl.H * wl.I
+    return f
+
+
+def decode_summary(wl, r, peak):
+    """Per-config decode line: tokens/s, us/layer, hit rate, per-stage us, FFN-kernel HBM roofline."""
+    import expert_offload_slot_gb300 as moe
+    prof = r["prof"]
+    n = max(1, prof["launches"])
+    ffn_ms = prof["stage_ms"][moe.STAGES.index("ffn")] + prof["stage_ms"][moe.STAGES.index("copy")]
+    ffn_b = ffn_algorithmic_bytes(wl, prof["sum_U"], prof["bytes_copied"], prof["launches"], r["T"])
+    ach = ffn_b / (ffn_ms / 1e3) / 1e9 if ffn_ms > 0 else 0.0
+    U = prof["sum_U"] / n
+    lay_us = sum(prof["stage_ms"]) * 1e3 / n
+    return {"T": r["T"], "tokens_per_s": r["steps"] * r["T"] * wl.L / (r["ms"] / 1e3),
+            "us_per_layer": r["ms"] * 1e3 / (r["steps"] * wl.L), "steps": r["steps"],
+            "hit_rate": r["hits"] / max(1, r["hits"] + r["misses"]),
+            "miss_MB_per_layer": r["bytes_copied"] / 1e6 / (r["steps"] * wl.L),
+            "mean_U": U, "stage_us_per_layer": {k: v * 1e3 / n for k, v in zip(moe.STAGES, prof["stage_ms"])},
+            "ffn_roofline": {"bound": "hbm", "achieved": ach, "unit": "GB/s", "frac": ach / peak,
+                             "bytes_per_launch": ffn_b / n, "us_per_launch": ffn_ms * 1e3 / n},
+            "layer_frac": step_bytes(wl, U, r["T"]) / (lay_us * 1e-6) / 1e9 / peak if lay_us else 0.0,
+            "status": moe_status_name(r["status"]), "clocks": r.get("clocks")}
+
+
+def prefill_summary(wl, r, U, hbm_peak, tc_peak, link_gbs):
+    """Per-config staged-prefill line: the pipeline (bound by the host link: E records per layer)
+    and the in-HBM forward of one layer (route + plan + expert kernels) against both rooflines."""
+    import expert_offload_slot_gb300 as moe
+    T, L = r["T"], wl.L
+    prof = r["prof"]
+    n = max(1, prof["launches"])
+    st = {k: v * 1e3 / n for k, v in zip(moe.STAGES, prof["stage_ms"])}
+    us_layer = r["ms"] * 1e3 / (r["steps"] * L)
+    ffn_us = st["ffn"]
+    fl = prefill_flops(wl, T)
+    byt = (U + (1 if wl.shared else 0)) * expert_bytes(wl) + 2 * T * wl.H * wl.act_elt_bytes
+    staged_bytes = wl.E * wl.expert_layout()[4]
+    inhbm_us = st["route"] + st["plan"] + st["ffn"]
+    return {"T": T, "tokens_per_s": r["steps"] * T * L / (r["ms"] / 1e3), "us_per_layer": us_layer,
+            "steps": r["steps"], "staged_layers": r["staged"], "experts_with_tokens": U,
+            "link": {"bound": "host link", "bytes_per_layer": staged_bytes,
+                     "achieved": staged_bytes / (us_layer * 1e-6) / 1e9, "unit": "GB/s",
+                     "frac_of_measured_link": staged_bytes / (us_layer * 1e-6) / 1e9 / link_gbs if link_gbs else None},
+            "in_hbm": {"us_per_layer": inhbm_us, "tokens_per_s": T / (inhbm_us * 1e-6),
+                       "stage_us_per_layer": st,
+                       "ffn_tflops": fl / (ffn_us * 1e-6) / 1e12, "ffn_tc_frac": fl / (ffn_us * 1e-6) / 1e12 / tc_peak,
+                       "ffn_gbs": byt / (ffn_us * 1e-6) / 1e9, "ffn_hbm_frac": byt / (ffn_us * 1e-6) / 1e9 / hbm_peak,
+                       "flops_per_layer": fl, "bytes_per_layer": byt,
+                       "bound": "hbm" if fl / byt < tc_peak * 1e12 / (hbm_peak * 1e9) else "tensor"},
+            "status": moe_status_name(r["status"])}
+
+
+def moe_status_name(st):
+    import expert_offload_slot_gb300 as moe
+    return moe.STATUS_NAMES.get(st, st)
+
+
+def distinct_experts_last_call(bench, T):
+    r = bench.pool.routing(T)
+    return int(len(set(int(v) for v in r["ids"].reshape(-1))))
+
+
+def run_configs(names, dev, qwen_host, args, peaks, link_gbs):
+    """The other workload shapes at one GPU, each pool built, measured and freed in turn."""
+    import dataclasses
+
+    from synth import get_workload
+    hbm, tc = peaks
+    out = {}
+    q = get_workload("qwen3_decode")
+    for name in names:
+        t0 = time.time()
+        if name == "qwen3_hit":
+            # every expert resident (S = L*E): the hit path alone, no miss copies
+            b = PoolBench(q, 16, dev, host=qwen_host, slots=q.L * q.E)
+            res = {}
+            for T in (1, 16):
+                c = Clocks(torch_local())
+                res[str(T)] = decode_summary(q, b.decode(T, 8, 64, 8, c, 1, e2e=False), hbm)
+            b.close()
+            out[name] = {"workload": "qwen3-30b-a3b-shaped-decode, all 6144 experts resident", "decode": res}
+        elif name == "qwen3_prefill":
+            # the decode workload's expert weights and router matrix (same shapes and law) with the
+            # prefill router bias 0, so that all 128 experts receive tokens
+            p = dataclasses.replace(get_workload("qwen3_prefill"), name="qwen3_decode")
+            pr = get_workload("qwen3_prefill")
+            b = PoolBench(p, max(pr.prefill_T), dev, host=qwen_host, staging=True)
+            res = {}
+            for T in pr.prefill_T:
+                r = b.prefill(T, 3, 3)
+                res[str(T)] = prefill_summary(p, r, distinct_experts_last_call(b, T), hbm, tc, link_gbs)
+            b.close()
+            out[name] = {"workload": "qwen3-30b-a3b-shaped-prefill, staged (2 layer-sized regions)", "prefill": res}
+        elif name in ("dsv3", "mixtral"):
+            wl = get_workload(name)
+            max_T = max(wl.decode_T + wl.prefill_T)
+            b = PoolBench(wl, max_T, dev, staging=True)
+            dec = {}
+            for T in wl.decode_T:
+                K = 32 if name == "dsv3" else 24
+                dec[str(T)] = decode_summary(wl, b.decode(T, 3, K, 4, Clocks(torch_local()), 1, e2e=False), hbm)
+            pre = {}
+            for T in wl.prefill_T:
+                r = b.prefill(T, 3, 3)
+                pre[str(T)] = prefill_summary(wl, r, distinct_experts_last_call(b, T), hbm, tc, link_gbs)
+            b.close()
+            lbl = {"dsv3": "deepseek-v3-shaped (fp8 e4m3, 128x128 block scales, shared expert)",
+                   "mixtral": "mixtral-8x7b-shaped (64 slots, MRS eviction)"}[name]
+            out[name] = {"workload": lbl, "layers": wl.L, "slots": wl.S, "decode": dec, "prefill": pre}
+        out[name]["seconds"] = time.time() - t0
+    return out
+
+
+def torch_local():
+    import torch
+    return torch.cuda.current_device()
 
 
 # ------------------------------------------------------------------ oracle arm
@@ -451,20 +658,15 @@ def main():
     dev = torch.device("cuda", torch.cuda.current_device())
     sweep_T = [int(v) for v in args.sweep.split(",") if v.strip()] if args.sweep else []
     max_T = max([T] + sweep_T)
-    bench = DecodeBench(wl, max_T, dev)
-    try:
-        sweep = {}
-        for t in sweep_T:
-            r = bench.run(t, args.warmup, args.steps, max(4, args.prof_steps // 2), None, world, e2e=False)
-            sweep[str(t)] = {"tokens_per_s": r["steps"] * t * wl.L / (r["ms"] / 1e3),
-                             "us_per_layer": r["ms"] * 1e3 / (r["steps"] * wl.L),
-                             "hit_rate": r["hits"] / max(1, r["hits"] + r["misses"]),
-                             "stage_us_per_layer": {n: v * 1e3 / max(1, r["prof"]["launches"])
-                                                    for n, v in zip(moe.STAGES, r["prof"]["stage_ms"])}}
-        clocks = Clocks(local) if rank == 0 else None
-        r = bench.run(T, args.warmup, args.steps, args.prof_steps, clocks, world, e2e=not args.no_e2e)
-    finally:
-        pass
+    peak, peak_kind = load_peaks()
+    tc_peak = load_tc_peak()
+    bench = PoolBench(wl, max_T, dev)
+    sweep = {}
+    for t in sweep_T:
+        r = bench.decode(t, args.warmup, args.steps, max(4, args.prof_steps // 2), None, world, e2e=False)
+        sweep[str(t)] = decode_summary(wl, r, peak)
+    clocks = Clocks(local) if rank == 0 else None
+    r = bench.decode(T, args.warmup, args.steps, args.prof_steps, clocks, world, e2e=not args.no_e2e)
     ms = max_over_ranks(r["ms"], world)
     tokens = sum_over_ranks(r["steps"] * T * wl.L, world)
     value = tokens / (ms / 1e3)
@@ -472,7 +674,6 @@ def main():
     e2e_value = tokens / (e2e_ms / 1e3)
 
     prof = r["prof"]
-    peak, peak_kind = load_peaks()
     ffn_ms = prof["stage_ms"][moe.STAGES.index("ffn")] + prof["stage_ms"][moe.STAGES.index("copy")]
     layer_steps = prof["launches"]
     U_mean = prof["sum_U"] / max(1, layer_steps)
@@ -483,6 +684,14 @@ def main():
     if rank != 0:
         bench.close()
         return
+    bench.close(keep_host=True)
+    configs = {}
+    names = [v.strip() for v in args.configs.split(",") if v.strip()]
+    if world == 1 and names and args.workload == "qwen3_decode" and not args.layers:
+        link = probe_link(wl)
+        configs["link"] = link
+        configs.update(run_configs(names, dev, bench.host, args, (peak, tc_peak), link["dma_h2d_GBps"]))
+    bench.host.free()
     cpu = None
     if not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, T, args.cpu_sample, dev)
@@ -512,8 +721,8 @@ def main():
         "sweep": sweep,
         "setup_s": bench.setup_s,
         "cpu_baseline": cpu,
+        "configs": configs,
     }
-    bench.close()
     print(json.dumps(line))
 
 
