@@ -346,11 +346,12 @@ MOE_API moe_status moe_pool_create(const moe_config* cfg, const void* host_pool,
     P->sc.npad_max = np;
     PA(P->sc.wmat, (E + 1) * (size_t)np, 0);
     PA(P->sc.hbuf, (E + 1) * (size_t)np * d.I, 0);
-    PA(P->sc.partial, tc_partial_floats(d, P->sc), 0);
-    const size_t tiles = std::max((E + 1) * (size_t)((d.I + 127) / 128), (size_t)((d.H + 127) / 128));
-    P->sc.n_counters = 3 * tiles;
-    PA(P->sc.counters, P->sc.n_counters, 0);
-    PA(P->sc.grid_bar, 2, 0);
+    P->sc.partial_floats = tc_partial_floats(d, np);
+    PA(P->sc.partial, P->sc.partial_floats, 0);
+    P->sc.dn_partial_floats = tc_dn_partial_floats(d, np);
+    PA(P->sc.dn_partial, P->sc.dn_partial_floats, 0);
+    P->sc.n_ffn_sync = tc_ffn_sync_ints(d);
+    PA(P->sc.ffn_sync, P->sc.n_ffn_sync, 0);
     if ((size_t)tc_npad((int)Tm) > (size_t)np) {
       // gather path for calls with more tokens than the dense path takes
       PA(P->sc.inv, Tm * k, 0);

@@ -172,6 +172,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     missed[e] = 0;
   }
   if (tid < 12) sh_misc[tid] = 0;
+  // arrival counters and readiness flags of the expert kernel that follows
+  for (int i = tid; i < a.sc.n_ffn_sync; i += kPlanThreads) a.sc.ffn_sync[i] = 0;
   const bool hist = (a.flags & PLAN_HISTORY) != 0;
   const bool cache = (a.flags & PLAN_CACHE) != 0;
   int t_step = 0;

@@ -46,6 +46,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstring>
 
 #include "moeslot_internal.cuh"
@@ -569,38 +570,108 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap map_b, Args a) {
 
 // ----------------------------------------------------------------- fused decode FFN
 // One persistent kernel per layer for the dense token path (cooperative launch:
-// every CTA is resident, so CTAs may wait on each other with bounded spins):
-//   phase 0: gate/up of the entries already resident, while four copy warps
-//            per CTA pull this step's misses from the mapped host pool
-//            (NVLink-C2C reads) into their records;
-//   phase 1: gate/up of the entries copied this step — after grid barrier A
-//            (every CTA's copy warps done);
-//   phase 2: down + combine over all entries — after grid barrier B (every
-//            CTA's gate/up epilogue done, so h is complete).
-// The grid barriers are flip-bit counters: each CTA adds 1 (CTA 0 adds
-// 2^31 - (G-1)), so the high bit flips exactly when all G CTAs have arrived and
-// the low bits return to their old value, ready for the next launch.
-constexpr int kCopyWarps = 4;
+// every CTA is resident, so CTAs may wait on each other with bounded spins).
+// Work units in one global order, which CTA c walks as c, c+G, c+2G, ...:
+//   1. gate/up tiles of the entries already resident,
+//   2. down tiles of those entries,
+//   3. gate/up tiles of the entries copied this step (in copy-job order),
+//   4. down tiles of those entries;
+// meanwhile two copy warps per CTA pull this step's misses from the mapped
+// host pool (NVLink-C2C reads) into their records, one job after another.  A
+// unit waits only for what it reads: a copied record (jdone[job] == G: every
+// CTA's slice of that job is written) or the complete h of its entry
+// (hready[u] == the entry's gate/up tiles).  So the resident experts' whole FFN
+// overlaps the link-bound copies.
+// A down unit covers one entry: it writes an fp32 partial tile, and the last
+// unit to finish a 128-row output tile sums the partials of every entry in
+// entry order (ascending expert id, shared expert last).  The order is fixed,
+// and the split counts depend on the entry count alone, so the output does not
+// depend on which experts happened to be resident.
+// Partial tiles are row-major ([128 rows][columns]) so that each epilogue
+// thread (one row) moves its columns with 16-byte accesses.
+constexpr int kCopyWarps = 2;
 constexpr int kFusedThreads = kThreads + 32 * kCopyWarps;
+constexpr int kFusedBufs = 8;
 
 struct FusedArgs {
   const CopyJob* jobs;
   const int32_t* n_jobs;
-  uint32_t rec16;
-  unsigned long long magic;     // ceil(2^64 / rec16): job index = high word of idx * magic
-  uint32_t* grid_bar;           // [2]: A copies done, B gate/up done
-  const int32_t* sel[2];        // phase 0 / 1 entry lists
-  const int32_t* sel_count[2];
-  float* partial[3];            // per-phase split partial regions
-  int32_t* counters[3];
-  int max_split_units[3];
+  uint32_t rec16;               // record bytes / 16
+  const int32_t* elist;         // [2][E1]: resident entries, copied entries (work positions, ascending)
+  const int32_t* ecount;        // [2]
+  int E1;                       // E + 1
+  float* gu_partial;            // gate/up split partials
+  size_t gu_partial_floats;
+  float* dn_partial;            // per-entry down partials
+  size_t dn_partial_floats;
+  int32_t* gu_cnt;              // [E1 * MT_I] split arrivals per gate/up tile    } zeroed by the plan
+  uint32_t* dn_done;            // CTAs whose down units are all written           } kernel before
+  uint32_t* hready;             // [E1] finished gate/up tiles per entry           } every launch
+  uint32_t* jdone;              // [E1] CTAs done with each copy job               }
 };
 
-// Release this CTA's prior writes (of the calling thread, after a CTA-level
-// barrier) and arrive.
-__device__ __forceinline__ void grid_arrive(uint32_t* bar) {
-  const uint32_t inc = blockIdx.x == 0 ? 0x80000000u - (gridDim.x - 1u) : 1u;
-  asm volatile("fence.acq_rel.gpu;\n red.release.gpu.global.add.u32 [%0], %1;" ::"l"(bar), "r"(inc) : "memory");
+struct FSched {
+  int n, nh, nm, mt_i, kb_h, mt_h, kb_i, sg, sd, cols;
+  int p0, p1, p2, p3, total;
+};
+
+__device__ __forceinline__ FSched fused_sched(const Args& a, const FusedArgs& f, int G) {
+  FSched s;
+  s.n = *a.n_work;
+  s.nh = f.ecount[0];
+  s.nm = f.ecount[1];
+  s.mt_i = (a.I + BM - 1) / BM;
+  s.kb_h = (a.H + BK - 1) / BK;
+  s.mt_h = (a.H + BM - 1) / BM;
+  s.kb_i = (a.I + BK - 1) / BK;
+  s.cols = (a.T + 3) & ~3;            // partial columns kept: the tokens, rounded up to 4
+  // Splits: the fewest that give every CTA about two gate/up units and one down
+  // unit (all units of a step share one round-robin schedule, so per-phase wave
+  // quantisation matters little, while every unit costs a partial round trip).
+  const int gu_tiles = s.n * s.mt_i;
+  const size_t gcap = f.gu_partial_floats / ((size_t)2 * s.cols * BM);
+  s.sg = max(1, min(min(s.kb_h, 8), (2 * G + gu_tiles - 1) / max(gu_tiles, 1)));
+  while (s.sg > 1 && (size_t)gu_tiles * s.sg > gcap) --s.sg;
+  const int dn_tiles = s.n * s.mt_h;
+  const size_t dcap = f.dn_partial_floats / ((size_t)s.cols * BM);
+  s.sd = max(1, min(min(s.kb_i, 4), (G + dn_tiles - 1) / max(dn_tiles, 1)));
+  while (s.sd > 1 && (size_t)dn_tiles * s.sd > dcap) --s.sd;
+  s.p0 = s.nh * s.mt_i * s.sg;
+  s.p1 = s.nh * s.mt_h * s.sd;
+  s.p2 = s.nm * s.mt_i * s.sg;
+  s.p3 = s.nm * s.mt_h * s.sd;
+  s.total = s.p0 + s.p1 + s.p2 + s.p3;
+  return s;
+}
+
+struct FUnit {
+  int gu, miss, li, u, mt, sp, kb0, kb1;
+};
+
+__device__ __forceinline__ FUnit fused_unit(const FSched& s, const FusedArgs& f, int g) {
+  FUnit r;
+  int loc = g;
+  if (loc < s.p0) {
+    r.gu = 1, r.miss = 0;
+  } else if ((loc -= s.p0) < s.p1) {
+    r.gu = 0, r.miss = 0;
+  } else if ((loc -= s.p1) < s.p2) {
+    r.gu = 1, r.miss = 1;
+  } else {
+    loc -= s.p2;
+    r.gu = 0, r.miss = 1;
+  }
+  // entry-major: an entry's h completes early, and its down units come soon after
+  const int spn = r.gu ? s.sg : s.sd, kbn = r.gu ? s.kb_h : s.kb_i;
+  const int per = (r.gu ? s.mt_i : s.mt_h) * spn;
+  r.li = loc / per;
+  const int rem = loc - r.li * per;
+  r.mt = rem / spn;
+  r.sp = rem - r.mt * spn;
+  r.kb0 = r.sp * kbn / spn;
+  r.kb1 = (r.sp + 1) * kbn / spn;
+  r.u = f.elist[r.miss * f.E1 + r.li];
+  return r;
 }
 
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
@@ -609,24 +680,32 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   return v;
 }
 
-// Wait until the barrier's high bit differs from its value at kernel start (~1 s bound).
-__device__ __noinline__ bool grid_wait(uint32_t* bar, uint32_t start_bit) {
+// Release this thread's prior writes (and, after a CTA barrier, the CTA's) and add 1.
+__device__ __forceinline__ void release_add(uint32_t* p) {
+  asm volatile("fence.acq_rel.gpu;\n red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p) : "memory");
+}
+
+// Wait until *p >= target (~1 s bound); gives up at once if another CTA has
+// already recorded an error, so one failure cannot chain into many timeouts.
+__device__ __noinline__ bool wait_count(const uint32_t* p, uint32_t target, const int32_t* status) {
   const uint64_t t0 = global_ns();
   for (uint32_t it = 0;; ++it) {
-    if ((ld_acquire(bar) & 0x80000000u) != start_bit) return true;
-    if ((it & 63u) == 63u && global_ns() - t0 > 1000000000ull) return false;
-    __nanosleep(32);
+    if (ld_acquire(p) >= target) return true;
+    if ((it & 15u) == 15u) {
+      if (*reinterpret_cast<const volatile int32_t*>(status) != 0) return false;
+      if (global_ns() - t0 > 1000000000ull) return false;
+    }
+    __nanosleep(64);
   }
 }
 
-template <int MODE>
-__device__ __forceinline__ Plan phase_plan(Args a, const FusedArgs& f, int phase, int grid) {
-  if (phase < 2) {
-    a.sel = f.sel[phase];
-    a.sel_count = f.sel_count[phase];
-  }
-  a.max_split_units = f.max_split_units[phase];
-  return make_plan<MODE>(a, grid);
+// 32 KB of weight tiles plus two activation tiles of N x 64 bf16 (1 KB aligned)
+__host__ __device__ constexpr uint32_t fused_stage_bytes(int N) {
+  return (2 * kTileBytes + 2u * (uint32_t)N * BK * 2 + 1023u) & ~1023u;
+}
+
+__device__ __forceinline__ void st_f4(float* p, float a, float b, float c, float d) {
+  *reinterpret_cast<float4*>(p) = make_float4(a, b, c, d);
 }
 
 __global__ void __launch_bounds__(kFusedThreads, 1)
@@ -634,8 +713,8 @@ tc_fused_decode_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
                        FusedArgs f) {
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
-  __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
-  __shared__ uint32_t tmem_base_sh, start_bit_sh[2];
+  __shared__ __align__(8) uint64_t tfull_bar[kFusedBufs], tempty_bar[kFusedBufs], drain_bar;
+  __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_sh, last_sh;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -643,22 +722,24 @@ tc_fused_decode_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = a.N;
   const int S = a.stages;
+  const int G = gridDim.x;
+  // A stage holds 32 KB of weights and up to two activation tiles:
+  //   gate/up: [gate tile | up tile | x tile], one K block;
+  //   down:    [W tile kb | W tile kb+1 | h tile kb | h tile kb+1], two K blocks.
   const uint32_t b_bytes = (uint32_t)N * BK * 2;
-  const uint32_t stage_bytes = (2 * kTileBytes + b_bytes + 1023) & ~1023u;   // sized for gate/up
-  const int nbuf = 4 * N <= 512 ? 2 : 1;
+  const uint32_t stage_bytes = fused_stage_bytes(N);
+  // as many TMEM accumulator buffers as fit (up to 8): the MMA warp runs ahead of the epilogue
+  const int nbuf = min(kFusedBufs, 512 / (2 * N));
   const uint32_t acc_cols = (uint32_t)(2 * N);
   uint32_t ncols = 32;
   while (ncols < (uint32_t)nbuf * acc_cols) ncols <<= 1;
 
   if (threadIdx.x == 0) {
-    // the barriers cannot have flipped yet: this CTA has not arrived
-    start_bit_sh[0] = *reinterpret_cast<volatile uint32_t*>(&f.grid_bar[0]) & 0x80000000u;
-    start_bit_sh[1] = *reinterpret_cast<volatile uint32_t*>(&f.grid_bar[1]) & 0x80000000u;
     for (int s = 0; s < S; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kFusedBufs; ++b) {
       mbar_init(&tfull_bar[b], 1);
       mbar_init(&tempty_bar[b], 4);
     }
@@ -672,71 +753,71 @@ tc_fused_decode_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
   fence_after();
   const uint32_t tmem = tmem_base_sh;
   const uint32_t idesc = idesc_bf16(N);
-  const int kb_h = (a.H + BK - 1) / BK, kb_i = (a.I + BK - 1) / BK;
 
   if (warp == 0) {
     // ------------------------------------------------------------- producer
     if (lane == 0) {
+      const FSched sc = fused_sched(a, f, G);
       uint32_t it = 0;
       bool ok = true;
-      // phase-2 stages whose weight tile is in flight but whose h tile waits for barrier B
-      int pend_s[kMaxStages], pend_kb[kMaxStages], pend_u[kMaxStages];
-      int npend = 0;
-      bool h_ready = false;
-      auto resolve_h = [&]() -> bool {
-        if (!grid_wait(&f.grid_bar[1], start_bit_sh[1])) return false;
-        asm volatile("fence.proxy.async.global;" ::: "memory");   // generic writes -> async-proxy reads
-        for (int q = 0; q < npend; ++q)
-          tma_load_3d(smem + (size_t)pend_s[q] * stage_bytes + kTileBytes, &map_h, &full_bar[pend_s[q]],
-                      pend_kb[q] * BK, 0, pend_u[q]);
-        npend = 0;
-        h_ready = true;
-        return true;
-      };
-      for (int ph = 0; ph < 3 && ok; ++ph) {
-        const bool gu = ph < 2;
-        if (ph == 1) {
-          if (!grid_wait(&f.grid_bar[0], start_bit_sh[0])) { ok = false; break; }
-          asm volatile("fence.proxy.async.global;" ::: "memory");   // copied records -> bulk-copy reads
+      int pend_s[kMaxStages], pend_kb[kMaxStages], pend_nk[kMaxStages];
+      for (int g = blockIdx.x; g < sc.total && ok; g += G) {
+        const FUnit r = fused_unit(sc, f, g);
+        if (r.miss) {
+          // a copied record: every CTA's slice of its job must have landed (down units
+          // too: their weight tiles are issued before h is complete)
+          if (!wait_count(&f.jdone[r.li], (uint32_t)G, a.status)) { ok = false; break; }
+          asm volatile("fence.proxy.async.global;" ::: "memory");   // generic writes -> bulk-copy reads
         }
-        const Plan pl = gu ? phase_plan<kModeGateUp>(a, f, ph, gridDim.x) : phase_plan<kModeDown>(a, f, ph, gridDim.x);
-        Args aa = a;
-        if (gu) { aa.sel = f.sel[ph]; aa.sel_count = f.sel_count[ph]; }
-        const uint32_t a_bytes = gu ? 2 * kTileBytes : kTileBytes;
-        for (int unit = blockIdx.x; unit < pl.units && ok; unit += gridDim.x) {
-          const UnitRange r = gu ? unit_range<kModeGateUp>(pl, aa, unit) : unit_range<kModeDown>(pl, aa, unit);
-          for (int u = r.u0; u < r.u1 && ok; ++u) {
-            const WorkEntry we = a.work[u];
-            const uint8_t* wbase = a.records + (size_t)we.rid * a.rec + (gu ? a.off13 : a.off2) +
-                                   (size_t)r.mt * (gu ? kb_h : kb_i) * a_bytes;
-            for (int kb = r.kb0; kb < r.kb1; ++kb, ++it) {
-              const int s = it % S;
-              // a ring full of stages waiting for h can only drain once h is complete
-              if (!gu && !h_ready && npend == S && !resolve_h()) { ok = false; break; }
-              if (it >= (uint32_t)S && !mbar_wait(&empty_bar[s], ((it / S) - 1) & 1)) { ok = false; break; }
-              if (abort_sh) { ok = false; break; }
-              uint8_t* st = smem + (size_t)s * stage_bytes;
-              mbar_expect_tx(&full_bar[s], a_bytes + b_bytes);
-              bulk_load(st, wbase + (size_t)kb * a_bytes, a_bytes, &full_bar[s]);
-              if (gu) {
-                tma_load_3d(st + a_bytes, &map_x, &full_bar[s], kb * BK, 0, 0);
-              } else if (h_ready) {
-                tma_load_3d(st + a_bytes, &map_h, &full_bar[s], kb * BK, 0, u);
-              } else {
-                pend_s[npend] = s;
-                pend_kb[npend] = kb;
-                pend_u[npend] = u;
-                ++npend;
-              }
-            }
+        // down: h of this entry complete?  If not yet, weight tiles are issued
+        // ahead and their h tiles once it is (at the latest when the ring is full)
+        bool h_ok = r.gu || ld_acquire(&f.hready[r.u]) >= (uint32_t)sc.mt_i;
+        if (!r.gu && h_ok) asm volatile("fence.proxy.async.global;" ::: "memory");
+        int npend = 0;
+        auto resolve = [&]() -> bool {
+          if (!wait_count(&f.hready[r.u], (uint32_t)sc.mt_i, a.status)) return false;
+          asm volatile("fence.proxy.async.global;" ::: "memory");   // h written by other CTAs -> TMA reads
+          for (int q = 0; q < npend; ++q)
+            for (int j = 0; j < pend_nk[q]; ++j)
+              tma_load_3d(smem + (size_t)pend_s[q] * stage_bytes + 2 * kTileBytes + j * b_bytes, &map_h,
+                          &full_bar[pend_s[q]], (pend_kb[q] + j) * BK, 0, r.u);
+          npend = 0;
+          h_ok = true;
+          return true;
+        };
+        const WorkEntry we = a.work[r.u];
+        const uint8_t* wbase = a.records + (size_t)we.rid * a.rec + (r.gu ? a.off13 : a.off2) +
+                               (size_t)r.mt * (r.gu ? sc.kb_h * 2 * kTileBytes : sc.kb_i * kTileBytes);
+        const int kstep = r.gu ? 1 : 2;
+        for (int kb = r.kb0; kb < r.kb1; kb += kstep, ++it) {
+          const int s = it % S;
+          const int nk = min(kstep, r.kb1 - kb);
+          if (!h_ok && npend == S && !resolve()) { ok = false; break; }
+          if (it >= (uint32_t)S && !mbar_wait(&empty_bar[s], ((it / S) - 1) & 1)) { ok = false; break; }
+          if (abort_sh) { ok = false; break; }
+          uint8_t* st = smem + (size_t)s * stage_bytes;
+          const uint32_t wb = r.gu ? 2 * kTileBytes : (uint32_t)nk * kTileBytes;
+          mbar_expect_tx(&full_bar[s], wb + (uint32_t)nk * b_bytes);
+          bulk_load(st, wbase + (size_t)kb * (r.gu ? 2 * kTileBytes : kTileBytes), wb, &full_bar[s]);
+          if (r.gu) {
+            tma_load_3d(st + 2 * kTileBytes, &map_x, &full_bar[s], kb * BK, 0, 0);
+          } else if (h_ok) {
+            for (int j = 0; j < nk; ++j)
+              tma_load_3d(st + 2 * kTileBytes + j * b_bytes, &map_h, &full_bar[s], (kb + j) * BK, 0, r.u);
+          } else {
+            pend_s[npend] = s;
+            pend_kb[npend] = kb;
+            pend_nk[npend] = nk;
+            ++npend;
           }
         }
+        if (ok && npend > 0 && !resolve()) ok = false;
       }
-      if (ok && !h_ready && !resolve_h()) ok = false;   // every CTA waits for barrier B once
       if (!ok) {
         set_status(a.status, MOE_ERR_TIMEOUT);
         abort_sh = 1;
       }
+      // drain: the last fill of every stage must have landed before the CTA exits
       const uint32_t issued = it;
       for (int s = 0; s < S; ++s) {
         if ((uint32_t)s < issued) {
@@ -748,41 +829,48 @@ tc_fused_decode_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
+      const FSched sc = fused_sched(a, f, G);
       uint32_t it = 0;
       int local = 0;
       bool ok = true;
-      for (int ph = 0; ph < 3 && ok; ++ph) {
-        const bool gu = ph < 2;
-        const Plan pl = gu ? phase_plan<kModeGateUp>(a, f, ph, gridDim.x) : phase_plan<kModeDown>(a, f, ph, gridDim.x);
-        Args aa = a;
-        if (gu) { aa.sel = f.sel[ph]; aa.sel_count = f.sel_count[ph]; }
-        const uint32_t a_bytes = gu ? 2 * kTileBytes : kTileBytes;
-        for (int unit = blockIdx.x; unit < pl.units && ok; unit += gridDim.x, ++local) {
-          const UnitRange r = gu ? unit_range<kModeGateUp>(pl, aa, unit) : unit_range<kModeDown>(pl, aa, unit);
-          const int buf = local % nbuf, use = local / nbuf;
-          if (use > 0 && !mbar_wait(&tempty_bar[buf], (use - 1) & 1)) { ok = false; break; }
+      for (int g = blockIdx.x; g < sc.total && ok; g += G, ++local) {
+        const FUnit r = fused_unit(sc, f, g);
+        const int buf = local % nbuf, use = local / nbuf;
+        if (use > 0 && !mbar_wait(&tempty_bar[buf], (use - 1) & 1)) { ok = false; break; }
+        fence_after();
+        const uint32_t dacc = tmem + (uint32_t)buf * acc_cols;
+        uint32_t acc = 0;
+        const int kstep = r.gu ? 1 : 2;
+        for (int kb = r.kb0; kb < r.kb1; kb += kstep, ++it) {
+          const int s = it % S;
+          if (!mbar_wait(&full_bar[s], (it / S) & 1) || abort_sh) { ok = false; break; }
           fence_after();
-          const uint32_t dacc = tmem + (uint32_t)buf * acc_cols;
-          uint32_t acc = 0;
-          for (int u = r.u0; u < r.u1 && ok; ++u) {
-            for (int kb = r.kb0; kb < r.kb1; ++kb, ++it) {
-              const int s = it % S;
-              if (!mbar_wait(&full_bar[s], (it / S) & 1) || abort_sh) { ok = false; break; }
-              fence_after();
-              const uint32_t base = smem_u32(smem + (size_t)s * stage_bytes);
-              const uint64_t da = desc_sw128(base);
-              const uint64_t db = desc_sw128(base + a_bytes);
+          const uint32_t base = smem_u32(smem + (size_t)s * stage_bytes);
+          if (r.gu) {
+            const uint64_t da = desc_sw128(base);
+            const uint64_t db = desc_sw128(base + 2 * kTileBytes);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              // advance 16 bf16 = 32 bytes along K inside the swizzle atom
+              mma_bf16(dacc, da + 2 * kk, db + 2 * kk, idesc, acc);
+              mma_bf16(dacc + N, da + (kTileBytes >> 4) + 2 * kk, db + 2 * kk, idesc, acc);
+              acc = 1;
+            }
+          } else {
+            const int nk = min(2, r.kb1 - kb);
+            for (int j = 0; j < nk; ++j) {
+              const uint64_t da = desc_sw128(base + j * kTileBytes);
+              const uint64_t db = desc_sw128(base + 2 * kTileBytes + j * b_bytes);
 #pragma unroll
               for (int kk = 0; kk < BK / 16; ++kk) {
                 mma_bf16(dacc, da + 2 * kk, db + 2 * kk, idesc, acc);
-                if (gu) mma_bf16(dacc + N, da + (kTileBytes >> 4) + 2 * kk, db + 2 * kk, idesc, acc);
                 acc = 1;
               }
-              mma_commit(&empty_bar[s]);
             }
           }
-          if (ok) mma_commit(&tfull_bar[buf]);
+          mma_commit(&empty_bar[s]);
         }
+        if (ok) mma_commit(&tfull_bar[buf]);
       }
       if (!ok) {
         set_status(a.status, MOE_ERR_TIMEOUT);
@@ -793,61 +881,70 @@ tc_fused_decode_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
     }
   } else if (warp < kThreads / 32) {
     // ------------------------------------------------------------- epilogue (warps 2..5)
+    // Every epilogue warp runs the same units and reaches every named barrier,
+    // even after a timeout, so no warp is left waiting.
+    const FSched sc = fused_sched(a, f, G);
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const uint32_t trow0 = tmem + ((uint32_t)(q * 32) << 16);
+    const int cols = sc.cols;
     int local = 0;
-    for (int ph = 0; ph < 3; ++ph) {
-      const bool gu = ph < 2;
-      if (ph == 2) {
-        // every gate/up epilogue of this CTA is done: tell the grid (barrier B)
-        __threadfence();
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (warp == 2 && lane == 0) grid_arrive(&f.grid_bar[1]);
+    for (int g = blockIdx.x; g < sc.total; g += G, ++local) {
+      const FUnit r = fused_unit(sc, f, g);
+      const int buf = local % nbuf;
+      const uint32_t trow = trow0 + (uint32_t)buf * acc_cols;
+      bool live = !abort_sh;
+      if (live && !mbar_wait(&tfull_bar[buf], (local / nbuf) & 1)) {
+        set_status(a.status, MOE_ERR_TIMEOUT);
+        abort_sh = 1;
+        live = false;
       }
-      const Plan pl = gu ? phase_plan<kModeGateUp>(a, f, ph, gridDim.x) : phase_plan<kModeDown>(a, f, ph, gridDim.x);
-      Args aa = a;
-      if (gu) { aa.sel = f.sel[ph]; aa.sel_count = f.sel_count[ph]; }
-      for (int unit = blockIdx.x; unit < pl.units; unit += gridDim.x, ++local) {
-        const UnitRange r = gu ? unit_range<kModeGateUp>(pl, aa, unit) : unit_range<kModeDown>(pl, aa, unit);
-        const int buf = local % nbuf;
-        const uint32_t trow = trow0 + (uint32_t)buf * acc_cols;
-        bool live = !abort_sh;
-        if (live && !mbar_wait(&tfull_bar[buf], (local / nbuf) & 1)) {
-          set_status(a.status, MOE_ERR_TIMEOUT);
-          abort_sh = 1;
-          live = false;
-        }
-        if (live) fence_after();
+      if (live) fence_after();
+      if (r.gu) {
+        // ------------------------------ gate/up: h[u][t][m] = w(u,t) SiLU(g) u
         const int m = r.mt * BM + row;
-        if (pl.splits == 1) {
-          if (!live) continue;
-          for (int c0 = 0; c0 < N; c0 += 16) {
-            float d0[16], d1[16];
-            tmem_ld16(trow + c0, d0);
-            if (gu) {
-              tmem_ld16(trow + N + c0, d1);
-              store_chunk<kModeGateUp>(a, r, m, c0, d0, d1, 0, 0);
-            } else {
-              store_chunk<kModeDown>(a, r, m, c0, d0, d1, 0, 0);
-            }
+        const float* wrow = a.wmat + (size_t)r.u * N;
+        uint16_t* hrow = a.hbuf + (size_t)r.u * N * a.I + m;
+        auto store_h = [&](int c0, const float* g16, const float* u16) {
+          if (m >= a.I) return;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int t = c0 + j;
+            const float wgt = t < a.T ? wrow[t] : 0.f;
+            const float hv = wgt != 0.f ? wgt * silu(g16[j]) * u16[j] : 0.f;
+            hrow[(size_t)t * a.I] = f32_to_bf16_rn(hv);
           }
-          fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tempty_bar[buf]);
-        } else {
-          const int nacc = gu ? 2 : 1;
-          float* part = f.partial[ph];
+        };
+        bool done_h = false;   // this CTA wrote the finished h tile
+        if (sc.sg == 1) {
           if (live) {
-            float* mine = part + ((size_t)r.tile * pl.splits + r.split) * nacc * N * BM;
             for (int c0 = 0; c0 < N; c0 += 16) {
               float d0[16], d1[16];
               tmem_ld16(trow + c0, d0);
-              if (gu) tmem_ld16(trow + N + c0, d1);
+              tmem_ld16(trow + N + c0, d1);
+              store_h(c0, d0, d1);
+            }
+            fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+            done_h = true;
+          }
+        } else {
+          // split partial [2][row][cols]: gate then up, this thread's row contiguous
+          const size_t tile = (size_t)r.u * sc.mt_i + r.mt;
+          const size_t pstride = (size_t)2 * BM * cols;
+          if (live) {
+            float* mine = f.gu_partial + (tile * sc.sg + r.sp) * pstride + (size_t)row * cols;
+            for (int c0 = 0; c0 < N; c0 += 16) {
+              float d0[16], d1[16];
+              tmem_ld16(trow + c0, d0);
+              tmem_ld16(trow + N + c0, d1);
 #pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                mine[(size_t)(c0 + j) * BM + row] = d0[j];
-                if (gu) mine[(size_t)N * BM + (size_t)(c0 + j) * BM + row] = d1[j];
+              for (int j = 0; j < 16; j += 4) {
+                if (c0 + j < cols) {
+                  st_f4(mine + c0 + j, d0[j], d0[j + 1], d0[j + 2], d0[j + 3]);
+                  st_f4(mine + (size_t)BM * cols + c0 + j, d1[j], d1[j + 1], d1[j + 2], d1[j + 3]);
+                }
               }
             }
             fence_before();
@@ -859,77 +956,148 @@ tc_fused_decode_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
           if (warp == 2 && lane == 0) {
             last_sh = 0;
             if (!abort_sh) {
-              const int old = atomicAdd(&f.counters[ph][r.tile], 1);
-              if (old == pl.splits - 1) {
+              const int old = atomicAdd(&f.gu_cnt[tile], 1);
+              if (old == sc.sg - 1) {
                 last_sh = 1;
-                f.counters[ph][r.tile] = 0;
+                f.gu_cnt[tile] = 0;
               }
             }
           }
           asm volatile("bar.sync 1, 128;" ::: "memory");
           if (last_sh && live) {
             __threadfence();
-            const float* base = part + (size_t)r.tile * pl.splits * nacc * N * BM;
+            const float* base = f.gu_partial + tile * sc.sg * pstride + (size_t)row * cols;
             for (int c0 = 0; c0 < N; c0 += 16) {
               float s0[16], s1[16];
 #pragma unroll
               for (int j = 0; j < 16; ++j) { s0[j] = 0.f; s1[j] = 0.f; }
-              for (int sp = 0; sp < pl.splits; ++sp) {
-                const float* pt = base + (size_t)sp * nacc * N * BM + (size_t)c0 * BM + row;
-                float v0[16], v1[16];
+              // 4 columns at a time: every split's gate and up values in flight, added in split order
 #pragma unroll
-                for (int j = 0; j < 16; ++j) v0[j] = __ldcg(pt + (size_t)j * BM);
-                if (gu) {
+              for (int h4 = 0; h4 < 16; h4 += 4) {
+                if (c0 + h4 >= cols) continue;
+                float4 v0[8], v1[8];
 #pragma unroll
-                  for (int j = 0; j < 16; ++j) v1[j] = __ldcg(pt + (size_t)N * BM + (size_t)j * BM);
+                for (int b = 0; b < 8; ++b) {
+                  if (b < sc.sg) {
+                    const float* pt = base + (size_t)b * pstride + c0 + h4;
+                    v0[b] = __ldcg(reinterpret_cast<const float4*>(pt));
+                    v1[b] = __ldcg(reinterpret_cast<const float4*>(pt + (size_t)BM * cols));
+                  }
                 }
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                  s0[j] += v0[j];
-                  if (gu) s1[j] += v1[j];
+                for (int b = 0; b < 8; ++b) {
+                  if (b < sc.sg) {
+                    float* a0 = s0 + h4;
+                    float* a1 = s1 + h4;
+                    a0[0] += v0[b].x; a0[1] += v0[b].y; a0[2] += v0[b].z; a0[3] += v0[b].w;
+                    a1[0] += v1[b].x; a1[1] += v1[b].y; a1[2] += v1[b].z; a1[3] += v1[b].w;
+                  }
                 }
               }
-              if (gu) store_chunk<kModeGateUp>(a, r, m, c0, s0, s1, 0, 0);
-              else store_chunk<kModeDown>(a, r, m, c0, s0, s1, 0, 0);
+              store_h(c0, s0, s1);
             }
+            done_h = true;
           }
-          asm volatile("bar.sync 1, 128;" ::: "memory");
+        }
+        // publish: this entry has one more finished gate/up tile
+        if (done_h) __threadfence();
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (warp == 2 && lane == 0 && done_h && !abort_sh) release_add(&f.hready[r.u]);
+      } else {
+        // ------------------------------ down: this entry's partial [row][cols]
+        if (live) {
+          float* mine = f.dn_partial + (((size_t)r.u * sc.mt_h + r.mt) * sc.sd + r.sp) * ((size_t)BM * cols) +
+                        (size_t)row * cols;
+          for (int c0 = 0; c0 < cols; c0 += 16) {
+            float d0[16];
+            tmem_ld16(trow + c0, d0);
+#pragma unroll
+            for (int j = 0; j < 16; j += 4)
+              if (c0 + j < cols) st_f4(mine + c0 + j, d0[j], d0[j + 1], d0[j + 2], d0[j + 3]);
+          }
+          fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty_bar[buf]);
         }
       }
     }
+    __threadfence();   // this thread's partials, before the CTA reports them written
   } else {
-    // ------------------------------------------------------------- copy warps (6..9)
+    // ------------------------------------------------------------- copy warps (6, 7)
+    // Job by job: this CTA's slice of each record, then one release per job.
     const uint32_t n = (uint32_t)*f.n_jobs;
-    const uint32_t total = n * f.rec16;
-    const uint32_t stride = gridDim.x * (32u * kCopyWarps);
+    const uint32_t stride = (uint32_t)G * (32u * kCopyWarps);
     const uint32_t ctid = (uint32_t)(warp - kThreads / 32) * 32u + lane;
     constexpr int CU = 16;   // loads in flight per copy thread
-    for (uint32_t base = blockIdx.x * (32u * kCopyWarps) + ctid; base < total; base += stride * CU) {
-      uint4 v[CU];
-      uint4* dst[CU];
+    for (uint32_t j = 0; j < n; ++j) {
+      const uint4* src = reinterpret_cast<const uint4*>(f.jobs[j].src);
+      uint4* dst = reinterpret_cast<uint4*>(f.jobs[j].dst);
+      for (uint32_t base = blockIdx.x * (32u * kCopyWarps) + ctid; base < f.rec16; base += stride * CU) {
+        uint4 v[CU];
 #pragma unroll
-      for (int u = 0; u < CU; ++u) {
-        const uint32_t idx = base + (uint32_t)u * stride;
-        dst[u] = nullptr;
-        if (idx < total) {
-          const uint32_t j = (uint32_t)__umul64hi((unsigned long long)idx, f.magic);
-          const uint32_t c = idx - j * f.rec16;
-          v[u] = __ldcs(reinterpret_cast<const uint4*>(f.jobs[j].src) + c);
-          dst[u] = reinterpret_cast<uint4*>(f.jobs[j].dst) + c;
+        for (int u = 0; u < CU; ++u) {
+          const uint32_t idx = base + (uint32_t)u * stride;
+          if (idx < f.rec16) v[u] = __ldcs(src + idx);
+        }
+#pragma unroll
+        for (int u = 0; u < CU; ++u) {
+          const uint32_t idx = base + (uint32_t)u * stride;
+          if (idx < f.rec16) __stcs(dst + idx, v[u]);
         }
       }
-#pragma unroll
-      for (int u = 0; u < CU; ++u)
-        if (dst[u]) __stcs(dst[u], v[u]);
+      __threadfence();
+      asm volatile("bar.sync 2, %0;" ::"n"(32 * kCopyWarps) : "memory");
+      if (warp == kThreads / 32 && lane == 0) release_add(&f.jdone[j]);
     }
-    __threadfence();
-    asm volatile("bar.sync 2, %0;" ::"n"(32 * kCopyWarps) : "memory");
-    if (warp == kThreads / 32 && lane == 0) grid_arrive(&f.grid_bar[0]);
   }
   fence_before();
   __syncthreads();
   fence_after();
   if (warp == 1) tmem_dealloc(tmem, ncols);
+
+  // ---- combine: once every CTA's down partials are written, all threads of all
+  // CTAs sum them element-parallel, each element over (entry, split) in order
+  if (threadIdx.x == 0) {
+    last_sh = 0;
+    if (!abort_sh) {
+      release_add(f.dn_done);
+      last_sh = wait_count(f.dn_done, (uint32_t)G, a.status) ? 1 : 0;
+      if (!last_sh) set_status(a.status, MOE_ERR_TIMEOUT);
+    }
+  }
+  __syncthreads();
+  if (last_sh) {
+    __threadfence();
+    const FSched sc = fused_sched(a, f, G);
+    const int cols = sc.cols;
+    const size_t tile_el = (size_t)BM * cols;
+    const size_t total_el = (size_t)sc.mt_h * tile_el;
+    const size_t ustride = (size_t)sc.mt_h * sc.sd * tile_el;
+    const int parts = sc.n * sc.sd;
+    for (size_t e0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e0 < total_el; e0 += (size_t)G * blockDim.x) {
+      const int mt = (int)(e0 / tile_el);
+      const size_t rem = e0 - (size_t)mt * tile_el;
+      const int rw = (int)(rem / cols), t = (int)(rem - (size_t)rw * cols);
+      const int m = mt * BM + rw;
+      if (t >= a.T || m >= a.H) continue;
+      const float* base = f.dn_partial + (size_t)mt * sc.sd * tile_el + rem;
+      float acc = 0.f;
+      for (int p0 = 0; p0 < parts; p0 += 32) {
+        float v[32];
+#pragma unroll
+        for (int b = 0; b < 32; ++b) {
+          if (p0 + b < parts) {
+            const int u = (p0 + b) / sc.sd, sp = (p0 + b) - u * sc.sd;
+            v[b] = __ldcg(base + (size_t)u * ustride + (size_t)sp * tile_el);
+          }
+        }
+#pragma unroll
+        for (int b = 0; b < 32; ++b)
+          if (p0 + b < parts) acc += v[b];
+      }
+      a.out[(size_t)t * a.H + m] = f32_to_bf16_rn(acc);
+    }
+  }
 }
 
 // ----------------------------------------------------------------- gather / combine (T > 256)
@@ -1042,10 +1210,21 @@ void tc_maps_destroy(TcMaps* m) { delete m; }
 
 int tc_npad(int T) { return (T + 15) / 16 * 16; }
 
-// Three equal regions (one per phase of the fused kernel); the unfused kernels use the first.
-size_t tc_partial_floats(const PoolDev& p, const Scratch& sc) {
-  (void)p;
-  return (size_t)3 * 4 * sm_count() * 2 * sc.npad_max * tc::BM;
+// Gate/up split partials: up to 8 splits of every (entry, 128-row tile), capped at 64 MB.
+size_t tc_partial_floats(const PoolDev& p, int npad_max) {
+  const size_t need = (size_t)(p.E + 1) * ((p.I + 127) / 128) * 8 * 2 * npad_max * tc::BM;
+  return std::min(need, (size_t)16 << 20);
+}
+
+// Per-entry down partials: one split always fits; up to 4 within 64 MB.
+size_t tc_dn_partial_floats(const PoolDev& p, int npad_max) {
+  const size_t one = (size_t)(p.E + 1) * ((p.H + 127) / 128) * npad_max * tc::BM;
+  return std::max(one, std::min(4 * one, (size_t)16 << 20));
+}
+
+// [gu_cnt: (E+1) * MT_I][dn_done (+ MT_H - 1 spare)][hready: E+1][jdone: E+1]
+int tc_ffn_sync_ints(const PoolDev& p) {
+  return (p.E + 1) * ((p.I + 127) / 128) + (p.H + 127) / 128 + 2 * (p.E + 1);
 }
 
 static tc::Args tc_args(const PoolDev& p, const Scratch& sc, int T, int N) {
@@ -1070,35 +1249,10 @@ static tc::Args tc_args(const PoolDev& p, const Scratch& sc, int T, int N) {
   a.hbuf = sc.hbuf;
   a.out = nullptr;
   a.partial = sc.partial;
-  a.counters = sc.counters;
+  a.counters = sc.ffn_sync;
   a.status = p.status;
-  a.max_split_units = (int)(tc_partial_floats(p, sc) / 3 / ((size_t)2 * N * tc::BM));
+  a.max_split_units = 0;
   return a;
-}
-
-int launch_tc_gate_up(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, const void* x, int sel,
-                      cudaStream_t s) {
-  (void)m;
-  tc::Args a = tc_args(p, sc, T, tc_npad(T));
-  if (sel >= 0) {
-    a.sel = sc.elist + (size_t)sel * (p.E + 1);
-    a.sel_count = sc.ecount + sel;
-  }
-  CUtensorMap xm;   // x [T][H] as a 3-D map with one "record"
-  if (!tc::make_map_3d(&xm, x, (uint64_t)p.H, (uint64_t)T, 1, (uint64_t)p.H * 2, (uint64_t)p.H * 2 * T, a.N))
-    return -1;
-  return tc::launch_mode<tc::kModeGateUp>(a, xm, s);
-}
-
-int launch_tc_down(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, void* out, cudaStream_t s) {
-  (void)m;
-  tc::Args a = tc_args(p, sc, T, tc_npad(T));
-  a.out = static_cast<uint16_t*>(out);
-  a.max_split_units = (int)(tc_partial_floats(p, sc) / 3 / ((size_t)1 * a.N * tc::BM));
-  CUtensorMap hm;   // hbuf [E+1][N][I]
-  const uint64_t I = p.I, N = a.N;
-  if (!tc::make_map_3d(&hm, sc.hbuf, I, N, (uint64_t)p.E + 1, I * 2, N * I * 2, a.N)) return -1;
-  return tc::launch_mode<tc::kModeDown>(a, hm, s);
 }
 
 // Gather path: xp = x rows by expert; h = gate/up per row; y = down per row; out = combine.
@@ -1135,7 +1289,7 @@ int launch_tc_fused_decode(const PoolDev& p, const Scratch& sc, const TcMaps* m,
   const int N = tc_npad(T);
   tc::Args a = tc_args(p, sc, T, N);
   a.out = static_cast<uint16_t*>(out);
-  a.stages = tc::stages_for(2, N);
+  a.stages = std::min<int>(tc::kMaxStages, (int)(tc::kSmemBudget / tc::fused_stage_bytes(N)));
   CUtensorMap xm, hm;
   if (!tc::make_map_3d(&xm, x, (uint64_t)p.H, (uint64_t)T, 1, (uint64_t)p.H * 2, (uint64_t)p.H * 2 * T, N)) return -1;
   const uint64_t I = p.I;
@@ -1144,26 +1298,25 @@ int launch_tc_fused_decode(const PoolDev& p, const Scratch& sc, const TcMaps* m,
   f.jobs = sc.copies;
   f.n_jobs = sc.n_copy;
   f.rec16 = (uint32_t)(p.lay.rec / 16);
-  f.magic = ~0ull / f.rec16 + 1ull;
-  f.grid_bar = sc.grid_bar;
-  for (int ph = 0; ph < 2; ++ph) {
-    f.sel[ph] = sc.elist + (size_t)ph * (p.E + 1);
-    f.sel_count[ph] = sc.ecount + ph;
-  }
-  const size_t region = tc_partial_floats(p, sc) / 3;
-  const size_t ctiles = sc.n_counters / 3;
-  for (int ph = 0; ph < 3; ++ph) {
-    f.partial[ph] = sc.partial + region * ph;
-    f.counters[ph] = sc.counters + ctiles * ph;
-  }
-  for (int ph = 0; ph < 3; ++ph) f.max_split_units[ph] = (int)(region / ((size_t)(ph < 2 ? 2 : 1) * N * tc::BM));
+  f.elist = sc.elist;
+  f.ecount = sc.ecount;
+  f.E1 = p.E + 1;
+  f.gu_partial = sc.partial;
+  f.gu_partial_floats = sc.partial_floats;
+  f.dn_partial = sc.dn_partial;
+  f.dn_partial_floats = sc.dn_partial_floats;
+  const int mt_i = (p.I + 127) / 128, mt_h = (p.H + 127) / 128;
+  f.gu_cnt = sc.ffn_sync;
+  f.dn_done = reinterpret_cast<uint32_t*>(sc.ffn_sync + (size_t)(p.E + 1) * mt_i);
+  f.hready = f.dn_done + mt_h;
+  f.jdone = f.hready + (p.E + 1);
   static bool configured = false;
   if (!configured) {
     cudaFuncSetAttribute(tc::tc_fused_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          tc::kSmemBudget + 1024);
     configured = true;
   }
-  const size_t smem = (size_t)a.stages * (((2 * tc::BM * tc::BK * 2 + N * tc::BK * 2) + 1023) & ~1023) + 1024;
+  const size_t smem = (size_t)a.stages * tc::fused_stage_bytes(N) + 1024;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sm_count());
   cfg.blockDim = dim3(tc::kFusedThreads);

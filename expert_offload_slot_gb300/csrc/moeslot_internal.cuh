@@ -93,10 +93,12 @@ struct Scratch {
   int32_t npad_max;   // largest padded token count of that path (<= 256)
   float* wmat;        // [E+1][npad] routing weight of each token for each work entry (0 if not routed)
   uint16_t* hbuf;     // [E+1][npad][I] bf16: w * SiLU(g) * u
-  float* partial;     // split-reduce partial tiles
-  int32_t* counters;  // per-tile arrival counters (self-resetting), 3 regions
-  size_t n_counters;
-  uint32_t* grid_bar; // [2] flip-bit grid barriers of the fused decode kernel
+  float* partial;     // gate/up split partials
+  size_t partial_floats;
+  float* dn_partial;  // per-entry down partials of the fused decode kernel
+  size_t dn_partial_floats;
+  int32_t* ffn_sync;  // arrival counters and readiness flags of the fused decode kernel,
+  int32_t n_ffn_sync; // zeroed by the plan kernel before every expert launch
   int32_t* elist;     // [2][E+1]: work entries already resident / copied this step
   int32_t* ecount;    // [2]
   // tensor-core gather path (T > npad_max)
@@ -156,11 +158,10 @@ struct TcMaps;                      // host-side tensor maps of a pool (k_tc.cu)
 TcMaps* tc_maps_create(const PoolDev& p, const Scratch& sc);
 void tc_maps_destroy(TcMaps* m);
 int tc_npad(int T);                 // padded token count (multiple of 16)
-size_t tc_partial_floats(const PoolDev& p, const Scratch& sc);   // size of Scratch::partial
-// sel: 0 = resident entries, 1 = entries copied this step, -1 = all
-int launch_tc_gate_up(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, const void* x, int sel,
-                      cudaStream_t s);
-int launch_tc_down(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, void* out, cudaStream_t s);
+// scratch sizes for a pool whose dense path takes up to npad_max token columns
+size_t tc_partial_floats(const PoolDev& p, int npad_max);      // Scratch::partial
+size_t tc_dn_partial_floats(const PoolDev& p, int npad_max);   // Scratch::dn_partial
+int tc_ffn_sync_ints(const PoolDev& p);                         // Scratch::ffn_sync
 int launch_tc_gather(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, const void* x, void* out,
                      cudaStream_t s);
 int launch_tc_fused_decode(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, const void* x, void* out,

@@ -65,6 +65,28 @@ def test_all_resident_pool_equals_offloaded_pool():
             r.close()
 
 
+def test_tensor_core_output_independent_of_resident_set():
+    """bf16 tensor-core path, sizes where many entries share the grid: the output of a step is the
+    same bits whether all, some or few of its experts were resident (misses copied in-kernel)."""
+    wl = variant(get_workload("qwen3_decode"), name="resident_set", L=2, E=64, k=8, H=1024, I=512)
+    rigs = [Rig(wl, S=wl.L * wl.E, lut=np.arange(wl.L * wl.E, dtype=np.int32).reshape(wl.L, wl.E)),
+            Rig(wl, S=wl.L * wl.E // 3), Rig(wl, S=6)]
+    try:
+        for l in range(wl.L):
+            xs = gen.store_act(wl, gen.decode_hidden(wl, l, 16, 4))
+            for t in range(4):
+                outs = [r.forward(l, xs[t]) for r in rigs]
+                for o in outs[1:]:
+                    assert np.array_equal(outs[0], o)
+            ref, _ = rigs[0].oracle_forward(l, xs[3])
+            check_output(wl, outs[0], ref)
+        assert rigs[0].pool.stats()["misses"] == 0
+        assert rigs[1].pool.stats()["misses"] > 0 and rigs[2].pool.stats()["bypass"] > 0
+    finally:
+        for r in rigs:
+            r.close()
+
+
 def test_load_slot_matches_oracle_and_keeps_output():
     wl = variant(get_workload("qwen3_decode"), name="loadslot", L=2, E=16, k=2, H=256, I=256)
     rig = Rig(wl, S=6)
