@@ -579,7 +579,9 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap map_b, Args a) {
 // meanwhile two copy warps per CTA pull this step's misses from the mapped
 // host pool (NVLink-C2C reads) into their records, one job after another.  A
 // unit waits only for what it reads: a copied record (jdone[job] == G: every
-// CTA's slice of that job is written) or the complete h of its entry
+// CTA's slice of that job is written) or the complete h of its entry.  (Finer
+// readiness within a job costs the copy warps a fence per part, which slows the
+// link-bound copy more than it shortens the tail.)
 // (hready[u] == the entry's gate/up tiles).  So the resident experts' whole FFN
 // overlaps the link-bound copies.
 // A down unit covers one entry: it writes an fp32 partial tile, and the last
@@ -590,13 +592,14 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap map_b, Args a) {
 // Partial tiles are row-major ([128 rows][columns]) so that each epilogue
 // thread (one row) moves its columns with 16-byte accesses.
 constexpr int kCopyWarps = 2;
+constexpr int kCopyUnroll = 16;  // 16-byte host reads in flight per copy lane
 constexpr int kFusedThreads = kThreads + 32 * kCopyWarps;
 constexpr int kFusedBufs = 8;
 
 struct FusedArgs {
   const CopyJob* jobs;
   const int32_t* n_jobs;
-  uint32_t rec16;               // record bytes / 16
+  uint32_t tile16;              // tile data of a record (w13 then w2), in 16 B units
   const int32_t* elist;         // [2][E1]: resident entries, copied entries (work positions, ascending)
   const int32_t* ecount;        // [2]
   int E1;                       // E + 1
@@ -716,6 +719,7 @@ tc_fused_decode_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
   __shared__ __align__(8) uint64_t tfull_bar[kFusedBufs], tempty_bar[kFusedBufs], drain_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_sh, last_sh;
+  __shared__ FSched sched_sh;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -746,6 +750,7 @@ tc_fused_decode_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
     mbar_init(&drain_bar, 1);
     abort_sh = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    sched_sh = fused_sched(a, f, G);   // the unit decomposition, identical in every role and CTA
   }
   if (warp == 1) tmem_alloc(&tmem_base_sh, ncols);
   fence_before();
@@ -757,7 +762,7 @@ tc_fused_decode_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
   if (warp == 0) {
     // ------------------------------------------------------------- producer
     if (lane == 0) {
-      const FSched sc = fused_sched(a, f, G);
+      const FSched sc = sched_sh;
       uint32_t it = 0;
       bool ok = true;
       int pend_s[kMaxStages], pend_kb[kMaxStages], pend_nk[kMaxStages];
@@ -765,7 +770,7 @@ tc_fused_decode_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
         const FUnit r = fused_unit(sc, f, g);
         if (r.miss) {
           // a copied record: every CTA's slice of its job must have landed (down units
-          // too: their weight tiles are issued before h is complete)
+          // too: their weight tiles go out before h is complete)
           if (!wait_count(&f.jdone[r.li], (uint32_t)G, a.status)) { ok = false; break; }
           asm volatile("fence.proxy.async.global;" ::: "memory");   // generic writes -> bulk-copy reads
         }
@@ -829,7 +834,7 @@ tc_fused_decode_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const FSched sc = fused_sched(a, f, G);
+      const FSched sc = sched_sh;
       uint32_t it = 0;
       int local = 0;
       bool ok = true;
@@ -883,7 +888,7 @@ tc_fused_decode_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
     // ------------------------------------------------------------- epilogue (warps 2..5)
     // Every epilogue warp runs the same units and reaches every named barrier,
     // even after a timeout, so no warp is left waiting.
-    const FSched sc = fused_sched(a, f, G);
+    const FSched sc = sched_sh;
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const uint32_t trow0 = tmem + ((uint32_t)(q * 32) << 16);
@@ -1024,25 +1029,24 @@ tc_fused_decode_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
     __threadfence();   // this thread's partials, before the CTA reports them written
   } else {
     // ------------------------------------------------------------- copy warps (6, 7)
-    // Job by job: this CTA's slice of each record, then one release per job.
+    // Job by job: this CTA's slice of each record's tile data, then one release per job.
     const uint32_t n = (uint32_t)*f.n_jobs;
     const uint32_t stride = (uint32_t)G * (32u * kCopyWarps);
     const uint32_t ctid = (uint32_t)(warp - kThreads / 32) * 32u + lane;
-    constexpr int CU = 16;   // loads in flight per copy thread
     for (uint32_t j = 0; j < n; ++j) {
       const uint4* src = reinterpret_cast<const uint4*>(f.jobs[j].src);
       uint4* dst = reinterpret_cast<uint4*>(f.jobs[j].dst);
-      for (uint32_t base = blockIdx.x * (32u * kCopyWarps) + ctid; base < f.rec16; base += stride * CU) {
-        uint4 v[CU];
+      for (uint32_t base = blockIdx.x * (32u * kCopyWarps) + ctid; base < f.tile16; base += stride * kCopyUnroll) {
+        uint4 v[kCopyUnroll];
 #pragma unroll
-        for (int u = 0; u < CU; ++u) {
+        for (int u = 0; u < kCopyUnroll; ++u) {
           const uint32_t idx = base + (uint32_t)u * stride;
-          if (idx < f.rec16) v[u] = __ldcs(src + idx);
+          if (idx < f.tile16) v[u] = __ldcs(src + idx);
         }
 #pragma unroll
-        for (int u = 0; u < CU; ++u) {
+        for (int u = 0; u < kCopyUnroll; ++u) {
           const uint32_t idx = base + (uint32_t)u * stride;
-          if (idx < f.rec16) __stcs(dst + idx, v[u]);
+          if (idx < f.tile16) __stcs(dst + idx, v[u]);
         }
       }
       __threadfence();
@@ -1068,27 +1072,28 @@ tc_fused_decode_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
   __syncthreads();
   if (last_sh) {
     __threadfence();
-    const FSched sc = fused_sched(a, f, G);
-    const int cols = sc.cols;
-    const size_t tile_el = (size_t)BM * cols;
-    const size_t total_el = (size_t)sc.mt_h * tile_el;
+    const FSched sc = sched_sh;
+    const uint32_t cols = (uint32_t)sc.cols;
+    const uint32_t tile_el = (uint32_t)BM * cols;
+    const uint32_t total_el = (uint32_t)sc.mt_h * tile_el;
     const size_t ustride = (size_t)sc.mt_h * sc.sd * tile_el;
     const int parts = sc.n * sc.sd;
-    for (size_t e0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e0 < total_el; e0 += (size_t)G * blockDim.x) {
-      const int mt = (int)(e0 / tile_el);
-      const size_t rem = e0 - (size_t)mt * tile_el;
-      const int rw = (int)(rem / cols), t = (int)(rem - (size_t)rw * cols);
-      const int m = mt * BM + rw;
-      if (t >= a.T || m >= a.H) continue;
+    for (uint32_t e0 = blockIdx.x * blockDim.x + threadIdx.x; e0 < total_el; e0 += (uint32_t)G * blockDim.x) {
+      const uint32_t mt = e0 / tile_el;
+      const uint32_t rem = e0 - mt * tile_el;
+      const uint32_t rw = rem / cols, t = rem - rw * cols;
+      const uint32_t m = mt * BM + rw;
+      if (t >= (uint32_t)a.T || m >= (uint32_t)a.H) continue;
       const float* base = f.dn_partial + (size_t)mt * sc.sd * tile_el + rem;
       float acc = 0.f;
+      int u = 0, sp = 0;
       for (int p0 = 0; p0 < parts; p0 += 32) {
         float v[32];
 #pragma unroll
         for (int b = 0; b < 32; ++b) {
           if (p0 + b < parts) {
-            const int u = (p0 + b) / sc.sd, sp = (p0 + b) - u * sc.sd;
             v[b] = __ldcg(base + (size_t)u * ustride + (size_t)sp * tile_el);
+            if (++sp == sc.sd) { sp = 0; ++u; }
           }
         }
 #pragma unroll
@@ -1222,9 +1227,16 @@ size_t tc_dn_partial_floats(const PoolDev& p, int npad_max) {
   return std::max(one, std::min(4 * one, (size_t)16 << 20));
 }
 
+// tile data of a record (the w13 tiles, then the w2 tiles), in 16-byte units
+static uint32_t tile16(const PoolDev& p) {
+  const size_t kb_i = (p.I + 63) / 64, mt_h = (p.H + 127) / 128;
+  return (uint32_t)((p.lay.off2 + mt_h * kb_i * tc::kTileBytes) / 16);
+}
+
 // [gu_cnt: (E+1) * MT_I][dn_done (+ MT_H - 1 spare)][hready: E+1][jdone: E+1]
 int tc_ffn_sync_ints(const PoolDev& p) {
-  return (p.E + 1) * ((p.I + 127) / 128) + (p.H + 127) / 128 + 2 * (p.E + 1);
+  const int mt_i = (p.I + 127) / 128, mt_h = (p.H + 127) / 128;
+  return (p.E + 1) * mt_i + mt_h + 2 * (p.E + 1);
 }
 
 static tc::Args tc_args(const PoolDev& p, const Scratch& sc, int T, int N) {
@@ -1297,7 +1309,7 @@ int launch_tc_fused_decode(const PoolDev& p, const Scratch& sc, const TcMaps* m,
   tc::FusedArgs f;
   f.jobs = sc.copies;
   f.n_jobs = sc.n_copy;
-  f.rec16 = (uint32_t)(p.lay.rec / 16);
+  f.tile16 = tile16(p);
   f.elist = sc.elist;
   f.ecount = sc.ecount;
   f.E1 = p.E + 1;
