@@ -352,6 +352,7 @@ MOE_API moe_status moe_pool_create(const moe_config* cfg, const void* host_pool,
     PA(P->sc.dn_partial, P->sc.dn_partial_floats, 0);
     P->sc.n_ffn_sync = tc_ffn_sync_ints(d);
     PA(P->sc.ffn_sync, P->sc.n_ffn_sync, 0);
+    PA(P->sc.dsync, 64, 0);
     if ((size_t)tc_npad((int)Tm) > (size_t)np) {
       // gather path for calls with more tokens than the dense path takes
       PA(P->sc.inv, Tm * k, 0);
@@ -485,6 +486,24 @@ static moe_status run_layer(moe_pool* P, int layer, const void* x, int T, void* 
       cudaEventRecord(P->prof_ev[(size_t)layer * NB + i], s);
   };
   mark(0);
+  const bool tc = P->tc_maps != nullptr;                 // bf16 weights: tensor-core path
+  const bool use_tc = tc && tc_npad(T) <= sc.npad_max;   // dense token columns
+  const bool gather = tc && !use_tc;                     // expert-grouped token tiles
+  if (use_tc && !ids_in && !staged && tc_decode_layer_ok(d, sc, T)) {
+    // router, gate, plan, miss copies, gate/up, down and combine in one cooperative kernel
+    mark(1);
+    mark(2);
+    mark(3);
+    const int n = launch_tc_decode_layer(d, sc, P->tc_maps, layer, T, x, P->router_w, P->router_b, out, s);
+    if (n == -1) return fail(MOE_ERR_INVALID, "x must be 16-byte aligned for the tensor-core path");
+    if (n < 0) return fail(MOE_ERR_CUDA, "cooperative launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+    P->launches += n;
+    mark(4);
+    CUDA_TRY(cudaGetLastError());
+    P->last_T = T;
+    P->last_gap_valid = true;
+    return MOE_OK;
+  }
   if (!ids_in) {
     if (route_fused_ok(d, T)) {
       P->launches += launch_route_gate_fused(d, layer, x, T, P->router_w, P->router_b, sc, s);
@@ -495,9 +514,6 @@ static moe_status run_layer(moe_pool* P, int layer, const void* x, int T, void* 
   }
   mark(1);
   const int flags = staged ? (PLAN_HISTORY | PLAN_PERMUTE | PLAN_STAGED) : (PLAN_HISTORY | PLAN_CACHE | PLAN_PERMUTE);
-  const bool tc = P->tc_maps != nullptr;                 // bf16 weights: tensor-core path
-  const bool use_tc = tc && tc_npad(T) <= sc.npad_max;   // dense token columns
-  const bool gather = tc && !use_tc;                     // expert-grouped token tiles
   P->launches += launch_plan(d, sc, layer, T, ids, w, probs, gather ? (flags | PLAN_GATHER) : flags, region,
                              use_tc ? tc_npad(T) : 0, s);
   mark(2);
@@ -612,6 +628,9 @@ MOE_API moe_status moe_clear_status(moe_pool* P) {
   CUDA_TRY(cudaSetDevice(P->device));
   CUDA_TRY(cudaDeviceSynchronize());
   CUDA_TRY(cudaMemset(P->d.status, 0, sizeof(int32_t)));
+  // counters a timed-out launch may have left behind
+  if (P->sc.dsync) CUDA_TRY(cudaMemset(P->sc.dsync, 0, 64 * sizeof(uint32_t)));
+  if (P->sc.ticket) CUDA_TRY(cudaMemset(P->sc.ticket, 0, sizeof(int32_t)));
   return MOE_OK;
 }
 

@@ -8,26 +8,9 @@
 //     sigmoid-renorm sigma(z_j) / sum_topk sigma(z_i).  It also writes the
 //     per-expert probability (full softmax or sigmoid) used by the routing
 //     history, and the gap between the k-th and (k+1)-th logit.
-#include "moeslot_internal.cuh"
+#include "gate_body.cuh"
 
 namespace moeslot {
-
-template <typename AT> struct Vec16;
-template <> struct Vec16<float> {
-  static constexpr int C = 4;
-  __device__ __forceinline__ static void load(const float* p, float* v) {
-    float4 q = __ldg(reinterpret_cast<const float4*>(p));
-    v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
-  }
-};
-template <> struct Vec16<uint16_t> {   // bf16 bit patterns
-  static constexpr int C = 8;
-  __device__ __forceinline__ static void load(const uint16_t* p, float* v) {
-    uint4 q = __ldg(reinterpret_cast<const uint4*>(p));
-    v[0] = bf16lo(q.x); v[1] = bf16hi(q.x); v[2] = bf16lo(q.y); v[3] = bf16hi(q.y);
-    v[4] = bf16lo(q.z); v[5] = bf16hi(q.z); v[6] = bf16lo(q.w); v[7] = bf16hi(q.w);
-  }
-};
 
 constexpr int kRouteWarps = 8;   // experts per CTA (one per warp)
 constexpr int kRouteTok = 8;     // tokens per CTA row
@@ -86,7 +69,6 @@ int launch_route_logits(const PoolDev& p, int layer, const void* x, int T, const
 
 // ------------------------------------------------------------------ gate + top-k
 constexpr int kGateWarps = 8;
-constexpr int kMaxPerLane = 8;   // E <= 256
 
 __global__ void __launch_bounds__(kGateWarps * 32)
 gate_topk_kernel(const float* __restrict__ z, int T, int E, int k, int gating, int32_t* __restrict__ ids,
@@ -183,83 +165,6 @@ constexpr int kFusedRouteT = 32;
 constexpr int kFusedRouteThreads = 256;
 
 template <typename AT>
-__device__ __forceinline__ void gate_one_token(const float* __restrict__ z, int t, int E, int k, int gating,
-                                               int32_t* ids, float* w, float* probs, float* gap,
-                                               unsigned long long* stats, float* zsel_w) {
-  const int lane = threadIdx.x & 31;
-  float v[kMaxPerLane];
-  bool taken[kMaxPerLane];
-  float zmax = -INFINITY;
-#pragma unroll
-  for (int j = 0; j < kMaxPerLane; ++j) {
-    const int e = lane + 32 * j;
-    taken[j] = e >= E;
-    v[j] = e < E ? __ldcg(z + (size_t)t * E + e) : -INFINITY;
-    zmax = fmaxf(zmax, v[j]);
-  }
-  zmax = warp_max(zmax);
-  if (gating == MOE_GATE_SOFTMAX_RENORM) {
-    float part = 0.f, ex[kMaxPerLane];
-#pragma unroll
-    for (int j = 0; j < kMaxPerLane; ++j) {
-      ex[j] = taken[j] ? 0.f : expf(v[j] - zmax);
-      part += ex[j];
-    }
-    const float den = warp_sum(part);
-#pragma unroll
-    for (int j = 0; j < kMaxPerLane; ++j)
-      if (!taken[j]) probs[(size_t)t * E + lane + 32 * j] = ex[j] / den;
-  } else {
-#pragma unroll
-    for (int j = 0; j < kMaxPerLane; ++j)
-      if (!taken[j]) probs[(size_t)t * E + lane + 32 * j] = 1.f / (1.f + expf(-v[j]));
-  }
-  float next_best = INFINITY;
-  const int rounds = k < E ? k + 1 : k;
-  for (int r = 0; r < rounds; ++r) {
-    float bv = -INFINITY;
-    int be = 0x7fffffff;
-#pragma unroll
-    for (int j = 0; j < kMaxPerLane; ++j) {
-      const int e = lane + 32 * j;
-      if (!taken[j] && (v[j] > bv || (v[j] == bv && e < be))) { bv = v[j]; be = e; }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
-    }
-    if (r < k) {
-#pragma unroll
-      for (int j = 0; j < kMaxPerLane; ++j)
-        if (lane + 32 * j == be) taken[j] = true;
-      if (lane == 0) {
-        ids[(size_t)t * k + r] = be;
-        zsel_w[r] = bv;
-      }
-    } else {
-      next_best = bv;
-    }
-  }
-  __syncwarp();
-  const float zk = zsel_w[k - 1];
-  const float g = k < E ? zk - next_best : INFINITY;
-  if (lane == 0) {
-    gap[t] = g;
-    if (g < 1e-4f) atomicAdd(&stats[ST_NEAR_TIES], 1ull);
-  }
-  float num = 0.f;
-  if (lane < k) {
-    const float zj = zsel_w[lane];
-    num = gating == MOE_GATE_SOFTMAX_RENORM ? expf(zj - zmax) : 1.f / (1.f + expf(-zj));
-  }
-  const float den = warp_sum(num);
-  if (lane < k) w[(size_t)t * k + lane] = num / den;
-  __syncwarp();
-}
-
-template <typename AT>
 __global__ void __launch_bounds__(kFusedRouteThreads)
 route_gate_fused_kernel(const AT* __restrict__ x, const AT* __restrict__ wr, const float* __restrict__ b,
                         float* __restrict__ z, int T, int E, int H, int k, int gating, int32_t* ids, float* w,
@@ -320,7 +225,7 @@ route_gate_fused_kernel(const AT* __restrict__ x, const AT* __restrict__ wr, con
   if (!last) return;
   __threadfence();
   for (int t = warp; t < T; t += kFusedRouteThreads / 32)
-    gate_one_token<AT>(z, t, E, k, gating, ids, w, probs, gap, stats, zsel[warp]);
+    gate_one_token(z, t, E, k, gating, ids, w, probs, gap, stats, zsel[warp]);
 }
 
 int launch_route_gate_fused(const PoolDev& p, int layer, const void* x, int T, const void* router_w,

@@ -49,7 +49,9 @@
 #include <algorithm>
 #include <cstring>
 
+#include "gate_body.cuh"
 #include "moeslot_internal.cuh"
+#include "plan_body.cuh"
 
 namespace moeslot {
 
@@ -711,16 +713,21 @@ __device__ __forceinline__ void st_f4(float* p, float a, float b, float c, float
   *reinterpret_cast<float4*>(p) = make_float4(a, b, c, d);
 }
 
-__global__ void __launch_bounds__(kFusedThreads, 1)
-tc_fused_decode_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_h, Args a,
-                       FusedArgs f) {
+// The fused FFN of one layer call, run by every CTA of a cooperative grid of
+// kFusedThreads-thread CTAs; smem_raw: the CTA's dynamic shared memory.  pre()
+// runs on every thread between the CTA's setup (barriers, TMEM) and the first
+// read of the step's work lists, and returns false if they will not come.
+template <typename Pre>
+__device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUtensorMap* map_h_p, const Args& a,
+                                          const FusedArgs& f, uint8_t* smem_raw, Pre pre) {
+  const CUtensorMap& map_x = *map_x_p;
+  const CUtensorMap& map_h = *map_h_p;
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
   __shared__ __align__(8) uint64_t tfull_bar[kFusedBufs], tempty_bar[kFusedBufs], drain_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_sh, last_sh;
   __shared__ FSched sched_sh;
-  extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -750,12 +757,21 @@ tc_fused_decode_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
     mbar_init(&drain_bar, 1);
     abort_sh = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    sched_sh = fused_sched(a, f, G);   // the unit decomposition, identical in every role and CTA
   }
   if (warp == 1) tmem_alloc(&tmem_base_sh, ncols);
   fence_before();
   __syncthreads();
   fence_after();
+  const bool go = pre();
+  if (threadIdx.x == 0) {
+    if (go) {
+      sched_sh = fused_sched(a, f, G);   // the unit decomposition, identical in every role and CTA
+    } else {
+      sched_sh = FSched{};
+      abort_sh = 1;
+    }
+  }
+  __syncthreads();
   const uint32_t tmem = tmem_base_sh;
   const uint32_t idesc = idesc_bf16(N);
 
@@ -1030,7 +1046,7 @@ tc_fused_decode_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
   } else {
     // ------------------------------------------------------------- copy warps (6, 7)
     // Job by job: this CTA's slice of each record's tile data, then one release per job.
-    const uint32_t n = (uint32_t)*f.n_jobs;
+    const uint32_t n = go ? (uint32_t)*f.n_jobs : 0u;
     const uint32_t stride = (uint32_t)G * (32u * kCopyWarps);
     const uint32_t ctid = (uint32_t)(warp - kThreads / 32) * 32u + lane;
     for (uint32_t j = 0; j < n; ++j) {
@@ -1101,6 +1117,155 @@ tc_fused_decode_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
           if (p0 + b < parts) acc += v[b];
       }
       a.out[(size_t)t * a.H + m] = f32_to_bf16_rn(acc);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kFusedThreads, 1)
+tc_fused_decode_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_h, Args a,
+                       FusedArgs f) {
+  extern __shared__ uint8_t smem_raw[];
+  fused_ffn(&map_x, &map_h, a, f, smem_raw, [] { return true; });
+}
+
+
+// ----------------------------------------------------------------- decode layer kernel
+// A decode call with few tokens (T <= 32) and bf16 weights is one cooperative
+// launch: steps a1/a2 (router and gate), a3-a5/a7 (history, table, victims,
+// permutation) and the fused FFN (a6, a8, a9), without the launch gaps and
+// global round trips of three kernels.
+//   route: CTA (t, b), t < T, b < nblk, computes the logits of token t for
+//          experts [b * eb, (b + 1) * eb); the last CTA of token t (ticket)
+//          runs its gate and top-k in one warp;
+//   plan:  CTA 0, once every token is gated, runs the plan with its 256
+//          threads from shared memory that the FFN's stage ring reuses later;
+//   FFN:   every CTA, once the plan is published.
+// Counters: route_done (tokens gated) is reset by CTA 0 when it has seen all
+// of them, a token's ticket by its last arrival, and plan_done (with the exit
+// counter and, after a timeout, the others) by the last CTA to leave, so each
+// launch starts from zero.
+struct DecodeArgs {
+  const uint16_t* x;        // [T][H] bf16
+  const uint16_t* wr;       // this layer's router [E][H] bf16
+  const float* rb;          // [E]
+  float* z;                 // [T][E] logits scratch
+  int eb, nblk;             // experts per routing CTA, routing CTAs per token
+  PlanArgs plan;
+  uint32_t* dsync;          // [0] route_done, [1] plan_done, [2] exit count, [3 + t] ticket of token t
+};
+
+constexpr int kDecodeMaxT = 32;
+constexpr int kRouteChunks = 16;   // router-row loads in flight per lane (H <= 4096 in one round)
+
+__global__ void __launch_bounds__(kFusedThreads, 1)
+tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_h, Args a,
+                       FusedArgs f, DecodeArgs d) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ float zsel[kFusedThreads / 32][32];
+  __shared__ volatile int flag_sh;
+  uint8_t* dsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = a.T, H = a.H, E = d.plan.p.E;
+  const int G = gridDim.x;
+  uint32_t* route_done = d.dsync;
+  uint32_t* plan_done = d.dsync + 1;
+  uint32_t* exit_cnt = d.dsync + 2;
+  uint32_t* ticket = d.dsync + 3;
+
+  // ---- route: logits of token t for one block of experts, then (last CTA) its gate
+  if ((int)blockIdx.x < T * d.nblk) {
+    const int t = blockIdx.x / d.nblk, b = blockIdx.x - t * d.nblk;
+    uint16_t* xs = reinterpret_cast<uint16_t*>(dsm);            // x[t] staged once, H bf16
+    for (int h = threadIdx.x * 8; h < H; h += kFusedThreads * 8)
+      *reinterpret_cast<uint4*>(xs + h) = __ldg(reinterpret_cast<const uint4*>(d.x + (size_t)t * H + h));
+    __syncthreads();
+    const int e0 = b * d.eb, e1 = min(E, e0 + d.eb);
+    for (int e = e0 + warp; e < e1; e += kFusedThreads / 32) {
+      const uint16_t* wrow = d.wr + (size_t)e * H;
+      float acc = 0.f;
+      // the row's 16-byte chunks of this lane, kRouteChunks loads in flight at once
+      for (int h0 = lane * 8; h0 < H; h0 += 32 * 8 * kRouteChunks) {
+        uint4 wq[kRouteChunks];
+#pragma unroll
+        for (int c = 0; c < kRouteChunks; ++c) {
+          const int h = h0 + c * 32 * 8;
+          if (h < H) wq[c] = __ldg(reinterpret_cast<const uint4*>(wrow + h));
+        }
+#pragma unroll
+        for (int c = 0; c < kRouteChunks; ++c) {
+          const int h = h0 + c * 32 * 8;
+          if (h < H) {
+            const uint4 q = *reinterpret_cast<const uint4*>(xs + h);
+            acc = fmaf(bf16lo(wq[c].x), bf16lo(q.x), acc);
+            acc = fmaf(bf16hi(wq[c].x), bf16hi(q.x), acc);
+            acc = fmaf(bf16lo(wq[c].y), bf16lo(q.y), acc);
+            acc = fmaf(bf16hi(wq[c].y), bf16hi(q.y), acc);
+            acc = fmaf(bf16lo(wq[c].z), bf16lo(q.z), acc);
+            acc = fmaf(bf16hi(wq[c].z), bf16hi(q.z), acc);
+            acc = fmaf(bf16lo(wq[c].w), bf16lo(q.w), acc);
+            acc = fmaf(bf16hi(wq[c].w), bf16hi(q.w), acc);
+          }
+        }
+      }
+      acc = warp_sum(acc);
+      if (lane == 0) d.z[(size_t)t * E + e] = acc + d.rb[e];
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const uint32_t old = atomicAdd(&ticket[t], 1u);
+      flag_sh = old == (uint32_t)d.nblk - 1;
+      if (flag_sh) ticket[t] = 0u;
+    }
+    __syncthreads();
+    if (flag_sh && warp == 0) {
+      __threadfence();
+      gate_one_token(d.z, t, E, d.plan.p.k, d.plan.p.gating, d.plan.sc.ids, d.plan.sc.w, d.plan.sc.probs,
+                     d.plan.sc.gap, d.plan.p.stats, zsel[0]);
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) release_add(route_done);
+    }
+    __syncthreads();
+  }
+
+  // ---- plan (CTA 0, once every token is gated) while the other CTAs set up;
+  // then every CTA runs the FFN once the plan is published
+  fused_ffn(&map_x, &map_h, a, f, smem_raw, [&]() -> bool {
+    if (blockIdx.x == 0) {
+      if (threadIdx.x == 0) {
+        flag_sh = wait_count(route_done, (uint32_t)T, a.status) ? 1 : 0;
+        if (flag_sh) *route_done = 0u;
+        else set_status(a.status, MOE_ERR_TIMEOUT);
+      }
+      __syncthreads();
+      if (flag_sh) {
+        __threadfence();
+        plan_body<kFusedThreads>(d.plan, dsm);
+      }
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0) release_add(plan_done);
+    }
+    if (threadIdx.x == 0) {
+      flag_sh = wait_count(plan_done, 1u, a.status) ? 1 : 0;
+      if (!flag_sh) set_status(a.status, MOE_ERR_TIMEOUT);
+    }
+    __syncthreads();
+    const bool ok = flag_sh != 0;
+    if (ok) __threadfence();
+    __syncthreads();
+    return ok;
+  });
+  // ---- leave: the last CTA resets the counters for the next launch
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t old = atomicAdd(exit_cnt, 1u);
+    if (old == (uint32_t)G - 1) {
+      *route_done = 0u;
+      *plan_done = 0u;
+      for (int t = 0; t < kDecodeMaxT; ++t) ticket[t] = 0u;
+      *exit_cnt = 0u;
     }
   }
 }
@@ -1294,18 +1459,17 @@ int launch_tc_gather(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T
 }
 
 
-// Fused dense decode FFN (miss copies + gate/up + down + combine), one cooperative launch.
-int launch_tc_fused_decode(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, const void* x, void* out,
-                           cudaStream_t s) {
-  (void)m;
+// Arguments of the fused FFN for a call of T tokens (dense token columns).
+static bool fused_setup(const PoolDev& p, const Scratch& sc, int T, const void* x, void* out, tc::Args* ap,
+                        tc::FusedArgs* fp, CUtensorMap* xm, CUtensorMap* hm) {
   const int N = tc_npad(T);
   tc::Args a = tc_args(p, sc, T, N);
   a.out = static_cast<uint16_t*>(out);
   a.stages = std::min<int>(tc::kMaxStages, (int)(tc::kSmemBudget / tc::fused_stage_bytes(N)));
-  CUtensorMap xm, hm;
-  if (!tc::make_map_3d(&xm, x, (uint64_t)p.H, (uint64_t)T, 1, (uint64_t)p.H * 2, (uint64_t)p.H * 2 * T, N)) return -1;
+  if (!tc::make_map_3d(xm, x, (uint64_t)p.H, (uint64_t)T, 1, (uint64_t)p.H * 2, (uint64_t)p.H * 2 * T, N))
+    return false;
   const uint64_t I = p.I;
-  if (!tc::make_map_3d(&hm, sc.hbuf, I, (uint64_t)N, (uint64_t)p.E + 1, I * 2, (uint64_t)N * I * 2, N)) return -1;
+  if (!tc::make_map_3d(hm, sc.hbuf, I, (uint64_t)N, (uint64_t)p.E + 1, I * 2, (uint64_t)N * I * 2, N)) return false;
   tc::FusedArgs f;
   f.jobs = sc.copies;
   f.n_jobs = sc.n_copy;
@@ -1322,13 +1486,14 @@ int launch_tc_fused_decode(const PoolDev& p, const Scratch& sc, const TcMaps* m,
   f.dn_done = reinterpret_cast<uint32_t*>(sc.ffn_sync + (size_t)(p.E + 1) * mt_i);
   f.hready = f.dn_done + mt_h;
   f.jdone = f.hready + (p.E + 1);
-  static bool configured = false;
-  if (!configured) {
-    cudaFuncSetAttribute(tc::tc_fused_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         tc::kSmemBudget + 1024);
-    configured = true;
-  }
-  const size_t smem = (size_t)a.stages * tc::fused_stage_bytes(N) + 1024;
+  *ap = a;
+  *fp = f;
+  return true;
+}
+
+static size_t fused_smem(int N, int stages) { return (size_t)stages * tc::fused_stage_bytes(N) + 1024; }
+
+static int launch_cooperative(const void* fn, size_t smem, cudaStream_t s, void** args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sm_count());
   cfg.blockDim = dim3(tc::kFusedThreads);
@@ -1339,8 +1504,84 @@ int launch_tc_fused_decode(const PoolDev& p, const Scratch& sc, const TcMaps* m,
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, tc::tc_fused_decode_kernel, xm, hm, a, f) != cudaSuccess) return -2;
-  return 1;
+  return cudaLaunchKernelExC(&cfg, fn, args) == cudaSuccess ? 1 : -2;
+}
+
+// Fused dense decode FFN (miss copies + gate/up + down + combine), one cooperative launch.
+int launch_tc_fused_decode(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, const void* x, void* out,
+                           cudaStream_t s) {
+  (void)m;
+  tc::Args a;
+  tc::FusedArgs f;
+  CUtensorMap xm, hm;
+  if (!fused_setup(p, sc, T, x, out, &a, &f, &xm, &hm)) return -1;
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!configured[dev & 63]) {
+    cudaFuncSetAttribute(tc::tc_fused_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         tc::kSmemBudget + 1024);
+    configured[dev & 63] = true;
+  }
+  void* args[] = {&xm, &hm, &a, &f};
+  return launch_cooperative(reinterpret_cast<const void*>(tc::tc_fused_decode_kernel), fused_smem(a.N, a.stages), s,
+                            args);
+}
+
+// Shared memory of the decode layer kernel's plan (256 threads), 0 if it does not fit.
+static size_t decode_plan_smem(const PoolDev& p, int T, int* cap, int* rows) {
+  const size_t b = plan_smem_bytes_nt<tc::kFusedThreads>(p, T, cap, rows, tc::kSmemBudget - 1024);
+  return b + 16 <= (size_t)tc::kSmemBudget ? b + 16 : 0;
+}
+
+bool tc_decode_layer_ok(const PoolDev& p, const Scratch& sc, int T) {
+  int cap = 0, rows = 0;
+  return sc.dsync != nullptr && p.adt == MOE_BF16 && T >= 1 && T <= tc::kDecodeMaxT && tc_npad(T) <= sc.npad_max &&
+         p.H % 8 == 0 && (size_t)p.H * 2 + 16 <= (size_t)tc::kSmemBudget && decode_plan_smem(p, T, &cap, &rows) > 0;
+}
+
+// Router, gate, plan and fused FFN of one decode call, one cooperative launch.
+int launch_tc_decode_layer(const PoolDev& p, const Scratch& sc, const TcMaps* m, int layer, int T, const void* x,
+                           const void* router_w, const float* router_b, void* out, cudaStream_t s) {
+  (void)m;
+  tc::Args a;
+  tc::FusedArgs f;
+  CUtensorMap xm, hm;
+  if (!fused_setup(p, sc, T, x, out, &a, &f, &xm, &hm)) return -1;
+  tc::DecodeArgs d;
+  d.x = static_cast<const uint16_t*>(x);
+  d.wr = static_cast<const uint16_t*>(router_w) + (size_t)layer * p.E * p.H;
+  d.rb = router_b + (size_t)layer * p.E;
+  d.z = sc.logits;
+  const int G = sm_count();
+  int nblk = std::max(1, std::min(G / T, (p.E + 7) / 8));
+  d.eb = (p.E + nblk - 1) / nblk;
+  d.nblk = (p.E + d.eb - 1) / d.eb;
+  PlanArgs& pa = d.plan;
+  pa.p = p;
+  pa.sc = sc;
+  pa.layer = layer;
+  pa.T = T;
+  pa.flags = PLAN_HISTORY | PLAN_CACHE | PLAN_PERMUTE;
+  pa.region = 0;
+  pa.npad = a.N;
+  pa.ids = sc.ids;
+  pa.w = sc.w;
+  pa.probs = sc.probs;
+  const size_t psm = decode_plan_smem(p, T, &pa.owner_cap, &pa.tok_rows);
+  if (psm == 0) return -1;
+  d.dsync = sc.dsync;
+  const size_t smem = std::max(std::max(fused_smem(a.N, a.stages), psm + 1024), (size_t)p.H * 2 + 16 + 1024);
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!configured[dev & 63]) {
+    cudaFuncSetAttribute(tc::tc_decode_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         tc::kSmemBudget + 1024);
+    configured[dev & 63] = true;
+  }
+  void* args[] = {&xm, &hm, &a, &f, &d};
+  return launch_cooperative(reinterpret_cast<const void*>(tc::tc_decode_layer_kernel), smem, s, args);
 }
 
 }  // namespace moeslot

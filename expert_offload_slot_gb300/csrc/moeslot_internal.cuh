@@ -99,6 +99,7 @@ struct Scratch {
   size_t dn_partial_floats;
   int32_t* ffn_sync;  // arrival counters and readiness flags of the fused decode kernel,
   int32_t n_ffn_sync; // zeroed by the plan kernel before every expert launch
+  uint32_t* dsync;    // [3 + 32] counters of the decode layer kernel (reset by its last CTA)
   int32_t* elist;     // [2][E+1]: work entries already resident / copied this step
   int32_t* ecount;    // [2]
   // tensor-core gather path (T > npad_max)
@@ -166,6 +167,10 @@ int launch_tc_gather(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T
                      cudaStream_t s);
 int launch_tc_fused_decode(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, const void* x, void* out,
                            cudaStream_t s);
+// router + gate + plan + fused FFN of a decode call in one cooperative launch (bf16, T <= 32)
+bool tc_decode_layer_ok(const PoolDev& p, const Scratch& sc, int T);
+int launch_tc_decode_layer(const PoolDev& p, const Scratch& sc, const TcMaps* m, int layer, int T, const void* x,
+                           const void* router_w, const float* router_b, void* out, cudaStream_t s);
 int launch_load_slot(const PoolDev& p, const Scratch& sc, int layer, int expert, int slot, cudaStream_t s);
 int launch_rebuild_owner(const PoolDev& p, cudaStream_t s);
 
