@@ -375,10 +375,25 @@ def expert_bytes(wl):
     return be
 
 
-def ffn_algorithmic_bytes(wl, sum_U, bytes_copied, layer_steps, T):
-    """HBM bytes the expert FFN must move: the U expert records it reads, the miss bytes it writes
-    into slots, and x in / out once per layer-step."""
-    return sum_U * expert_bytes(wl) + bytes_copied + layer_steps * 2 * T * wl.H * wl.act_elt_bytes
+def ffn_algorithmic_bytes(wl, sum_U, bytes_copied, layer_steps, T, router=False):
+    """HBM bytes the expert kernel must move: the U expert records it reads, the miss bytes it
+    writes into slots, x in / out once per layer-step, and (router=True, when the router runs in
+    the same kernel) the router matrix once per layer-step."""
+    b = sum_U * expert_bytes(wl) + bytes_copied + layer_steps * 2 * T * wl.H * wl.act_elt_bytes
+    if router:
+        b += layer_steps * wl.E * wl.H * wl.act_elt_bytes
+    return b
+
+
+def fused_layer(stage_ms):
+    """True when the profile attributes the whole layer to the expert stage (one decode layer kernel)."""
+    import expert_offload_slot_gb300 as moe
+    return stage_ms[moe.STAGES.index("ffn")] > 0 and all(
+        stage_ms[moe.STAGES.index(n)] == 0 for n in ("route", "plan", "copy"))
+
+
+KERNEL_LABEL = {True: "tc_decode_layer_kernel (router, gate, plan, miss copies, gate/up, down, combine)",
+                False: "tc_fused_decode_kernel (miss copies + gate/up + down + combine)"}
 
 
 def step_bytes(wl, U_per_layer, T):
@@ -400,7 +415,8 @@ def decode_summary(wl, r, peak):
     prof = r["prof"]
     n = max(1, prof["launches"])
     ffn_ms = prof["stage_ms"][moe.STAGES.index("ffn")] + prof["stage_ms"][moe.STAGES.index("copy")]
-    ffn_b = ffn_algorithmic_bytes(wl, prof["sum_U"], prof["bytes_copied"], prof["launches"], r["T"])
+    fused = fused_layer(prof["stage_ms"])
+    ffn_b = ffn_algorithmic_bytes(wl, prof["sum_U"], prof["bytes_copied"], prof["launches"], r["T"], router=fused)
     ach = ffn_b / (ffn_ms / 1e3) / 1e9 if ffn_ms > 0 else 0.0
     U = prof["sum_U"] / n
     lay_us = sum(prof["stage_ms"]) * 1e3 / n
@@ -409,7 +425,9 @@ def decode_summary(wl, r, peak):
             "hit_rate": r["hits"] / max(1, r["hits"] + r["misses"]),
             "miss_MB_per_layer": r["bytes_copied"] / 1e6 / (r["steps"] * wl.L),
             "mean_U": U, "stage_us_per_layer": {k: v * 1e3 / n for k, v in zip(moe.STAGES, prof["stage_ms"])},
-            "ffn_roofline": {"bound": "hbm", "achieved": ach, "unit": "GB/s", "frac": ach / peak,
+            "ffn_roofline": {"bound": "hbm", "kernel": KERNEL_LABEL[fused] if wl.weight_dtype == 1 else
+                             "ffn_gate_up_kernel + ffn_down_combine_kernel",
+                             "achieved": ach, "unit": "GB/s", "frac": ach / peak,
                              "bytes_per_launch": ffn_b / n, "us_per_launch": ffn_ms * 1e3 / n},
             "layer_frac": step_bytes(wl, U, r["T"]) / (lay_us * 1e-6) / 1e9 / peak if lay_us else 0.0,
             "status": moe_status_name(r["status"]), "clocks": r.get("clocks")}
@@ -677,7 +695,8 @@ def main():
     ffn_ms = prof["stage_ms"][moe.STAGES.index("ffn")] + prof["stage_ms"][moe.STAGES.index("copy")]
     layer_steps = prof["launches"]
     U_mean = prof["sum_U"] / max(1, layer_steps)
-    ffn_bytes = ffn_algorithmic_bytes(wl, prof["sum_U"], prof["bytes_copied"], layer_steps, T)
+    fused = fused_layer(prof["stage_ms"])
+    ffn_bytes = ffn_algorithmic_bytes(wl, prof["sum_U"], prof["bytes_copied"], layer_steps, T, router=fused)
     achieved = ffn_bytes / (ffn_ms / 1e3) / 1e9 if ffn_ms > 0 else 0.0
     prof_layer_us = sum(prof["stage_ms"]) * 1e3 / max(1, layer_steps)
     layer_bytes = step_bytes(wl, U_mean, T)
@@ -706,7 +725,7 @@ def main():
         "miss_copy_GB": r["bytes_copied"] / 1e9,
         "e2e": {"value": e2e_value, "unit": "MoE-layer tokens/s",
                 "h2d_bytes_per_step": r.get("e2e", {}).get("h2d"), "d2h_bytes_per_step": r.get("e2e", {}).get("d2h")},
-        "roofline": {"bound": "hbm", "kernel": "tc_fused_decode_kernel (miss copies + gate/up + down + combine)",
+        "roofline": {"bound": "hbm", "kernel": KERNEL_LABEL[fused],
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
                      "peak_source": f"{peak_kind} hbm_gbs", "launches_timed": prof["launches"],
                      "bytes_per_launch": ffn_bytes / max(1, prof["launches"]),

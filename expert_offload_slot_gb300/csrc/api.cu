@@ -81,6 +81,7 @@ struct moe_pool {
   std::vector<void*> allocs;
   bool prof_on = false;
   std::vector<cudaEvent_t> prof_ev;   // [L][MOE_NUM_STAGES + 1]
+  std::vector<uint8_t> prof_fused;    // [L]: the layer's last call ran as one decode layer kernel
   TcMaps* tc_maps = nullptr;          // tensor maps of the record array (bf16 weights)
   cudaStream_t side = nullptr;        // miss copies run here, beside gate/up over resident experts
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
@@ -340,7 +341,8 @@ MOE_API moe_status moe_pool_create(const moe_config* cfg, const void* host_pool,
     PA(hb, rows * (size_t)d.I * asz, 0);
     P->sc.h = hb;
   }
-  if (cfg->weight_dtype == MOE_BF16) {
+  if (cfg->weight_dtype == MOE_BF16 ||
+      (cfg->weight_dtype == MOE_FP8_E4M3_B128 && cfg->act_dtype == MOE_BF16 && tc_fp8_ok(d))) {
     // tensor-core expert path (T <= 256): dense routing weights, h buffer, split partials
     const int np = std::min(tc_npad((int)Tm), 256);
     P->sc.npad_max = np;
@@ -353,8 +355,8 @@ MOE_API moe_status moe_pool_create(const moe_config* cfg, const void* host_pool,
     P->sc.n_ffn_sync = tc_ffn_sync_ints(d);
     PA(P->sc.ffn_sync, P->sc.n_ffn_sync, 0);
     PA(P->sc.dsync, 64, 0);
-    if ((size_t)tc_npad((int)Tm) > (size_t)np) {
-      // gather path for calls with more tokens than the dense path takes
+    if ((size_t)tc_npad((int)Tm) > (size_t)np && cfg->weight_dtype == MOE_BF16) {
+      // gather path for calls with more tokens than the dense path takes (bf16 weights)
       PA(P->sc.inv, Tm * k, 0);
       PA(P->sc.ntile0, E + 2, 0);
       PA(P->sc.n_rows, 1, 0);
@@ -486,14 +488,13 @@ static moe_status run_layer(moe_pool* P, int layer, const void* x, int T, void* 
       cudaEventRecord(P->prof_ev[(size_t)layer * NB + i], s);
   };
   mark(0);
-  const bool tc = P->tc_maps != nullptr;                 // bf16 weights: tensor-core path
+  const bool tc = P->tc_maps != nullptr;                 // bf16 or fp8 weights: tensor-core path
   const bool use_tc = tc && tc_npad(T) <= sc.npad_max;   // dense token columns
-  const bool gather = tc && !use_tc;                     // expert-grouped token tiles
+  const bool gather = tc && !use_tc && d.wdt == MOE_BF16; // expert-grouped token tiles
   if (use_tc && !ids_in && !staged && tc_decode_layer_ok(d, sc, T)) {
-    // router, gate, plan, miss copies, gate/up, down and combine in one cooperative kernel
-    mark(1);
-    mark(2);
-    mark(3);
+    // router, gate, plan, miss copies, gate/up, down and combine in one cooperative kernel;
+    // its profile is one interval (mark 0 to mark 4)
+    if (P->prof_on) P->prof_fused[layer] = 1;
     const int n = launch_tc_decode_layer(d, sc, P->tc_maps, layer, T, x, P->router_w, P->router_b, out, s);
     if (n == -1) return fail(MOE_ERR_INVALID, "x must be 16-byte aligned for the tensor-core path");
     if (n < 0) return fail(MOE_ERR_CUDA, "cooperative launch failed: %s", cudaGetErrorString(cudaGetLastError()));
@@ -504,6 +505,7 @@ static moe_status run_layer(moe_pool* P, int layer, const void* x, int T, void* 
     P->last_gap_valid = true;
     return MOE_OK;
   }
+  if (P->prof_on) P->prof_fused[layer] = 0;
   if (!ids_in) {
     if (route_fused_ok(d, T)) {
       P->launches += launch_route_gate_fused(d, layer, x, T, P->router_w, P->router_b, sc, s);
@@ -694,6 +696,7 @@ MOE_API moe_status moe_profile_enable(moe_pool* P, int32_t on) {
   if (on && P->prof_ev.empty()) {
     const size_t n = (size_t)P->d.L * (MOE_NUM_STAGES + 1);
     P->prof_ev.resize(n, nullptr);
+    P->prof_fused.assign((size_t)P->d.L, 0);
     for (size_t i = 0; i < n; ++i) CUDA_TRY(cudaEventCreate(&P->prof_ev[i]));
   }
   P->prof_on = on != 0;
@@ -706,6 +709,13 @@ MOE_API moe_status moe_profile_read(moe_pool* P, int32_t layer, float* stage_ms)
   if (P->prof_ev.empty()) return fail(MOE_ERR_INVALID, "profiling was never enabled");
   CUDA_TRY(cudaSetDevice(P->device));
   const size_t b = (size_t)layer * (MOE_NUM_STAGES + 1);
+  if (P->prof_fused[layer]) {
+    // one kernel: every stage is attributed to the expert stage
+    for (int i = 0; i < MOE_NUM_STAGES; ++i) stage_ms[i] = 0.f;
+    CUDA_TRY(cudaEventSynchronize(P->prof_ev[b + MOE_NUM_STAGES]));
+    CUDA_TRY(cudaEventElapsedTime(&stage_ms[MOE_STAGE_FFN], P->prof_ev[b], P->prof_ev[b + MOE_NUM_STAGES]));
+    return MOE_OK;
+  }
   for (int i = 0; i < MOE_NUM_STAGES; ++i) {
     CUDA_TRY(cudaEventSynchronize(P->prof_ev[b + i + 1]));
     CUDA_TRY(cudaEventElapsedTime(&stage_ms[i], P->prof_ev[b + i], P->prof_ev[b + i + 1]));

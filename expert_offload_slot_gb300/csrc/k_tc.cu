@@ -45,6 +45,8 @@
 // its own copies and MMAs (again with bounded waits) before freeing TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include <algorithm>
 #include <cstring>
@@ -56,7 +58,11 @@
 namespace moeslot {
 
 struct TcMaps {
-  int dummy;         // weights need no tensor map (tiled records, bulk copies)
+  // bf16 weights need no tensor map (tiled records, bulk copies); fp8 weights are
+  // read as 128-row x 64-byte tiles of the record array: w13 [n_records][2I][H]
+  // and w2 [n_records][H][I] (row-major codes)
+  bool fp8 = false;
+  CUtensorMap w13{}, w2{};
 };
 
 namespace tc {
@@ -301,6 +307,22 @@ __device__ __forceinline__ UnitRange unit_range(const Plan& p, const Args& a, in
 }
 
 __device__ __forceinline__ float silu(float v) { return v / (1.f + expf(-v)); }
+
+// Four fp8 e4m3 codes (little-endian in w) as floats; the decode is exact.
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float* v) {
+  const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
+  const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+  v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+}
+
+// Two floats rounded to bf16 (nearest, ties to even), lo in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 
 // Epilogue store of one 16-column chunk.  Gate/up: d0 = W_gate x, d1 = W_up x;
 // down: d0 = D.  Column j is token c0+j (dense) or row row_base+c0+j (gather).
@@ -597,11 +619,26 @@ constexpr int kCopyWarps = 2;
 constexpr int kCopyUnroll = 16;  // 16-byte host reads in flight per copy lane
 constexpr int kFusedThreads = kThreads + 32 * kCopyWarps;
 constexpr int kFusedBufs = 8;
+// Weight formats of the fused kernels: bf16 records pre-tiled in the MMA's
+// swizzled order (bulk copies), or fp8 e4m3 row-major records with one fp32
+// scale per 128 x 128 block (TMA tiles of codes, expanded to bf16 in place by
+// converter warps, the block scale applied in the expansion).
+constexpr int kWfBf16 = 0, kWfFp8 = 1;
+constexpr int kConvWarps = 4;
+template <int WF> struct FusedShape {
+  static constexpr int conv_warps = WF == kWfFp8 ? kConvWarps : 0;
+  static constexpr int conv_warp0 = kThreads / 32;               // after the epilogue warps
+  static constexpr int copy_warp0 = conv_warp0 + conv_warps;
+  static constexpr int threads = (copy_warp0 + kCopyWarps) * 32;
+};
 
 struct FusedArgs {
   const CopyJob* jobs;
   const int32_t* n_jobs;
-  uint32_t tile16;              // tile data of a record (w13 then w2), in 16 B units
+  uint32_t tile16;              // bytes of a record the miss copy moves, in 16 B units
+  // fp8 records: scale tables at os13 ([2I/128][H/128] fp32) and os2 ([H/128][I/128])
+  size_t os13, os2;
+  int sc_h, sc_i;               // scale row lengths: H / 128 and I / 128
   const int32_t* elist;         // [2][E1]: resident entries, copied entries (work positions, ascending)
   const int32_t* ecount;        // [2]
   int E1;                       // E + 1
@@ -717,14 +754,18 @@ __device__ __forceinline__ void st_f4(float* p, float a, float b, float c, float
 // kFusedThreads-thread CTAs; smem_raw: the CTA's dynamic shared memory.  pre()
 // runs on every thread between the CTA's setup (barriers, TMEM) and the first
 // read of the step's work lists, and returns false if they will not come.
-template <typename Pre>
-__device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUtensorMap* map_h_p, const Args& a,
+template <int WF, typename Pre>
+__device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUtensorMap* map_h_p,
+                                          const CUtensorMap* map_w13_p, const CUtensorMap* map_w2_p, const Args& a,
                                           const FusedArgs& f, uint8_t* smem_raw, Pre pre) {
+  using Shape = FusedShape<WF>;
   const CUtensorMap& map_x = *map_x_p;
   const CUtensorMap& map_h = *map_h_p;
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
   __shared__ __align__(8) uint64_t tfull_bar[kFusedBufs], tempty_bar[kFusedBufs], drain_bar;
+  __shared__ __align__(8) uint64_t conv_bar[WF == kWfFp8 ? kMaxStages : 1];   // stage expanded to bf16
+  __shared__ float scale_sh[WF == kWfFp8 ? 2 : 1][WF == kWfFp8 ? 128 : 1];    // the unit's block scales
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_sh, last_sh;
   __shared__ FSched sched_sh;
@@ -749,6 +790,7 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
     for (int s = 0; s < S; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
+      if (WF == kWfFp8) mbar_init(&conv_bar[s], 32 * kConvWarps);
     }
     for (int b = 0; b < kFusedBufs; ++b) {
       mbar_init(&tfull_bar[b], 1);
@@ -817,9 +859,22 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
           if (it >= (uint32_t)S && !mbar_wait(&empty_bar[s], ((it / S) - 1) & 1)) { ok = false; break; }
           if (abort_sh) { ok = false; break; }
           uint8_t* st = smem + (size_t)s * stage_bytes;
-          const uint32_t wb = r.gu ? 2 * kTileBytes : (uint32_t)nk * kTileBytes;
-          mbar_expect_tx(&full_bar[s], wb + (uint32_t)nk * b_bytes);
-          bulk_load(st, wbase + (size_t)kb * (r.gu ? 2 * kTileBytes : kTileBytes), wb, &full_bar[s]);
+          if (WF == kWfFp8) {
+            // fp8 code tiles (128 rows x 64 bytes) into the upper half of each bf16 tile slot
+            const uint32_t raw = kTileBytes / 2;
+            mbar_expect_tx(&full_bar[s], (r.gu ? 2u : (uint32_t)nk) * raw + (uint32_t)nk * b_bytes);
+            if (r.gu) {
+              tma_load_3d(st + raw, &map_w13_p[0], &full_bar[s], kb * BK, r.mt * BM, we.rid);
+              tma_load_3d(st + kTileBytes + raw, &map_w13_p[0], &full_bar[s], kb * BK, a.I + r.mt * BM, we.rid);
+            } else {
+              for (int j = 0; j < nk; ++j)
+                tma_load_3d(st + j * kTileBytes + raw, &map_w2_p[0], &full_bar[s], (kb + j) * BK, r.mt * BM, we.rid);
+            }
+          } else {
+            const uint32_t wb = r.gu ? 2 * kTileBytes : (uint32_t)nk * kTileBytes;
+            mbar_expect_tx(&full_bar[s], wb + (uint32_t)nk * b_bytes);
+            bulk_load(st, wbase + (size_t)kb * (r.gu ? 2 * kTileBytes : kTileBytes), wb, &full_bar[s]);
+          }
           if (r.gu) {
             tma_load_3d(st + 2 * kTileBytes, &map_x, &full_bar[s], kb * BK, 0, 0);
           } else if (h_ok) {
@@ -864,7 +919,7 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
         const int kstep = r.gu ? 1 : 2;
         for (int kb = r.kb0; kb < r.kb1; kb += kstep, ++it) {
           const int s = it % S;
-          if (!mbar_wait(&full_bar[s], (it / S) & 1) || abort_sh) { ok = false; break; }
+          if (!mbar_wait(WF == kWfFp8 ? &conv_bar[s] : &full_bar[s], (it / S) & 1) || abort_sh) { ok = false; break; }
           fence_after();
           const uint32_t base = smem_u32(smem + (size_t)s * stage_bytes);
           if (r.gu) {
@@ -1043,12 +1098,98 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
       }
     }
     __threadfence();   // this thread's partials, before the CTA reports them written
+  } else if (WF == kWfFp8 && warp < Shape::copy_warp0) {
+    // ------------------------------------------------------------- converter warps (fp8)
+    // Per stage: every thread reads its 4 x 16 code bytes of each tile, then (all
+    // reads done) writes them back as bf16 (code * block scale, one rounding) in
+    // the 128-byte-swizzled order, over the same slot.  The unit's block scales
+    // are staged in shared memory at unit start (a copied record's only after
+    // its first stage has landed, which orders them after the copy).
+    // Every converter thread passes every named barrier of every stage, also after
+    // a timeout (then it only skips the work), so none is left waiting.
+    const FSched sc = sched_sh;
+    const int ct = threadIdx.x - Shape::conv_warp0 * 32;        // 0..127
+    uint32_t it = 0;
+    int local = 0;
+    bool stop = false;
+    for (int g = blockIdx.x; g < sc.total; g += G, ++local) {
+      const FUnit r = fused_unit(sc, f, g);
+      const int rid = a.work[r.u].rid;
+      const float* scl = reinterpret_cast<const float*>(a.records + (size_t)rid * a.rec + (r.gu ? f.os13 : f.os2));
+      const int b0 = r.kb0 / 2, nblk = (r.kb1 - 1) / 2 - b0 + 1;   // 128-wide scale blocks the unit spans (<= 64)
+      const int sbuf = local & 1;
+      // gate (or down) scales at [0, 64), up scales at [64, 128)
+      auto stage_scales = [&]() {
+        if (stop) return;
+        if (ct < nblk) {
+          scale_sh[sbuf][ct] = scl[(size_t)(r.gu ? r.mt * f.sc_h : r.mt * f.sc_i) + b0 + ct];
+        } else if (r.gu && ct >= 64 && ct - 64 < nblk) {
+          scale_sh[sbuf][ct] = scl[(size_t)(a.I / BM + r.mt) * f.sc_h + b0 + (ct - 64)];
+        }
+      };
+      if (!r.miss) stage_scales();
+      const int kstep = r.gu ? 1 : 2;
+      bool first = true;
+      for (int kb = r.kb0; kb < r.kb1; kb += kstep, ++it) {
+        const int s = it % S;
+        if (!stop && (!mbar_wait(&full_bar[s], (it / S) & 1) || abort_sh)) {
+          stop = true;
+          set_status(a.status, MOE_ERR_TIMEOUT);
+          abort_sh = 1;
+        }
+        if (first) {
+          if (r.miss) stage_scales();
+          asm volatile("bar.sync 3, %0;" ::"n"(32 * kConvWarps) : "memory");
+          first = false;
+        }
+        uint8_t* st = smem + (size_t)s * stage_bytes;
+        const int nt = r.gu ? 2 : min(2, r.kb1 - kb);
+        uint4 raw[2][4];
+        if (!stop) {
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+            if (q < nt) {
+#pragma unroll
+              for (int m = 0; m < 4; ++m)
+                raw[q][m] = *reinterpret_cast<const uint4*>(st + q * kTileBytes + kTileBytes / 2 + (ct + 128 * m) * 16);
+            }
+        }
+        asm volatile("bar.sync 3, %0;" ::"n"(32 * kConvWarps) : "memory");
+        if (!stop) {
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+            if (q < nt) {
+              const float sv = r.gu ? scale_sh[sbuf][(q ? 64 : 0) + kb / 2 - b0] : scale_sh[sbuf][(kb + q) / 2 - b0];
+#pragma unroll
+              for (int m = 0; m < 4; ++m) {
+                const int c16 = ct + 128 * m, row = c16 >> 2, cq = c16 & 3;   // 16 codes: columns cq*16..+16
+                const uint32_t w4[4] = {raw[q][m].x, raw[q][m].y, raw[q][m].z, raw[q][m].w};
+                uint32_t o[8];
+#pragma unroll
+                for (int wq = 0; wq < 4; ++wq) {
+                  float v[4];
+                  e4m3x4_to_f32(w4[wq], v);
+                  o[2 * wq] = pack_bf16x2(v[0] * sv, v[1] * sv);
+                  o[2 * wq + 1] = pack_bf16x2(v[2] * sv, v[3] * sv);
+                }
+                uint8_t* rowp = st + q * kTileBytes + row * 128;
+                const int c0 = 2 * cq;
+                *reinterpret_cast<uint4*>(rowp + ((c0 ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ (row & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+              }
+            }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> MMA reads
+          mbar_arrive(&conv_bar[s]);
+        }
+      }
+      asm volatile("bar.sync 3, %0;" ::"n"(32 * kConvWarps) : "memory");   // before the scale buffer is reused
+    }
   } else {
-    // ------------------------------------------------------------- copy warps (6, 7)
+    // ------------------------------------------------------------- copy warps
     // Job by job: this CTA's slice of each record's tile data, then one release per job.
     const uint32_t n = go ? (uint32_t)*f.n_jobs : 0u;
     const uint32_t stride = (uint32_t)G * (32u * kCopyWarps);
-    const uint32_t ctid = (uint32_t)(warp - kThreads / 32) * 32u + lane;
+    const uint32_t ctid = (uint32_t)(warp - Shape::copy_warp0) * 32u + lane;
     for (uint32_t j = 0; j < n; ++j) {
       const uint4* src = reinterpret_cast<const uint4*>(f.jobs[j].src);
       uint4* dst = reinterpret_cast<uint4*>(f.jobs[j].dst);
@@ -1067,7 +1208,7 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
       }
       __threadfence();
       asm volatile("bar.sync 2, %0;" ::"n"(32 * kCopyWarps) : "memory");
-      if (warp == kThreads / 32 && lane == 0) release_add(&f.jdone[j]);
+      if (warp == Shape::copy_warp0 && lane == 0) release_add(&f.jdone[j]);
     }
   }
   fence_before();
@@ -1121,11 +1262,13 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
   }
 }
 
-__global__ void __launch_bounds__(kFusedThreads, 1)
-tc_fused_decode_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_h, Args a,
+template <int WF>
+__global__ void __launch_bounds__(FusedShape<WF>::threads, 1)
+tc_fused_decode_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_h,
+                       const __grid_constant__ CUtensorMap map_w13, const __grid_constant__ CUtensorMap map_w2, Args a,
                        FusedArgs f) {
   extern __shared__ uint8_t smem_raw[];
-  fused_ffn(&map_x, &map_h, a, f, smem_raw, [] { return true; });
+  fused_ffn<WF>(&map_x, &map_h, &map_w13, &map_w2, a, f, smem_raw, [] { return true; });
 }
 
 
@@ -1134,11 +1277,13 @@ tc_fused_decode_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
 // launch: steps a1/a2 (router and gate), a3-a5/a7 (history, table, victims,
 // permutation) and the fused FFN (a6, a8, a9), without the launch gaps and
 // global round trips of three kernels.
-//   route: CTA (t, b), t < T, b < nblk, computes the logits of token t for
-//          experts [b * eb, (b + 1) * eb); the last CTA of token t (ticket)
-//          runs its gate and top-k in one warp;
-//   plan:  CTA 0, once every token is gated, runs the plan with its 256
-//          threads from shared memory that the FFN's stage ring reuses later;
+//   route: CTA 1 + t * nblk + b, t < T, b < nblk, computes the logits of token
+//          t for experts [b * eb, (b + 1) * eb); the last CTA of token t
+//          (ticket) runs its gate and top-k in one warp;
+//   plan:  CTA 0 starts copying the plan's routing-independent inputs (history
+//          rings, slot owners) into shared memory at once, and once every token
+//          is gated runs the plan with its 256 threads, from shared memory that
+//          the FFN's stage ring reuses later;
 //   FFN:   every CTA, once the plan is published.
 // Counters: route_done (tokens gated) is reset by CTA 0 when it has seen all
 // of them, a token's ticket by its last arrival, and plan_done (with the exit
@@ -1157,11 +1302,14 @@ struct DecodeArgs {
 constexpr int kDecodeMaxT = 32;
 constexpr int kRouteChunks = 16;   // router-row loads in flight per lane (H <= 4096 in one round)
 
-__global__ void __launch_bounds__(kFusedThreads, 1)
-tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_h, Args a,
+template <int WF>
+__global__ void __launch_bounds__(FusedShape<WF>::threads, 1)
+tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_h,
+                       const __grid_constant__ CUtensorMap map_w13, const __grid_constant__ CUtensorMap map_w2, Args a,
                        FusedArgs f, DecodeArgs d) {
+  constexpr int NT = FusedShape<WF>::threads;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ float zsel[kFusedThreads / 32][32];
+  __shared__ float zsel[NT / 32][32];
   __shared__ volatile int flag_sh;
   uint8_t* dsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1172,15 +1320,17 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
   uint32_t* exit_cnt = d.dsync + 2;
   uint32_t* ticket = d.dsync + 3;
 
+  if (blockIdx.x == 0) plan_prestage<NT>(d.plan, dsm);
   // ---- route: logits of token t for one block of experts, then (last CTA) its gate
-  if ((int)blockIdx.x < T * d.nblk) {
-    const int t = blockIdx.x / d.nblk, b = blockIdx.x - t * d.nblk;
+  if (blockIdx.x >= 1 && (int)blockIdx.x <= T * d.nblk) {
+    const int rb = blockIdx.x - 1;
+    const int t = rb / d.nblk, b = rb - t * d.nblk;
     uint16_t* xs = reinterpret_cast<uint16_t*>(dsm);            // x[t] staged once, H bf16
-    for (int h = threadIdx.x * 8; h < H; h += kFusedThreads * 8)
+    for (int h = threadIdx.x * 8; h < H; h += NT * 8)
       *reinterpret_cast<uint4*>(xs + h) = __ldg(reinterpret_cast<const uint4*>(d.x + (size_t)t * H + h));
     __syncthreads();
     const int e0 = b * d.eb, e1 = min(E, e0 + d.eb);
-    for (int e = e0 + warp; e < e1; e += kFusedThreads / 32) {
+    for (int e = e0 + warp; e < e1; e += NT / 32) {
       const uint16_t* wrow = d.wr + (size_t)e * H;
       float acc = 0.f;
       // the row's 16-byte chunks of this lane, kRouteChunks loads in flight at once
@@ -1231,7 +1381,7 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
 
   // ---- plan (CTA 0, once every token is gated) while the other CTAs set up;
   // then every CTA runs the FFN once the plan is published
-  fused_ffn(&map_x, &map_h, a, f, smem_raw, [&]() -> bool {
+  fused_ffn<WF>(&map_x, &map_h, &map_w13, &map_w2, a, f, smem_raw, [&]() -> bool {
     if (blockIdx.x == 0) {
       if (threadIdx.x == 0) {
         flag_sh = wait_count(route_done, (uint32_t)T, a.status) ? 1 : 0;
@@ -1241,7 +1391,9 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
       __syncthreads();
       if (flag_sh) {
         __threadfence();
-        plan_body<kFusedThreads>(d.plan, dsm);
+        plan_body<NT>(d.plan, dsm, true);
+      } else {
+        cp_async_wait_all();   // the prestaged copies land before this CTA moves on
       }
       __threadfence();
       __syncthreads();
@@ -1369,11 +1521,40 @@ int launch_mode(Args a, const CUtensorMap& mb, cudaStream_t s) {
 
 }  // namespace tc
 
+// uint8 tensor [d2][d1][d0] (d0 contiguous), byte strides s1, s2; box 64 x 128 x 1, no swizzle.
+static bool make_map_u8_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
+                           uint64_t s2) {
+  auto fn = tc::encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {s1, s2};
+  cuuint32_t box[3] = {(cuuint32_t)tc::BK, (cuuint32_t)tc::BM, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 TcMaps* tc_maps_create(const PoolDev& p, const Scratch& sc) {
-  (void)p;
   (void)sc;
   if (!tc::encode_fn()) return nullptr;
-  return new TcMaps();
+  TcMaps* m = new TcMaps();
+  if (p.wdt == MOE_FP8_E4M3_B128) {
+    m->fp8 = true;
+    const uint64_t H = p.H, I = p.I, n = p.n_records, rec = p.lay.rec;
+    if (!make_map_u8_3d(&m->w13, p.records + p.lay.off13, H, 2 * I, n, H, rec) ||
+        !make_map_u8_3d(&m->w2, p.records + p.lay.off2, I, H, n, I, rec)) {
+      delete m;
+      return nullptr;
+    }
+  }
+  return m;
+}
+
+// fp8 weights on the tensor cores: shapes whose tiles and scale rows the kernels cover
+bool tc_fp8_ok(const PoolDev& p) {
+  return p.H % 128 == 0 && p.I % 128 == 0 && p.H / 128 <= 64 && p.I / 128 <= 64 && p.lay.off2 % 16 == 0 &&
+         p.lay.rec % 16 == 0;
 }
 
 void tc_maps_destroy(TcMaps* m) { delete m; }
@@ -1473,7 +1654,12 @@ static bool fused_setup(const PoolDev& p, const Scratch& sc, int T, const void* 
   tc::FusedArgs f;
   f.jobs = sc.copies;
   f.n_jobs = sc.n_copy;
-  f.tile16 = tile16(p);
+  // a bf16 record's tile data; an fp8 record whole (codes, then its scale tables)
+  f.tile16 = p.wdt == MOE_FP8_E4M3_B128 ? (uint32_t)(p.lay.rec / 16) : tile16(p);
+  f.os13 = p.lay.offs13;
+  f.os2 = p.lay.offs2;
+  f.sc_h = p.H / 128;
+  f.sc_i = p.I / 128;
   f.elist = sc.elist;
   f.ecount = sc.ecount;
   f.E1 = p.E + 1;
@@ -1493,10 +1679,10 @@ static bool fused_setup(const PoolDev& p, const Scratch& sc, int T, const void* 
 
 static size_t fused_smem(int N, int stages) { return (size_t)stages * tc::fused_stage_bytes(N) + 1024; }
 
-static int launch_cooperative(const void* fn, size_t smem, cudaStream_t s, void** args) {
+static int launch_cooperative(const void* fn, int threads, size_t smem, cudaStream_t s, void** args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sm_count());
-  cfg.blockDim = dim3(tc::kFusedThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -1507,54 +1693,71 @@ static int launch_cooperative(const void* fn, size_t smem, cudaStream_t s, void*
   return cudaLaunchKernelExC(&cfg, fn, args) == cudaSuccess ? 1 : -2;
 }
 
+static void set_smem_attr_once(const void* fn, bool* configured) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!configured[dev & 63]) {
+    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemBudget + 1024);
+    configured[dev & 63] = true;
+  }
+}
+
 // Fused dense decode FFN (miss copies + gate/up + down + combine), one cooperative launch.
-int launch_tc_fused_decode(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, const void* x, void* out,
-                           cudaStream_t s) {
-  (void)m;
+template <int WF>
+static int launch_fused_decode_wf(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, const void* x,
+                                  void* out, cudaStream_t s) {
   tc::Args a;
   tc::FusedArgs f;
   CUtensorMap xm, hm;
   if (!fused_setup(p, sc, T, x, out, &a, &f, &xm, &hm)) return -1;
+  CUtensorMap w13 = WF == tc::kWfFp8 ? m->w13 : xm, w2 = WF == tc::kWfFp8 ? m->w2 : xm;
   static bool configured[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (!configured[dev & 63]) {
-    cudaFuncSetAttribute(tc::tc_fused_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         tc::kSmemBudget + 1024);
-    configured[dev & 63] = true;
-  }
-  void* args[] = {&xm, &hm, &a, &f};
-  return launch_cooperative(reinterpret_cast<const void*>(tc::tc_fused_decode_kernel), fused_smem(a.N, a.stages), s,
-                            args);
+  const void* fn = reinterpret_cast<const void*>(tc::tc_fused_decode_kernel<WF>);
+  set_smem_attr_once(fn, configured);
+  void* args[] = {&xm, &hm, &w13, &w2, &a, &f};
+  return launch_cooperative(fn, tc::FusedShape<WF>::threads, fused_smem(a.N, a.stages), s, args);
 }
 
-// Shared memory of the decode layer kernel's plan (256 threads), 0 if it does not fit.
+int launch_tc_fused_decode(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, const void* x, void* out,
+                           cudaStream_t s) {
+  return m->fp8 ? launch_fused_decode_wf<tc::kWfFp8>(p, sc, m, T, x, out, s)
+                : launch_fused_decode_wf<tc::kWfBf16>(p, sc, m, T, x, out, s);
+}
+
+// Shared memory of the decode layer kernel's plan (NT threads), 0 if it does not fit.
+template <int NT>
 static size_t decode_plan_smem(const PoolDev& p, int T, int* cap, int* rows) {
-  const size_t b = plan_smem_bytes_nt<tc::kFusedThreads>(p, T, cap, rows, tc::kSmemBudget - 1024);
+  const size_t b = plan_smem_bytes_nt<NT>(p, T, cap, rows, tc::kSmemBudget - 1024);
   return b + 16 <= (size_t)tc::kSmemBudget ? b + 16 : 0;
 }
 
 bool tc_decode_layer_ok(const PoolDev& p, const Scratch& sc, int T) {
   int cap = 0, rows = 0;
+  const size_t psm = p.wdt == MOE_FP8_E4M3_B128
+                         ? decode_plan_smem<tc::FusedShape<tc::kWfFp8>::threads>(p, T, &cap, &rows)
+                         : decode_plan_smem<tc::FusedShape<tc::kWfBf16>::threads>(p, T, &cap, &rows);
   return sc.dsync != nullptr && p.adt == MOE_BF16 && T >= 1 && T <= tc::kDecodeMaxT && tc_npad(T) <= sc.npad_max &&
-         p.H % 8 == 0 && (size_t)p.H * 2 + 16 <= (size_t)tc::kSmemBudget && decode_plan_smem(p, T, &cap, &rows) > 0;
+         p.H % 8 == 0 && (size_t)p.H * 2 + 16 <= (size_t)tc::kSmemBudget && psm > 0;
 }
 
 // Router, gate, plan and fused FFN of one decode call, one cooperative launch.
-int launch_tc_decode_layer(const PoolDev& p, const Scratch& sc, const TcMaps* m, int layer, int T, const void* x,
-                           const void* router_w, const float* router_b, void* out, cudaStream_t s) {
-  (void)m;
+template <int WF>
+static int launch_decode_layer_wf(const PoolDev& p, const Scratch& sc, const TcMaps* m, int layer, int T,
+                                  const void* x, const void* router_w, const float* router_b, void* out,
+                                  cudaStream_t s) {
+  constexpr int NT = tc::FusedShape<WF>::threads;
   tc::Args a;
   tc::FusedArgs f;
   CUtensorMap xm, hm;
   if (!fused_setup(p, sc, T, x, out, &a, &f, &xm, &hm)) return -1;
+  CUtensorMap w13 = WF == tc::kWfFp8 ? m->w13 : xm, w2 = WF == tc::kWfFp8 ? m->w2 : xm;
   tc::DecodeArgs d;
   d.x = static_cast<const uint16_t*>(x);
   d.wr = static_cast<const uint16_t*>(router_w) + (size_t)layer * p.E * p.H;
   d.rb = router_b + (size_t)layer * p.E;
   d.z = sc.logits;
   const int G = sm_count();
-  int nblk = std::max(1, std::min(G / T, (p.E + 7) / 8));
+  int nblk = std::max(1, std::min((G - 1) / T, (p.E + 7) / 8));   // CTA 0 plans, the others route
   d.eb = (p.E + nblk - 1) / nblk;
   d.nblk = (p.E + d.eb - 1) / d.eb;
   PlanArgs& pa = d.plan;
@@ -1568,20 +1771,21 @@ int launch_tc_decode_layer(const PoolDev& p, const Scratch& sc, const TcMaps* m,
   pa.ids = sc.ids;
   pa.w = sc.w;
   pa.probs = sc.probs;
-  const size_t psm = decode_plan_smem(p, T, &pa.owner_cap, &pa.tok_rows);
+  const size_t psm = decode_plan_smem<NT>(p, T, &pa.owner_cap, &pa.tok_rows);
   if (psm == 0) return -1;
   d.dsync = sc.dsync;
   const size_t smem = std::max(std::max(fused_smem(a.N, a.stages), psm + 1024), (size_t)p.H * 2 + 16 + 1024);
   static bool configured[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (!configured[dev & 63]) {
-    cudaFuncSetAttribute(tc::tc_decode_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         tc::kSmemBudget + 1024);
-    configured[dev & 63] = true;
-  }
-  void* args[] = {&xm, &hm, &a, &f, &d};
-  return launch_cooperative(reinterpret_cast<const void*>(tc::tc_decode_layer_kernel), smem, s, args);
+  const void* fn = reinterpret_cast<const void*>(tc::tc_decode_layer_kernel<WF>);
+  set_smem_attr_once(fn, configured);
+  void* args[] = {&xm, &hm, &w13, &w2, &a, &f, &d};
+  return launch_cooperative(fn, NT, smem, s, args);
+}
+
+int launch_tc_decode_layer(const PoolDev& p, const Scratch& sc, const TcMaps* m, int layer, int T, const void* x,
+                           const void* router_w, const float* router_b, void* out, cudaStream_t s) {
+  return m->fp8 ? launch_decode_layer_wf<tc::kWfFp8>(p, sc, m, layer, T, x, router_w, router_b, out, s)
+                : launch_decode_layer_wf<tc::kWfBf16>(p, sc, m, layer, T, x, router_w, router_b, out, s);
 }
 
 }  // namespace moeslot

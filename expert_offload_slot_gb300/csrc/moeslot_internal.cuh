@@ -157,6 +157,7 @@ int launch_ffn_down(const PoolDev& p, const Scratch& sc, int T, void* out, cudaS
 // tensor-core (tcgen05) expert path: bf16 weights, T <= 256 tokens
 struct TcMaps;                      // host-side tensor maps of a pool (k_tc.cu)
 TcMaps* tc_maps_create(const PoolDev& p, const Scratch& sc);
+bool tc_fp8_ok(const PoolDev& p);   // fp8 pool shapes the tensor-core kernels take
 void tc_maps_destroy(TcMaps* m);
 int tc_npad(int T);                 // padded token count (multiple of 16)
 // scratch sizes for a pool whose dense path takes up to npad_max token columns

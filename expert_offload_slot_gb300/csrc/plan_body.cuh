@@ -104,10 +104,41 @@ __device__ __forceinline__ void stage_copy(T* dst, const T* __restrict__ src, in
   }
 }
 
-// The plan of one layer call, run by all NT threads of one CTA.  dsm: dynamic shared
-// memory laid out by plan_smem_layout(E, W, a.tok_rows, a.owner_cap, NT / 32).
+// Asynchronous global -> shared copy of n bytes (cp.async, no registers): 16-byte
+// pieces while both addresses are 16-byte aligned, the rest with plain loads.  The
+// copies land by the next cp_async_wait_all() of each issuing thread.
 template <int NT>
-__device__ void plan_body(const PlanArgs& a, uint8_t* dsm) {
+__device__ __forceinline__ void stage_async(void* dst, const void* src, size_t n) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  const char* sp = static_cast<const char*>(src);
+  size_t n16 = ((d | reinterpret_cast<uintptr_t>(sp)) & 15u) == 0 ? n / 16 : 0;
+  for (size_t i = threadIdx.x; i < n16; i += NT)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d + (uint32_t)(16 * i)), "l"(sp + 16 * i) : "memory");
+  for (size_t i = 16 * n16 + threadIdx.x; i < n; i += NT) static_cast<char*>(dst)[i] = sp[i];
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// The parts of the plan's input that do not depend on the step's routing (the
+// layer's history rings and the owner of every slot): started early, in flight
+// until plan_body waits for them.
+template <int NT>
+__device__ void plan_prestage(const PlanArgs& a, uint8_t* dsm) {
+  const PoolDev& p = a.p;
+  const int E = p.E, l = a.layer, W = p.W;
+  const SmemLayout SL = plan_smem_layout(E, W, a.tok_rows, a.owner_cap, NT / 32);
+  if (a.flags & PLAN_HISTORY) {
+    stage_async<NT>(dsm + SL.hs, p.hist_s + (size_t)l * W * E, (size_t)W * E * 4);
+    stage_async<NT>(dsm + SL.hsel, p.hist_sel + (size_t)l * W * E, (size_t)W * E);
+  }
+  if ((a.flags & PLAN_CACHE) && a.owner_cap >= p.S) stage_async<NT>(dsm + SL.owner, p.owner, (size_t)p.S * 4);
+}
+
+// The plan of one layer call, run by all NT threads of one CTA.  dsm: dynamic shared
+// memory laid out by plan_smem_layout(E, W, a.tok_rows, a.owner_cap, NT / 32);
+// prestaged: plan_prestage<NT> already ran on this CTA.
+template <int NT>
+__device__ void plan_body(const PlanArgs& a, uint8_t* dsm, bool prestaged = false) {
   constexpr int kPlanThreads = NT;
   constexpr int kPlanWarps = NT / 32;
   __shared__ int cnt[kMaxE];
@@ -160,16 +191,15 @@ __device__ void plan_body(const PlanArgs& a, uint8_t* dsm) {
   int t_step = 0;
   float ema0 = 0.f;
   int last0 = -1;
+  if (!prestaged) plan_prestage<NT>(a, dsm);
   if (ids_in_smem) {
-    stage_copy<NT>(ids_s, a.ids, Tk);
-    if (a.w && (a.flags & PLAN_PERMUTE)) stage_copy<NT>(w_s, a.w, Tk);
+    stage_async<NT>(ids_s, a.ids, (size_t)Tk * 4);
+    if (a.w && (a.flags & PLAN_PERMUTE)) stage_async<NT>(w_s, a.w, (size_t)Tk * 4);
   }
   if (hist) {
     t_step = p.step[l];
-    stage_copy<NT>(hs, p.hist_s + (size_t)l * W * E, W * E);
-    stage_copy<NT>(hsel, p.hist_sel + (size_t)l * W * E, W * E);
     if (T <= kTokBlock) {
-      stage_copy<NT>(tok, a.probs, T * E);
+      stage_async<NT>(tok, a.probs, (size_t)T * E * 4);
     } else {
       // block partial sums: tok[b][e] = sum of probs over tokens [32b, 32b+32), ascending
       const int nblk = (T + kTokBlock - 1) / kTokBlock;
@@ -193,11 +223,10 @@ __device__ void plan_body(const PlanArgs& a, uint8_t* dsm) {
   }
   if (cache) {
     if (tid < E) lut_s[tid] = p.lut[(size_t)l * E + tid];
-    if (owner_in_smem) {
-      stage_copy<NT>(owner_s, p.owner, p.S);
+    if (owner_in_smem)
       for (int j = tid; j < (p.S + 31) / 32; j += kPlanThreads) prot[j] = 0u;
-    }
   }
+  cp_async_wait_all();
   __syncthreads();
   for (int i = tid; i < Tk; i += kPlanThreads) {
     const int e = ids[i];
@@ -446,8 +475,26 @@ __device__ void plan_body(const PlanArgs& a, uint8_t* dsm) {
     for (int e = tid; e < E; e += kPlanThreads) base[e] = offs[e];
     for (int e = tid; e <= E; e += kPlanThreads) a.sc.offs[e] = offs[e];
     __syncthreads();
-    // stable scatter, 1024 entries per pass
-    for (int c0 = 0; c0 < Tk; c0 += kPlanThreads) {
+    if (Tk <= kPlanThreads) {
+      // one entry per thread: its rank among the earlier entries of the same expert
+      const int i = tid;
+      int e = -1;
+      if (i < Tk) {
+        e = ids[i];
+        if ((unsigned)e >= (unsigned)E) e = -1;
+      }
+      if (e >= 0) {
+        int rank = 0;
+        for (int j = 0; j < i; ++j) rank += ids[j] == e;
+        const int r = offs[e] + rank;
+        a.sc.perm_tok[r] = i / k;
+        a.sc.perm_w[r] = wrt[i];
+        a.sc.perm_ent[r] = i;
+        if (a.flags & PLAN_GATHER) a.sc.inv[i] = r;
+      }
+    }
+    // stable scatter, kPlanThreads entries per pass
+    for (int c0 = 0; Tk > kPlanThreads && c0 < Tk; c0 += kPlanThreads) {
       const int i = c0 + tid;
       int e = -1;
       if (i < Tk) {

@@ -209,8 +209,11 @@ MOE_API moe_status moe_get_stats(moe_pool* pool, moe_stats* out);
 /* Per-stage timing with CUDA events (off by default).  While enabled, every
  * forward records pool-owned events on its stream between its stages (inside
  * a captured graph they become event nodes); moe_profile_read returns, for the
- * latest forward of `layer`, the elapsed milliseconds of each stage.  Enabling
- * creates L*(MOE_NUM_STAGES+1) events and is blocking. */
+ * latest forward of `layer`, the elapsed milliseconds of each stage.  When the
+ * forward ran as one decode layer kernel (bf16 weights, T <= 32: router, gate,
+ * plan and experts in one launch) the whole call is reported under
+ * MOE_STAGE_FFN and the other stages are 0.  Enabling creates
+ * L*(MOE_NUM_STAGES+1) events and is blocking. */
 enum { MOE_STAGE_ROUTE = 0,     /* router GEMV + gate/top-k                        */
        MOE_STAGE_PLAN = 1,      /* history, table, victims, permutation            */
        MOE_STAGE_COPY = 2,      /* miss copies run as their own kernel (0 when the
