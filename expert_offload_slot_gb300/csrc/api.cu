@@ -355,8 +355,8 @@ MOE_API moe_status moe_pool_create(const moe_config* cfg, const void* host_pool,
     P->sc.n_ffn_sync = tc_ffn_sync_ints(d);
     PA(P->sc.ffn_sync, P->sc.n_ffn_sync, 0);
     PA(P->sc.dsync, 64, 0);
-    if ((size_t)tc_npad((int)Tm) > (size_t)np && cfg->weight_dtype == MOE_BF16) {
-      // gather path for calls with more tokens than the dense path takes (bf16 weights)
+    if ((size_t)tc_npad((int)Tm) > (size_t)np) {
+      // gather path for calls with more tokens than the dense path takes
       PA(P->sc.inv, Tm * k, 0);
       PA(P->sc.ntile0, E + 2, 0);
       PA(P->sc.n_rows, 1, 0);
@@ -490,7 +490,7 @@ static moe_status run_layer(moe_pool* P, int layer, const void* x, int T, void* 
   mark(0);
   const bool tc = P->tc_maps != nullptr;                 // bf16 or fp8 weights: tensor-core path
   const bool use_tc = tc && tc_npad(T) <= sc.npad_max;   // dense token columns
-  const bool gather = tc && !use_tc && d.wdt == MOE_BF16; // expert-grouped token tiles
+  const bool gather = tc && !use_tc;                     // expert-grouped token tiles
   if (use_tc && !ids_in && !staged && tc_decode_layer_ok(d, sc, T)) {
     // router, gate, plan, miss copies, gate/up, down and combine in one cooperative kernel;
     // its profile is one interval (mark 0 to mark 4)

@@ -361,15 +361,84 @@ __device__ __forceinline__ void store_chunk(const Args& a, const UnitRange& r, i
   }
 }
 
-template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
-tc_expert_kernel(const __grid_constant__ CUtensorMap map_b, Args a) {
+// Weight formats: bf16 records pre-tiled in the MMA's swizzled order (bulk
+// copies), or fp8 e4m3 row-major records with one fp32 scale per 128 x 128
+// block (TMA tiles of codes, expanded to bf16 in place by converter warps, the
+// block scale applied in the expansion).
+constexpr int kWfBf16 = 0, kWfFp8 = 1;
+constexpr int kConvWarps = 4;
+
+// Converter warps (ct = 0..127): expand the fp8 code tiles q < nt of one stage in
+// place.  Each tile slot is 16 KB; its codes (128 rows x 64 bytes) sit in the
+// upper 8 KB.  Every thread reads its 4 x 16 code bytes of each tile, then (after
+// the named barrier, all reads done) writes them back as bf16 (code * scale, one
+// rounding) in the 128-byte-swizzled order.  Every converter thread calls this
+// for every stage, work or not, so the named barrier is always complete.
+__device__ __forceinline__ void fp8_expand_stage(uint8_t* st, int nt, float s0, float s1, int ct, bool work) {
+  uint4 raw[2][4];
+  if (work) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+      if (q < nt) {
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+          raw[q][m] = *reinterpret_cast<const uint4*>(st + q * kTileBytes + kTileBytes / 2 + (ct + 128 * m) * 16);
+      }
+  }
+  asm volatile("bar.sync 3, %0;" ::"n"(32 * kConvWarps) : "memory");
+  if (!work) return;
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+    if (q < nt) {
+      const float sv = q ? s1 : s0;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int c16 = ct + 128 * m, row = c16 >> 2, cq = c16 & 3;   // 16 codes: columns cq*16..+16
+        const uint32_t w4[4] = {raw[q][m].x, raw[q][m].y, raw[q][m].z, raw[q][m].w};
+        uint32_t o[8];
+#pragma unroll
+        for (int wq = 0; wq < 4; ++wq) {
+          float v[4];
+          e4m3x4_to_f32(w4[wq], v);
+          o[2 * wq] = pack_bf16x2(v[0] * sv, v[1] * sv);
+          o[2 * wq + 1] = pack_bf16x2(v[2] * sv, v[3] * sv);
+        }
+        uint8_t* rowp = st + q * kTileBytes + row * 128;
+        const int c0 = 2 * cq;
+        *reinterpret_cast<uint4*>(rowp + ((c0 ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ (row & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+      }
+    }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> MMA reads
+}
+
+// fp8 record geometry for the converters: scale tables at os13 ([2I/128][H/128]
+// fp32) and os2 ([H/128][I/128]).
+struct Fp8Args {
+  size_t os13, os2;
+  int sc_h, sc_i;               // H / 128, I / 128
+};
+
+template <int WF> struct GatherShape {
+  static constexpr int threads = kThreads + (WF == kWfFp8 ? 32 * kConvWarps : 0);
+};
+
+// Gather modes (T > 256 tokens): unit = (entry u, 128-token tile nt, 128-row tile
+// mt), full K.  Gate/up: A = gate and up tiles of the entry, B = its gathered x
+// rows; epilogue h = w * SiLU(g) * u per row.  Down: A = W_down tile, B = its h
+// rows; epilogue one bf16 row of y per (token, expert).
+template <int MODE, int WF>
+__global__ void __launch_bounds__(GatherShape<WF>::threads, 1)
+tc_gather_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_w, Args a,
+                 Fp8Args w8) {
   constexpr int NACC = is_gate_up(MODE) ? 2 : 1;
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t conv_bar[WF == kWfFp8 ? kMaxStages : 1];
   __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
+  __shared__ float scale_sh[WF == kWfFp8 ? 2 : 1][WF == kWfFp8 ? 128 : 1];
   __shared__ uint32_t tmem_base_sh;
-  __shared__ volatile int abort_sh, last_sh;
+  __shared__ volatile int abort_sh;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -379,7 +448,6 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap map_b, Args a) {
   const uint32_t a_bytes = NACC * kTileBytes;                 // 16 KB (down) or 32 KB (gate + up)
   const uint32_t b_bytes = (uint32_t)N * BK * 2;              // N rows of 128 B
   const uint32_t stage_bytes = (a_bytes + b_bytes + 1023) & ~1023u;
-  // two accumulator buffers when they fit, so one unit's epilogue overlaps the next unit's MMAs
   const int nbuf = 2 * NACC * N <= 512 ? 2 : 1;
   const uint32_t acc_cols = (uint32_t)(NACC * N);
   uint32_t ncols = 32;
@@ -389,6 +457,7 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap map_b, Args a) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
+      if (WF == kWfFp8) mbar_init(&conv_bar[s], 32 * kConvWarps);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull_bar[b], 1);
@@ -415,22 +484,29 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap map_b, Args a) {
       bool ok = true;
       for (int unit = blockIdx.x; unit < pl.units && ok; unit += gridDim.x) {
         const UnitRange r = unit_range<MODE>(pl, a, unit);
-        for (int u = r.u0; u < r.u1 && ok; ++u) {
-          const WorkEntry we = a.work[u];
-          const uint8_t* wbase = a.records + (size_t)we.rid * a.rec +
-                                 (is_gate_up(MODE) ? a.off13 : a.off2) +
-                                 (size_t)r.mt * kb_per_row * a_bytes;
-          const int brow = is_gather(MODE) ? we.row0 + r.nt * kGatherBN : 0;
-          for (int kb = r.kb0; kb < r.kb1; ++kb, ++it) {
-            const int s = it % S;
-            if (it >= (uint32_t)S && !mbar_wait(&empty_bar[s], ((it / S) - 1) & 1)) { ok = false; break; }
-            if (abort_sh) { ok = false; break; }
-            uint8_t* st = smem + (size_t)s * stage_bytes;
+        const WorkEntry we = a.work[r.u0];
+        const uint8_t* wbase = a.records + (size_t)we.rid * a.rec + (is_gate_up(MODE) ? a.off13 : a.off2) +
+                               (size_t)r.mt * kb_per_row * a_bytes;
+        const int brow = we.row0 + r.nt * kGatherBN;
+        for (int kb = r.kb0; kb < r.kb1; ++kb, ++it) {
+          const int s = it % S;
+          if (it >= (uint32_t)S && !mbar_wait(&empty_bar[s], ((it / S) - 1) & 1)) { ok = false; break; }
+          if (abort_sh) { ok = false; break; }
+          uint8_t* st = smem + (size_t)s * stage_bytes;
+          if (WF == kWfFp8) {
+            const uint32_t raw = kTileBytes / 2;
+            mbar_expect_tx(&full_bar[s], NACC * raw + b_bytes);
+            if (is_gate_up(MODE)) {
+              tma_load_3d(st + raw, &map_w, &full_bar[s], kb * BK, r.mt * BM, we.rid);
+              tma_load_3d(st + kTileBytes + raw, &map_w, &full_bar[s], kb * BK, a.I + r.mt * BM, we.rid);
+            } else {
+              tma_load_3d(st + raw, &map_w, &full_bar[s], kb * BK, r.mt * BM, we.rid);
+            }
+          } else {
             mbar_expect_tx(&full_bar[s], a_bytes + b_bytes);
             bulk_load(st, wbase + (size_t)kb * a_bytes, a_bytes, &full_bar[s]);
-            const int bsel = MODE == kModeDown ? u : 0;
-            tma_load_3d(st + a_bytes, &map_b, &full_bar[s], kb * BK, brow, bsel);
           }
+          tma_load_3d(st + a_bytes, &map_b, &full_bar[s], kb * BK, brow, 0);
         }
       }
       if (!ok) {
@@ -459,23 +535,21 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap map_b, Args a) {
         fence_after();
         const uint32_t dacc = tmem + (uint32_t)buf * acc_cols;
         uint32_t acc = 0;
-        for (int u = r.u0; u < r.u1 && ok; ++u) {
-          for (int kb = r.kb0; kb < r.kb1; ++kb, ++it) {
-            const int s = it % S;
-            if (!mbar_wait(&full_bar[s], (it / S) & 1) || abort_sh) { ok = false; break; }
-            fence_after();
-            const uint32_t base = smem_u32(smem + (size_t)s * stage_bytes);
-            const uint64_t da = desc_sw128(base);
-            const uint64_t db = desc_sw128(base + a_bytes);
+        for (int kb = r.kb0; kb < r.kb1; ++kb, ++it) {
+          const int s = it % S;
+          if (!mbar_wait(WF == kWfFp8 ? &conv_bar[s] : &full_bar[s], (it / S) & 1) || abort_sh) { ok = false; break; }
+          fence_after();
+          const uint32_t base = smem_u32(smem + (size_t)s * stage_bytes);
+          const uint64_t da = desc_sw128(base);
+          const uint64_t db = desc_sw128(base + a_bytes);
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
-              // advance 16 bf16 = 32 bytes along K inside the swizzle atom
-              mma_bf16(dacc, da + 2 * kk, db + 2 * kk, idesc, acc);
-              if (NACC == 2) mma_bf16(dacc + N, da + (kTileBytes >> 4) + 2 * kk, db + 2 * kk, idesc, acc);
-              acc = 1;
-            }
-            mma_commit(&empty_bar[s]);
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            // advance 16 bf16 = 32 bytes along K inside the swizzle atom
+            mma_bf16(dacc, da + 2 * kk, db + 2 * kk, idesc, acc);
+            if (NACC == 2) mma_bf16(dacc + N, da + (kTileBytes >> 4) + 2 * kk, db + 2 * kk, idesc, acc);
+            acc = 1;
           }
+          mma_commit(&empty_bar[s]);
         }
         if (ok) mma_commit(&tfull_bar[buf]);
       }
@@ -487,10 +561,8 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap map_b, Args a) {
       mma_commit(&drain_bar);
       mbar_wait(&drain_bar, 0);
     }
-  } else {
+  } else if (warp < kThreads / 32) {
     // ------------------------------------------------------------- epilogue (warps 2..5)
-    // Every epilogue warp runs the same number of iterations and reaches every
-    // named barrier even after a timeout, so no warp can be left waiting.
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;          // tile row == TMEM lane
     const uint32_t trow0 = tmem + ((uint32_t)(q * 32) << 16);
@@ -499,91 +571,58 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap map_b, Args a) {
       const UnitRange r = unit_range<MODE>(pl, a, unit);
       const int buf = local % nbuf;
       const uint32_t trow = trow0 + (uint32_t)buf * acc_cols;
-      bool live = !abort_sh;
-      if (live && !mbar_wait(&tfull_bar[buf], (local / nbuf) & 1)) {
+      if (abort_sh) continue;
+      if (!mbar_wait(&tfull_bar[buf], (local / nbuf) & 1)) {
         set_status(a.status, MOE_ERR_TIMEOUT);
         abort_sh = 1;
-        live = false;
+        continue;
       }
-      if (live) fence_after();
+      fence_after();
       const int m = r.mt * BM + row;                           // output row (i for gate/up, h for down)
-      int row_base = 0, row_end = 0;
-      if (is_gather(MODE)) {
-        const WorkEntry we = a.work[r.u0];
-        row_base = we.row0 + r.nt * kGatherBN;
-        row_end = we.row0 + we.n;
+      const WorkEntry we = a.work[r.u0];
+      const int row_base = we.row0 + r.nt * kGatherBN, row_end = we.row0 + we.n;
+      for (int c0 = 0; c0 < N; c0 += 16) {
+        float d0[16], d1[16];
+        tmem_ld16(trow + c0, d0);
+        if (NACC == 2) tmem_ld16(trow + N + c0, d1);
+        store_chunk<MODE>(a, r, m, c0, d0, d1, row_base, row_end);
       }
-      if (pl.splits == 1) {
-        if (!live) continue;
-        for (int c0 = 0; c0 < N; c0 += 16) {
-          float d0[16], d1[16];
-          tmem_ld16(trow + c0, d0);
-          if (NACC == 2) tmem_ld16(trow + N + c0, d1);
-          store_chunk<MODE>(a, r, m, c0, d0, d1, row_base, row_end);
-        }
-        fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty_bar[buf]);
-      } else {
-        if (live) {
-          // this split's partial tile, [acc][column][row] fp32
-          float* mine = a.partial + ((size_t)r.tile * pl.splits + r.split) * NACC * N * BM;
-          for (int c0 = 0; c0 < N; c0 += 16) {
-            float d0[16], d1[16];
-            tmem_ld16(trow + c0, d0);
-            if (NACC == 2) tmem_ld16(trow + N + c0, d1);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              mine[(size_t)(c0 + j) * BM + row] = d0[j];
-              if (NACC == 2) mine[(size_t)N * BM + (size_t)(c0 + j) * BM + row] = d1[j];
-            }
-          }
-          fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tempty_bar[buf]);
-          __threadfence();
-        }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (warp == 2 && lane == 0) {
-          last_sh = 0;
-          if (!abort_sh) {
-            const int old = atomicAdd(&a.counters[r.tile], 1);
-            if (old == pl.splits - 1) {
-              last_sh = 1;
-              a.counters[r.tile] = 0;
-            }
-          }
-        }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (last_sh && live) {
-          __threadfence();
-          const float* base = a.partial + (size_t)r.tile * pl.splits * NACC * N * BM;
-          for (int c0 = 0; c0 < N; c0 += 16) {
-            // 16 columns at a time: each split's 16 (x2) values are loaded together,
-            // then added in split order (deterministic)
-            float s0[16], s1[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) { s0[j] = 0.f; s1[j] = 0.f; }
-            for (int sp = 0; sp < pl.splits; ++sp) {
-              const float* pt = base + (size_t)sp * NACC * N * BM + (size_t)c0 * BM + row;
-              float v0[16], v1[16];
-#pragma unroll
-              for (int j = 0; j < 16; ++j) v0[j] = __ldcg(pt + (size_t)j * BM);
-              if (NACC == 2) {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) v1[j] = __ldcg(pt + (size_t)N * BM + (size_t)j * BM);
-              }
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                s0[j] += v0[j];
-                if (NACC == 2) s1[j] += v1[j];
-              }
-            }
-            store_chunk<MODE>(a, r, m, c0, s0, s1, row_base, row_end);
-          }
-        }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
+      fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+    }
+  } else if (WF == kWfFp8) {
+    // ------------------------------------------------------------- converter warps (fp8)
+    const int ct = threadIdx.x - kThreads;        // 0..127
+    uint32_t it = 0;
+    int local = 0;
+    bool stop = false;
+    for (int unit = blockIdx.x; unit < pl.units; unit += gridDim.x, ++local) {
+      const UnitRange r = unit_range<MODE>(pl, a, unit);
+      const WorkEntry we = a.work[r.u0];
+      const float* scl =
+          reinterpret_cast<const float*>(a.records + (size_t)we.rid * a.rec + (is_gate_up(MODE) ? w8.os13 : w8.os2));
+      const int b0 = r.kb0 / 2, nblk = (r.kb1 - 1) / 2 - b0 + 1;
+      const int sbuf = local & 1;
+      if (ct < nblk) {
+        scale_sh[sbuf][ct] = scl[(size_t)(is_gate_up(MODE) ? r.mt * w8.sc_h : r.mt * w8.sc_i) + b0 + ct];
+      } else if (is_gate_up(MODE) && ct >= 64 && ct - 64 < nblk) {
+        scale_sh[sbuf][ct] = scl[(size_t)(a.I / BM + r.mt) * w8.sc_h + b0 + (ct - 64)];
       }
+      asm volatile("bar.sync 3, %0;" ::"n"(32 * kConvWarps) : "memory");
+      for (int kb = r.kb0; kb < r.kb1; ++kb, ++it) {
+        const int s = it % S;
+        if (!stop && (!mbar_wait(&full_bar[s], (it / S) & 1) || abort_sh)) {
+          stop = true;
+          set_status(a.status, MOE_ERR_TIMEOUT);
+          abort_sh = 1;
+        }
+        const float s0 = scale_sh[sbuf][kb / 2 - b0];
+        const float s1 = is_gate_up(MODE) ? scale_sh[sbuf][64 + kb / 2 - b0] : 0.f;
+        fp8_expand_stage(smem + (size_t)s * stage_bytes, NACC, s0, s1, ct, !stop);
+        if (!stop) mbar_arrive(&conv_bar[s]);
+      }
+      asm volatile("bar.sync 3, %0;" ::"n"(32 * kConvWarps) : "memory");   // before the scale buffer is reused
     }
   }
   fence_before();
@@ -619,12 +658,6 @@ constexpr int kCopyWarps = 2;
 constexpr int kCopyUnroll = 16;  // 16-byte host reads in flight per copy lane
 constexpr int kFusedThreads = kThreads + 32 * kCopyWarps;
 constexpr int kFusedBufs = 8;
-// Weight formats of the fused kernels: bf16 records pre-tiled in the MMA's
-// swizzled order (bulk copies), or fp8 e4m3 row-major records with one fp32
-// scale per 128 x 128 block (TMA tiles of codes, expanded to bf16 in place by
-// converter warps, the block scale applied in the expansion).
-constexpr int kWfBf16 = 0, kWfFp8 = 1;
-constexpr int kConvWarps = 4;
 template <int WF> struct FusedShape {
   static constexpr int conv_warps = WF == kWfFp8 ? kConvWarps : 0;
   static constexpr int conv_warp0 = kThreads / 32;               // after the epilogue warps
@@ -1142,45 +1175,11 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
           asm volatile("bar.sync 3, %0;" ::"n"(32 * kConvWarps) : "memory");
           first = false;
         }
-        uint8_t* st = smem + (size_t)s * stage_bytes;
         const int nt = r.gu ? 2 : min(2, r.kb1 - kb);
-        uint4 raw[2][4];
-        if (!stop) {
-#pragma unroll
-          for (int q = 0; q < 2; ++q)
-            if (q < nt) {
-#pragma unroll
-              for (int m = 0; m < 4; ++m)
-                raw[q][m] = *reinterpret_cast<const uint4*>(st + q * kTileBytes + kTileBytes / 2 + (ct + 128 * m) * 16);
-            }
-        }
-        asm volatile("bar.sync 3, %0;" ::"n"(32 * kConvWarps) : "memory");
-        if (!stop) {
-#pragma unroll
-          for (int q = 0; q < 2; ++q)
-            if (q < nt) {
-              const float sv = r.gu ? scale_sh[sbuf][(q ? 64 : 0) + kb / 2 - b0] : scale_sh[sbuf][(kb + q) / 2 - b0];
-#pragma unroll
-              for (int m = 0; m < 4; ++m) {
-                const int c16 = ct + 128 * m, row = c16 >> 2, cq = c16 & 3;   // 16 codes: columns cq*16..+16
-                const uint32_t w4[4] = {raw[q][m].x, raw[q][m].y, raw[q][m].z, raw[q][m].w};
-                uint32_t o[8];
-#pragma unroll
-                for (int wq = 0; wq < 4; ++wq) {
-                  float v[4];
-                  e4m3x4_to_f32(w4[wq], v);
-                  o[2 * wq] = pack_bf16x2(v[0] * sv, v[1] * sv);
-                  o[2 * wq + 1] = pack_bf16x2(v[2] * sv, v[3] * sv);
-                }
-                uint8_t* rowp = st + q * kTileBytes + row * 128;
-                const int c0 = 2 * cq;
-                *reinterpret_cast<uint4*>(rowp + ((c0 ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-                *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ (row & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
-              }
-            }
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> MMA reads
-          mbar_arrive(&conv_bar[s]);
-        }
+        const float s0 = scale_sh[sbuf][kb / 2 - b0];
+        const float s1 = r.gu ? scale_sh[sbuf][64 + kb / 2 - b0] : (nt > 1 ? scale_sh[sbuf][(kb + 1) / 2 - b0] : 0.f);
+        fp8_expand_stage(smem + (size_t)s * stage_bytes, nt, s0, s1, ct, !stop);
+        if (!stop) mbar_arrive(&conv_bar[s]);
       }
       asm volatile("bar.sync 3, %0;" ::"n"(32 * kConvWarps) : "memory");   // before the scale buffer is reused
     }
@@ -1493,14 +1492,6 @@ bool make_map_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uin
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE>
-void configure_once() {
-  static bool done = false;
-  if (!done) {
-    cudaFuncSetAttribute(tc_expert_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget + 1024);
-    done = true;
-  }
-}
 
 int stages_for(int nacc, int N) {
   const int stage = ((nacc * BM * BK * 2 + N * BK * 2) + 1023) & ~1023;
@@ -1509,13 +1500,20 @@ int stages_for(int nacc, int N) {
   return s;
 }
 
-template <int MODE>
-int launch_mode(Args a, const CUtensorMap& mb, cudaStream_t s) {
+template <int MODE, int WF>
+int launch_mode(Args a, const CUtensorMap& mb, const CUtensorMap& mw, const Fp8Args& w8, cudaStream_t s) {
   constexpr int NACC = is_gate_up(MODE) ? 2 : 1;
   a.stages = stages_for(NACC, a.N);
-  configure_once<MODE>();
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!configured[dev & 63]) {
+    cudaFuncSetAttribute(tc_gather_kernel<MODE, WF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         kSmemBudget + 1024);
+    configured[dev & 63] = true;
+  }
   const size_t smem = (size_t)a.stages * (((NACC * BM * BK * 2 + a.N * BK * 2) + 1023) & ~1023) + 1024;
-  tc_expert_kernel<MODE><<<sm_count(), kThreads, smem, s>>>(mb, a);
+  tc_gather_kernel<MODE, WF><<<sm_count(), GatherShape<WF>::threads, smem, s>>>(mb, mw, a, w8);
   return 1;
 }
 
@@ -1616,7 +1614,6 @@ static tc::Args tc_args(const PoolDev& p, const Scratch& sc, int T, int N) {
 // Gather path: xp = x rows by expert; h = gate/up per row; y = down per row; out = combine.
 int launch_tc_gather(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, const void* x, void* out,
                      cudaStream_t s) {
-  (void)m;
   const int rows_max = T * p.k + (p.shared ? T : 0);
   tc::gather_rows_kernel<<<2 * sm_count(), 256, 0, s>>>(static_cast<const uint16_t*>(x), sc.perm_tok, sc.n_rows,
                                                          sc.xp, p.H);
@@ -1627,14 +1624,22 @@ int launch_tc_gather(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T
   if (!tc::make_map_3d(&xm, sc.xp, (uint64_t)p.H, (uint64_t)rows_max, 1, (uint64_t)p.H * 2,
                        (uint64_t)p.H * 2 * rows_max, tc::kGatherBN))
     return -1;
-  int n = 1 + tc::launch_mode<tc::kModeGateUpGather>(a, xm, s);
+  tc::Fp8Args w8;
+  w8.os13 = p.lay.offs13;
+  w8.os2 = p.lay.offs2;
+  w8.sc_h = p.H / 128;
+  w8.sc_i = p.I / 128;
+  const bool fp8 = m->fp8;
+  int n = 1 + (fp8 ? tc::launch_mode<tc::kModeGateUpGather, tc::kWfFp8>(a, xm, m->w13, w8, s)
+                   : tc::launch_mode<tc::kModeGateUpGather, tc::kWfBf16>(a, xm, xm, w8, s));
   tc::Args b = a;
   b.out = sc.y;
   CUtensorMap hm;
   if (!tc::make_map_3d(&hm, sc.h, (uint64_t)p.I, (uint64_t)rows_max, 1, (uint64_t)p.I * 2,
                        (uint64_t)p.I * 2 * rows_max, tc::kGatherBN))
     return -1;
-  n += tc::launch_mode<tc::kModeDownGather>(b, hm, s);
+  n += fp8 ? tc::launch_mode<tc::kModeDownGather, tc::kWfFp8>(b, hm, m->w2, w8, s)
+           : tc::launch_mode<tc::kModeDownGather, tc::kWfBf16>(b, hm, hm, w8, s);
   tc::combine_rows_kernel<<<T, 256, 0, s>>>(sc.y, sc.inv, T, p.k, p.shared, static_cast<uint16_t*>(out), p.H);
   return n + 1;
 }

@@ -186,3 +186,22 @@ def test_bf16_dense_and_gather_paths_with_shared_expert(T):
         assert rig.pool.status() == moe.MOE_OK
     finally:
         rig.close()
+
+
+@pytest.mark.parametrize("T", [24, 300])
+def test_fp8_dense_and_gather_paths_with_shared_expert(T):
+    """fp8 e4m3 with 128x128 block scales on the tensor cores: T <= 256 on the dense path,
+    larger T on the gather path; the shared expert is streamed by every call."""
+    wl = variant(get_workload("dsv3"), name="gather_fp8", L=2, E=32, k=4, H=512, I=256, residency=0.5)
+    assert wl.weight_dtype == FP8_E4M3_B128 and wl.shared
+    rig = Rig(wl, max_tokens=320)
+    try:
+        for l in range(wl.L):
+            xs = gen.store_act(wl, gen.prefill_hidden(wl, l, T))
+            out = rig.forward(l, xs)
+            ref, r = rig.oracle_forward(l, xs)
+            ok = check_routing(rig.pool.routing(320), r, wl.k)
+            check_output(wl, out, ref, ok)
+        assert rig.pool.status() == moe.MOE_OK
+    finally:
+        rig.close()
