@@ -355,6 +355,7 @@ MOE_API moe_status moe_pool_create(const moe_config* cfg, const void* host_pool,
     P->sc.n_ffn_sync = tc_ffn_sync_ints(d);
     PA(P->sc.ffn_sync, P->sc.n_ffn_sync, 0);
     PA(P->sc.dsync, 64, 0);
+    if (Tm > 32 && cfg->act_dtype == MOE_BF16) PA(P->sc.rpart, (size_t)32 * Tm * E, 0);
     if ((size_t)tc_npad((int)Tm) > (size_t)np) {
       // gather path for calls with more tokens than the dense path takes
       PA(P->sc.inv, Tm * k, 0);
@@ -509,9 +510,16 @@ static moe_status run_layer(moe_pool* P, int layer, const void* x, int T, void* 
   if (!ids_in) {
     if (route_fused_ok(d, T)) {
       P->launches += launch_route_gate_fused(d, layer, x, T, P->router_w, P->router_b, sc, s);
+    } else if (tc_router_ok(d, sc, T)) {
+      int nsp = 0;
+      const int n = launch_tc_router(d, sc, layer, x, T, P->router_w, &nsp, s);
+      if (n < 0) return fail(MOE_ERR_INVALID, "x must be 16-byte aligned for the tensor-core router");
+      P->launches += n;
+      P->launches += launch_gate_topk(d, sc.rpart, nsp, P->router_b + (size_t)layer * d.E, T, sc.ids, sc.w,
+                                      sc.probs, sc.gap, s);
     } else {
       P->launches += launch_route_logits(d, layer, x, T, P->router_w, P->router_b, sc.logits, s);
-      P->launches += launch_gate_topk(d, sc.logits, T, sc.ids, sc.w, sc.probs, sc.gap, s);
+      P->launches += launch_gate_topk(d, sc.logits, 0, nullptr, T, sc.ids, sc.w, sc.probs, sc.gap, s);
     }
   }
   mark(1);

@@ -93,7 +93,7 @@ MOE_API moe_status moe_route_topk_noalloc(int32_t num_experts, int32_t top_k, in
   p.stats = stats;   // near-tie counter of this entry point; never read back
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   launch_route_logits(p, 0, x, T, router_w, router_b, logits, s);
-  launch_gate_topk(p, logits, T, ids, w, probs, gap, s);
+  launch_gate_topk(p, logits, 0, nullptr, T, ids, w, probs, gap, s);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? MOE_OK : set_last_error(MOE_ERR_CUDA, cudaGetErrorString(e));
 }

@@ -70,10 +70,12 @@ int launch_route_logits(const PoolDev& p, int layer, const void* x, int T, const
 // ------------------------------------------------------------------ gate + top-k
 constexpr int kGateWarps = 8;
 
+// z: the logits [T][E]; or, with nsp > 0, nsp partial sums [nsp][T][E] of the
+// projection (tensor-core router), added in split order, plus the bias.
 __global__ void __launch_bounds__(kGateWarps * 32)
-gate_topk_kernel(const float* __restrict__ z, int T, int E, int k, int gating, int32_t* __restrict__ ids,
-                 float* __restrict__ w, float* __restrict__ probs, float* __restrict__ gap,
-                 unsigned long long* stats) {
+gate_topk_kernel(const float* __restrict__ z, int nsp, const float* __restrict__ bias, int T, int E, int k,
+                 int gating, int32_t* __restrict__ ids, float* __restrict__ w, float* __restrict__ probs,
+                 float* __restrict__ gap, unsigned long long* stats) {
   __shared__ float zsel[kGateWarps][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kGateWarps + warp;
@@ -85,7 +87,15 @@ gate_topk_kernel(const float* __restrict__ z, int T, int E, int k, int gating, i
   for (int j = 0; j < kMaxPerLane; ++j) {
     const int e = lane + 32 * j;
     taken[j] = e >= E;
-    v[j] = e < E ? z[(size_t)t * E + e] : -INFINITY;
+    if (e >= E) {
+      v[j] = -INFINITY;
+    } else if (nsp > 0) {
+      float acc = 0.f;
+      for (int sp = 0; sp < nsp; ++sp) acc += z[((size_t)sp * T + t) * E + e];
+      v[j] = acc + bias[e];
+    } else {
+      v[j] = z[(size_t)t * E + e];
+    }
     zmax = fmaxf(zmax, v[j]);
   }
   zmax = warp_max(zmax);
@@ -249,10 +259,10 @@ bool route_fused_ok(const PoolDev& p, int T) {
   return T <= kFusedRouteT && p.H <= 4 * C * kFusedRouteThreads;
 }
 
-int launch_gate_topk(const PoolDev& p, const float* logits, int T, int32_t* ids, float* w, float* probs,
-                     float* gap, cudaStream_t s) {
+int launch_gate_topk(const PoolDev& p, const float* logits, int nsp, const float* bias, int T, int32_t* ids,
+                     float* w, float* probs, float* gap, cudaStream_t s) {
   const int grid = (T + kGateWarps - 1) / kGateWarps;
-  gate_topk_kernel<<<grid, kGateWarps * 32, 0, s>>>(logits, T, p.E, p.k, p.gating, ids, w, probs, gap,
+  gate_topk_kernel<<<grid, kGateWarps * 32, 0, s>>>(logits, nsp, bias, T, p.E, p.k, p.gating, ids, w, probs, gap,
                                                      p.stats);
   return 1;
 }

@@ -1299,6 +1299,7 @@ struct DecodeArgs {
 };
 
 constexpr int kDecodeMaxT = 32;
+constexpr int kRouterMaxSplits = 32;   // K splits of the tensor-core router
 constexpr int kRouteChunks = 16;   // router-row loads in flight per lane (H <= 4096 in one round)
 
 template <int WF>
@@ -1419,6 +1420,125 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
       *exit_cnt = 0u;
     }
   }
+}
+
+// ----------------------------------------------------------------- router GEMM (T > 32)
+// z = X W_r^T for many tokens on the tensor cores (RapidMoE §2.1: the gate is a
+// linear projection): unit = (128-token tile mt, K split sp), M = the tokens,
+// N = the experts (padded to 16), fp32 accumulators in TMEM.  Each unit writes
+// its partial [T][E] slice; the gate kernel adds the splits in order and the
+// bias, so the logits are deterministic.
+struct RouterArgs {
+  int T, E, N, kb_h, nsp;
+  float* part;          // [nsp][T][E]
+  int32_t* status;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+tc_router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w, RouterArgs r) {
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t tfull_bar, drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ volatile int abort_sh;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = r.N;
+  const uint32_t a_bytes = kTileBytes, b_bytes = (uint32_t)N * BK * 2;
+  const uint32_t stage_bytes = (a_bytes + b_bytes + 1023) & ~1023u;
+  const int S = min(kMaxStages, (int)(kSmemBudget / stage_bytes));
+  uint32_t ncols = 32;
+  while (ncols < (uint32_t)N) ncols <<= 1;
+  const int mt = blockIdx.x / r.nsp, sp = blockIdx.x - mt * r.nsp;
+  const int kb0 = sp * r.kb_h / r.nsp, kb1 = (sp + 1) * r.kb_h / r.nsp;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(&tfull_bar, 1);
+    mbar_init(&drain_bar, 1);
+    abort_sh = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(&tmem_base_sh, ncols);
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int kb = kb0; kb < kb1; ++kb, ++it) {
+        const int s = it % S;
+        if (it >= (uint32_t)S && !mbar_wait(&empty_bar[s], ((it / S) - 1) & 1)) { ok = false; break; }
+        uint8_t* st = smem + (size_t)s * stage_bytes;
+        mbar_expect_tx(&full_bar[s], a_bytes + b_bytes);
+        tma_load_3d(st, &map_x, &full_bar[s], kb * BK, mt * BM, 0);
+        tma_load_3d(st + a_bytes, &map_w, &full_bar[s], kb * BK, 0, 0);
+      }
+      if (!ok) {
+        set_status(r.status, MOE_ERR_TIMEOUT);
+        abort_sh = 1;
+      }
+      const uint32_t issued = it;
+      for (int s = 0; s < S; ++s) {
+        if ((uint32_t)s < issued) {
+          const uint32_t last = issued - 1 - ((issued - 1 - s) % S);
+          mbar_wait(&full_bar[s], (last / S) & 1);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(N);
+      uint32_t it = 0, acc = 0;
+      bool ok = true;
+      for (int kb = kb0; kb < kb1; ++kb, ++it) {
+        const int s = it % S;
+        if (!mbar_wait(&full_bar[s], (it / S) & 1) || abort_sh) { ok = false; break; }
+        fence_after();
+        const uint32_t base = smem_u32(smem + (size_t)s * stage_bytes);
+        const uint64_t da = desc_sw128(base), db = desc_sw128(base + a_bytes);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          mma_bf16(tmem, da + 2 * kk, db + 2 * kk, idesc, acc);
+          acc = 1;
+        }
+        mma_commit(&empty_bar[s]);
+      }
+      if (!ok) {
+        set_status(r.status, MOE_ERR_TIMEOUT);
+        abort_sh = 1;
+      }
+      mma_commit(&tfull_bar);
+      mbar_wait(&tfull_bar, 0);
+    }
+  } else {
+    // epilogue: TMEM lane = token row of the tile
+    const int q = warp & 3, row = q * 32 + lane;
+    const int t = mt * BM + row;
+    if (mbar_wait(&tfull_bar, 0) && !abort_sh) {
+      fence_after();
+      for (int c0 = 0; c0 < N; c0 += 16) {
+        float d[16];
+        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c0, d);
+        if (t < r.T) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (c0 + j < r.E) r.part[((size_t)sp * r.T + t) * r.E + c0 + j] = d[j];
+        }
+      }
+    } else {
+      set_status(r.status, MOE_ERR_TIMEOUT);
+    }
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  if (warp == 1) tmem_dealloc(tmem, ncols);
 }
 
 // ----------------------------------------------------------------- gather / combine (T > 256)
@@ -1791,6 +1911,46 @@ int launch_tc_decode_layer(const PoolDev& p, const Scratch& sc, const TcMaps* m,
                            const void* router_w, const float* router_b, void* out, cudaStream_t s) {
   return m->fp8 ? launch_decode_layer_wf<tc::kWfFp8>(p, sc, m, layer, T, x, router_w, router_b, out, s)
                 : launch_decode_layer_wf<tc::kWfBf16>(p, sc, m, layer, T, x, router_w, router_b, out, s);
+}
+
+
+// Router on the tensor cores for T > 32 tokens: partial logits per K split.
+bool tc_router_ok(const PoolDev& p, const Scratch& sc, int T) {
+  return sc.rpart != nullptr && p.adt == MOE_BF16 && T > 32 && T <= sc.tmax && p.E <= 256 && p.H % 64 == 0;
+}
+
+int launch_tc_router(const PoolDev& p, const Scratch& sc, int layer, const void* x, int T, const void* router_w,
+                     int* nsp_out, cudaStream_t s) {
+  const int mtiles = (T + tc::BM - 1) / tc::BM;
+  const int kb_h = p.H / tc::BK;
+  const int G = sm_count();
+  int nsp = std::max(1, std::min(std::min(kb_h, tc::kRouterMaxSplits), G / mtiles));
+  tc::RouterArgs r;
+  r.T = T;
+  r.E = p.E;
+  r.N = (p.E + 15) / 16 * 16;
+  r.kb_h = kb_h;
+  r.nsp = nsp;
+  r.part = sc.rpart;
+  r.status = p.status;
+  CUtensorMap xm, wm;
+  if (!tc::make_map_3d(&xm, x, (uint64_t)p.H, (uint64_t)T, 1, (uint64_t)p.H * 2, (uint64_t)p.H * 2 * T, tc::BM))
+    return -1;
+  const uint16_t* wr = static_cast<const uint16_t*>(router_w) + (size_t)layer * p.E * p.H;
+  if (!tc::make_map_3d(&wm, wr, (uint64_t)p.H, (uint64_t)p.E, 1, (uint64_t)p.H * 2, (uint64_t)p.H * 2 * p.E, r.N))
+    return -1;
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!configured[dev & 63]) {
+    cudaFuncSetAttribute(tc::tc_router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemBudget + 1024);
+    configured[dev & 63] = true;
+  }
+  const uint32_t stage = (tc::kTileBytes + (uint32_t)r.N * tc::BK * 2 + 1023) & ~1023u;
+  const int S = std::min(tc::kMaxStages, (int)(tc::kSmemBudget / stage));
+  tc::tc_router_kernel<<<mtiles * nsp, tc::kThreads, (size_t)S * stage + 1024, s>>>(xm, wm, r);
+  *nsp_out = nsp;
+  return 1;
 }
 
 }  // namespace moeslot

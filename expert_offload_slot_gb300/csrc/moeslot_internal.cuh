@@ -100,6 +100,7 @@ struct Scratch {
   int32_t* ffn_sync;  // arrival counters and readiness flags of the fused decode kernel,
   int32_t n_ffn_sync; // zeroed by the plan kernel before every expert launch
   uint32_t* dsync;    // [3 + 32] counters of the decode layer kernel (reset by its last CTA)
+  float* rpart;       // [32][Tmax][E] K-split partial logits of the tensor-core router (Tmax > 32)
   int32_t* elist;     // [2][E+1]: work entries already resident / copied this step
   int32_t* ecount;    // [2]
   // tensor-core gather path (T > npad_max)
@@ -142,8 +143,9 @@ __device__ __forceinline__ float warp_max(float v) {
 // launch itself surface through cudaGetLastError in the caller.
 int launch_route_logits(const PoolDev& p, int layer, const void* x, int T, const void* router_w,
                         const float* router_b, float* logits, cudaStream_t s);
-int launch_gate_topk(const PoolDev& p, const float* logits, int T, int32_t* ids, float* w, float* probs,
-                     float* gap, cudaStream_t s);
+// logits [T][E], or (nsp > 0) nsp partial projections [nsp][T][E] summed in order plus bias
+int launch_gate_topk(const PoolDev& p, const float* logits, int nsp, const float* bias, int T, int32_t* ids,
+                     float* w, float* probs, float* gap, cudaStream_t s);
 // one launch for router + gate when T and H are small enough (decode)
 bool route_fused_ok(const PoolDev& p, int T);
 int launch_route_gate_fused(const PoolDev& p, int layer, const void* x, int T, const void* router_w,
@@ -170,6 +172,10 @@ int launch_tc_fused_decode(const PoolDev& p, const Scratch& sc, const TcMaps* m,
                            cudaStream_t s);
 // router + gate + plan + fused FFN of a decode call in one cooperative launch (bf16, T <= 32)
 bool tc_decode_layer_ok(const PoolDev& p, const Scratch& sc, int T);
+// router projection on the tensor cores (bf16, T > 32): partial logits, *nsp_out splits
+bool tc_router_ok(const PoolDev& p, const Scratch& sc, int T);
+int launch_tc_router(const PoolDev& p, const Scratch& sc, int layer, const void* x, int T, const void* router_w,
+                     int* nsp_out, cudaStream_t s);
 int launch_tc_decode_layer(const PoolDev& p, const Scratch& sc, const TcMaps* m, int layer, int T, const void* x,
                            const void* router_w, const float* router_b, void* out, cudaStream_t s);
 int launch_load_slot(const PoolDev& p, const Scratch& sc, int layer, int expert, int slot, cudaStream_t s);
