@@ -665,7 +665,24 @@ template <int WF> struct FusedShape {
   static constexpr int threads = (copy_warp0 + kCopyWarps) * 32;
 };
 
+// A step's entry lists derived by every CTA itself from the gated routing and
+// a snapshot of the layer's table row taken before the plan may change it
+// (decode layer kernel): same positions and order as the plan's work list.
+constexpr int kLocalMaxTk = 256;   // routing entries (T * k) the local lists take
+struct LocalPlan {
+  int n, nh, nm, tk, k;
+  int elist[2][kMaxE + 1];         // resident entries, entries copied this step (work positions)
+  int expert[kMaxE + 1];           // expert of each work position (-1: the shared expert)
+  int rid[kMaxE + 1];              // record of each resident entry
+  int32_t ids[kLocalMaxTk];        // the step's routing
+  float w[kLocalMaxTk];
+};
+
 struct FusedArgs {
+  const LocalPlan* lp;          // null: the plan's work lists in global memory
+  int cta0_plans;               // CTA 0 runs the plan and takes no expert units
+  const uint32_t* jobs_ready;   // with lp: the copy jobs are published once this is nonzero
+  const uint32_t* plan_done;    // with lp: the plan's work list (copied entries' records) likewise
   const CopyJob* jobs;
   const int32_t* n_jobs;
   uint32_t tile16;              // bytes of a record the miss copy moves, in 16 B units
@@ -692,9 +709,16 @@ struct FSched {
 
 __device__ __forceinline__ FSched fused_sched(const Args& a, const FusedArgs& f, int G) {
   FSched s;
-  s.n = *a.n_work;
-  s.nh = f.ecount[0];
-  s.nm = f.ecount[1];
+  if (f.lp) {
+    s.n = f.lp->n;
+    s.nh = f.lp->nh;
+    s.nm = f.lp->nm;
+  } else {
+    s.n = *a.n_work;
+    s.nh = f.ecount[0];
+    s.nm = f.ecount[1];
+  }
+  G -= f.cta0_plans;
   s.mt_i = (a.I + BM - 1) / BM;
   s.kb_h = (a.H + BK - 1) / BK;
   s.mt_h = (a.H + BM - 1) / BM;
@@ -745,7 +769,7 @@ __device__ __forceinline__ FUnit fused_unit(const FSched& s, const FusedArgs& f,
   r.sp = rem - r.mt * spn;
   r.kb0 = r.sp * kbn / spn;
   r.kb1 = (r.sp + 1) * kbn / spn;
-  r.u = f.elist[r.miss * f.E1 + r.li];
+  r.u = f.lp ? f.lp->elist[r.miss][r.li] : f.elist[r.miss * f.E1 + r.li];
   return r;
 }
 
@@ -802,6 +826,7 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_sh, last_sh;
   __shared__ FSched sched_sh;
+  __shared__ float wloc_sh[32];                                              // routing weights of one entry (local lists)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -838,6 +863,8 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
   __syncthreads();
   fence_after();
   const bool go = pre();
+  const int Gc = G - f.cta0_plans;                          // CTAs that take expert units
+  const int cta = (int)blockIdx.x - f.cta0_plans;           // this CTA's index among them (-1: none)
   if (threadIdx.x == 0) {
     if (go) {
       sched_sh = fused_sched(a, f, G);   // the unit decomposition, identical in every role and CTA
@@ -857,13 +884,17 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
       uint32_t it = 0;
       bool ok = true;
       int pend_s[kMaxStages], pend_kb[kMaxStages], pend_nk[kMaxStages];
-      for (int g = blockIdx.x; g < sc.total && ok; g += G) {
+      for (int g = cta; cta >= 0 && g < sc.total && ok; g += Gc) {
         const FUnit r = fused_unit(sc, f, g);
+        int rid = 0;
+        if (!r.miss) rid = f.lp ? f.lp->rid[r.u] : a.work[r.u].rid;
         if (r.miss) {
           // a copied record: every CTA's slice of its job must have landed (down units
           // too: their weight tiles go out before h is complete)
           if (!wait_count(&f.jdone[r.li], (uint32_t)G, a.status)) { ok = false; break; }
+          if (f.plan_done && !wait_count(f.plan_done, 1u, a.status)) { ok = false; break; }
           asm volatile("fence.proxy.async.global;" ::: "memory");   // generic writes -> bulk-copy reads
+          rid = __ldcg(&a.work[r.u].rid);                            // the plan's choice (slot or one-step record)
         }
         // down: h of this entry complete?  If not yet, weight tiles are issued
         // ahead and their h tiles once it is (at the latest when the ring is full)
@@ -881,8 +912,7 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
           h_ok = true;
           return true;
         };
-        const WorkEntry we = a.work[r.u];
-        const uint8_t* wbase = a.records + (size_t)we.rid * a.rec + (r.gu ? a.off13 : a.off2) +
+        const uint8_t* wbase = a.records + (size_t)rid * a.rec + (r.gu ? a.off13 : a.off2) +
                                (size_t)r.mt * (r.gu ? sc.kb_h * 2 * kTileBytes : sc.kb_i * kTileBytes);
         const int kstep = r.gu ? 1 : 2;
         for (int kb = r.kb0; kb < r.kb1; kb += kstep, ++it) {
@@ -897,11 +927,11 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
             const uint32_t raw = kTileBytes / 2;
             mbar_expect_tx(&full_bar[s], (r.gu ? 2u : (uint32_t)nk) * raw + (uint32_t)nk * b_bytes);
             if (r.gu) {
-              tma_load_3d(st + raw, &map_w13_p[0], &full_bar[s], kb * BK, r.mt * BM, we.rid);
-              tma_load_3d(st + kTileBytes + raw, &map_w13_p[0], &full_bar[s], kb * BK, a.I + r.mt * BM, we.rid);
+              tma_load_3d(st + raw, &map_w13_p[0], &full_bar[s], kb * BK, r.mt * BM, rid);
+              tma_load_3d(st + kTileBytes + raw, &map_w13_p[0], &full_bar[s], kb * BK, a.I + r.mt * BM, rid);
             } else {
               for (int j = 0; j < nk; ++j)
-                tma_load_3d(st + j * kTileBytes + raw, &map_w2_p[0], &full_bar[s], (kb + j) * BK, r.mt * BM, we.rid);
+                tma_load_3d(st + j * kTileBytes + raw, &map_w2_p[0], &full_bar[s], (kb + j) * BK, r.mt * BM, rid);
             }
           } else {
             const uint32_t wb = r.gu ? 2 * kTileBytes : (uint32_t)nk * kTileBytes;
@@ -942,7 +972,7 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
       uint32_t it = 0;
       int local = 0;
       bool ok = true;
-      for (int g = blockIdx.x; g < sc.total && ok; g += G, ++local) {
+      for (int g = cta; cta >= 0 && g < sc.total && ok; g += Gc, ++local) {
         const FUnit r = fused_unit(sc, f, g);
         const int buf = local % nbuf, use = local / nbuf;
         if (use > 0 && !mbar_wait(&tempty_bar[buf], (use - 1) & 1)) { ok = false; break; }
@@ -998,7 +1028,7 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
     const uint32_t trow0 = tmem + ((uint32_t)(q * 32) << 16);
     const int cols = sc.cols;
     int local = 0;
-    for (int g = blockIdx.x; g < sc.total; g += G, ++local) {
+    for (int g = cta; cta >= 0 && g < sc.total; g += Gc, ++local) {
       const FUnit r = fused_unit(sc, f, g);
       const int buf = local % nbuf;
       const uint32_t trow = trow0 + (uint32_t)buf * acc_cols;
@@ -1013,6 +1043,25 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
         // ------------------------------ gate/up: h[u][t][m] = w(u,t) SiLU(g) u
         const int m = r.mt * BM + row;
         const float* wrow = a.wmat + (size_t)r.u * N;
+        if (f.lp) {
+          // routing weight of each token for this entry, from the step's routing (N <= 32 here)
+          const int et = threadIdx.x - 64;
+          if (et < N) {
+            const int e = f.lp->expert[r.u];
+            float wv = 0.f;
+            if (et < a.T) {
+              if (e < 0) {
+                wv = 1.f;
+              } else {
+                for (int j = 0; j < f.lp->k; ++j)
+                  if (f.lp->ids[et * f.lp->k + j] == e) wv += f.lp->w[et * f.lp->k + j];
+              }
+            }
+            wloc_sh[et] = wv;
+          }
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+          wrow = wloc_sh;
+        }
         uint16_t* hrow = a.hbuf + (size_t)r.u * N * a.I + m;
         auto store_h = [&](int c0, const float* g16, const float* u16) {
           if (m >= a.I) return;
@@ -1145,15 +1194,17 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
     uint32_t it = 0;
     int local = 0;
     bool stop = false;
-    for (int g = blockIdx.x; g < sc.total; g += G, ++local) {
+    for (int g = cta; cta >= 0 && g < sc.total; g += Gc, ++local) {
       const FUnit r = fused_unit(sc, f, g);
-      const int rid = a.work[r.u].rid;
-      const float* scl = reinterpret_cast<const float*>(a.records + (size_t)rid * a.rec + (r.gu ? f.os13 : f.os2));
+      const float* scl = nullptr;
       const int b0 = r.kb0 / 2, nblk = (r.kb1 - 1) / 2 - b0 + 1;   // 128-wide scale blocks the unit spans (<= 64)
       const int sbuf = local & 1;
       // gate (or down) scales at [0, 64), up scales at [64, 128)
       auto stage_scales = [&]() {
         if (stop) return;
+        // a copied entry's record (the plan's choice) is read once its first stage has landed
+        const int rid = r.miss ? __ldcg(&a.work[r.u].rid) : (f.lp ? f.lp->rid[r.u] : a.work[r.u].rid);
+        scl = reinterpret_cast<const float*>(a.records + (size_t)rid * a.rec + (r.gu ? f.os13 : f.os2));
         if (ct < nblk) {
           scale_sh[sbuf][ct] = scl[(size_t)(r.gu ? r.mt * f.sc_h : r.mt * f.sc_i) + b0 + ct];
         } else if (r.gu && ct >= 64 && ct - 64 < nblk) {
@@ -1186,12 +1237,21 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
   } else {
     // ------------------------------------------------------------- copy warps
     // Job by job: this CTA's slice of each record's tile data, then one release per job.
-    const uint32_t n = go ? (uint32_t)*f.n_jobs : 0u;
+    bool jobs_ok = go;
+    if (go && f.jobs_ready) {
+      // local lists: the copy jobs come from the plan, published with jobs_ready
+      if (lane == 0) jobs_ok = wait_count(f.jobs_ready, 1u, a.status);
+      jobs_ok = __shfl_sync(0xffffffffu, jobs_ok, 0);
+    }
+    const uint32_t n = jobs_ok ? (uint32_t)__ldcg(f.n_jobs) : 0u;
     const uint32_t stride = (uint32_t)G * (32u * kCopyWarps);
     const uint32_t ctid = (uint32_t)(warp - Shape::copy_warp0) * 32u + lane;
     for (uint32_t j = 0; j < n; ++j) {
-      const uint4* src = reinterpret_cast<const uint4*>(f.jobs[j].src);
-      uint4* dst = reinterpret_cast<uint4*>(f.jobs[j].dst);
+      const CopyJob job = f.lp ? CopyJob{reinterpret_cast<const uint8_t*>(__ldcg(reinterpret_cast<const unsigned long long*>(&f.jobs[j].src))),
+                                         reinterpret_cast<uint8_t*>(__ldcg(reinterpret_cast<const unsigned long long*>(&f.jobs[j].dst)))}
+                               : f.jobs[j];
+      const uint4* src = reinterpret_cast<const uint4*>(job.src);
+      uint4* dst = reinterpret_cast<uint4*>(job.dst);
       for (uint32_t base = blockIdx.x * (32u * kCopyWarps) + ctid; base < f.tile16; base += stride * kCopyUnroll) {
         uint4 v[kCopyUnroll];
 #pragma unroll
@@ -1289,13 +1349,15 @@ tc_fused_decode_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
 // counter and, after a timeout, the others) by the last CTA to leave, so each
 // launch starts from zero.
 struct DecodeArgs {
+  int local;                // every CTA derives the step's entry lists itself (T * k <= kLocalMaxTk)
   const uint16_t* x;        // [T][H] bf16
   const uint16_t* wr;       // this layer's router [E][H] bf16
   const float* rb;          // [E]
   float* z;                 // [T][E] logits scratch
   int eb, nblk;             // experts per routing CTA, routing CTAs per token
   PlanArgs plan;
-  uint32_t* dsync;          // [0] route_done, [1] plan_done, [2] exit count, [3 + t] ticket of token t
+  uint32_t* dsync;          // [0] route_done, [1] plan_done, [2] exit count, [3 + t] ticket of token t,
+                            // [35] CTAs holding their copy of the layer's table row, [36] copy jobs ready
 };
 
 constexpr int kDecodeMaxT = 32;
@@ -1311,6 +1373,9 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
   extern __shared__ uint8_t smem_raw[];
   __shared__ float zsel[NT / 32][32];
   __shared__ volatile int flag_sh;
+  __shared__ LocalPlan lp_sh;
+  __shared__ int lut_snap[kMaxE];
+  __shared__ int cnt_sh[kMaxE];
   uint8_t* dsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = a.T, H = a.H, E = d.plan.p.E;
@@ -1319,8 +1384,26 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
   uint32_t* plan_done = d.dsync + 1;
   uint32_t* exit_cnt = d.dsync + 2;
   uint32_t* ticket = d.dsync + 3;
+  uint32_t* snap_done = d.dsync + 35;
+  uint32_t* jobs_ready = d.dsync + 36;
+  const PoolDev& p = d.plan.p;
+  const int l = d.plan.layer;
 
-  if (blockIdx.x == 0) plan_prestage<NT>(d.plan, dsm);
+  if (d.local) {
+    // this CTA's copy of the layer's table row, taken before the plan may change it
+    for (int e = threadIdx.x; e < E; e += NT) lut_snap[e] = p.lut[(size_t)l * E + e];
+    __syncthreads();
+    if (threadIdx.x == 0) release_add(snap_done);
+  }
+  if (blockIdx.x == 0) {
+    plan_prestage<NT>(d.plan, dsm);
+    // the expert kernel's counters start from zero: one more arrival on route_done
+    // (which every CTA waits for) publishes that
+    for (int i = threadIdx.x; i < d.plan.sc.n_ffn_sync; i += NT) d.plan.sc.ffn_sync[i] = 0;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) release_add(route_done);
+  }
   // ---- route: logits of token t for one block of experts, then (last CTA) its gate
   if (blockIdx.x >= 1 && (int)blockIdx.x <= T * d.nblk) {
     const int rb = blockIdx.x - 1;
@@ -1381,33 +1464,106 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
 
   // ---- plan (CTA 0, once every token is gated) while the other CTAs set up;
   // then every CTA runs the FFN once the plan is published
-  fused_ffn<WF>(&map_x, &map_h, &map_w13, &map_w2, a, f, smem_raw, [&]() -> bool {
-    if (blockIdx.x == 0) {
-      if (threadIdx.x == 0) {
-        flag_sh = wait_count(route_done, (uint32_t)T, a.status) ? 1 : 0;
-        if (flag_sh) *route_done = 0u;
-        else set_status(a.status, MOE_ERR_TIMEOUT);
-      }
-      __syncthreads();
-      if (flag_sh) {
-        __threadfence();
-        plan_body<NT>(d.plan, dsm, true);
-      } else {
-        cp_async_wait_all();   // the prestaged copies land before this CTA moves on
-      }
-      __threadfence();
-      __syncthreads();
-      if (threadIdx.x == 0) release_add(plan_done);
-    }
+  FusedArgs fl = f;
+  if (d.local) {
+    fl.lp = &lp_sh;
+    fl.cta0_plans = 1;
+    fl.jobs_ready = jobs_ready;
+    fl.plan_done = plan_done;
+  }
+  fused_ffn<WF>(&map_x, &map_h, &map_w13, &map_w2, a, fl, smem_raw, [&]() -> bool {
+    // every token gated (and the counters zeroed)
     if (threadIdx.x == 0) {
-      flag_sh = wait_count(plan_done, 1u, a.status) ? 1 : 0;
+      flag_sh = wait_count(route_done, (uint32_t)T + 1u, a.status) ? 1 : 0;
       if (!flag_sh) set_status(a.status, MOE_ERR_TIMEOUT);
     }
     __syncthreads();
-    const bool ok = flag_sh != 0;
-    if (ok) __threadfence();
+    if (!flag_sh) {
+      if (blockIdx.x == 0) cp_async_wait_all();   // the prestaged copies land before this CTA moves on
+      return false;
+    }
+    __threadfence();
+    if (d.local) {
+      // the step's entry lists, as the plan orders them: experts with tokens ascending,
+      // then the shared expert; resident / copied by the table row at the step's start
+      const int tk = T * p.k;
+      for (int e = threadIdx.x; e < E; e += NT) cnt_sh[e] = 0;
+      for (int i = threadIdx.x; i < tk; i += NT) {
+        lp_sh.ids[i] = __ldcg(d.plan.sc.ids + i);
+        lp_sh.w[i] = __ldcg(d.plan.sc.w + i);
+      }
+      __syncthreads();
+      for (int i = threadIdx.x; i < tk; i += NT) {
+        const int e = lp_sh.ids[i];
+        if ((unsigned)e < (unsigned)E) atomicAdd(&cnt_sh[e], 1);
+      }
+      __syncthreads();
+      if (warp == 0) {
+        int pos_run = 0, nh_run = 0, nm_run = 0;
+        const unsigned lower = (1u << lane) - 1u;
+        for (int e0 = 0; e0 < E; e0 += 32) {
+          const int e = e0 + lane;
+          const bool has = e < E && cnt_sh[e] > 0;
+          const int sl = has ? lut_snap[e] : -1;
+          const bool hit = has && sl >= 0 && sl < p.S;
+          const unsigned mhas = __ballot_sync(0xffffffffu, has), mhit = __ballot_sync(0xffffffffu, hit),
+                         mmis = __ballot_sync(0xffffffffu, has && !hit);
+          if (has) {
+            const int pos = pos_run + __popc(mhas & lower);
+            lp_sh.expert[pos] = e;
+            lp_sh.rid[pos] = hit ? sl : -1;
+            if (hit) lp_sh.elist[0][nh_run + __popc(mhit & lower)] = pos;
+            else lp_sh.elist[1][nm_run + __popc(mmis & lower)] = pos;
+          }
+          pos_run += __popc(mhas);
+          nh_run += __popc(mhit);
+          nm_run += __popc(mmis);
+        }
+        if (lane == 0) {
+          if (p.shared) {
+            lp_sh.expert[pos_run] = -1;
+            lp_sh.rid[pos_run] = p.rid_shared0 + l;
+            lp_sh.elist[0][nh_run++] = pos_run;
+            ++pos_run;
+          }
+          lp_sh.n = pos_run;
+          lp_sh.nh = nh_run;
+          lp_sh.nm = nm_run;
+          lp_sh.tk = tk;
+          lp_sh.k = p.k;
+        }
+      }
+      __syncthreads();
+    }
+    if (blockIdx.x == 0) {
+      // the plan: history, victims, table, copy jobs, permutation (for the routing dump)
+      plan_body<NT>(d.plan, dsm, true);
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0) release_add(plan_done);
+    } else if (d.local && lp_sh.nm > 0) {
+      // misses: the copies over the host link are this step's critical path, so the
+      // resident work waits until the plan has published them (the plan then runs
+      // with HBM quiet instead of behind the weight stream)
+      if (threadIdx.x == 0) {
+        flag_sh = wait_count(jobs_ready, 1u, a.status) ? 1 : 0;
+        if (!flag_sh) set_status(a.status, MOE_ERR_TIMEOUT);
+      }
+      __syncthreads();
+      if (!flag_sh) return false;
+    }
+    if (!d.local) {
+      // the plan's work lists
+      if (threadIdx.x == 0) {
+        flag_sh = wait_count(plan_done, 1u, a.status) ? 1 : 0;
+        if (!flag_sh) set_status(a.status, MOE_ERR_TIMEOUT);
+      }
+      __syncthreads();
+      if (!flag_sh) return false;
+      __threadfence();
+    }
     __syncthreads();
-    return ok;
+    return true;
   });
   // ---- leave: the last CTA resets the counters for the next launch
   __syncthreads();
@@ -1416,6 +1572,8 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
     if (old == (uint32_t)G - 1) {
       *route_done = 0u;
       *plan_done = 0u;
+      *snap_done = 0u;
+      *jobs_ready = 0u;
       for (int t = 0; t < kDecodeMaxT; ++t) ticket[t] = 0u;
       *exit_cnt = 0u;
     }
@@ -1777,6 +1935,10 @@ static bool fused_setup(const PoolDev& p, const Scratch& sc, int T, const void* 
   const uint64_t I = p.I;
   if (!tc::make_map_3d(hm, sc.hbuf, I, (uint64_t)N, (uint64_t)p.E + 1, I * 2, (uint64_t)N * I * 2, N)) return false;
   tc::FusedArgs f;
+  f.lp = nullptr;
+  f.cta0_plans = 0;
+  f.jobs_ready = nullptr;
+  f.plan_done = nullptr;
   f.jobs = sc.copies;
   f.n_jobs = sc.n_copy;
   // a bf16 record's tile data; an fp8 record whole (codes, then its scale tables)
@@ -1896,6 +2058,11 @@ static int launch_decode_layer_wf(const PoolDev& p, const Scratch& sc, const TcM
   pa.ids = sc.ids;
   pa.w = sc.w;
   pa.probs = sc.probs;
+  d.local = T * p.k <= tc::kLocalMaxTk && p.E <= kMaxE ? 1 : 0;
+  pa.zero_sync = false;                      // CTA 0 zeroes the counters at kernel start
+  pa.snap_wait = d.local ? sc.dsync + 35 : nullptr;
+  pa.jobs_flag = d.local ? sc.dsync + 36 : nullptr;
+  pa.snap_target = (uint32_t)G;
   const size_t psm = decode_plan_smem<NT>(p, T, &pa.owner_cap, &pa.tok_rows);
   if (psm == 0) return -1;
   d.dsync = sc.dsync;

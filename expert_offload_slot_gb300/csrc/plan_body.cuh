@@ -21,6 +21,10 @@ struct PlanArgs {
   const float* probs;
   int owner_cap;        // slots staged in shared memory (S, or 0 for the global-memory path)
   int tok_rows;         // rows of the token staging area
+  bool zero_sync = true;                 // zero the expert kernel's counters (false: the caller does)
+  const uint32_t* snap_wait = nullptr;   // if set: before writing the table, wait for *snap_wait >= snap_target
+  uint32_t snap_target = 0;              // (other CTAs' reads of this layer's table row)
+  uint32_t* jobs_flag = nullptr;         // if set: released once the copy jobs are written
 };
 
 // Orderable key: (score ascending, slot ascending).  -0 is folded into +0.
@@ -185,7 +189,8 @@ __device__ void plan_body(const PlanArgs& a, uint8_t* dsm, bool prestaged = fals
   }
   if (tid < 12) sh_misc[tid] = 0;
   // arrival counters and readiness flags of the expert kernel that follows
-  for (int i = tid; i < a.sc.n_ffn_sync; i += kPlanThreads) a.sc.ffn_sync[i] = 0;
+  if (a.zero_sync)
+    for (int i = tid; i < a.sc.n_ffn_sync; i += kPlanThreads) a.sc.ffn_sync[i] = 0;
   const bool hist = (a.flags & PLAN_HISTORY) != 0;
   const bool cache = (a.flags & PLAN_CACHE) != 0;
   int t_step = 0;
@@ -421,6 +426,18 @@ __device__ void plan_body(const PlanArgs& a, uint8_t* dsm, bool prestaged = fals
       }
       __syncthreads();
     }
+    if (a.snap_wait) {
+      // the table row may change only once every reader has its copy (bounded wait, ~1 s)
+      if (tid == 0) {
+        const uint64_t t0 = clock64();
+        uint32_t v = 0;
+        do {
+          asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a.snap_wait) : "memory");
+        } while (v < a.snap_target && clock64() - t0 < 4000000000ull);
+        if (v < a.snap_target) set_status(p.status, MOE_ERR_TIMEOUT);
+      }
+      __syncthreads();
+    }
     // apply the decisions in parallel: table, owners, tags, copy list (one copy per miss)
     if (tid < n_miss) {
       const int e = miss_list[tid], v = victim_s[tid], old = old_s[tid];
@@ -447,8 +464,17 @@ __device__ void plan_body(const PlanArgs& a, uint8_t* dsm, bool prestaged = fals
       atomicAdd(&p.stats[ST_BYTES], (unsigned long long)n_miss * rec);   // slot fills + one-step records
     }
     __syncthreads();
+    if (a.jobs_flag) {
+      // the copy jobs are complete: copies may start while the plan goes on
+      __threadfence();
+      __syncthreads();
+      if (tid == 0)
+        asm volatile("fence.acq_rel.gpu;\n red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.jobs_flag) : "memory");
+    }
   } else if (tid == 0) {
     *a.sc.n_copy = 0;
+    if (a.jobs_flag)
+      asm volatile("fence.acq_rel.gpu;\n red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.jobs_flag) : "memory");
   }
 
   // ------------------------------------------------------ a7 permutation
