@@ -62,6 +62,7 @@ _sig = {
     "moe_clear_status": (_i32, [_vp]),
     "moe_get_routing": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _P(_i32)]),
     "moe_get_state": (_i32, [_vp, _vp, _vp, _vp, _vp]),
+    "moe_read_slot": (_i32, [_vp, _i32, _vp, _sz]),
     "moe_get_stats": (_i32, [_vp, _P(moe_stats)]),
     "moe_launch_count": (ctypes.c_uint64, [_vp]),
     "moe_profile_enable": (_i32, [_vp, _i32]),
@@ -243,6 +244,13 @@ class Pool:
                "moe_get_state")
         return {"lut": lut.reshape(c.num_layers, c.num_experts), "owner": owner, "tag": tag,
                 "score": score.reshape(c.num_layers, c.num_experts)}
+
+    def read_slot(self, slot):
+        """The record bytes slot `slot` holds (host copy, blocking)."""
+        rec = moe_expert_layout(self.cfg)[4]
+        buf = np.zeros(rec, np.uint8)
+        _check(_lib.moe_read_slot(self.h, int(slot), buf.ctypes.data, rec), "moe_read_slot")
+        return buf
 
     def stats(self):
         s = moe_stats()

@@ -288,10 +288,13 @@ MOE_API moe_status moe_pool_create(const moe_config* cfg, const void* host_pool,
     if (st != MOE_OK) goto fail_out;             \
   } while (0)
   {
-    // one record array: [S slots | one-step records for misses that get no slot | 2E staging | L shared]
+    // one record array: [S slots | one-step records for misses that get no slot |
+    // landing records of the decode layer kernel | 2E staging | L shared]
     const long long need = std::min<long long>((long long)E, (long long)Tm * (long long)k) - (long long)S;
     d.n_bypass = need > 0 ? (int)need : 0;
-    d.rid_staging0 = (int)S + d.n_bypass;
+    d.rid_land0 = (int)S + d.n_bypass;
+    d.n_land = decode_landing_records(d, cfg->max_tokens);
+    d.rid_staging0 = d.rid_land0 + d.n_land;
     const int n_stage = cfg->staging_regions == 2 ? 2 * (int)E : 0;
     d.rid_shared0 = d.rid_staging0 + n_stage;
     d.n_records = d.rid_shared0 + (cfg->has_shared_expert ? (int)L : 0);
@@ -676,6 +679,17 @@ MOE_API moe_status moe_get_state(moe_pool* P, int32_t* lut, int32_t* owner, uint
   if (owner) CUDA_TRY(cudaMemcpy(owner, P->d.owner, sizeof(int32_t) * S, cudaMemcpyDeviceToHost));
   if (tag) CUDA_TRY(cudaMemcpy(tag, P->d.tag, sizeof(uint32_t) * S, cudaMemcpyDeviceToHost));
   if (score) CUDA_TRY(cudaMemcpy(score, P->d.score, sizeof(float) * LE, cudaMemcpyDeviceToHost));
+  return MOE_OK;
+}
+
+MOE_API moe_status moe_read_slot(moe_pool* P, int32_t slot, void* out, size_t out_bytes) {
+  if (!P || !out) return fail(MOE_ERR_INVALID, "NULL argument");
+  if (slot < 0 || slot >= P->d.S) return fail(MOE_ERR_INVALID, "moe_read_slot: slot %d out of [0, %d)", slot, P->d.S);
+  if (out_bytes < P->d.lay.rec) return fail(MOE_ERR_INVALID, "moe_read_slot: buffer of %zu bytes < record %zu", out_bytes,
+                                            P->d.lay.rec);
+  CUDA_TRY(cudaSetDevice(P->device));
+  CUDA_TRY(cudaDeviceSynchronize());
+  CUDA_TRY(cudaMemcpy(out, P->d.records + (size_t)slot * P->d.lay.rec, P->d.lay.rec, cudaMemcpyDeviceToHost));
   return MOE_OK;
 }
 

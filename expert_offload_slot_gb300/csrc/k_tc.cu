@@ -681,8 +681,13 @@ struct LocalPlan {
 struct FusedArgs {
   const LocalPlan* lp;          // null: the plan's work lists in global memory
   int cta0_plans;               // CTA 0 runs the plan and takes no expert units
-  const uint32_t* jobs_ready;   // with lp: the copy jobs are published once this is nonzero
-  const uint32_t* plan_done;    // with lp: the plan's work list (copied entries' records) likewise
+  // with lp: a miss j (j-th copied entry) is copied from the host pool into landing
+  // record rid_land0 + j at once, read from there, and written to its slot once the
+  // plan (plan_done) has chosen it
+  const uint32_t* plan_done;
+  const uint8_t* host_layer;    // host pool records of this layer (device view)
+  const int32_t* lut_row;       // this layer's table row
+  int rid_land0, S;
   const CopyJob* jobs;
   const int32_t* n_jobs;
   uint32_t tile16;              // bytes of a record the miss copy moves, in 16 B units
@@ -889,12 +894,12 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
         int rid = 0;
         if (!r.miss) rid = f.lp ? f.lp->rid[r.u] : a.work[r.u].rid;
         if (r.miss) {
-          // a copied record: every CTA's slice of its job must have landed (down units
-          // too: their weight tiles go out before h is complete)
-          if (!wait_count(&f.jdone[r.li], (uint32_t)G, a.status)) { ok = false; break; }
-          if (f.plan_done && !wait_count(f.plan_done, 1u, a.status)) { ok = false; break; }
+          // a copied record: every copying CTA's slice of its job must have landed (down
+          // units too: their weight tiles go out before h is complete)
+          if (!wait_count(&f.jdone[r.li], (uint32_t)Gc, a.status)) { ok = false; break; }
           asm volatile("fence.proxy.async.global;" ::: "memory");   // generic writes -> bulk-copy reads
-          rid = __ldcg(&a.work[r.u].rid);                            // the plan's choice (slot or one-step record)
+          // the landing record, or the plan's choice (slot or one-step record)
+          rid = f.lp ? f.rid_land0 + r.li : __ldcg(&a.work[r.u].rid);
         }
         // down: h of this entry complete?  If not yet, weight tiles are issued
         // ahead and their h tiles once it is (at the latest when the ring is full)
@@ -1202,13 +1207,15 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
       // gate (or down) scales at [0, 64), up scales at [64, 128)
       auto stage_scales = [&]() {
         if (stop) return;
-        // a copied entry's record (the plan's choice) is read once its first stage has landed
-        const int rid = r.miss ? __ldcg(&a.work[r.u].rid) : (f.lp ? f.lp->rid[r.u] : a.work[r.u].rid);
+        // a copied entry's record is read once its first stage has landed (L2, not L1:
+        // other CTAs wrote it)
+        const int rid = r.miss ? (f.lp ? f.rid_land0 + r.li : __ldcg(&a.work[r.u].rid))
+                               : (f.lp ? f.lp->rid[r.u] : a.work[r.u].rid);
         scl = reinterpret_cast<const float*>(a.records + (size_t)rid * a.rec + (r.gu ? f.os13 : f.os2));
         if (ct < nblk) {
-          scale_sh[sbuf][ct] = scl[(size_t)(r.gu ? r.mt * f.sc_h : r.mt * f.sc_i) + b0 + ct];
+          scale_sh[sbuf][ct] = __ldcg(scl + (size_t)(r.gu ? r.mt * f.sc_h : r.mt * f.sc_i) + b0 + ct);
         } else if (r.gu && ct >= 64 && ct - 64 < nblk) {
-          scale_sh[sbuf][ct] = scl[(size_t)(a.I / BM + r.mt) * f.sc_h + b0 + (ct - 64)];
+          scale_sh[sbuf][ct] = __ldcg(scl + (size_t)(a.I / BM + r.mt) * f.sc_h + b0 + (ct - 64));
         }
       };
       if (!r.miss) stage_scales();
@@ -1237,37 +1244,102 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
   } else {
     // ------------------------------------------------------------- copy warps
     // Job by job: this CTA's slice of each record's tile data, then one release per job.
-    bool jobs_ok = go;
-    if (go && f.jobs_ready) {
-      // local lists: the copy jobs come from the plan, published with jobs_ready
-      if (lane == 0) jobs_ok = wait_count(f.jobs_ready, 1u, a.status);
-      jobs_ok = __shfl_sync(0xffffffffu, jobs_ok, 0);
-    }
-    const uint32_t n = jobs_ok ? (uint32_t)__ldcg(f.n_jobs) : 0u;
-    const uint32_t stride = (uint32_t)G * (32u * kCopyWarps);
-    const uint32_t ctid = (uint32_t)(warp - Shape::copy_warp0) * 32u + lane;
-    for (uint32_t j = 0; j < n; ++j) {
-      const CopyJob job = f.lp ? CopyJob{reinterpret_cast<const uint8_t*>(__ldcg(reinterpret_cast<const unsigned long long*>(&f.jobs[j].src))),
-                                         reinterpret_cast<uint8_t*>(__ldcg(reinterpret_cast<const unsigned long long*>(&f.jobs[j].dst)))}
-                               : f.jobs[j];
-      const uint4* src = reinterpret_cast<const uint4*>(job.src);
-      uint4* dst = reinterpret_cast<uint4*>(job.dst);
-      for (uint32_t base = blockIdx.x * (32u * kCopyWarps) + ctid; base < f.tile16; base += stride * kCopyUnroll) {
-        uint4 v[kCopyUnroll];
-#pragma unroll
-        for (int u = 0; u < kCopyUnroll; ++u) {
-          const uint32_t idx = base + (uint32_t)u * stride;
-          if (idx < f.tile16) v[u] = __ldcs(src + idx);
+    // A lane's 16-byte chunks are w0 + lane + (i * kCopyUnroll + u) * stride, with
+    // w0 the warp's first chunk; the loops run on w0, so every lane of a warp takes
+    // the same trip count (the warp-wide shuffles below need that).
+    const uint32_t stride = (uint32_t)Gc * (32u * kCopyWarps);
+    const uint32_t w0 = (uint32_t)cta * (32u * kCopyWarps) + (uint32_t)(warp - Shape::copy_warp0) * 32u;
+    // slot record the plan gave expert e (null: none, the miss stays in its landing record)
+    auto slot_record = [&](int e) -> uint4* {
+      int slot = -1;
+      if (lane == 0) slot = __ldcg(f.lut_row + e);
+      slot = __shfl_sync(0xffffffffu, slot, 0);
+      return slot >= 0 && slot < f.S ? reinterpret_cast<uint4*>(const_cast<uint8_t*>(a.records) + (size_t)slot * a.rec)
+                                     : nullptr;
+    };
+    if (go && cta >= 0) {
+      const uint32_t n = f.lp ? (uint32_t)f.lp->nm : (uint32_t)__ldcg(f.n_jobs);
+      // local lists: each miss lands in its landing record at once; from the moment the
+      // plan is seen, its chunks go to the chosen slot as well.  (j_dual, c_dual): the
+      // first job and warp chunk written to both; what came before is copied over later.
+      bool planned = !f.lp;
+      uint32_t j_dual = n, c_dual = 0;
+      for (uint32_t j = 0; j < n; ++j) {
+        const uint4* src;
+        uint4* dst;
+        uint4* dst2 = nullptr;
+        int e = -1;
+        if (f.lp) {
+          e = f.lp->expert[f.lp->elist[1][j]];
+          src = reinterpret_cast<const uint4*>(f.host_layer + (size_t)e * a.rec);
+          dst = reinterpret_cast<uint4*>(const_cast<uint8_t*>(a.records) + (size_t)(f.rid_land0 + (int)j) * a.rec);
+          if (planned) dst2 = slot_record(e);
+        } else {
+          src = reinterpret_cast<const uint4*>(f.jobs[j].src);
+          dst = reinterpret_cast<uint4*>(f.jobs[j].dst);
         }
+        for (uint32_t wb = w0; wb < f.tile16; wb += stride * kCopyUnroll) {
+          if (!planned) {
+            uint32_t pv = 0;
+            if (lane == 0) pv = ld_acquire(f.plan_done);
+            planned = __shfl_sync(0xffffffffu, pv, 0) != 0u;
+            if (planned) {
+              dst2 = slot_record(e);
+              j_dual = j;
+              c_dual = wb;
+            }
+          }
+          const uint32_t base = wb + lane;
+          uint4 v[kCopyUnroll];
 #pragma unroll
-        for (int u = 0; u < kCopyUnroll; ++u) {
-          const uint32_t idx = base + (uint32_t)u * stride;
-          if (idx < f.tile16) __stcs(dst + idx, v[u]);
+          for (int u = 0; u < kCopyUnroll; ++u) {
+            const uint32_t idx = base + (uint32_t)u * stride;
+            if (idx < f.tile16) v[u] = __ldcs(src + idx);
+          }
+#pragma unroll
+          for (int u = 0; u < kCopyUnroll; ++u) {
+            const uint32_t idx = base + (uint32_t)u * stride;
+            if (idx < f.tile16) {
+              __stcs(dst + idx, v[u]);
+              if (dst2) __stcs(dst2 + idx, v[u]);
+            }
+          }
+        }
+        __threadfence();
+        asm volatile("bar.sync 2, %0;" ::"n"(32 * kCopyWarps) : "memory");
+        if (warp == Shape::copy_warp0 && lane == 0) release_add(&f.jdone[j]);
+      }
+      if (f.lp && n > 0) {
+        // the chunks that landed before the plan was seen, into their slots: this
+        // thread re-reads only what it wrote
+        if (!planned) {
+          bool ok = true;
+          if (lane == 0) ok = wait_count(f.plan_done, 1u, a.status);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) set_status(a.status, MOE_ERR_TIMEOUT);
+          planned = ok;
+        }
+        for (uint32_t j = 0; planned && j < n && j <= j_dual; ++j) {
+          uint4* dst = slot_record(f.lp->expert[f.lp->elist[1][j]]);
+          if (!dst) continue;
+          const uint4* src = reinterpret_cast<const uint4*>(a.records + (size_t)(f.rid_land0 + (int)j) * a.rec);
+          const uint32_t wend = j < j_dual ? f.tile16 : min(c_dual, f.tile16);
+          for (uint32_t wb = w0; wb < wend; wb += stride * kCopyUnroll) {
+            const uint32_t base = wb + lane;
+            uint4 v[kCopyUnroll];
+#pragma unroll
+            for (int u = 0; u < kCopyUnroll; ++u) {
+              const uint32_t idx = base + (uint32_t)u * stride;
+              if (idx < f.tile16) v[u] = __ldcs(src + idx);
+            }
+#pragma unroll
+            for (int u = 0; u < kCopyUnroll; ++u) {
+              const uint32_t idx = base + (uint32_t)u * stride;
+              if (idx < f.tile16) __stcs(dst + idx, v[u]);
+            }
+          }
         }
       }
-      __threadfence();
-      asm volatile("bar.sync 2, %0;" ::"n"(32 * kCopyWarps) : "memory");
-      if (warp == Shape::copy_warp0 && lane == 0) release_add(&f.jdone[j]);
     }
   }
   fence_before();
@@ -1332,22 +1404,29 @@ tc_fused_decode_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
 
 
 // ----------------------------------------------------------------- decode layer kernel
-// A decode call with few tokens (T <= 32) and bf16 weights is one cooperative
-// launch: steps a1/a2 (router and gate), a3-a5/a7 (history, table, victims,
-// permutation) and the fused FFN (a6, a8, a9), without the launch gaps and
-// global round trips of three kernels.
+// A decode call with few tokens (T <= 32) and bf16 or fp8 weights is one
+// cooperative launch: steps a1/a2 (router and gate), a3-a5/a7 (history, table,
+// victims, permutation) and the fused FFN (a6, a8, a9), without the launch gaps
+// and global round trips of three kernels.
 //   route: CTA 1 + t * nblk + b, t < T, b < nblk, computes the logits of token
 //          t for experts [b * eb, (b + 1) * eb); the last CTA of token t
 //          (ticket) runs its gate and top-k in one warp;
 //   plan:  CTA 0 starts copying the plan's routing-independent inputs (history
 //          rings, slot owners) into shared memory at once, and once every token
-//          is gated runs the plan with its 256 threads, from shared memory that
-//          the FFN's stage ring reuses later;
-//   FFN:   every CTA, once the plan is published.
-// Counters: route_done (tokens gated) is reset by CTA 0 when it has seen all
-// of them, a token's ticket by its last arrival, and plan_done (with the exit
-// counter and, after a timeout, the others) by the last CTA to leave, so each
-// launch starts from zero.
+//          is gated runs the plan, from shared memory that the FFN's stage ring
+//          reuses later;
+//   FFN:   local lists (T k <= kLocalMaxTk): every CTA snapshots the
+//          layer's table row at kernel start and, once every token is gated,
+//          derives the step's entry lists from the routing and the snapshot.
+//          Resident entries start at once (the plan never evicts an expert the
+//          step uses); each copied entry is pulled from the host pool into a
+//          landing record at once and computed from there, and written to its
+//          slot once the plan has chosen it.  Otherwise every CTA waits for the
+//          plan's work lists.
+// Counters: route_done (tokens gated) counts T gates plus CTA 0's zeroing of
+// the expert counters; tickets reset on their last arrival; plan_done,
+// snap_done (and, after a timeout, the others) are reset by the last CTA to
+// leave, so each launch starts from zero.
 struct DecodeArgs {
   int local;                // every CTA derives the step's entry lists itself (T * k <= kLocalMaxTk)
   const uint16_t* x;        // [T][H] bf16
@@ -1357,7 +1436,7 @@ struct DecodeArgs {
   int eb, nblk;             // experts per routing CTA, routing CTAs per token
   PlanArgs plan;
   uint32_t* dsync;          // [0] route_done, [1] plan_done, [2] exit count, [3 + t] ticket of token t,
-                            // [35] CTAs holding their copy of the layer's table row, [36] copy jobs ready
+                            // [35] CTAs holding their copy of the layer's table row
 };
 
 constexpr int kDecodeMaxT = 32;
@@ -1385,7 +1464,6 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
   uint32_t* exit_cnt = d.dsync + 2;
   uint32_t* ticket = d.dsync + 3;
   uint32_t* snap_done = d.dsync + 35;
-  uint32_t* jobs_ready = d.dsync + 36;
   const PoolDev& p = d.plan.p;
   const int l = d.plan.layer;
 
@@ -1468,8 +1546,11 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
   if (d.local) {
     fl.lp = &lp_sh;
     fl.cta0_plans = 1;
-    fl.jobs_ready = jobs_ready;
     fl.plan_done = plan_done;
+    fl.host_layer = p.host_dev + (size_t)l * E * p.lay.rec;
+    fl.lut_row = p.lut + (size_t)l * E;
+    fl.rid_land0 = p.rid_land0;
+    fl.S = p.S;
   }
   fused_ffn<WF>(&map_x, &map_h, &map_w13, &map_w2, a, fl, smem_raw, [&]() -> bool {
     // every token gated (and the counters zeroed)
@@ -1541,16 +1622,6 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
       __threadfence();
       __syncthreads();
       if (threadIdx.x == 0) release_add(plan_done);
-    } else if (d.local && lp_sh.nm > 0) {
-      // misses: the copies over the host link are this step's critical path, so the
-      // resident work waits until the plan has published them (the plan then runs
-      // with HBM quiet instead of behind the weight stream)
-      if (threadIdx.x == 0) {
-        flag_sh = wait_count(jobs_ready, 1u, a.status) ? 1 : 0;
-        if (!flag_sh) set_status(a.status, MOE_ERR_TIMEOUT);
-      }
-      __syncthreads();
-      if (!flag_sh) return false;
     }
     if (!d.local) {
       // the plan's work lists
@@ -1573,7 +1644,6 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
       *route_done = 0u;
       *plan_done = 0u;
       *snap_done = 0u;
-      *jobs_ready = 0u;
       for (int t = 0; t < kDecodeMaxT; ++t) ticket[t] = 0u;
       *exit_cnt = 0u;
     }
@@ -1833,6 +1903,15 @@ bool tc_fp8_ok(const PoolDev& p) {
          p.lay.rec % 16 == 0;
 }
 
+// Landing records for the copied entries of one decode layer call with local lists:
+// at most min(T k, E) entries, T <= kDecodeMaxT and T k <= kLocalMaxTk.
+int decode_landing_records(const PoolDev& p, int max_tokens) {
+  const bool tc = p.adt == MOE_BF16 && (p.wdt == MOE_BF16 || (p.wdt == MOE_FP8_E4M3_B128 && tc_fp8_ok(p)));
+  if (!tc || p.E > kMaxE || p.k > tc::kLocalMaxTk) return 0;
+  const int t = std::min(std::min(max_tokens, tc::kDecodeMaxT), tc::kLocalMaxTk / p.k);
+  return std::min(p.E, t * p.k);
+}
+
 void tc_maps_destroy(TcMaps* m) { delete m; }
 
 int tc_npad(int T) { return (T + 15) / 16 * 16; }
@@ -1937,8 +2016,11 @@ static bool fused_setup(const PoolDev& p, const Scratch& sc, int T, const void* 
   tc::FusedArgs f;
   f.lp = nullptr;
   f.cta0_plans = 0;
-  f.jobs_ready = nullptr;
   f.plan_done = nullptr;
+  f.host_layer = nullptr;
+  f.lut_row = nullptr;
+  f.rid_land0 = 0;
+  f.S = p.S;
   f.jobs = sc.copies;
   f.n_jobs = sc.n_copy;
   // a bf16 record's tile data; an fp8 record whole (codes, then its scale tables)
@@ -2058,10 +2140,10 @@ static int launch_decode_layer_wf(const PoolDev& p, const Scratch& sc, const TcM
   pa.ids = sc.ids;
   pa.w = sc.w;
   pa.probs = sc.probs;
-  d.local = T * p.k <= tc::kLocalMaxTk && p.E <= kMaxE ? 1 : 0;
+  // local lists: the copied entries (at most min(T k, E)) land in the landing records
+  d.local = T * p.k <= tc::kLocalMaxTk && p.E <= kMaxE && std::min(T * p.k, p.E) <= p.n_land ? 1 : 0;
   pa.zero_sync = false;                      // CTA 0 zeroes the counters at kernel start
   pa.snap_wait = d.local ? sc.dsync + 35 : nullptr;
-  pa.jobs_flag = d.local ? sc.dsync + 36 : nullptr;
   pa.snap_target = (uint32_t)G;
   const size_t psm = decode_plan_smem<NT>(p, T, &pa.owner_cap, &pa.tok_rows);
   if (psm == 0) return -1;

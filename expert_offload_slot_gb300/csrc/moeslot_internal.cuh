@@ -50,9 +50,10 @@ struct PoolDev {           // device-side pointers handed to kernels by value
   float lam, one_minus_lam, cw0, cw1, cw2, cw3;
   Layout lay;
   const uint8_t* host_dev;     // device-visible base of the mapped host pool
-  // One record array: [S slots | n_bypass one-step records | 2E staging | L shared].
+  // One record array: [S slots | n_bypass one-step records | n_land landing records |
+  // 2E staging | L shared].
   uint8_t* records;
-  int32_t n_bypass, rid_staging0, rid_shared0, n_records;
+  int32_t n_bypass, rid_land0, n_land, rid_staging0, rid_shared0, n_records;
   uint8_t* slots;              // == records: the fixed base of the slot pool
   uint8_t* staging;            // records + rid_staging0 * rec, or null
   const uint8_t* shared_w;     // records + rid_shared0 * rec, or null
@@ -160,6 +161,7 @@ int launch_ffn_down(const PoolDev& p, const Scratch& sc, int T, void* out, cudaS
 struct TcMaps;                      // host-side tensor maps of a pool (k_tc.cu)
 TcMaps* tc_maps_create(const PoolDev& p, const Scratch& sc);
 bool tc_fp8_ok(const PoolDev& p);   // fp8 pool shapes the tensor-core kernels take
+int decode_landing_records(const PoolDev& p, int max_tokens);   // landing records the decode layer kernel needs
 void tc_maps_destroy(TcMaps* m);
 int tc_npad(int T);                 // padded token count (multiple of 16)
 // scratch sizes for a pool whose dense path takes up to npad_max token columns

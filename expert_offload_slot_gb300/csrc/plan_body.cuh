@@ -24,7 +24,6 @@ struct PlanArgs {
   bool zero_sync = true;                 // zero the expert kernel's counters (false: the caller does)
   const uint32_t* snap_wait = nullptr;   // if set: before writing the table, wait for *snap_wait >= snap_target
   uint32_t snap_target = 0;              // (other CTAs' reads of this layer's table row)
-  uint32_t* jobs_flag = nullptr;         // if set: released once the copy jobs are written
 };
 
 // Orderable key: (score ascending, slot ascending).  -0 is folded into +0.
@@ -463,18 +462,8 @@ __device__ void plan_body(const PlanArgs& a, uint8_t* dsm, bool prestaged = fals
       atomicAdd(&p.stats[ST_EVICT], (unsigned long long)sh_misc[5]);
       atomicAdd(&p.stats[ST_BYTES], (unsigned long long)n_miss * rec);   // slot fills + one-step records
     }
-    __syncthreads();
-    if (a.jobs_flag) {
-      // the copy jobs are complete: copies may start while the plan goes on
-      __threadfence();
-      __syncthreads();
-      if (tid == 0)
-        asm volatile("fence.acq_rel.gpu;\n red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.jobs_flag) : "memory");
-    }
   } else if (tid == 0) {
     *a.sc.n_copy = 0;
-    if (a.jobs_flag)
-      asm volatile("fence.acq_rel.gpu;\n red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.jobs_flag) : "memory");
   }
 
   // ------------------------------------------------------ a7 permutation

@@ -203,6 +203,12 @@ MOE_API moe_status moe_get_routing(moe_pool* pool, int32_t* ids, float* w, float
  *   score [L*E] fp32 (eviction score as of each layer's last update). */
 MOE_API moe_status moe_get_state(moe_pool* pool, int32_t* lut, int32_t* owner, uint32_t* tag, float* score);
 
+/* Blocking: host copy of the record held by `slot` (0 <= slot < num_slots),
+ * record_bytes of moe_expert_layout into `out` (host, at least that many bytes,
+ * out_bytes says how many).  For checks: a slot owned by (l, e) holds the bytes
+ * of host record l*E+e.  MOE_ERR_INVALID on a bad slot or a short buffer. */
+MOE_API moe_status moe_read_slot(moe_pool* pool, int32_t slot, void* out, size_t out_bytes);
+
 /* Blocking: cumulative counters. */
 MOE_API moe_status moe_get_stats(moe_pool* pool, moe_stats* out);
 

@@ -87,6 +87,45 @@ def test_tensor_core_output_independent_of_resident_set():
             r.close()
 
 
+@pytest.mark.parametrize("shape", ["bf16_small", "bf16_qwen3_layer", "fp8"])
+def test_slots_hold_their_owners_records_after_decode_steps(shape):
+    """After decode steps whose misses were copied in-kernel (landing record, then slot), every owned
+    slot holds exactly the host record of its owner (SeqMoE "Mechanism": a miss fills the slot the
+    table points at), and the table agrees with the oracle's simulator."""
+    if shape == "fp8":
+        wl = variant(get_workload("dsv3"), name="slots_fp8", L=2, E=32, k=4, H=512, I=256)
+        S, Ts = 20, (1, 8, 24)
+    elif shape == "bf16_small":
+        wl = variant(get_workload("qwen3_decode"), name="slots_bf16", L=2, E=64, k=8, H=1024, I=512)
+        S, Ts = 40, (1, 4, 16)
+    else:
+        wl = variant(get_workload("qwen3_decode"), name="slots_qwen3", L=2, E=128, k=8, H=2048, I=768)
+        S, Ts = 110, (16,)
+    rig = Rig(wl, S=S, max_tokens=32)
+    try:
+        host = rig.host.numpy()
+        misses = 0
+        for T in Ts:
+            for step in range(3):
+                for l in range(wl.L):
+                    x = gen.store_act(wl, gen.decode_hidden(wl, l, T, 1, base_seed=97 * T + step)[0])
+                    rig.forward(l, x)
+                    r = rig.pool.routing(T)
+                    rig.sim.update_scores(l, r["ids"], r["probs"])
+                    misses += rig.sim.plan(l, r["ids"])["misses"]
+            st = rig.pool.state()
+            np.testing.assert_array_equal(st["lut"], rig.sim.lut)
+            np.testing.assert_array_equal(st["owner"], rig.sim.owner)
+            for slot in range(S):
+                o = int(st["owner"][slot])
+                if o >= 0:
+                    got = rig.pool.read_slot(slot)
+                    assert np.array_equal(got, host[o * rig.rec:(o + 1) * rig.rec]), (T, slot, o)
+        assert misses > 0 and rig.pool.status() == 0
+    finally:
+        rig.close()
+
+
 def test_load_slot_matches_oracle_and_keeps_output():
     wl = variant(get_workload("qwen3_decode"), name="loadslot", L=2, E=16, k=2, H=256, I=256)
     rig = Rig(wl, S=6)
