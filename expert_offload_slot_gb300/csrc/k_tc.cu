@@ -655,7 +655,7 @@ tc_gather_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constan
 // Partial tiles are row-major ([128 rows][columns]) so that each epilogue
 // thread (one row) moves its columns with 16-byte accesses.
 constexpr int kCopyWarps = 2;
-constexpr int kCopyUnroll = 16;  // 16-byte host reads in flight per copy lane
+constexpr int kCopyUnroll = 8;   // 16-byte host reads in flight per copy lane
 constexpr int kFusedThreads = kThreads + 32 * kCopyWarps;
 constexpr int kFusedBufs = 8;
 template <int WF> struct FusedShape {
@@ -683,8 +683,8 @@ struct FusedArgs {
   int cta0_plans;               // CTA 0 runs the plan and takes no expert units
   // with lp: a miss j (j-th copied entry) is copied from the host pool into landing
   // record rid_land0 + j at once, read from there, and written to its slot once the
-  // plan (plan_done) has chosen it
-  const uint32_t* plan_done;
+  // plan has chosen it (slots_ready: the table holds this step's slots)
+  const uint32_t* slots_ready;
   const uint8_t* host_layer;    // host pool records of this layer (device view)
   const int32_t* lut_row;       // this layer's table row
   int rid_land0, S;
@@ -782,6 +782,13 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+
+// Add with acquire-release semantics at GPU scope; returns the old value.
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
 }
 
 // Release this thread's prior writes (and, after a CTA barrier, the CTA's) and add 1.
@@ -1113,14 +1120,16 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
             fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty_bar[buf]);
-            __threadfence();
           }
+          // One acquire-release add per CTA: it releases this CTA's partials (every thread's
+          // stores are ordered before it by the barrier), and the last split to arrive
+          // acquires the others' (its threads' loads are ordered after it by the next barrier).
           asm volatile("bar.sync 1, 128;" ::: "memory");
           if (warp == 2 && lane == 0) {
             last_sh = 0;
             if (!abort_sh) {
-              const int old = atomicAdd(&f.gu_cnt[tile], 1);
-              if (old == sc.sg - 1) {
+              const uint32_t old = atom_add_acq_rel(reinterpret_cast<uint32_t*>(&f.gu_cnt[tile]), 1u);
+              if (old == (uint32_t)sc.sg - 1) {
                 last_sh = 1;
                 f.gu_cnt[tile] = 0;
               }
@@ -1128,7 +1137,6 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
           }
           asm volatile("bar.sync 1, 128;" ::: "memory");
           if (last_sh && live) {
-            __threadfence();
             const float* base = f.gu_partial + tile * sc.sg * pstride + (size_t)row * cols;
             for (int c0 = 0; c0 < N; c0 += 16) {
               float s0[16], s1[16];
@@ -1162,8 +1170,8 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
             done_h = true;
           }
         }
-        // publish: this entry has one more finished gate/up tile
-        if (done_h) __threadfence();
+        // publish: this entry has one more finished gate/up tile (the barrier orders
+        // every thread's h stores before the one release, which is cumulative)
         asm volatile("bar.sync 1, 128;" ::: "memory");
         if (warp == 2 && lane == 0 && done_h && !abort_sh) release_add(&f.hready[r.u]);
       } else {
@@ -1260,8 +1268,9 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
     if (go && cta >= 0) {
       const uint32_t n = f.lp ? (uint32_t)f.lp->nm : (uint32_t)__ldcg(f.n_jobs);
       // local lists: each miss lands in its landing record at once; from the moment the
-      // plan is seen, its chunks go to the chosen slot as well.  (j_dual, c_dual): the
-      // first job and warp chunk written to both; what came before is copied over later.
+      // table is seen final (slots_ready), its chunks go to the chosen slot as well.
+      // (j_dual, c_dual): the first job and warp chunk written to both; what came before
+      // is copied over later.
       bool planned = !f.lp;
       uint32_t j_dual = n, c_dual = 0;
       for (uint32_t j = 0; j < n; ++j) {
@@ -1281,7 +1290,7 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
         for (uint32_t wb = w0; wb < f.tile16; wb += stride * kCopyUnroll) {
           if (!planned) {
             uint32_t pv = 0;
-            if (lane == 0) pv = ld_acquire(f.plan_done);
+            if (lane == 0) pv = ld_acquire(f.slots_ready);
             planned = __shfl_sync(0xffffffffu, pv, 0) != 0u;
             if (planned) {
               dst2 = slot_record(e);
@@ -1310,11 +1319,11 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
         if (warp == Shape::copy_warp0 && lane == 0) release_add(&f.jdone[j]);
       }
       if (f.lp && n > 0) {
-        // the chunks that landed before the plan was seen, into their slots: this
+        // the chunks that landed before the table was seen final, into their slots: this
         // thread re-reads only what it wrote
         if (!planned) {
           bool ok = true;
-          if (lane == 0) ok = wait_count(f.plan_done, 1u, a.status);
+          if (lane == 0) ok = wait_count(f.slots_ready, 1u, a.status);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) set_status(a.status, MOE_ERR_TIMEOUT);
           planned = ok;
@@ -1425,8 +1434,8 @@ tc_fused_decode_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
 //          plan's work lists.
 // Counters: route_done (tokens gated) counts T gates plus CTA 0's zeroing of
 // the expert counters; tickets reset on their last arrival; plan_done,
-// snap_done (and, after a timeout, the others) are reset by the last CTA to
-// leave, so each launch starts from zero.
+// snap_done, slots_ready (and, after a timeout, the others) are reset by the
+// last CTA to leave, so each launch starts from zero.
 struct DecodeArgs {
   int local;                // every CTA derives the step's entry lists itself (T * k <= kLocalMaxTk)
   const uint16_t* x;        // [T][H] bf16
@@ -1436,7 +1445,7 @@ struct DecodeArgs {
   int eb, nblk;             // experts per routing CTA, routing CTAs per token
   PlanArgs plan;
   uint32_t* dsync;          // [0] route_done, [1] plan_done, [2] exit count, [3 + t] ticket of token t,
-                            // [35] CTAs holding their copy of the layer's table row
+                            // [35] CTAs holding their copy of the layer's table row, [36] table final
 };
 
 constexpr int kDecodeMaxT = 32;
@@ -1464,6 +1473,7 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
   uint32_t* exit_cnt = d.dsync + 2;
   uint32_t* ticket = d.dsync + 3;
   uint32_t* snap_done = d.dsync + 35;
+  uint32_t* slots_ready = d.dsync + 36;
   const PoolDev& p = d.plan.p;
   const int l = d.plan.layer;
 
@@ -1546,7 +1556,7 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
   if (d.local) {
     fl.lp = &lp_sh;
     fl.cta0_plans = 1;
-    fl.plan_done = plan_done;
+    fl.slots_ready = slots_ready;
     fl.host_layer = p.host_dev + (size_t)l * E * p.lay.rec;
     fl.lut_row = p.lut + (size_t)l * E;
     fl.rid_land0 = p.rid_land0;
@@ -1644,6 +1654,7 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
       *route_done = 0u;
       *plan_done = 0u;
       *snap_done = 0u;
+      *slots_ready = 0u;
       for (int t = 0; t < kDecodeMaxT; ++t) ticket[t] = 0u;
       *exit_cnt = 0u;
     }
@@ -2016,7 +2027,7 @@ static bool fused_setup(const PoolDev& p, const Scratch& sc, int T, const void* 
   tc::FusedArgs f;
   f.lp = nullptr;
   f.cta0_plans = 0;
-  f.plan_done = nullptr;
+  f.slots_ready = nullptr;
   f.host_layer = nullptr;
   f.lut_row = nullptr;
   f.rid_land0 = 0;
@@ -2144,6 +2155,7 @@ static int launch_decode_layer_wf(const PoolDev& p, const Scratch& sc, const TcM
   d.local = T * p.k <= tc::kLocalMaxTk && p.E <= kMaxE && std::min(T * p.k, p.E) <= p.n_land ? 1 : 0;
   pa.zero_sync = false;                      // CTA 0 zeroes the counters at kernel start
   pa.snap_wait = d.local ? sc.dsync + 35 : nullptr;
+  pa.slots_flag = d.local ? sc.dsync + 36 : nullptr;
   pa.snap_target = (uint32_t)G;
   const size_t psm = decode_plan_smem<NT>(p, T, &pa.owner_cap, &pa.tok_rows);
   if (psm == 0) return -1;

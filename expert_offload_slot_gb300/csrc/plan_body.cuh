@@ -24,6 +24,7 @@ struct PlanArgs {
   bool zero_sync = true;                 // zero the expert kernel's counters (false: the caller does)
   const uint32_t* snap_wait = nullptr;   // if set: before writing the table, wait for *snap_wait >= snap_target
   uint32_t snap_target = 0;              // (other CTAs' reads of this layer's table row)
+  uint32_t* slots_flag = nullptr;        // if set: released once the table holds this step's slots
 };
 
 // Orderable key: (score ascending, slot ascending).  -0 is folded into +0.
@@ -464,6 +465,13 @@ __device__ void plan_body(const PlanArgs& a, uint8_t* dsm, bool prestaged = fals
     }
   } else if (tid == 0) {
     *a.sc.n_copy = 0;
+  }
+  if (a.slots_flag) {
+    // the table is final for this step: copies may move to the chosen slots
+    __threadfence();
+    __syncthreads();
+    if (tid == 0)
+      asm volatile("fence.acq_rel.gpu;\n red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.slots_flag) : "memory");
   }
 
   // ------------------------------------------------------ a7 permutation
