@@ -357,7 +357,7 @@ MOE_API moe_status moe_pool_create(const moe_config* cfg, const void* host_pool,
     PA(P->sc.dn_partial, P->sc.dn_partial_floats, 0);
     P->sc.n_ffn_sync = tc_ffn_sync_ints(d);
     PA(P->sc.ffn_sync, P->sc.n_ffn_sync, 0);
-    PA(P->sc.dsync, 64, 0);
+    PA(P->sc.dsync, tc_dsync_ints(), 0);
     if (Tm > 32 && cfg->act_dtype == MOE_BF16) PA(P->sc.rpart, (size_t)32 * Tm * E, 0);
     if ((size_t)tc_npad((int)Tm) > (size_t)np) {
       // gather path for calls with more tokens than the dense path takes
@@ -642,7 +642,7 @@ MOE_API moe_status moe_clear_status(moe_pool* P) {
   CUDA_TRY(cudaDeviceSynchronize());
   CUDA_TRY(cudaMemset(P->d.status, 0, sizeof(int32_t)));
   // counters a timed-out launch may have left behind
-  if (P->sc.dsync) CUDA_TRY(cudaMemset(P->sc.dsync, 0, 64 * sizeof(uint32_t)));
+  if (P->sc.dsync) CUDA_TRY(cudaMemset(P->sc.dsync, 0, tc_dsync_ints() * sizeof(uint32_t)));
   if (P->sc.ticket) CUDA_TRY(cudaMemset(P->sc.ticket, 0, sizeof(int32_t)));
   return MOE_OK;
 }

@@ -639,8 +639,10 @@ tc_gather_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constan
 //   2. down tiles of those entries,
 //   3. gate/up tiles of the entries copied this step (in copy-job order),
 //   4. down tiles of those entries;
-// meanwhile two copy warps per CTA pull this step's misses from the mapped
-// host pool (NVLink-C2C reads) into their records, one job after another.  A
+// meanwhile this step's misses are pulled from the mapped host pool (NVLink-C2C
+// reads) into their records, one job after another: by kCopyCtas copy-only CTAs
+// with all their threads in the decode layer kernel, else by two copy warps in
+// every CTA.  A
 // unit waits only for what it reads: a copied record (jdone[job] == G: every
 // CTA's slice of that job is written) or the complete h of its entry.  (Finer
 // readiness within a job costs the copy warps a fence per part, which slows the
@@ -655,8 +657,8 @@ tc_gather_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constan
 // Partial tiles are row-major ([128 rows][columns]) so that each epilogue
 // thread (one row) moves its columns with 16-byte accesses.
 constexpr int kCopyWarps = 2;
+constexpr int kCopyCtas = 32;   // copy-only CTAs of a decode layer call with misses (local lists)
 constexpr int kCopyUnroll = 8;   // 16-byte host reads in flight per copy lane
-constexpr int kFusedThreads = kThreads + 32 * kCopyWarps;
 constexpr int kFusedBufs = 8;
 template <int WF> struct FusedShape {
   static constexpr int conv_warps = WF == kWfFp8 ? kConvWarps : 0;
@@ -691,6 +693,8 @@ struct FusedArgs {
   const CopyJob* jobs;
   const int32_t* n_jobs;
   uint32_t tile16;              // bytes of a record the miss copy moves, in 16 B units
+  uint32_t part16;              // its first part, all that gate/up units read (bf16: the W_gate/W_up
+                                // tiles; fp8: the whole record), in 16 B units
   // fp8 records: scale tables at os13 ([2I/128][H/128] fp32) and os2 ([H/128][I/128])
   size_t os13, os2;
   int sc_h, sc_i;               // scale row lengths: H / 128 and I / 128
@@ -704,7 +708,8 @@ struct FusedArgs {
   int32_t* gu_cnt;              // [E1 * MT_I] split arrivals per gate/up tile    } zeroed by the plan
   uint32_t* dn_done;            // CTAs whose down units are all written           } kernel before
   uint32_t* hready;             // [E1] finished gate/up tiles per entry           } every launch
-  uint32_t* jdone;              // [E1] CTAs done with each copy job               }
+  uint32_t* jdone;              // [E1] CTAs done with each copy job's first part  }
+  uint32_t* jdone_w2;           // [E1] ... and with the whole record              }
 };
 
 struct FSched {
@@ -875,8 +880,14 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
   __syncthreads();
   fence_after();
   const bool go = pre();
-  const int Gc = G - f.cta0_plans;                          // CTAs that take expert units
-  const int cta = (int)blockIdx.x - f.cta0_plans;           // this CTA's index among them (-1: none)
+  // Local lists and a step with misses: CTAs cta0_plans .. + kCopyCtas - 1 copy the misses
+  // with all their threads and take no expert units, so that the expert CTAs' stores and
+  // fences never queue behind host reads.  Otherwise the copy warps of every CTA copy.
+  const int ncopy = go && f.lp && f.lp->nm > 0 ? min(kCopyCtas, G - f.cta0_plans - 1) : 0;
+  const int Gc = G - f.cta0_plans - ncopy;                  // CTAs that take expert units
+  const int cta = (int)blockIdx.x - f.cta0_plans - ncopy;   // this CTA's index among them (< 0: none)
+  const bool copy_cta = ncopy > 0 && (int)blockIdx.x >= f.cta0_plans && cta < 0;
+  const uint32_t njd = ncopy > 0 ? (uint32_t)ncopy : (uint32_t)(G - f.cta0_plans);   // CTAs releasing each job
   if (threadIdx.x == 0) {
     if (go) {
       sched_sh = fused_sched(a, f, G);   // the unit decomposition, identical in every role and CTA
@@ -889,7 +900,125 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
   const uint32_t tmem = tmem_base_sh;
   const uint32_t idesc = idesc_bf16(N);
 
-  if (warp == 0) {
+  // Record copies, job by job and part by part (first the gate/up part, which releases
+  // jdone[j], then the rest, which releases jdone_w2[j]; both count the copying CTAs):
+  // nthr threads of each of ncta CTAs copy; thread tid of copying CTA cidx takes the
+  // 16-byte chunks wb + lane + u * stride (u < kCopyUnroll) of the lattice rows
+  // wb = w0 + i * kCopyUnroll * stride, w0 = its warp's first chunk, that fall in the
+  // part.  The loops run on wb, so all lanes of a warp take the same trip count (the
+  // warp-wide shuffles below need that).
+  auto copy_jobs = [&](uint32_t nthr, uint32_t tid, uint32_t cidx, uint32_t ncta) {
+    const uint32_t stride = ncta * nthr;
+    const uint32_t step = stride * kCopyUnroll;
+    const uint32_t w0 = cidx * nthr + (tid & ~31u);
+    auto first_row = [&](uint32_t lo) { return lo <= w0 ? w0 : w0 + (lo - w0) / step * step; };
+    // slot record the plan gave expert e (null: none, the miss stays in its landing record)
+    auto slot_record = [&](int e) -> uint4* {
+      int slot = -1;
+      if (lane == 0) slot = __ldcg(f.lut_row + e);
+      slot = __shfl_sync(0xffffffffu, slot, 0);
+      return slot >= 0 && slot < f.S ? reinterpret_cast<uint4*>(const_cast<uint8_t*>(a.records) + (size_t)slot * a.rec)
+                                     : nullptr;
+    };
+    // chunks [lo, hi) of rows wb < wend: src -> dst
+    auto copy_range = [&](const uint4* src, uint4* dst, uint32_t lo, uint32_t hi, uint32_t wend) {
+      for (uint32_t wb = first_row(lo); wb < min(hi, wend); wb += step) {
+        const uint32_t base = wb + lane;
+        uint4 v[kCopyUnroll];
+#pragma unroll
+        for (int u = 0; u < kCopyUnroll; ++u) {
+          const uint32_t idx = base + (uint32_t)u * stride;
+          if (idx >= lo && idx < hi) v[u] = __ldcs(src + idx);
+        }
+#pragma unroll
+        for (int u = 0; u < kCopyUnroll; ++u) {
+          const uint32_t idx = base + (uint32_t)u * stride;
+          if (idx >= lo && idx < hi) __stcs(dst + idx, v[u]);
+        }
+      }
+    };
+    const uint32_t n = f.lp ? (uint32_t)f.lp->nm : (uint32_t)__ldcg(f.n_jobs);
+    // local lists: each miss lands in its landing record at once; from the moment the
+    // table is seen final (slots_ready), its chunks go to the chosen slot as well.
+    // (j_dual, p_dual, c_dual): the first job, part and row written to both; what came
+    // before is copied over at the end.
+    bool planned = !f.lp;
+    uint32_t j_dual = n, p_dual = 0, c_dual = 0;
+    for (uint32_t j = 0; j < n; ++j) {
+      const uint4* src;
+      uint4* dst;
+      uint4* dst2 = nullptr;
+      int e = -1;
+      if (f.lp) {
+        e = f.lp->expert[f.lp->elist[1][j]];
+        src = reinterpret_cast<const uint4*>(f.host_layer + (size_t)e * a.rec);
+        dst = reinterpret_cast<uint4*>(const_cast<uint8_t*>(a.records) + (size_t)(f.rid_land0 + (int)j) * a.rec);
+        if (planned) dst2 = slot_record(e);
+      } else {
+        src = reinterpret_cast<const uint4*>(f.jobs[j].src);
+        dst = reinterpret_cast<uint4*>(f.jobs[j].dst);
+      }
+      for (uint32_t part = 0; part < 2; ++part) {
+        const uint32_t lo = part ? f.part16 : 0u, hi = part ? f.tile16 : f.part16;
+        for (uint32_t wb = first_row(lo); wb < hi; wb += step) {
+          if (!planned) {
+            uint32_t pv = 0;
+            if (lane == 0) pv = ld_acquire(f.slots_ready);
+            planned = __shfl_sync(0xffffffffu, pv, 0) != 0u;
+            if (planned) {
+              dst2 = slot_record(e);
+              j_dual = j;
+              p_dual = part;
+              c_dual = wb;
+            }
+          }
+          const uint32_t base = wb + lane;
+          uint4 v[kCopyUnroll];
+#pragma unroll
+          for (int u = 0; u < kCopyUnroll; ++u) {
+            const uint32_t idx = base + (uint32_t)u * stride;
+            if (idx >= lo && idx < hi) v[u] = __ldcs(src + idx);
+          }
+#pragma unroll
+          for (int u = 0; u < kCopyUnroll; ++u) {
+            const uint32_t idx = base + (uint32_t)u * stride;
+            if (idx >= lo && idx < hi) {
+              __stcs(dst + idx, v[u]);
+              if (dst2) __stcs(dst2 + idx, v[u]);
+            }
+          }
+        }
+        __threadfence();
+        asm volatile("bar.sync 2, %0;" ::"r"(nthr) : "memory");
+        if (tid == 0) release_add(part ? &f.jdone_w2[j] : &f.jdone[j]);
+      }
+    }
+    if (f.lp && n > 0) {
+      // the chunks that landed before the table was seen final, into their slots: this
+      // thread re-reads only what it wrote
+      if (!planned) {
+        bool ok = true;
+        if (lane == 0) ok = wait_count(f.slots_ready, 1u, a.status);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) set_status(a.status, MOE_ERR_TIMEOUT);
+        planned = ok;
+      }
+      for (uint32_t j = 0; planned && j < n && j <= j_dual; ++j) {
+        uint4* dst = slot_record(f.lp->expert[f.lp->elist[1][j]]);
+        if (!dst) continue;
+        const uint4* src = reinterpret_cast<const uint4*>(a.records + (size_t)(f.rid_land0 + (int)j) * a.rec);
+        for (uint32_t part = 0; part < 2; ++part) {
+          const bool before = j < j_dual || part < p_dual;
+          if (!before && part > p_dual) break;
+          copy_range(src, dst, part ? f.part16 : 0u, part ? f.tile16 : f.part16, before ? f.tile16 : c_dual);
+        }
+      }
+    }
+  };
+
+  if (copy_cta) {
+    copy_jobs(blockDim.x, threadIdx.x, (uint32_t)((int)blockIdx.x - f.cta0_plans), (uint32_t)ncopy);
+  } else if (warp == 0) {
     // ------------------------------------------------------------- producer
     if (lane == 0) {
       const FSched sc = sched_sh;
@@ -901,9 +1030,9 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
         int rid = 0;
         if (!r.miss) rid = f.lp ? f.lp->rid[r.u] : a.work[r.u].rid;
         if (r.miss) {
-          // a copied record: every copying CTA's slice of its job must have landed (down
-          // units too: their weight tiles go out before h is complete)
-          if (!wait_count(&f.jdone[r.li], (uint32_t)Gc, a.status)) { ok = false; break; }
+          // a copied record: every copying CTA's slice of the part this unit reads must
+          // have landed (down units too: their weight tiles go out before h is complete)
+          if (!wait_count(r.gu ? &f.jdone[r.li] : &f.jdone_w2[r.li], njd, a.status)) { ok = false; break; }
           asm volatile("fence.proxy.async.global;" ::: "memory");   // generic writes -> bulk-copy reads
           // the landing record, or the plan's choice (slot or one-step record)
           rid = f.lp ? f.rid_land0 + r.li : __ldcg(&a.work[r.u].rid);
@@ -1249,107 +1378,9 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
       }
       asm volatile("bar.sync 3, %0;" ::"n"(32 * kConvWarps) : "memory");   // before the scale buffer is reused
     }
-  } else {
+  } else if (!f.lp && go) {
     // ------------------------------------------------------------- copy warps
-    // Job by job: this CTA's slice of each record's tile data, then one release per job.
-    // A lane's 16-byte chunks are w0 + lane + (i * kCopyUnroll + u) * stride, with
-    // w0 the warp's first chunk; the loops run on w0, so every lane of a warp takes
-    // the same trip count (the warp-wide shuffles below need that).
-    const uint32_t stride = (uint32_t)Gc * (32u * kCopyWarps);
-    const uint32_t w0 = (uint32_t)cta * (32u * kCopyWarps) + (uint32_t)(warp - Shape::copy_warp0) * 32u;
-    // slot record the plan gave expert e (null: none, the miss stays in its landing record)
-    auto slot_record = [&](int e) -> uint4* {
-      int slot = -1;
-      if (lane == 0) slot = __ldcg(f.lut_row + e);
-      slot = __shfl_sync(0xffffffffu, slot, 0);
-      return slot >= 0 && slot < f.S ? reinterpret_cast<uint4*>(const_cast<uint8_t*>(a.records) + (size_t)slot * a.rec)
-                                     : nullptr;
-    };
-    if (go && cta >= 0) {
-      const uint32_t n = f.lp ? (uint32_t)f.lp->nm : (uint32_t)__ldcg(f.n_jobs);
-      // local lists: each miss lands in its landing record at once; from the moment the
-      // table is seen final (slots_ready), its chunks go to the chosen slot as well.
-      // (j_dual, c_dual): the first job and warp chunk written to both; what came before
-      // is copied over later.
-      bool planned = !f.lp;
-      uint32_t j_dual = n, c_dual = 0;
-      for (uint32_t j = 0; j < n; ++j) {
-        const uint4* src;
-        uint4* dst;
-        uint4* dst2 = nullptr;
-        int e = -1;
-        if (f.lp) {
-          e = f.lp->expert[f.lp->elist[1][j]];
-          src = reinterpret_cast<const uint4*>(f.host_layer + (size_t)e * a.rec);
-          dst = reinterpret_cast<uint4*>(const_cast<uint8_t*>(a.records) + (size_t)(f.rid_land0 + (int)j) * a.rec);
-          if (planned) dst2 = slot_record(e);
-        } else {
-          src = reinterpret_cast<const uint4*>(f.jobs[j].src);
-          dst = reinterpret_cast<uint4*>(f.jobs[j].dst);
-        }
-        for (uint32_t wb = w0; wb < f.tile16; wb += stride * kCopyUnroll) {
-          if (!planned) {
-            uint32_t pv = 0;
-            if (lane == 0) pv = ld_acquire(f.slots_ready);
-            planned = __shfl_sync(0xffffffffu, pv, 0) != 0u;
-            if (planned) {
-              dst2 = slot_record(e);
-              j_dual = j;
-              c_dual = wb;
-            }
-          }
-          const uint32_t base = wb + lane;
-          uint4 v[kCopyUnroll];
-#pragma unroll
-          for (int u = 0; u < kCopyUnroll; ++u) {
-            const uint32_t idx = base + (uint32_t)u * stride;
-            if (idx < f.tile16) v[u] = __ldcs(src + idx);
-          }
-#pragma unroll
-          for (int u = 0; u < kCopyUnroll; ++u) {
-            const uint32_t idx = base + (uint32_t)u * stride;
-            if (idx < f.tile16) {
-              __stcs(dst + idx, v[u]);
-              if (dst2) __stcs(dst2 + idx, v[u]);
-            }
-          }
-        }
-        __threadfence();
-        asm volatile("bar.sync 2, %0;" ::"n"(32 * kCopyWarps) : "memory");
-        if (warp == Shape::copy_warp0 && lane == 0) release_add(&f.jdone[j]);
-      }
-      if (f.lp && n > 0) {
-        // the chunks that landed before the table was seen final, into their slots: this
-        // thread re-reads only what it wrote
-        if (!planned) {
-          bool ok = true;
-          if (lane == 0) ok = wait_count(f.slots_ready, 1u, a.status);
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) set_status(a.status, MOE_ERR_TIMEOUT);
-          planned = ok;
-        }
-        for (uint32_t j = 0; planned && j < n && j <= j_dual; ++j) {
-          uint4* dst = slot_record(f.lp->expert[f.lp->elist[1][j]]);
-          if (!dst) continue;
-          const uint4* src = reinterpret_cast<const uint4*>(a.records + (size_t)(f.rid_land0 + (int)j) * a.rec);
-          const uint32_t wend = j < j_dual ? f.tile16 : min(c_dual, f.tile16);
-          for (uint32_t wb = w0; wb < wend; wb += stride * kCopyUnroll) {
-            const uint32_t base = wb + lane;
-            uint4 v[kCopyUnroll];
-#pragma unroll
-            for (int u = 0; u < kCopyUnroll; ++u) {
-              const uint32_t idx = base + (uint32_t)u * stride;
-              if (idx < f.tile16) v[u] = __ldcs(src + idx);
-            }
-#pragma unroll
-            for (int u = 0; u < kCopyUnroll; ++u) {
-              const uint32_t idx = base + (uint32_t)u * stride;
-              if (idx < f.tile16) __stcs(dst + idx, v[u]);
-            }
-          }
-        }
-      }
-    }
+    copy_jobs(32u * kCopyWarps, (uint32_t)(warp - Shape::copy_warp0) * 32u + lane, blockIdx.x, (uint32_t)G);
   }
   fence_before();
   __syncthreads();
@@ -1444,9 +1475,14 @@ struct DecodeArgs {
   float* z;                 // [T][E] logits scratch
   int eb, nblk;             // experts per routing CTA, routing CTAs per token
   PlanArgs plan;
-  uint32_t* dsync;          // [0] route_done, [1] plan_done, [2] exit count, [3 + t] ticket of token t,
-                            // [35] CTAs holding their copy of the layer's table row, [36] table final
+  uint32_t* dsync;          // counters, one per 128-byte line (kSyncLine ints): route_done, plan_done, exit
+                            // count, CTAs holding their copy of the layer's table row, table final, then
+                            // the ticket of token t at line kDsTicket + t
 };
+// Every counter that many CTAs poll or add to has a line of its own, so that the
+// polls of one do not queue in front of the atomics of another.
+constexpr int kSyncLine = 32;
+constexpr int kDsRoute = 0, kDsPlan = 1, kDsExit = 2, kDsSnap = 3, kDsSlots = 4, kDsTicket = 8;
 
 constexpr int kDecodeMaxT = 32;
 constexpr int kRouterMaxSplits = 32;   // K splits of the tensor-core router
@@ -1468,12 +1504,12 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = a.T, H = a.H, E = d.plan.p.E;
   const int G = gridDim.x;
-  uint32_t* route_done = d.dsync;
-  uint32_t* plan_done = d.dsync + 1;
-  uint32_t* exit_cnt = d.dsync + 2;
-  uint32_t* ticket = d.dsync + 3;
-  uint32_t* snap_done = d.dsync + 35;
-  uint32_t* slots_ready = d.dsync + 36;
+  uint32_t* route_done = d.dsync + kDsRoute * kSyncLine;
+  uint32_t* plan_done = d.dsync + kDsPlan * kSyncLine;
+  uint32_t* exit_cnt = d.dsync + kDsExit * kSyncLine;
+  uint32_t* snap_done = d.dsync + kDsSnap * kSyncLine;
+  uint32_t* slots_ready = d.dsync + kDsSlots * kSyncLine;
+  auto ticket = [&](int t) -> uint32_t* { return d.dsync + (kDsTicket + t) * kSyncLine; };
   const PoolDev& p = d.plan.p;
   const int l = d.plan.layer;
 
@@ -1534,9 +1570,9 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
-      const uint32_t old = atomicAdd(&ticket[t], 1u);
+      const uint32_t old = atomicAdd(ticket(t), 1u);
       flag_sh = old == (uint32_t)d.nblk - 1;
-      if (flag_sh) ticket[t] = 0u;
+      if (flag_sh) *ticket(t) = 0u;
     }
     __syncthreads();
     if (flag_sh && warp == 0) {
@@ -1655,7 +1691,7 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
       *plan_done = 0u;
       *snap_done = 0u;
       *slots_ready = 0u;
-      for (int t = 0; t < kDecodeMaxT; ++t) ticket[t] = 0u;
+      for (int t = 0; t < kDecodeMaxT; ++t) *ticket(t) = 0u;
       *exit_cnt = 0u;
     }
   }
@@ -1945,11 +1981,16 @@ static uint32_t tile16(const PoolDev& p) {
   return (uint32_t)((p.lay.off2 + mt_h * kb_i * tc::kTileBytes) / 16);
 }
 
-// [gu_cnt: (E+1) * MT_I][dn_done (+ MT_H - 1 spare)][hready: E+1][jdone: E+1]
-int tc_ffn_sync_ints(const PoolDev& p) {
-  const int mt_i = (p.I + 127) / 128, mt_h = (p.H + 127) / 128;
-  return (p.E + 1) * mt_i + mt_h + 2 * (p.E + 1);
+// [gu_cnt: (E+1) * MT_I, padded to a 128-byte line][dn_done: a line of its own][hready: E+1]
+// [jdone: E+1][jdone_w2: E+1]
+static int dn_done_index(const PoolDev& p) {
+  const int mt_i = (p.I + 127) / 128;
+  return ((p.E + 1) * mt_i + tc::kSyncLine - 1) / tc::kSyncLine * tc::kSyncLine;
 }
+int tc_ffn_sync_ints(const PoolDev& p) { return dn_done_index(p) + tc::kSyncLine + 3 * (p.E + 1); }
+
+// decode layer kernel counters: a line for each of kDsTicket named ones and for every token's ticket
+int tc_dsync_ints() { return (tc::kDsTicket + tc::kDecodeMaxT) * tc::kSyncLine; }
 
 static tc::Args tc_args(const PoolDev& p, const Scratch& sc, int T, int N) {
   tc::Args a;
@@ -2036,6 +2077,7 @@ static bool fused_setup(const PoolDev& p, const Scratch& sc, int T, const void* 
   f.n_jobs = sc.n_copy;
   // a bf16 record's tile data; an fp8 record whole (codes, then its scale tables)
   f.tile16 = p.wdt == MOE_FP8_E4M3_B128 ? (uint32_t)(p.lay.rec / 16) : tile16(p);
+  f.part16 = p.wdt == MOE_FP8_E4M3_B128 ? f.tile16 : (uint32_t)(p.lay.off2 / 16);
   f.os13 = p.lay.offs13;
   f.os2 = p.lay.offs2;
   f.sc_h = p.H / 128;
@@ -2047,11 +2089,11 @@ static bool fused_setup(const PoolDev& p, const Scratch& sc, int T, const void* 
   f.gu_partial_floats = sc.partial_floats;
   f.dn_partial = sc.dn_partial;
   f.dn_partial_floats = sc.dn_partial_floats;
-  const int mt_i = (p.I + 127) / 128, mt_h = (p.H + 127) / 128;
   f.gu_cnt = sc.ffn_sync;
-  f.dn_done = reinterpret_cast<uint32_t*>(sc.ffn_sync + (size_t)(p.E + 1) * mt_i);
-  f.hready = f.dn_done + mt_h;
+  f.dn_done = reinterpret_cast<uint32_t*>(sc.ffn_sync + dn_done_index(p));
+  f.hready = f.dn_done + tc::kSyncLine;
   f.jdone = f.hready + (p.E + 1);
+  f.jdone_w2 = f.jdone + (p.E + 1);
   *ap = a;
   *fp = f;
   return true;
@@ -2154,8 +2196,8 @@ static int launch_decode_layer_wf(const PoolDev& p, const Scratch& sc, const TcM
   // local lists: the copied entries (at most min(T k, E)) land in the landing records
   d.local = T * p.k <= tc::kLocalMaxTk && p.E <= kMaxE && std::min(T * p.k, p.E) <= p.n_land ? 1 : 0;
   pa.zero_sync = false;                      // CTA 0 zeroes the counters at kernel start
-  pa.snap_wait = d.local ? sc.dsync + 35 : nullptr;
-  pa.slots_flag = d.local ? sc.dsync + 36 : nullptr;
+  pa.snap_wait = d.local ? sc.dsync + tc::kDsSnap * tc::kSyncLine : nullptr;
+  pa.slots_flag = d.local ? sc.dsync + tc::kDsSlots * tc::kSyncLine : nullptr;
   pa.snap_target = (uint32_t)G;
   const size_t psm = decode_plan_smem<NT>(p, T, &pa.owner_cap, &pa.tok_rows);
   if (psm == 0) return -1;

@@ -100,7 +100,7 @@ struct Scratch {
   size_t dn_partial_floats;
   int32_t* ffn_sync;  // arrival counters and readiness flags of the fused decode kernel,
   int32_t n_ffn_sync; // zeroed by the plan kernel before every expert launch
-  uint32_t* dsync;    // [3 + 32] counters of the decode layer kernel (reset by its last CTA)
+  uint32_t* dsync;    // [tc_dsync_ints()] counters of the decode layer kernel (reset by its last CTA)
   float* rpart;       // [32][Tmax][E] K-split partial logits of the tensor-core router (Tmax > 32)
   int32_t* elist;     // [2][E+1]: work entries already resident / copied this step
   int32_t* ecount;    // [2]
@@ -168,6 +168,7 @@ int tc_npad(int T);                 // padded token count (multiple of 16)
 size_t tc_partial_floats(const PoolDev& p, int npad_max);      // Scratch::partial
 size_t tc_dn_partial_floats(const PoolDev& p, int npad_max);   // Scratch::dn_partial
 int tc_ffn_sync_ints(const PoolDev& p);                         // Scratch::ffn_sync
+int tc_dsync_ints();                                          // Scratch::dsync
 int launch_tc_gather(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, const void* x, void* out,
                      cudaStream_t s);
 int launch_tc_fused_decode(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, const void* x, void* out,
