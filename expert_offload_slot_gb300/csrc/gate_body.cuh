@@ -103,4 +103,90 @@ __device__ __forceinline__ void gate_one_token(const float* __restrict__ z, int 
   __syncwarp();
 }
 
+// Gate and top-k of token t by a whole CTA of NT >= E threads, thread e holding
+// expert e (the decode layer kernel: a token's last routing CTA has all its
+// threads free, and one warp's serial arg-max rounds are the long pole).  Same
+// results as gate_one_token: softmax (or sigmoid) probabilities of every expert,
+// the k largest logits in descending order with ties to the lower expert id
+// (expert e is the r-th largest for r = #{e' : z[e'] > z[e] or (z[e'] == z[e]
+// and e' < e)}; NaN ranks as -inf), the gap to the best unselected logit, and
+// the renormalised weights of the selected.
+struct GateCtaScratch {
+  float zs[kMaxPerLane * 32 + 4];   // logits as ranked
+  float zsel[36];                   // selected logits by rank, then the best unselected
+  float red[32];                    // per-warp partials
+  float bcast;
+};
+
+template <int NT>
+__device__ __forceinline__ void gate_token_cta(const float* __restrict__ z, int t, int E, int k, int gating,
+                                               int32_t* ids, float* w, float* probs, float* gap,
+                                               unsigned long long* stats, GateCtaScratch& gs) {
+  static_assert(NT >= kMaxPerLane * 32, "one thread per expert");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int NW = NT / 32;
+  const int E4 = (E + 3) & ~3;
+  const float v = tid < E ? __ldcg(z + (size_t)t * E + tid) : -INFINITY;
+  if (tid < E4) gs.zs[tid] = tid < E && !isnan(v) ? v : -INFINITY;   // padding never outranks: index >= E
+  // max of the logits (NaN ignored)
+  float m = warp_max(v);
+  if (lane == 0) gs.red[warp] = m;
+  __syncthreads();
+  if (tid == 0) {
+    float mm = gs.red[0];
+    for (int i = 1; i < NW; ++i) mm = fmaxf(mm, gs.red[i]);
+    gs.bcast = mm;
+  }
+  __syncthreads();
+  const float zmax = gs.bcast;
+  // per-expert probability for the routing history
+  float ex = 0.f;
+  if (gating == MOE_GATE_SOFTMAX_RENORM) {
+    ex = tid < E ? expf(v - zmax) : 0.f;
+    const float part = warp_sum(ex);
+    __syncthreads();   // every thread has read bcast
+    if (lane == 0) gs.red[warp] = part;
+    __syncthreads();
+    if (tid == 0) {
+      float den = 0.f;
+      for (int i = 0; i < NW; ++i) den += gs.red[i];
+      gs.bcast = den;
+    }
+    __syncthreads();
+    if (tid < E) probs[(size_t)t * E + tid] = ex / gs.bcast;
+  } else if (tid < E) {
+    probs[(size_t)t * E + tid] = 1.f / (1.f + expf(-v));
+  }
+  // rank of expert tid
+  if (tid < E) {
+    const float u = gs.zs[tid];
+    int rank = 0;
+    for (int e0 = 0; e0 < E4; e0 += 4) {
+      const float4 q = *reinterpret_cast<const float4*>(gs.zs + e0);
+      rank += (q.x > u || (q.x == u && e0 < tid)) ? 1 : 0;
+      rank += (q.y > u || (q.y == u && e0 + 1 < tid)) ? 1 : 0;
+      rank += (q.z > u || (q.z == u && e0 + 2 < tid)) ? 1 : 0;
+      rank += (q.w > u || (q.w == u && e0 + 3 < tid)) ? 1 : 0;
+    }
+    if (rank <= k) gs.zsel[rank] = u;
+    if (rank < k) ids[(size_t)t * k + rank] = tid;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const float zk = gs.zsel[k - 1];
+    const float g = k < E ? zk - gs.zsel[k] : INFINITY;
+    if (lane == 0) {
+      gap[t] = g;
+      if (g < 1e-4f) atomicAdd(&stats[ST_NEAR_TIES], 1ull);
+    }
+    float num = 0.f;
+    if (lane < k) {
+      const float zj = gs.zsel[lane];
+      num = gating == MOE_GATE_SOFTMAX_RENORM ? expf(zj - zmax) : 1.f / (1.f + expf(-zj));
+    }
+    const float den = warp_sum(num);
+    if (lane < k) w[(size_t)t * k + lane] = num / den;
+  }
+}
+
 }  // namespace moeslot

@@ -1495,7 +1495,6 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
                        FusedArgs f, DecodeArgs d) {
   constexpr int NT = FusedShape<WF>::threads;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ float zsel[NT / 32][32];
   __shared__ volatile int flag_sh;
   __shared__ LocalPlan lp_sh;
   __shared__ int lut_snap[kMaxE];
@@ -1567,21 +1566,21 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
       acc = warp_sum(acc);
       if (lane == 0) d.z[(size_t)t * E + e] = acc + d.rb[e];
     }
-    __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
-      const uint32_t old = atomicAdd(ticket(t), 1u);
+      // one acquire-release add: it releases this CTA's logits (ordered before it by the
+      // barrier), and the token's last CTA acquires every other CTA's
+      const uint32_t old = atom_add_acq_rel(ticket(t), 1u);
       flag_sh = old == (uint32_t)d.nblk - 1;
       if (flag_sh) *ticket(t) = 0u;
     }
     __syncthreads();
-    if (flag_sh && warp == 0) {
-      __threadfence();
-      gate_one_token(d.z, t, E, d.plan.p.k, d.plan.p.gating, d.plan.sc.ids, d.plan.sc.w, d.plan.sc.probs,
-                     d.plan.sc.gap, d.plan.p.stats, zsel[0]);
-      __threadfence();
-      __syncwarp();
-      if (lane == 0) release_add(route_done);
+    if (flag_sh) {
+      // the token's gate by the whole CTA; scratch: the dynamic shared memory x was staged in
+      gate_token_cta<NT>(d.z, t, E, d.plan.p.k, d.plan.p.gating, d.plan.sc.ids, d.plan.sc.w, d.plan.sc.probs,
+                         d.plan.sc.gap, d.plan.p.stats, *reinterpret_cast<GateCtaScratch*>(dsm));
+      __syncthreads();
+      if (threadIdx.x == 0) release_add(route_done);
     }
     __syncthreads();
   }
