@@ -657,7 +657,8 @@ tc_gather_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constan
 // Partial tiles are row-major ([128 rows][columns]) so that each epilogue
 // thread (one row) moves its columns with 16-byte accesses.
 constexpr int kCopyWarps = 2;
-constexpr int kCopyCtas = 32;   // copy-only CTAs of a decode layer call with misses (local lists)
+constexpr int kCopyCtas = 32;   // CTAs that copy first in a decode layer call with misses (local lists)
+constexpr int kUnitQ = 32;      // a CTA's queue of units handed out (it is at most stages + TMEM buffers ahead)
 constexpr int kCopyUnroll = 8;   // 16-byte host reads in flight per copy lane
 constexpr int kFusedBufs = 8;
 template <int WF> struct FusedShape {
@@ -682,7 +683,7 @@ struct LocalPlan {
 
 struct FusedArgs {
   const LocalPlan* lp;          // null: the plan's work lists in global memory
-  int cta0_plans;               // CTA 0 runs the plan and takes no expert units
+  int cta0_plans;               // CTA 0 runs the plan first (copying CTAs are counted after it)
   // with lp: a miss j (j-th copied entry) is copied from the host pool into landing
   // record rid_land0 + j at once, read from there, and written to its slot once the
   // plan has chosen it (slots_ready: the table holds this step's slots)
@@ -710,6 +711,8 @@ struct FusedArgs {
   uint32_t* hready;             // [E1] finished gate/up tiles per entry           } every launch
   uint32_t* jdone;              // [E1] CTAs done with each copy job's first part  }
   uint32_t* jdone_w2;           // [E1] ... and with the whole record              }
+  uint32_t* next_unit;          // the next resident entries' unit to hand out     }
+  uint32_t* next_miss;          // the next copied entries' unit to hand out       }
 };
 
 struct FSched {
@@ -759,22 +762,28 @@ struct FUnit {
 
 __device__ __forceinline__ FUnit fused_unit(const FSched& s, const FusedArgs& f, int g) {
   FUnit r;
-  int loc = g;
-  if (loc < s.p0) {
-    r.gu = 1, r.miss = 0;
-  } else if ((loc -= s.p0) < s.p1) {
-    r.gu = 0, r.miss = 0;
-  } else if ((loc -= s.p1) < s.p2) {
-    r.gu = 1, r.miss = 1;
+  int loc = g, rem;
+  if (loc < s.p0 + s.p1) {
+    // resident entries: all gate/up units, then all down units, each entry-major (an
+    // entry's h completes early, and its down units come soon after)
+    r.miss = 0;
+    r.gu = loc < s.p0;
+    if (!r.gu) loc -= s.p0;
+    const int per = r.gu ? s.mt_i * s.sg : s.mt_h * s.sd;
+    r.li = loc / per;
+    rem = loc - r.li * per;
   } else {
-    loc -= s.p2;
-    r.gu = 0, r.miss = 1;
+    // copied entries, job by job: its gate/up units, then its down units (the order in
+    // which the two parts of its record land)
+    loc -= s.p0 + s.p1;
+    const int gu_per = s.mt_i * s.sg, job_per = gu_per + s.mt_h * s.sd;
+    r.miss = 1;
+    r.li = loc / job_per;
+    rem = loc - r.li * job_per;
+    r.gu = rem < gu_per;
+    if (!r.gu) rem -= gu_per;
   }
-  // entry-major: an entry's h completes early, and its down units come soon after
   const int spn = r.gu ? s.sg : s.sd, kbn = r.gu ? s.kb_h : s.kb_i;
-  const int per = (r.gu ? s.mt_i : s.mt_h) * spn;
-  r.li = loc / per;
-  const int rem = loc - r.li * per;
   r.mt = rem / spn;
   r.sp = rem - r.mt * spn;
   r.kb0 = r.sp * kbn / spn;
@@ -844,6 +853,9 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
   __shared__ volatile int abort_sh, last_sh;
   __shared__ FSched sched_sh;
   __shared__ float wloc_sh[32];                                              // routing weights of one entry (local lists)
+  __shared__ int unit_q[kUnitQ];                                             // this CTA's units, in the order taken
+  __shared__ volatile int unit_n;                                            // entries of unit_q published
+  __shared__ volatile int epi_unit_sh[2], conv_unit_sh[2];                   // a unit handed to the epilogue / converter warps
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -880,15 +892,15 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
   __syncthreads();
   fence_after();
   const bool go = pre();
-  // Local lists and a step with misses: CTAs cta0_plans .. + kCopyCtas - 1 copy the misses
-  // with all their threads and take no expert units, so that the expert CTAs' stores and
-  // fences never queue behind host reads.  Otherwise the copy warps of every CTA copy.
+  // Local lists and a step with misses: CTAs cta0_plans .. + kCopyCtas - 1 first copy the
+  // misses with all their threads, so that the other CTAs' stores and fences never queue
+  // behind host reads, and take expert units only afterwards.  Otherwise the copy warps of
+  // every CTA copy.
   const int ncopy = go && f.lp && f.lp->nm > 0 ? min(kCopyCtas, G - f.cta0_plans - 1) : 0;
-  const int Gc = G - f.cta0_plans - ncopy;                  // CTAs that take expert units
-  const int cta = (int)blockIdx.x - f.cta0_plans - ncopy;   // this CTA's index among them (< 0: none)
-  const bool copy_cta = ncopy > 0 && (int)blockIdx.x >= f.cta0_plans && cta < 0;
+  const bool copy_cta = ncopy > 0 && (int)blockIdx.x >= f.cta0_plans && (int)blockIdx.x < f.cta0_plans + ncopy;
   const uint32_t njd = ncopy > 0 ? (uint32_t)ncopy : (uint32_t)(G - f.cta0_plans);   // CTAs releasing each job
   if (threadIdx.x == 0) {
+    unit_n = 0;
     if (go) {
       sched_sh = fused_sched(a, f, G);   // the unit decomposition, identical in every role and CTA
     } else {
@@ -899,6 +911,32 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
   __syncthreads();
   const uint32_t tmem = tmem_base_sh;
   const uint32_t idesc = idesc_bf16(N);
+
+  // Units are handed out at run time: the producer takes the next unit of the step's
+  // schedule from a grid-wide counter whenever it moves on, so CTAs that finish early
+  // (or join late: the planner, the copy CTAs) take more; the CTA's other roles read
+  // the units it took, in order, from unit_q (-1 ends the list).  The producer is at
+  // most stages + TMEM buffers units ahead of the epilogue, well inside kUnitQ.
+  auto publish_unit = [&](int k, int g) {
+    unit_q[k % kUnitQ] = g;
+    __threadfence_block();
+    unit_n = k + 1;
+  };
+  auto unit_at = [&](int k) -> int {   // bounded wait (~1 s); -1 also after a timeout
+    if (unit_n <= k) {
+      const uint64_t t0 = global_ns();
+      while (unit_n <= k) {
+        if (abort_sh || global_ns() - t0 > 1000000000ull) {
+          set_status(a.status, MOE_ERR_TIMEOUT);
+          abort_sh = 1;
+          return -1;
+        }
+        __nanosleep(32);
+      }
+    }
+    __threadfence_block();
+    return unit_q[k % kUnitQ];
+  };
 
   // Record copies, job by job and part by part (first the gate/up part, which releases
   // jdone[j], then the rest, which releases jdone_w2[j]; both count the copying CTAs):
@@ -1016,17 +1054,47 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
     }
   };
 
-  if (copy_cta) {
-    copy_jobs(blockDim.x, threadIdx.x, (uint32_t)((int)blockIdx.x - f.cta0_plans), (uint32_t)ncopy);
-  } else if (warp == 0) {
+  if (copy_cta) copy_jobs(blockDim.x, threadIdx.x, (uint32_t)((int)blockIdx.x - f.cta0_plans), (uint32_t)ncopy);
+  if (warp == 0) {
     // ------------------------------------------------------------- producer
     if (lane == 0) {
       const FSched sc = sched_sh;
       uint32_t it = 0;
       bool ok = true;
       int pend_s[kMaxStages], pend_kb[kMaxStages], pend_nk[kMaxStages];
-      for (int g = cta; cta >= 0 && g < sc.total && ok; g += Gc) {
-        const FUnit r = fused_unit(sc, f, g);
+      int npub = 0;   // units published; the list ends with -1 right after them, never over one
+      // Two queues: the resident entries' units (next_unit, one taken ahead) and the copied
+      // entries' units, job by job (next_miss).  A copied entry's unit whose part of the
+      // record has landed goes first, so the copies' tail is spread over every CTA that is
+      // between units then; once the resident units are gone, the copied ones in any case.
+      constexpr uint32_t kNone = 0xffffffffu;
+      const uint32_t nhit = (uint32_t)(sc.p0 + sc.p1), nmu = (uint32_t)sc.total - nhit;
+      const int gu_per = sc.mt_i * sc.sg, job_per = gu_per + sc.mt_h * sc.sd;
+      uint32_t hn = go ? atomicAdd(f.next_unit, 1u) : kNone;
+      for (;;) {
+        if (!ok || abort_sh || !go) break;
+        uint32_t g = kNone;
+        if (nmu > 0) {
+          const uint32_t m = *reinterpret_cast<volatile uint32_t*>(f.next_miss);
+          bool take = m < nmu && hn >= nhit;
+          if (m < nmu && !take) {
+            const int j = (int)m / job_per;
+            const uint32_t* part = (int)m - j * job_per < gu_per ? &f.jdone[j] : &f.jdone_w2[j];
+            take = *reinterpret_cast<const volatile uint32_t*>(part) >= njd;
+          }
+          if (take) {
+            const uint32_t got = atomicAdd(f.next_miss, 1u);
+            if (got < nmu) g = nhit + got;
+          }
+        }
+        if (g == kNone && hn < nhit) {
+          g = hn;
+          hn = atomicAdd(f.next_unit, 1u);   // the next one, while this one's loads go out
+        }
+        if (g == kNone) break;
+        publish_unit(npub, (int)g);
+        ++npub;
+        const FUnit r = fused_unit(sc, f, (int)g);
         int rid = 0;
         if (!r.miss) rid = f.lp ? f.lp->rid[r.u] : a.work[r.u].rid;
         if (r.miss) {
@@ -1093,6 +1161,7 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
         }
         if (ok && npend > 0 && !resolve()) ok = false;
       }
+      publish_unit(npub, -1);
       if (!ok) {
         set_status(a.status, MOE_ERR_TIMEOUT);
         abort_sh = 1;
@@ -1113,7 +1182,9 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
       uint32_t it = 0;
       int local = 0;
       bool ok = true;
-      for (int g = cta; cta >= 0 && g < sc.total && ok; g += Gc, ++local) {
+      for (;; ++local) {
+        const int g = unit_at(local);
+        if (g < 0 || !ok) break;
         const FUnit r = fused_unit(sc, f, g);
         const int buf = local % nbuf, use = local / nbuf;
         if (use > 0 && !mbar_wait(&tempty_bar[buf], (use - 1) & 1)) { ok = false; break; }
@@ -1169,7 +1240,13 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
     const uint32_t trow0 = tmem + ((uint32_t)(q * 32) << 16);
     const int cols = sc.cols;
     int local = 0;
-    for (int g = cta; cta >= 0 && g < sc.total; g += Gc, ++local) {
+    for (;; ++local) {
+      // one thread waits for the unit; the barrier hands it to all four warps, so they
+      // always run the same units (two slots: a slot is rewritten only after the next barrier)
+      if (threadIdx.x == 64) epi_unit_sh[local & 1] = unit_at(local);
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      const int g = epi_unit_sh[local & 1];
+      if (g < 0) break;
       const FUnit r = fused_unit(sc, f, g);
       const int buf = local % nbuf;
       const uint32_t trow = trow0 + (uint32_t)buf * acc_cols;
@@ -1336,7 +1413,11 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
     uint32_t it = 0;
     int local = 0;
     bool stop = false;
-    for (int g = cta; cta >= 0 && g < sc.total; g += Gc, ++local) {
+    for (;; ++local) {
+      if (ct == 0) conv_unit_sh[local & 1] = unit_at(local);   // handed to all four converter warps
+      asm volatile("bar.sync 3, %0;" ::"n"(32 * kConvWarps) : "memory");
+      const int g = conv_unit_sh[local & 1];
+      if (g < 0) break;
       const FUnit r = fused_unit(sc, f, g);
       const float* scl = nullptr;
       const int b0 = r.kb0 / 2, nblk = (r.kb1 - 1) / 2 - b0 + 1;   // 128-wide scale blocks the unit spans (<= 64)
@@ -1608,7 +1689,7 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
       if (blockIdx.x == 0) cp_async_wait_all();   // the prestaged copies land before this CTA moves on
       return false;
     }
-    __threadfence();
+    // (thread 0's acquire of route_done and the barrier order every thread's reads of the routing)
     if (d.local) {
       // the step's entry lists, as the plan orders them: experts with tokens ascending,
       // then the shared expert; resident / copied by the table row at the step's start
@@ -1981,12 +2062,15 @@ static uint32_t tile16(const PoolDev& p) {
 }
 
 // [gu_cnt: (E+1) * MT_I, padded to a 128-byte line][dn_done: a line of its own][hready: E+1]
-// [jdone: E+1][jdone_w2: E+1]
+// [jdone: E+1][jdone_w2: E+1, padded][next_unit: a line][next_miss: a line]
 static int dn_done_index(const PoolDev& p) {
   const int mt_i = (p.I + 127) / 128;
   return ((p.E + 1) * mt_i + tc::kSyncLine - 1) / tc::kSyncLine * tc::kSyncLine;
 }
-int tc_ffn_sync_ints(const PoolDev& p) { return dn_done_index(p) + tc::kSyncLine + 3 * (p.E + 1); }
+static int next_unit_index(const PoolDev& p) {
+  return (dn_done_index(p) + tc::kSyncLine + 3 * (p.E + 1) + tc::kSyncLine - 1) / tc::kSyncLine * tc::kSyncLine;
+}
+int tc_ffn_sync_ints(const PoolDev& p) { return next_unit_index(p) + 2 * tc::kSyncLine; }
 
 // decode layer kernel counters: a line for each of kDsTicket named ones and for every token's ticket
 int tc_dsync_ints() { return (tc::kDsTicket + tc::kDecodeMaxT) * tc::kSyncLine; }
@@ -2093,6 +2177,8 @@ static bool fused_setup(const PoolDev& p, const Scratch& sc, int T, const void* 
   f.hready = f.dn_done + tc::kSyncLine;
   f.jdone = f.hready + (p.E + 1);
   f.jdone_w2 = f.jdone + (p.E + 1);
+  f.next_unit = reinterpret_cast<uint32_t*>(sc.ffn_sync + next_unit_index(p));
+  f.next_miss = f.next_unit + tc::kSyncLine;
   *ap = a;
   *fp = f;
   return true;
