@@ -4,7 +4,8 @@
 Workload (default): the Qwen3-30B-A3B-shaped decode — 48 MoE layers, hidden
 2048, 128 experts, top-8, intermediate 768, bf16 weights and activations, a
 shared slot pool of round(0.45 * 48 * 128) = 2765 slots, Zipf(s=1.0) router
-bias, AR(1) (rho = 0.8) drift of the hidden states, MoE-CORE eviction score.
+bias, AR(1) (rho = 0.8) drift of the hidden states, Minus-Recent-Score eviction
+(HybriMoE; on this trace it misses less often than the MoE-CORE score or LRU).
 Weights are random (seeded), never a checkpoint.
 
 One "step" is one decode step of T tokens through all 48 layers: every stage
@@ -335,7 +336,7 @@ class PoolBench:
 
     def prefill(self, T, W, K, prof_steps=1):
         """Staged prefill of T tokens through all L layers (two swapped layer-sized staging regions,
-        layer l+2 copied while l+1 computes), eager launches: W warm-up and K timed steps."""
+        layer l+1 copied while l computes), eager launches: W warm-up and K timed steps."""
         import torch
         wl, moe = self.wl, self.moe
         x = __import__("synth").gen.torch_prefill_hidden(wl, T, self.device)
@@ -543,7 +544,7 @@ def run_configs(names, dev, qwen_host, args, peaks, link_gbs):
                 r = b.prefill(T, 3, 3)
                 pre[str(T)] = prefill_summary(wl, r, distinct_experts_last_call(b, T), hbm, tc, link_gbs)
             b.close()
-            lbl = {"dsv3": "deepseek-v3-shaped (fp8 e4m3, 128x128 block scales, shared expert)",
+            lbl = {"dsv3": "deepseek-v3-shaped (fp8 e4m3, 128x128 block scales, shared expert, MRS eviction)",
                    "mixtral": "mixtral-8x7b-shaped (64 slots, MRS eviction)"}[name]
             out[name] = {"workload": lbl, "layers": wl.L, "slots": wl.S, "decode": dec, "prefill": pre}
         out[name]["seconds"] = time.time() - t0

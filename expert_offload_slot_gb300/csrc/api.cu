@@ -10,8 +10,7 @@
 //
 // Staged prefill (MoE-CORE "Mechanism"): two staging regions, each one whole
 // MoE layer; layer l reads region l mod 2; while it computes, the other region
-// holds (or receives) layer l+1, and the region l releases is refilled with
-// layer l+2 on the pool's copy stream.
+// receives layer l+1 on the pool's copy stream (once layer l-1 has released it).
 #include <cstdarg>
 #include <cstdio>
 #include <algorithm>
@@ -76,6 +75,7 @@ struct moe_pool {
   cudaEvent_t ready[2] = {nullptr, nullptr};
   cudaEvent_t released[2] = {nullptr, nullptr};
   int staged_layer[2] = {-1, -1};
+  int ready_pending = -1;             // region whose copy is the last on copy_stream, ready not yet recorded
   uint64_t staged_count = 0;
   uint64_t launches = 0;
   std::vector<void*> allocs;
@@ -456,12 +456,29 @@ MOE_API moe_status moe_load_slot(moe_pool* P, int32_t layer, int32_t expert, int
   return MOE_OK;
 }
 
+// Staging (MoE-CORE's two prefill regions): a layer's records are copied into a
+// region on the pool's copy stream once the layer that used the region last has
+// released it.  The copy's `ready` event is recorded only when its layer is about
+// to run (mark_ready), not right after the copy is issued: where the copy stream
+// and the caller's stream share one hardware work queue, a record issued right
+// after a long copy holds back everything the caller enqueues behind it (the next
+// layer's kernels) until that copy ends, which serialises copies and compute.  The
+// record still comes right after its copy in the copy stream's order, because a
+// pending record is made before any later copy is issued.
+static void mark_ready(moe_pool* P, int r) {
+  if (P->ready_pending == r) {
+    cudaEventRecord(P->ready[r], P->copy_stream);
+    P->ready_pending = -1;
+  }
+}
+
 static void stage_layer(moe_pool* P, int layer, int r) {
   const size_t bytes = (size_t)P->d.E * P->d.lay.rec;
+  if (P->ready_pending >= 0) mark_ready(P, P->ready_pending);
   cudaStreamWaitEvent(P->copy_stream, P->released[r], 0);
   cudaMemcpyAsync(P->d.staging + (size_t)r * bytes, P->host_pool + (size_t)layer * bytes, bytes,
                   cudaMemcpyHostToDevice, P->copy_stream);
-  cudaEventRecord(P->ready[r], P->copy_stream);
+  P->ready_pending = r;
   P->staged_layer[r] = layer;
   P->staged_count += 1;
 }
@@ -475,8 +492,12 @@ static moe_status run_layer(moe_pool* P, int layer, const void* x, int T, void* 
   const float* probs = probs_in ? probs_in : sc.probs;
   int region = 0;
   if (staged) {
+    // this layer's region (copied during the previous layer's call, else now), then the next
+    // layer's copy into the other region, issued before this layer's kernels so that it runs
+    // beside them
     region = layer % 2;
     if (P->staged_layer[region] != layer) stage_layer(P, layer, region);
+    mark_ready(P, region);
     if (layer + 1 < d.L && P->staged_layer[1 - region] != layer + 1) stage_layer(P, layer + 1, 1 - region);
     CUDA_TRY(cudaStreamWaitEvent(s, P->ready[region], 0));
   }
@@ -552,7 +573,6 @@ static moe_status run_layer(moe_pool* P, int layer, const void* x, int T, void* 
   mark(4);
   if (staged) {
     CUDA_TRY(cudaEventRecord(P->released[region], s));
-    if (layer + 2 < d.L) stage_layer(P, layer + 2, region);
   }
   CUDA_TRY(cudaGetLastError());
   if (ids_in) {

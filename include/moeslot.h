@@ -162,9 +162,10 @@ MOE_API moe_status moe_load_slot(moe_pool* pool, int32_t layer, int32_t expert, 
  *         MOE_MODE_AUTO: staged when staging_regions == 2 and
  *         T >= floor(K_l / k), K_l being the slots layer l holds now
  *         (MoE-CORE "Mechanism"), else the slot pool path.
- * A staged call stages layer l (if not already there) and queues layer l+2
- * into the region it releases; it synchronises the host with nothing but may
- * make `stream` wait for the pool's internal copy stream. */
+ * A staged call stages layer l (if not already there), then queues layer l+1
+ * into the other region (after layer l-1 has released it) ahead of layer l's
+ * kernels, so that the copy runs beside them; it synchronises the host with
+ * nothing but makes `stream` wait for the pool's internal copy stream. */
 MOE_API moe_status moe_forward(moe_pool* pool, int32_t layer, const void* x, int32_t T, void* out,
                                int32_t mode, void* stream);
 

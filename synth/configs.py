@@ -96,7 +96,7 @@ WORKLOADS = {
         decode_T=(4,), decode_steps=8, notes="1 layer, 4 slots holding a seeded random 4 experts"),
     "qwen3_decode": Workload(
         name="qwen3_decode", L=48, E=128, k=8, H=2048, I=768, weight_dtype=BF16, act_dtype=BF16,
-        gating=GATE_SOFTMAX_RENORM, residency=0.45, zipf_s=1.0,
+        gating=GATE_SOFTMAX_RENORM, residency=0.45, zipf_s=1.0, evict=EVICT_MRS,
         decode_T=(1, 4, 16), decode_steps=256),
     "qwen3_prefill": Workload(
         name="qwen3_prefill", L=48, E=128, k=8, H=2048, I=768, weight_dtype=BF16, act_dtype=BF16,
@@ -104,7 +104,7 @@ WORKLOADS = {
         prefill_zipf_s=0.0, notes="router bias 0 so that all 128 experts receive tokens"),
     "dsv3": Workload(
         name="dsv3", L=4, E=256, k=8, H=7168, I=2048, weight_dtype=FP8_E4M3_B128, act_dtype=BF16,
-        gating=GATE_SIGMOID_RENORM, residency=0.40, zipf_s=1.2, shared=True,
+        gating=GATE_SIGMOID_RENORM, residency=0.40, zipf_s=1.2, shared=True, evict=EVICT_MRS,
         decode_T=(1, 8, 32), decode_steps=64, prefill_T=(1024,), prefill_zipf_s=1.2),
     "mixtral": Workload(
         name="mixtral", L=32, E=8, k=2, H=4096, I=14336, weight_dtype=BF16, act_dtype=BF16,
