@@ -642,18 +642,16 @@ tc_gather_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constan
 // meanwhile this step's misses are pulled from the mapped host pool (NVLink-C2C
 // reads) into their records, one job after another: by kCopyCtas copy-only CTAs
 // with all their threads in the decode layer kernel, else by two copy warps in
-// every CTA.  A
-// unit waits only for what it reads: a copied record (jdone[job] == G: every
-// CTA's slice of that job is written) or the complete h of its entry.  (Finer
-// readiness within a job costs the copy warps a fence per part, which slows the
-// link-bound copy more than it shortens the tail.)
+// every CTA.  A unit waits only for what it reads: the part of a copied record
+// it reads (jdone[job] for the gate/up tiles, jdone_w2[job] for the rest: every
+// copying CTA has released its slice), or the complete h of its entry
 // (hready[u] == the entry's gate/up tiles).  So the resident experts' whole FFN
 // overlaps the link-bound copies.
-// A down unit covers one entry: it writes an fp32 partial tile, and the last
-// unit to finish a 128-row output tile sums the partials of every entry in
-// entry order (ascending expert id, shared expert last).  The order is fixed,
-// and the split counts depend on the entry count alone, so the output does not
-// depend on which experts happened to be resident.
+// A down unit covers one entry and writes an fp32 partial tile; once every
+// CTA's partials are written, all CTAs sum them element-parallel in entry order
+// (ascending expert id, shared expert last).  The order is fixed, and the split
+// counts depend on the entry count alone, so the output does not depend on
+// which experts happened to be resident.
 // Partial tiles are row-major ([128 rows][columns]) so that each epilogue
 // thread (one row) moves its columns with 16-byte accesses.
 constexpr int kCopyWarps = 2;
@@ -1070,7 +1068,12 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
       constexpr uint32_t kNone = 0xffffffffu;
       const uint32_t nhit = (uint32_t)(sc.p0 + sc.p1), nmu = (uint32_t)sc.total - nhit;
       const int gu_per = sc.mt_i * sc.sg, job_per = gu_per + sc.mt_h * sc.sd;
-      uint32_t hn = go ? atomicAdd(f.next_unit, 1u) : kNone;
+      // A CTA that starts on expert work at once (not the planner, not a copy CTA) takes
+      // its first resident unit by its own index, without a round trip to the grid's
+      // counter; the counter hands out the units after those.
+      const int first = (int)blockIdx.x - f.cta0_plans - ncopy;
+      const uint32_t nfirst = (uint32_t)(G - f.cta0_plans - ncopy);
+      uint32_t hn = !go ? kNone : first >= 0 ? (uint32_t)first : nfirst + atomicAdd(f.next_unit, 1u);
       for (;;) {
         if (!ok || abort_sh || !go) break;
         uint32_t g = kNone;
@@ -1089,7 +1092,7 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
         }
         if (g == kNone && hn < nhit) {
           g = hn;
-          hn = atomicAdd(f.next_unit, 1u);   // the next one, while this one's loads go out
+          hn = nfirst + atomicAdd(f.next_unit, 1u);   // the next one, while this one's loads go out
         }
         if (g == kNone) break;
         publish_unit(npub, (int)g);
@@ -1494,19 +1497,21 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
       const uint32_t m = mt * BM + rw;
       if (t >= (uint32_t)a.T || m >= (uint32_t)a.H) continue;
       const float* base = f.dn_partial + (size_t)mt * sc.sd * tile_el + rem;
+      // part q = (entry u, split sp), q = u * sd + sp, at base + u * ustride + sp * tile_el.
+      // Each batch's addresses come straight from q (past the end: the last part again, never
+      // added), so its 16 loads are independent and all in flight at once.
       float acc = 0.f;
-      int u = 0, sp = 0;
-      for (int p0 = 0; p0 < parts; p0 += 32) {
-        float v[32];
+      const int sd = sc.sd;
+      for (int p0 = 0; p0 < parts; p0 += 16) {
+        float v[16];
 #pragma unroll
-        for (int b = 0; b < 32; ++b) {
-          if (p0 + b < parts) {
-            v[b] = __ldcg(base + (size_t)u * ustride + (size_t)sp * tile_el);
-            if (++sp == sc.sd) { sp = 0; ++u; }
-          }
+        for (int b = 0; b < 16; ++b) {
+          const int q = min(p0 + b, parts - 1);
+          const int u = sd == 1 ? q : q / sd;
+          v[b] = __ldcg(base + (size_t)u * ustride + (size_t)(q - u * sd) * tile_el);
         }
 #pragma unroll
-        for (int b = 0; b < 32; ++b)
+        for (int b = 0; b < 16; ++b)
           if (p0 + b < parts) acc += v[b];
       }
       a.out[(size_t)t * a.H + m] = f32_to_bf16_rn(acc);
@@ -1593,11 +1598,27 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
   const PoolDev& p = d.plan.p;
   const int l = d.plan.layer;
 
-  if (d.local) {
-    // this CTA's copy of the layer's table row, taken before the plan may change it
-    for (int e = threadIdx.x; e < E; e += NT) lut_snap[e] = p.lut[(size_t)l * E + e];
+  // this CTA's copy of the layer's table row, taken before the plan may change it: loaded
+  // now; a routing CTA stores and releases it after its logits, off the routing's path
+  constexpr int kSnapPer = (kMaxE + NT - 1) / NT;
+  int snap_v[kSnapPer];
+  const bool routing = blockIdx.x >= 1 && (int)blockIdx.x <= T * d.nblk;
+  auto take_snapshot = [&]() {
+#pragma unroll
+    for (int i = 0; i < kSnapPer; ++i) {
+      const int e = threadIdx.x + i * NT;
+      if (e < E) lut_snap[e] = snap_v[i];
+    }
     __syncthreads();
     if (threadIdx.x == 0) release_add(snap_done);
+  };
+  if (d.local) {
+#pragma unroll
+    for (int i = 0; i < kSnapPer; ++i) {
+      const int e = threadIdx.x + i * NT;
+      snap_v[i] = e < E ? p.lut[(size_t)l * E + e] : -1;
+    }
+    if (!routing) take_snapshot();
   }
   if (blockIdx.x == 0) {
     plan_prestage<NT>(d.plan, dsm);
@@ -1609,30 +1630,31 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
     if (threadIdx.x == 0) release_add(route_done);
   }
   // ---- route: logits of token t for one block of experts, then (last CTA) its gate
-  if (blockIdx.x >= 1 && (int)blockIdx.x <= T * d.nblk) {
+  if (routing) {
     const int rb = blockIdx.x - 1;
     const int t = rb / d.nblk, b = rb - t * d.nblk;
-    uint16_t* xs = reinterpret_cast<uint16_t*>(dsm);            // x[t] staged once, H bf16
-    for (int h = threadIdx.x * 8; h < H; h += NT * 8)
-      *reinterpret_cast<uint4*>(xs + h) = __ldg(reinterpret_cast<const uint4*>(d.x + (size_t)t * H + h));
-    __syncthreads();
+    const uint16_t* xrow = d.x + (size_t)t * H;   // read by every warp: L1 after the first
     const int e0 = b * d.eb, e1 = min(E, e0 + d.eb);
     for (int e = e0 + warp; e < e1; e += NT / 32) {
       const uint16_t* wrow = d.wr + (size_t)e * H;
       float acc = 0.f;
-      // the row's 16-byte chunks of this lane, kRouteChunks loads in flight at once
+      // the row's 16-byte chunks of this lane and the matching x chunks, kRouteChunks of
+      // each in flight at once
       for (int h0 = lane * 8; h0 < H; h0 += 32 * 8 * kRouteChunks) {
-        uint4 wq[kRouteChunks];
+        uint4 wq[kRouteChunks], xq[kRouteChunks];
 #pragma unroll
         for (int c = 0; c < kRouteChunks; ++c) {
           const int h = h0 + c * 32 * 8;
-          if (h < H) wq[c] = __ldg(reinterpret_cast<const uint4*>(wrow + h));
+          if (h < H) {
+            wq[c] = __ldg(reinterpret_cast<const uint4*>(wrow + h));
+            xq[c] = __ldg(reinterpret_cast<const uint4*>(xrow + h));
+          }
         }
 #pragma unroll
         for (int c = 0; c < kRouteChunks; ++c) {
           const int h = h0 + c * 32 * 8;
           if (h < H) {
-            const uint4 q = *reinterpret_cast<const uint4*>(xs + h);
+            const uint4 q = xq[c];
             acc = fmaf(bf16lo(wq[c].x), bf16lo(q.x), acc);
             acc = fmaf(bf16hi(wq[c].x), bf16hi(q.x), acc);
             acc = fmaf(bf16lo(wq[c].y), bf16lo(q.y), acc);
@@ -1664,6 +1686,7 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
       if (threadIdx.x == 0) release_add(route_done);
     }
     __syncthreads();
+    if (d.local) take_snapshot();
   }
 
   // ---- plan (CTA 0, once every token is gated) while the other CTAs set up;
