@@ -63,6 +63,10 @@ struct TcMaps {
   // and w2 [n_records][H][I] (row-major codes)
   bool fp8 = false;
   CUtensorMap w13{}, w2{};
+  // bf16 pools, streaming decode path: 16-row segments of the tiled records, as
+  // [n_records][mt][tile (kb, gate/up)][row][128 B] and [n_records][mt][kb][row][128 B]
+  bool stream = false;
+  CUtensorMap sw13{}, sw2{};
 };
 
 namespace tc {
@@ -118,6 +122,27 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
       "[%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// Tiled tensor loads of 4 and 5 dimensions (coordinates innermost first); the
+// 5-dimensional one carries the weights' evict-first L2 policy.
+__device__ __forceinline__ uint64_t l2_evict_first_policy();
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2,
+                                            int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], "
+      "[%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_5d_ef(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
+                                               int c2, int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, "
+      "%4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+      "l"(l2_evict_first_policy())
       : "memory");
 }
 
@@ -822,6 +847,124 @@ __device__ __noinline__ bool wait_count(const uint32_t* p, uint32_t target, cons
   }
 }
 
+// Record copies, job by job and part by part (first the gate/up part, which releases
+// jdone[j], then the rest, which releases jdone_w2[j]; both count the copying CTAs):
+// nthr threads of each of ncta CTAs copy; thread tid of copying CTA cidx takes the
+// 16-byte chunks wb + lane + u * stride (u < kCopyUnroll) of the lattice rows
+// wb = w0 + i * kCopyUnroll * stride, w0 = its warp's first chunk, that fall in the
+// part.  The loops run on wb, so all lanes of a warp take the same trip count (the
+// warp-wide shuffles below need that).
+__device__ __noinline__ void copy_records(const Args& a, const FusedArgs& f, uint32_t nthr, uint32_t tid,
+                                        uint32_t cidx, uint32_t ncta) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t stride = ncta * nthr;
+  const uint32_t step = stride * kCopyUnroll;
+  const uint32_t w0 = cidx * nthr + (tid & ~31u);
+  auto first_row = [&](uint32_t lo) { return lo <= w0 ? w0 : w0 + (lo - w0) / step * step; };
+  // slot record the plan gave expert e (null: none, the miss stays in its landing record)
+  auto slot_record = [&](int e) -> uint4* {
+    int slot = -1;
+    if (lane == 0) slot = __ldcg(f.lut_row + e);
+    slot = __shfl_sync(0xffffffffu, slot, 0);
+    return slot >= 0 && slot < f.S ? reinterpret_cast<uint4*>(const_cast<uint8_t*>(a.records) + (size_t)slot * a.rec)
+                                   : nullptr;
+  };
+  // chunks [lo, hi) of rows wb < wend: src -> dst
+  auto copy_range = [&](const uint4* src, uint4* dst, uint32_t lo, uint32_t hi, uint32_t wend) {
+    for (uint32_t wb = first_row(lo); wb < min(hi, wend); wb += step) {
+      const uint32_t base = wb + lane;
+      uint4 v[kCopyUnroll];
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u) {
+        const uint32_t idx = base + (uint32_t)u * stride;
+        if (idx >= lo && idx < hi) v[u] = __ldcs(src + idx);
+      }
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u) {
+        const uint32_t idx = base + (uint32_t)u * stride;
+        if (idx >= lo && idx < hi) __stcs(dst + idx, v[u]);
+      }
+    }
+  };
+  const uint32_t n = f.lp ? (uint32_t)f.lp->nm : (uint32_t)__ldcg(f.n_jobs);
+  // local lists: each miss lands in its landing record at once; from the moment the
+  // table is seen final (slots_ready), its chunks go to the chosen slot as well.
+  // (j_dual, p_dual, c_dual): the first job, part and row written to both; what came
+  // before is copied over at the end.
+  bool planned = !f.lp;
+  uint32_t j_dual = n, p_dual = 0, c_dual = 0;
+  for (uint32_t j = 0; j < n; ++j) {
+    const uint4* src;
+    uint4* dst;
+    uint4* dst2 = nullptr;
+    int e = -1;
+    if (f.lp) {
+      e = f.lp->expert[f.lp->elist[1][j]];
+      src = reinterpret_cast<const uint4*>(f.host_layer + (size_t)e * a.rec);
+      dst = reinterpret_cast<uint4*>(const_cast<uint8_t*>(a.records) + (size_t)(f.rid_land0 + (int)j) * a.rec);
+      if (planned) dst2 = slot_record(e);
+    } else {
+      src = reinterpret_cast<const uint4*>(f.jobs[j].src);
+      dst = reinterpret_cast<uint4*>(f.jobs[j].dst);
+    }
+    for (uint32_t part = 0; part < 2; ++part) {
+      const uint32_t lo = part ? f.part16 : 0u, hi = part ? f.tile16 : f.part16;
+      for (uint32_t wb = first_row(lo); wb < hi; wb += step) {
+        if (!planned) {
+          uint32_t pv = 0;
+          if (lane == 0) pv = ld_acquire(f.slots_ready);
+          planned = __shfl_sync(0xffffffffu, pv, 0) != 0u;
+          if (planned) {
+            dst2 = slot_record(e);
+            j_dual = j;
+            p_dual = part;
+            c_dual = wb;
+          }
+        }
+        const uint32_t base = wb + lane;
+        uint4 v[kCopyUnroll];
+#pragma unroll
+        for (int u = 0; u < kCopyUnroll; ++u) {
+          const uint32_t idx = base + (uint32_t)u * stride;
+          if (idx >= lo && idx < hi) v[u] = __ldcs(src + idx);
+        }
+#pragma unroll
+        for (int u = 0; u < kCopyUnroll; ++u) {
+          const uint32_t idx = base + (uint32_t)u * stride;
+          if (idx >= lo && idx < hi) {
+            __stcs(dst + idx, v[u]);
+            if (dst2) __stcs(dst2 + idx, v[u]);
+          }
+        }
+      }
+      __threadfence();
+      asm volatile("bar.sync 2, %0;" ::"r"(nthr) : "memory");
+      if (tid == 0) release_add(part ? &f.jdone_w2[j] : &f.jdone[j]);
+    }
+  }
+  if (f.lp && n > 0) {
+    // the chunks that landed before the table was seen final, into their slots: this
+    // thread re-reads only what it wrote
+    if (!planned) {
+      bool ok = true;
+      if (lane == 0) ok = wait_count(f.slots_ready, 1u, a.status);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) set_status(a.status, MOE_ERR_TIMEOUT);
+      planned = ok;
+    }
+    for (uint32_t j = 0; planned && j < n && j <= j_dual; ++j) {
+      uint4* dst = slot_record(f.lp->expert[f.lp->elist[1][j]]);
+      if (!dst) continue;
+      const uint4* src = reinterpret_cast<const uint4*>(a.records + (size_t)(f.rid_land0 + (int)j) * a.rec);
+      for (uint32_t part = 0; part < 2; ++part) {
+        const bool before = j < j_dual || part < p_dual;
+        if (!before && part > p_dual) break;
+        copy_range(src, dst, part ? f.part16 : 0u, part ? f.tile16 : f.part16, before ? f.tile16 : c_dual);
+      }
+    }
+  }
+}
+
 // 32 KB of weight tiles plus two activation tiles of N x 64 bf16 (1 KB aligned)
 __host__ __device__ constexpr uint32_t fused_stage_bytes(int N) {
   return (2 * kTileBytes + 2u * (uint32_t)N * BK * 2 + 1023u) & ~1023u;
@@ -936,123 +1079,7 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
     return unit_q[k % kUnitQ];
   };
 
-  // Record copies, job by job and part by part (first the gate/up part, which releases
-  // jdone[j], then the rest, which releases jdone_w2[j]; both count the copying CTAs):
-  // nthr threads of each of ncta CTAs copy; thread tid of copying CTA cidx takes the
-  // 16-byte chunks wb + lane + u * stride (u < kCopyUnroll) of the lattice rows
-  // wb = w0 + i * kCopyUnroll * stride, w0 = its warp's first chunk, that fall in the
-  // part.  The loops run on wb, so all lanes of a warp take the same trip count (the
-  // warp-wide shuffles below need that).
-  auto copy_jobs = [&](uint32_t nthr, uint32_t tid, uint32_t cidx, uint32_t ncta) {
-    const uint32_t stride = ncta * nthr;
-    const uint32_t step = stride * kCopyUnroll;
-    const uint32_t w0 = cidx * nthr + (tid & ~31u);
-    auto first_row = [&](uint32_t lo) { return lo <= w0 ? w0 : w0 + (lo - w0) / step * step; };
-    // slot record the plan gave expert e (null: none, the miss stays in its landing record)
-    auto slot_record = [&](int e) -> uint4* {
-      int slot = -1;
-      if (lane == 0) slot = __ldcg(f.lut_row + e);
-      slot = __shfl_sync(0xffffffffu, slot, 0);
-      return slot >= 0 && slot < f.S ? reinterpret_cast<uint4*>(const_cast<uint8_t*>(a.records) + (size_t)slot * a.rec)
-                                     : nullptr;
-    };
-    // chunks [lo, hi) of rows wb < wend: src -> dst
-    auto copy_range = [&](const uint4* src, uint4* dst, uint32_t lo, uint32_t hi, uint32_t wend) {
-      for (uint32_t wb = first_row(lo); wb < min(hi, wend); wb += step) {
-        const uint32_t base = wb + lane;
-        uint4 v[kCopyUnroll];
-#pragma unroll
-        for (int u = 0; u < kCopyUnroll; ++u) {
-          const uint32_t idx = base + (uint32_t)u * stride;
-          if (idx >= lo && idx < hi) v[u] = __ldcs(src + idx);
-        }
-#pragma unroll
-        for (int u = 0; u < kCopyUnroll; ++u) {
-          const uint32_t idx = base + (uint32_t)u * stride;
-          if (idx >= lo && idx < hi) __stcs(dst + idx, v[u]);
-        }
-      }
-    };
-    const uint32_t n = f.lp ? (uint32_t)f.lp->nm : (uint32_t)__ldcg(f.n_jobs);
-    // local lists: each miss lands in its landing record at once; from the moment the
-    // table is seen final (slots_ready), its chunks go to the chosen slot as well.
-    // (j_dual, p_dual, c_dual): the first job, part and row written to both; what came
-    // before is copied over at the end.
-    bool planned = !f.lp;
-    uint32_t j_dual = n, p_dual = 0, c_dual = 0;
-    for (uint32_t j = 0; j < n; ++j) {
-      const uint4* src;
-      uint4* dst;
-      uint4* dst2 = nullptr;
-      int e = -1;
-      if (f.lp) {
-        e = f.lp->expert[f.lp->elist[1][j]];
-        src = reinterpret_cast<const uint4*>(f.host_layer + (size_t)e * a.rec);
-        dst = reinterpret_cast<uint4*>(const_cast<uint8_t*>(a.records) + (size_t)(f.rid_land0 + (int)j) * a.rec);
-        if (planned) dst2 = slot_record(e);
-      } else {
-        src = reinterpret_cast<const uint4*>(f.jobs[j].src);
-        dst = reinterpret_cast<uint4*>(f.jobs[j].dst);
-      }
-      for (uint32_t part = 0; part < 2; ++part) {
-        const uint32_t lo = part ? f.part16 : 0u, hi = part ? f.tile16 : f.part16;
-        for (uint32_t wb = first_row(lo); wb < hi; wb += step) {
-          if (!planned) {
-            uint32_t pv = 0;
-            if (lane == 0) pv = ld_acquire(f.slots_ready);
-            planned = __shfl_sync(0xffffffffu, pv, 0) != 0u;
-            if (planned) {
-              dst2 = slot_record(e);
-              j_dual = j;
-              p_dual = part;
-              c_dual = wb;
-            }
-          }
-          const uint32_t base = wb + lane;
-          uint4 v[kCopyUnroll];
-#pragma unroll
-          for (int u = 0; u < kCopyUnroll; ++u) {
-            const uint32_t idx = base + (uint32_t)u * stride;
-            if (idx >= lo && idx < hi) v[u] = __ldcs(src + idx);
-          }
-#pragma unroll
-          for (int u = 0; u < kCopyUnroll; ++u) {
-            const uint32_t idx = base + (uint32_t)u * stride;
-            if (idx >= lo && idx < hi) {
-              __stcs(dst + idx, v[u]);
-              if (dst2) __stcs(dst2 + idx, v[u]);
-            }
-          }
-        }
-        __threadfence();
-        asm volatile("bar.sync 2, %0;" ::"r"(nthr) : "memory");
-        if (tid == 0) release_add(part ? &f.jdone_w2[j] : &f.jdone[j]);
-      }
-    }
-    if (f.lp && n > 0) {
-      // the chunks that landed before the table was seen final, into their slots: this
-      // thread re-reads only what it wrote
-      if (!planned) {
-        bool ok = true;
-        if (lane == 0) ok = wait_count(f.slots_ready, 1u, a.status);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) set_status(a.status, MOE_ERR_TIMEOUT);
-        planned = ok;
-      }
-      for (uint32_t j = 0; planned && j < n && j <= j_dual; ++j) {
-        uint4* dst = slot_record(f.lp->expert[f.lp->elist[1][j]]);
-        if (!dst) continue;
-        const uint4* src = reinterpret_cast<const uint4*>(a.records + (size_t)(f.rid_land0 + (int)j) * a.rec);
-        for (uint32_t part = 0; part < 2; ++part) {
-          const bool before = j < j_dual || part < p_dual;
-          if (!before && part > p_dual) break;
-          copy_range(src, dst, part ? f.part16 : 0u, part ? f.tile16 : f.part16, before ? f.tile16 : c_dual);
-        }
-      }
-    }
-  };
-
-  if (copy_cta) copy_jobs(blockDim.x, threadIdx.x, (uint32_t)((int)blockIdx.x - f.cta0_plans), (uint32_t)ncopy);
+  if (copy_cta) copy_records(a, f, blockDim.x, threadIdx.x, (uint32_t)((int)blockIdx.x - f.cta0_plans), (uint32_t)ncopy);
   if (warp == 0) {
     // ------------------------------------------------------------- producer
     if (lane == 0) {
@@ -1074,7 +1101,15 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
       const int first = (int)blockIdx.x - f.cta0_plans - ncopy;
       const uint32_t nfirst = (uint32_t)(G - f.cta0_plans - ncopy);
       uint32_t hn = !go ? kNone : first >= 0 ? (uint32_t)first : nfirst + atomicAdd(f.next_unit, 1u);
+      // The counter's answer for the next unit is read only when the next unit starts (after
+      // this one's loads went out), so its round trip never holds up a unit's first load.
+      uint32_t hraw = 0;
+      bool hpend = false;
       for (;;) {
+        if (hpend) {
+          hn = nfirst + hraw;
+          hpend = false;
+        }
         if (!ok || abort_sh || !go) break;
         uint32_t g = kNone;
         if (nmu > 0) {
@@ -1092,7 +1127,8 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
         }
         if (g == kNone && hn < nhit) {
           g = hn;
-          hn = nfirst + atomicAdd(f.next_unit, 1u);   // the next one, while this one's loads go out
+          hraw = atomicAdd(f.next_unit, 1u);   // the next one, while this one's loads go out
+          hpend = true;
         }
         if (g == kNone) break;
         publish_unit(npub, (int)g);
@@ -1464,7 +1500,7 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
     }
   } else if (!f.lp && go) {
     // ------------------------------------------------------------- copy warps
-    copy_jobs(32u * kCopyWarps, (uint32_t)(warp - Shape::copy_warp0) * 32u + lane, blockIdx.x, (uint32_t)G);
+    copy_records(a, f, 32u * kCopyWarps, (uint32_t)(warp - Shape::copy_warp0) * 32u + lane, blockIdx.x, (uint32_t)G);
   }
   fence_before();
   __syncthreads();
@@ -1515,6 +1551,450 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
           if (p0 + b < parts) acc += v[b];
       }
       a.out[(size_t)t * a.H + m] = f32_to_bf16_rn(acc);
+    }
+  }
+}
+
+// ----------------------------------------------------------------- streaming decode FFN (one token)
+// With one token, a layer call is one matrix-vector product per expert: each
+// weight streams from HBM once and feeds one multiply-add, which the CUDA cores
+// keep up with, so the tensor cores buy nothing.  What costs
+// time on the tensor-core path at these sizes is its structure: gate/up tiles
+// split along K (partials, arrivals and a reduction per tile before the down
+// projection may start) and a grid-wide combine of per-entry down partials.
+// This path has neither:
+//   phase 1: unit = (work entry u, 16 rows of a 128-row tile of I), all of K.  The
+//            unit's gate and up rows stream through a shared-memory ring (one
+//            bulk copy per 2 KB row segment of a swizzled 128 x 64 tile); each
+//            compute warp owns two rows of gate and of up and finishes
+//            h = w(u,t) SiLU(W_gate x_t) (W_up x_t) itself, in fp32, into global
+//            scratch (rows past I as 0).
+//   arrival: every CTA's phase-1 units are done (one grid-wide counter).
+//   phase 2: unit = 16 rows of H, every entry in work order (ascending expert id,
+//            shared expert last): each stage carries W_down row segments of one
+//            entry and the matching slice of its h; each compute warp owns two
+//            output rows and sums over entries and K in registers, and writes
+//            out directly: no partials, no combine.  A CTA issues the weight
+//            segments of its first phase-2 stages before the arrival (they need
+//            no h) and their h slices after it.
+// A stage is one tiled tensor load (phase 2: two, W_down and h): the 16-row segments of
+// 8 tiles, 32 KB, arrive in one request instead of sixteen 2 KB copies.
+// Misses are copied as on the tensor-core path (copy CTAs, landing records);
+// a copied entry's phase-1 units wait for its gate/up part and its phase-2
+// stages for the rest.  Every sum runs in one fixed order (each lane's partial in
+// stage and element order, then a butterfly over the lanes), and no unit's rows
+// depend on which experts are resident, so neither does the output.
+// Tokens the path takes.  The code is written for up to four, but measured on the
+// Qwen3-shaped layer it beats the tensor-core path only at one token (all experts
+// resident: 39.6 vs 43.2 us per call); at four it is slower (83 vs ~60 us): its
+// 16-row units read each tile as 2 KB pieces, whose loads wait far longer than
+// the tensor-core path's contiguous 32 KB stages.
+constexpr int kStreamMaxT = 1;
+constexpr int kStreamRows = 16;                  // rows per unit
+constexpr int kStreamKb = 8;                     // 64-column K blocks per stage
+constexpr int kStreamWarps = 8;                  // compute warps; warp kStreamWarps issues the copies
+constexpr int kStreamThreads = (kStreamWarps + 1) * 32;
+constexpr uint32_t kStreamSeg = kStreamRows * 128;            // one row segment of a tile: 2 KB
+constexpr uint32_t kStreamStage = 2 * kStreamKb * kStreamSeg; // 32 KB: gate and up segments of 8 K blocks
+constexpr uint32_t kStreamHOff = kStreamKb * kStreamSeg;      // phase 2: h slices after the W_down segments
+constexpr int kStreamQ = 64;
+constexpr int kStreamEnd1 = -2, kStreamEnd = -1, kStreamP2 = 1 << 30;
+
+// 8 bf16 weights (one 16-byte chunk) as floats
+__device__ __forceinline__ void unpack8_bf16(const uint4& w, float* f) {
+  f[0] = bf16lo(w.x); f[1] = bf16hi(w.x); f[2] = bf16lo(w.y); f[3] = bf16hi(w.y);
+  f[4] = bf16lo(w.z); f[5] = bf16hi(w.z); f[6] = bf16lo(w.w); f[7] = bf16hi(w.w);
+}
+
+// dot product of 8 weights with 8 activations, in element order
+__device__ __forceinline__ float dot8(const float* w, const float* v, float acc) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc = fmaf(w[i], v[i], acc);
+  return acc;
+}
+
+// 16 bytes from shared memory at a shared-window address (explicitly shared: the
+// ring's pointers come from aligned integer arithmetic, which generic loads would
+// route through the global path)
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ float butterfly_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// smem_raw: the CTA's dynamic shared memory; pre(): as for fused_ffn.  bf16 tiled
+// records, local lists (f.lp), T <= kStreamMaxT.
+// map_w13 / map_w2: the row-segment maps of the records (TcMaps::sw13 / sw2); map_h: h as
+// [work position][T][Ip / 64][64] fp32, boxes of 8 K blocks of every token.
+template <typename Pre>
+__device__ __forceinline__ void stream_ffn(const CUtensorMap* map_w13, const CUtensorMap* map_w2,
+                                           const CUtensorMap* map_h, const Args& a, const FusedArgs& f,
+                                           const uint16_t* __restrict__ x, uint8_t* smem_raw, Pre pre) {
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+  __shared__ int unit_q[kStreamQ];
+  __shared__ volatile int unit_n;
+  __shared__ volatile int abort_sh;
+  __shared__ int jpos_sh[kMaxE + 1];     // copied index of each work position, or -1
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x;
+  const int T = a.T, H = a.H, I = a.I;
+  const int S = a.stages;
+  const int kb_h = (H + 63) / 64, kb_i = (I + 63) / 64, mt_i = (I + 127) / 128, mt_h = (H + 127) / 128;
+  const int Hp = kb_h * 64, Ip = kb_i * 64;
+  const int rg_tile = 128 / kStreamRows;
+  float* xs = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = reinterpret_cast<uint8_t*>(xs) + (((size_t)T * Hp * 4 + 1023) & ~(size_t)1023);
+  float* hf = reinterpret_cast<float*>(a.hbuf);   // [work position][T][Ip] fp32
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], kStreamWarps);
+    }
+    unit_n = 0;
+    abort_sh = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const bool go = pre();
+  if (!go && threadIdx.x == 0) abort_sh = 1;
+  const LocalPlan* lp = f.lp;
+  const int n = go ? lp->n : 0, nh = go ? lp->nh : 0, nm = go ? lp->nm : 0;
+  const int ncopy = go && nm > 0 ? min(kCopyCtas, G - f.cta0_plans - 1) : 0;
+  const bool copy_cta = ncopy > 0 && (int)blockIdx.x >= f.cta0_plans && (int)blockIdx.x < f.cta0_plans + ncopy;
+  const uint32_t njd = (uint32_t)max(ncopy, 1);
+  if (go) {
+    for (int i = threadIdx.x; i <= kMaxE; i += blockDim.x) jpos_sh[i] = -1;
+    __syncthreads();
+    for (int j = threadIdx.x; j < nm; j += blockDim.x) jpos_sh[lp->elist[1][j]] = j;
+    __syncthreads();
+  }
+  if (copy_cta) copy_records(a, f, blockDim.x, threadIdx.x, (uint32_t)((int)blockIdx.x - f.cta0_plans), (uint32_t)ncopy);
+  const int per1 = mt_i * rg_tile;                  // phase-1 units per entry
+  const uint32_t n1 = (uint32_t)(n * per1);         // resident entries' units first, then copied
+  const uint32_t n2 = (uint32_t)(mt_h * rg_tile);   // phase-2 units
+  uint32_t* p1_done = f.dn_done;
+  auto publish = [&](int k, int g) {
+    unit_q[k % kStreamQ] = g;
+    __threadfence_block();
+    unit_n = k + 1;
+  };
+  auto unit_at = [&](int k) -> int {   // bounded wait; kStreamEnd after a timeout
+    if (unit_n <= k) {
+      const uint64_t t0 = global_ns();
+      while (unit_n <= k) {
+        if (abort_sh || global_ns() - t0 > 1000000000ull) {
+          set_status(a.status, MOE_ERR_TIMEOUT);
+          abort_sh = 1;
+          return kStreamEnd;
+        }
+        __nanosleep(32);
+      }
+    }
+    __threadfence_block();
+    return unit_q[k % kStreamQ];
+  };
+  // record of work position u: resident slot record, or the landing record of its copy job
+  auto record_of = [&](int u) -> int { return jpos_sh[u] >= 0 ? f.rid_land0 + jpos_sh[u] : lp->rid[u]; };
+
+  if (warp == kStreamWarps) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      int npub = 0;
+      bool ok = go;
+      auto slot = [&](int& s) -> bool {   // the next ring stage, once its previous fill is consumed
+        s = (int)(it % (uint32_t)S);
+        if (it >= (uint32_t)S && !mbar_wait(&empty_bar[s], ((it / S) - 1) & 1)) return false;
+        return !abort_sh;
+      };
+      // phase 1: a CTA that starts on expert work at once takes its first unit by index
+      const int first = (int)blockIdx.x - f.cta0_plans - ncopy;
+      const uint32_t nfirst = (uint32_t)(G - f.cta0_plans - ncopy);
+      uint32_t g = first >= 0 ? (uint32_t)first : nfirst + atomicAdd(f.next_unit, 1u);
+      while (ok && g < n1) {
+        // the next one, while this one's loads go out (its value is read after them)
+        const uint32_t graw = atomicAdd(f.next_unit, 1u);
+        const int li = (int)g / per1, rem = (int)g - li * per1;
+        const int mt = rem / rg_tile, rg = rem - mt * rg_tile;
+        const bool miss = li >= nh;
+        const int u = miss ? lp->elist[1][li - nh] : lp->elist[0][li];
+        if (miss) {
+          // the copied record's gate/up part, written by the copy CTAs
+          if (!wait_count(&f.jdone[li - nh], njd, a.status)) { ok = false; break; }
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+        publish(npub++, (int)g);
+        const int rid = record_of(u);
+        for (int kb0 = 0; kb0 < kb_h; kb0 += kStreamKb, ++it) {
+          int s;
+          if (!slot(s)) { ok = false; break; }
+          // tiles 2 kb0 .. 2 kb0 + 15 (gate, up of 8 K blocks; past the last: zeros), rows rg * 16 ..
+          mbar_expect_tx(&full_bar[s], kStreamStage);
+          tma_load_5d_ef(ring + (size_t)s * kStreamStage, map_w13, &full_bar[s], 0, rg * kStreamRows, 2 * kb0, mt, rid);
+        }
+        g = nfirst + graw;
+      }
+      publish(npub++, kStreamEnd1);
+      // phase 2: units handed out by a second counter.  Until every CTA's h is written,
+      // stages go out with their W_down segments only; their h slices follow the arrival.
+      bool h_ok = false;
+      int pend_s[kMaxStages], pend_u[kMaxStages], pend_kb[kMaxStages], npend = 0;
+      auto issue_h = [&](int s, int u, int kb0) {   // K blocks kb0 .. kb0 + 7 of every token's h
+        tma_load_4d(ring + (size_t)s * kStreamStage + kStreamHOff, map_h, &full_bar[s], 0, kb0, 0, u);
+      };
+      auto arrival = [&]() -> bool {
+        if (!wait_count(p1_done, (uint32_t)G * kStreamWarps, a.status)) return false;
+        asm volatile("fence.proxy.async.global;" ::: "memory");   // h written by every CTA -> bulk reads
+        h_ok = true;
+        for (int q = 0; q < npend; ++q) issue_h(pend_s[q], pend_u[q], pend_kb[q]);
+        npend = 0;
+        return true;
+      };
+      while (ok) {
+        const uint32_t g2 = atomicAdd(f.next_miss, 1u);
+        if (g2 >= n2) break;
+        publish(npub++, kStreamP2 | (int)g2);
+        const int mt = (int)g2 / rg_tile, rg = (int)g2 - mt * rg_tile;
+        for (int u = 0; ok && u < n; ++u) {
+          if (jpos_sh[u] >= 0) {
+            // a copied record's W_down part (it lands after every gate/up part, so the
+            // arrival comes first: the stages already issued get their h meanwhile)
+            if (!h_ok && npend > 0 && !arrival()) { ok = false; break; }
+            if (!wait_count(&f.jdone_w2[jpos_sh[u]], njd, a.status)) { ok = false; break; }
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+          }
+          const int rid = record_of(u);
+          for (int kb0 = 0; kb0 < kb_i; kb0 += kStreamKb, ++it) {
+            // every ring stage waiting for its h slice: the arrival first (the oldest stage
+            // cannot be consumed before it)
+            if (!h_ok && npend == S && !arrival()) { ok = false; break; }
+            int s;
+            if (!slot(s)) { ok = false; break; }
+            // W_down tiles kb0 .. kb0 + 7 (past the last: zeros), rows rg * 16 .., and the h slice
+            mbar_expect_tx(&full_bar[s], kStreamHOff + (uint32_t)T * kStreamKb * 256);
+            tma_load_5d_ef(ring + (size_t)s * kStreamStage, map_w2, &full_bar[s], 0, rg * kStreamRows, kb0, mt, rid);
+            if (h_ok) {
+              issue_h(s, u, kb0);
+            } else {
+              pend_s[npend] = s;
+              pend_u[npend] = u;
+              pend_kb[npend] = kb0;
+              ++npend;
+            }
+          }
+        }
+      }
+      if (ok && npend > 0 && !arrival()) ok = false;
+      publish(npub++, kStreamEnd);
+      if (!ok) {
+        set_status(a.status, MOE_ERR_TIMEOUT);
+        abort_sh = 1;
+        // stages still waiting for their h slice get one anyway (in-bounds reads of the
+        // scratch), so that their weight copies can be waited for below
+        for (int q = 0; q < npend; ++q) issue_h(pend_s[q], pend_u[q], pend_kb[q]);
+        npend = 0;
+      }
+      // drain: the last fill of every stage must have landed before the CTA exits
+      const uint32_t issued = it;
+      for (int s = 0; s < S; ++s) {
+        if ((uint32_t)s < issued) {
+          const uint32_t last = issued - 1 - ((issued - 1 - s) % S);
+          mbar_wait(&full_bar[s], (last / S) & 1);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------- compute warps
+    constexpr int NC = kStreamWarps * 32;
+    // x staged once as fp32 [T][Hp], zero past H
+    for (int i = threadIdx.x; i < T * (Hp / 8); i += NC) {
+      const int t = i / (Hp / 8), c = i - t * (Hp / 8);
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (go && c * 8 < H) v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H + c * 8));
+      float f[8];
+      unpack8_bf16(v, f);
+      reinterpret_cast<float4*>(xs)[2 * i] = make_float4(f[0], f[1], f[2], f[3]);
+      reinterpret_cast<float4*>(xs)[2 * i + 1] = make_float4(f[4], f[5], f[6], f[7]);
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(NC) : "memory");
+    uint32_t it = 0;
+    const uint32_t xs_a = smem_u32(xs), ring_a = smem_u32(ring);
+    auto stage_wait = [&](int s) {
+      if (!abort_sh && !mbar_try(&full_bar[s], (it / S) & 1) && !mbar_wait(&full_bar[s], (it / S) & 1)) {
+        set_status(a.status, MOE_ERR_TIMEOUT);
+        abort_sh = 1;
+      }
+    };
+    for (int k = 0;; ++k) {
+      const int g = unit_at(k);
+      if (g == kStreamEnd) break;
+      if (g == kStreamEnd1) {
+        // this warp's h stores are done: one release per warp (the warp barrier orders
+        // the lanes' stores before lane 0's cumulative release)
+        __syncwarp();
+        if (lane == 0 && !abort_sh) release_add(p1_done);
+        continue;
+      }
+      if (!(g & kStreamP2)) {
+        // ---- phase 1: rows warp and warp + 8 of 16 rows of tile mt of entry u's gate and up
+        const int li = g / per1, rem = g - li * per1;
+        const int mt = rem / rg_tile, rg = rem - mt * rg_tile;
+        const int u = li >= nh ? lp->elist[1][li - nh] : lp->elist[0][li];
+        // lane t: the routing weight of token t for this entry (1 for the shared expert), read
+        // from the step's routing once per unit, while the unit's first stage is in flight
+        float wt_lane = 0.f;
+        if (lane < T) {
+          const int e = lp->expert[u], kk = lp->k;
+          if (e < 0) {
+            wt_lane = 1.f;
+          } else {
+            for (int j = 0; j < kk; ++j)
+              if (lp->ids[lane * kk + j] == e) wt_lane += lp->w[lane * kk + j];
+          }
+        }
+        float acc[4][kStreamMaxT];
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+#pragma unroll
+          for (int t = 0; t < kStreamMaxT; ++t) acc[p][t] = 0.f;
+        for (int kb0 = 0; kb0 < kb_h; kb0 += kStreamKb, ++it) {
+          const int s = (int)(it % (uint32_t)S);
+          stage_wait(s);
+          const int nk = min(kStreamKb, kb_h - kb0);
+          if (!abort_sh) {
+            // this lane's chunks c = lane and lane + 32 of the stage (chunk c % 8 of K block
+            // c / 8): a chunk's shared-memory loads first, then its multiply-adds
+            const uint32_t st = ring_a + (uint32_t)s * kStreamStage;
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              const int c = lane + 32 * cc, kbi = c >> 3, q = c & 7;
+              if (kbi < nk) {
+                uint4 xq[kStreamMaxT][2], wq[4];
+#pragma unroll
+                for (int t = 0; t < kStreamMaxT; ++t) {
+                  if (t < T) {
+                    const uint32_t xa = xs_a + (uint32_t)(t * Hp + (kb0 + kbi) * 64 + q * 8) * 4u;
+                    xq[t][0] = lds128(xa);
+                    xq[t][1] = lds128(xa + 16);
+                  }
+                }
+#pragma unroll
+                for (int pr = 0; pr < 4; ++pr) {   // gate row warp, gate row warp + 8, up row warp, up row warp + 8
+                  const int m = pr >> 1, lr = warp + 8 * (pr & 1);
+                  wq[pr] = lds128(st + (uint32_t)(kbi * 2 + m) * kStreamSeg + lr * 128 + ((q ^ (lr & 7)) << 4));
+                }
+#pragma unroll
+                for (int pr = 0; pr < 4; ++pr) {
+                  float wv[8];
+                  unpack8_bf16(wq[pr], wv);   // once per chunk, for every token
+#pragma unroll
+                  for (int t = 0; t < kStreamMaxT; ++t) {
+                    if (t < T) {
+                      const float xv[8] = {__uint_as_float(xq[t][0].x), __uint_as_float(xq[t][0].y),
+                                           __uint_as_float(xq[t][0].z), __uint_as_float(xq[t][0].w),
+                                           __uint_as_float(xq[t][1].x), __uint_as_float(xq[t][1].y),
+                                           __uint_as_float(xq[t][1].z), __uint_as_float(xq[t][1].w)};
+                      acc[pr][t] = dot8(wv, xv, acc[pr][t]);
+                    }
+                  }
+                }
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty_bar[s]);
+        }
+#pragma unroll
+        for (int ri = 0; ri < 2; ++ri) {
+          const int i = mt * 128 + rg * kStreamRows + warp + 8 * ri;
+#pragma unroll
+          for (int t = 0; t < kStreamMaxT; ++t) {
+            if (t < T) {
+              const float gs = butterfly_sum(acc[ri][t]);
+              const float us = butterfly_sum(acc[2 + ri][t]);
+              const float wt = __shfl_sync(0xffffffffu, wt_lane, t);
+              if (lane == 0 && i < Ip) hf[((size_t)u * T + t) * Ip + i] = i < I && wt != 0.f ? wt * silu(gs) * us : 0.f;
+            }
+          }
+        }
+      } else {
+        // ---- phase 2: rows 2 warp and 2 warp + 1 of 16 rows of tile mt of H, every entry
+        const int g2 = g & ~kStreamP2;
+        const int mt = g2 / rg_tile, rg = g2 - mt * rg_tile;
+        float acc[2][kStreamMaxT];
+#pragma unroll
+        for (int ri = 0; ri < 2; ++ri)
+#pragma unroll
+          for (int t = 0; t < kStreamMaxT; ++t) acc[ri][t] = 0.f;
+        for (int u = 0; u < n; ++u) {
+          for (int kb0 = 0; kb0 < kb_i; kb0 += kStreamKb, ++it) {
+            const int s = (int)(it % (uint32_t)S);
+            stage_wait(s);
+            const int nk = min(kStreamKb, kb_i - kb0);
+            if (!abort_sh) {
+              // this lane's chunks c = lane and lane + 32: a chunk's h slices and W_down rows
+              // first, then its multiply-adds
+              const uint32_t st = ring_a + (uint32_t)s * kStreamStage;
+#pragma unroll
+              for (int cc = 0; cc < 2; ++cc) {
+                const int c = lane + 32 * cc, kbi = c >> 3, q = c & 7;
+                if (kbi < nk) {
+                  uint4 hq[kStreamMaxT][2], wq[2];
+#pragma unroll
+                  for (int t = 0; t < kStreamMaxT; ++t) {
+                    if (t < T) {
+                      const uint32_t hp = st + kStreamHOff + (uint32_t)t * kStreamKb * 256 + (uint32_t)(kbi * 64 + q * 8) * 4u;
+                      hq[t][0] = lds128(hp);
+                      hq[t][1] = lds128(hp + 16);
+                    }
+                  }
+#pragma unroll
+                  for (int ri = 0; ri < 2; ++ri) {
+                    const int lr = 2 * warp + ri;
+                    wq[ri] = lds128(st + (uint32_t)kbi * kStreamSeg + lr * 128 + ((q ^ (lr & 7)) << 4));
+                  }
+#pragma unroll
+                  for (int ri = 0; ri < 2; ++ri) {
+                    float wv[8];
+                    unpack8_bf16(wq[ri], wv);   // once per chunk, for every token
+#pragma unroll
+                    for (int t = 0; t < kStreamMaxT; ++t) {
+                      if (t < T) {
+                        const float hv[8] = {__uint_as_float(hq[t][0].x), __uint_as_float(hq[t][0].y),
+                                             __uint_as_float(hq[t][0].z), __uint_as_float(hq[t][0].w),
+                                             __uint_as_float(hq[t][1].x), __uint_as_float(hq[t][1].y),
+                                             __uint_as_float(hq[t][1].z), __uint_as_float(hq[t][1].w)};
+                        acc[ri][t] = dot8(wv, hv, acc[ri][t]);
+                      }
+                    }
+                  }
+                }
+              }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[s]);
+          }
+        }
+#pragma unroll
+        for (int ri = 0; ri < 2; ++ri) {
+          const int m = mt * 128 + rg * kStreamRows + 2 * warp + ri;
+#pragma unroll
+          for (int t = 0; t < kStreamMaxT; ++t) {
+            if (t < T) {
+              const float v = butterfly_sum(acc[ri][t]);
+              if (lane == 0 && m < H && !abort_sh) a.out[(size_t)t * H + m] = f32_to_bf16_rn(v);
+            }
+          }
+        }
+      }
     }
   }
 }
@@ -1574,12 +2054,18 @@ constexpr int kDecodeMaxT = 32;
 constexpr int kRouterMaxSplits = 32;   // K splits of the tensor-core router
 constexpr int kRouteChunks = 16;   // router-row loads in flight per lane (H <= 4096 in one round)
 
-template <int WF>
-__global__ void __launch_bounds__(FusedShape<WF>::threads, 1)
+// STREAM: the CUDA-core streaming FFN (bf16 tiled records, T <= kStreamMaxT, local lists)
+// instead of the tensor-core one.
+template <int WF, bool STREAM> struct DecodeShape {
+  static constexpr int threads = STREAM ? kStreamThreads : FusedShape<WF>::threads;
+};
+
+template <int WF, bool STREAM>
+__global__ void __launch_bounds__(DecodeShape<WF, STREAM>::threads, 1)
 tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_h,
                        const __grid_constant__ CUtensorMap map_w13, const __grid_constant__ CUtensorMap map_w2, Args a,
                        FusedArgs f, DecodeArgs d) {
-  constexpr int NT = FusedShape<WF>::threads;
+  constexpr int NT = DecodeShape<WF, STREAM>::threads;
   extern __shared__ uint8_t smem_raw[];
   __shared__ volatile int flag_sh;
   __shared__ LocalPlan lp_sh;
@@ -1701,7 +2187,7 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
     fl.rid_land0 = p.rid_land0;
     fl.S = p.S;
   }
-  fused_ffn<WF>(&map_x, &map_h, &map_w13, &map_w2, a, fl, smem_raw, [&]() -> bool {
+  auto pre = [&]() -> bool {
     // every token gated (and the counters zeroed)
     if (threadIdx.x == 0) {
       flag_sh = wait_count(route_done, (uint32_t)T + 1u, a.status) ? 1 : 0;
@@ -1784,7 +2270,12 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
     }
     __syncthreads();
     return true;
-  });
+  };
+  if constexpr (STREAM) {
+    stream_ffn(&map_w13, &map_w2, &map_h, a, fl, d.x, smem_raw, pre);
+  } else {
+    fused_ffn<WF>(&map_x, &map_h, &map_w13, &map_w2, a, fl, smem_raw, pre);
+  }
   // ---- leave: the last CTA resets the counters for the next launch
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -2031,10 +2522,35 @@ static bool make_map_u8_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tiled map without swizzle (the bf16 records are stored swizzled already), zero fill
+// past the edges.  strides: the rank - 1 outer strides in bytes.
+static bool make_map_nd(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const cuuint64_t* dims,
+                        const cuuint64_t* strides, const cuuint32_t* box) {
+  auto fn = tc::encode_fn();
+  if (!fn) return false;
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(m, dt, rank, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 TcMaps* tc_maps_create(const PoolDev& p, const Scratch& sc) {
   (void)sc;
   if (!tc::encode_fn()) return nullptr;
   TcMaps* m = new TcMaps();
+  if (p.wdt == MOE_BF16) {
+    // 16-row segments of 8 consecutive tiles: w13 tiles (kb, gate/up) of one 128-row block mt of
+    // I, w2 tiles kb of one 128-row block of H, in any record
+    const uint64_t kb_h = (p.H + 63) / 64, kb_i = (p.I + 63) / 64, mt_i = (p.I + 127) / 128, mt_h = (p.H + 127) / 128;
+    const cuuint64_t d13[5] = {128, 128, 2 * kb_h, mt_i, (cuuint64_t)p.n_records};
+    const cuuint64_t s13[4] = {128, tc::kTileBytes, 2 * kb_h * tc::kTileBytes, p.lay.rec};
+    const cuuint32_t b13[5] = {128, tc::kStreamRows, 2 * tc::kStreamKb, 1, 1};
+    const cuuint64_t d2[5] = {128, 128, kb_i, mt_h, (cuuint64_t)p.n_records};
+    const cuuint64_t s2[4] = {128, tc::kTileBytes, kb_i * tc::kTileBytes, p.lay.rec};
+    const cuuint32_t b2[5] = {128, tc::kStreamRows, tc::kStreamKb, 1, 1};
+    m->stream = make_map_nd(&m->sw13, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, p.records + p.lay.off13, d13, s13, b13) &&
+                make_map_nd(&m->sw2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, p.records + p.lay.off2, d2, s2, b2);
+  }
   if (p.wdt == MOE_FP8_E4M3_B128) {
     m->fp8 = true;
     const uint64_t H = p.H, I = p.I, n = p.n_records, rec = p.lay.rec;
@@ -2271,11 +2787,31 @@ bool tc_decode_layer_ok(const PoolDev& p, const Scratch& sc, int T) {
 }
 
 // Router, gate, plan and fused FFN of one decode call, one cooperative launch.
+template <int WF, bool STREAM>
+static int launch_decode_layer_impl(const PoolDev& p, const Scratch& sc, const TcMaps* m, int layer, int T,
+                                    const void* x, const void* router_w, const float* router_b, void* out,
+                                    cudaStream_t s);
+
 template <int WF>
 static int launch_decode_layer_wf(const PoolDev& p, const Scratch& sc, const TcMaps* m, int layer, int T,
                                   const void* x, const void* router_w, const float* router_b, void* out,
                                   cudaStream_t s) {
-  constexpr int NT = tc::FusedShape<WF>::threads;
+  // bf16 pools and one to four tokens: the CUDA-core streaming FFN
+  if constexpr (WF == tc::kWfBf16) {
+    if (m->stream && T <= tc::kStreamMaxT && T * p.k <= tc::kLocalMaxTk && p.E <= kMaxE &&
+        std::min(T * p.k, p.E) <= p.n_land &&
+        (size_t)(p.E + 1) * T * ((p.I + 63) / 64 * 64) * 4 <= (size_t)(p.E + 1) * sc.npad_max * p.I * 2 &&
+        (size_t)T * ((p.H + 63) / 64 * 64) * 4 + 1024 + 2 * tc::kStreamStage <= (size_t)tc::kSmemBudget)
+      return launch_decode_layer_impl<WF, true>(p, sc, m, layer, T, x, router_w, router_b, out, s);
+  }
+  return launch_decode_layer_impl<WF, false>(p, sc, m, layer, T, x, router_w, router_b, out, s);
+}
+
+template <int WF, bool STREAM>
+static int launch_decode_layer_impl(const PoolDev& p, const Scratch& sc, const TcMaps* m, int layer, int T,
+                                    const void* x, const void* router_w, const float* router_b, void* out,
+                                    cudaStream_t s) {
+  constexpr int NT = tc::DecodeShape<WF, STREAM>::threads;
   tc::Args a;
   tc::FusedArgs f;
   CUtensorMap xm, hm;
@@ -2310,9 +2846,24 @@ static int launch_decode_layer_wf(const PoolDev& p, const Scratch& sc, const TcM
   const size_t psm = decode_plan_smem<NT>(p, T, &pa.owner_cap, &pa.tok_rows);
   if (psm == 0) return -1;
   d.dsync = sc.dsync;
-  const size_t smem = std::max(std::max(fused_smem(a.N, a.stages), psm + 1024), (size_t)p.H * 2 + 16 + 1024);
+  size_t ffn_smem = fused_smem(a.N, a.stages);
+  if (STREAM) {
+    // h as [work position][T][Ip / 64][64] fp32 in the h scratch; boxes of 8 K blocks x T tokens
+    const uint64_t kb_i = (p.I + 63) / 64, Ip = kb_i * 64;
+    const cuuint64_t dh[4] = {64, kb_i, (cuuint64_t)T, (cuuint64_t)p.E + 1};
+    const cuuint64_t sh[3] = {256, Ip * 4, (cuuint64_t)T * Ip * 4};
+    const cuuint32_t bh[4] = {64, tc::kStreamKb, (cuuint32_t)T, 1};
+    if (!make_map_nd(&hm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, sc.hbuf, dh, sh, bh)) return -1;
+    w13 = m->sw13;
+    w2 = m->sw2;
+    // [x: T x H fp32, whole K blocks, 1 KB aligned][ring of 32 KB stages]
+    const size_t xb = ((size_t)T * ((p.H + 63) / 64 * 64) * 4 + 1023) & ~(size_t)1023;
+    a.stages = std::min<int>(tc::kMaxStages, (int)((tc::kSmemBudget - xb) / tc::kStreamStage));
+    ffn_smem = 1024 + xb + (size_t)a.stages * tc::kStreamStage;
+  }
+  const size_t smem = std::max(std::max(ffn_smem, psm + 1024), (size_t)p.H * 2 + 16 + 1024);
   static bool configured[64] = {};
-  const void* fn = reinterpret_cast<const void*>(tc::tc_decode_layer_kernel<WF>);
+  const void* fn = reinterpret_cast<const void*>(tc::tc_decode_layer_kernel<WF, STREAM>);
   set_smem_attr_once(fn, configured);
   void* args[] = {&xm, &hm, &w13, &w2, &a, &f, &d};
   return launch_cooperative(fn, NT, smem, s, args);

@@ -87,6 +87,31 @@ def test_tensor_core_output_independent_of_resident_set():
             r.close()
 
 
+@pytest.mark.parametrize("T", [1, 2, 4])
+def test_streaming_output_independent_of_resident_set(T):
+    """One-token calls take the bf16 streaming path, two and four tokens the tensor-core path: on
+    either, the output of a step is the same bits whether all, a third or six of the layer's
+    experts were resident (misses copied in-kernel, bypass records), and it matches the oracle."""
+    wl = variant(get_workload("qwen3_decode"), name="resident_set_stream", L=2, E=64, k=8, H=1024, I=512)
+    rigs = [Rig(wl, S=wl.L * wl.E, lut=np.arange(wl.L * wl.E, dtype=np.int32).reshape(wl.L, wl.E)),
+            Rig(wl, S=wl.L * wl.E // 3), Rig(wl, S=6)]
+    try:
+        for l in range(wl.L):
+            xs = gen.store_act(wl, gen.decode_hidden(wl, l, T, 4))
+            for t in range(4):
+                outs = [r.forward(l, xs[t]) for r in rigs]
+                for o in outs[1:]:
+                    assert np.array_equal(outs[0], o)
+                ref, _ = rigs[0].oracle_forward(l, xs[t])
+                check_output(wl, outs[0], ref)
+        assert rigs[0].pool.stats()["misses"] == 0
+        assert rigs[1].pool.stats()["misses"] > 0 and rigs[2].pool.stats()["misses"] > 0
+        assert all(r.pool.status() == moe.MOE_OK for r in rigs)
+    finally:
+        for r in rigs:
+            r.close()
+
+
 @pytest.mark.parametrize("shape", ["bf16_small", "bf16_qwen3_layer", "fp8"])
 def test_slots_hold_their_owners_records_after_decode_steps(shape):
     """After decode steps whose misses were copied in-kernel (landing record, then slot), every owned

@@ -170,9 +170,10 @@ def test_fp8_block_scaled_with_shared_expert():
         rig.close()
 
 
-@pytest.mark.parametrize("T", [17, 257, 600])
+@pytest.mark.parametrize("T", [1, 17, 257, 600])
 def test_bf16_dense_and_gather_paths_with_shared_expert(T):
-    """T <= 256 takes the dense tensor-core path, larger T the expert-grouped (gather) path."""
+    """T = 1 takes the CUDA-core streaming path, T <= 256 the dense tensor-core path, larger T the
+    expert-grouped (gather) path; I = 320 leaves the last 128-row tile of I partly padding."""
     wl = variant(get_workload("qwen3_decode"), name="gather_bf16", L=2, E=32, k=4, H=512, I=320,
                  residency=0.5, shared=True, zipf_s=0.5)
     rig = Rig(wl, max_tokens=640)
