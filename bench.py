@@ -425,6 +425,17 @@ KERNEL_LABEL = {True: "tc_decode_layer_kernel (router, gate, plan, miss copies, 
                 False: "tc_fused_decode_kernel (miss copies + gate/up + down + combine)"}
 
 
+def kernel_label(wl, fused, T):
+    """The decode FFN kernel a call of T tokens runs: fp32 weights take the CUDA-core streaming
+    kernels, bf16 single-token decode layer calls the CUDA-core streaming variant of the layer kernel,
+    everything else the tensor-core kernels."""
+    if wl.weight_dtype == 0:
+        return "ffn_gate_up_kernel + ffn_down_combine_kernel"
+    if fused and wl.weight_dtype == 1 and T == 1:
+        return "tc_decode_layer_kernel, streaming FFN variant (router, gate, plan, miss copies, gate/up, down)"
+    return KERNEL_LABEL[fused]
+
+
 def step_bytes(wl, U_per_layer, T):
     """Algorithmic HBM bytes of one layer-step: router + U expert records + x in and out."""
     return wl.E * wl.H * wl.act_elt_bytes + U_per_layer * expert_bytes(wl) + 2 * T * wl.H * wl.act_elt_bytes
@@ -454,8 +465,7 @@ def decode_summary(wl, r, peak):
             "hit_rate": r["hits"] / max(1, r["hits"] + r["misses"]),
             "miss_MB_per_layer": r["bytes_copied"] / 1e6 / (r["steps"] * wl.L),
             "mean_U": U, "stage_us_per_layer": {k: v * 1e3 / n for k, v in zip(moe.STAGES, prof["stage_ms"])},
-            "ffn_roofline": {"bound": "hbm", "kernel": KERNEL_LABEL[fused] if wl.weight_dtype == 1 else
-                             "ffn_gate_up_kernel + ffn_down_combine_kernel",
+            "ffn_roofline": {"bound": "hbm", "kernel": kernel_label(wl, fused, r["T"]),
                              "achieved": ach, "unit": "GB/s", "frac": ach / peak,
                              "bytes_per_launch": ffn_b / n, "us_per_launch": ffn_ms * 1e3 / n},
             "layer_frac": step_bytes(wl, U, r["T"]) / (lay_us * 1e-6) / 1e9 / peak if lay_us else 0.0,
