@@ -145,7 +145,9 @@ MOE_API moe_status moe_pool_destroy(moe_pool* pool);   /* blocking; NULL is a no
  *             may appear at most once.
  * Every assigned slot is filled from the host pool on `stream` and its tag is
  * incremented.  Routing history is kept.  Blocking on the host only for the
- * small table upload. */
+ * small table upload: the slot copies (one record per assigned slot) are still
+ * running when the call returns, so work on another stream that reads the pool
+ * (moe_forward included) must first wait for `stream`. */
 MOE_API moe_status moe_set_lut(moe_pool* pool, const int32_t* lut_host, void* stream);
 
 /* Host-initiated placement of expert (layer, expert) into `slot`: the slot's

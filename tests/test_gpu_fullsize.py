@@ -48,6 +48,9 @@ def _pool(wl, host, wr_dev, b_dev, max_T=T):
     pool = moe.Pool(cfg, host.ptr, host.nbytes, wr_dev, b_dev)
     lut0 = gen.initial_lut(wl)
     pool.set_lut(lut0)
+    # set_lut fills the slots asynchronously on the current stream; the graph test runs its steps on
+    # a stream of its own, which must not start before every slot holds its record
+    torch.cuda.synchronize()
     return pool, lut0
 
 
