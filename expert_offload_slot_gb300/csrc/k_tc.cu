@@ -1558,14 +1558,14 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
 // ----------------------------------------------------------------- streaming decode FFN (one token)
 // With one token, a layer call is one matrix-vector product per expert: each
 // weight streams from HBM once and feeds one multiply-add, which the CUDA cores
-// keep up with, so the tensor cores buy nothing.  What costs
-// time on the tensor-core path at these sizes is its structure: gate/up tiles
+// keep up with, so the tensor cores buy nothing.  What costs time on the
+// tensor-core path at this size is its structure: gate/up tiles
 // split along K (partials, arrivals and a reduction per tile before the down
 // projection may start) and a grid-wide combine of per-entry down partials.
 // This path has neither:
 //   phase 1: unit = (work entry u, 16 rows of a 128-row tile of I), all of K.  The
-//            unit's gate and up rows stream through a shared-memory ring (one
-//            bulk copy per 2 KB row segment of a swizzled 128 x 64 tile); each
+//            unit's gate and up rows stream through a shared-memory ring (the 2 KB
+//            16-row segments of the swizzled 128 x 64 tiles); each
 //            compute warp owns two rows of gate and of up and finishes
 //            h = w(u,t) SiLU(W_gate x_t) (W_up x_t) itself, in fp32, into global
 //            scratch (rows past I as 0).
@@ -1586,7 +1586,7 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
 // depend on which experts are resident, so neither does the output.
 // Tokens the path takes.  The code is written for up to four, but measured on the
 // Qwen3-shaped layer it beats the tensor-core path only at one token (all experts
-// resident: 39.6 vs 43.2 us per call); at four it is slower (83 vs ~60 us): its
+// resident: 35.7-39.8 vs 43 us per call); at four it is slower (83 vs ~60 us): its
 // 16-row units read each tile as 2 KB pieces, whose loads wait far longer than
 // the tensor-core path's contiguous 32 KB stages.
 constexpr int kStreamMaxT = 1;
@@ -1614,8 +1614,8 @@ __device__ __forceinline__ float dot8(const float* w, const float* v, float acc)
 }
 
 // 16 bytes from shared memory at a shared-window address (explicitly shared: the
-// ring's pointers come from aligned integer arithmetic, which generic loads would
-// route through the global path)
+// ring's pointers come from aligned integer arithmetic, so the compiler cannot tell
+// they address shared memory and would emit generic loads)
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
