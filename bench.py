@@ -436,6 +436,18 @@ def kernel_label(wl, fused, T):
     return KERNEL_LABEL[fused]
 
 
+def layer_floor(layer_bytes, miss_bytes, us_per_layer, hbm_gbs, link_gbs):
+    """Lower bound on a decode layer-step's time from its two streams, which can overlap: the
+    algorithmic HBM bytes at the measured HBM copy peak, and the miss records at the measured host
+    link rate (None when the link was not measured).  frac = floor / measured time."""
+    hbm_us = layer_bytes / (hbm_gbs * 1e9) * 1e6
+    link_us = miss_bytes / (link_gbs * 1e9) * 1e6 if link_gbs else None
+    floor = max(hbm_us, link_us or 0.0)
+    return {"hbm_us": hbm_us, "link_us": link_us, "floor_us": floor, "us_per_layer": us_per_layer,
+            "frac": floor / us_per_layer if us_per_layer > 0 else 0.0, "link_GBps": link_gbs,
+            "bound": "link" if link_us is not None and link_us > hbm_us else "hbm"}
+
+
 def step_bytes(wl, U_per_layer, T):
     """Algorithmic HBM bytes of one layer-step: router + U expert records + x in and out."""
     return wl.E * wl.H * wl.act_elt_bytes + U_per_layer * expert_bytes(wl) + 2 * T * wl.H * wl.act_elt_bytes
@@ -753,6 +765,12 @@ def main():
     cpu = None
     if not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, T, args.cpu_sample, dev)
+    us_layer = ms * 1e3 / (r["steps"] * wl.L)
+    try:
+        floor = layer_floor(layer_bytes, r["bytes_copied"] / (r["steps"] * wl.L), us_layer, peak,
+                            configs.get("link", {}).get("dma_h2d_GBps"))
+    except (KeyError, TypeError, ZeroDivisionError):
+        floor = None
     line = {
         "metric": "MoE-layer tokens/s (decode)", "value": value, "unit": "MoE-layer tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / r["steps"], "higher_is_better": True,
@@ -773,6 +791,7 @@ def main():
         "layer_roofline": {"algorithmic_bytes_per_layer": layer_bytes, "mean_U": U_mean,
                            "us_per_layer_profiled": prof_layer_us,
                            "frac": layer_bytes / (prof_layer_us * 1e-6) / 1e9 / peak if prof_layer_us else 0.0},
+        "layer_floor": floor,
         "stage_us_per_layer": {n: v * 1e3 / max(1, layer_steps) for n, v in zip(moe.STAGES, prof["stage_ms"])},
         "clocks": r["clocks"],
         "gpu_launches": r["launches_per_step"] * r["steps"],
