@@ -16,9 +16,11 @@ MoE-layer tokens/s = (steps * T * 48) / elapsed.
 
 Printed (rank 0, one JSON line): value (inputs already in HBM), e2e (same
 metric through the C ABI with host buffers: per-step pinned H2D of x and D2H of
-the output inside the timed region), roofline of the dominant kernel (expert
-gate/up streaming, timed per launch with CUDA events in a profiling pass of the
-same workload), clocks sampled with nvidia-smi during the timed region, and the
+the output inside the timed region), roofline of the dominant kernel (the decode
+layer kernel, timed per launch with CUDA events in a profiling pass of the same
+workload), layer_floor (the layer-step's bound from HBM bytes and miss records
+over the measured host link), clocks sampled with nvidia-smi during the timed
+region, the other decode batches (sweep) and workload shapes (configs), and the
 CPU oracle timed on a bounded sample as cpu_baseline.
 
 --impl reference times the CPU oracle itself on the same workload and prints
