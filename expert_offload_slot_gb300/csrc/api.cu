@@ -243,6 +243,8 @@ MOE_API moe_status moe_pool_create(const moe_config* cfg, const void* host_pool,
   if (host_pool_bytes < L * E * lay.rec)
     return fail(MOE_ERR_INVALID, "host_pool_bytes %zu < L*E*record_bytes %zu", host_pool_bytes, L * E * lay.rec);
   if (!router_w || !router_b) return fail(MOE_ERR_INVALID, "router weights are NULL");
+  if ((reinterpret_cast<uintptr_t>(router_w) & 15) || (reinterpret_cast<uintptr_t>(router_b) & 3))
+    return fail(MOE_ERR_INVALID, "router_w must be 16-byte aligned and router_b 4-byte aligned");
   if (cfg->has_shared_expert && !shared_w) return fail(MOE_ERR_INVALID, "shared_w is NULL but has_shared_expert");
   int ndev = 0;
   CUDA_TRY(cudaGetDeviceCount(&ndev));
@@ -629,6 +631,10 @@ MOE_API moe_status moe_forward_routed(moe_pool* P, int32_t layer, const void* x,
   if (T == 0) return MOE_OK;
   if (!x || !out || !ids || !w || !probs) return fail(MOE_ERR_INVALID, "NULL argument");
   if (x == out) return fail(MOE_ERR_INVALID, "out must not alias x");
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(out)) & 15)
+    return fail(MOE_ERR_INVALID, "x and out must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(ids) | reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(probs)) & 3)
+    return fail(MOE_ERR_INVALID, "ids, w and probs must be 4-byte aligned");
   CUDA_TRY(cudaSetDevice(P->device));
   return run_layer(P, layer, x, T, out, false, ids, w, probs, static_cast<cudaStream_t>(stream));
 }

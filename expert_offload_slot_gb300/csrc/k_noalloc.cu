@@ -63,6 +63,12 @@ MOE_API moe_status moe_route_topk_noalloc(int32_t num_experts, int32_t top_k, in
   if (T == 0) return MOE_OK;
   if (!x || !router_w || !router_b || !ids || !w || !probs || !gap)
     return set_last_error(MOE_ERR_INVALID, "NULL argument");
+  // the router kernel reads x and router_w 16 bytes at a time; the rest are 4-byte elements
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(router_w)) & 15)
+    return set_last_error(MOE_ERR_INVALID, "x and router_w must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(router_b) | reinterpret_cast<uintptr_t>(ids) | reinterpret_cast<uintptr_t>(w) |
+       reinterpret_cast<uintptr_t>(probs) | reinterpret_cast<uintptr_t>(gap)) & 3)
+    return set_last_error(MOE_ERR_INVALID, "router_b, ids, w, probs and gap must be 4-byte aligned");
 
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)

@@ -22,8 +22,7 @@
 //
 // Score arithmetic uses explicitly rounded fp32 operations in a fixed order
 // (no contraction), because the scores decide integer victim choices.  The
-// token average sums blocks of 32 consecutive tokens in ascending order, then
-// the block sums in ascending order.
+// token average sums each expert's probabilities in ascending token order.
 #include "plan_body.cuh"
 
 namespace moeslot {

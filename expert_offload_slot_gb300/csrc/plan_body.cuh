@@ -203,24 +203,8 @@ __device__ void plan_body(const PlanArgs& a, uint8_t* dsm, bool prestaged = fals
   }
   if (hist) {
     t_step = p.step[l];
-    if (T <= kTokBlock) {
-      stage_async<NT>(tok, a.probs, (size_t)T * E * 4);
-    } else {
-      // block partial sums: tok[b][e] = sum of probs over tokens [32b, 32b+32), ascending
-      const int nblk = (T + kTokBlock - 1) / kTokBlock;
-      for (int j = tid; j < nblk * E; j += kPlanThreads) {
-        const int b = j / E, e = j - b * E;
-        const int t0 = b * kTokBlock, t1 = min(T, t0 + kTokBlock);
-        float v[kTokBlock];
-#pragma unroll
-        for (int q = 0; q < kTokBlock; ++q) v[q] = t0 + q < t1 ? a.probs[(size_t)(t0 + q) * E + e] : 0.f;
-        float s = 0.f;
-#pragma unroll
-        for (int q = 0; q < kTokBlock; ++q)
-          if (t0 + q < t1) s = __fadd_rn(s, v[q]);
-        tok[j] = s;
-      }
-    }
+    // short steps stage the probabilities; longer ones are summed from global memory below
+    if (T <= kTokBlock) stage_async<NT>(tok, a.probs, (size_t)T * E * 4);
     if (tid < E) {
       ema0 = p.ema[(size_t)l * E + tid];
       last0 = p.last_sel[(size_t)l * E + tid];
@@ -249,11 +233,21 @@ __device__ void plan_body(const PlanArgs& a, uint8_t* dsm, bool prestaged = fals
     int count = 0, age = 0;
     if (mine) {
       const int e = tid;
+      // token-averaged probability: one sum per expert in ascending token order
       if (T <= kTokBlock) {
         for (int tt = 0; tt < T; ++tt) s = __fadd_rn(s, tok[tt * E + e]);
       } else {
-        const int nblk = (T + kTokBlock - 1) / kTokBlock;
-        for (int b = 0; b < nblk; ++b) s = __fadd_rn(s, tok[b * E + e]);
+        // coalesced across the threads (consecutive experts); 16 loads in flight, then the adds in order
+        const float* pe = a.probs + e;
+        int tt = 0;
+        for (; tt + 16 <= T; tt += 16) {
+          float v[16];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) v[q] = pe[(size_t)(tt + q) * E];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) s = __fadd_rn(s, v[q]);
+        }
+        for (; tt < T; ++tt) s = __fadd_rn(s, pe[(size_t)tt * E]);
       }
       s = __fdiv_rn(s, (float)T);
       const int sel = cnt[e] > 0 ? 1 : 0;
@@ -684,10 +678,10 @@ __device__ void plan_body(const PlanArgs& a, uint8_t* dsm, bool prestaged = fals
 template <int NT>
 inline size_t plan_smem_bytes_nt(const PoolDev& p, int Tmax, int* owner_cap_out, int* tok_rows_out,
                                  size_t budget = 200 * 1024) {
-  // T <= 32 stages the probabilities themselves (up to 32 rows); larger T stages
-  // one partial sum per 32-token block
-  const int nblk = (Tmax + kTokBlock - 1) / kTokBlock;
-  const int tok_rows = nblk > kTokBlock ? nblk : kTokBlock;
+  // T <= 32 stages the probabilities themselves (up to 32 rows); larger T reads them
+  // from global memory
+  (void)Tmax;
+  const int tok_rows = kTokBlock;
   int cap = p.S <= kOwnerSmemMax ? p.S : 0;
   SmemLayout L = plan_smem_layout(p.E, p.W, tok_rows, cap, NT / 32);
   if (L.total > budget) {          // very large pools: owners stay in global memory

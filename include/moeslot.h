@@ -249,7 +249,9 @@ MOE_API moe_status moe_profile_read(moe_pool* pool, int32_t layer, float* stage_
  *   router_b  device fp32 [num_experts]
  *   ids [T, top_k] int32, w [T, top_k] fp32, probs [T, num_experts] fp32,
  *   gap [T] fp32: device outputs, as moe_get_routing describes them.
- * Argument errors return MOE_ERR_INVALID; T == 0 returns MOE_OK. */
+ * x and router_w must be 16-byte aligned (they are read 16 bytes at a time),
+ * the other pointers 4-byte aligned.  Argument errors, misalignment included,
+ * return MOE_ERR_INVALID before anything is launched; T == 0 returns MOE_OK. */
 #define MOE_NOALLOC_MAX_LOGITS 65536
 MOE_API moe_status moe_route_topk_noalloc(int32_t num_experts, int32_t top_k, int32_t hidden, int32_t act_dtype,
                                           int32_t gating, const void* x, int32_t T, const void* router_w,

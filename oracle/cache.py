@@ -16,10 +16,8 @@ Oracle; test infrastructure only.  Sources:
 
 Readings taken where the pages are silent (each is listed in the design notes):
   * s_e(t) = (sum over tokens of the full softmax / sigmoid probability) / T,
-    the sum taken in blocks of 32 consecutive tokens (each block summed in
-    ascending token order, then the block sums added in ascending block
-    order; for T <= 32 this is the plain ascending sum).  sel_e(t) = 1 if any
-    token selected e.
+    the sum taken in ascending token order.  sel_e(t) = 1 if any token
+    selected e.
   * History lives per (layer, expert) for all E experts and is not reset on
     eviction; ring buffers of W steps start at zero.  Each layer counts its own
     steps t = 0, 1, 2, ...
@@ -106,11 +104,8 @@ class SlotPoolSim:
         E, W = self.E, self.W
         t = int(self.step[l])
         s = np.zeros(E, F32)
-        for b0 in range(0, T, 32):                # blocks of 32 tokens, ascending
-            blk = np.zeros(E, F32)
-            for tt in range(b0, min(T, b0 + 32)):
-                blk = blk + p[tt]
-            s = s + blk
+        for tt in range(T):                       # ascending token order
+            s = s + p[tt]
         s = s / F32(T)
         sel = np.zeros(E, np.uint8)
         sel[ids.reshape(-1)] = 1

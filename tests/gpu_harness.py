@@ -138,3 +138,14 @@ def check_routing(gpu, ref, k):
             assert abs(gw[e] - rw[e]) <= 1e-5, (t, e, gw[e], rw[e])
     np.testing.assert_allclose(gpu["probs"], ref["probs"], atol=2e-6, rtol=1e-4)
     return ok
+
+
+def synthetic_routing(rng, T, E, k):
+    """Seeded routing for the cache-decision tests: distinct ids per token, softmax-like probs."""
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    z = rng.standard_normal((T, E)).astype(np.float32) * 2
+    p = np.exp(z - z.max(1, keepdims=True))
+    probs = (p / p.sum(1, keepdims=True)).astype(np.float32)
+    w = np.take_along_axis(probs, ids.astype(np.int64), axis=1)
+    w = (w / w.sum(1, keepdims=True)).astype(np.float32)
+    return ids, w, probs

@@ -55,3 +55,19 @@ def test_record_layout_matches_the_generator():
     for wl in WORKLOADS.values():
         cfg = moe.make_config(wl.L, wl.E, wl.k, wl.H, wl.I, wl.S, wl.weight_dtype, wl.act_dtype)
         assert moe.moe_expert_layout(cfg) == wl.expert_layout(), wl.name
+
+
+def test_noalloc_rejects_misaligned_pointers_before_any_launch():
+    """The router reads x and W_r 16 bytes at a time: a misaligned view must be refused on the host
+    (MOE_ERR_INVALID), never reach a kernel.  The addresses are never dereferenced."""
+    import expert_offload_slot_gb300 as moe
+    lib = moe._lib
+    E, k, H, T = 8, 2, 256, 4
+    good, odd8 = 1 << 20, (1 << 20) + 8
+    args = dict(x=good, wr=good, b=good, ids=good, w=good, probs=good, gap=good)
+    for name, bad in (("x", odd8), ("wr", odd8), ("x", good + 2), ("b", good + 2), ("probs", good + 1)):
+        a = dict(args, **{name: bad})
+        st = lib.moe_route_topk_noalloc(E, k, H, moe.MOE_BF16, moe.MOE_GATE_SOFTMAX_RENORM, a["x"], T, a["wr"],
+                                        a["b"], a["ids"], a["w"], a["probs"], a["gap"], None)
+        assert st == moe.MOE_ERR_INVALID, name
+        assert b"aligned" in lib.moe_last_error()

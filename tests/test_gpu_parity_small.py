@@ -16,7 +16,7 @@ import expert_offload_slot_gb300 as moe
 from oracle.cache import EVICT_CORE, EVICT_LRU, EVICT_MRS, permute
 from synth import gen, get_workload
 from synth.configs import BF16, F32, FP8_E4M3_B128, GATE_SIGMOID_RENORM
-from tests.gpu_harness import Rig, check_output, check_routing, variant
+from tests.gpu_harness import Rig, check_output, check_routing, synthetic_routing, variant
 
 pytestmark = pytest.mark.gpu
 
@@ -88,14 +88,7 @@ def test_bf16_multilayer_trace(gating, policy):
         rig.close()
 
 
-def _synthetic_routing(rng, T, E, k):
-    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
-    z = rng.standard_normal((T, E)).astype(np.float32) * 2
-    p = np.exp(z - z.max(1, keepdims=True))
-    probs = (p / p.sum(1, keepdims=True)).astype(np.float32)
-    w = np.take_along_axis(probs, ids.astype(np.int64), axis=1)
-    w = (w / w.sum(1, keepdims=True)).astype(np.float32)
-    return ids, w, probs
+_synthetic_routing = synthetic_routing
 
 
 @pytest.mark.parametrize("policy", [EVICT_CORE, EVICT_MRS, EVICT_LRU])

@@ -180,16 +180,39 @@ def test_permutation_properties_and_python_sorted():
             assert np.all(np.diff(rows // k) > 0)          # stable: ascending tokens within an expert
 
 
-def test_token_average_is_blocked_in_32s_and_plain_for_short_steps():
+def test_token_average_sums_tokens_in_ascending_order():
+    """s_e(t) is the fp32 sum of the probabilities in ascending token order, / T.
+
+    The values are chosen so that every other order gives another float32:
+    1 followed by 99 copies of 2^-24 rounds back to 1 at every add (a tie to
+    even), while the small values first sum exactly to 99 * 2^-24.
+    """
+    tiny = 2.0 ** -24
+    T = 100
+    # expert 0: the large value first; expert 1: the large value last;
+    # expert 2: every token equal (exact in any order)
+    p = np.zeros((T, 3), np.float32)
+    p[:, 0] = tiny
+    p[0, 0] = 1.0
+    p[:, 1] = tiny
+    p[T - 1, 1] = 1.0
+    p[:, 2] = 0.5
+    sim = SlotPoolSim(L=1, E=3, S=2, policy=EVICT_MRS, window=2)
+    s = sim.update_scores(0, np.zeros((T, 1), np.int64), p)
+    assert s[0] == np.float32(1.0) / np.float32(T)
+    large_last = np.float32(99 * tiny) + np.float32(1.0)     # 99 * 2^-24 is exact in fp32
+    assert large_last == np.float32(1.0 + 50 * 2.0 ** -23)   # 49.5 ulps rounds to even
+    assert s[1] == large_last / np.float32(T)
+    assert s[2] == np.float32(0.5)
+    # a blocked or reversed order would change expert 0: 32-token blocks give
+    # 1 + 68 * 2^-24 before the division
+    assert np.float32(1.0) + np.float32(68 * tiny) != np.float32(1.0)
+
+
+def test_token_average_short_steps_match_float64_mean():
     rng = np.random.default_rng(5)
     for T in (1, 7, 32, 33, 100):
         p = rng.random((T, 6)).astype(np.float32)
         sim = SlotPoolSim(L=1, E=6, S=2, policy=EVICT_MRS, window=2)
         s = sim.update_scores(0, np.zeros((T, 1), np.int64), p)
-        blocks = [p[b:b + 32].astype(np.float64).sum(0) for b in range(0, T, 32)]
-        np.testing.assert_allclose(s, np.sum(blocks, 0) / T, rtol=1e-5)
-        if T <= 32:
-            acc = np.zeros(6, np.float32)
-            for row in p:
-                acc = acc + row
-            np.testing.assert_array_equal(s, acc / np.float32(T))
+        np.testing.assert_allclose(s, p.astype(np.float64).mean(0), rtol=1e-5)
