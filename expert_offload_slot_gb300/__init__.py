@@ -49,6 +49,7 @@ _vp, _i32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
 _P = ctypes.POINTER
 _sig = {
     "moe_expert_layout": (_i32, [_P(moe_config), _P(_sz), _P(_sz), _P(_sz), _P(_sz), _P(_sz)]),
+    "moe_pack_expert_record": (_i32, [_P(moe_config), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz]),
     "moe_host_alloc": (_i32, [_sz, _P(_vp)]),
     "moe_host_free": (_i32, [_vp]),
     "moe_pool_create": (_i32, [_P(moe_config), _vp, _sz, _vp, _vp, _vp, ctypes.c_int, _P(_vp)]),
@@ -126,6 +127,18 @@ def moe_expert_layout(cfg):
     v = [_sz() for _ in range(5)]
     _check(_lib.moe_expert_layout(ctypes.byref(cfg), *[ctypes.byref(x) for x in v]), "moe_expert_layout")
     return tuple(x.value for x in v)   # (w13_off, w2_off, s13_off, s2_off, record_bytes)
+
+
+def moe_pack_expert_record(cfg, w_gate, w_up, w_down, s_gate=None, s_up=None, s_down=None):
+    """One record (uint8 numpy array) from row-major numpy matrices in the weight dtype's storage."""
+    rec = moe_expert_layout(cfg)[4]
+    out = np.zeros(rec, np.uint8)
+    mats = [np.ascontiguousarray(m) for m in (w_gate, w_up, w_down)]
+    scales = [None if v is None else np.ascontiguousarray(v, np.float32) for v in (s_gate, s_up, s_down)]
+    _check(_lib.moe_pack_expert_record(ctypes.byref(cfg), *(m.ctypes.data for m in mats),
+                                       *(None if v is None else v.ctypes.data for v in scales),
+                                       out.ctypes.data, rec), "moe_pack_expert_record")
+    return out
 
 
 MOE_NOALLOC_MAX_LOGITS = 65536

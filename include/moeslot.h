@@ -35,18 +35,39 @@
  *     router and shared-expert weights, x and out.
  *   - A decode call (MOE_MODE_DECODE) performs no host synchronisation and
  *     allocates nothing, so a sequence of such calls can be captured into a
- *     CUDA graph.
+ *     CUDA graph.  MOE_MODE_AUTO on a pool with staging regions does
+ *     synchronise (see moe_forward).
+ *   - Every device-side wait (a copy landing, another CTA's arrival) is
+ *     bounded; one that runs out records MOE_ERR_TIMEOUT, and the kernel
+ *     drains its own copies and returns.
  *   - One pool must not be used from two streams at once: calls on one pool
  *     share its scratch and its table.
  *
- * Expert record (the unit of the host pool, of a slot and of a staging region)
- *   w13  [2I, H] row-major: rows 0..I-1 are W_gate, rows I..2I-1 are W_up
- *   w2   [H, I]  row-major: W_down
- *   s13  [2I/128, H/128] fp32 block scales   (MOE_FP8_E4M3_B128 only)
- *   s2   [H/128, I/128]  fp32 block scales   (MOE_FP8_E4M3_B128 only)
- *   The record is padded to a multiple of 4096 bytes; moe_expert_layout()
- *   returns the offsets.  Element (i, j) of a block-scaled fp8 matrix is
- *   e4m3(q[i,j]) * scale[i/128][j/128].
+ * Expert record (the unit of the host pool, of a slot and of a staging region;
+ * SeqMoE "Mechanism": one fixed-base pool of [num_slots, record] entries).
+ * moe_expert_layout() returns the offsets; moe_pack_expert_record() writes a
+ * record from plain row-major W_gate, W_up, W_down.  The layout depends on
+ * weight_dtype:
+ *   MOE_F32, MOE_FP8_E4M3_B128 (row-major):
+ *     w13  [2I, H]: rows 0..I-1 are W_gate, rows I..2I-1 are W_up
+ *     w2   [H, I]:  W_down
+ *     s13  [2I/128, H/128] fp32 block scales   (MOE_FP8_E4M3_B128 only)
+ *     s2   [H/128, I/128]  fp32 block scales   (MOE_FP8_E4M3_B128 only)
+ *     Element (i, j) of a block-scaled fp8 matrix is e4m3(q[i,j]) * scale[i/128][j/128].
+ *   MOE_BF16 (tiled; NOT row-major): each matrix is cut into tiles of 128 rows
+ *     x 64 columns (16384 bytes; rows and columns past the matrix are zero),
+ *     and inside a tile element (r, c) is at byte
+ *         r*128 + ((c/8) XOR (r mod 8))*16 + (c mod 8)*2
+ *     (the tensor cores' 128-byte-swizzled operand order, so a pipeline stage
+ *     is one contiguous copy).  Tile order:
+ *     w13 at w13_off: tile (m, b, g) of W_gate (g = 0) or W_up (g = 1), rows
+ *         128m.., columns 64b.., at ((m*ceil(H/64) + b)*2 + g) * 16384
+ *     w2 at w2_off:   tile (m, b) of W_down at (m*ceil(I/64) + b) * 16384
+ *     So element (i, j) of W_up is at byte
+ *         w13_off + (((i/128)*ceil(H/64) + j/64)*2 + 1)*16384 + tile byte of (i mod 128, j mod 64).
+ *     A row-major bf16 record gives wrong outputs without any error: pack
+ *     bf16 records with moe_pack_expert_record.
+ *   Every record is padded to a multiple of 4096 bytes.
  */
 #ifndef MOESLOT_H
 #define MOESLOT_H
@@ -71,8 +92,9 @@ typedef enum {
   MOE_ERR_INVALID = 1,    /* bad argument or configuration                      */
   MOE_ERR_OOM = 2,        /* a device allocation failed                         */
   MOE_ERR_CUDA = 3,       /* a CUDA runtime call failed                         */
-  MOE_ERR_CAPACITY = 4,   /* T exceeds the pool's max_tokens                    */
-  MOE_ERR_TIMEOUT = 5,    /* a bounded device-side wait gave up (reserved)      */
+  MOE_ERR_CAPACITY = 4,   /* T exceeds the pool's max_tokens, or a one-step
+                             record / static scratch is too small              */
+  MOE_ERR_TIMEOUT = 5,    /* a bounded device-side wait gave up                 */
   MOE_ERR_TAG = 6,        /* a slot tag did not match (reserved)                */
   MOE_ERR_BOUNDS = 7      /* the device met an expert id or slot out of range   */
 } moe_status;
@@ -114,9 +136,25 @@ typedef struct {   /* cumulative counters of a pool */
 } moe_stats;
 
 /* Byte layout of one expert record for `cfg` (see the header comment).  Any
- * output pointer may be NULL.  Returns MOE_ERR_INVALID for a bad config. */
+ * output pointer may be NULL.  Returns MOE_ERR_INVALID for a bad config.
+ * Host only: no CUDA call. */
 MOE_API moe_status moe_expert_layout(const moe_config* cfg, size_t* w13_off, size_t* w2_off,
                                      size_t* s13_off, size_t* s2_off, size_t* record_bytes);
+
+/* Write one expert's record (the layout of the header comment) from plain
+ * row-major matrices.  Host memory in and out; no CUDA call, no allocation,
+ * safe from any thread.
+ *   w_gate [I, H], w_up [I, H], w_down [H, I]: row-major, elements in the
+ *       storage of cfg->weight_dtype (MOE_F32: float; MOE_BF16: bf16 bit
+ *       patterns, uint16; MOE_FP8_E4M3_B128: e4m3 codes, uint8)
+ *   s_gate [I/128, H/128], s_up [I/128, H/128], s_down [H/128, I/128]: fp32
+ *       block scales, MOE_FP8_E4M3_B128 only (NULL otherwise)
+ *   record: record_bytes >= moe_expert_layout's record_bytes; the padding is
+ *       zeroed.  Host-pool record (l, e) goes to host_pool + (l*E + e)*record_bytes.
+ * MOE_ERR_INVALID for a bad config, a NULL matrix or a short buffer. */
+MOE_API moe_status moe_pack_expert_record(const moe_config* cfg, const void* w_gate, const void* w_up,
+                                          const void* w_down, const float* s_gate, const float* s_up,
+                                          const float* s_down, void* record, size_t record_bytes);
 
 /* Pinned, mapped host memory for a host pool (cudaHostAlloc with the mapped
  * and portable flags).  Blocking.  Free it with moe_host_free. */
@@ -124,7 +162,10 @@ MOE_API moe_status moe_host_alloc(size_t bytes, void** out);
 MOE_API moe_status moe_host_free(void* p);
 
 /* Create a pool on `device`.  Blocking; allocates all device memory the pool
- * will ever use (slots: num_slots records at one fixed base address).
+ * will ever use (slots: num_slots records at one fixed base address —
+ * SeqMoE "Mechanism": a pool of cache slots shared by every MoE layer at a
+ * fixed base, experts kept in pinned, mapped host memory; MoE-CORE
+ * "Mechanism": two layer-sized regions for full-layer prefill).
  *   host_pool       caller-owned pinned host memory (moe_host_alloc, or
  *                   cudaHostAlloc/cudaHostRegister with the mapped flag) holding
  *                   L*E expert records, record (l, e) at (l*E + e)*record_bytes;
@@ -152,7 +193,9 @@ MOE_API moe_status moe_set_lut(moe_pool* pool, const int32_t* lut_host, void* st
 
 /* Host-initiated placement of expert (layer, expert) into `slot`: the slot's
  * occupant is evicted, a previous slot of this expert becomes free, the record
- * is copied by the device-side copy kernel and the slot's tag incremented. */
+ * is copied by the device-side copy kernel and the slot's tag incremented
+ * (SeqMoE "Mechanism": a slot's tag grows with every new occupant, so a copy
+ * into it can be told apart from the next).  Stream-ordered on `stream`. */
 MOE_API moe_status moe_load_slot(moe_pool* pool, int32_t layer, int32_t expert, int32_t slot, void* stream);
 
 /* One MoE layer forward (steps a1..a9, or a10 for a staged prefill).
@@ -163,7 +206,11 @@ MOE_API moe_status moe_load_slot(moe_pool* pool, int32_t layer, int32_t expert, 
  *         region (needs staging_regions == 2); the history is still updated;
  *         MOE_MODE_AUTO: staged when staging_regions == 2 and
  *         T >= floor(K_l / k), K_l being the slots layer l holds now
- *         (MoE-CORE "Mechanism"), else the slot pool path.
+ *         (MoE-CORE "Mechanism"), else the slot pool path.  To count K_l
+ *         the call reads the pool's slot owners back to the host, so AUTO on
+ *         a pool with staging regions SYNCHRONISES the host with the device
+ *         and cannot be captured in a CUDA graph; pass MOE_MODE_DECODE or
+ *         MOE_MODE_PREFILL_STAGED to choose without a synchronisation.
  * A staged call stages layer l (if not already there), then queues layer l+1
  * into the other region (after layer l-1 has released it) ahead of layer l's
  * kernels, so that the copy runs beside them; it synchronises the host with
@@ -181,7 +228,11 @@ MOE_API moe_status moe_forward_routed(moe_pool* pool, int32_t layer, const void*
                                       void* out, void* stream);
 
 /* Step a3 alone: one history/score update of `layer` from device ids [T, k]
- * and device fp32 probs [T, E]. */
+ * and device fp32 probs [T, E] (MoE-CORE "Mechanism": selection count over a
+ * window, EMA of selections, current router score, age since the last
+ * selection; HybriMoE "Mechanism": Minus Recent Score; RapidMoE §4.3: the
+ * router score of a T-token step is the token-averaged probability, summed in
+ * ascending token order).  Stream-ordered; the table is not touched. */
 MOE_API moe_status moe_update_scores(moe_pool* pool, int32_t layer, const int32_t* ids, const float* probs,
                                      int32_t T, void* stream);
 
@@ -190,7 +241,10 @@ MOE_API moe_status moe_update_scores(moe_pool* pool, int32_t layer, const int32_
 MOE_API moe_status moe_get_status(moe_pool* pool);
 MOE_API moe_status moe_clear_status(moe_pool* pool);
 
-/* Blocking: host copies of the last forward's routing (any pointer may be NULL).
+/* Blocking: host copies of the last forward's routing (any pointer may be NULL),
+ * for parity checks: the top-k ids and renormalised weights (RapidMoE §2.1;
+ * CAP §II-A Eq. 1), the full probabilities, the expert_id -> slot_id rewrite
+ * (SeqMoE "Mechanism") and the expert-sorted permutation of token rows.
  *   ids [T,k] int32, w [T,k] fp32, probs [T,E] fp32, gap [T] fp32 (the k-th
  *   minus the (k+1)-th fp32 logit; +inf when k == E or the routing was
  *   supplied), slots [T,k] int32 (slot read; -1 = a one-step copy, -2 = a

@@ -199,3 +199,52 @@ def test_fp8_dense_and_gather_paths_with_shared_expert(T):
         assert rig.pool.status() == moe.MOE_OK
     finally:
         rig.close()
+
+
+@pytest.mark.parametrize("wname", ["qwen3_decode", "dsv3"])
+def test_pool_from_library_packed_records_matches_oracle(wname):
+    """A caller with plain row-major weights packs its host pool with moe_pack_expert_record; the
+    oracle gets the row-major matrices themselves (no record parsing on its side)."""
+    from oracle import layer as olayer
+    from oracle.numerics import decode_act
+    from tests.gpu_harness import act_to_f64, to_device_act
+    wl = variant(get_workload(wname), name=f"packed_{wname}", L=2, E=16, k=4, H=256 if wname != "dsv3" else 512,
+                 I=192 if wname != "dsv3" else 256, residency=0.5, shared=False)
+    cfg = moe.make_config(wl.L, wl.E, wl.k, wl.H, wl.I, wl.S, wl.weight_dtype, wl.act_dtype, wl.gating, False,
+                          wl.evict, wl.window, 0.9, (0.25,) * 4, 0, 16)
+    rec = moe.moe_expert_layout(cfg)[4]
+    host = moe.HostPool(wl.L * wl.E * rec)
+    stored = {}
+    I = wl.I
+    for l in range(wl.L):
+        for e in range(wl.E):
+            st = gen.expert_stored(wl, l, e)
+            stored[l, e] = st
+            kw = {}
+            if "s13" in st:
+                kw = dict(s_gate=st["s13"][:I // 128], s_up=st["s13"][I // 128:], s_down=st["s2"])
+            off = (l * wl.E + e) * rec
+            host.numpy()[off:off + rec] = moe.moe_pack_expert_record(cfg, st["w13"][:I], st["w13"][I:], st["w2"],
+                                                                     **kw)
+    w_r, b = gen.routers(wl)
+    wr_dev = torch.from_numpy(np.ascontiguousarray(w_r.view(np.int16))).cuda()
+    b_dev = torch.from_numpy(b).cuda()
+    pool = moe.Pool(cfg, host.ptr, host.nbytes, wr_dev, b_dev)
+    try:
+        pool.set_lut(gen.initial_lut(wl))
+        for T in (1, 4, 16):
+            for l in range(wl.L):
+                xs = gen.store_act(wl, gen.decode_hidden(wl, l, T, 1)[0])
+                x = to_device_act(wl, xs)
+                out = torch.empty_like(x)
+                pool.forward(l, x, out)
+                torch.cuda.synchronize()
+                xf = decode_act(xs, wl.act_dtype)
+                r = olayer.route(xf, decode_act(w_r[l], wl.act_dtype), b[l], wl.k, wl.gating)
+                ref = olayer.moe_layer(xf, r, lambda e: olayer.expert_mats(stored[l, e], wl.weight_dtype, I), None)
+                ok = check_routing(pool.routing(16), r, wl.k)
+                check_output(wl, act_to_f64(wl, out), ref, ok)
+        assert pool.status() == moe.MOE_OK and pool.stats()["misses"] > 0
+    finally:
+        pool.close()
+        host.free()
