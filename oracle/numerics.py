@@ -28,12 +28,34 @@ def e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
     return np.where(nan, np.nan, val)
 
 
+_E4M3_VALUES = None
+
+
+def e4m3_value_table() -> np.ndarray:
+    """e4m3_to_f64 of every one of the 256 codes, indexed by code."""
+    global _E4M3_VALUES
+    if _E4M3_VALUES is None:
+        _E4M3_VALUES = e4m3_to_f64(np.arange(256, dtype=np.uint8))
+    return _E4M3_VALUES
+
+
 def dequant_fp8_blocks(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
-    """W[i, j] = e4m3(codes[i, j]) * scales[i // 128, j // 128]  (float64, exact)."""
-    w = e4m3_to_f64(codes)
+    """W[i, j] = e4m3(codes[i, j]) * scales[i // 128, j // 128]  (float64, exact).
+
+    Each code is decoded by looking up its value in e4m3_to_f64 of all 256 codes
+    (the same values, without re-evaluating the formula per element); the rows
+    and columns are multiplied by their block's scale.
+    """
+    c = np.asarray(codes, dtype=np.uint8)
+    R, C = c.shape
+    w = e4m3_value_table()[c]
     s = np.asarray(scales, dtype=np.float32).astype(np.float64)
+    if R % 128 == 0 and C % 128 == 0:
+        blocks = w.reshape(R // 128, 128, C // 128, 128)
+        blocks *= s[:, None, :, None]
+        return w
     s_full = np.repeat(np.repeat(s, 128, axis=0), 128, axis=1)
-    return w * s_full[: w.shape[0], : w.shape[1]]
+    return w * s_full[:R, :C]
 
 
 def decode_weight(stored, key: str, dtype: int) -> np.ndarray:
