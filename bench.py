@@ -37,6 +37,13 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+# The CPU oracle's BLAS thread count, fixed before numpy loads: every host core this process may
+# run on, unless the caller set it (the one-thread baseline runs in a child with it set to 1).
+HOST_CORES = len(os.sched_getaffinity(0))
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(HOST_CORES))
+ORACLE_THREADS = int(os.environ["OPENBLAS_NUM_THREADS"])
+
 WORKLOAD_LABEL = {"qwen3_decode": "qwen3-30b-a3b-shaped-decode"}
 
 
@@ -55,10 +62,12 @@ def parse_args():
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: run the workload's layer shape with fewer layers (0 = all)")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--configs", default="qwen3_hit,qwen3_prefill,dsv3,mixtral",
+    ap.add_argument("--configs", default="qwen3_hit,s_independence,qwen3_prefill,dsv3,mixtral",
                     help="other workloads measured at N=1 and reported under 'configs' ('' for none)")
     ap.add_argument("--probe-link", action="store_true",
                     help="measure the host->GPU link: device-started record copies vs DMA, then exit")
+    ap.add_argument("--cpu-sample-only", type=int, default=0,
+                    help="internal: time the oracle on this many layer-steps, print one JSON line, exit")
     return ap.parse_args()
 
 
@@ -260,7 +269,10 @@ class PoolBench:
         import torch
         wl, moe = self.wl, self.moe
         dev = self.device
-        xs = __import__("synth").gen.torch_decode_hidden(wl, T, W + K, dev)
+        # one AR(1) trace: warm-up [0, W), timed [W, W+K), profiling pass after it, then the
+        # end-to-end pass on steps of its own (never a replay of steps the pool has already seen)
+        P = prof_steps if prof_steps > 0 else 0
+        xs = __import__("synth").gen.torch_decode_hidden(wl, T, W + K + P + (K if e2e else 0), dev)
         s = torch.cuda.Stream()
         x_in = torch.empty((wl.L, T, wl.H), dtype=xs.dtype, device=dev)
         out = torch.empty_like(x_in)
@@ -279,29 +291,36 @@ class PoolBench:
         barrier(world)
         torch.cuda.synchronize()
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        nq = 4 if K >= 8 else 1                   # quarters of the timed region, for the spread
+        bounds = [j * K // nq for j in range(nq + 1)]
+        evq = [torch.cuda.Event(enable_timing=True) for _ in range(nq + 1)]
         if clocks:
             clocks.start()
         with torch.cuda.stream(s):
             ev0.record(s)
+            evq[0].record(s)
             for i in range(W, W + K):
                 x_in.copy_(xs[i])
                 g.replay()
+                if i - W + 1 in bounds[1:]:
+                    evq[bounds.index(i - W + 1, 1)].record(s)
             ev1.record(s)
         s.synchronize()
         torch.cuda.synchronize()
         ms = ev0.elapsed_time(ev1)
+        q_ms = [(evq[j].elapsed_time(evq[j + 1]), bounds[j + 1] - bounds[j]) for j in range(nq)]
         clk = clocks.stop() if clocks else None
         barrier(world)
         st1 = self.pool.stats()
-        res = {"T": T, "ms": ms, "steps": K, "launches_per_step": launches_per_step,
+        res = {"T": T, "ms": ms, "steps": K, "launches_per_step": launches_per_step, "quarter_ms": q_ms,
                "hits": st1["hits"] - st0["hits"], "misses": st1["misses"] - st0["misses"],
                "bytes_copied": st1["bytes_copied"] - st0["bytes_copied"], "clocks": clk}
         res["status"] = self.pool.status()
         # profiling pass: per-stage CUDA-event times of every layer, same workload continued
-        res["prof"] = self.profile_decode(xs, x_in, out, s, T, prof_steps) if prof_steps > 0 else \
+        res["prof"] = self.profile_decode(xs[W + K:W + K + P], x_in, out, s, T, prof_steps) if prof_steps > 0 else \
             {"launches": 0, "stage_ms": [0.0] * self.moe.MOE_NUM_STAGES, "sum_U": 0, "T": T, "bytes_copied": 0}
         if e2e:
-            res["e2e"] = self.run_e2e(xs, g, x_in, out, s, W, K)
+            res["e2e"] = self.run_e2e(xs[W + K + P:], g, x_in, out, s, K)
         del g
         return res
 
@@ -373,12 +392,14 @@ class PoolBench:
                 "staged": st1["staged_layers"] - st0["staged_layers"],
                 "prof": {"launches": n, "stage_ms": stage}}
 
-    def run_e2e(self, xs, g, x_in, out, s, W, K):
-        """Same metric through the C ABI with host buffers: H2D of x and D2H of out every step."""
+    def run_e2e(self, xs, g, x_in, out, s, K):
+        """Same metric through the C ABI with host buffers: H2D of x and D2H of out every step, on K
+        steps of the trace that follow every step the pool has run so far."""
         import torch
-        x_host = xs[W:W + K].cpu().pin_memory()
+        x_host = xs[:K].cpu().pin_memory()
         out_host = torch.empty_like(x_host).pin_memory()
         torch.cuda.synchronize()
+        st0 = self.pool.stats()
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(s):
             ev0.record(s)
@@ -389,8 +410,40 @@ class PoolBench:
             ev1.record(s)
         s.synchronize()
         ms = ev0.elapsed_time(ev1)
+        st1 = self.pool.stats()
         nb = x_in.numel() * x_in.element_size()
-        return {"ms": ms, "h2d": nb, "d2h": nb}
+        hits, misses = st1["hits"] - st0["hits"], st1["misses"] - st0["misses"]
+        return {"ms": ms, "h2d": nb, "d2h": nb, "hit_rate": hits / max(1, hits + misses),
+                "misses": misses, "steps": K}
+
+    def decode_repeat(self, T, W, K):
+        """W + K decode steps that all route the same hidden state (one step of the AR(1) trace):
+        after the first step the table holds every expert the step needs, so the timed steps are
+        pure hit-path forwards whatever the slot count."""
+        import torch
+        wl, moe = self.wl, self.moe
+        xs = __import__("synth").gen.torch_decode_hidden(wl, T, 1, self.device)
+        s = torch.cuda.Stream()
+        x_in = xs[0].clone()
+        out = torch.empty_like(x_in)
+        g, _ = self.capture(x_in, out, s)
+        with torch.cuda.stream(s):
+            for _ in range(W):
+                g.replay()
+        s.synchronize()
+        st0 = self.pool.stats()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            ev0.record(s)
+            for _ in range(K):
+                g.replay()
+            ev1.record(s)
+        s.synchronize()
+        st1 = self.pool.stats()
+        del g
+        hits, misses = st1["hits"] - st0["hits"], st1["misses"] - st0["misses"]
+        return {"slots": self.S, "us_per_layer": ev0.elapsed_time(ev1) * 1e3 / (K * wl.L), "steps": K,
+                "hit_rate": hits / max(1, hits + misses), "status": moe_status_name(self.pool.status())}
 
     def close(self, keep_host=False):
         self.pool.close()
@@ -534,6 +587,8 @@ def run_configs(names, dev, qwen_host, args, peaks, link_gbs):
     q = get_workload("qwen3_decode")
     for name in names:
         t0 = time.time()
+        if name not in ("qwen3_hit", "s_independence") and qwen_host is not None and qwen_host.ptr:
+            qwen_host.free()             # the remaining configs bring host pools of their own
         if name == "qwen3_hit":
             # every expert resident (S = L*E): the hit path alone, no miss copies
             b = PoolBench(q, 16, dev, host=qwen_host, slots=q.L * q.E)
@@ -543,18 +598,33 @@ def run_configs(names, dev, qwen_host, args, peaks, link_gbs):
                 res[str(T)] = decode_summary(q, b.decode(T, 8, 64, 8, c, 1, e2e=False), hbm)
             b.close()
             out[name] = {"workload": "qwen3-30b-a3b-shaped-decode, all 6144 experts resident", "decode": res}
+        elif name == "s_independence":
+            # SeqMoE "Mechanism": a slot count above the expert count leaves the fused kernel's latency
+            # unchanged.  Same repeated step (every needed expert resident) at 45 %, 100 % and 200 % of
+            # the L*E experts as slots.
+            res = []
+            for S in (q.S, q.L * q.E, 2 * q.L * q.E):
+                b = PoolBench(q, 16, dev, host=qwen_host, slots=S)
+                res.append(b.decode_repeat(16, 8, 64))
+                b.close()
+            us = [r["us_per_layer"] for r in res]
+            out[name] = {"workload": "qwen3-30b-a3b-shaped-decode, T=16, one step repeated (hit path only)",
+                         "by_slots": res, "max_over_min": max(us) / min(us)}
         elif name == "qwen3_prefill":
             # the decode workload's expert weights and router matrix (same shapes and law) with the
             # prefill router bias 0, so that all 128 experts receive tokens
+            # a fresh host pool of its own: inside one long run the staged copies from the decode
+            # workload's host pool ran at half the link rate, fresh pools at the full rate
             p = dataclasses.replace(get_workload("qwen3_prefill"), name="qwen3_decode")
             pr = get_workload("qwen3_prefill")
-            b = PoolBench(p, max(pr.prefill_T), dev, host=qwen_host, staging=True)
+            b = PoolBench(p, max(pr.prefill_T), dev, staging=True)
             res = {}
             for T in pr.prefill_T:
                 r = b.prefill(T, 3, 3)
                 res[str(T)] = prefill_summary(p, r, distinct_experts_last_call(b, T), hbm, tc, link_gbs)
             b.close()
-            out[name] = {"workload": "qwen3-30b-a3b-shaped-prefill, staged (2 layer-sized regions)", "prefill": res}
+            out[name] = {"workload": "qwen3-30b-a3b-shaped-prefill, staged (2 layer-sized regions), fresh host pool",
+                         "prefill": res}
         elif name in ("dsv3", "mixtral"):
             wl = get_workload(name)
             max_T = max(wl.decode_T + wl.prefill_T)
@@ -624,22 +694,33 @@ class OracleSample:
         return done, el
 
 
-def blas_threads():
-    try:
-        from threadpoolctl import threadpool_info
-        return max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
-    except Exception:
-        return os.cpu_count()
-
-
-def cpu_baseline(wl, T, n_layer_steps, device):
+def oracle_sample(wl, T, n_layer_steps, device):
     n_layers = min(4, wl.L)
     n_steps = (n_layer_steps + n_layers - 1) // n_layers
     o = OracleSample(wl, T, n_layers, n_steps, device)
     done, el = o.run(n_layer_steps)
-    return {"value": done * T / el, "unit": "MoE-layer tokens/s", "cores": blas_threads(), "kind": "oracle",
+    return {"value": done * T / el, "unit": "MoE-layer tokens/s", "threads": ORACLE_THREADS,
+            "us_per_layer": el * 1e6 / done,
             "sample": f"{done} layer-steps (layers 0-{n_layers - 1} x first {n_steps} decode steps, T={T}) "
                       f"of the same workload, numpy float64, {el:.1f} s"}
+
+
+def cpu_baseline(wl, T, n_layer_steps, device, n_single):
+    """The oracle on every host core (BLAS threads = the affinity mask's cores), and on one thread in
+    a child process started with the BLAS thread count set to 1 before numpy loads."""
+    allt = oracle_sample(wl, T, n_layer_steps, device)
+    single = None
+    if n_single > 0:
+        env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-sample-only", str(n_single),
+                            "--batch", str(T), "--workload", wl.name], env=env, capture_output=True, text=True)
+        try:
+            single = json.loads(r.stdout.strip().splitlines()[-1])
+        except (IndexError, ValueError):
+            single = {"error": (r.stderr or r.stdout)[-300:]}
+    return {"value": allt["value"], "unit": allt["unit"], "cores": HOST_CORES, "threads": allt["threads"],
+            "kind": "oracle", "sample": allt["sample"], "us_per_layer": allt["us_per_layer"],
+            "single_thread": single}
 
 
 def probe_link(wl):
@@ -693,6 +774,9 @@ def main():
     if args.layers:
         # a reduced case for profiler captures: same layer shape, fewer layers, same residency
         wl = dataclasses.replace(wl, L=args.layers)
+    if args.cpu_sample_only:
+        print(json.dumps(oracle_sample(wl, args.batch, args.cpu_sample_only, "cuda")))
+        return
     rank, world, local = dist_setup(args.gpus)
     if args.probe_link:
         if rank == 0:
@@ -719,7 +803,8 @@ def main():
                 "ms_per_step": el * 1e3 / done, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "f64", "data": "synthetic (seeded random weights, AR(1) hidden states)",
                 "config": dict(base_cfg, reference_step="one layer-step of the oracle (T tokens, one layer)"),
-                "cpu_baseline": {"value": v, "unit": "MoE-layer tokens/s", "cores": blas_threads(),
+                "cpu_baseline": {"value": v, "unit": "MoE-layer tokens/s", "cores": HOST_CORES,
+                                 "threads": ORACLE_THREADS, "us_per_layer": el * 1e6 / done,
                                  "kind": "oracle", "sample": f"{done} layer-steps of the requested {args.steps}"},
                 "e2e": {"value": v, "unit": "MoE-layer tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
@@ -766,7 +851,7 @@ def main():
     bench.host.free()
     cpu = None
     if not args.no_cpu_baseline:
-        cpu = cpu_baseline(wl, T, args.cpu_sample, dev)
+        cpu = cpu_baseline(wl, T, args.cpu_sample, dev, max(2, args.cpu_sample // 8))
     us_layer = ms * 1e3 / (r["steps"] * wl.L)
     try:
         floor = layer_floor(layer_bytes, r["bytes_copied"] / (r["steps"] * wl.L), us_layer, peak,
@@ -783,7 +868,11 @@ def main():
         "hit_rate": r["hits"] / max(1, r["hits"] + r["misses"]),
         "miss_copy_GB": r["bytes_copied"] / 1e9,
         "e2e": {"value": e2e_value, "unit": "MoE-layer tokens/s",
-                "h2d_bytes_per_step": r.get("e2e", {}).get("h2d"), "d2h_bytes_per_step": r.get("e2e", {}).get("d2h")},
+                "h2d_bytes_per_step": r.get("e2e", {}).get("h2d"), "d2h_bytes_per_step": r.get("e2e", {}).get("d2h"),
+                "hit_rate": r.get("e2e", {}).get("hit_rate"), "misses": r.get("e2e", {}).get("misses"),
+                "steps": "the K decode steps that follow the timed and profiling passes in the same trace"},
+        "spread": {"quarter_tokens_per_s": [n * T * wl.L / (q / 1e3) for q, n in r["quarter_ms"]],
+                   "timed_misses": r["misses"]},
         "roofline": {"bound": "hbm", "kernel": KERNEL_LABEL[fused],
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": captured_traffic(KERNEL_LABEL[fused].split()[0]),

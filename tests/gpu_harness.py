@@ -66,6 +66,7 @@ class Rig:
         self.sim = SlotPoolSim(wl.L, wl.E, self.S, self.policy, self.window, ema, core_w)
         self.sim.set_lut(self.lut0)
         self._mats = {}
+        self._shared = {}
 
     # ------------------------------------------------------------- oracle side
     def stored(self, l, e):
@@ -81,8 +82,11 @@ class Rig:
     def shared_mats(self, l):
         if self.shared_np is None:
             return None
-        st = gen.record_to_stored(self.wl, self.shared_np[l * self.rec:(l + 1) * self.rec])
-        return olayer.expert_mats(st, self.wl.weight_dtype, self.wl.I)
+        key = ("shared", l)
+        if key not in self._shared:
+            st = gen.record_to_stored(self.wl, self.shared_np[l * self.rec:(l + 1) * self.rec])
+            self._shared[key] = olayer.expert_mats(st, self.wl.weight_dtype, self.wl.I)
+        return self._shared[key]
 
     def oracle_forward(self, l, x_stored):
         wl = self.wl
