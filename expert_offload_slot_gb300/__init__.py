@@ -59,6 +59,7 @@ _sig = {
     "moe_forward": (_i32, [_vp, _i32, _vp, _i32, _vp, _i32, _vp]),
     "moe_forward_routed": (_i32, [_vp, _i32, _vp, _i32, _vp, _vp, _vp, _vp, _vp]),
     "moe_update_scores": (_i32, [_vp, _i32, _vp, _vp, _i32, _vp]),
+    "moe_set_wait_limit": (_i32, [_vp, ctypes.c_uint64]),
     "moe_get_status": (_i32, [_vp]),
     "moe_clear_status": (_i32, [_vp]),
     "moe_get_routing": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _P(_i32)]),
@@ -223,6 +224,9 @@ class Pool:
     def update_scores(self, layer, ids, probs, stream=None):
         _check(_lib.moe_update_scores(self.h, layer, _ptr(ids), _ptr(probs), ids.shape[0], _stream(stream)),
                "moe_update_scores")
+
+    def set_wait_limit(self, ns):
+        _check(_lib.moe_set_wait_limit(self.h, int(ns)), "moe_set_wait_limit")
 
     def status(self):
         return _lib.moe_get_status(self.h)

@@ -87,6 +87,8 @@ struct moe_pool {
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
 };
 
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;   // 1 s
+
 static size_t elt_bytes(int dt) { return dt == MOE_F32 ? 4 : dt == MOE_BF16 ? 2 : 1; }
 
 static moe_status check_config(const moe_config* c) {
@@ -280,6 +282,7 @@ MOE_API moe_status moe_pool_create(const moe_config* cfg, const void* host_pool,
   d.cw0 = cfg->core_w[0]; d.cw1 = cfg->core_w[1]; d.cw2 = cfg->core_w[2]; d.cw3 = cfg->core_w[3];
   d.lay = lay;
   d.host_dev = static_cast<const uint8_t*>(hdev);
+  d.wait_ns = kDefaultWaitNs;
 
   const size_t S = d.S, W = d.W, Tm = cfg->max_tokens, k = d.k;
   const size_t rows = Tm * k + Tm;
@@ -650,6 +653,14 @@ MOE_API moe_status moe_update_scores(moe_pool* P, int32_t layer, const int32_t* 
   P->launches += launch_plan(P->d, P->sc, layer, T, ids, nullptr, probs, PLAN_HISTORY, 0, 0,
                              static_cast<cudaStream_t>(stream));
   CUDA_TRY(cudaGetLastError());
+  return MOE_OK;
+}
+
+MOE_API moe_status moe_set_wait_limit(moe_pool* P, uint64_t ns) {
+  if (!P) return fail(MOE_ERR_INVALID, "pool is NULL");
+  if (ns == 0) ns = kDefaultWaitNs;
+  if (ns < 1000ull || ns > 10000000000ull) return fail(MOE_ERR_INVALID, "wait limit must be 1 us .. 10 s (0: default)");
+  P->d.wait_ns = ns;
   return MOE_OK;
 }
 

@@ -232,6 +232,7 @@ struct Args {
   float* partial;
   int32_t* counters;
   int32_t* status;
+  uint64_t wait_ns;          // limit of every wait on another CTA (global-timer ns)
 };
 
 __host__ __device__ constexpr bool is_gate_up(int mode) { return mode == kModeGateUp || mode == kModeGateUpGather; }
@@ -833,15 +834,16 @@ __device__ __forceinline__ void release_add(uint32_t* p) {
   asm volatile("fence.acq_rel.gpu;\n red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p) : "memory");
 }
 
-// Wait until *p >= target (~1 s bound); gives up at once if another CTA has
-// already recorded an error, so one failure cannot chain into many timeouts.
-__device__ __noinline__ bool wait_count(const uint32_t* p, uint32_t target, const int32_t* status) {
+// Wait until *p >= target, for at most limit_ns of global time (1 s unless the
+// pool's wait limit was changed); gives up at once if another CTA has already
+// recorded an error, so one failure cannot chain into many timeouts.
+__device__ __noinline__ bool wait_count(const uint32_t* p, uint32_t target, const int32_t* status, uint64_t limit_ns) {
   const uint64_t t0 = global_ns();
   for (uint32_t it = 0;; ++it) {
     if (ld_acquire(p) >= target) return true;
     if ((it & 15u) == 15u) {
       if (*reinterpret_cast<const volatile int32_t*>(status) != 0) return false;
-      if (global_ns() - t0 > 1000000000ull) return false;
+      if (global_ns() - t0 > limit_ns) return false;
     }
     __nanosleep(64);
   }
@@ -947,7 +949,7 @@ __device__ __noinline__ void copy_records(const Args& a, const FusedArgs& f, uin
     // thread re-reads only what it wrote
     if (!planned) {
       bool ok = true;
-      if (lane == 0) ok = wait_count(f.slots_ready, 1u, a.status);
+      if (lane == 0) ok = wait_count(f.slots_ready, 1u, a.status, a.wait_ns);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) set_status(a.status, MOE_ERR_TIMEOUT);
       planned = ok;
@@ -1067,7 +1069,7 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
     if (unit_n <= k) {
       const uint64_t t0 = global_ns();
       while (unit_n <= k) {
-        if (abort_sh || global_ns() - t0 > 1000000000ull) {
+        if (abort_sh || global_ns() - t0 > a.wait_ns) {
           set_status(a.status, MOE_ERR_TIMEOUT);
           abort_sh = 1;
           return -1;
@@ -1139,7 +1141,7 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
         if (r.miss) {
           // a copied record: every copying CTA's slice of the part this unit reads must
           // have landed (down units too: their weight tiles go out before h is complete)
-          if (!wait_count(r.gu ? &f.jdone[r.li] : &f.jdone_w2[r.li], njd, a.status)) { ok = false; break; }
+          if (!wait_count(r.gu ? &f.jdone[r.li] : &f.jdone_w2[r.li], njd, a.status, a.wait_ns)) { ok = false; break; }
           asm volatile("fence.proxy.async.global;" ::: "memory");   // generic writes -> bulk-copy reads
           // the landing record, or the plan's choice (slot or one-step record)
           rid = f.lp ? f.rid_land0 + r.li : __ldcg(&a.work[r.u].rid);
@@ -1150,7 +1152,7 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
         if (!r.gu && h_ok) asm volatile("fence.proxy.async.global;" ::: "memory");
         int npend = 0;
         auto resolve = [&]() -> bool {
-          if (!wait_count(&f.hready[r.u], (uint32_t)sc.mt_i, a.status)) return false;
+          if (!wait_count(&f.hready[r.u], (uint32_t)sc.mt_i, a.status, a.wait_ns)) return false;
           asm volatile("fence.proxy.async.global;" ::: "memory");   // h written by other CTAs -> TMA reads
           for (int q = 0; q < npend; ++q)
             for (int j = 0; j < pend_nk[q]; ++j)
@@ -1513,7 +1515,7 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
     last_sh = 0;
     if (!abort_sh) {
       release_add(f.dn_done);
-      last_sh = wait_count(f.dn_done, (uint32_t)G, a.status) ? 1 : 0;
+      last_sh = wait_count(f.dn_done, (uint32_t)G, a.status, a.wait_ns) ? 1 : 0;
       if (!last_sh) set_status(a.status, MOE_ERR_TIMEOUT);
     }
   }
@@ -1690,7 +1692,7 @@ __device__ __forceinline__ void stream_ffn(const CUtensorMap* map_w13, const CUt
     if (unit_n <= k) {
       const uint64_t t0 = global_ns();
       while (unit_n <= k) {
-        if (abort_sh || global_ns() - t0 > 1000000000ull) {
+        if (abort_sh || global_ns() - t0 > a.wait_ns) {
           set_status(a.status, MOE_ERR_TIMEOUT);
           abort_sh = 1;
           return kStreamEnd;
@@ -1728,7 +1730,7 @@ __device__ __forceinline__ void stream_ffn(const CUtensorMap* map_w13, const CUt
         const int u = miss ? lp->elist[1][li - nh] : lp->elist[0][li];
         if (miss) {
           // the copied record's gate/up part, written by the copy CTAs
-          if (!wait_count(&f.jdone[li - nh], njd, a.status)) { ok = false; break; }
+          if (!wait_count(&f.jdone[li - nh], njd, a.status, a.wait_ns)) { ok = false; break; }
           asm volatile("fence.proxy.async.global;" ::: "memory");
         }
         publish(npub++, (int)g);
@@ -1751,7 +1753,7 @@ __device__ __forceinline__ void stream_ffn(const CUtensorMap* map_w13, const CUt
         tma_load_4d(ring + (size_t)s * kStreamStage + kStreamHOff, map_h, &full_bar[s], 0, kb0, 0, u);
       };
       auto arrival = [&]() -> bool {
-        if (!wait_count(p1_done, (uint32_t)G * kStreamWarps, a.status)) return false;
+        if (!wait_count(p1_done, (uint32_t)G * kStreamWarps, a.status, a.wait_ns)) return false;
         asm volatile("fence.proxy.async.global;" ::: "memory");   // h written by every CTA -> bulk reads
         h_ok = true;
         for (int q = 0; q < npend; ++q) issue_h(pend_s[q], pend_u[q], pend_kb[q]);
@@ -1768,7 +1770,7 @@ __device__ __forceinline__ void stream_ffn(const CUtensorMap* map_w13, const CUt
             // a copied record's W_down part (it lands after every gate/up part, so the
             // arrival comes first: the stages already issued get their h meanwhile)
             if (!h_ok && npend > 0 && !arrival()) { ok = false; break; }
-            if (!wait_count(&f.jdone_w2[jpos_sh[u]], njd, a.status)) { ok = false; break; }
+            if (!wait_count(&f.jdone_w2[jpos_sh[u]], njd, a.status, a.wait_ns)) { ok = false; break; }
             asm volatile("fence.proxy.async.global;" ::: "memory");
           }
           const int rid = record_of(u);
@@ -2190,7 +2192,7 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
   auto pre = [&]() -> bool {
     // every token gated (and the counters zeroed)
     if (threadIdx.x == 0) {
-      flag_sh = wait_count(route_done, (uint32_t)T + 1u, a.status) ? 1 : 0;
+      flag_sh = wait_count(route_done, (uint32_t)T + 1u, a.status, a.wait_ns) ? 1 : 0;
       if (!flag_sh) set_status(a.status, MOE_ERR_TIMEOUT);
     }
     __syncthreads();
@@ -2261,7 +2263,7 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
     if (!d.local) {
       // the plan's work lists
       if (threadIdx.x == 0) {
-        flag_sh = wait_count(plan_done, 1u, a.status) ? 1 : 0;
+        flag_sh = wait_count(plan_done, 1u, a.status, a.wait_ns) ? 1 : 0;
         if (!flag_sh) set_status(a.status, MOE_ERR_TIMEOUT);
       }
       __syncthreads();
@@ -2638,6 +2640,7 @@ static tc::Args tc_args(const PoolDev& p, const Scratch& sc, int T, int N) {
   a.partial = sc.partial;
   a.counters = sc.ffn_sync;
   a.status = p.status;
+  a.wait_ns = p.wait_ns;
   a.max_split_units = 0;
   return a;
 }

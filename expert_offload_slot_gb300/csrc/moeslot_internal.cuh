@@ -70,6 +70,7 @@ struct PoolDev {           // device-side pointers handed to kernels by value
   int32_t* step;               // [L]
   int32_t* status;             // sticky
   unsigned long long* stats;   // [ST_COUNT]
+  uint64_t wait_ns;            // limit of a kernel's wait on another CTA (global-timer ns)
 };
 
 struct Scratch {

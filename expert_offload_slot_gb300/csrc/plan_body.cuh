@@ -421,13 +421,16 @@ __device__ void plan_body(const PlanArgs& a, uint8_t* dsm, bool prestaged = fals
       __syncthreads();
     }
     if (a.snap_wait) {
-      // the table row may change only once every reader has its copy (bounded wait, ~1 s)
+      // the table row may change only once every reader has its copy (bounded wait: the
+      // pool's wait limit of global time, 1 s by default)
       if (tid == 0) {
-        const uint64_t t0 = clock64();
+        uint64_t t0, now;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
         uint32_t v = 0;
         do {
           asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a.snap_wait) : "memory");
-        } while (v < a.snap_target && clock64() - t0 < 4000000000ull);
+          asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
+        } while (v < a.snap_target && now - t0 < p.wait_ns);
         if (v < a.snap_target) set_status(p.status, MOE_ERR_TIMEOUT);
       }
       __syncthreads();

@@ -236,6 +236,19 @@ MOE_API moe_status moe_forward_routed(moe_pool* pool, int32_t layer, const void*
 MOE_API moe_status moe_update_scores(moe_pool* pool, int32_t layer, const int32_t* ids, const float* probs,
                                      int32_t T, void* stream);
 
+/* Limit of every wait a kernel of this pool makes on another CTA of its grid
+ * (a miss record landing, the routing or the plan being published, a tile's
+ * partial sums, the final arrival before the combine): `ns` nanoseconds of
+ * global time, 1 s by default (ns == 0 restores it); 1 us .. 10 s.  A wait
+ * that runs out records MOE_ERR_TIMEOUT; the kernel then skips its remaining
+ * work, waits for its own copies and tensor-core operations (those waits keep
+ * their 1 s limit), frees its tensor memory and returns.  The output of that
+ * call is undefined and its table changes may not have reached the slots:
+ * after moe_clear_status, moe_set_lut restores a consistent pool.  Host-side
+ * setting; applies to the calls issued after it.  Short limits are for tests
+ * of this path. */
+MOE_API moe_status moe_set_wait_limit(moe_pool* pool, uint64_t ns);
+
 /* Blocking: synchronises the device, returns the sticky device status (MOE_OK
  * if no device-side error was recorded).  moe_clear_status resets it. */
 MOE_API moe_status moe_get_status(moe_pool* pool);
