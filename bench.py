@@ -368,6 +368,7 @@ class PoolBench:
             for l in range(wl.L):
                 self.pool.forward(l, x[l], out[l], moe.MOE_MODE_PREFILL_STAGED, stream=s)
 
+        link_now = {"fresh_buffer_GBps": dma_probe(), "pool_buffer_GBps": dma_probe(self.host)}
         for _ in range(W):
             step()
         s.synchronize()
@@ -388,7 +389,7 @@ class PoolBench:
             s.synchronize()
             n = self._collect(stage, n)
         self.pool.profile_enable(False)
-        return {"T": T, "ms": ms, "steps": K, "status": self.pool.status(),
+        return {"T": T, "ms": ms, "steps": K, "status": self.pool.status(), "link_now": link_now,
                 "staged": st1["staged_layers"] - st0["staged_layers"],
                 "prof": {"launches": n, "stage_ms": stage}}
 
@@ -449,6 +450,26 @@ class PoolBench:
         self.pool.close()
         if self.own_host and not keep_host:
             self.host.free()
+
+
+def dma_probe(host=None, nbytes=1 << 30):
+    """Host -> GPU DMA GB/s of one copy of nbytes: from a freshly pinned buffer, or from the start of
+    an existing host pool."""
+    import torch
+    if host is None:
+        src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    else:
+        nbytes = min(nbytes, host.nbytes)
+        src = host.torch()[:nbytes]
+    dst = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    dst.copy_(src, non_blocking=True)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    dst.copy_(src, non_blocking=True)
+    ev1.record()
+    torch.cuda.synchronize()
+    return nbytes / (ev0.elapsed_time(ev1) / 1e3) / 1e9
 
 
 def expert_bytes(wl):
@@ -564,7 +585,7 @@ def prefill_summary(wl, r, U, hbm_peak, tc_peak, link_gbs):
                        "ffn_gbs": byt / (ffn_us * 1e-6) / 1e9, "ffn_hbm_frac": byt / (ffn_us * 1e-6) / 1e9 / hbm_peak,
                        "flops_per_layer": fl, "bytes_per_layer": byt,
                        "bound": "hbm" if fl / byt < tc_peak * 1e12 / (hbm_peak * 1e9) else "tensor"},
-            "status": moe_status_name(r["status"])}
+            "link_now": r.get("link_now"), "status": moe_status_name(r["status"])}
 
 
 def moe_status_name(st):
