@@ -61,11 +61,17 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: run the workload's layer shape with fewer layers (0 = all)")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="profiling only: the workload's expert shape with this many routed experts (0 = all)")
+    ap.add_argument("--top-k", type=int, default=0, help="profiling only: top-k with --experts (0 = the workload's)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--configs", default="qwen3_hit,s_independence,qwen3_prefill,dsv3,mixtral",
                     help="other workloads measured at N=1 and reported under 'configs' ('' for none)")
     ap.add_argument("--probe-link", action="store_true",
                     help="measure the host->GPU link: device-started record copies vs DMA, then exit")
+    ap.add_argument("--prefill", type=int, default=0,
+                    help="only a staged prefill of this many tokens through the workload's layers (with --layers: "
+                         "fewer layers of the same shape); prints one JSON line of its measurement, then exits")
     ap.add_argument("--cpu-sample-only", type=int, default=0,
                     help="internal: time the oracle on this many layer-steps, print one JSON line, exit")
     return ap.parse_args()
@@ -795,10 +801,26 @@ def main():
     if args.layers:
         # a reduced case for profiler captures: same layer shape, fewer layers, same residency
         wl = dataclasses.replace(wl, L=args.layers)
+    if args.experts:
+        # a reduced case for profiler captures: same expert matrices (H, I, dtype), fewer experts
+        k = args.top_k or min(wl.k, args.experts)
+        wl = dataclasses.replace(wl, E=args.experts, k=k, fixed_slots=0)
     if args.cpu_sample_only:
         print(json.dumps(oracle_sample(wl, args.batch, args.cpu_sample_only, "cuda")))
         return
     rank, world, local = dist_setup(args.gpus)
+    if args.prefill:
+        import expert_offload_slot_gb300 as moe  # noqa: F401  (fails loudly without the library)
+        hbm, _ = load_peaks()
+        # the decode pool is not used by staged calls: one slot per expert at most
+        b = PoolBench(wl, args.prefill, torch.device("cuda", torch.cuda.current_device()), staging=True,
+                      slots=max(1, min(wl.S, wl.E)))
+        r = b.prefill(args.prefill, max(1, args.warmup), max(1, args.steps))
+        out = prefill_summary(wl, r, distinct_experts_last_call(b, args.prefill), hbm, load_tc_peak(), None)
+        b.close()
+        if rank == 0:
+            print(json.dumps(dict(out, workload=wl.name, layers=wl.L)))
+        return
     if args.probe_link:
         if rank == 0:
             print(json.dumps(probe_link(wl)))

@@ -50,6 +50,8 @@ _P = ctypes.POINTER
 _sig = {
     "moe_expert_layout": (_i32, [_P(moe_config), _P(_sz), _P(_sz), _P(_sz), _P(_sz), _P(_sz)]),
     "moe_pack_expert_record": (_i32, [_P(moe_config), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz]),
+    "moe_plan_quotas": (_i32, [_P(moe_config), _vp, _vp, _i32, _i32, _i32, _i32, ctypes.c_double, _vp, _vp]),
+    "moe_profile_lut": (_i32, [_P(moe_config), _vp, _i32, _i32, _vp, _vp]),
     "moe_host_alloc": (_i32, [_sz, _P(_vp)]),
     "moe_host_free": (_i32, [_vp]),
     "moe_pool_create": (_i32, [_P(moe_config), _vp, _sz, _vp, _vp, _vp, ctypes.c_int, _P(_vp)]),
@@ -140,6 +142,30 @@ def moe_pack_expert_record(cfg, w_gate, w_up, w_down, s_gate=None, s_up=None, s_
                                        *(None if v is None else v.ctypes.data for v in scales),
                                        out.ctypes.data, rec), "moe_pack_expert_record")
     return out
+
+
+def moe_plan_quotas(cfg, ids, probs, budget, delta_k, tau_low):
+    """Per-layer slot quotas from a profiling trace (ids int32 [steps,L,T,k], probs float32
+    [steps,L,T,E], host numpy).  Returns (quota int32 [L], hit rate float64 [L])."""
+    ids = np.ascontiguousarray(ids, np.int32)
+    probs = np.ascontiguousarray(probs, np.float32)
+    steps, L, T = ids.shape[:3]
+    quota = np.zeros(L, np.int32)
+    hit = np.zeros(L, np.float64)
+    _check(_lib.moe_plan_quotas(ctypes.byref(cfg), ids.ctypes.data, probs.ctypes.data, steps, T, budget, delta_k,
+                                float(tau_low), quota.ctypes.data, hit.ctypes.data), "moe_plan_quotas")
+    return quota, hit
+
+
+def moe_profile_lut(cfg, probs, quota):
+    """Initial table [L, E] from a profiling trace's probabilities (host numpy) and per-layer quotas."""
+    probs = np.ascontiguousarray(probs, np.float32)
+    steps, L, T, E = probs.shape
+    q = np.ascontiguousarray(quota, np.int32)
+    lut = np.zeros((L, E), np.int32)
+    _check(_lib.moe_profile_lut(ctypes.byref(cfg), probs.ctypes.data, steps, T, q.ctypes.data, lut.ctypes.data),
+           "moe_profile_lut")
+    return lut
 
 
 MOE_NOALLOC_MAX_LOGITS = 65536

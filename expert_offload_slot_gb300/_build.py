@@ -16,9 +16,9 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoeslot.so")
 
-SOURCES = ["api.cu", "pack.cu", "k_route.cu", "k_plan.cu", "k_copy.cu", "k_ffn.cu", "k_noalloc.cu", "k_tc.cu"]
+SOURCES = ["api.cu", "pack.cu", "quota.cu", "k_route.cu", "k_plan.cu", "k_copy.cu", "k_ffn.cu", "k_noalloc.cu", "k_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden", f"-I{INCLUDE}"]
+FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden,-ffp-contract=off", f"-I{INCLUDE}"]
 
 
 def _nvcc():

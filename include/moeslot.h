@@ -299,6 +299,32 @@ enum { MOE_STAGE_ROUTE = 0,     /* router GEMV + gate/top-k                     
 MOE_API moe_status moe_profile_enable(moe_pool* pool, int32_t on);
 MOE_API moe_status moe_profile_read(moe_pool* pool, int32_t layer, float* stage_ms /* [MOE_NUM_STAGES] */);
 
+/* Offline cache shaping (MoE-CORE "Mechanism"): host code only, no CUDA call.
+ * A profiling trace of the routing drives both calls:
+ *   ids    host int32 [steps][L][T][k]   the experts each token selected
+ *   probs  host fp32  [steps][L][T][E]   the router probabilities (as moe_get_routing
+ *                                        returns them)
+ * moe_plan_quotas splits a budget of `budget` slots over the L layers.  Layer l's
+ * hit-rate curve h_l(K) is a replay of its trace through a K-slot cache filled
+ * from the profile (below) with this config's eviction policy, window, EMA rate
+ * and weights; h = hits / needed experts.  It starts from the uniform split
+ * (floor(budget/L), one more for the first budget mod L layers, at most E) and
+ * then moves delta_k slots at a time from the donor (hit rate still >= the median
+ * after shrinking, at least one slot left; the smallest drop) to the receiver (hit
+ * rate <= median - tau_low, at most E slots; the largest gain), ties to the lower
+ * layer, as long as the gain exceeds the drop.  quota [L] receives the slot
+ * counts, hit [L] (or NULL) h_l at them.
+ * moe_profile_lut writes the initial table lut [L*E] for moe_set_lut: layer l's
+ * quota[l] experts of highest mean probability over the trace (ties to the lower
+ * id), slots numbered layer by layer in that order; the quotas must sum to at
+ * most cfg->num_slots.
+ * MOE_ERR_INVALID for a bad config or trace (an id outside 0..E-1). */
+MOE_API moe_status moe_plan_quotas(const moe_config* cfg, const int32_t* ids, const float* probs, int32_t steps,
+                                   int32_t T, int32_t budget, int32_t delta_k, double tau_low, int32_t* quota,
+                                   double* hit);
+MOE_API moe_status moe_profile_lut(const moe_config* cfg, const float* probs, int32_t steps, int32_t T,
+                                   const int32_t* quota, int32_t* lut);
+
 /* Router projection + gate/top-k (steps a1, a2) with no device allocation.
  * The pages have no counterpart: this exists for callers that cannot call
  * cudaMalloc where they route tokens — code running while a CUDA graph is
