@@ -65,7 +65,7 @@ def parse_args():
                     help="profiling only: the workload's expert shape with this many routed experts (0 = all)")
     ap.add_argument("--top-k", type=int, default=0, help="profiling only: top-k with --experts (0 = the workload's)")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--configs", default="qwen3_hit,s_independence,qwen3_prefill,dsv3,mixtral",
+    ap.add_argument("--configs", default="qwen3_hit,s_independence,prefetch,quotas,qwen3_prefill,dsv3,mixtral",
                     help="other workloads measured at N=1 and reported under 'configs' ('' for none)")
     ap.add_argument("--probe-link", action="store_true",
                     help="measure the host->GPU link: device-started record copies vs DMA, then exit")
@@ -232,7 +232,7 @@ class PoolBench:
     all-resident hit path).  staging adds the two layer-sized prefill regions.
     """
 
-    def __init__(self, wl, max_T, device, host=None, slots=None, staging=False):
+    def __init__(self, wl, max_T, device, host=None, slots=None, staging=False, lut=None):
         import numpy as np
         import torch
 
@@ -257,7 +257,7 @@ class PoolBench:
         self.shared = torch.from_numpy(gen.shared_records(wl)).to(device) if wl.shared else None
         self.pool = moe.Pool(self.cfg, self.host.ptr, self.host.nbytes, self.w_r, self.b, self.shared,
                              device=torch.cuda.current_device())
-        self.pool.set_lut(gen.initial_lut(wl, S=self.S))
+        self.pool.set_lut(gen.initial_lut(wl, S=self.S) if lut is None else lut)
         torch.cuda.synchronize()
         self.setup_s = time.time() - t0
 
@@ -320,7 +320,9 @@ class PoolBench:
         st1 = self.pool.stats()
         res = {"T": T, "ms": ms, "steps": K, "launches_per_step": launches_per_step, "quarter_ms": q_ms,
                "hits": st1["hits"] - st0["hits"], "misses": st1["misses"] - st0["misses"],
-               "bytes_copied": st1["bytes_copied"] - st0["bytes_copied"], "clocks": clk}
+               "bytes_copied": st1["bytes_copied"] - st0["bytes_copied"], "clocks": clk,
+               "prefetch": {n: st1["prefetch_" + n] - st0["prefetch_" + n]
+                            for n in ("issued", "committed", "demanded", "bytes")}}
         res["status"] = self.pool.status()
         # profiling pass: per-stage CUDA-event times of every layer, same workload continued
         res["prof"] = self.profile_decode(xs[W + K:W + K + P], x_in, out, s, T, prof_steps) if prof_steps > 0 else \
@@ -543,6 +545,21 @@ def prefill_flops(wl, T):
     return f
 
 
+def prefetch_summary(wl, r, base=None):
+    """Per layer-step: demand misses, prefetches issued / committed / demanded before their commit,
+    and the bytes over the host link (demand copies + prefetch copies), next to tokens/s."""
+    n = r["steps"] * wl.L
+    pf = r["prefetch"]
+    out = {"tokens_per_s": r["steps"] * r["T"] * wl.L / (r["ms"] / 1e3), "us_per_layer": r["ms"] * 1e3 / n,
+           "hit_rate": r["hits"] / max(1, r["hits"] + r["misses"]), "demand_misses_per_layer_step": r["misses"] / n,
+           "prefetch_issued_per_layer_step": pf["issued"] / n, "prefetch_committed_per_layer_step": pf["committed"] / n,
+           "prefetch_demanded_per_layer_step": pf["demanded"] / n,
+           "link_MB_per_layer_step": (r["bytes_copied"] + pf["bytes"]) / 1e6 / n, "status": moe_status_name(r["status"])}
+    if base is not None:
+        out["vs_no_prefetch"] = out["tokens_per_s"] / base["tokens_per_s"]
+    return out
+
+
 def decode_summary(wl, r, peak):
     """Per-config decode line: tokens/s, us/layer, hit rate, per-stage us, FFN-kernel HBM roofline."""
     import expert_offload_slot_gb300 as moe
@@ -604,6 +621,31 @@ def distinct_experts_last_call(bench, T):
     return int(len(set(int(v) for v in r["ids"].reshape(-1))))
 
 
+def profile_trace(wl, T, steps, dev):
+    """A profiling trace of the decode workload's routing (steps of its AR(1) hidden states drawn
+    with another seed), routed on the GPU by moe_route_topk_noalloc: ids [steps, L, T, k] int32 and
+    probs [steps, L, T, E] float32 on the host."""
+    import numpy as np
+    import torch
+
+    import expert_offload_slot_gb300 as moe
+    from synth import gen
+    xs = gen.torch_decode_hidden(wl, T, steps, dev, base_seed=1)
+    w_r, b = gen.routers(wl)
+    wr = torch.from_numpy(np.ascontiguousarray(w_r.view(np.int16))).to(dev)
+    bd = torch.from_numpy(b).to(dev)
+    ids = torch.empty((steps, wl.L, T, wl.k), dtype=torch.int32, device=dev)
+    probs = torch.empty((steps, wl.L, T, wl.E), dtype=torch.float32, device=dev)
+    w = torch.empty((T, wl.k), dtype=torch.float32, device=dev)
+    gap = torch.empty(T, dtype=torch.float32, device=dev)
+    for st in range(steps):
+        for l in range(wl.L):
+            moe.moe_route_topk_noalloc(wl.E, wl.k, wl.H, wl.act_dtype, wl.gating, xs[st, l].view(torch.int16), wr[l],
+                                       bd[l], ids[st, l], w, probs[st, l], gap)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy(), probs.cpu().numpy()
+
+
 def run_configs(names, dev, qwen_host, args, peaks, link_gbs):
     """The other workload shapes at one GPU, each pool built, measured and freed in turn."""
     import dataclasses
@@ -614,7 +656,7 @@ def run_configs(names, dev, qwen_host, args, peaks, link_gbs):
     q = get_workload("qwen3_decode")
     for name in names:
         t0 = time.time()
-        if name not in ("qwen3_hit", "s_independence") and qwen_host is not None and qwen_host.ptr:
+        if name not in ("qwen3_hit", "s_independence", "quotas", "prefetch") and qwen_host is not None and qwen_host.ptr:
             qwen_host.free()             # the remaining configs bring host pools of their own
         if name == "qwen3_hit":
             # every expert resident (S = L*E): the hit path alone, no miss copies
@@ -637,6 +679,47 @@ def run_configs(names, dev, qwen_host, args, peaks, link_gbs):
             us = [r["us_per_layer"] for r in res]
             out[name] = {"workload": "qwen3-30b-a3b-shaped-decode, T=16, one step repeated (hit path only)",
                          "by_slots": res, "max_over_min": max(us) / min(us)}
+        elif name == "prefetch":
+            # SeqMoE asynchronous prefetch: the headline decode (T = 16) without prefetch, then with one
+            # and two prefetches per layer-step (each pool fresh from the same table and trace)
+            res = {}
+            base = None
+            for per in (0, 1, 2):
+                b = PoolBench(q, 16, dev, host=qwen_host)
+                b.pool.prefetch_enable(per)
+                r = b.decode(16, 8, 64, 0, Clocks(torch_local()), 1, e2e=False)
+                b.close()
+                res[str(per)] = prefetch_summary(q, r, base)
+                if per == 0:
+                    base = res["0"]
+            out[name] = {"workload": "qwen3-30b-a3b-shaped-decode, T=16, 2765 slots, MRS; per_step 0 / 1 / 2",
+                         "by_per_step": res}
+        elif name == "quotas":
+            # MoE-CORE cache shaping: the headline decode (T = 16, 2765 slots) with the table filled
+            # from a profiling trace, uniform quotas and the replayed nonuniform ones
+            import numpy as np
+
+            import expert_offload_slot_gb300 as moe
+            ids, probs = profile_trace(q, 16, 64, dev)
+            cfg = moe.make_config(q.L, q.E, q.k, q.H, q.I, q.S, q.weight_dtype, q.act_dtype, q.gating, False,
+                                  q.evict, q.window)
+            uniform = np.array([q.quota(l) for l in range(q.L)], np.int32)
+            t_plan = time.time()
+            planned, hit = moe.moe_plan_quotas(cfg, ids, probs, q.S, 4, 0.01)
+            t_plan = time.time() - t_plan
+            res = {}
+            for label, quotas in (("uniform_profile_fill", uniform), ("planned_profile_fill", planned)):
+                b = PoolBench(q, 16, dev, host=qwen_host, lut=moe.moe_profile_lut(cfg, probs, quotas))
+                r = decode_summary(q, b.decode(16, 8, 64, 8, Clocks(torch_local()), 1, e2e=False), hbm)
+                b.close()
+                res[label] = {"tokens_per_s": r["tokens_per_s"], "us_per_layer": r["us_per_layer"],
+                              "hit_rate": r["hit_rate"], "quota_min": int(quotas.min()), "quota_max": int(quotas.max())}
+            out[name] = {"workload": "qwen3-30b-a3b-shaped-decode, T=16, 2765 slots; profile: 64 steps of another "
+                                     "seed routed by moe_route_topk_noalloc",
+                         "plan": {"delta_k": 4, "tau_low": 0.01, "replayed_hit_rate_min": float(hit.min()),
+                                  "replayed_hit_rate_max": float(hit.max()), "layers_changed":
+                                  int((planned != uniform).sum()), "seconds": t_plan},
+                         "decode": res}
         elif name == "qwen3_prefill":
             # the decode workload's expert weights and router matrix (same shapes and law) with the
             # prefill router bias 0, so that all 128 experts receive tokens
@@ -660,6 +743,16 @@ def run_configs(names, dev, qwen_host, args, peaks, link_gbs):
             for T in wl.decode_T:
                 K = 32 if name == "dsv3" else 24
                 dec[str(T)] = decode_summary(wl, b.decode(T, 3, K, 4, Clocks(torch_local()), 1, e2e=False), hbm)
+            pf = None
+            if name == "mixtral":
+                # the link-bound decode with one prefetch per layer-step (same pool, continued trace)
+                r0 = b.decode(1, 3, 24, 0, None, 1, e2e=False)
+                b.pool.prefetch_enable(1)
+                r1 = b.decode(1, 3, 24, 0, None, 1, e2e=False)
+                b.pool.prefetch_enable(0)
+                b.pool.prefetch_drain()
+                base = prefetch_summary(wl, r0)
+                pf = {"0": base, "1": prefetch_summary(wl, r1, base)}
             pre = {}
             for T in wl.prefill_T:
                 r = b.prefill(T, 3, 3)
@@ -668,6 +761,8 @@ def run_configs(names, dev, qwen_host, args, peaks, link_gbs):
             lbl = {"dsv3": "deepseek-v3-shaped (fp8 e4m3, 128x128 block scales, shared expert, MRS eviction)",
                    "mixtral": "mixtral-8x7b-shaped (64 slots, MRS eviction)"}[name]
             out[name] = {"workload": lbl, "layers": wl.L, "slots": wl.S, "decode": dec, "prefill": pre}
+            if pf:
+                out[name]["decode_prefetch_T1"] = pf
         out[name]["seconds"] = time.time() - t0
     return out
 

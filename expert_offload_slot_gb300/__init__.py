@@ -42,7 +42,8 @@ class moe_config(ctypes.Structure):
 
 class moe_stats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in ("steps", "hits", "misses", "bypass", "evictions",
-                                               "bytes_copied", "near_ties", "staged_layers")]
+                                               "bytes_copied", "near_ties", "staged_layers", "prefetch_issued",
+                                               "prefetch_committed", "prefetch_demanded", "prefetch_bytes")]
 
 
 _vp, _i32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
@@ -62,6 +63,9 @@ _sig = {
     "moe_forward_routed": (_i32, [_vp, _i32, _vp, _i32, _vp, _vp, _vp, _vp, _vp]),
     "moe_update_scores": (_i32, [_vp, _i32, _vp, _vp, _i32, _vp]),
     "moe_set_wait_limit": (_i32, [_vp, ctypes.c_uint64]),
+    "moe_prefetch_enable": (_i32, [_vp, _i32]),
+    "moe_prefetch_drain": (_i32, [_vp]),
+    "moe_prefetch_inject_wrong_tags": (_i32, [_vp, ctypes.c_uint32]),
     "moe_get_status": (_i32, [_vp]),
     "moe_clear_status": (_i32, [_vp]),
     "moe_get_routing": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _P(_i32)]),
@@ -250,6 +254,15 @@ class Pool:
     def update_scores(self, layer, ids, probs, stream=None):
         _check(_lib.moe_update_scores(self.h, layer, _ptr(ids), _ptr(probs), ids.shape[0], _stream(stream)),
                "moe_update_scores")
+
+    def prefetch_enable(self, per_step):
+        _check(_lib.moe_prefetch_enable(self.h, int(per_step)), "moe_prefetch_enable")
+
+    def prefetch_drain(self):
+        _check(_lib.moe_prefetch_drain(self.h), "moe_prefetch_drain")
+
+    def prefetch_inject_wrong_tags(self, n):
+        _check(_lib.moe_prefetch_inject_wrong_tags(self.h, int(n)), "moe_prefetch_inject_wrong_tags")
 
     def set_wait_limit(self, ns):
         _check(_lib.moe_set_wait_limit(self.h, int(ns)), "moe_set_wait_limit")

@@ -11,11 +11,14 @@
 // Staged prefill (MoE-CORE "Mechanism"): two staging regions, each one whole
 // MoE layer; layer l reads region l mod 2; while it computes, the other region
 // receives layer l+1 on the pool's copy stream (once layer l-1 has released it).
+#include <atomic>
+#include <chrono>
 #include <cstdarg>
 #include <cstdio>
 #include <algorithm>
 #include <cstring>
 #include <string>
+#include <thread>
 #include <vector>
 
 #include "moeslot_internal.cuh"
@@ -85,6 +88,15 @@ struct moe_pool {
   TcMaps* tc_maps = nullptr;          // tensor maps of the record array (bf16 weights)
   cudaStream_t side = nullptr;        // miss copies run here, beside gate/up over resident experts
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  // asynchronous prefetch: the mapped control region, the host thread and its stream
+  PfCtl* pf_ctl = nullptr;            // host view
+  uint32_t* pf_tagbuf = nullptr;      // pinned: the tags the thread writes back, [kPfRing]
+  cudaStream_t pf_stream = nullptr;
+  std::thread pf_thread;
+  std::atomic<bool> pf_stop{false};
+  std::atomic<uint32_t> pf_taken{0};  // requests the thread has enqueued
+  std::atomic<uint32_t> pf_corrupt{0};
+  std::atomic<uint64_t> pf_bytes{0};
 };
 
 constexpr uint64_t kDefaultWaitNs = 1000000000ull;   // 1 s
@@ -213,7 +225,19 @@ static moe_status palloc(moe_pool* P, T** out, size_t count, int fill_byte) {
   return MOE_OK;
 }
 
+static void prefetch_stop(moe_pool* P) {
+  if (P->pf_thread.joinable()) {
+    P->pf_stop.store(true);
+    P->pf_thread.join();
+  }
+}
+
 static void pool_free_all(moe_pool* P) {
+  prefetch_stop(P);
+  if (P->pf_stream) cudaStreamSynchronize(P->pf_stream);
+  if (P->pf_stream) cudaStreamDestroy(P->pf_stream);
+  if (P->pf_ctl) cudaFreeHost(P->pf_ctl);
+  if (P->pf_tagbuf) cudaFreeHost(P->pf_tagbuf);
   if (P->tc_maps) tc_maps_destroy(P->tc_maps);
   P->tc_maps = nullptr;
   for (void* p : P->allocs) cudaFree(p);
@@ -326,6 +350,19 @@ MOE_API moe_status moe_pool_create(const moe_config* cfg, const void* host_pool,
   PA(d.step, L, 0);
   PA(d.status, 1, 0);
   PA(d.stats, ST_COUNT, 0);
+  {
+    int32_t* pe = nullptr;
+    uint32_t* ld = nullptr;
+    PA(pe, S, 0xff);
+    d.pf_expert = pe;
+    PA(d.pf_slot, L * E, 0xff);
+    PA(d.pf_tag, S, 0);
+    PA(ld, S, 0);
+    d.landed = ld;
+    PA(d.pf_list, kPfMaxPending, 0);
+    PA(d.pf_n, 1, 0);
+    PA(d.pf_head, 1, 0);
+  }
   P->sc.tmax = (int32_t)Tm;
   PA(P->sc.logits, Tm * E, 0);
   PA(P->sc.probs, Tm * E, 0);
@@ -436,6 +473,16 @@ MOE_API moe_status moe_set_lut(moe_pool* P, const int32_t* lut_host, void* strea
   CUDA_TRY(cudaSetDevice(P->device));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   CUDA_TRY(cudaStreamSynchronize(s));
+  if (P->d.pf_used) {
+    // every prefetch copy lands before the slots are refilled; no slot stays pending
+    moe_status st = moe_prefetch_drain(P);
+    if (st != MOE_OK) return st;
+    CUDA_TRY(cudaMemset(P->d.pf_expert, 0xff, sizeof(int32_t) * S));
+    CUDA_TRY(cudaMemset(P->d.pf_slot, 0xff, sizeof(int32_t) * L * E));
+    CUDA_TRY(cudaMemset(P->d.pf_n, 0, sizeof(int32_t)));
+    CUDA_TRY(cudaMemcpy(const_cast<uint32_t*>(P->d.landed), P->d.pf_tag, sizeof(uint32_t) * S,
+                        cudaMemcpyDeviceToDevice));
+  }
   CUDA_TRY(cudaMemcpy(P->d.lut, lut_host, sizeof(int32_t) * L * E, cudaMemcpyHostToDevice));
   CUDA_TRY(cudaMemcpy(P->d.owner, owner.data(), sizeof(int32_t) * S, cudaMemcpyHostToDevice));
   P->launches += launch_rebuild_owner(P->d, s);
@@ -453,6 +500,7 @@ MOE_API moe_status moe_load_slot(moe_pool* P, int32_t layer, int32_t expert, int
   if (!P) return fail(MOE_ERR_INVALID, "pool is NULL");
   if (layer < 0 || layer >= P->d.L || expert < 0 || expert >= P->d.E || slot < 0 || slot >= P->d.S)
     return fail(MOE_ERR_INVALID, "moe_load_slot: layer/expert/slot out of range");
+  if (P->d.pf_used) return fail(MOE_ERR_INVALID, "moe_load_slot: not available on a pool that has used prefetch");
   CUDA_TRY(cudaSetDevice(P->device));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   P->launches += launch_load_slot(P->d, P->sc, layer, expert, slot, s);
@@ -656,6 +704,111 @@ MOE_API moe_status moe_update_scores(moe_pool* P, int32_t layer, const int32_t* 
   return MOE_OK;
 }
 
+// ---------------------------------------------------------------- asynchronous prefetch
+// The pool's only host thread (SeqMoE "Mechanism"): it polls the mapped control region,
+// takes the device's requests in order and, on a stream of its own that no compute waits
+// for, copies each record from the host pool into its slot and then writes the request's
+// tag into landed[slot]; the device commits the slot only when that tag matches its own.
+// It also reads the GPU's position and miss flag: when the layer call now running has
+// demand misses (their copies use the same link), it holds the next prefetch back until
+// the position moves on, for at most one record's copy time.
+static void prefetch_main(moe_pool* P) {
+  cudaSetDevice(P->device);
+  PfCtl* c = P->pf_ctl;
+  const size_t rec = P->d.lay.rec;
+  const auto defer = std::chrono::nanoseconds((long long)(rec / 200.0));   // ~200 GB/s host link
+  uint32_t tail = P->pf_taken.load(), inflight = 0, seen_demand = c->demand;
+  while (!P->pf_stop.load()) {
+    const uint32_t head = c->head;
+    if (head == tail) {
+      std::this_thread::sleep_for(std::chrono::microseconds(2));
+      continue;
+    }
+    std::atomic_thread_fence(std::memory_order_acquire);   // the requests were written before the head
+    const uint32_t dm = c->demand;
+    if (dm != seen_demand) {
+      seen_demand = dm;
+      const int32_t l0 = c->layer, s0 = c->step;
+      const auto t0 = std::chrono::steady_clock::now();
+      while (c->layer == l0 && c->step == s0 && std::chrono::steady_clock::now() - t0 < defer &&
+             !P->pf_stop.load())
+        std::this_thread::sleep_for(std::chrono::microseconds(2));
+    }
+    const volatile PfReq& q = c->req[tail % kPfRing];
+    const int32_t slot = q.slot, flat = q.flat;
+    uint32_t tag = q.tag;
+    uint32_t bad = P->pf_corrupt.load();
+    while (bad > 0 && !P->pf_corrupt.compare_exchange_weak(bad, bad - 1)) {
+    }
+    if (bad > 0) tag += 0x5A5A0000u;   // a wrong tag (test injection): the device must not commit it
+    if (inflight >= kPfRing / 2) {     // the tag buffer entry about to be reused has been read
+      cudaStreamSynchronize(P->pf_stream);
+      inflight = 0;
+    }
+    uint32_t* tb = P->pf_tagbuf + (tail % kPfRing);
+    *tb = tag;
+    if (slot >= 0 && slot < P->d.S && flat >= 0 && flat < P->d.L * P->d.E) {
+      cudaMemcpyAsync(P->d.records + (size_t)slot * rec, P->host_pool + (size_t)flat * rec, rec,
+                      cudaMemcpyHostToDevice, P->pf_stream);
+      cudaMemcpyAsync(const_cast<uint32_t*>(P->d.landed) + slot, tb, sizeof(uint32_t), cudaMemcpyHostToDevice,
+                      P->pf_stream);
+      P->pf_bytes.fetch_add(rec);
+      ++inflight;
+    }
+    ++tail;
+    c->tail = tail;
+    P->pf_taken.store(tail);
+  }
+}
+
+MOE_API moe_status moe_prefetch_enable(moe_pool* P, int32_t per_step) {
+  if (!P) return fail(MOE_ERR_INVALID, "pool is NULL");
+  if (per_step < 0 || per_step > kPfMaxPerStep) return fail(MOE_ERR_INVALID, "per_step must be 0..%d", kPfMaxPerStep);
+  CUDA_TRY(cudaSetDevice(P->device));
+  if (per_step > 0 && !P->pf_ctl) {
+    void* c = nullptr;
+    void* dc = nullptr;
+    CUDA_TRY(cudaHostAlloc(&c, sizeof(PfCtl), cudaHostAllocMapped | cudaHostAllocPortable));
+    std::memset(c, 0, sizeof(PfCtl));
+    P->pf_ctl = static_cast<PfCtl*>(c);
+    CUDA_TRY(cudaHostGetDevicePointer(&dc, c, 0));
+    void* tb = nullptr;
+    CUDA_TRY(cudaHostAlloc(&tb, sizeof(uint32_t) * kPfRing, cudaHostAllocPortable));
+    P->pf_tagbuf = static_cast<uint32_t*>(tb);
+    CUDA_TRY(cudaStreamCreateWithFlags(&P->pf_stream, cudaStreamNonBlocking));
+    P->d.pf_ctl = static_cast<PfCtl*>(dc);
+    P->d.pf_used = 1;
+  }
+  if (per_step > 0 && !P->pf_thread.joinable()) {
+    P->pf_stop.store(false);
+    P->pf_thread = std::thread(prefetch_main, P);
+  }
+  P->d.pf_per_step = per_step;
+  return MOE_OK;
+}
+
+MOE_API moe_status moe_prefetch_drain(moe_pool* P) {
+  if (!P) return fail(MOE_ERR_INVALID, "pool is NULL");
+  if (!P->pf_ctl) return MOE_OK;
+  CUDA_TRY(cudaSetDevice(P->device));
+  CUDA_TRY(cudaDeviceSynchronize());               // every plan that may write a request has run
+  const uint32_t head = P->pf_ctl->head;
+  const auto t0 = std::chrono::steady_clock::now();
+  while (P->pf_taken.load() - head > 0x7fffffffu) {  // taken < head (wrapping)
+    if (!P->pf_thread.joinable() || std::chrono::steady_clock::now() - t0 > std::chrono::seconds(10))
+      return fail(MOE_ERR_TIMEOUT, "moe_prefetch_drain: the prefetch thread did not take the requests");
+    std::this_thread::sleep_for(std::chrono::microseconds(20));
+  }
+  CUDA_TRY(cudaStreamSynchronize(P->pf_stream));
+  return MOE_OK;
+}
+
+MOE_API moe_status moe_prefetch_inject_wrong_tags(moe_pool* P, uint32_t n) {
+  if (!P) return fail(MOE_ERR_INVALID, "pool is NULL");
+  P->pf_corrupt.fetch_add(n);
+  return MOE_OK;
+}
+
 MOE_API moe_status moe_set_wait_limit(moe_pool* P, uint64_t ns) {
   if (!P) return fail(MOE_ERR_INVALID, "pool is NULL");
   if (ns == 0) ns = kDefaultWaitNs;
@@ -744,6 +897,10 @@ MOE_API moe_status moe_get_stats(moe_pool* P, moe_stats* out) {
   out->bytes_copied = v[ST_BYTES];
   out->near_ties = v[ST_NEAR_TIES];
   out->staged_layers = P->staged_count;
+  out->prefetch_issued = v[ST_PF_ISSUED];
+  out->prefetch_committed = v[ST_PF_COMMITTED];
+  out->prefetch_demanded = v[ST_PF_DEMANDED];
+  out->prefetch_bytes = P->pf_bytes.load();
   return MOE_OK;
 }
 

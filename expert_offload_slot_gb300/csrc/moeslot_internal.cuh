@@ -28,7 +28,31 @@ struct CopyJob {
 };
 
 enum StatIdx {
-  ST_STEPS = 0, ST_HITS, ST_MISSES, ST_BYPASS, ST_EVICT, ST_BYTES, ST_NEAR_TIES, ST_STAGED, ST_COUNT
+  ST_STEPS = 0, ST_HITS, ST_MISSES, ST_BYPASS, ST_EVICT, ST_BYTES, ST_NEAR_TIES, ST_STAGED,
+  ST_PF_ISSUED, ST_PF_COMMITTED, ST_PF_DEMANDED, ST_COUNT
+};
+
+// Asynchronous prefetch (SeqMoE "Mechanism"): the control region in pinned, mapped host
+// memory.  The device writes requests and its position; the pool's host thread takes the
+// requests in order, copies each record into its slot on a stream of its own, and then
+// writes the request's tag into the pool's landed[slot] (device memory), in stream order.
+constexpr int kPfRing = 256;              // requests the ring holds
+constexpr int kPfMaxPending = 256;        // slots pending at once
+constexpr int kPfMaxPerStep = 8;
+struct PfReq {
+  int32_t slot;
+  int32_t flat;        // l * E + e
+  uint32_t tag;
+  int32_t pad;
+};
+struct PfCtl {
+  volatile uint32_t head;     // requests written by the device
+  volatile uint32_t tail;     // requests taken by the host thread
+  volatile int32_t layer;     // GPU position: the last layer call that planned ...
+  volatile int32_t step;      // ... and that layer's step
+  volatile uint32_t demand;   // miss flag: bumped by every layer call with demand misses
+  volatile uint32_t pad[3];
+  PfReq req[kPfRing];
 };
 
 // Plan-kernel switches.
@@ -71,6 +95,17 @@ struct PoolDev {           // device-side pointers handed to kernels by value
   int32_t* status;             // sticky
   unsigned long long* stats;   // [ST_COUNT]
   uint64_t wait_ns;            // limit of a kernel's wait on another CTA (global-timer ns)
+  // asynchronous prefetch: pf_used once it was ever enabled (pending slots are handled from
+  // then on); pf_per_step > 0 while the plans issue requests
+  int32_t pf_used, pf_per_step;
+  int32_t* pf_expert;          // [S] l*E+e whose prefetch the slot holds (owner -2), or -1
+  int32_t* pf_slot;            // [L*E] slot of the expert's pending prefetch, or -1
+  uint32_t* pf_tag;            // [S] tag the slot's last prefetch was issued with
+  const uint32_t* landed;      // [S] tag the host wrote back once that copy had landed
+  int32_t* pf_list;            // [kPfMaxPending] pending slots, in request order
+  int32_t* pf_n;               // [1]
+  uint32_t* pf_head;           // [1] the device's count of requests written
+  PfCtl* pf_ctl;               // control region, device view of the mapped host memory
 };
 
 struct Scratch {

@@ -63,7 +63,7 @@ __device__ unsigned long long block_min_u64(unsigned long long v, unsigned long 
 }
 
 struct SmemLayout {
-  size_t hs, hsel, tok, owner, prot, ids, w, total;
+  size_t hs, hsel, tok, owner, prot, ids, w, pfs, total;
 };
 
 __host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~size_t(15); }
@@ -86,6 +86,8 @@ __host__ __device__ inline SmemLayout plan_smem_layout(int E, int W, int tok_row
   off = align16(off + (size_t)kIdsSmemMax * 4);
   L.w = off;
   off = align16(off + (size_t)kIdsSmemMax * 4);
+  L.pfs = off;   // the layer's pending-prefetch slot of each expert
+  off = align16(off + (size_t)E * 4);
   L.total = off;
   return L;
 }
@@ -210,8 +212,11 @@ __device__ void plan_body(const PlanArgs& a, uint8_t* dsm, bool prestaged = fals
       last0 = p.last_sel[(size_t)l * E + tid];
     }
   }
+  int* pfs = reinterpret_cast<int*>(dsm + SL.pfs);
+  const bool pf = cache && p.pf_used;
   if (cache) {
     if (tid < E) lut_s[tid] = p.lut[(size_t)l * E + tid];
+    if (pf && tid < E) pfs[tid] = p.pf_slot[(size_t)l * E + tid];
     if (owner_in_smem)
       for (int j = tid; j < (p.S + 31) / 32; j += kPlanThreads) prot[j] = 0u;
   }
@@ -225,11 +230,12 @@ __device__ void plan_body(const PlanArgs& a, uint8_t* dsm, bool prestaged = fals
   __syncthreads();
 
   // ------------------------------------------------------------ a3 history
+  float s = 0.f;                      // this thread's expert's router score of the step (tid < E)
   if (hist) {
     const int t = t_step;
     const int ring = t % W;
     const bool mine = tid < E;
-    float s = 0.f, m = 0.f;
+    float m = 0.f;
     int count = 0, age = 0;
     if (mine) {
       const int e = tid;
@@ -363,20 +369,27 @@ __device__ void plan_body(const PlanArgs& a, uint8_t* dsm, bool prestaged = fals
     const int n_miss = sh_misc[0];
     // victims, one miss at a time (ascending expert id): lowest free slot, else the
     // lowest-score slot of this layer that this step does not need, else of another layer
+    // a slot whose prefetch copy may still be in flight (its tag not yet written back) is
+    // never a victim: the late copy would overwrite the new occupant
+    auto busy = [&](int s2) -> bool {
+      return pf && *reinterpret_cast<const volatile uint32_t*>(p.landed + s2) != p.pf_tag[s2];
+    };
     for (int mi = 0; mi < n_miss; ++mi) {
+      // a miss whose expert is pending (its prefetch not committed): the pending slot takes it
+      const int pend = pf ? pfs[miss_list[mi]] : -1;
       unsigned long long key = ~0ull;
-      for (int s2 = tid; s2 < S; s2 += kPlanThreads) {
+      for (int s2 = tid; pend < 0 && s2 < S; s2 += kPlanThreads) {
         const int o = owner_in_smem ? owner_s[s2] : p.owner[s2];
-        if (o < 0) { key = (unsigned long long)s2; break; }
+        if (o == -1) { key = (unsigned long long)s2; break; }
       }
-      key = block_min_u64<NT>(key, red64);
-      int victim = key == ~0ull ? -1 : (int)key;
+      if (pend < 0) key = block_min_u64<NT>(key, red64);
+      int victim = pend >= 0 ? pend : key == ~0ull ? -1 : (int)key;
       if (victim < 0) {
         key = ~0ull;
         for (int s2 = tid; s2 < S; s2 += kPlanThreads) {
           const int o = owner_in_smem ? owner_s[s2] : p.owner[s2];
           const bool pr = owner_in_smem ? ((prot[s2 >> 5] >> (s2 & 31)) & 1u) != 0u : p.prot_epoch[s2] == ep;
-          if (o >= 0 && o < p.L * E && o / E == l && !pr) {
+          if (o >= 0 && o < p.L * E && o / E == l && !pr && !busy(s2)) {
             const unsigned long long kk = score_key(score_s[o - l * E], s2);
             key = kk < key ? kk : key;
           }
@@ -385,7 +398,7 @@ __device__ void plan_body(const PlanArgs& a, uint8_t* dsm, bool prestaged = fals
         if (key == ~0ull) {
           for (int s2 = tid; s2 < S; s2 += kPlanThreads) {
             const int o = owner_in_smem ? owner_s[s2] : p.owner[s2];
-            if (o >= 0 && o < p.L * E && o / E != l) {
+            if (o >= 0 && o < p.L * E && o / E != l && !busy(s2)) {
               const unsigned long long kk = score_key(p.score[o], s2);
               key = kk < key ? kk : key;
             }
@@ -405,8 +418,8 @@ __device__ void plan_body(const PlanArgs& a, uint8_t* dsm, bool prestaged = fals
           else set_status(p.status, MOE_ERR_CAPACITY);
           bypass_rid[e] = rid;
         } else {
-          const int old = owner_in_smem ? owner_s[victim] : p.owner[victim];
-          old_s[mi] = old;
+          const int old = pend >= 0 ? -3 : owner_in_smem ? owner_s[victim] : p.owner[victim];
+          old_s[mi] = old;             // -3: the expert's own pending slot
           if (old >= 0) sh_misc[5] += 1;
           if (owner_in_smem) {
             owner_s[victim] = l * E + e;
@@ -442,6 +455,11 @@ __device__ void plan_body(const PlanArgs& a, uint8_t* dsm, bool prestaged = fals
       job.src = p.host_dev + ((size_t)l * E + e) * rec;
       if (v >= 0) {
         if (old >= 0 && old < p.L * E) p.lut[old] = -1;
+        if (old == -3) {               // a pending prefetch of e, demanded before its commit
+          p.pf_expert[v] = -1;
+          p.pf_slot[(size_t)l * E + e] = -1;
+          atomicAdd(&p.stats[ST_PF_DEMANDED], 1ull);
+        }
         p.lut[(size_t)l * E + e] = v;
         p.owner[v] = l * E + e;
         atomicAdd(&p.tag[v], 1u);
@@ -469,6 +487,122 @@ __device__ void plan_body(const PlanArgs& a, uint8_t* dsm, bool prestaged = fals
     __syncthreads();
     if (tid == 0)
       asm volatile("fence.acq_rel.gpu;\n red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.slots_flag) : "memory");
+  }
+
+  // ------------------------------------------------ asynchronous prefetch (SeqMoE)
+  // Issue: up to pf_per_step minus this step's misses (the copy volume already committed to
+  // the layer, HybriMoE's priority) of the layer's experts the step does not need, neither
+  // resident nor pending, highest router score first; each takes the lowest free slot, else
+  // the lowest-score slot of this layer the step does not need.  The slot turns pending
+  // (owner -2) with a fresh tag, and the request goes to the host thread through the
+  // mapped control region.  Commit: every pending slot whose written-back tag equals its
+  // own becomes resident; a stale or superseded write-back never matches.
+  if (cache && p.pf_used) {
+    __syncthreads();
+    const int S = p.S;
+    const int n_miss = sh_misc[0];
+    int* pfs = reinterpret_cast<int*>(dsm + SL.pfs);
+    auto busy = [&](int s2) -> bool {
+      return *reinterpret_cast<const volatile uint32_t*>(p.landed + s2) != p.pf_tag[s2];
+    };
+    if (tid == 0) {
+      int b = p.pf_per_step - n_miss;
+      b = min(b, kPfRing - (int)(*p.pf_head - p.pf_ctl->tail));
+      b = min(b, kPfMaxPending - *p.pf_n);
+      sh_misc[7] = b > 0 ? b : 0;
+      sh_misc[8] = 0;
+    }
+    __syncthreads();
+    const int budget = sh_misc[7];
+    const int ep = owner_in_smem ? 0 : *p.epoch;
+    for (int b = 0; b < budget; ++b) {
+      unsigned long long ck = ~0ull;
+      if (tid < E && cnt[tid] == 0 && lut_s[tid] < 0 && pfs[tid] < 0) ck = score_key(-s, tid);
+      ck = block_min_u64<NT>(ck, red64);
+      if (ck == ~0ull) break;
+      const int e = (int)(ck & 0xffffffffu);
+      unsigned long long key = ~0ull;
+      for (int s2 = tid; s2 < S; s2 += kPlanThreads) {
+        const int o = owner_in_smem ? owner_s[s2] : p.owner[s2];
+        if (o == -1) { key = (unsigned long long)s2; break; }
+      }
+      key = block_min_u64<NT>(key, red64);
+      int v = key == ~0ull ? -1 : (int)key;
+      if (v < 0) {
+        key = ~0ull;
+        for (int s2 = tid; s2 < S; s2 += kPlanThreads) {
+          const int o = owner_in_smem ? owner_s[s2] : p.owner[s2];
+          const bool pr = owner_in_smem ? ((prot[s2 >> 5] >> (s2 & 31)) & 1u) != 0u : p.prot_epoch[s2] == ep;
+          if (o >= 0 && o < p.L * E && o / E == l && !pr && !busy(s2)) {
+            const unsigned long long kk = score_key(score_s[o - l * E], s2);
+            key = kk < key ? kk : key;
+          }
+        }
+        key = block_min_u64<NT>(key, red64);
+        v = key == ~0ull ? -1 : (int)(key & 0xffffffffu);
+      }
+      if (v < 0) break;
+      if (tid == 0) {
+        const int old = owner_in_smem ? owner_s[v] : p.owner[v];
+        if (old >= 0 && old < p.L * E) {
+          p.lut[old] = -1;
+          if (old / E == l) lut_s[old - l * E] = -1;
+          atomicAdd(&p.stats[ST_EVICT], 1ull);
+        }
+        if (owner_in_smem) owner_s[v] = -2;
+        p.owner[v] = -2;
+        p.pf_expert[v] = l * E + e;
+        p.pf_slot[(size_t)l * E + e] = v;
+        pfs[e] = v;
+        const uint32_t tg = atomicAdd(&p.tag[v], 1u) + 1u;
+        p.pf_tag[v] = tg;
+        const int k2 = sh_misc[8];
+        volatile PfReq* r = &p.pf_ctl->req[(*p.pf_head + (uint32_t)k2) % kPfRing];   // mapped host memory
+        r->slot = v;
+        r->flat = l * E + e;
+        r->tag = tg;
+        p.pf_list[*p.pf_n + k2] = v;
+        sh_misc[8] = k2 + 1;
+      }
+      __syncthreads();
+    }
+    if (tid == 0) {
+      const int issued = sh_misc[8];
+      if (issued > 0) {
+        *p.pf_n += issued;
+        const uint32_t h = *p.pf_head + (uint32_t)issued;
+        *p.pf_head = h;
+        __threadfence_system();        // the requests before the head that publishes them
+        p.pf_ctl->head = h;
+        atomicAdd(&p.stats[ST_PF_ISSUED], (unsigned long long)issued);
+      }
+      // commits, in request order
+      const int n = *p.pf_n;
+      int w = 0, committed = 0;
+      for (int i = 0; i < n; ++i) {
+        const int q = p.pf_list[i];
+        const int x = p.pf_expert[q];
+        if (x < 0) continue;                                        // demanded before its commit
+        if (*reinterpret_cast<const volatile uint32_t*>(p.landed + q) == p.pf_tag[q]) {
+          p.owner[q] = x;
+          p.lut[x] = q;
+          p.pf_slot[x] = -1;
+          p.pf_expert[q] = -1;
+          if (x / E == l) lut_s[x - l * E] = q;
+          if (owner_in_smem) owner_s[q] = x;
+          ++committed;
+          continue;
+        }
+        p.pf_list[w++] = q;
+      }
+      *p.pf_n = w;
+      if (committed) atomicAdd(&p.stats[ST_PF_COMMITTED], (unsigned long long)committed);
+      // the GPU's position and the miss flag, for the host thread
+      p.pf_ctl->layer = l;
+      p.pf_ctl->step = t_step;
+      if (n_miss > 0) p.pf_ctl->demand = p.pf_ctl->demand + 1u;
+    }
+    __syncthreads();
   }
 
   // ------------------------------------------------------ a7 permutation

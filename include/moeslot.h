@@ -95,7 +95,8 @@ typedef enum {
   MOE_ERR_CAPACITY = 4,   /* T exceeds the pool's max_tokens, or a one-step
                              record / static scratch is too small              */
   MOE_ERR_TIMEOUT = 5,    /* a bounded device-side wait gave up                 */
-  MOE_ERR_TAG = 6,        /* a slot tag did not match (reserved)                */
+  MOE_ERR_TAG = 6,        /* reserved (a prefetch whose tag does not match is
+                             simply not committed)                             */
   MOE_ERR_BOUNDS = 7      /* the device met an expert id or slot out of range   */
 } moe_status;
 
@@ -133,6 +134,10 @@ typedef struct {   /* cumulative counters of a pool */
   uint64_t bytes_copied;     /* host -> device bytes moved by miss copies          */
   uint64_t near_ties;        /* tokens whose k-th/(k+1)-th logit gap is < 1e-4     */
   uint64_t staged_layers;    /* layers copied into a staging region               */
+  uint64_t prefetch_issued;  /* prefetch requests the device wrote (moe_prefetch_enable) */
+  uint64_t prefetch_committed; /* prefetched slots committed on a matching tag      */
+  uint64_t prefetch_demanded;  /* pending prefetches a step needed before their commit */
+  uint64_t prefetch_bytes;   /* record bytes the host thread copied for prefetches */
 } moe_stats;
 
 /* Byte layout of one expert record for `cfg` (see the header comment).  Any
@@ -236,6 +241,29 @@ MOE_API moe_status moe_forward_routed(moe_pool* pool, int32_t layer, const void*
 MOE_API moe_status moe_update_scores(moe_pool* pool, int32_t layer, const int32_t* ids, const float* probs,
                                      int32_t T, void* stream);
 
+/* Asynchronous prefetch (SeqMoE "Mechanism"; HybriMoE "Mechanism" for the order).
+ * per_step > 0 starts the pool's one host thread and makes every layer call's plan
+ * issue up to per_step minus that step's misses prefetches for its layer: the
+ * experts the step does not need, neither resident nor pending, highest router
+ * score first, each into the lowest free slot or the lowest-score slot of the
+ * layer the step does not need.  Such a slot turns pending (not resident, never a
+ * victim) and its tag grows by one.  The device writes the request (slot, expert,
+ * tag) and its position and a miss flag into a mapped control region; the thread
+ * copies the record into the slot on a stream of its own and then writes the tag
+ * into device memory, in stream order.  A later plan commits the slot only if that
+ * tag equals the slot's tag, so a stale or wrong write-back is never committed; a
+ * step that needs a pending expert copies it into that slot itself.  No kernel ever
+ * waits for the thread.  per_step 0 stops issuing (slots already pending are still
+ * committed or demanded); 0..8.  Set it before capturing calls into a CUDA graph:
+ * a captured call keeps the setting it was captured with.  Once prefetch was used,
+ * moe_load_slot is refused; moe_set_lut drains it first. */
+MOE_API moe_status moe_prefetch_enable(moe_pool* pool, int32_t per_step);
+/* Blocking: every request issued so far has been copied and its tag written back. */
+MOE_API moe_status moe_prefetch_drain(moe_pool* pool);
+/* Fault injection on the host side: the next n tags the thread writes back are wrong
+ * (their slots are never committed). */
+MOE_API moe_status moe_prefetch_inject_wrong_tags(moe_pool* pool, uint32_t n);
+
 /* Limit of every wait a kernel of this pool makes on another CTA of its grid
  * (a miss record landing, the routing or the plan being published, a tile's
  * partial sums, the final arrival before the combine): `ns` nanoseconds of
@@ -269,7 +297,8 @@ MOE_API moe_status moe_get_routing(moe_pool* pool, int32_t* ids, float* w, float
                                    int32_t* T_out);
 
 /* Blocking: host copies of the cache state (any pointer may be NULL).
- *   lut [L*E] int32, owner [S] int32 (l*E+e or -1), tag [S] uint32,
+ *   lut [L*E] int32, owner [S] int32 (l*E+e, -1 free, -2 holding a pending
+ *   prefetch), tag [S] uint32,
  *   score [L*E] fp32 (eviction score as of each layer's last update). */
 MOE_API moe_status moe_get_state(moe_pool* pool, int32_t* lut, int32_t* owner, uint32_t* tag, float* score);
 

@@ -28,7 +28,9 @@ Readings taken where the pages are silent (each is listed in the design notes):
     committed (owner and table point at the expert), in request order.
   * A step that needs a pending expert counts it as a miss; its slot is the
     miss's slot (no eviction), committed at once with the tag grown by one, and
-    the demand copy goes into it.
+    the demand copy goes into it.  Until the prefetch's own tag has been
+    written back, that slot is never a victim (its late copy would overwrite a
+    new occupant).
   * The host writes back a request's tag once its copy has landed.  drain()
     stands for "every request issued so far has landed" (the GPU tests wait
     for the host thread between calls); corrupt(n) makes the next n
@@ -152,18 +154,22 @@ class PrefetchSim(SlotPoolSim):
         best = None
         for q in range(self.S):
             o = int(self.owner[q])
-            if o >= 0 and o // E == l and q not in protected:
+            if o >= 0 and o // E == l and q not in protected and not self._busy(q):
                 sc = self.score[o // E, o % E]
                 if best is None or sc < best[0]:
                     best = (sc, q)
         if best is None and other_layers:
             for q in range(self.S):
                 o = int(self.owner[q])
-                if o >= 0 and o // E != l:
+                if o >= 0 and o // E != l and not self._busy(q):
                     sc = self.score[o // E, o % E]
                     if best is None or sc < best[0]:
                         best = (sc, q)
         return -1 if best is None else best[1]
+
+    def _busy(self, q):
+        """A prefetch copy into slot q may still be in flight: its tag is not yet written back."""
+        return self.pf_tag[q] != self.landed[q]
 
     def _install(self, l, e, victim):
         E = self.E

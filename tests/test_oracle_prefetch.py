@@ -95,3 +95,16 @@ def test_misses_use_the_budget():
     sim2 = _two_layer_pool(per_step=2)
     _step(sim2, 0, 3, [0.1, 0.2, 0.3, 0.4])
     assert sim2.pf_issued == 1 and sim2.pf_expert[sim2.pending[0]] == 2     # expert 2: the best remaining
+
+
+def test_a_demanded_slot_is_not_a_victim_until_its_prefetch_has_landed():
+    """Expert 2 is demanded before its prefetch landed (slot 1, tag 3 now, prefetch tag 2).  Until
+    the host writes tag 2 back, slot 1 is not evictable, so layer 0's next miss takes slot 0."""
+    sim = _two_layer_pool()
+    _step(sim, 0, 0, [0.4, 0.1, 0.3, 0.2])
+    _step(sim, 0, 2, [0.1, 0.1, 0.7, 0.1])          # demanded: slot 1 holds expert 2, copy in flight
+    assert sim._busy(1)
+    r = _step(sim, 0, 3, [0.1, 0.1, 0.1, 0.7])      # expert 3 misses; slot 1 (lower LRU score?) is busy
+    assert r["misses"] == 1 and sim.lut[0, 3] == 0 and sim.lut[0, 2] == 1
+    sim.drain()
+    assert not sim._busy(1)
