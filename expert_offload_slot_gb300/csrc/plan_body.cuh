@@ -421,6 +421,7 @@ __device__ void plan_body(const PlanArgs& a, uint8_t* dsm, bool prestaged = fals
           const int old = pend >= 0 ? -3 : owner_in_smem ? owner_s[victim] : p.owner[victim];
           old_s[mi] = old;             // -3: the expert's own pending slot
           if (old >= 0) sh_misc[5] += 1;
+          if (old >= 0 && old / E == l) lut_s[old - l * E] = -1;   // the row stays current in shared memory
           if (owner_in_smem) {
             owner_s[victim] = l * E + e;
             prot[victim >> 5] |= 1u << (victim & 31);
@@ -494,7 +495,7 @@ __device__ void plan_body(const PlanArgs& a, uint8_t* dsm, bool prestaged = fals
   // the layer, HybriMoE's priority) of the layer's experts the step does not need, neither
   // resident nor pending, highest router score first; each takes the lowest free slot, else
   // the lowest-score slot of this layer the step does not need.  The slot turns pending
-  // (owner -2) with a fresh tag, and the request goes to the host thread through the
+  // (owner -2 - its expert) with a fresh tag, and the request goes to the host thread through the
   // mapped control region.  Commit: every pending slot whose written-back tag equals its
   // own becomes resident; a stale or superseded write-back never matches.
   if (cache && p.pf_used) {
@@ -515,9 +516,11 @@ __device__ void plan_body(const PlanArgs& a, uint8_t* dsm, bool prestaged = fals
     __syncthreads();
     const int budget = sh_misc[7];
     const int ep = owner_in_smem ? 0 : *p.epoch;
+    // candidates are fixed when the phase starts (an expert this phase evicts is not one)
+    const bool cand = tid < E && cnt[tid] == 0 && lut_s[tid] < 0 && pfs[tid] < 0;
     for (int b = 0; b < budget; ++b) {
       unsigned long long ck = ~0ull;
-      if (tid < E && cnt[tid] == 0 && lut_s[tid] < 0 && pfs[tid] < 0) ck = score_key(-s, tid);
+      if (cand && pfs[tid] < 0) ck = score_key(-s, tid);
       ck = block_min_u64<NT>(ck, red64);
       if (ck == ~0ull) break;
       const int e = (int)(ck & 0xffffffffu);
@@ -549,8 +552,8 @@ __device__ void plan_body(const PlanArgs& a, uint8_t* dsm, bool prestaged = fals
           if (old / E == l) lut_s[old - l * E] = -1;
           atomicAdd(&p.stats[ST_EVICT], 1ull);
         }
-        if (owner_in_smem) owner_s[v] = -2;
-        p.owner[v] = -2;
+        if (owner_in_smem) owner_s[v] = -2 - (l * E + e);    // pending: -2 - the expert it will hold
+        p.owner[v] = -2 - (l * E + e);
         p.pf_expert[v] = l * E + e;
         p.pf_slot[(size_t)l * E + e] = v;
         pfs[e] = v;

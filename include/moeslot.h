@@ -297,8 +297,8 @@ MOE_API moe_status moe_get_routing(moe_pool* pool, int32_t* ids, float* w, float
                                    int32_t* T_out);
 
 /* Blocking: host copies of the cache state (any pointer may be NULL).
- *   lut [L*E] int32, owner [S] int32 (l*E+e, -1 free, -2 holding a pending
- *   prefetch), tag [S] uint32,
+ *   lut [L*E] int32, owner [S] int32 (l*E+e, -1 free, -2 - (l*E+e) holding a
+ *   pending prefetch of (l, e)), tag [S] uint32,
  *   score [L*E] fp32 (eviction score as of each layer's last update). */
 MOE_API moe_status moe_get_state(moe_pool* pool, int32_t* lut, int32_t* owner, uint32_t* tag, float* score);
 

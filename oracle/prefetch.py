@@ -17,13 +17,14 @@ Readings taken where the pages are silent (each is listed in the design notes):
   * At the end of layer l's plan, once its own misses have their slots, the
     device issues up to (per_step - misses of this step) prefetches for layer
     l: the experts of layer l that this step does not need, that are neither
-    resident nor already prefetched, in descending order of this step's
-    router score s_e(t) (ties to the lower id).  Each takes the lowest free
+    resident nor already prefetched when this phase starts (an expert one of
+    these prefetches evicts is not a candidate), in descending order of this
+    step's router score s_e(t) (ties to the lower id).  Each takes the lowest free
     slot, else the lowest-eviction-score slot of layer l that holds an expert
     this step does not need (ties to the lower slot); with no such slot no more
     prefetches are issued.  The slot's occupant is evicted, the slot becomes
-    pending for the expert (owner -2, not resident, never a victim) and its
-    tag grows by one; the request carries that tag.
+    pending for the expert (owner -2 - (l * E + e): not resident, never a
+    victim) and its tag grows by one; the request carries that tag.
   * After that, every pending slot whose written-back tag equals its own tag is
     committed (owner and table point at the expert), in request order.
   * A step that needs a pending expert counts it as a miss; its slot is the
@@ -40,7 +41,9 @@ import numpy as np
 
 from .cache import F32, SlotPoolSim
 
-PENDING = -2
+def pending_owner(flat):
+    """Owner value of a slot holding a pending prefetch of expert l * E + e."""
+    return -2 - int(flat)
 
 
 class PrefetchSim(SlotPoolSim):
@@ -126,7 +129,7 @@ class PrefetchSim(SlotPoolSim):
                 if old >= 0:
                     self.lut[old // E, old % E] = -1
                     self.evictions += 1
-                self.owner[victim] = PENDING
+                self.owner[victim] = pending_owner(l * E + e)
                 self.pf_expert[victim] = l * E + e
                 self.tag[victim] += 1
                 self.pf_tag[victim] = self.tag[victim]

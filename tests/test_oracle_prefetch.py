@@ -3,7 +3,7 @@ import numpy as np
 import pytest
 
 from oracle.cache import EVICT_CORE, EVICT_LRU, EVICT_MRS, SlotPoolSim
-from oracle.prefetch import PENDING, PrefetchSim
+from oracle.prefetch import PrefetchSim, pending_owner
 
 
 @pytest.mark.parametrize("policy", [EVICT_CORE, EVICT_MRS, EVICT_LRU])
@@ -53,7 +53,7 @@ def test_prefetch_lands_is_committed_and_then_hits():
     sim = _two_layer_pool()
     r = _step(sim, 0, 0, [0.4, 0.1, 0.3, 0.2])
     assert (r["hits"], r["misses"]) == (1, 0)
-    assert sim.owner[1] == PENDING and sim.pf_expert[1] == 2 and sim.tag[1] == 2 and sim.lut[0, 1] == -1
+    assert sim.owner[1] == pending_owner(2) and sim.pf_expert[1] == 2 and sim.tag[1] == 2 and sim.lut[0, 1] == -1
     assert sim.lut[0, 2] == -1 and sim.pf_issued == 1 and sim.evictions == 1
     sim.drain()
     _step(sim, 1, 0, [0.4, 0.3, 0.2, 0.1])          # layer 1's plan commits layer 0's prefetch
@@ -69,7 +69,7 @@ def test_a_wrong_tag_is_never_committed_and_demand_takes_the_slot():
     sim.drain()
     for _ in range(3):
         _step(sim, 1, 0, [0.4, 0.3, 0.2, 0.1])
-    assert sim.owner[1] == PENDING and sim.lut[0, 2] == -1 and sim.pf_committed == 0
+    assert sim.owner[1] == pending_owner(2) and sim.lut[0, 2] == -1 and sim.pf_committed == 0
     r = _step(sim, 0, 2, [0.1, 0.1, 0.7, 0.1])     # demand: a miss, served into the pending slot
     assert r["misses"] == 1 and sim.lut[0, 2] == 1 and sim.owner[1] == 2 and sim.tag[1] == 3
     # evictions: expert 1 of layer 0 (its prefetch) and expert 1 of layer 1 (layer 1's own prefetch of
