@@ -43,7 +43,8 @@ class moe_config(ctypes.Structure):
 class moe_stats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in ("steps", "hits", "misses", "bypass", "evictions",
                                                "bytes_copied", "near_ties", "staged_layers", "prefetch_issued",
-                                               "prefetch_committed", "prefetch_demanded", "prefetch_bytes")]
+                                               "prefetch_committed", "prefetch_demanded", "prefetch_bytes",
+                                               "aes_substitutions")]
 
 
 _vp, _i32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
@@ -64,6 +65,7 @@ _sig = {
     "moe_update_scores": (_i32, [_vp, _i32, _vp, _vp, _i32, _vp]),
     "moe_set_wait_limit": (_i32, [_vp, ctypes.c_uint64]),
     "moe_prefetch_enable": (_i32, [_vp, _i32]),
+    "moe_set_aes": (_i32, [_vp, _i32, ctypes.c_float]),
     "moe_prefetch_drain": (_i32, [_vp]),
     "moe_prefetch_inject_wrong_tags": (_i32, [_vp, ctypes.c_uint32]),
     "moe_get_status": (_i32, [_vp]),
@@ -254,6 +256,9 @@ class Pool:
     def update_scores(self, layer, ids, probs, stream=None):
         _check(_lib.moe_update_scores(self.h, layer, _ptr(ids), _ptr(probs), ids.shape[0], _stream(stream)),
                "moe_update_scores")
+
+    def set_aes(self, on, alpha=0.0):
+        _check(_lib.moe_set_aes(self.h, int(on), float(alpha)), "moe_set_aes")
 
     def prefetch_enable(self, per_step):
         _check(_lib.moe_prefetch_enable(self.h, int(per_step)), "moe_prefetch_enable")

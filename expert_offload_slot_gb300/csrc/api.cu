@@ -593,10 +593,11 @@ static moe_status run_layer(moe_pool* P, int layer, const void* x, int T, void* 
       if (n < 0) return fail(MOE_ERR_INVALID, "x must be 16-byte aligned for the tensor-core router");
       P->launches += n;
       P->launches += launch_gate_topk(d, sc.rpart, nsp, P->router_b + (size_t)layer * d.E, T, sc.ids, sc.w,
-                                      sc.probs, sc.gap, s);
+                                      sc.probs, sc.gap, s, d.aes_on ? d.lut + (size_t)layer * d.E : nullptr);
     } else {
       P->launches += launch_route_logits(d, layer, x, T, P->router_w, P->router_b, sc.logits, s);
-      P->launches += launch_gate_topk(d, sc.logits, 0, nullptr, T, sc.ids, sc.w, sc.probs, sc.gap, s);
+      P->launches += launch_gate_topk(d, sc.logits, 0, nullptr, T, sc.ids, sc.w, sc.probs, sc.gap, s,
+                                      d.aes_on ? d.lut + (size_t)layer * d.E : nullptr);
     }
   }
   mark(1);
@@ -809,6 +810,14 @@ MOE_API moe_status moe_prefetch_inject_wrong_tags(moe_pool* P, uint32_t n) {
   return MOE_OK;
 }
 
+MOE_API moe_status moe_set_aes(moe_pool* P, int32_t on, float alpha) {
+  if (!P) return fail(MOE_ERR_INVALID, "pool is NULL");
+  if (on && !(alpha >= 0.f && alpha < INFINITY)) return fail(MOE_ERR_INVALID, "alpha must be finite and >= 0");
+  P->d.aes_on = on ? 1 : 0;
+  P->d.aes_alpha = on ? alpha : 0.f;
+  return MOE_OK;
+}
+
 MOE_API moe_status moe_set_wait_limit(moe_pool* P, uint64_t ns) {
   if (!P) return fail(MOE_ERR_INVALID, "pool is NULL");
   if (ns == 0) ns = kDefaultWaitNs;
@@ -901,6 +910,7 @@ MOE_API moe_status moe_get_stats(moe_pool* P, moe_stats* out) {
   out->prefetch_committed = v[ST_PF_COMMITTED];
   out->prefetch_demanded = v[ST_PF_DEMANDED];
   out->prefetch_bytes = P->pf_bytes.load();
+  out->aes_substitutions = v[ST_AES];
   return MOE_OK;
 }
 

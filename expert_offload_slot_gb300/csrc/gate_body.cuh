@@ -25,11 +25,58 @@ template <> struct Vec16<uint16_t> {   // bf16 bit patterns
   }
 };
 
+// Approximate expert substitution (MoE-CORE "Mechanism"), opt-in: after a warp's top-k of
+// token t (ids[t][0..k) in rank order, this lane's logits v and selection flags taken,
+// the selected logits zsel in rank order, the best unselected logit `boundary`), each
+// selected expert that is not resident (res_row: the layer's table row at the step's
+// start) and whose logit is within alpha of the boundary takes, in rank order, the
+// token's best resident unselected expert (ties to the lower id), one each; it keeps the
+// missed expert's position and so its weight.  k < E only.
+__device__ __forceinline__ void aes_warp(const float* v, bool* taken, const float* zsel, float boundary, int t,
+                                         int E, int k, float alpha, const int32_t* __restrict__ res_row,
+                                         int32_t* ids, unsigned long long* stats) {
+  const int lane = threadIdx.x & 31;
+  bool res[kMaxPerLane];
+#pragma unroll
+  for (int j = 0; j < kMaxPerLane; ++j) {
+    const int e = lane + 32 * j;
+    res[j] = e < E && res_row[e] >= 0;
+  }
+  __syncwarp();   // ids[t][..] as lane 0 wrote them
+  int n = 0;
+  for (int r = 0; r < k; ++r) {
+    const int e = ids[(size_t)t * k + r];
+    if (res_row[e] >= 0 || !(zsel[r] - boundary <= alpha)) continue;
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < kMaxPerLane; ++j) {
+      const int ee = lane + 32 * j;
+      if (!taken[j] && res[j] && (v[j] > bv || (v[j] == bv && ee < be))) { bv = v[j]; be = ee; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+    }
+    if (be == 0x7fffffff) break;        // no resident unselected expert left
+#pragma unroll
+    for (int j = 0; j < kMaxPerLane; ++j)
+      if (lane + 32 * j == be) taken[j] = true;
+    if (lane == 0) ids[(size_t)t * k + r] = be;
+    ++n;
+  }
+  if (lane == 0 && n) atomicAdd(&stats[ST_AES], (unsigned long long)n);
+  __syncwarp();
+}
+
 // One warp: gate and top-k of token t from its logits z[t][0..E).  zsel_w: k floats
 // of shared memory private to the warp.
 __device__ __forceinline__ void gate_one_token(const float* __restrict__ z, int t, int E, int k, int gating,
                                                int32_t* ids, float* w, float* probs, float* gap,
-                                               unsigned long long* stats, float* zsel_w) {
+                                               unsigned long long* stats, float* zsel_w,
+                                               const int32_t* aes_row = nullptr, float aes_alpha = 0.f) {
   const int lane = threadIdx.x & 31;
   float v[kMaxPerLane];
   bool taken[kMaxPerLane];
@@ -87,6 +134,7 @@ __device__ __forceinline__ void gate_one_token(const float* __restrict__ z, int 
     }
   }
   __syncwarp();
+  if (aes_row && k < E) aes_warp(v, taken, zsel_w, next_best, t, E, k, aes_alpha, aes_row, ids, stats);
   const float zk = zsel_w[k - 1];
   const float g = k < E ? zk - next_best : INFINITY;
   if (lane == 0) {
@@ -116,12 +164,15 @@ struct GateCtaScratch {
   float zsel[36];                   // selected logits by rank, then the best unselected
   float red[32];                    // per-warp partials
   float bcast;
+  int byrank[kMaxPerLane * 32];     // expert of each rank (substitution only)
+  uint8_t resr[kMaxPerLane * 32];   // whether the expert of each rank is resident
 };
 
 template <int NT>
 __device__ __forceinline__ void gate_token_cta(const float* __restrict__ z, int t, int E, int k, int gating,
                                                int32_t* ids, float* w, float* probs, float* gap,
-                                               unsigned long long* stats, GateCtaScratch& gs) {
+                                               unsigned long long* stats, GateCtaScratch& gs,
+                                               const int32_t* aes_row = nullptr, float aes_alpha = 0.f) {
   static_assert(NT >= kMaxPerLane * 32, "one thread per expert");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int NW = NT / 32;
@@ -170,8 +221,27 @@ __device__ __forceinline__ void gate_token_cta(const float* __restrict__ z, int 
     }
     if (rank <= k) gs.zsel[rank] = u;
     if (rank < k) ids[(size_t)t * k + rank] = tid;
+    if (aes_row) {
+      gs.byrank[rank] = tid;
+      gs.resr[rank] = aes_row[tid] >= 0 ? 1 : 0;
+    }
   }
   __syncthreads();
+  if (aes_row && k < E && tid == 0) {
+    // approximate expert substitution, as aes_warp: low-score misses in rank order take the
+    // resident unselected experts in rank order
+    const float bnd = gs.zsel[k];
+    int j = k, n = 0;
+    for (int r = 0; r < k; ++r) {
+      if (gs.resr[r] || !(gs.zsel[r] - bnd <= aes_alpha)) continue;
+      while (j < E && !gs.resr[j]) ++j;
+      if (j >= E) break;
+      ids[(size_t)t * k + r] = gs.byrank[j];
+      ++j;
+      ++n;
+    }
+    if (n) atomicAdd(&stats[ST_AES], (unsigned long long)n);
+  }
   if (warp == 0) {
     const float zk = gs.zsel[k - 1];
     const float g = k < E ? zk - gs.zsel[k] : INFINITY;

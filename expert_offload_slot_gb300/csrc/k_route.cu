@@ -75,7 +75,8 @@ constexpr int kGateWarps = 8;
 __global__ void __launch_bounds__(kGateWarps * 32)
 gate_topk_kernel(const float* __restrict__ z, int nsp, const float* __restrict__ bias, int T, int E, int k,
                  int gating, int32_t* __restrict__ ids, float* __restrict__ w, float* __restrict__ probs,
-                 float* __restrict__ gap, unsigned long long* stats) {
+                 float* __restrict__ gap, unsigned long long* stats, const int32_t* __restrict__ aes_row,
+                 float aes_alpha) {
   __shared__ float zsel[kGateWarps][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kGateWarps + warp;
@@ -149,6 +150,7 @@ gate_topk_kernel(const float* __restrict__ z, int nsp, const float* __restrict__
     }
   }
   __syncwarp();
+  if (aes_row && k < E) aes_warp(v, taken, zsel[warp], next_best, t, E, k, aes_alpha, aes_row, ids, stats);
   const float zk = zsel[warp][k - 1];
   const float g = k < E ? zk - next_best : INFINITY;
   if (lane == 0) {
@@ -178,7 +180,8 @@ template <typename AT>
 __global__ void __launch_bounds__(kFusedRouteThreads)
 route_gate_fused_kernel(const AT* __restrict__ x, const AT* __restrict__ wr, const float* __restrict__ b,
                         float* __restrict__ z, int T, int E, int H, int k, int gating, int32_t* ids, float* w,
-                        float* probs, float* gap, unsigned long long* stats, int32_t* ticket) {
+                        float* probs, float* gap, unsigned long long* stats, int32_t* ticket,
+                        const int32_t* aes_row, float aes_alpha) {
   constexpr int C = Vec16<AT>::C;
   constexpr int kMaxChunks = 4;        // H <= kMaxChunks * C * kFusedRouteThreads
   __shared__ float red[kFusedRouteThreads / 32][kFusedRouteT];
@@ -235,21 +238,22 @@ route_gate_fused_kernel(const AT* __restrict__ x, const AT* __restrict__ wr, con
   if (!last) return;
   __threadfence();
   for (int t = warp; t < T; t += kFusedRouteThreads / 32)
-    gate_one_token(z, t, E, k, gating, ids, w, probs, gap, stats, zsel[warp]);
+    gate_one_token(z, t, E, k, gating, ids, w, probs, gap, stats, zsel[warp], aes_row, aes_alpha);
 }
 
 int launch_route_gate_fused(const PoolDev& p, int layer, const void* x, int T, const void* router_w,
                             const float* router_b, const Scratch& sc, cudaStream_t s) {
   const size_t wofs = (size_t)layer * p.E * p.H;
   const float* b = router_b + (size_t)layer * p.E;
+  const int32_t* aes_row = p.aes_on ? p.lut + (size_t)layer * p.E : nullptr;   // the table at the step's start
   if (p.adt == MOE_BF16) {
     route_gate_fused_kernel<uint16_t><<<p.E, kFusedRouteThreads, 0, s>>>(
         (const uint16_t*)x, (const uint16_t*)router_w + wofs, b, sc.logits, T, p.E, p.H, p.k, p.gating, sc.ids,
-        sc.w, sc.probs, sc.gap, p.stats, sc.ticket);
+        sc.w, sc.probs, sc.gap, p.stats, sc.ticket, aes_row, p.aes_alpha);
   } else {
     route_gate_fused_kernel<float><<<p.E, kFusedRouteThreads, 0, s>>>(
         (const float*)x, (const float*)router_w + wofs, b, sc.logits, T, p.E, p.H, p.k, p.gating, sc.ids, sc.w,
-        sc.probs, sc.gap, p.stats, sc.ticket);
+        sc.probs, sc.gap, p.stats, sc.ticket, aes_row, p.aes_alpha);
   }
   return 1;
 }
@@ -260,10 +264,10 @@ bool route_fused_ok(const PoolDev& p, int T) {
 }
 
 int launch_gate_topk(const PoolDev& p, const float* logits, int nsp, const float* bias, int T, int32_t* ids,
-                     float* w, float* probs, float* gap, cudaStream_t s) {
+                     float* w, float* probs, float* gap, cudaStream_t s, const int32_t* aes_row) {
   const int grid = (T + kGateWarps - 1) / kGateWarps;
   gate_topk_kernel<<<grid, kGateWarps * 32, 0, s>>>(logits, nsp, bias, T, p.E, p.k, p.gating, ids, w, probs, gap,
-                                                     p.stats);
+                                                     p.stats, aes_row, p.aes_alpha);
   return 1;
 }
 

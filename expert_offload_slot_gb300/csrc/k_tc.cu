@@ -2168,8 +2168,10 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
     __syncthreads();
     if (flag_sh) {
       // the token's gate by the whole CTA; scratch: the dynamic shared memory x was staged in
+      // (substitution reads the layer's table row: the plan changes it only after every gate)
       gate_token_cta<NT>(d.z, t, E, d.plan.p.k, d.plan.p.gating, d.plan.sc.ids, d.plan.sc.w, d.plan.sc.probs,
-                         d.plan.sc.gap, d.plan.p.stats, *reinterpret_cast<GateCtaScratch*>(dsm));
+                         d.plan.sc.gap, d.plan.p.stats, *reinterpret_cast<GateCtaScratch*>(dsm),
+                         p.aes_on ? p.lut + (size_t)l * E : nullptr, p.aes_alpha);
       __syncthreads();
       if (threadIdx.x == 0) release_add(route_done);
     }

@@ -29,7 +29,7 @@ struct CopyJob {
 
 enum StatIdx {
   ST_STEPS = 0, ST_HITS, ST_MISSES, ST_BYPASS, ST_EVICT, ST_BYTES, ST_NEAR_TIES, ST_STAGED,
-  ST_PF_ISSUED, ST_PF_COMMITTED, ST_PF_DEMANDED, ST_COUNT
+  ST_PF_ISSUED, ST_PF_COMMITTED, ST_PF_DEMANDED, ST_AES, ST_COUNT
 };
 
 // Asynchronous prefetch (SeqMoE "Mechanism"): the control region in pinned, mapped host
@@ -106,6 +106,9 @@ struct PoolDev {           // device-side pointers handed to kernels by value
   int32_t* pf_n;               // [1]
   uint32_t* pf_head;           // [1] the device's count of requests written
   PfCtl* pf_ctl;               // control region, device view of the mapped host memory
+  // approximate expert substitution (opt-in): the gates rewrite low-score misses
+  int32_t aes_on;
+  float aes_alpha;
 };
 
 struct Scratch {
@@ -182,7 +185,7 @@ int launch_route_logits(const PoolDev& p, int layer, const void* x, int T, const
                         const float* router_b, float* logits, cudaStream_t s);
 // logits [T][E], or (nsp > 0) nsp partial projections [nsp][T][E] summed in order plus bias
 int launch_gate_topk(const PoolDev& p, const float* logits, int nsp, const float* bias, int T, int32_t* ids,
-                     float* w, float* probs, float* gap, cudaStream_t s);
+                     float* w, float* probs, float* gap, cudaStream_t s, const int32_t* aes_row = nullptr);
 // one launch for router + gate when T and H are small enough (decode)
 bool route_fused_ok(const PoolDev& p, int T);
 int launch_route_gate_fused(const PoolDev& p, int layer, const void* x, int T, const void* router_w,

@@ -138,6 +138,7 @@ typedef struct {   /* cumulative counters of a pool */
   uint64_t prefetch_committed; /* prefetched slots committed on a matching tag      */
   uint64_t prefetch_demanded;  /* pending prefetches a step needed before their commit */
   uint64_t prefetch_bytes;   /* record bytes the host thread copied for prefetches */
+  uint64_t aes_substitutions; /* (token, expert) misses replaced by a resident expert */
 } moe_stats;
 
 /* Byte layout of one expert record for `cfg` (see the header comment).  Any
@@ -263,6 +264,17 @@ MOE_API moe_status moe_prefetch_drain(moe_pool* pool);
 /* Fault injection on the host side: the next n tags the thread writes back are wrong
  * (their slots are never committed). */
 MOE_API moe_status moe_prefetch_inject_wrong_tags(moe_pool* pool, uint32_t n);
+
+/* Approximate expert substitution (MoE-CORE "Mechanism"), off by default.  It
+ * CHANGES RESULTS: with on = 1, a token's selected expert that is not resident at
+ * the start of the step and whose router logit is within alpha of the best
+ * logit the token did not select (the rank-(k+1) boundary) is replaced, in rank
+ * order, by the token's best resident unselected expert (ties to the lower id),
+ * which keeps the missed expert's routing weight.  A miss above the band still
+ * takes the exact copy.  The rest of the step (history, table, misses, experts,
+ * combine) sees the rewritten routing; moe_get_routing returns it.  Applies to
+ * the calls issued after it (a captured call keeps its setting). */
+MOE_API moe_status moe_set_aes(moe_pool* pool, int32_t on, float alpha);
 
 /* Limit of every wait a kernel of this pool makes on another CTA of its grid
  * (a miss record landing, the routing or the plan being published, a tile's
