@@ -11,7 +11,7 @@ from dataclasses import dataclass, field
 from typing import Tuple
 
 # dtype codes shared with the C ABI header (moeslot.h): values only, no logic.
-F32, BF16, FP8_E4M3_B128 = 0, 1, 2
+F32, BF16, FP8_E4M3_B128, RESPLIT_Q4R4 = 0, 1, 2, 3
 GATE_SOFTMAX_RENORM, GATE_SIGMOID_RENORM = 0, 1
 EVICT_CORE, EVICT_MRS, EVICT_LRU = 0, 1, 2
 
@@ -54,7 +54,7 @@ class Workload:
 
     @property
     def weight_elt_bytes(self) -> int:
-        return {F32: 4, BF16: 2, FP8_E4M3_B128: 1}[self.weight_dtype]
+        return {F32: 4, BF16: 2, FP8_E4M3_B128: 1, RESPLIT_Q4R4: 1}[self.weight_dtype]
 
     @property
     def act_elt_bytes(self) -> int:
@@ -70,6 +70,11 @@ class Workload:
         w2 as [H/128][I/64] tiles, 16 KiB each.  Records are padded to 4096 bytes.
         """
         eb = self.weight_elt_bytes
+        if self.weight_dtype == RESPLIT_Q4R4:
+            # [q13 | r13 | l2 | h2 | sq13 | sr13 | sl2 | sh2]: 4-bit codes two per byte, 8-bit codes,
+            # fp32 scales per 128-column group; (w13_off, w2_off, s13_off, s2_off) = (q13, l2, sq13, sl2)
+            o = resplit_offsets(self.H, self.I)
+            return o["q13"], o["l2"], o["sq13"], o["sl2"], o["record"]
         if self.weight_dtype == BF16:
             mt_i, kb_h = -(-self.I // 128), -(-self.H // 64)
             mt_h, kb_i = -(-self.H // 128), -(-self.I // 64)
@@ -87,6 +92,19 @@ class Workload:
         raw = w13 + w2 + s13 + s2
         rec = (raw + 4095) // 4096 * 4096
         return off13, off2, offs13, offs2, rec
+
+
+def resplit_offsets(H, I):
+    """Byte offsets of the residual-split record's regions and its padded size."""
+    IH = I * H
+    sizes = [("q13", IH), ("r13", IH), ("l2", IH // 2), ("h2", IH), ("sq13", 2 * I * (H // 128) * 4),
+             ("sr13", 2 * I * (H // 128) * 4), ("sl2", H * (I // 128) * 4), ("sh2", H * (I // 128) * 4)]
+    off, out = 0, {}
+    for name, n in sizes:
+        out[name] = off
+        off += n
+    out["record"] = (off + 4095) // 4096 * 4096
+    return out
 
 
 WORKLOADS = {

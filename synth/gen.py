@@ -24,7 +24,7 @@ import math
 
 import numpy as np
 
-from .configs import F32, BF16, FP8_E4M3_B128, Workload
+from .configs import F32, BF16, FP8_E4M3_B128, RESPLIT_Q4R4, Workload, resplit_offsets
 
 FP8_MAX = 448.0
 
@@ -78,6 +78,49 @@ def expert_fp32(wl: Workload, layer: int, expert: int, base_seed: int = 0):
     return w_gate, w_up, w_down
 
 
+def quantize_groups(w: np.ndarray, bits: int):
+    """Symmetric integer codes per 128-column group: scale = group amax / (2^(bits-1) - 1) (1 for an
+    all-zero group), code = round-half-even(w / scale) clipped to +-(2^(bits-1) - 1).  fp32 arithmetic.
+    Returns (int8 codes [R, C], fp32 scales [R, C/128])."""
+    w = np.ascontiguousarray(w, np.float32)
+    R, C = w.shape
+    qmax = np.float32(2 ** (bits - 1) - 1)
+    g = w.reshape(R, C // 128, 128)
+    amax = np.abs(g).max(-1)
+    scale = np.where(amax > 0, amax / qmax, np.float32(1.0)).astype(np.float32)
+    q = np.clip(np.rint(g / scale[..., None]), -qmax, qmax).astype(np.int8)
+    return q.reshape(R, C), scale
+
+
+def resplit_encode(w13, w_down):
+    """Residual-split storage (RapidMoE Alg. 3, own codec): gate/up as 4-bit codes W^Q and 4-bit codes of
+    the residual W - W^Q (W^R); down as 4-bit (W^L) and 8-bit (W^H) codes.  W^Q = q * scale in fp32."""
+    q13, sq13 = quantize_groups(w13, 4)
+    deq = (q13.reshape(q13.shape[0], -1, 128).astype(np.float32) * sq13[..., None]).reshape(q13.shape)
+    r13, sr13 = quantize_groups(np.asarray(w13, np.float32) - deq, 4)
+    l2, sl2 = quantize_groups(w_down, 4)
+    h2, sh2 = quantize_groups(w_down, 8)
+    return {"q13": q13, "sq13": sq13, "r13": r13, "sr13": sr13, "l2": l2, "sl2": sl2, "h2": h2, "sh2": sh2}
+
+
+def pack_int4(q: np.ndarray) -> np.ndarray:
+    """int4 codes [R, C] (C even) -> bytes [R, C/2]: element 2j in the low nibble, 2j+1 in the high."""
+    u = (np.asarray(q, np.int8).astype(np.uint8) & 0x0F)
+    return (u[:, 0::2] | (u[:, 1::2] << 4)).astype(np.uint8)
+
+
+def unpack_int4(b: np.ndarray, C: int) -> np.ndarray:
+    """Inverse of pack_int4 (two's-complement nibbles)."""
+    b = np.asarray(b, np.uint8)
+    lo = (b & 0x0F).astype(np.int16)
+    hi = (b >> 4).astype(np.int16)
+    out = np.empty((b.shape[0], C), np.int16)
+    out[:, 0::2] = lo
+    out[:, 1::2] = hi
+    out[out >= 8] -= 16
+    return out.astype(np.int8)
+
+
 def encode_expert(wl: Workload, w_gate, w_up, w_down):
     """Stored form of one expert: dict with w13 [2I,H], w2 [H,I] (+ s13, s2 for fp8)."""
     w13 = np.concatenate([w_gate, w_up], axis=0)
@@ -85,6 +128,8 @@ def encode_expert(wl: Workload, w_gate, w_up, w_down):
         return {"w13": w13.astype(np.float32), "w2": np.asarray(w_down, np.float32)}
     if wl.weight_dtype == BF16:
         return {"w13": f32_to_bf16_bits(w13), "w2": f32_to_bf16_bits(w_down)}
+    if wl.weight_dtype == RESPLIT_Q4R4:
+        return resplit_encode(w13, w_down)
     c13, s13 = quantize_fp8_blocks(w13)
     c2, s2 = quantize_fp8_blocks(w_down)
     return {"w13": c13, "w2": c2, "s13": s13, "s2": s2}
@@ -140,6 +185,16 @@ def expert_record_bytes(wl: Workload, stored) -> bytes:
     """Pack one stored expert into the host-pool record layout (padded)."""
     o13, o2, os13, os2, rec = wl.expert_layout()
     buf = np.zeros(rec, np.uint8)
+    if wl.weight_dtype == RESPLIT_Q4R4:
+        o = resplit_offsets(wl.H, wl.I)
+        parts = {"q13": pack_int4(stored["q13"]), "r13": pack_int4(stored["r13"]), "l2": pack_int4(stored["l2"]),
+                 "h2": np.asarray(stored["h2"], np.int8).view(np.uint8)}
+        for key in ("sq13", "sr13", "sl2", "sh2"):
+            parts[key] = np.ascontiguousarray(stored[key], np.float32).view(np.uint8)
+        for key, raw in parts.items():
+            raw = np.ascontiguousarray(raw).reshape(-1)
+            buf[o[key]:o[key] + raw.size] = raw
+        return buf
     if wl.weight_dtype == BF16:
         I = wl.I
         g = tile_sw128(stored["w13"][:I])
@@ -283,6 +338,19 @@ def record_to_stored(wl: Workload, rec: np.ndarray):
     """Parse one host-pool record (uint8) back into the stored dict (w13, w2[, s13, s2])."""
     o13, o2, os13, os2, _ = wl.expert_layout()
     H, I = wl.H, wl.I
+    if wl.weight_dtype == RESPLIT_Q4R4:
+        o = resplit_offsets(H, I)
+
+        def region(key, n, dt=np.uint8):
+            return rec[o[key]:o[key] + n].view(dt)
+        return {"q13": unpack_int4(region("q13", I * H).reshape(2 * I, H // 2), H),
+                "r13": unpack_int4(region("r13", I * H).reshape(2 * I, H // 2), H),
+                "l2": unpack_int4(region("l2", I * H // 2).reshape(H, I // 2), I),
+                "h2": region("h2", I * H).view(np.int8).reshape(H, I).copy(),
+                "sq13": region("sq13", 8 * I * (H // 128), np.float32).reshape(2 * I, H // 128).copy(),
+                "sr13": region("sr13", 8 * I * (H // 128), np.float32).reshape(2 * I, H // 128).copy(),
+                "sl2": region("sl2", 4 * H * (I // 128), np.float32).reshape(H, I // 128).copy(),
+                "sh2": region("sh2", 4 * H * (I // 128), np.float32).reshape(H, I // 128).copy()}
     if wl.weight_dtype == BF16:
         mt_i, kb_h = -(-I // 128), -(-H // 64)
         mt_h, kb_i = -(-H // 128), -(-I // 64)
