@@ -20,7 +20,7 @@ _lib = ctypes.CDLL(LIB)
 
 MOE_OK, MOE_ERR_INVALID, MOE_ERR_OOM, MOE_ERR_CUDA, MOE_ERR_CAPACITY = 0, 1, 2, 3, 4
 MOE_ERR_TIMEOUT, MOE_ERR_TAG, MOE_ERR_BOUNDS = 5, 6, 7
-MOE_F32, MOE_BF16, MOE_FP8_E4M3_B128 = 0, 1, 2
+MOE_F32, MOE_BF16, MOE_FP8_E4M3_B128, MOE_RESPLIT_Q4R4 = 0, 1, 2, 3
 MOE_GATE_SOFTMAX_RENORM, MOE_GATE_SIGMOID_RENORM = 0, 1
 MOE_EVICT_CORE, MOE_EVICT_MRS, MOE_EVICT_LRU = 0, 1, 2
 MOE_MODE_AUTO, MOE_MODE_DECODE, MOE_MODE_PREFILL_STAGED = 0, 1, 2
@@ -44,7 +44,7 @@ class moe_stats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in ("steps", "hits", "misses", "bypass", "evictions",
                                                "bytes_copied", "near_ties", "staged_layers", "prefetch_issued",
                                                "prefetch_committed", "prefetch_demanded", "prefetch_bytes",
-                                               "aes_substitutions")]
+                                               "aes_substitutions", "critical_entries")]
 
 
 _vp, _i32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
@@ -66,6 +66,7 @@ _sig = {
     "moe_set_wait_limit": (_i32, [_vp, ctypes.c_uint64]),
     "moe_prefetch_enable": (_i32, [_vp, _i32]),
     "moe_set_aes": (_i32, [_vp, _i32, ctypes.c_float]),
+    "moe_set_umia": (_i32, [_vp, ctypes.c_float, _vp, ctypes.c_float, ctypes.c_float]),
     "moe_prefetch_drain": (_i32, [_vp]),
     "moe_prefetch_inject_wrong_tags": (_i32, [_vp, ctypes.c_uint32]),
     "moe_get_status": (_i32, [_vp]),
@@ -256,6 +257,11 @@ class Pool:
     def update_scores(self, layer, ids, probs, stream=None):
         _check(_lib.moe_update_scores(self.h, layer, _ptr(ids), _ptr(probs), ids.shape[0], _stream(stream)),
                "moe_update_scores")
+
+    def set_umia(self, theta, beta=None, gamma_decode=1.0, gamma_prefill=1.0):
+        b = None if beta is None else np.ascontiguousarray(beta, np.float32)
+        _check(_lib.moe_set_umia(self.h, float(theta), None if b is None else b.ctypes.data, float(gamma_decode),
+                                 float(gamma_prefill)), "moe_set_umia")
 
     def set_aes(self, on, alpha=0.0):
         _check(_lib.moe_set_aes(self.h, int(on), float(alpha)), "moe_set_aes")

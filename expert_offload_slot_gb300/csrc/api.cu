@@ -101,7 +101,7 @@ struct moe_pool {
 
 constexpr uint64_t kDefaultWaitNs = 1000000000ull;   // 1 s
 
-static size_t elt_bytes(int dt) { return dt == MOE_F32 ? 4 : dt == MOE_BF16 ? 2 : 1; }
+static size_t elt_bytes(int dt) { return dt == MOE_F32 ? 4 : dt == MOE_BF16 ? 2 : 1; }   // RESPLIT: bytes of codes
 
 static moe_status check_config(const moe_config* c) {
   if (!c) return fail(MOE_ERR_INVALID, "config is NULL");
@@ -125,22 +125,38 @@ static moe_status check_config(const moe_config* c) {
     if (!(c->core_w[i] >= 0.f)) return fail(MOE_ERR_INVALID, "core_w must be nonnegative");
   const bool ok_pair = (c->weight_dtype == MOE_F32 && c->act_dtype == MOE_F32) ||
                        (c->weight_dtype == MOE_BF16 && c->act_dtype == MOE_BF16) ||
-                       (c->weight_dtype == MOE_FP8_E4M3_B128 && c->act_dtype == MOE_BF16);
-  if (!ok_pair) return fail(MOE_ERR_INVALID, "supported (weight, act) dtypes: (f32,f32), (bf16,bf16), (fp8,bf16)");
+                       (c->weight_dtype == MOE_FP8_E4M3_B128 && c->act_dtype == MOE_BF16) ||
+                       (c->weight_dtype == MOE_RESPLIT_Q4R4 && c->act_dtype == MOE_BF16);
+  if (!ok_pair)
+    return fail(MOE_ERR_INVALID, "supported (weight, act) dtypes: (f32,f32), (bf16,bf16), (fp8,bf16), (resplit,bf16)");
   const int cw = (int)(16 / elt_bytes(c->weight_dtype));
   const int ca = (int)(16 / elt_bytes(c->act_dtype));
   const int q = cw > ca ? cw : ca;
   if (c->hidden < q || c->hidden % q || c->inter < q || c->inter % q)
     return fail(MOE_ERR_INVALID, "hidden and inter must be positive multiples of %d for these dtypes", q);
-  if (c->weight_dtype == MOE_FP8_E4M3_B128 && (c->hidden % 128 || c->inter % 128))
-    return fail(MOE_ERR_INVALID, "fp8 block-scaled weights need hidden and inter multiples of 128");
+  if ((c->weight_dtype == MOE_FP8_E4M3_B128 || c->weight_dtype == MOE_RESPLIT_Q4R4) && (c->hidden % 128 || c->inter % 128))
+    return fail(MOE_ERR_INVALID, "fp8 and residual-split weights need hidden and inter multiples of 128");
   return MOE_OK;
 }
 
 static Layout layout_of(const moe_config* c) {
-  Layout L;
+  Layout L{};
   const size_t eb = elt_bytes(c->weight_dtype);
   const size_t H = c->hidden, I = c->inter;
+  if (c->weight_dtype == MOE_RESPLIT_Q4R4) {
+    // [q13 | r13 | l2 | h2 | sq13 | sr13 | sl2 | sh2]
+    const size_t IH = I * H, s13 = 2 * I * (H / 128) * 4, s2 = H * (I / 128) * 4;
+    L.off13 = 0;
+    L.offr13 = IH;
+    L.off2 = 2 * IH;
+    L.offh2 = 2 * IH + IH / 2;
+    L.offs13 = 3 * IH + IH / 2;
+    L.offsr13 = L.offs13 + s13;
+    L.offs2 = L.offsr13 + s13;
+    L.offsh2 = L.offs2 + s2;
+    L.rec = (L.offsh2 + s2 + 4095) / 4096 * 4096;
+    return L;
+  }
   if (c->weight_dtype == MOE_BF16) {
     // 128 x 64 tiles in 128-byte-swizzled order: w13 [I/128][H/64][gate, up], w2 [H/128][I/64]
     const size_t mt_i = (I + 127) / 128, kb_h = (H + 63) / 64, mt_h = (H + 127) / 128, kb_i = (I + 63) / 64;
@@ -362,6 +378,16 @@ MOE_API moe_status moe_pool_create(const moe_config* cfg, const void* host_pool,
     PA(d.pf_list, kPfMaxPending, 0);
     PA(d.pf_n, 1, 0);
     PA(d.pf_head, 1, 0);
+    float* ub = nullptr;
+    PA(ub, L, 0);
+    std::vector<float> ones(L, 1.f);
+    if (cudaMemcpy(ub, ones.data(), sizeof(float) * L, cudaMemcpyHostToDevice) != cudaSuccess) {
+      st = fail(MOE_ERR_CUDA, "initialising the UMIA coefficients failed");
+      goto fail_out;
+    }
+    d.umia_beta = ub;
+    d.umia_theta = 0.f;
+    d.umia_gamma_decode = d.umia_gamma_prefill = 1.f;
   }
   P->sc.tmax = (int32_t)Tm;
   PA(P->sc.logits, Tm * E, 0);
@@ -810,6 +836,25 @@ MOE_API moe_status moe_prefetch_inject_wrong_tags(moe_pool* P, uint32_t n) {
   return MOE_OK;
 }
 
+MOE_API moe_status moe_set_umia(moe_pool* P, float theta, const float* beta, float gamma_decode,
+                                float gamma_prefill) {
+  if (!P) return fail(MOE_ERR_INVALID, "pool is NULL");
+  if (!(theta >= 0.f && gamma_decode >= 0.f && gamma_prefill >= 0.f && theta < INFINITY))
+    return fail(MOE_ERR_INVALID, "theta and the gammas must be finite and >= 0");
+  CUDA_TRY(cudaSetDevice(P->device));
+  std::vector<float> b((size_t)P->d.L, 1.f);
+  if (beta)
+    for (int l = 0; l < P->d.L; ++l) {
+      if (!(beta[l] >= 0.f && beta[l] < INFINITY)) return fail(MOE_ERR_INVALID, "beta must be finite and >= 0");
+      b[l] = beta[l];
+    }
+  CUDA_TRY(cudaMemcpy(const_cast<float*>(P->d.umia_beta), b.data(), sizeof(float) * b.size(), cudaMemcpyHostToDevice));
+  P->d.umia_theta = theta;
+  P->d.umia_gamma_decode = gamma_decode;
+  P->d.umia_gamma_prefill = gamma_prefill;
+  return MOE_OK;
+}
+
 MOE_API moe_status moe_set_aes(moe_pool* P, int32_t on, float alpha) {
   if (!P) return fail(MOE_ERR_INVALID, "pool is NULL");
   if (on && !(alpha >= 0.f && alpha < INFINITY)) return fail(MOE_ERR_INVALID, "alpha must be finite and >= 0");
@@ -911,6 +956,7 @@ MOE_API moe_status moe_get_stats(moe_pool* P, moe_stats* out) {
   out->prefetch_demanded = v[ST_PF_DEMANDED];
   out->prefetch_bytes = P->pf_bytes.load();
   out->aes_substitutions = v[ST_AES];
+  out->critical_entries = v[ST_CRIT];
   return MOE_OK;
 }
 

@@ -18,7 +18,11 @@
 //             The combine is therefore fused, deterministic and atomic-free.
 // Weights may be fp32, bf16, or fp8 e4m3 with 128x128 fp32 block scales (the
 // scale multiplies each 16-element partial dot product, which stays inside
-// one 128-wide block).
+// one 128-wide block), or residual-split codes (RapidMoE §4.4 Alg. 3): 4-bit
+// W^Q and W^R for gate/up, 4-bit W^L or 8-bit W^H for down, fp32 scales per
+// 128-column group.  A critical expert (UMIA, RapidMoE §4.3) computes
+// (W^Q + W^R) x as sq * (q . x) + sr * (r . x) per group and uses W^H_down;
+// the others read W^Q and W^L_down only.
 #include <cuda_fp8.h>
 
 #include "moeslot_internal.cuh"
@@ -35,6 +39,7 @@ struct FfnArgs {
   void* out;
   int H, I, T;
   size_t off13, off2, offs13, offs2;
+  size_t offr13, offh2, offsr13, offsh2;   // residual-split records
 };
 
 template <typename WT> struct WTraits;
@@ -182,6 +187,103 @@ ffn_gate_up_kernel(FfnArgs a) {
   }
 }
 
+// ---------------------------------------------------------------- residual-split records
+// 8 two's-complement nibbles of a little-endian word: element k is bits 4k .. 4k+3.
+__device__ __forceinline__ void nib8(uint32_t w, float* v) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) v[k] = (float)((int)(w << (28 - 4 * k)) >> 28);
+}
+__device__ __forceinline__ void int8x4(uint32_t w, float* v) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) v[k] = (float)((int)(w << (24 - 8 * k)) >> 24);
+}
+// dot product of 32 codes (one 16-byte chunk of nibbles) with 32 activations
+__device__ __forceinline__ float dot32_nib(const uint4& q, const float* x) {
+  float c[8], d = 0.f;
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    nib8(w[j], c);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) d = fmaf(c[k], x[8 * j + k], d);
+  }
+  return d;
+}
+
+// gate/up: every warp owns a contiguous range of (entry, row i) pairs, as ffn_gate_up_kernel;
+// each lane takes 32 columns (16 bytes of codes) at a time
+template <typename AT>
+__global__ void __launch_bounds__(kFfnWarps * 32)
+ffn_resplit_gate_up_kernel(FfnArgs a) {
+  constexpr int NT = kTokChunk;
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * kFfnWarps + (threadIdx.x >> 5);
+  const int nw = gridDim.x * kFfnWarps;
+  const int n_work = *a.n_work;
+  const int H = a.H, I = a.I;
+  const long long total = (long long)n_work * I;
+  const long long p0 = total * gw / nw, p1 = total * (gw + 1) / nw;
+  const AT* __restrict__ x = static_cast<const AT*>(a.x);
+  AT* __restrict__ hout = static_cast<AT*>(a.h);
+  const int G = H / 128;
+  for (long long pp = p0; pp < p1; ++pp) {
+    const int u = (int)(pp / I), i = (int)(pp % I);
+    const WorkEntry ent = a.work[u];
+    const bool crit = ent.crit != 0;
+    const uint8_t* qg = ent.rec + a.off13 + (size_t)i * (H / 2);
+    const uint8_t* qu = ent.rec + a.off13 + (size_t)(I + i) * (H / 2);
+    const uint8_t* rg = ent.rec + a.offr13 + (size_t)i * (H / 2);
+    const uint8_t* ru = ent.rec + a.offr13 + (size_t)(I + i) * (H / 2);
+    const float* sqg = reinterpret_cast<const float*>(ent.rec + a.offs13) + (size_t)i * G;
+    const float* squ = reinterpret_cast<const float*>(ent.rec + a.offs13) + (size_t)(I + i) * G;
+    const float* srg = reinterpret_cast<const float*>(ent.rec + a.offsr13) + (size_t)i * G;
+    const float* sru = reinterpret_cast<const float*>(ent.rec + a.offsr13) + (size_t)(I + i) * G;
+    for (int tc = 0; tc < ent.n; tc += NT) {
+      const int nr = min(NT, ent.n - tc);
+      int tok[NT];
+#pragma unroll
+      for (int r = 0; r < NT; ++r) tok[r] = r < nr ? a.perm_tok[ent.row0 + tc + r] : 0;
+      float ag[NT], au[NT];
+#pragma unroll
+      for (int r = 0; r < NT; ++r) { ag[r] = 0.f; au[r] = 0.f; }
+      for (int h = lane * 32; h < H; h += 32 * 32) {
+        const uint4 cqg = __ldcs(reinterpret_cast<const uint4*>(qg + h / 2));
+        const uint4 cqu = __ldcs(reinterpret_cast<const uint4*>(qu + h / 2));
+        uint4 crg = make_uint4(0u, 0u, 0u, 0u), cru = crg;
+        float s_rg = 0.f, s_ru = 0.f;
+        if (crit) {
+          crg = __ldcs(reinterpret_cast<const uint4*>(rg + h / 2));
+          cru = __ldcs(reinterpret_cast<const uint4*>(ru + h / 2));
+          s_rg = srg[h / 128];
+          s_ru = sru[h / 128];
+        }
+        const float s_qg = sqg[h / 128], s_qu = squ[h / 128];
+#pragma unroll
+        for (int r = 0; r < NT; ++r) {
+          if (r < nr) {
+            float xv[32];
+            Act<AT, 32>::load(x + (size_t)tok[r] * H + h, xv);
+            ag[r] = fmaf(s_qg, dot32_nib(cqg, xv), ag[r]);
+            au[r] = fmaf(s_qu, dot32_nib(cqu, xv), au[r]);
+            if (crit) {
+              ag[r] = fmaf(s_rg, dot32_nib(crg, xv), ag[r]);
+              au[r] = fmaf(s_ru, dot32_nib(cru, xv), au[r]);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < NT; ++r) {
+        if (r < nr) {
+          const float g = warp_sum(ag[r]);
+          const float uu = warp_sum(au[r]);
+          if (lane == 0) Act<AT, 8>::store1(hout + (size_t)(ent.row0 + tc + r) * I + i, silu(g) * uu);
+        }
+      }
+    }
+  }
+}
+
 constexpr int kDownRowsPerWarp = 2;
 constexpr int kDownRows = kFfnWarps * kDownRowsPerWarp;   // output features per CTA
 
@@ -266,6 +368,102 @@ ffn_down_combine_kernel(FfnArgs a) {
   }
 }
 
+// down + combine for residual-split records: as ffn_down_combine_kernel, reading W^H_down (8-bit,
+// 16 columns per lane chunk) for a critical entry and W^L_down (4-bit, 32 columns) otherwise
+template <typename AT>
+__global__ void __launch_bounds__(kFfnWarps * 32)
+ffn_resplit_down_kernel(FfnArgs a) {
+  constexpr int NT = kTokChunk;
+  constexpr int RPW = kDownRowsPerWarp;
+  extern __shared__ float acc_s[];   // [kDownRows][T]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int H = a.H, I = a.I, T = a.T;
+  const int h0 = blockIdx.x * kDownRows;
+  for (int j = threadIdx.x; j < kDownRows * T; j += blockDim.x) acc_s[j] = 0.f;
+  __syncthreads();
+  const int n_work = *a.n_work;
+  const AT* __restrict__ hin = static_cast<const AT*>(a.h);
+  const int G = I / 128;
+  int hr[RPW];
+#pragma unroll
+  for (int rr = 0; rr < RPW; ++rr) hr[rr] = min(h0 + warp * RPW + rr, H - 1);
+  for (int u = 0; u < n_work; ++u) {
+    const WorkEntry ent = a.work[u];
+    const bool crit = ent.crit != 0;
+    const uint8_t* w2 = ent.rec + (crit ? a.offh2 : a.off2);
+    const float* s2 = reinterpret_cast<const float*>(ent.rec + (crit ? a.offsh2 : a.offs2));
+    const int cw = crit ? 16 : 32;                 // columns per 16-byte chunk
+    const size_t row_bytes = crit ? (size_t)I : (size_t)I / 2;
+    for (int tc = 0; tc < ent.n; tc += NT) {
+      const int nr = min(NT, ent.n - tc);
+      float acc[RPW][NT];
+#pragma unroll
+      for (int rr = 0; rr < RPW; ++rr)
+#pragma unroll
+        for (int r = 0; r < NT; ++r) acc[rr][r] = 0.f;
+      for (int i0 = lane * cw; i0 < I; i0 += 32 * cw) {
+        float wv[RPW][32];
+        float sc[RPW];
+#pragma unroll
+        for (int rr = 0; rr < RPW; ++rr) {
+          const uint4 q = __ldcs(reinterpret_cast<const uint4*>(w2 + (size_t)hr[rr] * row_bytes + (crit ? (size_t)i0 : (size_t)i0 / 2)));
+          const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+          if (crit) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) int8x4(w[j], wv[rr] + 4 * j);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) nib8(w[j], wv[rr] + 8 * j);
+          }
+          sc[rr] = s2[(size_t)hr[rr] * G + i0 / 128];
+        }
+#pragma unroll
+        for (int r = 0; r < NT; ++r) {
+          if (r < nr) {
+            float hv[32];
+            if (crit) Act<AT, 16>::load(hin + (size_t)(ent.row0 + tc + r) * I + i0, hv);
+            else Act<AT, 32>::load(hin + (size_t)(ent.row0 + tc + r) * I + i0, hv);
+#pragma unroll
+            for (int rr = 0; rr < RPW; ++rr) {
+              float d = 0.f;
+              if (crit) {
+#pragma unroll
+                for (int c = 0; c < 16; ++c) d = fmaf(wv[rr][c], hv[c], d);
+              } else {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) d = fmaf(wv[rr][c], hv[c], d);
+              }
+              acc[rr][r] = fmaf(sc[rr], d, acc[rr][r]);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < NT; ++r) {
+        if (r < nr) {
+          const int row = ent.row0 + tc + r;
+          const int t = a.perm_tok[row];
+          const float wgt = a.perm_w[row];
+#pragma unroll
+          for (int rr = 0; rr < RPW; ++rr) {
+            const float v = warp_sum(acc[rr][r]);
+            if (lane == 0 && h0 + warp * RPW + rr < H) {
+              float* dst = &acc_s[(warp * RPW + rr) * T + t];
+              *dst = *dst + wgt * v;
+            }
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  AT* __restrict__ out = static_cast<AT*>(a.out);
+  for (int j = threadIdx.x; j < kDownRows * T; j += blockDim.x) {
+    const int t = j / kDownRows, rr = j % kDownRows;
+    if (h0 + rr < H) Act<AT, 8>::store1(out + (size_t)t * H + h0 + rr, acc_s[rr * T + t]);
+  }
+}
+
 static FfnArgs ffn_args(const PoolDev& p, const Scratch& sc, int T, const void* x, void* out) {
   FfnArgs a;
   a.work = sc.work;
@@ -282,6 +480,10 @@ static FfnArgs ffn_args(const PoolDev& p, const Scratch& sc, int T, const void* 
   a.off2 = p.lay.off2;
   a.offs13 = p.lay.offs13;
   a.offs2 = p.lay.offs2;
+  a.offr13 = p.lay.offr13;
+  a.offh2 = p.lay.offh2;
+  a.offsr13 = p.lay.offsr13;
+  a.offsh2 = p.lay.offsh2;
   return a;
 }
 
@@ -290,6 +492,7 @@ int launch_ffn_gate_up(const PoolDev& p, const Scratch& sc, int T, const void* x
   const int grid = 2 * sm_count();
   if (p.wdt == MOE_F32) ffn_gate_up_kernel<float, float><<<grid, kFfnWarps * 32, 0, s>>>(a);
   else if (p.wdt == MOE_BF16) ffn_gate_up_kernel<uint16_t, uint16_t><<<grid, kFfnWarps * 32, 0, s>>>(a);
+  else if (p.wdt == MOE_RESPLIT_Q4R4) ffn_resplit_gate_up_kernel<uint16_t><<<grid, kFfnWarps * 32, 0, s>>>(a);
   else ffn_gate_up_kernel<uint8_t, uint16_t><<<grid, kFfnWarps * 32, 0, s>>>(a);
   return 1;
 }
@@ -308,9 +511,22 @@ static void launch_down_t(const FfnArgs& a, int T, cudaStream_t s) {
 
 int launch_ffn_down(const PoolDev& p, const Scratch& sc, int T, void* out, cudaStream_t s) {
   const FfnArgs a = ffn_args(p, sc, T, nullptr, out);
-  if (p.wdt == MOE_F32) launch_down_t<float, float>(a, T, s);
-  else if (p.wdt == MOE_BF16) launch_down_t<uint16_t, uint16_t>(a, T, s);
-  else launch_down_t<uint8_t, uint16_t>(a, T, s);
+  if (p.wdt == MOE_F32) {
+    launch_down_t<float, float>(a, T, s);
+  } else if (p.wdt == MOE_BF16) {
+    launch_down_t<uint16_t, uint16_t>(a, T, s);
+  } else if (p.wdt == MOE_RESPLIT_Q4R4) {
+    static bool configured = false;
+    if (!configured) {
+      cudaFuncSetAttribute(ffn_resplit_down_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           200 * 1024);
+      configured = true;
+    }
+    const size_t smem = (size_t)kDownRows * T * sizeof(float);
+    ffn_resplit_down_kernel<uint16_t><<<(a.H + kDownRows - 1) / kDownRows, kFfnWarps * 32, smem, s>>>(a);
+  } else {
+    launch_down_t<uint8_t, uint16_t>(a, T, s);
+  }
   return 1;
 }
 

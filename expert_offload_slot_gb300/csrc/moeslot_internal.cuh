@@ -19,6 +19,7 @@ struct WorkEntry {
   int32_t n;
   int32_t expert;   // routed expert id, or -1 for the shared expert
   int32_t rid;      // record index in the pool's record array
+  int32_t crit;     // residual-split records: 1 = high precision (UMIA critical set)
 };
 
 // One device-started miss copy: record bytes from the mapped host pool to a slot.
@@ -29,7 +30,7 @@ struct CopyJob {
 
 enum StatIdx {
   ST_STEPS = 0, ST_HITS, ST_MISSES, ST_BYPASS, ST_EVICT, ST_BYTES, ST_NEAR_TIES, ST_STAGED,
-  ST_PF_ISSUED, ST_PF_COMMITTED, ST_PF_DEMANDED, ST_AES, ST_COUNT
+  ST_PF_ISSUED, ST_PF_COMMITTED, ST_PF_DEMANDED, ST_AES, ST_CRIT, ST_COUNT
 };
 
 // Asynchronous prefetch (SeqMoE "Mechanism"): the control region in pinned, mapped host
@@ -66,6 +67,7 @@ enum PlanFlags {
 
 struct Layout {
   size_t rec, off13, off2, offs13, offs2;
+  size_t offr13, offh2, offsr13, offsh2;   // residual-split records: W^R, W^H_down and their scales
 };
 
 struct PoolDev {           // device-side pointers handed to kernels by value
@@ -109,6 +111,10 @@ struct PoolDev {           // device-side pointers handed to kernels by value
   // approximate expert substitution (opt-in): the gates rewrite low-score misses
   int32_t aes_on;
   float aes_alpha;
+  // UMIA (residual-split records): an expert of the step is critical when its token-averaged
+  // router probability reaches (theta * beta[l]) * gamma (gamma of the decode or the prefill phase)
+  float umia_theta, umia_gamma_decode, umia_gamma_prefill;
+  const float* umia_beta;      // [L]
 };
 
 struct Scratch {

@@ -725,6 +725,15 @@ __device__ void plan_body(const PlanArgs& a, uint8_t* dsm, bool prestaged = fals
       we.n = offs[e + 1] - offs[e];
       we.expert = e;
       we.rid = rid;
+      // UMIA (residual-split records): critical when the step's token-averaged probability s
+      // reaches (theta * beta[l]) * gamma of the call's phase
+      we.crit = 1;
+      if (p.wdt == MOE_RESPLIT_Q4R4) {
+        const float g = (a.flags & PLAN_STAGED) ? p.umia_gamma_prefill : p.umia_gamma_decode;
+        const float thr = __fmul_rn(__fmul_rn(p.umia_theta, p.umia_beta[l]), g);
+        we.crit = s >= thr ? 1 : 0;
+        if (we.crit) atomicAdd(&p.stats[ST_CRIT], 1ull);
+      }
       a.sc.work[pos] = we;
       pos_of[e] = pos;
       // entries that need no copy this step, and entries that do (both in expert order)
@@ -749,6 +758,8 @@ __device__ void plan_body(const PlanArgs& a, uint8_t* dsm, bool prestaged = fals
         we.row0 = Tk;
         we.n = T;
         we.expert = -1;
+        we.crit = 1;                          // the shared expert runs at high precision
+        if (p.wdt == MOE_RESPLIT_Q4R4) atomicAdd(&p.stats[ST_CRIT], 1ull);
         a.sc.work[n] = we;
         n += 1;
       }

@@ -67,6 +67,20 @@
  *         w13_off + (((i/128)*ceil(H/64) + j/64)*2 + 1)*16384 + tile byte of (i mod 128, j mod 64).
  *     A row-major bf16 record gives wrong outputs without any error: pack
  *     bf16 records with moe_pack_expert_record.
+ *   MOE_RESPLIT_Q4R4 (RapidMoE §4.4 Alg. 3, with a codec defined here): gate/up
+ *     stored as W^Q plus a residual W^R, down stored twice (W^L, W^H), as
+ *     symmetric integer codes per 128-column group, scale = group amax /
+ *     (2^(b-1) - 1), code = round-half-even(w / scale) (fp32), row-major, in this
+ *     order (IH = I * H bytes):
+ *       q13  [2I][H/2]  4-bit codes of W^Q (gate rows, then up rows)   at 0
+ *       r13  [2I][H/2]  4-bit codes of W^R = Quantize(W - W^Q, 4)      at IH
+ *       l2   [H][I/2]   4-bit codes of W^L_down                        at 2 IH
+ *       h2   [H][I]     8-bit codes of W^H_down                        at 2.5 IH
+ *       sq13, sr13 [2I][H/128], then sl2, sh2 [H][I/128]: fp32 scales, from 3.5 IH
+ *     A byte holds columns 2j (low nibble) and 2j+1 (high nibble), two's
+ *     complement.  moe_expert_layout returns (q13, l2, sq13, sl2, record).
+ *     Critical experts (moe_set_umia) run W^Q + W^R and W^H_down, the others
+ *     W^Q and W^L_down.  H and I multiples of 128; activations bf16.
  *   Every record is padded to a multiple of 4096 bytes.
  */
 #ifndef MOESLOT_H
@@ -100,7 +114,8 @@ typedef enum {
   MOE_ERR_BOUNDS = 7      /* the device met an expert id or slot out of range   */
 } moe_status;
 
-enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_FP8_E4M3_B128 = 2 };          /* dtypes   */
+enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_FP8_E4M3_B128 = 2,            /* dtypes   */
+       MOE_RESPLIT_Q4R4 = 3 };                                       /* residual-split weights */
 enum { MOE_GATE_SOFTMAX_RENORM = 0, MOE_GATE_SIGMOID_RENORM = 1 };  /* gating   */
 enum { MOE_EVICT_CORE = 0, MOE_EVICT_MRS = 1, MOE_EVICT_LRU = 2 };  /* policy   */
 enum { MOE_MODE_AUTO = 0, MOE_MODE_DECODE = 1, MOE_MODE_PREFILL_STAGED = 2 };
@@ -139,6 +154,7 @@ typedef struct {   /* cumulative counters of a pool */
   uint64_t prefetch_demanded;  /* pending prefetches a step needed before their commit */
   uint64_t prefetch_bytes;   /* record bytes the host thread copied for prefetches */
   uint64_t aes_substitutions; /* (token, expert) misses replaced by a resident expert */
+  uint64_t critical_entries; /* residual-split experts run at high precision (UMIA) */
 } moe_stats;
 
 /* Byte layout of one expert record for `cfg` (see the header comment).  Any
@@ -152,7 +168,8 @@ MOE_API moe_status moe_expert_layout(const moe_config* cfg, size_t* w13_off, siz
  * safe from any thread.
  *   w_gate [I, H], w_up [I, H], w_down [H, I]: row-major, elements in the
  *       storage of cfg->weight_dtype (MOE_F32: float; MOE_BF16: bf16 bit
- *       patterns, uint16; MOE_FP8_E4M3_B128: e4m3 codes, uint8)
+ *       patterns, uint16; MOE_FP8_E4M3_B128: e4m3 codes, uint8;
+ *       MOE_RESPLIT_Q4R4: float, which this call quantizes as the header states)
  *   s_gate [I/128, H/128], s_up [I/128, H/128], s_down [H/128, I/128]: fp32
  *       block scales, MOE_FP8_E4M3_B128 only (NULL otherwise)
  *   record: record_bytes >= moe_expert_layout's record_bytes; the padding is
@@ -275,6 +292,16 @@ MOE_API moe_status moe_prefetch_inject_wrong_tags(moe_pool* pool, uint32_t n);
  * combine) sees the rewritten routing; moe_get_routing returns it.  Applies to
  * the calls issued after it (a captured call keeps its setting). */
 MOE_API moe_status moe_set_aes(moe_pool* pool, int32_t on, float alpha);
+
+/* UMIA (RapidMoE §4.3, Eq. 3-4) for MOE_RESPLIT_Q4R4 pools: an expert a step uses
+ * runs at high precision when its token-averaged router probability reaches
+ * Theta(l, t) = (theta * beta[l]) * gamma_t (fp32), gamma_t = gamma_decode for
+ * slot-pool calls and gamma_prefill for staged prefill calls; the shared expert
+ * always does.  beta: host float [L] (NULL: all 1).  Defaults: theta 0 (every
+ * expert critical), beta 1, gammas 1.  Blocking only for the beta upload; applies
+ * to the calls issued after it. */
+MOE_API moe_status moe_set_umia(moe_pool* pool, float theta, const float* beta, float gamma_decode,
+                                float gamma_prefill);
 
 /* Limit of every wait a kernel of this pool makes on another CTA of its grid
  * (a miss record landing, the routing or the plan being published, a tile's

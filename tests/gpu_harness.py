@@ -14,9 +14,11 @@ from oracle import layer as olayer
 from oracle.cache import SlotPoolSim
 from oracle.numerics import bf16_to_f64, decode_act
 from synth import gen
-from synth.configs import BF16, F32, FP8_E4M3_B128
+from synth.configs import BF16, F32, FP8_E4M3_B128, RESPLIT_Q4R4
 
-TOL = {F32: 1e-5, BF16: 2e-2, FP8_E4M3_B128: 5e-2}   # max|out - ref| <= TOL * max|ref|
+# max|out - ref| <= TOL * max|ref|; residual-split weights are compared with the oracle at the same
+# quantized precision, so only the bf16 activations and outputs round: the bf16 bound
+TOL = {F32: 1e-5, BF16: 2e-2, FP8_E4M3_B128: 5e-2, RESPLIT_Q4R4: 2e-2}
 NEAR_TIE = 1e-4
 
 

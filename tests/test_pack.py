@@ -99,3 +99,16 @@ def test_a_row_major_bf16_record_is_not_the_packed_record():
     # same multiset of elements: a permutation, not a re-encoding
     np.testing.assert_array_equal(np.sort(packed[:row_major.size].view(np.uint16)),
                                   np.sort(row_major.view(np.uint16)))
+
+
+def test_residual_split_records_equal_the_generators():
+    """The library's residual-split encoder (fp32 in) writes the generator's record byte for byte."""
+    from synth.configs import RESPLIT_Q4R4
+    wl = variant(get_workload("dsv3"), name="pack_resplit", L=1, E=2, k=1, H=512, I=256,
+                 weight_dtype=RESPLIT_Q4R4, shared=False)
+    cfg = _cfg(wl)
+    assert moe.moe_expert_layout(cfg) == wl.expert_layout()
+    for e in range(wl.E):
+        wg, wu, wd = gen.expert_fp32(wl, 0, e)
+        got = moe.moe_pack_expert_record(cfg, wg, wu, wd)
+        np.testing.assert_array_equal(got, gen.expert_record_bytes(wl, gen.expert_stored(wl, 0, e)))
