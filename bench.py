@@ -65,7 +65,8 @@ def parse_args():
                     help="profiling only: the workload's expert shape with this many routed experts (0 = all)")
     ap.add_argument("--top-k", type=int, default=0, help="profiling only: top-k with --experts (0 = the workload's)")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--configs", default="qwen3_hit,s_independence,prefetch,quotas,qwen3_prefill,dsv3,mixtral",
+    ap.add_argument("--configs",
+                    default="qwen3_hit,s_independence,prefetch,quotas,qwen3_prefill,dsv3,dsv3_resplit,mixtral",
                     help="other workloads measured at N=1 and reported under 'configs' ('' for none)")
     ap.add_argument("--probe-link", action="store_true",
                     help="measure the host->GPU link: device-started record copies vs DMA, then exit")
@@ -322,7 +323,8 @@ class PoolBench:
                "hits": st1["hits"] - st0["hits"], "misses": st1["misses"] - st0["misses"],
                "bytes_copied": st1["bytes_copied"] - st0["bytes_copied"], "clocks": clk,
                "prefetch": {n: st1["prefetch_" + n] - st0["prefetch_" + n]
-                            for n in ("issued", "committed", "demanded", "bytes")}}
+                            for n in ("issued", "committed", "demanded", "bytes")},
+               "critical_entries": st1["critical_entries"] - st0["critical_entries"]}
         res["status"] = self.pool.status()
         # profiling pass: per-stage CUDA-event times of every layer, same workload continued
         res["prof"] = self.profile_decode(xs[W + K:W + K + P], x_in, out, s, T, prof_steps) if prof_steps > 0 else \
@@ -694,6 +696,40 @@ def run_configs(names, dev, qwen_host, args, peaks, link_gbs):
                     base = res["0"]
             out[name] = {"workload": "qwen3-30b-a3b-shaped-decode, T=16, 2765 slots, MRS; per_step 0 / 1 / 2",
                          "by_per_step": res}
+        elif name == "dsv3_resplit":
+            # RapidMoE residual-split experts on the DeepSeek-V3 expert shape (4-bit W^Q + 4-bit
+            # residual for gate/up, 4- or 8-bit down, own codec), UMIA deciding each step's precision:
+            # every expert high (theta 0), every expert low, and a mixed threshold
+            from synth.configs import RESPLIT_Q4R4
+            wl = dataclasses.replace(get_workload("dsv3"), name="dsv3_resplit", weight_dtype=RESPLIT_Q4R4)
+            o = wl.expert_layout()
+            IH = wl.I * wl.H
+            b = PoolBench(wl, max(wl.decode_T), dev)
+            res = {}
+            for label, theta in (("all_high", 0.0), ("mixed_theta_0.8", 0.8), ("all_low", 10.0)):
+                b.pool.set_umia(theta)
+                per_T = {}
+                for T in wl.decode_T:
+                    r = b.decode(T, 3, 24, 0, Clocks(torch_local()), 1, e2e=False)
+                    n_ent = (r["hits"] + r["misses"]) + r["steps"] * wl.L      # routed + shared entries
+                    crit = r["critical_entries"]
+                    # HBM bytes the expert kernels read: W^Q + W^R + W^H_down (+ scales) for a critical
+                    # entry, W^Q + W^L_down (+ scales) for the others
+                    b_hi = IH + IH + IH + (2 * 2 * wl.I * (wl.H // 128) + wl.H * (wl.I // 128)) * 4
+                    b_lo = IH + IH // 2 + (2 * wl.I * (wl.H // 128) + wl.H * (wl.I // 128)) * 4
+                    byt = crit * b_hi + (n_ent - crit) * b_lo
+                    per_T[str(T)] = {"tokens_per_s": r["steps"] * T * wl.L / (r["ms"] / 1e3),
+                                     "us_per_layer": r["ms"] * 1e3 / (r["steps"] * wl.L),
+                                     "hit_rate": r["hits"] / max(1, r["hits"] + r["misses"]),
+                                     "critical_fraction": crit / max(1, n_ent),
+                                     "expert_GB_per_s_whole_layer": byt / (r["ms"] / 1e3) / 1e9,
+                                     "status": moe_status_name(r["status"])}
+                res[label] = per_T
+            b.close()
+            out[name] = {"workload": "deepseek-v3-shaped, residual-split records (%d B), 4 layers, 410 slots, MRS"
+                                     % o[4], "decode_by_umia": res,
+                         "note": "expert_GB_per_s_whole_layer counts the expert bytes read over the whole "
+                                 "layer call (router, plan and miss copies included)"}
         elif name == "quotas":
             # MoE-CORE cache shaping: the headline decode (T = 16, 2765 slots) with the table filled
             # from a profiling trace, uniform quotas and the replayed nonuniform ones

@@ -20,9 +20,9 @@
 // scale multiplies each 16-element partial dot product, which stays inside
 // one 128-wide block), or residual-split codes (RapidMoE §4.4 Alg. 3): 4-bit
 // W^Q and W^R for gate/up, 4-bit W^L or 8-bit W^H for down, fp32 scales per
-// 128-column group.  A critical expert (UMIA, RapidMoE §4.3) computes
-// (W^Q + W^R) x as sq * (q . x) + sr * (r . x) per group and uses W^H_down;
-// the others read W^Q and W^L_down only.
+// 128-column group.  A critical expert (UMIA, RapidMoE §4.3) reads W^Q and
+// W^R (each weight q * sq + r * sr, fp32) and W^H_down; the others read W^Q
+// and W^L_down only.
 #include <cuda_fp8.h>
 
 #include "moeslot_internal.cuh"
@@ -197,38 +197,57 @@ __device__ __forceinline__ void int8x4(uint32_t w, float* v) {
 #pragma unroll
   for (int k = 0; k < 4; ++k) v[k] = (float)((int)(w << (24 - 8 * k)) >> 24);
 }
-// dot product of 32 codes (one 16-byte chunk of nibbles) with 32 activations
-__device__ __forceinline__ float dot32_nib(const uint4& q, const float* x) {
-  float c[8], d = 0.f;
-  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+// 32 weights of one 16-byte chunk of nibbles: q * sq (+ r * sr for a critical entry), fp32
+__device__ __forceinline__ void decode32(const uint4& q, float sq, const uint4& r, float sr, bool crit, float* w) {
+  const uint32_t wq[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    nib8(w[j], c);
+    nib8(wq[j], w + 8 * j);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) d = fmaf(c[k], x[8 * j + k], d);
+    for (int k = 0; k < 8; ++k) w[8 * j + k] *= sq;
   }
-  return d;
+  if (crit) {
+    const uint32_t wr[4] = {r.x, r.y, r.z, r.w};
+    float c[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      nib8(wr[j], c);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) w[8 * j + k] = fmaf(c[k], sr, w[8 * j + k]);
+    }
+  }
 }
 
-// gate/up: every warp owns a contiguous range of (entry, row i) pairs, as ffn_gate_up_kernel;
-// each lane takes 32 columns (16 bytes of codes) at a time
+// gate/up: the work is (entry, chunk of NT tokens, row i) units, entries in order, each entry's
+// units chunk-major; every warp owns a contiguous, equal range of units, so an entry with many
+// tokens (the shared expert) spreads over many warps.  Each lane takes 32 columns (16 bytes of
+// codes) at a time and decodes them once for the unit's tokens.
 template <typename AT>
-__global__ void __launch_bounds__(kFfnWarps * 32)
+__global__ void __launch_bounds__(kFfnWarps * 32, 2)
 ffn_resplit_gate_up_kernel(FfnArgs a) {
-  constexpr int NT = kTokChunk;
+  constexpr int NT = 4;   // tokens per unit: four keep the kernel at two CTAs per SM
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * kFfnWarps + (threadIdx.x >> 5);
   const int nw = gridDim.x * kFfnWarps;
   const int n_work = *a.n_work;
   const int H = a.H, I = a.I;
-  const long long total = (long long)n_work * I;
+  long long total = 0;
+  for (int u = 0; u < n_work; ++u) total += (long long)((a.work[u].n + NT - 1) / NT) * I;
   const long long p0 = total * gw / nw, p1 = total * (gw + 1) / nw;
   const AT* __restrict__ x = static_cast<const AT*>(a.x);
   AT* __restrict__ hout = static_cast<AT*>(a.h);
   const int G = H / 128;
+  int u = 0;
+  long long base = 0;                            // first unit of entry u
   for (long long pp = p0; pp < p1; ++pp) {
-    const int u = (int)(pp / I), i = (int)(pp % I);
+    while (u < n_work && pp >= base + (long long)((a.work[u].n + NT - 1) / NT) * I) {
+      base += (long long)((a.work[u].n + NT - 1) / NT) * I;
+      ++u;
+    }
+    if (u >= n_work) break;
     const WorkEntry ent = a.work[u];
+    const long long local = pp - base;
+    const int tc = (int)(local / I) * NT, i = (int)(local % I);
     const bool crit = ent.crit != 0;
     const uint8_t* qg = ent.rec + a.off13 + (size_t)i * (H / 2);
     const uint8_t* qu = ent.rec + a.off13 + (size_t)(I + i) * (H / 2);
@@ -238,47 +257,43 @@ ffn_resplit_gate_up_kernel(FfnArgs a) {
     const float* squ = reinterpret_cast<const float*>(ent.rec + a.offs13) + (size_t)(I + i) * G;
     const float* srg = reinterpret_cast<const float*>(ent.rec + a.offsr13) + (size_t)i * G;
     const float* sru = reinterpret_cast<const float*>(ent.rec + a.offsr13) + (size_t)(I + i) * G;
-    for (int tc = 0; tc < ent.n; tc += NT) {
-      const int nr = min(NT, ent.n - tc);
-      int tok[NT];
+    const int nr = min(NT, ent.n - tc);
+    int tok[NT];
 #pragma unroll
-      for (int r = 0; r < NT; ++r) tok[r] = r < nr ? a.perm_tok[ent.row0 + tc + r] : 0;
-      float ag[NT], au[NT];
+    for (int r = 0; r < NT; ++r) tok[r] = r < nr ? a.perm_tok[ent.row0 + tc + r] : 0;
+    float ag[NT], au[NT];
 #pragma unroll
-      for (int r = 0; r < NT; ++r) { ag[r] = 0.f; au[r] = 0.f; }
-      for (int h = lane * 32; h < H; h += 32 * 32) {
-        const uint4 cqg = __ldcs(reinterpret_cast<const uint4*>(qg + h / 2));
-        const uint4 cqu = __ldcs(reinterpret_cast<const uint4*>(qu + h / 2));
-        uint4 crg = make_uint4(0u, 0u, 0u, 0u), cru = crg;
-        float s_rg = 0.f, s_ru = 0.f;
-        if (crit) {
-          crg = __ldcs(reinterpret_cast<const uint4*>(rg + h / 2));
-          cru = __ldcs(reinterpret_cast<const uint4*>(ru + h / 2));
-          s_rg = srg[h / 128];
-          s_ru = sru[h / 128];
-        }
-        const float s_qg = sqg[h / 128], s_qu = squ[h / 128];
-#pragma unroll
-        for (int r = 0; r < NT; ++r) {
-          if (r < nr) {
-            float xv[32];
-            Act<AT, 32>::load(x + (size_t)tok[r] * H + h, xv);
-            ag[r] = fmaf(s_qg, dot32_nib(cqg, xv), ag[r]);
-            au[r] = fmaf(s_qu, dot32_nib(cqu, xv), au[r]);
-            if (crit) {
-              ag[r] = fmaf(s_rg, dot32_nib(crg, xv), ag[r]);
-              au[r] = fmaf(s_ru, dot32_nib(cru, xv), au[r]);
-            }
-          }
-        }
+    for (int r = 0; r < NT; ++r) { ag[r] = 0.f; au[r] = 0.f; }
+    for (int h = lane * 32; h < H; h += 32 * 32) {
+      const uint4 cqg = __ldcs(reinterpret_cast<const uint4*>(qg + h / 2));
+      const uint4 cqu = __ldcs(reinterpret_cast<const uint4*>(qu + h / 2));
+      uint4 crg = make_uint4(0u, 0u, 0u, 0u), cru = crg;
+      if (crit) {
+        crg = __ldcs(reinterpret_cast<const uint4*>(rg + h / 2));
+        cru = __ldcs(reinterpret_cast<const uint4*>(ru + h / 2));
       }
+      float wg[32], wu[32];
+      decode32(cqg, sqg[h / 128], crg, crit ? srg[h / 128] : 0.f, crit, wg);
+      decode32(cqu, squ[h / 128], cru, crit ? sru[h / 128] : 0.f, crit, wu);
 #pragma unroll
       for (int r = 0; r < NT; ++r) {
         if (r < nr) {
-          const float g = warp_sum(ag[r]);
-          const float uu = warp_sum(au[r]);
-          if (lane == 0) Act<AT, 8>::store1(hout + (size_t)(ent.row0 + tc + r) * I + i, silu(g) * uu);
+          float xv[32];
+          Act<AT, 32>::load(x + (size_t)tok[r] * H + h, xv);
+          float dg = 0.f, du = 0.f;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) { dg = fmaf(wg[c], xv[c], dg); du = fmaf(wu[c], xv[c], du); }
+          ag[r] += dg;
+          au[r] += du;
         }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < NT; ++r) {
+      if (r < nr) {
+        const float g = warp_sum(ag[r]);
+        const float uu = warp_sum(au[r]);
+        if (lane == 0) Act<AT, 8>::store1(hout + (size_t)(ent.row0 + tc + r) * I + i, silu(g) * uu);
       }
     }
   }

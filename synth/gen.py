@@ -307,12 +307,44 @@ def torch_tile_sw128(w):
     return torch.gather(t, 4, idx).reshape(n, mt, kb, 128, 64).contiguous()
 
 
+def torch_quantize_groups(w, bits):
+    """Device version of quantize_groups for [n, R, C] fp32 -> (int8 [n,R,C], fp32 [n,R,C/128])."""
+    import torch
+    n, R, C = w.shape
+    qmax = float(2 ** (bits - 1) - 1)
+    g = w.reshape(n, R, C // 128, 128)
+    amax = g.abs().amax(dim=-1)
+    scale = torch.where(amax > 0, amax / qmax, torch.ones_like(amax))
+    q = torch.round(g / scale[..., None]).clamp(-qmax, qmax).to(torch.int8)
+    return q.reshape(n, R, C), scale.contiguous()
+
+
+def torch_pack_int4(q):
+    """[n, R, C] int8 codes -> [n, R, C/2] uint8, element 2j in the low nibble."""
+    import torch
+    u = q.view(torch.uint8) & 0x0F
+    return (u[..., 0::2] | (u[..., 1::2] << 4)).contiguous()
+
+
 def torch_encode_records(wl: Workload, w13, w2):
     """Stored records [n, record_bytes] uint8 on the device from fp32 w13/w2 chunks."""
     import torch
     n = w13.shape[0]
     o13, o2, os13, os2, rec = wl.expert_layout()
     out = torch.zeros((n, rec), dtype=torch.uint8, device=w13.device)
+    if wl.weight_dtype == RESPLIT_Q4R4:
+        o = resplit_offsets(wl.H, wl.I)
+        q13, sq13 = torch_quantize_groups(w13, 4)
+        deq = (q13.reshape(n, 2 * wl.I, -1, 128).float() * sq13[..., None]).reshape(w13.shape)
+        r13, sr13 = torch_quantize_groups(w13 - deq, 4)
+        l2, sl2 = torch_quantize_groups(w2, 4)
+        h2, sh2 = torch_quantize_groups(w2, 8)
+        parts = [("q13", torch_pack_int4(q13)), ("r13", torch_pack_int4(r13)), ("l2", torch_pack_int4(l2)),
+                 ("h2", h2.view(torch.uint8)), ("sq13", sq13), ("sr13", sr13), ("sl2", sl2), ("sh2", sh2)]
+        for key, t in parts:
+            raw = t.contiguous().view(n, -1).view(torch.uint8)
+            out[:, o[key]:o[key] + raw.shape[1]] = raw
+        return out
     if wl.weight_dtype == F32:
         parts = [(o13, w13.contiguous()), (o2, w2.contiguous())]
     elif wl.weight_dtype == BF16:
