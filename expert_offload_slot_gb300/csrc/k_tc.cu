@@ -2068,6 +2068,12 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
                        const __grid_constant__ CUtensorMap map_w13, const __grid_constant__ CUtensorMap map_w2, Args a,
                        FusedArgs f, DecodeArgs d) {
   constexpr int NT = DecodeShape<WF, STREAM>::threads;
+  // programmatic dependent launch: this grid may start while the previous kernel of the
+  // stream drains.  Everything below reads data earlier kernels wrote, so the wait comes
+  // first; the trigger after it lets the next layer call's grid be launched early (it waits
+  // the same way), which also keeps every kernel before the previous one complete here.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ uint8_t smem_raw[];
   __shared__ volatile int flag_sh;
   __shared__ LocalPlan lp_sh;
@@ -2730,18 +2736,33 @@ static bool fused_setup(const PoolDev& p, const Scratch& sc, int T, const void* 
 
 static size_t fused_smem(int N, int stages) { return (size_t)stages * tc::fused_stage_bytes(N) + 1024; }
 
-static int launch_cooperative(const void* fn, int threads, size_t smem, cudaStream_t s, void** args) {
+// pdl: programmatic dependent launch — the grid may be launched while the previous kernel
+// of the stream drains; the kernel waits for it (griddepcontrol.wait) before reading
+// anything.  If the driver refuses the combination with a cooperative launch, the launch
+// is repeated without it and later launches do not ask again.
+static int launch_cooperative(const void* fn, int threads, size_t smem, cudaStream_t s, void** args,
+                              bool pdl = false) {
+  static bool pdl_refused = false;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sm_count());
   cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelExC(&cfg, fn, args) == cudaSuccess ? 1 : -2;
+  cfg.numAttrs = pdl && !pdl_refused ? 2 : 1;
+  if (cudaLaunchKernelExC(&cfg, fn, args) == cudaSuccess) return 1;
+  if (cfg.numAttrs == 2) {
+    cudaGetLastError();
+    pdl_refused = true;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelExC(&cfg, fn, args) == cudaSuccess) return 1;
+  }
+  return -2;
 }
 
 static void set_smem_attr_once(const void* fn, bool* configured) {
@@ -2871,7 +2892,7 @@ static int launch_decode_layer_impl(const PoolDev& p, const Scratch& sc, const T
   const void* fn = reinterpret_cast<const void*>(tc::tc_decode_layer_kernel<WF, STREAM>);
   set_smem_attr_once(fn, configured);
   void* args[] = {&xm, &hm, &w13, &w2, &a, &f, &d};
-  return launch_cooperative(fn, NT, smem, s, args);
+  return launch_cooperative(fn, NT, smem, s, args, /*pdl=*/true);
 }
 
 int launch_tc_decode_layer(const PoolDev& p, const Scratch& sc, const TcMaps* m, int layer, int T, const void* x,
