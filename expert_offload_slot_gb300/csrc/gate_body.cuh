@@ -151,6 +151,107 @@ __device__ __forceinline__ void gate_one_token(const float* __restrict__ z, int 
   __syncwarp();
 }
 
+// Unsigned key of a logit whose integer order is the float order: NaN ranks as -inf
+// and -0 as +0 (equal logits tie, the lower id first); 0 is below every key and marks
+// a taken or absent expert.
+__device__ __forceinline__ uint32_t logit_key(float v) {
+  if (isnan(v)) v = -INFINITY;
+  if (v == 0.f) v = 0.f;
+  const uint32_t b = __float_as_uint(v);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_logit(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
+// One warp: gate and top-k of token t from its logits zs[t][0..E) in shared memory, as
+// gate_one_token (same selection, weights and probabilities), each arg-max round taken
+// by two warp reductions (the largest key, then the lowest expert id holding it).
+// PER: logits per lane (E <= 32 * PER).  ids_s / w_s: the token's k ids and weights in
+// rank order (shared memory); flag_s (shared memory, optional): set to 1 for every
+// selected expert.  When ids is not null the warp also writes the global routing outputs
+// (ids, w, probs, gap) and the near-tie count.
+template <int PER>
+__device__ __forceinline__ void gate_warp_keys(const float* zs, int t, int E, int k, int gating, int32_t* ids_s,
+                                               float* w_s, int32_t* ids, float* w, float* probs, float* gap,
+                                               unsigned long long* stats, int* flag_s) {
+  const int lane = threadIdx.x & 31;
+  float v[PER];
+  uint32_t key[PER];
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int e = lane + 32 * j;
+    v[j] = e < E ? zs[(size_t)t * E + e] : -INFINITY;
+    key[j] = e < E ? logit_key(v[j]) : 0u;
+  }
+  float zmax = -INFINITY, zmine = 0.f, next_best = INFINITY;
+  const int rounds = k < E ? k + 1 : k;
+  for (int r = 0; r < rounds; ++r) {
+    uint32_t bk = 0u, be = 0xffffffffu;
+#pragma unroll
+    for (int j = 0; j < PER; ++j)
+      if (key[j] > bk) { bk = key[j]; be = (uint32_t)(lane + 32 * j); }
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
+    const uint32_t emin = __reduce_min_sync(0xffffffffu, bk == kmax ? be : 0xffffffffu);
+    const float val = key_logit(kmax);
+    if (r == 0) zmax = val;
+    if (r < k) {
+#pragma unroll
+      for (int j = 0; j < PER; ++j)
+        if ((uint32_t)(lane + 32 * j) == emin) key[j] = 0u;
+      if (lane == r) zmine = val;
+      if (lane == 0) {
+        ids_s[t * k + r] = (int32_t)emin;
+        if (flag_s) flag_s[emin] = 1;
+        if (ids) ids[(size_t)t * k + r] = (int32_t)emin;
+      }
+    } else {
+      next_best = val;
+    }
+  }
+  float num = 0.f;
+  if (lane < k) num = gating == MOE_GATE_SOFTMAX_RENORM ? expf(zmine - zmax) : 1.f / (1.f + expf(-zmine));
+  const float den = warp_sum(num);
+  if (lane < k) {
+    w_s[t * k + lane] = num / den;
+    if (ids) w[(size_t)t * k + lane] = num / den;
+  }
+  if (ids) {
+    const float zk = __shfl_sync(0xffffffffu, zmine, k - 1);
+    const float g = k < E ? zk - next_best : INFINITY;
+    if (lane == 0) {
+      gap[t] = g;
+      if (g < 1e-4f) atomicAdd(&stats[ST_NEAR_TIES], 1ull);
+    }
+    if (gating == MOE_GATE_SOFTMAX_RENORM) {
+      float part = 0.f, ex[PER];
+#pragma unroll
+      for (int j = 0; j < PER; ++j) {
+        ex[j] = lane + 32 * j < E ? expf(v[j] - zmax) : 0.f;
+        part += ex[j];
+      }
+      const float pden = warp_sum(part);
+#pragma unroll
+      for (int j = 0; j < PER; ++j)
+        if (lane + 32 * j < E) probs[(size_t)t * E + lane + 32 * j] = ex[j] / pden;
+    } else {
+#pragma unroll
+      for (int j = 0; j < PER; ++j)
+        if (lane + 32 * j < E) probs[(size_t)t * E + lane + 32 * j] = 1.f / (1.f + expf(-v[j]));
+    }
+  }
+  __syncwarp();
+}
+
+// Every token of a step gated by the CTA's NW warps, one token per warp at a time.
+template <int PER>
+__device__ __forceinline__ void gate_tokens_warps(const float* zs, int T, int E, int k, int gating, int32_t* ids_s,
+                                                  float* w_s, int32_t* ids, float* w, float* probs, float* gap,
+                                                  unsigned long long* stats, int NW, int* flag_s) {
+  for (int t = threadIdx.x >> 5; t < T; t += NW)
+    gate_warp_keys<PER>(zs, t, E, k, gating, ids_s, w_s, ids, w, probs, gap, stats, flag_s);
+}
+
 // Gate and top-k of token t by a whole CTA of NT >= E threads, thread e holding
 // expert e (the decode layer kernel: a token's last routing CTA has all its
 // threads free, and one warp's serial arg-max rounds are the long pole).  Same

@@ -703,6 +703,7 @@ struct LocalPlan {
   int rid[kMaxE + 1];              // record of each resident entry
   int32_t ids[kLocalMaxTk];        // the step's routing
   float w[kLocalMaxTk];
+  int16_t epos[kMaxE];             // work position of each expert with tokens
 };
 
 struct FusedArgs {
@@ -727,9 +728,9 @@ struct FusedArgs {
   const int32_t* ecount;        // [2]
   int E1;                       // E + 1
   float* gu_partial;            // gate/up split partials
-  size_t gu_partial_floats;
+  int gu_cap;                   // (tile, split) partials gu_partial holds at this call's token count
   float* dn_partial;            // per-entry down partials
-  size_t dn_partial_floats;
+  int dn_cap;                   // (tile, split) partials dn_partial holds at this call's token count
   int32_t* gu_cnt;              // [E1 * MT_I] split arrivals per gate/up tile    } zeroed by the plan
   uint32_t* dn_done;            // CTAs whose down units are all written           } kernel before
   uint32_t* hready;             // [E1] finished gate/up tiles per entry           } every launch
@@ -765,13 +766,13 @@ __device__ __forceinline__ FSched fused_sched(const Args& a, const FusedArgs& f,
   // unit (all units of a step share one round-robin schedule, so per-phase wave
   // quantisation matters little, while every unit costs a partial round trip).
   const int gu_tiles = s.n * s.mt_i;
-  const size_t gcap = f.gu_partial_floats / ((size_t)2 * s.cols * BM);
+  const int gcap = f.gu_cap;
   s.sg = max(1, min(min(s.kb_h, 8), (2 * G + gu_tiles - 1) / max(gu_tiles, 1)));
-  while (s.sg > 1 && (size_t)gu_tiles * s.sg > gcap) --s.sg;
+  while (s.sg > 1 && gu_tiles * s.sg > gcap) --s.sg;
   const int dn_tiles = s.n * s.mt_h;
-  const size_t dcap = f.dn_partial_floats / ((size_t)s.cols * BM);
+  const int dcap = f.dn_cap;
   s.sd = max(1, min(min(s.kb_i, 4), (G + dn_tiles - 1) / max(dn_tiles, 1)));
-  while (s.sd > 1 && (size_t)dn_tiles * s.sd > dcap) --s.sd;
+  while (s.sd > 1 && dn_tiles * s.sd > dcap) --s.sd;
   s.p0 = s.nh * s.mt_i * s.sg;
   s.p1 = s.nh * s.mt_h * s.sd;
   s.p2 = s.nm * s.mt_i * s.sg;
@@ -1127,14 +1128,20 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
             if (got < nmu) g = nhit + got;
           }
         }
+        bool ask = false;
         if (g == kNone && hn < nhit) {
           g = hn;
-          hraw = atomicAdd(f.next_unit, 1u);   // the next one, while this one's loads go out
-          hpend = true;
+          ask = true;
         }
         if (g == kNone) break;
         publish_unit(npub, (int)g);
         ++npub;
+        if (ask) {
+          // the next one, while this one's loads go out; asked only after the publish, whose
+          // fence would otherwise wait for the counter's round trip
+          hraw = atomicAdd(f.next_unit, 1u);
+          hpend = true;
+        }
         const FUnit r = fused_unit(sc, f, (int)g);
         int rid = 0;
         if (!r.miss) rid = f.lp ? f.lp->rid[r.u] : a.work[r.u].rid;
@@ -1540,17 +1547,40 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
       // added), so its 16 loads are independent and all in flight at once.
       float acc = 0.f;
       const int sd = sc.sd;
-      for (int p0 = 0; p0 < parts; p0 += 16) {
-        float v[16];
+      if (f.lp) {
+        // local lists: only the token's own entries (every other entry's partial for it is
+        // +-0, its h column being zero), in the token's gate rank order, then the shared
+        // expert: a fixed order for a given routing
+        const LocalPlan& lp = *f.lp;
+        const int kq = lp.k, kp = kq + (lp.n > 0 && lp.expert[lp.n - 1] < 0 ? 1 : 0);
+        const int tparts = kp * sd;
+        for (int p0 = 0; p0 < tparts; p0 += 16) {
+          float v[16];
 #pragma unroll
-        for (int b = 0; b < 16; ++b) {
-          const int q = min(p0 + b, parts - 1);
-          const int u = sd == 1 ? q : q / sd;
-          v[b] = __ldcg(base + (size_t)u * ustride + (size_t)(q - u * sd) * tile_el);
+          for (int b = 0; b < 16; ++b) {
+            const int q = min(p0 + b, tparts - 1);
+            const int j = sd == 1 ? q : q / sd;
+            const int e = j < kq ? lp.ids[t * kq + j] : -1;
+            const int u = (unsigned)e < (unsigned)kMaxE ? lp.epos[e] : lp.n - 1;
+            v[b] = __ldcg(base + (size_t)u * ustride + (size_t)(q - j * sd) * tile_el);
+          }
+#pragma unroll
+          for (int b = 0; b < 16; ++b)
+            if (p0 + b < tparts) acc += v[b];
         }
+      } else {
+        for (int p0 = 0; p0 < parts; p0 += 16) {
+          float v[16];
 #pragma unroll
-        for (int b = 0; b < 16; ++b)
-          if (p0 + b < parts) acc += v[b];
+          for (int b = 0; b < 16; ++b) {
+            const int q = min(p0 + b, parts - 1);
+            const int u = sd == 1 ? q : q / sd;
+            v[b] = __ldcg(base + (size_t)u * ustride + (size_t)(q - u * sd) * tile_el);
+          }
+#pragma unroll
+          for (int b = 0; b < 16; ++b)
+            if (p0 + b < parts) acc += v[b];
+        }
       }
       a.out[(size_t)t * a.H + m] = f32_to_bf16_rn(acc);
     }
@@ -1722,8 +1752,6 @@ __device__ __forceinline__ void stream_ffn(const CUtensorMap* map_w13, const CUt
       const uint32_t nfirst = (uint32_t)(G - f.cta0_plans - ncopy);
       uint32_t g = first >= 0 ? (uint32_t)first : nfirst + atomicAdd(f.next_unit, 1u);
       while (ok && g < n1) {
-        // the next one, while this one's loads go out (its value is read after them)
-        const uint32_t graw = atomicAdd(f.next_unit, 1u);
         const int li = (int)g / per1, rem = (int)g - li * per1;
         const int mt = rem / rg_tile, rg = rem - mt * rg_tile;
         const bool miss = li >= nh;
@@ -1734,6 +1762,9 @@ __device__ __forceinline__ void stream_ffn(const CUtensorMap* map_w13, const CUt
           asm volatile("fence.proxy.async.global;" ::: "memory");
         }
         publish(npub++, (int)g);
+        // the next one, while this one's loads go out (its value is read after them; asked
+        // after the publish, whose fence would otherwise wait for the counter's round trip)
+        const uint32_t graw = atomicAdd(f.next_unit, 1u);
         const int rid = record_of(u);
         for (int kb0 = 0; kb0 < kb_h; kb0 += kStreamKb, ++it) {
           int s;
@@ -1753,7 +1784,7 @@ __device__ __forceinline__ void stream_ffn(const CUtensorMap* map_w13, const CUt
         tma_load_4d(ring + (size_t)s * kStreamStage + kStreamHOff, map_h, &full_bar[s], 0, kb0, 0, u);
       };
       auto arrival = [&]() -> bool {
-        if (!wait_count(p1_done, (uint32_t)G * kStreamWarps, a.status, a.wait_ns)) return false;
+        if (!wait_count(p1_done, (uint32_t)(G - f.cta0_plans) * kStreamWarps, a.status, a.wait_ns)) return false;
         asm volatile("fence.proxy.async.global;" ::: "memory");   // h written by every CTA -> bulk reads
         h_ok = true;
         for (int q = 0; q < npend; ++q) issue_h(pend_s[q], pend_u[q], pend_kb[q]);
@@ -1761,6 +1792,8 @@ __device__ __forceinline__ void stream_ffn(const CUtensorMap* map_w13, const CUt
         return true;
       };
       while (ok) {
+        // one unit at a time: a CTA reaching phase 2 early must not hold a second unit that
+        // a CTA arriving later would start sooner
         const uint32_t g2 = atomicAdd(f.next_miss, 1u);
         if (g2 >= n2) break;
         publish(npub++, kStreamP2 | (int)g2);
@@ -2031,12 +2064,19 @@ tc_fused_decode_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
 //          landing record at once and computed from there, and written to its
 //          slot once the plan has chosen it.  Otherwise every CTA waits for the
 //          plan's work lists.
-// Counters: route_done (tokens gated) counts T gates plus CTA 0's zeroing of
-// the expert counters; tickets reset on their last arrival; plan_done,
+// Fast gate (local lists without substitution): no ticket and no gating CTA; each
+// routing CTA adds one to route_done once its logits are written, and every CTA,
+// once all are, stages the step's logits [T][E] in shared memory and gates every
+// token itself, one warp per token (CTA 0 also writes the routing outputs the plan
+// and the routing dump read).
+// Counters: route_done counts T gates (fast gate: T * nblk routing CTAs) plus CTA
+// 0's zeroing of the expert counters; tickets reset on their last arrival; plan_done,
 // snap_done, slots_ready (and, after a timeout, the others) are reset by the
 // last CTA to leave, so each launch starts from zero.
 struct DecodeArgs {
   int local;                // every CTA derives the step's entry lists itself (T * k <= kLocalMaxTk)
+  int fast;                 // (streaming variant, local lists, no substitution) every CTA gates every token itself
+  int zoff;                 // fast: byte offset in dynamic shared memory of the staged logits [T][E]
   const uint16_t* x;        // [T][H] bf16
   const uint16_t* wr;       // this layer's router [E][H] bf16
   const float* rb;          // [E]
@@ -2065,8 +2105,8 @@ template <int WF, bool STREAM> struct DecodeShape {
 template <int WF, bool STREAM>
 __global__ void __launch_bounds__(DecodeShape<WF, STREAM>::threads, 1)
 tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_h,
-                       const __grid_constant__ CUtensorMap map_w13, const __grid_constant__ CUtensorMap map_w2, Args a,
-                       FusedArgs f, DecodeArgs d) {
+                       const __grid_constant__ CUtensorMap map_w13, const __grid_constant__ CUtensorMap map_w2,
+                       Args a, FusedArgs f, DecodeArgs d) {
   constexpr int NT = DecodeShape<WF, STREAM>::threads;
   // programmatic dependent launch: this grid may start while the previous kernel of the
   // stream drains.  Everything below reads data earlier kernels wrote, so the wait comes
@@ -2091,6 +2131,9 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
   auto ticket = [&](int t) -> uint32_t* { return d.dsync + (kDsTicket + t) * kSyncLine; };
   const PoolDev& p = d.plan.p;
   const int l = d.plan.layer;
+  // the fast gate exists in the streaming variant only (compiled out of the other, where it
+  // measured slower: several tokens per warp)
+  const bool fast = STREAM && d.fast;
 
   // this CTA's copy of the layer's table row, taken before the plan may change it: loaded
   // now; a routing CTA stores and releases it after its logits, off the routing's path
@@ -2107,6 +2150,7 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
     if (threadIdx.x == 0) release_add(snap_done);
   };
   if (d.local) {
+    for (int e = threadIdx.x; e < kMaxE; e += NT) cnt_sh[e] = 0;   // ordered before its use by later barriers
 #pragma unroll
     for (int i = 0; i < kSnapPer; ++i) {
       const int e = threadIdx.x + i * NT;
@@ -2164,7 +2208,10 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
       if (lane == 0) d.z[(size_t)t * E + e] = acc + d.rb[e];
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (fast) {
+      // this CTA's logits (ordered before the release by the barrier)
+      if (threadIdx.x == 0) release_add(route_done);
+    } else if (threadIdx.x == 0) {
       // one acquire-release add: it releases this CTA's logits (ordered before it by the
       // barrier), and the token's last CTA acquires every other CTA's
       const uint32_t old = atom_add_acq_rel(ticket(t), 1u);
@@ -2172,9 +2219,10 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
       if (flag_sh) *ticket(t) = 0u;
     }
     __syncthreads();
-    if (flag_sh) {
-      // the token's gate by the whole CTA; scratch: the dynamic shared memory x was staged in
-      // (substitution reads the layer's table row: the plan changes it only after every gate)
+    if (!fast && flag_sh) {
+      // the token's gate by the whole CTA (measured faster here than one warp's arg-max
+      // rounds); scratch: this CTA's dynamic shared memory (substitution reads the layer's
+      // table row: the plan changes it only after every gate)
       gate_token_cta<NT>(d.z, t, E, d.plan.p.k, d.plan.p.gating, d.plan.sc.ids, d.plan.sc.w, d.plan.sc.probs,
                          d.plan.sc.gap, d.plan.p.stats, *reinterpret_cast<GateCtaScratch*>(dsm),
                          p.aes_on ? p.lut + (size_t)l * E : nullptr, p.aes_alpha);
@@ -2198,9 +2246,10 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
     fl.S = p.S;
   }
   auto pre = [&]() -> bool {
-    // every token gated (and the counters zeroed)
+    // every token gated, or (fast gate) every logit written, and the counters zeroed
     if (threadIdx.x == 0) {
-      flag_sh = wait_count(route_done, (uint32_t)T + 1u, a.status, a.wait_ns) ? 1 : 0;
+      const uint32_t target = (uint32_t)(fast ? T * d.nblk : T) + 1u;
+      flag_sh = wait_count(route_done, target, a.status, a.wait_ns) ? 1 : 0;
       if (!flag_sh) set_status(a.status, MOE_ERR_TIMEOUT);
     }
     __syncthreads();
@@ -2213,18 +2262,39 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
       // the step's entry lists, as the plan orders them: experts with tokens ascending,
       // then the shared expert; resident / copied by the table row at the step's start
       const int tk = T * p.k;
-      for (int e = threadIdx.x; e < E; e += NT) cnt_sh[e] = 0;
-      for (int i = threadIdx.x; i < tk; i += NT) {
-        lp_sh.ids[i] = __ldcg(d.plan.sc.ids + i);
-        lp_sh.w[i] = __ldcg(d.plan.sc.w + i);
-      }
-      __syncthreads();
-      for (int i = threadIdx.x; i < tk; i += NT) {
-        const int e = lp_sh.ids[i];
-        if ((unsigned)e < (unsigned)E) atomicAdd(&cnt_sh[e], 1);
+      // cnt_sh (zeroed at kernel start): 1 for every expert with tokens
+      if (fast) {
+        // the step's logits into shared memory, then one warp per token
+        float* zs = reinterpret_cast<float*>(dsm + d.zoff);
+        const int n = T * E;
+        if ((E & 3) == 0) {
+          for (int i = threadIdx.x; i < n / 4; i += NT)
+            reinterpret_cast<float4*>(zs)[i] = __ldcg(reinterpret_cast<const float4*>(d.z) + i);
+        } else {
+          for (int i = threadIdx.x; i < n; i += NT) zs[i] = __ldcg(d.z + i);
+        }
+        __syncthreads();
+        // CTA 0 also writes the routing outputs
+        int32_t* gids = blockIdx.x == 0 ? d.plan.sc.ids : nullptr;
+        if (E <= 128)
+          gate_tokens_warps<4>(zs, T, E, p.k, p.gating, lp_sh.ids, lp_sh.w, gids, d.plan.sc.w, d.plan.sc.probs,
+                               d.plan.sc.gap, p.stats, NT / 32, cnt_sh);
+        else
+          gate_tokens_warps<kMaxPerLane>(zs, T, E, p.k, p.gating, lp_sh.ids, lp_sh.w, gids, d.plan.sc.w,
+                                         d.plan.sc.probs, d.plan.sc.gap, p.stats, NT / 32, cnt_sh);
+        if (gids) __threadfence();   // the routing outputs, before the plan reads them
+      } else {
+        for (int i = threadIdx.x; i < tk; i += NT) {
+          const int e = __ldcg(d.plan.sc.ids + i);
+          lp_sh.ids[i] = e;
+          lp_sh.w[i] = __ldcg(d.plan.sc.w + i);
+          if ((unsigned)e < (unsigned)E) cnt_sh[e] = 1;
+        }
       }
       __syncthreads();
       if (warp == 0) {
+        // the step's entry lists, as the plan orders them: experts with tokens ascending,
+        // then the shared expert; resident / copied by the table row at the step's start
         int pos_run = 0, nh_run = 0, nm_run = 0;
         const unsigned lower = (1u << lane) - 1u;
         for (int e0 = 0; e0 < E; e0 += 32) {
@@ -2236,6 +2306,7 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
                          mmis = __ballot_sync(0xffffffffu, has && !hit);
           if (has) {
             const int pos = pos_run + __popc(mhas & lower);
+            lp_sh.epos[e] = (int16_t)pos;
             lp_sh.expert[pos] = e;
             lp_sh.rid[pos] = hit ? sl : -1;
             if (hit) lp_sh.elist[0][nh_run + __popc(mhit & lower)] = pos;
@@ -2282,7 +2353,13 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
     return true;
   };
   if constexpr (STREAM) {
-    stream_ffn(&map_w13, &map_w2, &map_h, a, fl, d.x, smem_raw, pre);
+    // The planner takes no streaming units: at one to four tokens the plan lasts about as
+    // long as the FFN, and the FFN's phase barrier would wait for it (the other CTAs count
+    // G - 1 arrivals).  The streaming variant always runs on local lists.
+    if (blockIdx.x == 0)
+      pre();
+    else
+      stream_ffn(&map_w13, &map_w2, &map_h, a, fl, d.x, smem_raw, pre);
   } else {
     fused_ffn<WF>(&map_x, &map_h, &map_w13, &map_w2, a, fl, smem_raw, pre);
   }
@@ -2718,10 +2795,13 @@ static bool fused_setup(const PoolDev& p, const Scratch& sc, int T, const void* 
   f.elist = sc.elist;
   f.ecount = sc.ecount;
   f.E1 = p.E + 1;
+  // the partial buffers' capacities in (tile, split) partials of this call's columns (the
+  // token count rounded up to 4), worked out here so that no kernel divides 64-bit sizes
+  const size_t cols = (size_t)((T + 3) & ~3);
   f.gu_partial = sc.partial;
-  f.gu_partial_floats = sc.partial_floats;
+  f.gu_cap = (int)std::min<size_t>(sc.partial_floats / (2 * cols * tc::BM), (size_t)INT32_MAX);
   f.dn_partial = sc.dn_partial;
-  f.dn_partial_floats = sc.dn_partial_floats;
+  f.dn_cap = (int)std::min<size_t>(sc.dn_partial_floats / (cols * tc::BM), (size_t)INT32_MAX);
   f.gu_cnt = sc.ffn_sync;
   f.dn_done = reinterpret_cast<uint32_t*>(sc.ffn_sync + dn_done_index(p));
   f.hready = f.dn_done + tc::kSyncLine;
@@ -2887,7 +2967,15 @@ static int launch_decode_layer_impl(const PoolDev& p, const Scratch& sc, const T
     a.stages = std::min<int>(tc::kMaxStages, (int)((tc::kSmemBudget - xb) / tc::kStreamStage));
     ffn_smem = 1024 + xb + (size_t)a.stages * tc::kStreamStage;
   }
-  const size_t smem = std::max(std::max(ffn_smem, psm + 1024), (size_t)p.H * 2 + 16 + 1024);
+  size_t smem = std::max(std::max(ffn_smem, psm + 1024), (size_t)p.H * 2 + 16 + 1024);
+  // fast gate: the staged logits after the plan's shared memory (CTA 0 prestages the plan's
+  // inputs while it gates)
+  const size_t zoff = (psm + 15) & ~(size_t)15, zend = zoff + (size_t)T * p.E * 4 + 16;
+  // (the streaming variant, one token: a gate per token on its own routing CTA measured
+  // faster once a warp has to gate several tokens)
+  d.fast = STREAM && d.local && !p.aes_on && T <= NT / 32 && zend <= (size_t)tc::kSmemBudget + 1024 ? 1 : 0;
+  d.zoff = (int)zoff;
+  if (d.fast) smem = std::max(smem, zend);
   static bool configured[64] = {};
   const void* fn = reinterpret_cast<const void*>(tc::tc_decode_layer_kernel<WF, STREAM>);
   set_smem_attr_once(fn, configured);
