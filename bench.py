@@ -66,7 +66,7 @@ def parse_args():
     ap.add_argument("--top-k", type=int, default=0, help="profiling only: top-k with --experts (0 = the workload's)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--configs",
-                    default="qwen3_hit,s_independence,prefetch,quotas,qwen3_prefill,dsv3,dsv3_resplit,mixtral",
+                    default="qwen3_hit,s_independence,prefetch,quotas,aes,qwen3_prefill,dsv3,dsv3_resplit,mixtral",
                     help="other workloads measured at N=1 and reported under 'configs' ('' for none)")
     ap.add_argument("--probe-link", action="store_true",
                     help="measure the host->GPU link: device-started record copies vs DMA, then exit")
@@ -324,7 +324,8 @@ class PoolBench:
                "bytes_copied": st1["bytes_copied"] - st0["bytes_copied"], "clocks": clk,
                "prefetch": {n: st1["prefetch_" + n] - st0["prefetch_" + n]
                             for n in ("issued", "committed", "demanded", "bytes")},
-               "critical_entries": st1["critical_entries"] - st0["critical_entries"]}
+               "critical_entries": st1["critical_entries"] - st0["critical_entries"],
+               "aes_substitutions": st1["aes_substitutions"] - st0["aes_substitutions"]}
         res["status"] = self.pool.status()
         # profiling pass: per-stage CUDA-event times of every layer, same workload continued
         res["prof"] = self.profile_decode(xs[W + K:W + K + P], x_in, out, s, T, prof_steps) if prof_steps > 0 else \
@@ -658,7 +659,8 @@ def run_configs(names, dev, qwen_host, args, peaks, link_gbs):
     q = get_workload("qwen3_decode")
     for name in names:
         t0 = time.time()
-        if name not in ("qwen3_hit", "s_independence", "quotas", "prefetch") and qwen_host is not None and qwen_host.ptr:
+        if name not in ("qwen3_hit", "s_independence", "quotas", "prefetch", "aes") and qwen_host is not None and \
+                qwen_host.ptr:
             qwen_host.free()             # the remaining configs bring host pools of their own
         if name == "qwen3_hit":
             # every expert resident (S = L*E): the hit path alone, no miss copies
@@ -696,6 +698,58 @@ def run_configs(names, dev, qwen_host, args, peaks, link_gbs):
                     base = res["0"]
             out[name] = {"workload": "qwen3-30b-a3b-shaped-decode, T=16, 2765 slots, MRS; per_step 0 / 1 / 2",
                          "by_per_step": res}
+        elif name == "aes":
+            # MoE-CORE approximate expert substitution (off in the page's main numbers): the headline
+            # decode with substitution at two logit margins, reported as availability (hit rate,
+            # demand misses, time) and as output deviation.  The deviation compares each layer call's
+            # output with the exact routing's, which any pool without substitution computes (its
+            # output does not depend on its resident set): two pools fed the same inputs eagerly.
+            import torch
+
+            import expert_offload_slot_gb300 as moe
+            res = {}
+            base = None
+            for alpha in (None, 0.05, 0.2):
+                b = PoolBench(q, 16, dev, host=qwen_host)
+                if alpha is not None:
+                    b.pool.set_aes(1, alpha)
+                r = b.decode(16, 8, 64, 0, Clocks(torch_local()), 1, e2e=False)
+                steps = r["steps"] * q.L
+                row = {"tokens_per_s": r["steps"] * 16 * q.L / (r["ms"] / 1e3),
+                       "us_per_layer": r["ms"] * 1e3 / steps,
+                       "hit_rate": r["hits"] / max(1, r["hits"] + r["misses"]),
+                       "demand_misses_per_layer_step": r["misses"] / steps,
+                       "substitutions_per_layer_step": r["aes_substitutions"] / steps,
+                       "status": moe_status_name(r["status"])}
+                if alpha is not None:
+                    # output deviation over 4 eager steps of a continued trace (all 48 layers each)
+                    ex = PoolBench(q, 16, dev, host=qwen_host)
+                    xs = __import__("synth").gen.torch_decode_hidden(q, 16, 4, dev, base_seed=977)
+                    o1 = torch.empty_like(xs[0][0])
+                    o2 = torch.empty_like(o1)
+                    rel = []
+                    s_ = torch.cuda.Stream()
+                    with torch.cuda.stream(s_):
+                        for st in range(4):
+                            for l in range(q.L):
+                                b.pool.forward(l, xs[st][l], o1, moe.MOE_MODE_DECODE)
+                                ex.pool.forward(l, xs[st][l], o2, moe.MOE_MODE_DECODE)
+                                a_ = o1.float()
+                                e_ = o2.float()
+                                rel.append((torch.linalg.vector_norm(a_ - e_) / torch.linalg.vector_norm(e_)).item())
+                    ex.close()
+                    row["alpha"] = alpha
+                    row["output_rel_l2_mean"] = sum(rel) / len(rel)
+                    row["output_rel_l2_max"] = max(rel)
+                    row["vs_exact_time"] = base["us_per_layer"] / row["us_per_layer"]
+                b.close()
+                res["off" if alpha is None else "alpha_%g" % alpha] = row
+                if alpha is None:
+                    base = row
+            out[name] = {"workload": "qwen3-30b-a3b-shaped-decode, T=16, 2765 slots, MRS; substitution off / "
+                                     "logit margin 0.05 / 0.2",
+                         "by_alpha": res,
+                         "deviation": "relative L2 norm of (output - exact-routing output) per layer call"}
         elif name == "dsv3_resplit":
             # RapidMoE residual-split experts on the DeepSeek-V3 expert shape (4-bit W^Q + 4-bit
             # residual for gate/up, 4- or 8-bit down, own codec), UMIA deciding each step's precision:
