@@ -50,6 +50,7 @@ int launch_plan(const PoolDev& p, const Scratch& sc, int layer, int T, const int
   a.ids = ids;
   a.w = w;
   a.probs = probs;
+  a.gather_bn = gather_tile_rows(p, T);
   const size_t smem = plan_smem_bytes(p, sc.tmax, &a.owner_cap, &a.tok_rows);
   static size_t configured = 0;
   if (smem > configured) {

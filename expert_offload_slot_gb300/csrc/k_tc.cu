@@ -77,7 +77,6 @@ constexpr int kThreads = 192;
 constexpr int kMaxStages = 8;
 constexpr int kSmemBudget = 200 * 1024;
 constexpr int kModeGateUp = 0, kModeDown = 1, kModeGateUpGather = 2, kModeDownGather = 3;
-constexpr int kGatherBN = 128;   // tokens per tile in the gather modes
 constexpr uint32_t kTileBytes = BM * BK * 2;   // one 128 x 64 bf16 tile
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -220,7 +219,7 @@ struct Args {
   const int32_t* n_work;
   const int32_t* sel;        // gate_up dense: the entries to process (indices into work), or null for all
   const int32_t* sel_count;
-  const int32_t* ntile0;     // gather modes: first 128-token tile of each entry ([E+2], prefix)
+  const int32_t* ntile0;     // gather modes: first token tile of each entry ([E+2], prefix)
   const uint8_t* records;    // record array base
   size_t rec, off13, off2;   // record bytes, w13 / w2 tile offsets
   int T, N, H, I, num_sms, stages;
@@ -449,8 +448,8 @@ template <int WF> struct GatherShape {
   static constexpr int threads = kThreads + (WF == kWfFp8 ? 32 * kConvWarps : 0);
 };
 
-// Gather modes (T > 256 tokens): unit = (entry u, 128-token tile nt, 128-row tile
-// mt), full K.  Gate/up: A = gate and up tiles of the entry, B = its gathered x
+// Gather modes (T > 256 tokens): unit = (entry u, token tile nt of N = 128 or 256
+// rows, 128-row tile mt), full K (the plan's ntile0 counts tiles of the same N).  Gate/up: A = gate and up tiles of the entry, B = its gathered x
 // rows; epilogue h = w * SiLU(g) * u per row.  Down: A = W_down tile, B = its h
 // rows; epilogue one bf16 row of y per (token, expert).
 template <int MODE, int WF>
@@ -513,7 +512,7 @@ tc_gather_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constan
         const WorkEntry we = a.work[r.u0];
         const uint8_t* wbase = a.records + (size_t)we.rid * a.rec + (is_gate_up(MODE) ? a.off13 : a.off2) +
                                (size_t)r.mt * kb_per_row * a_bytes;
-        const int brow = we.row0 + r.nt * kGatherBN;
+        const int brow = we.row0 + r.nt * N;
         for (int kb = r.kb0; kb < r.kb1; ++kb, ++it) {
           const int s = it % S;
           if (it >= (uint32_t)S && !mbar_wait(&empty_bar[s], ((it / S) - 1) & 1)) { ok = false; break; }
@@ -606,7 +605,7 @@ tc_gather_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constan
       fence_after();
       const int m = r.mt * BM + row;                           // output row (i for gate/up, h for down)
       const WorkEntry we = a.work[r.u0];
-      const int row_base = we.row0 + r.nt * kGatherBN, row_end = we.row0 + we.n;
+      const int row_base = we.row0 + r.nt * N, row_end = we.row0 + we.n;
       for (int c0 = 0; c0 < N; c0 += 16) {
         float d0[16], d1[16];
         tmem_ld16(trow + c0, d0);
@@ -2730,18 +2729,23 @@ static tc::Args tc_args(const PoolDev& p, const Scratch& sc, int T, int N) {
   return a;
 }
 
+int gather_tile_rows(const PoolDev& p, int T) {
+  return (long long)T * p.k >= 192LL * p.E ? 256 : 128;
+}
+
 // Gather path: xp = x rows by expert; h = gate/up per row; y = down per row; out = combine.
 int launch_tc_gather(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, const void* x, void* out,
                      cudaStream_t s) {
   const int rows_max = T * p.k + (p.shared ? T : 0);
   tc::gather_rows_kernel<<<2 * sm_count(), 256, 0, s>>>(static_cast<const uint16_t*>(x), sc.perm_tok, sc.n_rows,
                                                          sc.xp, p.H);
-  tc::Args a = tc_args(p, sc, T, tc::kGatherBN);
+  const int bn = gather_tile_rows(p, T);
+  tc::Args a = tc_args(p, sc, T, bn);
   a.max_split_units = 0;
   a.hbuf = static_cast<uint16_t*>(sc.h);
   CUtensorMap xm;
   if (!tc::make_map_3d(&xm, sc.xp, (uint64_t)p.H, (uint64_t)rows_max, 1, (uint64_t)p.H * 2,
-                       (uint64_t)p.H * 2 * rows_max, tc::kGatherBN))
+                       (uint64_t)p.H * 2 * rows_max, bn))
     return -1;
   tc::Fp8Args w8;
   w8.os13 = p.lay.offs13;
@@ -2755,7 +2759,7 @@ int launch_tc_gather(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T
   b.out = sc.y;
   CUtensorMap hm;
   if (!tc::make_map_3d(&hm, sc.h, (uint64_t)p.I, (uint64_t)rows_max, 1, (uint64_t)p.I * 2,
-                       (uint64_t)p.I * 2 * rows_max, tc::kGatherBN))
+                       (uint64_t)p.I * 2 * rows_max, bn))
     return -1;
   n += fp8 ? tc::launch_mode<tc::kModeDownGather, tc::kWfFp8>(b, hm, m->w2, w8, s)
            : tc::launch_mode<tc::kModeDownGather, tc::kWfBf16>(b, hm, hm, w8, s);

@@ -151,7 +151,7 @@ struct Scratch {
   int32_t* ecount;    // [2]
   // tensor-core gather path (T > npad_max)
   int32_t* inv;       // [Tmax*k]   expert-sorted row of each flat entry t*k+j
-  int32_t* ntile0;    // [E+2]      first 128-token tile of each work entry (prefix)
+  int32_t* ntile0;    // [E+2]      first token tile of each work entry (prefix; tiles of gather_tile_rows)
   int32_t* n_rows;    // [1]        expert-sorted rows of this call (T*k [+ T shared])
   uint16_t* xp;       // [(Tmax*k + Tmax), H] x rows in expert-sorted order
   uint16_t* y;        // [(Tmax*k + Tmax), H] per-row expert outputs
@@ -214,6 +214,9 @@ size_t tc_partial_floats(const PoolDev& p, int npad_max);      // Scratch::parti
 size_t tc_dn_partial_floats(const PoolDev& p, int npad_max);   // Scratch::dn_partial
 int tc_ffn_sync_ints(const PoolDev& p);                         // Scratch::ffn_sync
 int tc_dsync_ints();                                          // Scratch::dsync
+// Token rows per tile of the gather path for a call of T tokens: 256 when its routed rows
+// average at least 192 per expert (one weight tile then serves twice the tokens), else 128.
+int gather_tile_rows(const PoolDev& p, int T);
 int launch_tc_gather(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, const void* x, void* out,
                      cudaStream_t s);
 int launch_tc_fused_decode(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, const void* x, void* out,

@@ -25,6 +25,7 @@ struct PlanArgs {
   const uint32_t* snap_wait = nullptr;   // if set: before writing the table, wait for *snap_wait >= snap_target
   uint32_t snap_target = 0;              // (other CTAs' reads of this layer's table row)
   uint32_t* slots_flag = nullptr;        // if set: released once the table holds this step's slots
+  int gather_bn = 128;                   // gather path: token rows per tile (128 or 256)
 };
 
 // Orderable key: (score ascending, slot ascending).  -0 is folded into +0.
@@ -781,13 +782,14 @@ __device__ void plan_body(const PlanArgs& a, uint8_t* dsm, bool prestaged = fals
       }
     }
     __syncthreads();
-    // gather path: first 128-token tile of every entry (entries in ascending expert id, shared last)
+    // gather path: first token tile of every entry (entries in ascending expert id, shared last)
     if ((a.flags & PLAN_GATHER) && warp == 0) {
+      const int bn = a.gather_bn;
       int run = 0;
       for (int e0 = 0; e0 < E; e0 += 32) {
         const int e = e0 + lane;
         const int c = e < E ? offs[e + 1] - offs[e] : 0;
-        const int v = (c + 127) / 128;
+        const int v = (c + bn - 1) / bn;
         int inc = v;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -801,7 +803,7 @@ __device__ void plan_body(const PlanArgs& a, uint8_t* dsm, bool prestaged = fals
         const int nw = sh_misc[6];
         if (p.shared) {
           a.sc.ntile0[nw - 1] = run;
-          run += (T + 127) / 128;
+          run += (T + bn - 1) / bn;
         }
         a.sc.ntile0[nw] = run;
         *a.sc.n_rows = Tk + (p.shared ? T : 0);

@@ -201,6 +201,26 @@ def test_fp8_dense_and_gather_paths_with_shared_expert(T):
         rig.close()
 
 
+@pytest.mark.parametrize("wname,I", [("qwen3_decode", 320), ("dsv3", 256)])
+def test_gather_path_with_256_row_token_tiles(wname, I):
+    """Few experts and many tokens (routed rows average >= 192 per expert): the gather path's token
+    tiles are 256 rows, one weight tile serving every row of a tile; experts whose rows are not a
+    multiple of 256 end in a ragged tile, and the shared expert's T rows span three tiles."""
+    wl = variant(get_workload(wname), name="gather256_" + wname, L=2, E=4, k=2, H=512, I=I, residency=0.5,
+                 shared=True, zipf_s=0.5)
+    rig = Rig(wl, max_tokens=640)
+    try:
+        for l in range(wl.L):
+            xs = gen.store_act(wl, gen.prefill_hidden(wl, l, 600))
+            out = rig.forward(l, xs)
+            ref, r = rig.oracle_forward(l, xs)
+            ok = check_routing(rig.pool.routing(640), r, wl.k)
+            check_output(wl, out, ref, ok)
+        assert rig.pool.status() == moe.MOE_OK
+    finally:
+        rig.close()
+
+
 @pytest.mark.parametrize("wname", ["qwen3_decode", "dsv3"])
 def test_pool_from_library_packed_records_matches_oracle(wname):
     """A caller with plain row-major weights packs its host pool with moe_pack_expert_record; the
