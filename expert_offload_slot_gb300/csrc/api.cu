@@ -562,6 +562,10 @@ static void stage_layer(moe_pool* P, int layer, int r) {
   P->staged_count += 1;
 }
 
+// CTAs of a residual-split call's miss copy: enough host reads in flight for the link (32 x 512
+// threads x 8 x 16 B = 2 MB), leaving the other SMs to the gate/up kernel running beside it
+constexpr int kSideCopyCtas = 32;
+
 static moe_status run_layer(moe_pool* P, int layer, const void* x, int T, void* out, bool staged,
                             const int32_t* ids_in, const float* w_in, const float* probs_in, cudaStream_t s) {
   PoolDev& d = P->d;
@@ -644,6 +648,19 @@ static moe_status run_layer(moe_pool* P, int layer, const void* x, int T, void* 
     const int n = launch_tc_gather(d, sc, P->tc_maps, T, x, out, s);
     if (n < 0) return fail(MOE_ERR_INVALID, "x must be 16-byte aligned for the tensor-core path");
     P->launches += n;
+  } else if (!staged && d.wdt == MOE_RESPLIT_Q4R4) {
+    // The miss copies on the side stream, beside gate/up over the resident entries (the plan
+    // never evicts an expert the step uses, so the copies write no slot those read); gate/up
+    // over the copied entries once they have landed, then down + combine over all entries.
+    CUDA_TRY(cudaEventRecord(P->ev_fork, s));
+    CUDA_TRY(cudaStreamWaitEvent(P->side, P->ev_fork, 0));
+    P->launches += launch_miss_copy(d, sc, P->side, kSideCopyCtas);
+    CUDA_TRY(cudaEventRecord(P->ev_join, P->side));
+    mark(3);
+    P->launches += launch_ffn_gate_up(d, sc, T, x, s, 0);
+    CUDA_TRY(cudaStreamWaitEvent(s, P->ev_join, 0));
+    P->launches += launch_ffn_gate_up(d, sc, T, x, s, 1);
+    P->launches += launch_ffn_down(d, sc, T, out, s);
   } else {
     if (!staged) P->launches += launch_miss_copy(d, sc, s);
     mark(3);

@@ -44,10 +44,10 @@ miss_copy_kernel(const CopyJob* __restrict__ jobs, const int32_t* __restrict__ n
   }
 }
 
-int launch_miss_copy(const PoolDev& p, const Scratch& sc, cudaStream_t s) {
+int launch_miss_copy(const PoolDev& p, const Scratch& sc, cudaStream_t s, int ctas) {
   const uint32_t rec16 = (uint32_t)(p.lay.rec / 16);
   const unsigned long long magic = ~0ull / rec16 + 1ull;
-  miss_copy_kernel<<<2 * sm_count(), kCopyThreads, 0, s>>>(sc.copies, sc.n_copy, rec16, magic);
+  miss_copy_kernel<<<ctas > 0 ? ctas : 2 * sm_count(), kCopyThreads, 0, s>>>(sc.copies, sc.n_copy, rec16, magic);
   return 1;
 }
 

@@ -40,6 +40,8 @@ struct FfnArgs {
   int H, I, T;
   size_t off13, off2, offs13, offs2;
   size_t offr13, offh2, offsr13, offsh2;   // residual-split records
+  const int32_t* sel;        // residual-split gate/up: the work positions to process (null: all)
+  const int32_t* sel_count;
 };
 
 template <typename WT> struct WTraits;
@@ -229,10 +231,11 @@ ffn_resplit_gate_up_kernel(FfnArgs a) {
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * kFfnWarps + (threadIdx.x >> 5);
   const int nw = gridDim.x * kFfnWarps;
-  const int n_work = *a.n_work;
+  const int n_work = a.sel ? *a.sel_count : *a.n_work;   // the selected entries, or all
+  auto entry = [&](int j) -> const WorkEntry& { return a.work[a.sel ? a.sel[j] : j]; };
   const int H = a.H, I = a.I;
   long long total = 0;
-  for (int u = 0; u < n_work; ++u) total += (long long)((a.work[u].n + NT - 1) / NT) * I;
+  for (int u = 0; u < n_work; ++u) total += (long long)((entry(u).n + NT - 1) / NT) * I;
   const long long p0 = total * gw / nw, p1 = total * (gw + 1) / nw;
   const AT* __restrict__ x = static_cast<const AT*>(a.x);
   AT* __restrict__ hout = static_cast<AT*>(a.h);
@@ -240,12 +243,12 @@ ffn_resplit_gate_up_kernel(FfnArgs a) {
   int u = 0;
   long long base = 0;                            // first unit of entry u
   for (long long pp = p0; pp < p1; ++pp) {
-    while (u < n_work && pp >= base + (long long)((a.work[u].n + NT - 1) / NT) * I) {
-      base += (long long)((a.work[u].n + NT - 1) / NT) * I;
+    while (u < n_work && pp >= base + (long long)((entry(u).n + NT - 1) / NT) * I) {
+      base += (long long)((entry(u).n + NT - 1) / NT) * I;
       ++u;
     }
     if (u >= n_work) break;
-    const WorkEntry ent = a.work[u];
+    const WorkEntry ent = entry(u);
     const long long local = pp - base;
     const int tc = (int)(local / I) * NT, i = (int)(local % I);
     const bool crit = ent.crit != 0;
@@ -499,11 +502,17 @@ static FfnArgs ffn_args(const PoolDev& p, const Scratch& sc, int T, const void* 
   a.offh2 = p.lay.offh2;
   a.offsr13 = p.lay.offsr13;
   a.offsh2 = p.lay.offsh2;
+  a.sel = nullptr;
+  a.sel_count = nullptr;
   return a;
 }
 
-int launch_ffn_gate_up(const PoolDev& p, const Scratch& sc, int T, const void* x, cudaStream_t s) {
-  const FfnArgs a = ffn_args(p, sc, T, x, nullptr);
+int launch_ffn_gate_up(const PoolDev& p, const Scratch& sc, int T, const void* x, cudaStream_t s, int part) {
+  FfnArgs a = ffn_args(p, sc, T, x, nullptr);
+  if (part >= 0 && p.wdt == MOE_RESPLIT_Q4R4) {
+    a.sel = sc.elist + (size_t)part * (p.E + 1);
+    a.sel_count = sc.ecount + part;
+  }
   const int grid = 2 * sm_count();
   if (p.wdt == MOE_F32) ffn_gate_up_kernel<float, float><<<grid, kFfnWarps * 32, 0, s>>>(a);
   else if (p.wdt == MOE_BF16) ffn_gate_up_kernel<uint16_t, uint16_t><<<grid, kFfnWarps * 32, 0, s>>>(a);

@@ -198,8 +198,10 @@ int launch_route_gate_fused(const PoolDev& p, int layer, const void* x, int T, c
                             const float* router_b, const Scratch& sc, cudaStream_t s);
 int launch_plan(const PoolDev& p, const Scratch& sc, int layer, int T, const int32_t* ids, const float* w,
                 const float* probs, int flags, int region, int npad, cudaStream_t s);
-int launch_miss_copy(const PoolDev& p, const Scratch& sc, cudaStream_t s);
-int launch_ffn_gate_up(const PoolDev& p, const Scratch& sc, int T, const void* x, cudaStream_t s);
+// ctas: grid size (0: two CTAs per SM)
+int launch_miss_copy(const PoolDev& p, const Scratch& sc, cudaStream_t s, int ctas = 0);
+// part: -1 every entry; 0 / 1 (residual-split pools) the resident / the copied entries of the plan's lists
+int launch_ffn_gate_up(const PoolDev& p, const Scratch& sc, int T, const void* x, cudaStream_t s, int part = -1);
 int launch_ffn_down(const PoolDev& p, const Scratch& sc, int T, void* out, cudaStream_t s);
 
 // tensor-core (tcgen05) expert path: bf16 weights, T <= 256 tokens
