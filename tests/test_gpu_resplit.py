@@ -66,6 +66,7 @@ def test_resplit_umia_decode_and_staged_prefill(shared):
         st = rig.pool.stats()
         assert st["critical_entries"] == crit_total
         assert crit_total > 0 and n_crit_lo > 0            # both precisions were exercised
+        assert st["misses"] > 0                             # copies beside the resident entries' gate/up
         assert rig.pool.status() == moe.MOE_OK
     finally:
         rig.close()
