@@ -27,8 +27,8 @@
 // HBM at full burst length.  Activations (x, h) come through TMA tensor maps.
 //
 // Large token counts (T > 256) use the gather modes: tokens are grouped by
-// expert (x rows gathered once), each (entry, 128-token tile, 128-row tile) is
-// a unit, gate/up writes w * SiLU(g) * u per expert row, down writes one bf16
+// expert (x rows gathered once), each (entry, token tile of 128 or 256 rows,
+// 128-row tile) is a unit, gate/up writes w * SiLU(g) * u per expert row, down writes one bf16
 // row per (token, expert) and a combine kernel sums each token's k rows in
 // ascending expert order (plus the shared expert).
 //
