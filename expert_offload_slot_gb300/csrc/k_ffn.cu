@@ -98,6 +98,11 @@ template <int N> struct Act<uint16_t, N> {
       v[8 * q + 4] = bf16lo(u.z); v[8 * q + 5] = bf16hi(u.z);
       v[8 * q + 6] = bf16lo(u.w); v[8 * q + 7] = bf16hi(u.w);
     }
+    if constexpr (N % 8 == 4) {   // a last 8-byte group
+      const uint2 u = *reinterpret_cast<const uint2*>(p + N - 4);
+      v[N - 4] = bf16lo(u.x); v[N - 3] = bf16hi(u.x);
+      v[N - 2] = bf16lo(u.y); v[N - 1] = bf16hi(u.y);
+    }
   }
   __device__ __forceinline__ static void store1(uint16_t* p, float v) { *p = f32_to_bf16_rn(v); }
 };
@@ -389,7 +394,7 @@ ffn_down_combine_kernel(FfnArgs a) {
 // down + combine for residual-split records: as ffn_down_combine_kernel, reading W^H_down (8-bit,
 // 16 columns per lane chunk) for a critical entry and W^L_down (4-bit, 32 columns) otherwise
 template <typename AT>
-__global__ void __launch_bounds__(kFfnWarps * 32)
+__global__ void __launch_bounds__(kFfnWarps * 32, 3)
 ffn_resplit_down_kernel(FfnArgs a) {
   constexpr int NT = kTokChunk;
   constexpr int RPW = kDownRowsPerWarp;
@@ -420,41 +425,58 @@ ffn_resplit_down_kernel(FfnArgs a) {
 #pragma unroll
         for (int r = 0; r < NT; ++r) acc[rr][r] = 0.f;
       for (int i0 = lane * cw; i0 < I; i0 += 32 * cw) {
-        float wv[RPW][32];
+        uint32_t w[RPW][4];
         float sc[RPW];
 #pragma unroll
         for (int rr = 0; rr < RPW; ++rr) {
           const uint4 q = __ldcs(reinterpret_cast<const uint4*>(w2 + (size_t)hr[rr] * row_bytes + (crit ? (size_t)i0 : (size_t)i0 / 2)));
-          const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-          if (crit) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) int8x4(w[j], wv[rr] + 4 * j);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) nib8(w[j], wv[rr] + 8 * j);
-          }
+          w[rr][0] = q.x;
+          w[rr][1] = q.y;
+          w[rr][2] = q.z;
+          w[rr][3] = q.w;
           sc[rr] = s2[(size_t)hr[rr] * G + i0 / 128];
         }
+        // one word of codes at a time (few registers, so more warps per SM): each (row, token)
+        // product still runs over the chunk's columns in ascending order
+        float d[RPW][NT];
 #pragma unroll
-        for (int r = 0; r < NT; ++r) {
-          if (r < nr) {
-            float hv[32];
-            if (crit) Act<AT, 16>::load(hin + (size_t)(ent.row0 + tc + r) * I + i0, hv);
-            else Act<AT, 32>::load(hin + (size_t)(ent.row0 + tc + r) * I + i0, hv);
+        for (int rr = 0; rr < RPW; ++rr)
 #pragma unroll
-            for (int rr = 0; rr < RPW; ++rr) {
-              float d = 0.f;
+          for (int r = 0; r < NT; ++r) d[rr][r] = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float wv[RPW][8];
+#pragma unroll
+          for (int rr = 0; rr < RPW; ++rr) {
+            if (crit) int8x4(w[rr][j], wv[rr]);
+            else nib8(w[rr][j], wv[rr]);
+          }
+#pragma unroll
+          for (int r = 0; r < NT; ++r) {
+            if (r < nr) {
+              float hv[8];
+              const AT* hp = hin + (size_t)(ent.row0 + tc + r) * I + i0;
               if (crit) {
+                Act<AT, 4>::load(hp + 4 * j, hv);
 #pragma unroll
-                for (int c = 0; c < 16; ++c) d = fmaf(wv[rr][c], hv[c], d);
+                for (int rr = 0; rr < RPW; ++rr)
+#pragma unroll
+                  for (int c = 0; c < 4; ++c) d[rr][r] = fmaf(wv[rr][c], hv[c], d[rr][r]);
               } else {
+                Act<AT, 8>::load(hp + 8 * j, hv);
 #pragma unroll
-                for (int c = 0; c < 32; ++c) d = fmaf(wv[rr][c], hv[c], d);
+                for (int rr = 0; rr < RPW; ++rr)
+#pragma unroll
+                  for (int c = 0; c < 8; ++c) d[rr][r] = fmaf(wv[rr][c], hv[c], d[rr][r]);
               }
-              acc[rr][r] = fmaf(sc[rr], d, acc[rr][r]);
             }
           }
         }
+#pragma unroll
+        for (int r = 0; r < NT; ++r)
+          if (r < nr)
+#pragma unroll
+            for (int rr = 0; rr < RPW; ++rr) acc[rr][r] = fmaf(sc[rr], d[rr][r], acc[rr][r]);
       }
 #pragma unroll
       for (int r = 0; r < NT; ++r) {
