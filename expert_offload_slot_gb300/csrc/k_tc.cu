@@ -27,7 +27,7 @@
 // HBM at full burst length.  Activations (x, h) come through TMA tensor maps.
 //
 // Large token counts (T > 256) use the gather modes: tokens are grouped by
-// expert (x rows gathered once), each (entry, token tile of 128 or 256 rows,
+// expert (x rows gathered once), each (entry, token tile of 64, 128 or 256 rows,
 // 128-row tile) is a unit, gate/up writes w * SiLU(g) * u per expert row, down writes one bf16
 // row per (token, expert) and a combine kernel sums each token's k rows in
 // ascending expert order (plus the shared expert).
@@ -391,34 +391,38 @@ __device__ __forceinline__ void store_chunk(const Args& a, const UnitRange& r, i
 // block (TMA tiles of codes, expanded to bf16 in place by converter warps, the
 // block scale applied in the expansion).
 constexpr int kWfBf16 = 0, kWfFp8 = 1;
-constexpr int kConvWarps = 4;
+constexpr int kConvWarps = 4;         // fused decode kernels
+constexpr int kGatherConvWarps = 8;   // prefill gather kernel
 
-// Converter warps (ct = 0..127): expand the fp8 code tiles q < nt of one stage in
-// place.  Each tile slot is 16 KB; its codes (128 rows x 64 bytes) sit in the
-// upper 8 KB.  Every thread reads its 4 x 16 code bytes of each tile, then (after
-// the named barrier, all reads done) writes them back as bf16 (code * scale, one
-// rounding) in the 128-byte-swizzled order.  Every converter thread calls this
-// for every stage, work or not, so the named barrier is always complete.
+// NCT converter threads (ct = 0..NCT-1): expand the fp8 code tiles q < nt of one
+// stage in place.  Each tile slot is 16 KB; its codes (128 rows x 64 bytes = 512
+// chunks of 16 bytes) sit in the upper 8 KB.  Every thread reads its 512 / NCT
+// chunks of each tile, then (after the named barrier, all reads done) writes them
+// back as bf16 (code * scale, one rounding) in the 128-byte-swizzled order.  Every
+// converter thread calls this for every stage, work or not, so the named barrier
+// is always complete.
+template <int NCT>
 __device__ __forceinline__ void fp8_expand_stage(uint8_t* st, int nt, float s0, float s1, int ct, bool work) {
-  uint4 raw[2][4];
+  constexpr int MPER = 512 / NCT;
+  uint4 raw[2][MPER];
   if (work) {
 #pragma unroll
     for (int q = 0; q < 2; ++q)
       if (q < nt) {
 #pragma unroll
-        for (int m = 0; m < 4; ++m)
-          raw[q][m] = *reinterpret_cast<const uint4*>(st + q * kTileBytes + kTileBytes / 2 + (ct + 128 * m) * 16);
+        for (int m = 0; m < MPER; ++m)
+          raw[q][m] = *reinterpret_cast<const uint4*>(st + q * kTileBytes + kTileBytes / 2 + (ct + NCT * m) * 16);
       }
   }
-  asm volatile("bar.sync 3, %0;" ::"n"(32 * kConvWarps) : "memory");
+  asm volatile("bar.sync 3, %0;" ::"n"(NCT) : "memory");
   if (!work) return;
 #pragma unroll
   for (int q = 0; q < 2; ++q)
     if (q < nt) {
       const float sv = q ? s1 : s0;
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int c16 = ct + 128 * m, row = c16 >> 2, cq = c16 & 3;   // 16 codes: columns cq*16..+16
+      for (int m = 0; m < MPER; ++m) {
+        const int c16 = ct + NCT * m, row = c16 >> 2, cq = c16 & 3;   // 16 codes: columns cq*16..+16
         const uint32_t w4[4] = {raw[q][m].x, raw[q][m].y, raw[q][m].z, raw[q][m].w};
         uint32_t o[8];
 #pragma unroll
@@ -445,10 +449,10 @@ struct Fp8Args {
 };
 
 template <int WF> struct GatherShape {
-  static constexpr int threads = kThreads + (WF == kWfFp8 ? 32 * kConvWarps : 0);
+  static constexpr int threads = kThreads + (WF == kWfFp8 ? 32 * kGatherConvWarps : 0);
 };
 
-// Gather modes (T > 256 tokens): unit = (entry u, token tile nt of N = 128 or 256
+// Gather modes (T > 256 tokens): unit = (entry u, token tile nt of N = 64, 128 or 256
 // rows, 128-row tile mt), full K (the plan's ntile0 counts tiles of the same N).  Gate/up: A = gate and up tiles of the entry, B = its gathered x
 // rows; epilogue h = w * SiLU(g) * u per row.  Down: A = W_down tile, B = its h
 // rows; epilogue one bf16 row of y per (token, expert).
@@ -482,7 +486,7 @@ tc_gather_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constan
     for (int s = 0; s < S; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
-      if (WF == kWfFp8) mbar_init(&conv_bar[s], 32 * kConvWarps);
+      if (WF == kWfFp8) mbar_init(&conv_bar[s], 32 * kGatherConvWarps);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull_bar[b], 1);
@@ -618,7 +622,7 @@ tc_gather_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constan
     }
   } else if (WF == kWfFp8) {
     // ------------------------------------------------------------- converter warps (fp8)
-    const int ct = threadIdx.x - kThreads;        // 0..127
+    const int ct = threadIdx.x - kThreads;        // 0 .. 32 * kGatherConvWarps - 1
     uint32_t it = 0;
     int local = 0;
     bool stop = false;
@@ -634,7 +638,7 @@ tc_gather_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constan
       } else if (is_gate_up(MODE) && ct >= 64 && ct - 64 < nblk) {
         scale_sh[sbuf][ct] = scl[(size_t)(a.I / BM + r.mt) * w8.sc_h + b0 + (ct - 64)];
       }
-      asm volatile("bar.sync 3, %0;" ::"n"(32 * kConvWarps) : "memory");
+      asm volatile("bar.sync 3, %0;" ::"n"(32 * kGatherConvWarps) : "memory");
       for (int kb = r.kb0; kb < r.kb1; ++kb, ++it) {
         const int s = it % S;
         if (!stop && (!mbar_wait(&full_bar[s], (it / S) & 1) || abort_sh)) {
@@ -644,10 +648,10 @@ tc_gather_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constan
         }
         const float s0 = scale_sh[sbuf][kb / 2 - b0];
         const float s1 = is_gate_up(MODE) ? scale_sh[sbuf][64 + kb / 2 - b0] : 0.f;
-        fp8_expand_stage(smem + (size_t)s * stage_bytes, NACC, s0, s1, ct, !stop);
+        fp8_expand_stage<32 * kGatherConvWarps>(smem + (size_t)s * stage_bytes, NACC, s0, s1, ct, !stop);
         if (!stop) mbar_arrive(&conv_bar[s]);
       }
-      asm volatile("bar.sync 3, %0;" ::"n"(32 * kConvWarps) : "memory");   // before the scale buffer is reused
+      asm volatile("bar.sync 3, %0;" ::"n"(32 * kGatherConvWarps) : "memory");   // before the scale buffer is reused
     }
   }
   fence_before();
@@ -1501,7 +1505,7 @@ __device__ __forceinline__ void fused_ffn(const CUtensorMap* map_x_p, const CUte
         const int nt = r.gu ? 2 : min(2, r.kb1 - kb);
         const float s0 = scale_sh[sbuf][kb / 2 - b0];
         const float s1 = r.gu ? scale_sh[sbuf][64 + kb / 2 - b0] : (nt > 1 ? scale_sh[sbuf][(kb + 1) / 2 - b0] : 0.f);
-        fp8_expand_stage(smem + (size_t)s * stage_bytes, nt, s0, s1, ct, !stop);
+        fp8_expand_stage<32 * kConvWarps>(smem + (size_t)s * stage_bytes, nt, s0, s1, ct, !stop);
         if (!stop) mbar_arrive(&conv_bar[s]);
       }
       asm volatile("bar.sync 3, %0;" ::"n"(32 * kConvWarps) : "memory");   // before the scale buffer is reused
@@ -2730,7 +2734,11 @@ static tc::Args tc_args(const PoolDev& p, const Scratch& sc, int T, int N) {
 }
 
 int gather_tile_rows(const PoolDev& p, int T) {
-  return (long long)T * p.k >= 192LL * p.E ? 256 : 128;
+  const long long rows = (long long)T * p.k;   // routed rows of the call
+  if (rows >= 192LL * p.E) return 256;
+  // fp8 records are expanded to bf16 once per unit: smaller tiles would expand each weight
+  // tile more often (measured slower), so they keep 128 rows
+  return rows >= 96LL * p.E || p.wdt == MOE_FP8_E4M3_B128 ? 128 : 64;
 }
 
 // Gather path: xp = x rows by expert; h = gate/up per row; y = down per row; out = combine.

@@ -216,8 +216,10 @@ size_t tc_partial_floats(const PoolDev& p, int npad_max);      // Scratch::parti
 size_t tc_dn_partial_floats(const PoolDev& p, int npad_max);   // Scratch::dn_partial
 int tc_ffn_sync_ints(const PoolDev& p);                         // Scratch::ffn_sync
 int tc_dsync_ints();                                          // Scratch::dsync
-// Token rows per tile of the gather path for a call of T tokens: 256 when its routed rows
-// average at least 192 per expert (one weight tile then serves twice the tokens), else 128.
+// Token rows per tile of the gather path for a call of T tokens, from its routed rows per
+// expert on average: 256 from 192 (one weight tile then serves twice the tokens), 128 from
+// 96 (and always for fp8 records), else 64 (fewer padding rows loaded and multiplied for
+// experts with few tokens).
 int gather_tile_rows(const PoolDev& p, int T);
 int launch_tc_gather(const PoolDev& p, const Scratch& sc, const TcMaps* m, int T, const void* x, void* out,
                      cudaStream_t s);

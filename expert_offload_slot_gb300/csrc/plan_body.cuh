@@ -25,7 +25,7 @@ struct PlanArgs {
   const uint32_t* snap_wait = nullptr;   // if set: before writing the table, wait for *snap_wait >= snap_target
   uint32_t snap_target = 0;              // (other CTAs' reads of this layer's table row)
   uint32_t* slots_flag = nullptr;        // if set: released once the table holds this step's slots
-  int gather_bn = 128;                   // gather path: token rows per tile (128 or 256)
+  int gather_bn = 128;                   // gather path: token rows per tile (64, 128 or 256)
 };
 
 // Orderable key: (score ascending, slot ascending).  -0 is folded into +0.
