@@ -401,7 +401,7 @@ constexpr int kGatherConvWarps = 8;   // prefill gather kernel
 // back as bf16 (code * scale, one rounding) in the 128-byte-swizzled order.  Every
 // converter thread calls this for every stage, work or not, so the named barrier
 // is always complete.
-template <int NCT>
+template <int NCT, int BAR = 3>
 __device__ __forceinline__ void fp8_expand_stage(uint8_t* st, int nt, float s0, float s1, int ct, bool work) {
   constexpr int MPER = 512 / NCT;
   uint4 raw[2][MPER];
@@ -414,7 +414,7 @@ __device__ __forceinline__ void fp8_expand_stage(uint8_t* st, int nt, float s0, 
           raw[q][m] = *reinterpret_cast<const uint4*>(st + q * kTileBytes + kTileBytes / 2 + (ct + NCT * m) * 16);
       }
   }
-  asm volatile("bar.sync 3, %0;" ::"n"(NCT) : "memory");
+  asm volatile("bar.sync %0, %1;" ::"n"(BAR), "n"(NCT) : "memory");
   if (!work) return;
 #pragma unroll
   for (int q = 0; q < 2; ++q)
@@ -486,7 +486,7 @@ tc_gather_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constan
     for (int s = 0; s < S; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
-      if (WF == kWfFp8) mbar_init(&conv_bar[s], 32 * kGatherConvWarps);
+      if (WF == kWfFp8) mbar_init(&conv_bar[s], 32 * kGatherConvWarps / 2);   // one group per stage
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull_bar[b], 1);
@@ -623,6 +623,7 @@ tc_gather_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constan
   } else if (WF == kWfFp8) {
     // ------------------------------------------------------------- converter warps (fp8)
     const int ct = threadIdx.x - kThreads;        // 0 .. 32 * kGatherConvWarps - 1
+    const int grp = ct >= 16 * kGatherConvWarps ? 1 : 0, gct = ct - grp * 16 * kGatherConvWarps;
     uint32_t it = 0;
     int local = 0;
     bool stop = false;
@@ -640,6 +641,9 @@ tc_gather_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constan
       }
       asm volatile("bar.sync 3, %0;" ::"n"(32 * kGatherConvWarps) : "memory");
       for (int kb = r.kb0; kb < r.kb1; ++kb, ++it) {
+        // two groups of converter warps take alternate stages, so that two expansions are in
+        // flight (each group's own named barrier orders its in-place reads before its writes)
+        if ((int)(it & 1u) != grp) continue;
         const int s = it % S;
         if (!stop && (!mbar_wait(&full_bar[s], (it / S) & 1) || abort_sh)) {
           stop = true;
@@ -648,7 +652,10 @@ tc_gather_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constan
         }
         const float s0 = scale_sh[sbuf][kb / 2 - b0];
         const float s1 = is_gate_up(MODE) ? scale_sh[sbuf][64 + kb / 2 - b0] : 0.f;
-        fp8_expand_stage<32 * kGatherConvWarps>(smem + (size_t)s * stage_bytes, NACC, s0, s1, ct, !stop);
+        if (grp == 0)
+          fp8_expand_stage<16 * kGatherConvWarps, 4>(smem + (size_t)s * stage_bytes, NACC, s0, s1, gct, !stop);
+        else
+          fp8_expand_stage<16 * kGatherConvWarps, 5>(smem + (size_t)s * stage_bytes, NACC, s0, s1, gct, !stop);
         if (!stop) mbar_arrive(&conv_bar[s]);
       }
       asm volatile("bar.sync 3, %0;" ::"n"(32 * kGatherConvWarps) : "memory");   // before the scale buffer is reused
