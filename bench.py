@@ -1023,11 +1023,12 @@ def main():
             return
         n = min(args.steps, 24)
         o = OracleSample(wl, T, min(4, wl.L), (n + 3) // 4, "cuda")
-        o.run(min(args.warmup, 2))
+        warm = min(args.warmup, 4)      # untimed oracle layer-steps (~0.4 s each)
+        o.run(warm)
         done, el = o.run(n)
         v = done * T / el
         line = {"impl": "reference", "metric": "MoE-layer tokens/s (decode)", "value": v,
-                "unit": "MoE-layer tokens/s", "n_gpus": 1, "steps": done, "warmup": min(args.warmup, 2),
+                "unit": "MoE-layer tokens/s", "n_gpus": 1, "steps": done, "warmup": warm,
                 "ms_per_step": el * 1e3 / done, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "f64", "data": "synthetic (seeded random weights, AR(1) hidden states)",
                 "config": dict(base_cfg, reference_step="one layer-step of the oracle (T tokens, one layer)"),
