@@ -31,15 +31,15 @@ def _compare_cache(rig, l):
 
 
 def _run_trace(rig, steps, T, layers=None):
-    """Returns (worst relative error, cache verdict).
+    """Returns (worst relative error, cache outcome).
 
-    The verdict is "same" while GPU and oracle tables agree bit for bit after every
+    The outcome is "same" while GPU and oracle tables agree bit for bit after every
     step, "near_tie" once a token's top-k set differed at a near tie (the two
     sides then legitimately hold different tables), and "diverged" otherwise.
     """
     wl = rig.wl
     layers = range(wl.L) if layers is None else layers
-    verdict = "same"
+    outcome = "same"
     worst = 0.0
     for l in layers:
         xs = gen.store_act(wl, gen.decode_hidden(wl, l, T, steps))
@@ -49,22 +49,22 @@ def _run_trace(rig, steps, T, layers=None):
             g = rig.pool.routing(T)
             ok = check_routing(g, r, wl.k)
             worst = max(worst, check_output(wl, out, ref, ok))
-            if verdict == "same" and not ok.all():
-                verdict = "near_tie"
-            if verdict == "same":
+            if outcome == "same" and not ok.all():
+                outcome = "near_tie"
+            if outcome == "same":
                 rig.sim.update_scores(l, r["ids"], r["probs"].astype(np.float32))
                 rig.sim.plan(l, r["ids"])
                 if not _compare_cache(rig, l):
-                    verdict = "diverged"
-    return worst, verdict
+                    outcome = "diverged"
+    return worst, outcome
 
 
 def test_tiny_workload_decode_trace():
     wl = get_workload("tiny")
     rig = Rig(wl)
     try:
-        worst, verdict = _run_trace(rig, steps=wl.decode_steps, T=4)
-        assert verdict == "same", verdict
+        worst, outcome = _run_trace(rig, steps=wl.decode_steps, T=4)
+        assert outcome == "same", outcome
         assert rig.pool.status() == moe.MOE_OK
         s = rig.pool.stats()
         assert s["steps"] == wl.decode_steps and s["hits"] + s["misses"] > 0
@@ -81,8 +81,8 @@ def test_bf16_multilayer_trace(gating, policy):
     rig = Rig(wl, policy=policy, window=8)
     try:
         for T in (1, 3, 8):
-            worst, verdict = _run_trace(rig, steps=6, T=T)
-            assert verdict != "diverged"
+            worst, outcome = _run_trace(rig, steps=6, T=T)
+            assert outcome != "diverged"
         assert rig.pool.status() == moe.MOE_OK
     finally:
         rig.close()
@@ -157,8 +157,8 @@ def test_fp8_block_scaled_with_shared_expert():
     assert wl.weight_dtype == FP8_E4M3_B128 and wl.shared and wl.gating == GATE_SIGMOID_RENORM
     rig = Rig(wl)
     try:
-        worst, verdict = _run_trace(rig, steps=4, T=5)
-        assert verdict != "diverged"
+        worst, outcome = _run_trace(rig, steps=4, T=5)
+        assert outcome != "diverged"
     finally:
         rig.close()
 
