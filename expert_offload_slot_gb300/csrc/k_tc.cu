@@ -2074,7 +2074,7 @@ tc_fused_decode_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
 //          landing record at once and computed from there, and written to its
 //          slot once the plan has chosen it.  Otherwise every CTA waits for the
 //          plan's work lists.
-// Fast gate (local lists without substitution): no ticket and no gating CTA; each
+// Fast gate (streaming variant, local lists, no substitution): no ticket and no gating CTA; each
 // routing CTA adds one to route_done once its logits are written, and every CTA,
 // once all are, stages the step's logits [T][E] in shared memory and gates every
 // token itself, one warp per token (CTA 0 also writes the routing outputs the plan
@@ -2363,9 +2363,9 @@ tc_decode_layer_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
     return true;
   };
   if constexpr (STREAM) {
-    // The planner takes no streaming units: at one to four tokens the plan lasts about as
-    // long as the FFN, and the FFN's phase barrier would wait for it (the other CTAs count
-    // G - 1 arrivals).  The streaming variant always runs on local lists.
+    // The planner takes no streaming units: at one token the plan lasts about as long as
+    // the FFN, and the FFN's phase barrier would wait for it (the other CTAs count G - 1
+    // arrivals).  The streaming variant always runs on local lists.
     if (blockIdx.x == 0)
       pre();
     else
